@@ -1,0 +1,267 @@
+"""Pins of the float64 oracle against things other than itself.
+
+* central finite differences of the oracle's own forward (every gradient, both
+  gate modes, varlen with two sequences, h0 and dht present, a sequence longer
+  than the oracle's 64-token checkpoint block);
+* closed forms: beta = 0 (the output is the decayed h0 only) and g = 0 with
+  beta = 0 (the state never moves), forward and backward;
+* the retrieval invariant of the delta rule with beta = 1 (the state returns
+  v for the key just written), which fixes the order of decay and update;
+* tangency of the L2-norm backward ("FlashKDA之backward（K1）", §3.3.2);
+* varlen equals separate per-sequence runs; linearity in (dO, dht);
+* the worked examples of the pages (tests/golden/).
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+
+from oracle import chunk_form, oracle
+from tests.fdiff import causal_conv1d, central_grad
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rand_case(rng, lens, H, D, gate="gdn", h0=True, dht=True):
+    T = sum(lens)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    N = len(lens)
+    c = dict(cu=cu, q=rng.standard_normal((T, H, D)), k=rng.standard_normal((T, H, D)),
+             v=rng.standard_normal((T, H, D)), b=rng.standard_normal((T, H)),
+             dO=rng.standard_normal((T, H, D)),
+             h0=0.3 * rng.standard_normal((N, H, D, D)) if h0 else None,
+             dht=0.3 * rng.standard_normal((N, H, D, D)) if dht else None, scale=D ** -0.5)
+    if gate == "gdn":
+        c["g"] = -np.logaddexp(0, rng.standard_normal((T, H)))
+    elif gate == "glog":
+        c["glog"] = -0.5 * np.logaddexp(0, rng.standard_normal((T, H, D)))
+    else:
+        c["g_raw"] = rng.standard_normal((T, H, D))
+        c["A_log"] = rng.uniform(-1, 0, H)
+        c["dt_bias"] = 0.1 * rng.standard_normal((H, D))
+    return c
+
+
+def _loss_gdn(c):
+    r = oracle.gdn(c["q"], c["k"], c["v"], c["g"], c["b"], c["scale"], c["cu"], h0=c["h0"])
+    L = (r["o"] * c["dO"]).sum()
+    if c["dht"] is not None:
+        L += (r["ht"] * c["dht"]).sum()
+    return L
+
+
+def _loss_kda(c):
+    r = oracle.kda(c["q"], c["k"], c["v"], c["g_raw"], c["A_log"], c["dt_bias"], c["b"],
+                   c["scale"], c["cu"], h0=c["h0"])
+    L = (r["o"] * c["dO"]).sum()
+    if c["dht"] is not None:
+        L += (r["ht"] * c["dht"]).sum()
+    return L
+
+
+def _check(fd, an, name):
+    err = np.abs(fd - an).max()
+    tol = 1e-7 + 1e-6 * np.abs(an).max()
+    assert err <= tol, f"{name}: max |fd - analytic| = {err:.3e} > {tol:.3e}"
+
+
+# ----------------------------------------------------------------------------
+# FD machinery convention, pinned by the conv worked example (page 2)
+# ----------------------------------------------------------------------------
+def test_fd_convention_on_conv_worked_example():
+    ex = json.load(open(os.path.join(GOLDEN, "causal_conv_backward_example.json")))
+    x = np.array(ex["x"], float)
+    w = np.array(ex["w"], float)
+    bias = np.array([float(ex["bias"])])
+    g = np.array(ex["g"], float)
+    loss = lambda: float((g * causal_conv1d(x, w, bias[0])).sum())
+    assert loss() == pytest.approx(ex["L"], abs=1e-9)
+    np.testing.assert_allclose(central_grad(loss, x), ex["dx"], atol=1e-6)
+    np.testing.assert_allclose(central_grad(loss, w), ex["dw"], atol=1e-6)
+    np.testing.assert_allclose(central_grad(loss, bias), [ex["dbias"]], atol=1e-6)
+
+
+def test_reverse_cumsum_worked_example():
+    ex = json.load(open(os.path.join(GOLDEN, "reverse_cumsum_example.json")))
+    np.testing.assert_array_equal(chunk_form.reverse_cumsum(np.array(ex["dgc"])),
+                                  ex["suffix_sums"])
+
+
+# ----------------------------------------------------------------------------
+# finite differences of the whole backward
+# ----------------------------------------------------------------------------
+@pytest.mark.parametrize("lens,D,sample", [((3, 5), 4, None), ((70, 81), 3, 160)])
+def test_gdn_backward_matches_fd(lens, D, sample):
+    rng = np.random.default_rng(11)
+    c = _rand_case(rng, lens, 2, D, "gdn")
+    an = oracle.gdn(c["q"], c["k"], c["v"], c["g"], c["b"], c["scale"], c["cu"], h0=c["h0"],
+                    dO=c["dO"], dht=c["dht"])
+    for name, key in (("q", "dq"), ("k", "dk"), ("v", "dv"), ("g", "dg"), ("b", "dbeta"),
+                      ("h0", "dh0")):
+        x = c[name]
+        idx = None if sample is None else rng.choice(x.size, min(sample, x.size), replace=False)
+        fd = central_grad(lambda: _loss_gdn(c), x, idx)
+        ref = an[key].reshape(-1) if idx is None else an[key].reshape(-1)[idx]
+        _check(fd, ref, name)
+
+
+def test_kda_backward_matches_fd():
+    rng = np.random.default_rng(12)
+    c = _rand_case(rng, (4, 3), 2, 4, "kda")
+    an = oracle.kda(c["q"], c["k"], c["v"], c["g_raw"], c["A_log"], c["dt_bias"], c["b"],
+                    c["scale"], c["cu"], h0=c["h0"], dO=c["dO"], dht=c["dht"])
+    for name, key in (("q", "dq"), ("k", "dk"), ("v", "dv"), ("g_raw", "dg_raw"),
+                      ("A_log", "dA_log"), ("dt_bias", "ddt_bias"), ("b", "dbeta"),
+                      ("h0", "dh0")):
+        fd = central_grad(lambda: _loss_kda(c), c[name])
+        _check(fd, an[key].reshape(-1), name)
+
+
+def test_dht_gradient_is_the_final_state():
+    # d L / d dht = ht, so FD in dht is the forward's final state; and the
+    # gradient w.r.t. dO is o.  This pins which output each cotangent pairs with.
+    rng = np.random.default_rng(13)
+    c = _rand_case(rng, (5,), 1, 3, "gdn")
+    r = oracle.gdn(c["q"], c["k"], c["v"], c["g"], c["b"], c["scale"], c["cu"], h0=c["h0"])
+    _check(central_grad(lambda: _loss_gdn(c), c["dht"]), r["ht"].reshape(-1), "dht")
+    _check(central_grad(lambda: _loss_gdn(c), c["dO"]), r["o"].reshape(-1), "dO")
+
+
+# ----------------------------------------------------------------------------
+# closed forms
+# ----------------------------------------------------------------------------
+def _l2n(x):
+    return x / np.sqrt((x * x).sum(-1, keepdims=True) + 1e-6)
+
+
+@pytest.mark.parametrize("zero_gate", [False, True])
+def test_beta_zero_closed_form(zero_gate):
+    """beta = 0: S_t = diag(exp(cumsum g)) h0, so o_t = scale (Gamma_t h0)^T qn_t and
+    dv = dk = 0, dh0 = sum_t scale Gamma_t qn_t dO_t^T + Gamma_T dht,
+    dg_t[d] = sum_{s>=t} scale qn_s[d] (Gamma_s h0 dO_s)[d] + (Gamma_T h0 . dht)[d, :].sum()."""
+    rng = np.random.default_rng(21)
+    L_, D = 9, 5
+    c = _rand_case(rng, (L_,), 1, D, "glog")
+    if zero_gate:
+        c["glog"][:] = 0.0
+    b = np.full((L_, 1), -np.inf)
+    r = oracle.gated_delta(c["q"], c["k"], c["v"], c["glog"], b, c["scale"], c["cu"], h0=c["h0"],
+                           dO=c["dO"], dht=c["dht"])
+    h0, dht, s = c["h0"][0, 0], c["dht"][0, 0], c["scale"]
+    qn = _l2n(c["q"][:, 0])
+    gam = np.exp(np.cumsum(c["glog"][:, 0], axis=0))          # [L, D]
+    o = np.stack([s * (gam[t][:, None] * h0).T @ qn[t] for t in range(L_)])
+    np.testing.assert_allclose(r["o"][:, 0], o, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(r["ht"][0, 0], gam[-1][:, None] * h0, rtol=1e-12, atol=1e-13)
+    assert np.abs(r["dv"]).max() == 0.0 and np.abs(r["dk"]).max() == 0.0
+    assert np.abs(r["dbeta"]).max() == 0.0
+    dh0 = sum(s * np.outer(gam[t] * qn[t], c["dO"][t, 0]) for t in range(L_)) + gam[-1][:, None] * dht
+    np.testing.assert_allclose(r["dh0"][0, 0], dh0, rtol=1e-11, atol=1e-12)
+    per_tok = np.stack([s * qn[t] * gam[t] * (h0 @ c["dO"][t, 0]) for t in range(L_)])
+    dg = np.flip(np.cumsum(np.flip(per_tok, 0), 0), 0) + (gam[-1][:, None] * h0 * dht).sum(1)[None]
+    np.testing.assert_allclose(r["dglog"][:, 0], dg, rtol=1e-10, atol=1e-12)
+    dqn = np.stack([s * (gam[t][:, None] * h0) @ c["dO"][t, 0] for t in range(L_)])
+    nq = np.sqrt((c["q"][:, 0] ** 2).sum(-1, keepdims=True) + 1e-6)
+    dq = (dqn - qn * (dqn * qn).sum(-1, keepdims=True)) / nq
+    np.testing.assert_allclose(r["dq"][:, 0], dq, rtol=1e-11, atol=1e-12)
+
+
+def test_retrieval_invariant_fixes_update_order():
+    """With beta = 1 and |kn| = 1 the delta rule overwrites the value stored
+    under the key just written: S_t^T kn_t = v_t.  With q = k the output is then
+    scale * v_t.  Holds for per-channel gates only with the decay applied before
+    the update."""
+    rng = np.random.default_rng(22)
+    c = _rand_case(rng, (12,), 2, 6, "glog")
+    b = np.full((12, 2), np.inf)
+    r = oracle.gated_delta(c["k"], c["k"], c["v"], c["glog"], b, 1.0, c["cu"], h0=c["h0"])
+    # |kn|^2 = |k|^2 / (|k|^2 + 1e-6): the identity holds to ~1e-6 relative
+    np.testing.assert_allclose(r["o"], c["v"], rtol=2e-5, atol=2e-5)
+
+
+def test_single_token_from_zero_state():
+    """T = 1, h0 = 0: S_1 = beta kn v^T, so o = scale * beta * <kn, qn> v."""
+    rng = np.random.default_rng(23)
+    c = _rand_case(rng, (1,), 3, 7, "glog", h0=False, dht=False)
+    r = oracle.gated_delta(c["q"], c["k"], c["v"], c["glog"], c["b"], c["scale"], c["cu"])
+    beta = 1 / (1 + np.exp(-c["b"][0]))
+    dot = (_l2n(c["k"][0]) * _l2n(c["q"][0])).sum(-1)
+    np.testing.assert_allclose(r["o"][0], (c["scale"] * beta * dot)[:, None] * c["v"][0],
+                               rtol=1e-12, atol=1e-14)
+
+
+# ----------------------------------------------------------------------------
+# invariants and consistency
+# ----------------------------------------------------------------------------
+def test_l2_backward_tangency():
+    rng = np.random.default_rng(31)
+    c = _rand_case(rng, (20,), 2, 8, "gdn")
+    r = oracle.gdn(c["q"], c["k"], c["v"], c["g"], c["b"], c["scale"], c["cu"], h0=c["h0"],
+                   dO=c["dO"], dht=c["dht"])
+    for x, dx in ((c["q"], r["dq"]), (c["k"], r["dk"])):
+        dots = (x * dx).sum(-1)
+        scale = np.linalg.norm(x, axis=-1) * np.linalg.norm(dx, axis=-1)
+        assert np.all(np.abs(dots) <= 1e-6 * scale + 1e-14)
+
+
+def test_varlen_equals_separate_runs():
+    rng = np.random.default_rng(32)
+    lens = (7, 1, 66, 0, 13)
+    c = _rand_case(rng, lens, 2, 4, "gdn")
+    r = oracle.gdn(c["q"], c["k"], c["v"], c["g"], c["b"], c["scale"], c["cu"], h0=c["h0"],
+                   dO=c["dO"], dht=c["dht"])
+    cu = c["cu"]
+    for s in range(len(lens)):
+        a, e = cu[s], cu[s + 1]
+        rs = oracle.gdn(c["q"][a:e], c["k"][a:e], c["v"][a:e], c["g"][a:e], c["b"][a:e],
+                        c["scale"], np.array([0, e - a]), h0=c["h0"][s:s + 1],
+                        dO=c["dO"][a:e], dht=c["dht"][s:s + 1])
+        for key in ("o", "dq", "dk", "dv", "dg", "dbeta"):
+            np.testing.assert_array_equal(r[key][a:e], rs[key])
+        for key in ("ht", "dh0"):
+            np.testing.assert_array_equal(r[key][s], rs[key][0])
+    # an empty sequence passes the state gradient straight through
+    np.testing.assert_array_equal(r["dh0"][3], c["dht"][3])
+    np.testing.assert_array_equal(r["ht"][3], c["h0"][3])
+
+
+def test_backward_is_linear_in_cotangents():
+    rng = np.random.default_rng(33)
+    c = _rand_case(rng, (10, 6), 2, 4, "gdn")
+    args = (c["q"], c["k"], c["v"], c["g"], c["b"], c["scale"], c["cu"])
+    dO2 = rng.standard_normal(c["dO"].shape)
+    dht2 = rng.standard_normal(c["dht"].shape)
+    r1 = oracle.gdn(*args, h0=c["h0"], dO=c["dO"], dht=c["dht"])
+    r2 = oracle.gdn(*args, h0=c["h0"], dO=dO2, dht=dht2)
+    r3 = oracle.gdn(*args, h0=c["h0"], dO=2 * c["dO"] - 3 * dO2, dht=2 * c["dht"] - 3 * dht2)
+    for key in ("dq", "dk", "dv", "dg", "dbeta", "dh0"):
+        np.testing.assert_allclose(r3[key], 2 * r1[key] - 3 * r2[key], rtol=1e-10, atol=1e-11)
+
+
+def test_gdn_is_kda_path_with_channel_constant_gate():
+    rng = np.random.default_rng(34)
+    c = _rand_case(rng, (9,), 2, 5, "gdn")
+    r = oracle.gdn(c["q"], c["k"], c["v"], c["g"], c["b"], c["scale"], c["cu"], h0=c["h0"],
+                   dO=c["dO"], dht=c["dht"])
+    glog = np.repeat(c["g"][:, :, None], 5, axis=2)
+    rk = oracle.gated_delta(c["q"], c["k"], c["v"], glog, c["b"], c["scale"], c["cu"],
+                            h0=c["h0"], dO=c["dO"], dht=c["dht"])
+    np.testing.assert_allclose(r["dg"], rk["dglog"].sum(2), rtol=1e-13, atol=1e-14)
+
+
+# ----------------------------------------------------------------------------
+# the chunk-form restatement agrees with the token recurrence
+# ----------------------------------------------------------------------------
+@pytest.mark.parametrize("gate", ["gdn", "glog"])
+def test_chunk_form_matches_token_oracle(gate):
+    rng = np.random.default_rng(41)
+    c = _rand_case(rng, (150, 64, 1), 2, 8, gate)
+    glog = np.repeat(c["g"][:, :, None], 8, 2) if gate == "gdn" else c["glog"]
+    a = oracle.gated_delta(c["q"], c["k"], c["v"], glog, c["b"], c["scale"], c["cu"], h0=c["h0"],
+                           dO=c["dO"], dht=c["dht"])
+    b = chunk_form.gated_delta(c["q"], c["k"], c["v"], glog, c["b"], c["scale"], c["cu"],
+                               h0=c["h0"], dO=c["dO"], dht=c["dht"])
+    for key in ("o", "ht", "dq", "dk", "dv", "dglog", "dbeta", "dh0"):
+        np.testing.assert_allclose(b[key], a[key], rtol=1e-8, atol=1e-9 * np.abs(a[key]).max(),
+                                   err_msg=key)
