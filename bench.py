@@ -1,0 +1,380 @@
+"""Benchmark of the chunked gated delta-rule backward on GB300.
+
+One step = one GDN backward and one KDA backward over the long-sequence
+workload (B=1, H=16, T=32768, D=128, chunk 64), each computing every gradient
+(dq, dk, dv, dg / dg_raw, dbeta, dh0, dA_log, ddt_bias) from the inputs alone
+(the chunk states are recomputed inside the call).  Inputs are seeded,
+synthetic, resident in HBM before timing, and larger than L2 (about 0.6 GB per
+variant), so no L2 flush is needed between steps.
+
+Prints one JSON line (rank 0).  Under torchrun each rank runs its own replica
+on its own GPU (weak scaling, no data-path collective); the barrier and the
+max over ranks are the only cross-rank operations.
+
+``--impl reference`` times the float64 CPU oracle instead (a bounded sample of
+the same workload on the host cores) on the same metric.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from chunked_gated_delta_bwd_gb300 import inputs  # noqa: E402
+
+WORKLOAD = "gdn+kda bwd, B=1 H=16 T=32768 D=128 chunk=64"
+METRIC = "GDN+KDA bwd Mtokens/s at H16 T32k D128"
+UNIT = "Mtokens/s"
+CASE_G, CASE_K = inputs.CASES["gdn_h16_t32k"], inputs.CASES["kda_h16_t32k"]
+TOKENS_PER_STEP = CASE_G.seq_len * CASE_G.num_seqs + CASE_K.seq_len * CASE_K.num_seqs
+
+# Algorithmic figures of the main backward kernel per token-head (D = 128, C = 64):
+# 16 products per chunk: 5 of C*D*D and 11 of C*C*D  ->  10 D^2 + 22 C D flops;
+# bytes: q,k,v,dO + beta + gate + S0 + dS_C + T read, dq,dk,dv + dbeta + dgate written.
+D_, C_ = 128, 64
+MAIN_FLOP_PER_TH = 10 * D_ * D_ + 22 * C_ * D_
+MAIN_BYTES_PER_TH = {"gdn": 4 * 2 * D_ + 2 + 4 + 2 * (2 * D_ * D_ // C_) + 2 * C_ + 3 * 2 * D_ + 2 + 4,
+                     "kda": 4 * 2 * D_ + 2 + 2 * D_ + 2 * (2 * D_ * D_ // C_) + 2 * C_ + 3 * 2 * D_ + 2 + 2 * D_}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d["hbm_gbs"], d["bf16_tflops"], d.get("bf16_tflops_sustained", d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def dist_info():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    return int(os.environ.get("RANK", "0")), ws, int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def max_over_ranks(x, world):
+    """Max of a float over ranks (identity for a single process)."""
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+class Clocks:
+    """Samples SM clocks and throttle reasons with nvidia-smi during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = max(mx, float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx or None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# oracle (CPU) timing: bounded sample of the same workload
+# ---------------------------------------------------------------------------
+def oracle_sample_seconds(tokens):
+    """Times the float64 oracle on the first `tokens` tokens of both variants, all heads."""
+    from oracle import oracle
+    import numpy as np
+    t0 = time.perf_counter()
+    for case in (CASE_G, CASE_K):
+        x = inputs.make(inputs.Case(case.name + "_sample", case.mode, 1, tokens, case.heads, case.dim,
+                                    case.seed, with_h0=case.with_h0, with_dht=case.with_dht))
+        f = lambda t: None if t is None else t.to(torch.float64).numpy()
+        cu = np.array([0, tokens])
+        if case.mode == "gdn":
+            oracle.gdn(f(x["q"]), f(x["k"]), f(x["v"]), f(x["g"]), f(x["beta_logit"]), x["scale"], cu,
+                       h0=f(x["h0"]), dO=f(x["dO"]), dht=f(x["dht"]))
+        else:
+            oracle.kda(f(x["q"]), f(x["k"]), f(x["v"]), f(x["g_raw"]), f(x["A_log"]), f(x["dt_bias"]),
+                       f(x["beta_logit"]), x["scale"], cu, h0=f(x["h0"]), dO=f(x["dO"]), dht=f(x["dht"]))
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(tokens):
+    from oracle import build as obuild, oracle
+    obuild.build()
+    secs = oracle_sample_seconds(tokens)
+    cores = min(oracle.max_threads(), CASE_G.heads)
+    return {"value": 2 * tokens / secs / 1e6, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": "float64 oracle, first %d tokens of the GDN and the KDA sequence, all %d heads "
+                      "(forward + backward); %.2f s on %d host threads (host has %d cores)"
+                      % (tokens, CASE_G.heads, secs, cores, os.cpu_count() or 0)}
+
+
+def run_reference(args):
+    rank, world, _ = dist_info()
+    if world > 1 and rank != 0:
+        return
+    tokens = args.ref_tokens
+    from oracle import build as obuild, oracle
+    obuild.build()
+    for _ in range(args.warmup):
+        oracle_sample_seconds(tokens)
+    secs = [oracle_sample_seconds(tokens) for _ in range(args.steps)]
+    total = sum(secs)
+    value = 2 * tokens * args.steps / total / 1e6
+    cores = min(oracle.max_threads(), CASE_G.heads)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD + " (oracle: first %d tokens per variant per step)" % tokens},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": "float64 oracle, first %d tokens of the GDN and the KDA sequence, "
+                                       "all %d heads, per step" % (tokens, CASE_G.heads)},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+def main_gpu(args):
+    import chunked_gated_delta_bwd_gb300 as gdr
+    from chunked_gated_delta_bwd_gb300 import api, build
+    rank, world, local = dist_info()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    build.build()
+
+    xg = inputs.make(CASE_G)
+    xk = inputs.make(CASE_K)
+    dev = lambda x: {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    G, K = dev(xg), dev(xk)
+    T, Hh, D = G["q"].shape
+    N = 1
+    ws_g = torch.empty(gdr.workspace_bytes(gdr.make_shape(N, T, Hh, D)), dtype=torch.uint8, device="cuda")
+    ws_k = torch.empty_like(ws_g)
+    out_g = gdr.alloc_outputs(T, Hh, D, N, "gdn")
+    out_k = gdr.alloc_outputs(T, Hh, D, N, "kda")
+
+    def step_g(A=G, o=out_g):
+        gdr.gdr_bwd(A["q"], A["k"], A["v"], A["g"], A["beta_logit"], A["dO"], h0=A["h0"], dht=A["dht"],
+                    num_seqs=N, scale=A["scale"], workspace=ws_g, out=o)
+
+    def step_k(A=K, o=out_k):
+        gdr.kda_bwd(A["q"], A["k"], A["v"], A["g_raw"], A["A_log"], A["dt_bias"], A["beta_logit"], A["dO"],
+                    h0=A["h0"], dht=A["dht"], num_seqs=N, scale=A["scale"], workspace=ws_k, out=o)
+
+    def step():
+        step_g()
+        step_k()
+
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    for w in (ws_g, ws_k):
+        st = gdr.workspace_status(w)
+        if st:
+            raise RuntimeError("device status %d raised by the warm-up steps" % st)
+
+    # ---- timed region (device-resident inputs) ----
+    api.profile_begin(16 * args.steps)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with Clocks(local) as clk:
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    prof = api.profile_end()
+    ms_local = e0.elapsed_time(e1) / args.steps
+    ms = max_over_ranks(ms_local, world)
+    value = world * TOKENS_PER_STEP / (ms * 1e-3) / 1e6
+    launches = sum(n for _, n in prof.values())
+
+    # per-variant step times (informational, separate short loops)
+    def time_loop(fn, n=max(3, args.steps // 2)):
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / n
+    ms_g, ms_k = time_loop(step_g), time_loop(step_k)
+
+    # ---- end to end: pinned host inputs -> device -> backward -> host gradients ----
+    def pinned(x):
+        return {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    hg, hk = pinned(xg), pinned(xk)
+    hout_g = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in out_g.items()}
+    hout_k = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in out_k.items()}
+    keys_g = [k for k, v in hg.items() if isinstance(v, torch.Tensor)]
+    keys_k = [k for k, v in hk.items() if isinstance(v, torch.Tensor)]
+    h2d = sum(hg[k].numel() * hg[k].element_size() for k in keys_g if k != "cu_seqlens") + \
+        sum(hk[k].numel() * hk[k].element_size() for k in keys_k if k != "cu_seqlens")
+    d2h = sum(v.numel() * v.element_size() for v in out_g.values()) + \
+        sum(v.numel() * v.element_size() for v in out_k.values())
+
+    def e2e_step():
+        for k in keys_g:
+            if k != "cu_seqlens":
+                G[k].copy_(hg[k], non_blocking=True)
+        for k in keys_k:
+            if k != "cu_seqlens":
+                K[k].copy_(hk[k], non_blocking=True)
+        step()
+        for k, v in out_g.items():
+            hout_g[k].copy_(v, non_blocking=True)
+        for k, v in out_k.items():
+            hout_k[k].copy_(v, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(a.elapsed_time(b) / args.steps, world)
+    e2e_value = world * TOKENS_PER_STEP / (e2e_ms * 1e-3) / 1e6
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    # ---- roofline of the dominant kernel ----
+    hbm, tf_burst, tf_sus, src = peaks()
+    dom = max(prof, key=lambda k: prof[k][0])
+    th = CASE_G.seq_len * CASE_G.heads  # token-heads per variant
+    roof = None
+    if dom == "main" and prof["main"][1] > 0:
+        n_main = prof["main"][1]
+        avg_s = prof["main"][0] / n_main * 1e-3
+        bytes_avg = th * (MAIN_BYTES_PER_TH["gdn"] + MAIN_BYTES_PER_TH["kda"]) / 2
+        flop = th * MAIN_FLOP_PER_TH
+        ach = bytes_avg / avg_s / 1e9
+        traffic = None
+        tp = os.path.join(ROOT, "profiles", "main_traffic.json")
+        if os.path.exists(tp):
+            t = json.load(open(tp))
+            if t.get("source_sha") == build_sha():
+                traffic = t.get("bytes_per_launch")
+        roof = {"kernel": "k_main (avg of the GDN and KDA launches)", "bound": "hbm", "achieved": ach,
+                "peak": hbm, "unit": "GB/s", "frac": ach / hbm, "traffic": traffic,
+                "peak_source": src + " (hbm_gbs)",
+                "tensor_tflops": flop / avg_s / 1e12, "tensor_frac": flop / avg_s / 1e12 / tf_sus,
+                "tensor_peak": tf_sus}
+    else:
+        k = dom
+        roof = {"kernel": k, "bound": "hbm", "achieved": None, "peak": hbm, "unit": "GB/s", "frac": None,
+                "traffic": None, "note": "dominant kernel has no algorithmic figure yet"}
+
+    csum = clk.summary()
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "variants_ms": {"gdn": ms_g, "kda": ms_k},
+                   "l2": "inputs larger than L2 (no flush)", "parallelism": "replicas" if world > 1 else "1 GPU"},
+        "roofline": roof,
+        "kernels_ms_per_step": {k: v[0] / args.steps for k, v in prof.items()},
+        "gpu_launches": launches,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms},
+        "clocks": csum,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.cpu_tokens)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def build_sha():
+    import hashlib
+    h = hashlib.sha1()
+    csrc = os.path.join(ROOT, "chunked_gated_delta_bwd_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:12]
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-tokens", type=int, default=8192)
+    ap.add_argument("--ref-tokens", type=int, default=1024)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        main_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

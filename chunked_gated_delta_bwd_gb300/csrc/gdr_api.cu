@@ -1,0 +1,360 @@
+// C ABI of the library (declared in include/gdr.h): argument checks, the
+// workspace layout, the varlen chunk table and the launch sequence.
+#include <stdio.h>
+#include <string.h>
+
+#include "../../include/gdr.h"
+#include "gdr_common.cuh"
+#include "gdr_internal.h"
+
+namespace gdr {
+
+static thread_local char g_err[512] = "";
+
+static gdr_status fail(gdr_status s, const char* fmt, const char* what = "") {
+    snprintf(g_err, sizeof(g_err), fmt, what);
+    return s;
+}
+
+static gdr_status cuda_fail(cudaError_t e, const char* where) {
+    snprintf(g_err, sizeof(g_err), "%s: %s", where, cudaGetErrorString(e));
+    return GDR_ERR_CUDA;
+}
+
+// chunk_off[s] = sum_{i<s} ceil(len_i / 64); validates cu_seqlens on the device.
+// One CTA of 1024 threads; thread t owns a contiguous range of sequences.
+__global__ void __launch_bounds__(1024) k_chunk_table(const int64_t* cu, int N, int64_t T, int* chunk_off,
+                                                      int* status) {
+    __shared__ int s_tot[1024];
+    __shared__ int s_bad;
+    const int t = threadIdx.x;
+    if (t == 0) s_bad = 0;
+    __syncthreads();
+    const int per = (N + 1023) / 1024;
+    const int a = min(N, t * per), b = min(N, a + per);
+    int cnt = 0;
+    bool bad = false;
+    for (int s = a; s < b; ++s) {
+        const int64_t l = cu[s + 1] - cu[s];
+        if (l < 0) bad = true;
+        else cnt += (int)((l + CH - 1) / CH);
+    }
+    if (t == 0 && (cu[0] != 0 || cu[N] != T)) bad = true;
+    if (bad) atomicOr(&s_bad, 1);
+    s_tot[t] = cnt;
+    __syncthreads();
+    // inclusive scan of the per-thread totals (Hillis-Steele)
+    for (int o = 1; o < 1024; o <<= 1) {
+        const int v = t >= o ? s_tot[t - o] : 0;
+        __syncthreads();
+        s_tot[t] += v;
+        __syncthreads();
+    }
+    if (s_bad) {
+        for (int s = t; s <= N; s += 1024) chunk_off[s] = 0;
+        if (t == 0) atomicOr(status, ST_BAD_SEQLENS);
+        return;
+    }
+    int run = s_tot[t] - cnt;
+    for (int s = a; s < b; ++s) {
+        chunk_off[s] = run;
+        run += (int)((cu[s + 1] - cu[s] + CH - 1) / CH);
+    }
+    if (t == 1023) chunk_off[N] = s_tot[1023];
+}
+
+cudaError_t launch_chunk_table(const Params& p, cudaStream_t s) {
+    k_chunk_table<<<1, 1024, 0, s>>>(p.cu_seqlens, p.N, p.T_total, const_cast<int*>(p.chunk_off), p.status);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// workspace layout
+// ---------------------------------------------------------------------------
+struct Layout {
+    int64_t max_chunks;
+    size_t status, chunk_off, W, U, Kr, R, T, gT, S0, dS, total;
+};
+
+static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+static gdr_status check_shape(const gdr_shape* sh) {
+    if (!sh) return fail(GDR_ERR_INVALID, "shape is NULL");
+    if (sh->num_seqs < 1 || sh->num_heads < 1 || sh->total_tokens < 0)
+        return fail(GDR_ERR_INVALID, "num_seqs and num_heads must be >= 1, total_tokens >= 0");
+    if (sh->head_dim != 64 && sh->head_dim != 128)
+        return fail(GDR_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+    if (!sh->cu_seqlens && sh->total_tokens % sh->num_seqs != 0)
+        return fail(GDR_ERR_INVALID, "dense layout needs total_tokens divisible by num_seqs");
+    if (sh->num_heads > 65535) return fail(GDR_ERR_INVALID, "num_heads must be <= 65535");
+    const int64_t N = sh->num_seqs, T = sh->total_tokens;
+    const int64_t mc = sh->cu_seqlens ? (T + (CH - 1) * N) / CH : N * ((T / N + CH - 1) / CH);
+    if (mc > (int64_t)1 << 30 || N * sh->num_heads * (sh->head_dim / 16) > ((int64_t)1 << 31) - 1)
+        return fail(GDR_ERR_INVALID, "problem too large for one call");
+    return GDR_OK;
+}
+
+static Layout layout(const gdr_shape* sh) {
+    Layout L{};
+    const int64_t N = sh->num_seqs, H = sh->num_heads, D = sh->head_dim, T = sh->total_tokens;
+    if (sh->cu_seqlens) L.max_chunks = (T + (CH - 1) * N) / CH;
+    else L.max_chunks = N * ((T / N + CH - 1) / CH);
+    const size_t mc = (size_t)L.max_chunks;
+    size_t o = 0;
+    L.status = o; o = align256(o + 16);
+    L.chunk_off = o; o = align256(o + 4 * (size_t)(N + 1));
+    L.W = o; o = align256(o + mc * H * CH * D * 2);
+    L.U = o; o = align256(o + mc * H * CH * D * 2);
+    L.Kr = o; o = align256(o + mc * H * CH * D * 2);
+    L.R = o; o = align256(o + mc * H * CH * D * 2);
+    L.T = o; o = align256(o + mc * H * CH * CH * 2);
+    L.gT = o; o = align256(o + mc * H * D * 4);
+    L.S0 = o; o = align256(o + mc * H * D * D * 2);
+    L.dS = o; o = align256(o + mc * H * D * D * 2);
+    L.total = o;
+    return L;
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+#define NEED(ptr)                                                                    \
+    do {                                                                             \
+        if (!(ptr)) return fail(GDR_ERR_INVALID, "required pointer %s is NULL", #ptr); \
+        if (!aligned16(ptr)) return fail(GDR_ERR_INVALID, "pointer %s is not 16-byte aligned", #ptr); \
+    } while (0)
+#define OPT(ptr)                                                                     \
+    do {                                                                             \
+        if ((ptr) && !aligned16(ptr)) return fail(GDR_ERR_INVALID, "pointer %s is not 16-byte aligned", #ptr); \
+    } while (0)
+
+static void base_params(Params& p, const gdr_shape* sh, const Layout& L, void* ws, int kda) {
+    memset(&p, 0, sizeof(p));
+    p.N = sh->num_seqs;
+    p.H = sh->num_heads;
+    p.D = sh->head_dim;
+    p.T_total = sh->total_tokens;
+    p.seq_len = sh->cu_seqlens ? 0 : sh->total_tokens / sh->num_seqs;
+    p.max_chunks = (int)L.max_chunks;
+    p.cu_seqlens = sh->cu_seqlens;
+    p.scale = sh->scale;
+    p.kda = kda;
+    unsigned char* w = static_cast<unsigned char*>(ws);
+    p.status = reinterpret_cast<int*>(w + L.status);
+    p.chunk_off = sh->cu_seqlens ? reinterpret_cast<int*>(w + L.chunk_off) : nullptr;
+    p.W = reinterpret_cast<__nv_bfloat16*>(w + L.W);
+    p.U = reinterpret_cast<__nv_bfloat16*>(w + L.U);
+    p.Kr = reinterpret_cast<__nv_bfloat16*>(w + L.Kr);
+    p.R = reinterpret_cast<__nv_bfloat16*>(w + L.R);
+    p.Tm = reinterpret_cast<__nv_bfloat16*>(w + L.T);
+    p.gT = reinterpret_cast<float*>(w + L.gT);
+    p.S0 = reinterpret_cast<__nv_bfloat16*>(w + L.S0);
+    p.dS = reinterpret_cast<__nv_bfloat16*>(w + L.dS);
+}
+
+// ---------------------------------------------------------------------------
+// optional per-kernel event timing (gdr_profile_begin / gdr_profile_end)
+// ---------------------------------------------------------------------------
+struct Prof {
+    bool on = false;
+    int max_launches = 0, n = 0;
+    cudaEvent_t* ev = nullptr;  // 2 per launch
+    int* kind = nullptr;
+};
+static Prof g_prof;
+
+// Launches `f` between two recorded events when profiling is on.
+template <class F>
+static cudaError_t timed(int kind, cudaStream_t s, F&& f) {
+    if (!g_prof.on || g_prof.n >= g_prof.max_launches) return f();
+    const int i = g_prof.n++;
+    g_prof.kind[i] = kind;
+    cudaEventRecord(g_prof.ev[2 * i], s);
+    cudaError_t e = f();
+    cudaEventRecord(g_prof.ev[2 * i + 1], s);
+    return e;
+}
+
+// status reset + chunk table (+ prep)
+static gdr_status common_front(const Params& p, cudaStream_t s) {
+    cudaError_t e = cudaMemsetAsync(p.status, 0, sizeof(int), s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(status)");
+    if (p.cu_seqlens) {
+        e = timed(GDR_KERNEL_CHUNK_TABLE, s, [&] { return launch_chunk_table(p, s); });
+        if (e != cudaSuccess) return cuda_fail(e, "chunk table launch");
+    }
+    e = timed(GDR_KERNEL_PREP, s, [&] { return launch_prep(p, s); });
+    if (e != cudaSuccess) return cuda_fail(e, "prep launch");
+    return GDR_OK;
+}
+
+static gdr_status fwd_states_impl(const gdr_shape* sh, const void* q, const void* k, const void* v,
+                                  const float* g, const void* g_raw, const float* A_log,
+                                  const float* dt_bias, const void* beta, const float* h0,
+                                  void* states, size_t states_bytes, void* ws, size_t ws_bytes,
+                                  void* stream, int kda) {
+    if (gdr_status st0 = check_shape(sh)) return st0;
+    NEED(q); NEED(k); NEED(v); NEED(beta); NEED(ws); NEED(states); OPT(h0);
+    if (kda) { NEED(g_raw); NEED(A_log); NEED(dt_bias); } else { NEED(g); }
+    const Layout L = layout(sh);
+    if (ws_bytes < L.total) return fail(GDR_ERR_WORKSPACE, "workspace too small%s");
+    if (states_bytes < gdr_states_bytes(sh)) return fail(GDR_ERR_WORKSPACE, "states buffer too small%s");
+    Params p;
+    base_params(p, sh, L, ws, kda);
+    p.q = (const __nv_bfloat16*)q; p.k = (const __nv_bfloat16*)k; p.v = (const __nv_bfloat16*)v;
+    p.beta_logit = (const __nv_bfloat16*)beta;
+    p.g = g; p.g_raw = (const __nv_bfloat16*)g_raw; p.A_log = A_log; p.dt_bias = dt_bias;
+    p.h0 = h0;
+    p.S0 = (__nv_bfloat16*)states;
+    cudaStream_t s = (cudaStream_t)stream;
+    gdr_status st = common_front(p, s);
+    if (st != GDR_OK) return st;
+    cudaError_t e = timed(GDR_KERNEL_STATES, s, [&] { return launch_states(p, true, false, s); });
+    if (e != cudaSuccess) return cuda_fail(e, "state recurrence launch");
+    g_err[0] = 0;
+    return GDR_OK;
+}
+
+static gdr_status bwd_impl(const gdr_shape* sh, const void* q, const void* k, const void* v,
+                           const float* g, const void* g_raw, const float* A_log, const float* dt_bias,
+                           const void* beta, const float* h0, const void* dO, const float* dht,
+                           const void* states, void* ws, size_t ws_bytes, void* dq, void* dk, void* dv,
+                           float* dg, void* dg_raw, void* dbeta, float* dh0, float* dA_log,
+                           float* ddt_bias, void* stream, int kda) {
+    if (gdr_status st0 = check_shape(sh)) return st0;
+    NEED(q); NEED(k); NEED(v); NEED(beta); NEED(dO); NEED(ws);
+    NEED(dq); NEED(dk); NEED(dv); NEED(dbeta); NEED(dh0);
+    OPT(h0); OPT(dht); OPT(states);
+    if (kda) { NEED(g_raw); NEED(A_log); NEED(dt_bias); NEED(dg_raw); NEED(dA_log); NEED(ddt_bias); }
+    else { NEED(g); NEED(dg); }
+    const Layout L = layout(sh);
+    if (ws_bytes < L.total) return fail(GDR_ERR_WORKSPACE, "workspace too small%s");
+    Params p;
+    base_params(p, sh, L, ws, kda);
+    p.q = (const __nv_bfloat16*)q; p.k = (const __nv_bfloat16*)k; p.v = (const __nv_bfloat16*)v;
+    p.dO = (const __nv_bfloat16*)dO; p.beta_logit = (const __nv_bfloat16*)beta;
+    p.g = g; p.g_raw = (const __nv_bfloat16*)g_raw; p.A_log = A_log; p.dt_bias = dt_bias;
+    p.h0 = h0; p.dht = dht;
+    if (states) p.S0 = (__nv_bfloat16*)states;
+    p.dq = (__nv_bfloat16*)dq; p.dk = (__nv_bfloat16*)dk; p.dv = (__nv_bfloat16*)dv;
+    p.dbeta = (__nv_bfloat16*)dbeta; p.dg = dg; p.dg_raw = (__nv_bfloat16*)dg_raw;
+    p.dh0 = dh0; p.dA_log = dA_log; p.ddt_bias = ddt_bias;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (kda) {
+        cudaError_t e = cudaMemsetAsync(dA_log, 0, sizeof(float) * p.H, s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(ddt_bias, 0, sizeof(float) * p.H * p.D, s);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(dA_log/ddt_bias)");
+    }
+    gdr_status st = common_front(p, s);
+    if (st != GDR_OK) return st;
+    cudaError_t e = timed(GDR_KERNEL_STATES, s, [&] { return launch_states(p, states == nullptr, true, s); });
+    if (e != cudaSuccess) return cuda_fail(e, "state recurrence launch");
+    e = timed(GDR_KERNEL_MAIN, s, [&] { return launch_main(p, s); });
+    if (e != cudaSuccess) return cuda_fail(e, "main backward launch");
+    g_err[0] = 0;
+    return GDR_OK;
+}
+
+}  // namespace gdr
+
+using namespace gdr;
+
+extern "C" {
+
+size_t gdr_workspace_bytes(const gdr_shape* shape) {
+    if (check_shape(shape) != GDR_OK) return 0;
+    return layout(shape).total;
+}
+
+size_t gdr_states_bytes(const gdr_shape* shape) {
+    if (check_shape(shape) != GDR_OK) return 0;
+    const Layout L = layout(shape);
+    return (size_t)L.max_chunks * shape->num_heads * shape->head_dim * shape->head_dim * 2;
+}
+
+gdr_status gdr_fwd_states(const gdr_shape* shape, const void* q, const void* k, const void* v,
+                          const float* g, const void* beta_logit, const float* h0, void* states,
+                          size_t states_bytes, void* workspace, size_t workspace_bytes, void* stream) {
+    return fwd_states_impl(shape, q, k, v, g, nullptr, nullptr, nullptr, beta_logit, h0, states,
+                           states_bytes, workspace, workspace_bytes, stream, 0);
+}
+
+gdr_status kda_fwd_states(const gdr_shape* shape, const void* q, const void* k, const void* v,
+                          const void* g_raw, const float* A_log, const float* dt_bias,
+                          const void* beta_logit, const float* h0, void* states, size_t states_bytes,
+                          void* workspace, size_t workspace_bytes, void* stream) {
+    return fwd_states_impl(shape, q, k, v, nullptr, g_raw, A_log, dt_bias, beta_logit, h0, states,
+                           states_bytes, workspace, workspace_bytes, stream, 1);
+}
+
+gdr_status gdr_bwd(const gdr_shape* shape, const void* q, const void* k, const void* v, const float* g,
+                   const void* beta_logit, const float* h0, const void* dO, const float* dht,
+                   const void* states, void* workspace, size_t workspace_bytes, void* dq, void* dk,
+                   void* dv, float* dg, void* dbeta, float* dh0, void* stream) {
+    return bwd_impl(shape, q, k, v, g, nullptr, nullptr, nullptr, beta_logit, h0, dO, dht, states,
+                    workspace, workspace_bytes, dq, dk, dv, dg, nullptr, dbeta, dh0, nullptr, nullptr,
+                    stream, 0);
+}
+
+gdr_status kda_bwd(const gdr_shape* shape, const void* q, const void* k, const void* v, const void* g_raw,
+                   const float* A_log, const float* dt_bias, const void* beta_logit, const float* h0,
+                   const void* dO, const float* dht, const void* states, void* workspace,
+                   size_t workspace_bytes, void* dq, void* dk, void* dv, void* dg_raw, void* dbeta,
+                   float* dh0, float* dA_log, float* ddt_bias, void* stream) {
+    return bwd_impl(shape, q, k, v, nullptr, g_raw, A_log, dt_bias, beta_logit, h0, dO, dht, states,
+                    workspace, workspace_bytes, dq, dk, dv, nullptr, dg_raw, dbeta, dh0, dA_log, ddt_bias,
+                    stream, 1);
+}
+
+gdr_status gdr_workspace_status(const void* workspace, void* stream, int* device_status) {
+    if (!workspace || !device_status) return fail(GDR_ERR_INVALID, "workspace and device_status must be non-NULL%s");
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    int v = 0;
+    e = cudaMemcpy(&v, workspace, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(status)");
+    *device_status = v;
+    return GDR_OK;
+}
+
+const char* gdr_last_error(void) { return g_err; }
+
+gdr_status gdr_profile_begin(int max_launches) {
+    if (max_launches <= 0) return fail(GDR_ERR_INVALID, "max_launches must be > 0%s");
+    if (g_prof.ev) {
+        for (int i = 0; i < 2 * g_prof.max_launches; ++i) cudaEventDestroy(g_prof.ev[i]);
+        delete[] g_prof.ev;
+        delete[] g_prof.kind;
+    }
+    g_prof = Prof();
+    g_prof.ev = new cudaEvent_t[2 * max_launches];
+    g_prof.kind = new int[max_launches];
+    for (int i = 0; i < 2 * max_launches; ++i) {
+        cudaError_t e = cudaEventCreate(&g_prof.ev[i]);
+        if (e != cudaSuccess) {
+            g_prof.max_launches = i / 2;
+            return cuda_fail(e, "cudaEventCreate");
+        }
+    }
+    g_prof.max_launches = max_launches;
+    g_prof.on = true;
+    return GDR_OK;
+}
+
+gdr_status gdr_profile_end(double* total_ms, int* launches) {
+    if (!total_ms || !launches) return fail(GDR_ERR_INVALID, "output arrays must be non-NULL%s");
+    for (int k = 0; k < GDR_KERNEL_COUNT; ++k) { total_ms[k] = 0.0; launches[k] = 0; }
+    g_prof.on = false;
+    for (int i = 0; i < g_prof.n; ++i) {
+        cudaError_t e = cudaEventSynchronize(g_prof.ev[2 * i + 1]);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaEventSynchronize");
+        float ms = 0.f;
+        e = cudaEventElapsedTime(&ms, g_prof.ev[2 * i], g_prof.ev[2 * i + 1]);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaEventElapsedTime");
+        total_ms[g_prof.kind[i]] += ms;
+        launches[g_prof.kind[i]] += 1;
+    }
+    g_prof.n = 0;
+    return GDR_OK;
+}
+
+}  // extern "C"

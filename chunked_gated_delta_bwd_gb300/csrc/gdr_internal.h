@@ -1,0 +1,46 @@
+// Internal launch parameters shared by the host launcher and the kernels.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace gdr {
+
+struct Params {
+    // shape
+    int N, H, D;
+    int64_t T_total;
+    int64_t seq_len;        // dense layout: tokens per sequence (T_total / N)
+    int max_chunks;         // upper bound on the number of chunks (grid size)
+    const int64_t* cu_seqlens;  // device [N+1] or nullptr (dense)
+    const int* chunk_off;   // device [N+1] chunk prefix sums, or nullptr (dense)
+    float scale;
+    int kda;                // 0: scalar GDN gate, 1: per-channel KDA gate
+
+    // inputs
+    const __nv_bfloat16 *q, *k, *v, *dO, *beta_logit;
+    const float* g;                 // GDN log gate [T,H]
+    const __nv_bfloat16* g_raw;     // KDA raw gate [T,H,D]
+    const float *A_log, *dt_bias;   // KDA [H], [H,D]
+    const float *h0, *dht;          // [N,H,D,D] or nullptr
+
+    // workspace
+    int* status;
+    __nv_bfloat16 *W, *U, *Kr, *R, *Tm;  // per chunk-head tiles: [C][D] x4, [C][C]
+    float* gT;                           // [chunk][H][D]
+    __nv_bfloat16 *S0, *dS;              // per chunk-head states [D][D]
+
+    // outputs
+    __nv_bfloat16 *dq, *dk, *dv, *dbeta;
+    float* dg;                      // GDN [T,H]
+    __nv_bfloat16* dg_raw;          // KDA [T,H,D]
+    float *dh0, *dA_log, *ddt_bias;
+};
+
+cudaError_t launch_chunk_table(const Params& p, cudaStream_t s);
+cudaError_t launch_prep(const Params& p, cudaStream_t s);
+cudaError_t launch_states(const Params& p, bool fwd, bool bwd, cudaStream_t s);
+cudaError_t launch_main(const Params& p, cudaStream_t s);
+
+}  // namespace gdr

@@ -1,0 +1,510 @@
+// Chunk-parallel main backward kernel: one CTA (8 warps) per (chunk, head).
+//
+// Given the chunk-start state S0 and the state gradient at the chunk end dS_C
+// (both from the serial recurrences), every gradient of the chunk is local.
+// Forward quantities are recomputed (chunk algebra of the gated delta rule,
+// UT/WY form):
+//   A  = strict_lower(diag(beta) kd' ki'^T),  P = lower(qd' ki'^T)
+//   E  = V - kd S0,  Y = diag(beta) E,  u = T Y   (T = (I + A)^-1 from the prep kernel)
+// and the reverse pass is, in order,
+//   dqd  = dO S0^T                              du  = P^T dO + kr dS_C
+//   dY   = T^T du,  dv = beta dY                dkd = -beta (dY S0^T)
+//   dkr  = u dS_C^T                             dgT = e^{gT} rowsum(dS_C . S0) + colsum(dkr . kr)
+//   dP   = lower(dO u^T)                        dA  = -strict_lower(dY u^T)
+//   dqd' = dP ki',  dkd' = (beta dA) ki'        dki' = dP^T qd' + (beta dA)^T kd'
+//   dlogit = (1 - beta) (<dY, beta E> + rowsum(dA . A))
+// and the elementwise assembly of "FlashKDA之backward（K1）" (§3.2-§3.3, §5):
+//   dqn = scale (dqd e^{gc} + dqd' e^{gc-ref})
+//   dkn = dkd e^{gc} + dkd' e^{gc-ref} + dki' e^{ref-gc} + dkr e^{gT-gc}
+//   dgc = qn dqn + kn (dkd e^{gc} + dkd' e^{gc-ref} - dki' e^{ref-gc} - dkr e^{gT-gc})
+//   L2-norm backward of dqn, dkn; dg = reverse_cumsum(dgc) + dgT; the GDN
+//   gate gradient is the channel sum, the KDA gate runs its chain rule and
+//   reduces dA_log, ddt_bias with one atomic per CTA and channel.
+// The per-element gradients w.r.t. qn and kn live in registers for the whole
+// kernel: every C x D product uses the same warp tiling.
+#include "gdr_chunk.cuh"
+
+namespace gdr {
+
+template <int D, bool KDA>
+struct MainSmem {
+    static constexpr int ROWB = 2 * D;
+    static constexpr int TCD = CH * ROWB;
+    static constexpr int TDD = D * ROWB;
+    static constexpr int TCC = CH * 128;
+    static constexpr int oK = 0, oV = oK + TCD, oDO = oV + TCD, oS0 = oDO + TCD, oDS = oS0 + TDD,
+                         oT = oDS + TDD, oA = oT + TCC, oP = oA + TCC, oU = oP + TCC, oX1 = oU + TCD,
+                         oX2 = oX1 + TCD, oG = oX2 + TCD, oSmall = oG + Gates<D, KDA>::floats() * 4;
+    // small arrays (floats): invQ, invK, beta, dbeta, fac[4][C], dgT[D], rowq[2][C], rowk[2][C], misc[64]
+    static constexpr int nSmall = CH * 4 + 4 * CH + D + 4 * CH + 64;
+    static constexpr int bytes = oSmall + nSmall * 4;
+    static_assert(2 * TDD >= CH * D * 4, "dgc scratch must fit in the state tiles");
+};
+
+template <int D, bool KDA>
+__global__ void __launch_bounds__(256, 1) k_main(const Params p) {
+    using SM = MainSmem<D, KDA>;
+    using TileCD = SwzTile<SM::ROWB>;
+    using TileCC = SwzTile<128>;
+    constexpr int NTD = D / 16;
+    extern __shared__ __align__(1024) unsigned char smem[];
+
+    const int chunk = blockIdx.x, h = blockIdx.y;
+    ChunkInfo ci;
+    if (!lookup_chunk(chunk, p.N, p.chunk_off, p.cu_seqlens, p.seq_len, ci)) return;
+
+    TileCD sK{smem + SM::oK}, sV{smem + SM::oV}, sDO{smem + SM::oDO}, sU{smem + SM::oU},
+        sX1{smem + SM::oX1}, sX2{smem + SM::oX2};
+    TileCD sS0{smem + SM::oS0}, sDS{smem + SM::oDS};  // D x D tiles, same row size
+    TileCC sT{smem + SM::oT}, sA{smem + SM::oA}, sP{smem + SM::oP};
+    float* gbase = reinterpret_cast<float*>(smem + SM::oG);
+    Gates<D, KDA> G;
+    G.gc = gbase;
+    G.ref = gbase + (KDA ? CH * G.LDG : CH);
+    G.gT = G.ref + (KDA ? D : 1);
+    float* sInvQ = reinterpret_cast<float*>(smem + SM::oSmall);
+    float* sInvK = sInvQ + CH;
+    float* sBeta = sInvK + CH;
+    float* sDbeta = sBeta + CH;
+    float* sFac = sDbeta + CH;      // GDN per-row factors [4][C]
+    float* sDgT = sFac + 4 * CH;    // [D]
+    float* sRowQ = sDgT + D;        // [2][C]
+    float* sRowK = sRowQ + 2 * CH;  // [2][C]
+    float* sMisc = sRowK + 2 * CH;  // [64]
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const size_t tdd = ((size_t)chunk * p.H + h) * D * D;
+    const size_t tcc = ((size_t)chunk * p.H + h) * CH * CH;
+
+    // ---- loads -------------------------------------------------------------
+    async_load_rows<D>(sK, p.k, p, ci, h);
+    async_load_rows<D>(sV, p.v, p, ci, h);
+    async_load_rows<D>(sDO, p.dO, p, ci, h);
+    async_load_tile<D, D>(sS0, p.S0 + tdd);
+    async_load_tile<D, D>(sDS, p.dS + tdd);
+    async_load_tile<CH, CH>(sT, p.Tm + tcc);
+    cp_async_commit();
+    load_gates<D, KDA>(p, ci, h, G, false);
+    load_beta(p, ci, h, sBeta);
+    row_inv_norms_global<D>(p.q, p, ci, h, sInvQ);
+    for (int i = threadIdx.x; i < CH; i += blockDim.x) sDbeta[i] = 0.f;
+    for (int i = threadIdx.x; i < D; i += blockDim.x) sDgT[i] = 0.f;
+    cp_async_wait<0>();
+    __syncthreads();
+    row_inv_norms_smem<D>(sK, sInvK);
+    if (!KDA) {
+        for (int r = threadIdx.x; r < CH; r += blockDim.x) {
+            sFac[0 * CH + r] = gate_factor<F_KD>(G, r, 0);
+            sFac[1 * CH + r] = gate_factor<F_KDP>(G, r, 0);
+            sFac[2 * CH + r] = gate_factor<F_KIP>(G, r, 0);
+            sFac[3 * CH + r] = gate_factor<F_KR>(G, r, 0);
+        }
+    }
+    __syncthreads();
+
+    auto fac = [&](int kind, int r, int d) -> float {
+        if (!KDA) return sFac[kind * CH + r];
+        switch (kind) {
+            case F_KD: return gate_factor<F_KD>(G, r, d);
+            case F_KDP: return gate_factor<F_KDP>(G, r, d);
+            case F_KIP: return gate_factor<F_KIP>(G, r, d);
+            default: return gate_factor<F_KR>(G, r, d);
+        }
+    };
+
+    // warp tilings
+    const int mC = 16 * (warp & 3), nC = 32 * (warp >> 2);       // C x C outputs: 16 x 32 per warp
+    const int mD = 16 * (warp & 3), nD = (D / 2) * (warp >> 2);  // C x D outputs: 16 x D/2 per warp
+
+    // gradients w.r.t. qn, and the two signed halves of the gradient w.r.t. kn
+    float dQn[1][NTD][4], dKp[1][NTD][4], dKm[1][NTD][4];
+    zero_acc(dQn);
+    zero_acc(dKp);
+    zero_acc(dKm);
+
+    // ---- forward recompute ------------------------------------------------
+    // kd' -> X1, ki' -> X2 ; A = strict_lower(beta kd' ki'^T)
+    build_tile<F_KDP, D, KDA, false>(sX1, sK, nullptr, p, ci, h, G, sInvK, nullptr, 1.f);
+    build_tile<F_KIP, D, KDA, false>(sX2, sK, nullptr, p, ci, h, G, sInvK, nullptr, 1.f);
+    __syncthreads();
+    {
+        float acc[1][4][4];
+        zero_acc(acc);
+        warp_mma<1, 4, A_ROW, B_COL>(acc, sX1, sX2, mC, nC, 0, D);
+        frag_foreach(acc, mC, nC, [&](int r, int c, float a0, float a1) {
+            *reinterpret_cast<uint32_t*>(sA.ptr(r, c)) =
+                pack_bf16(c < r ? sBeta[r] * a0 : 0.f, c + 1 < r ? sBeta[r] * a1 : 0.f);
+        });
+    }
+    __syncthreads();
+    // qd' -> X1 ; P = lower(qd' ki'^T)
+    build_tile<F_KDP, D, KDA, true>(sX1, sX1, p.q, p, ci, h, G, sInvQ, nullptr, p.scale);
+    __syncthreads();
+    {
+        float acc[1][4][4];
+        zero_acc(acc);
+        warp_mma<1, 4, A_ROW, B_COL>(acc, sX1, sX2, mC, nC, 0, D);
+        frag_foreach(acc, mC, nC, [&](int r, int c, float a0, float a1) {
+            *reinterpret_cast<uint32_t*>(sP.ptr(r, c)) = pack_bf16(c <= r ? a0 : 0.f, c + 1 <= r ? a1 : 0.f);
+        });
+    }
+    __syncthreads();
+    // kd -> X1 ; X = kd S0 ; V <- beta (V - X) ; dqd = dO S0^T
+    build_tile<F_KD, D, KDA, false>(sX1, sK, nullptr, p, ci, h, G, sInvK, nullptr, 1.f);
+    __syncthreads();
+    {
+        float acc[1][NTD][4];
+        zero_acc(acc);
+        warp_mma<1, NTD, A_ROW, B_ROW>(acc, sX1, sS0, mD, nD, 0, D);
+        frag_foreach(acc, mD, nD, [&](int r, int c, float a0, float a1) {
+            uint32_t* pv = reinterpret_cast<uint32_t*>(sV.ptr(r, c));
+            const float2 v = unpack_bf16(*pv);
+            *pv = pack_bf16(sBeta[r] * (v.x - a0), sBeta[r] * (v.y - a1));
+        });
+        zero_acc(acc);
+        warp_mma<1, NTD, A_ROW, B_COL>(acc, sDO, sS0, mD, nD, 0, D);
+#pragma unroll
+        for (int nt = 0; nt < NTD; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int r = mD + frag_g() + 8 * (e >> 1), c = nD + nt * 8 + 2 * frag_c() + (e & 1);
+                dQn[0][nt][e] += p.scale * acc[0][nt][e] * fac(F_KD, r, c);
+            }
+    }
+    __syncthreads();
+    // u = T (beta E) -> U
+    {
+        float acc[1][NTD][4];
+        zero_acc(acc);
+        warp_mma<1, NTD, A_ROW, B_ROW>(acc, sT, sV, mD, nD, 0, CH);
+        frag_foreach(acc, mD, nD, [&](int r, int c, float a0, float a1) {
+            *reinterpret_cast<uint32_t*>(sU.ptr(r, c)) = pack_bf16(a0, a1);
+        });
+    }
+    // kr -> X1 (X1's last reader was the X product, behind the barrier above)
+    build_tile<F_KR, D, KDA, false>(sX1, sK, nullptr, p, ci, h, G, sInvK, nullptr, 1.f);
+    __syncthreads();
+
+    // ---- reverse pass -----------------------------------------------------
+    // du = P^T dO + kr dS_C -> X2
+    {
+        float acc[1][NTD][4];
+        zero_acc(acc);
+        warp_mma<1, NTD, A_COL, B_ROW>(acc, sP, sDO, mD, nD, 0, CH);
+        warp_mma<1, NTD, A_ROW, B_ROW>(acc, sX1, sDS, mD, nD, 0, D);
+        frag_foreach(acc, mD, nD, [&](int r, int c, float a0, float a1) {
+            *reinterpret_cast<uint32_t*>(sX2.ptr(r, c)) = pack_bf16(a0, a1);
+        });
+    }
+    __syncthreads();
+    // dY = T^T du ; dv = beta dY ; dbeta += <dY, beta E> ; dY -> X2
+    {
+        float acc[1][NTD][4];
+        zero_acc(acc);
+        warp_mma<1, NTD, A_COL, B_ROW>(acc, sT, sX2, mD, nD, 0, CH);
+        float rs[2] = {0.f, 0.f};
+        frag_foreach(acc, mD, nD, [&](int r, int c, float a0, float a1) {
+            const float2 be = unpack_bf16(*reinterpret_cast<const uint32_t*>(sV.ptr(r, c)));
+            rs[(r - mD) >> 3] += a0 * be.x + a1 * be.y;
+            if (r < ci.len)
+                *reinterpret_cast<uint32_t*>(p.dv + ((ci.t0 + r) * p.H + h) * D + c) =
+                    pack_bf16(sBeta[r] * a0, sBeta[r] * a1);
+        });
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            rs[i] += __shfl_xor_sync(0xffffffffu, rs[i], 1);
+            rs[i] += __shfl_xor_sync(0xffffffffu, rs[i], 2);
+        }
+        if (frag_c() == 0) {
+            atomicAdd(&sDbeta[mD + frag_g()], rs[0]);
+            atomicAdd(&sDbeta[mD + frag_g() + 8], rs[1]);
+        }
+        __syncthreads();
+        frag_foreach(acc, mD, nD, [&](int r, int c, float a0, float a1) {
+            *reinterpret_cast<uint32_t*>(sX2.ptr(r, c)) = pack_bf16(a0, a1);
+        });
+    }
+    __syncthreads();
+    // dkd (from E) = -beta (dY S0^T) ; dkr = u dS_C^T
+    {
+        float acc[1][NTD][4];
+        zero_acc(acc);
+        warp_mma<1, NTD, A_ROW, B_COL>(acc, sX2, sS0, mD, nD, 0, D);
+#pragma unroll
+        for (int nt = 0; nt < NTD; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int r = mD + frag_g() + 8 * (e >> 1), c = nD + nt * 8 + 2 * frag_c() + (e & 1);
+                dKp[0][nt][e] -= sBeta[r] * acc[0][nt][e] * fac(F_KD, r, c);
+            }
+        zero_acc(acc);
+        warp_mma<1, NTD, A_ROW, B_COL>(acc, sU, sDS, mD, nD, 0, D);
+        float colsum[NTD][2];
+#pragma unroll
+        for (int nt = 0; nt < NTD; ++nt) colsum[nt][0] = colsum[nt][1] = 0.f;
+#pragma unroll
+        for (int nt = 0; nt < NTD; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int r = mD + frag_g() + 8 * (e >> 1), c = nD + nt * 8 + 2 * frag_c() + (e & 1);
+                const float t = acc[0][nt][e] * fac(F_KR, r, c);  // dkr e^{gT-gc}
+                dKm[0][nt][e] += t;
+                const float kn = bf2f(*reinterpret_cast<const __nv_bfloat16*>(sK.ptr(r, c))) * sInvK[r];
+                colsum[nt][e & 1] += t * kn;
+            }
+#pragma unroll
+        for (int nt = 0; nt < NTD; ++nt)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                float v = colsum[nt][j];
+                v += __shfl_xor_sync(0xffffffffu, v, 4);
+                v += __shfl_xor_sync(0xffffffffu, v, 8);
+                v += __shfl_xor_sync(0xffffffffu, v, 16);
+                if (frag_g() == 0) atomicAdd(&sDgT[nD + nt * 8 + 2 * frag_c() + j], v);
+            }
+    }
+    // dgT += e^{gT} rowsum(dS_C . S0)  (2 threads per state row for D = 128)
+    {
+        constexpr int TPR = 256 / D;  // threads per row
+        const int r = threadIdx.x / TPR, part = threadIdx.x % TPR;
+        float s = 0.f;
+        for (int j = part * (D / 8 / TPR); j < (part + 1) * (D / 8 / TPR); ++j) {
+            uint4 a = *reinterpret_cast<const uint4*>(sS0.chunk(r, j));
+            uint4 b = *reinterpret_cast<const uint4*>(sDS.chunk(r, j));
+            const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                float2 fa = unpack_bf16(wa[e]), fb = unpack_bf16(wb[e]);
+                s += fa.x * fb.x + fa.y * fb.y;
+            }
+        }
+#pragma unroll
+        for (int o = 1; o < TPR; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        if (part == 0) atomicAdd(&sDgT[r], s * __expf(G.gTv(r)));
+    }
+    // dP = lower(dO u^T) -> P
+    {
+        float acc[1][4][4];
+        zero_acc(acc);
+        warp_mma<1, 4, A_ROW, B_COL>(acc, sDO, sU, mC, nC, 0, D);
+        __syncthreads();  // all readers of P (du) are done long ago; readers of S0/dS finish here
+        frag_foreach(acc, mC, nC, [&](int r, int c, float a0, float a1) {
+            *reinterpret_cast<uint32_t*>(sP.ptr(r, c)) = pack_bf16(c <= r ? a0 : 0.f, c + 1 <= r ? a1 : 0.f);
+        });
+    }
+    // dA = -strict_lower(dY u^T) ; dbeta += rowsum(dA . A) ; A <- beta dA
+    {
+        float acc[1][4][4];
+        zero_acc(acc);
+        warp_mma<1, 4, A_ROW, B_COL>(acc, sX2, sU, mC, nC, 0, D);
+        float rs[2] = {0.f, 0.f};
+        frag_foreach(acc, mC, nC, [&](int r, int c, float a0, float a1) {
+            uint32_t* pa = reinterpret_cast<uint32_t*>(sA.ptr(r, c));
+            const float2 av = unpack_bf16(*pa);
+            const float d0 = c < r ? -a0 : 0.f, d1 = c + 1 < r ? -a1 : 0.f;
+            rs[(r - mC) >> 3] += d0 * av.x + d1 * av.y;
+            *pa = pack_bf16(sBeta[r] * d0, sBeta[r] * d1);
+        });
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            rs[i] += __shfl_xor_sync(0xffffffffu, rs[i], 1);
+            rs[i] += __shfl_xor_sync(0xffffffffu, rs[i], 2);
+        }
+        if (frag_c() == 0) {
+            atomicAdd(&sDbeta[mC + frag_g()], rs[0]);
+            atomicAdd(&sDbeta[mC + frag_g() + 8], rs[1]);
+        }
+    }
+    // ki' -> X1
+    build_tile<F_KIP, D, KDA, false>(sX1, sK, nullptr, p, ci, h, G, sInvK, nullptr, 1.f);
+    __syncthreads();
+    // dqd' = dP ki' ; dkd' = (beta dA) ki'
+    {
+        float acc[1][NTD][4];
+        zero_acc(acc);
+        warp_mma<1, NTD, A_ROW, B_ROW>(acc, sP, sX1, mD, nD, 0, CH);
+#pragma unroll
+        for (int nt = 0; nt < NTD; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int r = mD + frag_g() + 8 * (e >> 1), c = nD + nt * 8 + 2 * frag_c() + (e & 1);
+                dQn[0][nt][e] += p.scale * acc[0][nt][e] * fac(F_KDP, r, c);
+            }
+        zero_acc(acc);
+        warp_mma<1, NTD, A_ROW, B_ROW>(acc, sA, sX1, mD, nD, 0, CH);
+#pragma unroll
+        for (int nt = 0; nt < NTD; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int r = mD + frag_g() + 8 * (e >> 1), c = nD + nt * 8 + 2 * frag_c() + (e & 1);
+                dKp[0][nt][e] += acc[0][nt][e] * fac(F_KDP, r, c);
+            }
+    }
+    __syncthreads();
+    // qd' -> X1, kd' -> X2 ; dki' = dP^T qd' + (beta dA)^T kd'
+    build_tile<F_KDP, D, KDA, true>(sX1, sX1, p.q, p, ci, h, G, sInvQ, nullptr, p.scale);
+    build_tile<F_KDP, D, KDA, false>(sX2, sK, nullptr, p, ci, h, G, sInvK, nullptr, 1.f);
+    __syncthreads();
+    {
+        float acc[1][NTD][4];
+        zero_acc(acc);
+        warp_mma<1, NTD, A_COL, B_ROW>(acc, sP, sX1, mD, nD, 0, CH);
+        warp_mma<1, NTD, A_COL, B_ROW>(acc, sA, sX2, mD, nD, 0, CH);
+#pragma unroll
+        for (int nt = 0; nt < NTD; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int r = mD + frag_g() + 8 * (e >> 1), c = nD + nt * 8 + 2 * frag_c() + (e & 1);
+                dKm[0][nt][e] += acc[0][nt][e] * fac(F_KIP, r, c);
+            }
+    }
+
+    // ---- epilogue -----------------------------------------------------------
+    // row dots <dqn, qn>, <dkn, kn>
+    float qn[NTD][4], kn[NTD][4];
+    {
+        float rq[2] = {0.f, 0.f}, rk[2] = {0.f, 0.f};
+#pragma unroll
+        for (int nt = 0; nt < NTD; ++nt)
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const int r = mD + frag_g() + 8 * hf, c = nD + nt * 8 + 2 * frag_c();
+                float2 qv = make_float2(0.f, 0.f);
+                if (r < ci.len)
+                    qv = unpack_bf16(*reinterpret_cast<const uint32_t*>(p.q + ((ci.t0 + r) * p.H + h) * D + c));
+                const float2 kv = unpack_bf16(*reinterpret_cast<const uint32_t*>(sK.ptr(r, c)));
+                qn[nt][2 * hf] = qv.x * sInvQ[r];
+                qn[nt][2 * hf + 1] = qv.y * sInvQ[r];
+                kn[nt][2 * hf] = kv.x * sInvK[r];
+                kn[nt][2 * hf + 1] = kv.y * sInvK[r];
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int e = 2 * hf + j;
+                    rq[hf] += dQn[0][nt][e] * qn[nt][e];
+                    rk[hf] += (dKp[0][nt][e] + dKm[0][nt][e]) * kn[nt][e];
+                }
+            }
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            rq[i] += __shfl_xor_sync(0xffffffffu, rq[i], 1);
+            rq[i] += __shfl_xor_sync(0xffffffffu, rq[i], 2);
+            rk[i] += __shfl_xor_sync(0xffffffffu, rk[i], 1);
+            rk[i] += __shfl_xor_sync(0xffffffffu, rk[i], 2);
+        }
+        if (frag_c() == 0) {
+            const int half = warp >> 2;
+            sRowQ[half * CH + mD + frag_g()] = rq[0];
+            sRowQ[half * CH + mD + frag_g() + 8] = rq[1];
+            sRowK[half * CH + mD + frag_g()] = rk[0];
+            sRowK[half * CH + mD + frag_g() + 8] = rk[1];
+        }
+    }
+    __syncthreads();
+    // dq, dk stores; dgc -> fp32 scratch over the (now free) state tiles
+    float* sDgc = reinterpret_cast<float*>(smem + SM::oS0);  // [C][D]
+#pragma unroll
+    for (int nt = 0; nt < NTD; ++nt)
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+            const int r = mD + frag_g() + 8 * hf, c = nD + nt * 8 + 2 * frag_c();
+            const float tq = sRowQ[r] + sRowQ[CH + r], tk = sRowK[r] + sRowK[CH + r];
+            float oq[2], ok[2], og[2];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int e = 2 * hf + j;
+                const float dk_full = dKp[0][nt][e] + dKm[0][nt][e];
+                oq[j] = (dQn[0][nt][e] - qn[nt][e] * tq) * sInvQ[r];
+                ok[j] = (dk_full - kn[nt][e] * tk) * sInvK[r];
+                og[j] = qn[nt][e] * dQn[0][nt][e] + kn[nt][e] * (dKp[0][nt][e] - dKm[0][nt][e]);
+            }
+            if (r < ci.len) {
+                const size_t o = ((ci.t0 + r) * p.H + h) * D + c;
+                *reinterpret_cast<uint32_t*>(p.dq + o) = pack_bf16(oq[0], oq[1]);
+                *reinterpret_cast<uint32_t*>(p.dk + o) = pack_bf16(ok[0], ok[1]);
+            }
+            *reinterpret_cast<float2*>(sDgc + r * D + c) = make_float2(og[0], og[1]);
+        }
+    // dbeta in logit space
+    for (int r = threadIdx.x; r < ci.len; r += blockDim.x)
+        p.dbeta[(ci.t0 + r) * p.H + h] = __float2bfloat16((1.f - sBeta[r]) * sDbeta[r]);
+    __syncthreads();
+
+    // reverse cumsum of dgc plus the chunk constant dgT, then the gate front end
+    if constexpr (!KDA) {
+        // channel sums first (the scalar gate's gradient is the channel sum)
+        for (int rr = 0; rr < CH / 8; ++rr) {  // warp w sums rows 8w .. 8w+7
+            const int r = warp * (CH / 8) + rr;
+            float s = 0.f;
+            for (int d = lane; d < D; d += 32) s += sDgc[r * D + d];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+            if (lane == 0) sMisc[r] = s;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            float t = 0.f;
+            for (int d = lane; d < D; d += 32) t += sDgT[d];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+            // suffix sums over 64 rows: lane holds rows 2*lane, 2*lane+1
+            const float a = sMisc[2 * lane], b = sMisc[2 * lane + 1];
+            float s = a + b, incl = s;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                float v = __shfl_down_sync(0xffffffffu, incl, o);
+                if (lane + o < 32) incl += v;
+            }
+            // incl = sum of rows >= 2*lane
+            const float suf0 = incl + t, suf1 = incl - a + t;
+            if (2 * lane < ci.len) p.dg[(ci.t0 + 2 * lane) * p.H + h] = suf0;
+            if (2 * lane + 1 < ci.len) p.dg[(ci.t0 + 2 * lane + 1) * p.H + h] = suf1;
+        }
+    } else {
+        const float ea = expf(p.A_log[h]);
+        float dA_acc = 0.f;
+        for (int d = threadIdx.x; d < D; d += blockDim.x) {
+            const float dt = p.dt_bias[h * D + d];
+            float acc = sDgT[d], ddt = 0.f;
+            for (int r = CH - 1; r >= 0; --r) {
+                acc += sDgc[r * D + d];
+                if (r < ci.len) {
+                    const size_t o = ((ci.t0 + r) * p.H + h) * D + d;
+                    const float x = bf2f(p.g_raw[o]) + dt;
+                    const float gl = -ea * softplus_f(x);
+                    const float draw = acc * (-ea * sigmoid_f(x));
+                    p.dg_raw[o] = __float2bfloat16(draw);
+                    ddt += draw;
+                    dA_acc += acc * gl;
+                }
+            }
+            atomicAdd(&p.ddt_bias[h * D + d], ddt);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) dA_acc += __shfl_xor_sync(0xffffffffu, dA_acc, o);
+        if (lane == 0) sMisc[warp] = dA_acc;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float s = 0.f;
+            for (int w = 0; w < 8; ++w) s += sMisc[w];
+            atomicAdd(&p.dA_log[h], s);
+        }
+    }
+}
+
+template <int D, bool KDA>
+static cudaError_t launch_main_t(const Params& p, cudaStream_t s) {
+    const int bytes = MainSmem<D, KDA>::bytes;
+    cudaError_t e = cudaFuncSetAttribute(k_main<D, KDA>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    dim3 grid(p.max_chunks, p.H);
+    k_main<D, KDA><<<grid, 256, bytes, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_main(const Params& p, cudaStream_t s) {
+    if (p.max_chunks == 0) return cudaSuccess;
+    if (p.D == 128) return p.kda ? launch_main_t<128, true>(p, s) : launch_main_t<128, false>(p, s);
+    return p.kda ? launch_main_t<64, true>(p, s) : launch_main_t<64, false>(p, s);
+}
+
+}  // namespace gdr

@@ -1,0 +1,195 @@
+// Chunk-parallel preparation kernel: one CTA per (chunk, head).
+//
+// For each chunk it forms the intra-chunk UT/WY quantities that the two
+// serial state recurrences need (the X/R form of the FlashQLA dh kernel,
+// "FlashQLA ... GDN 反向", §三: X = W, R = Q - Lower(P) X):
+//
+//   A  = strict_lower(diag(beta) kd ki^T)        (fp32, from kd' ki'^T)
+//   T  = (I + A)^-1                               (fp32 blocked inverse)
+//   W  = T diag(beta) kd                          S_C = e^{gT} S0 + kr^T (U - W S0)
+//   U  = T diag(beta) V
+//   P  = lower(qd ki^T)                           (inclusive)
+//   R  = qd - P W                                 dS0 = e^{gT} dS_C + R^T dO - W^T (kr dS_C)
+//   kr = kn e^{gT-gc}
+//
+// Outputs per (chunk, head): W, U, Kr, R as bf16 [C][D], T as bf16 [C][C],
+// gT as fp32 [D].
+#include "gdr_chunk.cuh"
+
+namespace gdr {
+
+template <int D, bool KDA>
+struct PrepSmem {
+    static constexpr int ROWB = 2 * D;
+    static constexpr int TCD = CH * ROWB;   // C x D bf16 tile
+    static constexpr int TCC = CH * 128;    // C x C bf16 tile
+    static constexpr int LDF = 65;
+    static constexpr int oK = 0, oQ = oK + TCD, oV = oQ + TCD, oX1 = oV + TCD, oX2 = oX1 + TCD,
+                         oX3 = oX2 + TCD, oT = oX3 + TCD, oP = oT + TCC, oA = oP + TCC,
+                         oTf = oA + CH * LDF * 4, oTmp = oTf + CH * LDF * 4, oG = oTmp + 768 * 4,
+                         oSmall = oG + Gates<D, KDA>::floats() * 4,
+                         bytes = oSmall + 3 * CH * 4;
+};
+
+template <int D, bool KDA>
+__global__ void __launch_bounds__(256, 1) k_prep(const Params p) {
+    using SM = PrepSmem<D, KDA>;
+    using TileCD = SwzTile<SM::ROWB>;
+    using TileCC = SwzTile<128>;
+    constexpr int NTD = D / 16;  // n-tiles per warp for C x D outputs (a warp covers D/2 columns)
+    extern __shared__ __align__(1024) unsigned char smem[];
+
+    const int chunk = blockIdx.x, h = blockIdx.y;
+    ChunkInfo ci;
+    if (!lookup_chunk(chunk, p.N, p.chunk_off, p.cu_seqlens, p.seq_len, ci)) return;
+
+    TileCD sK{smem + SM::oK}, sQ{smem + SM::oQ}, sV{smem + SM::oV};
+    TileCD sX1{smem + SM::oX1}, sX2{smem + SM::oX2}, sX3{smem + SM::oX3};
+    TileCC sT{smem + SM::oT}, sP{smem + SM::oP};
+    float* sA = reinterpret_cast<float*>(smem + SM::oA);
+    float* sTf = reinterpret_cast<float*>(smem + SM::oTf);
+    float* sTmp = reinterpret_cast<float*>(smem + SM::oTmp);
+    float* gbase = reinterpret_cast<float*>(smem + SM::oG);
+    Gates<D, KDA> G;
+    G.gc = gbase;
+    G.ref = gbase + (KDA ? CH * G.LDG : CH);
+    G.gT = G.ref + (KDA ? D : 1);
+    float* sInvQ = reinterpret_cast<float*>(smem + SM::oSmall);
+    float* sInvK = sInvQ + CH;
+    float* sBeta = sInvK + CH;
+
+    const int warp = threadIdx.x >> 5;
+    const size_t tile_cd = ((size_t)chunk * p.H + h) * CH * D;
+    const size_t tile_cc = ((size_t)chunk * p.H + h) * CH * CH;
+
+    async_load_rows<D>(sQ, p.q, p, ci, h);
+    async_load_rows<D>(sK, p.k, p, ci, h);
+    async_load_rows<D>(sV, p.v, p, ci, h);
+    cp_async_commit();
+    load_gates<D, KDA>(p, ci, h, G, true);
+    load_beta(p, ci, h, sBeta);
+    cp_async_wait<0>();
+    __syncthreads();
+
+    row_inv_norms_smem<D>(sQ, sInvQ);
+    row_inv_norms_smem<D>(sK, sInvK);
+    __syncthreads();
+
+    build_tile<F_KDP, D, KDA, false>(sX1, sK, nullptr, p, ci, h, G, sInvK, nullptr, 1.f);
+    build_tile<F_KIP, D, KDA, false>(sX2, sK, nullptr, p, ci, h, G, sInvK, nullptr, 1.f);
+    build_tile<F_KDP, D, KDA, false>(sX3, sQ, nullptr, p, ci, h, G, sInvQ, nullptr, p.scale);
+    __syncthreads();
+
+    // A = strict_lower(diag(beta) kd' ki'^T) (fp32), P = lower(qd' ki'^T) (bf16)
+    {
+        const int m0 = 16 * (warp & 3), n0 = 32 * (warp >> 2);
+        float acc[1][4][4];
+        zero_acc(acc);
+        warp_mma<1, 4, A_ROW, B_COL>(acc, sX1, sX2, m0, n0, 0, D);
+        frag_foreach(acc, m0, n0, [&](int r, int c, float a0, float a1) {
+            sA[r * SM::LDF + c] = c < r ? sBeta[r] * a0 : 0.f;
+            sA[r * SM::LDF + c + 1] = c + 1 < r ? sBeta[r] * a1 : 0.f;
+        });
+        zero_acc(acc);
+        warp_mma<1, 4, A_ROW, B_COL>(acc, sX3, sX2, m0, n0, 0, D);
+        frag_foreach(acc, m0, n0, [&](int r, int c, float a0, float a1) {
+            *reinterpret_cast<uint32_t*>(sP.ptr(r, c)) = pack_bf16(c <= r ? a0 : 0.f, c + 1 <= r ? a1 : 0.f);
+        });
+    }
+    __syncthreads();
+
+    invert_unit_lower64(sA, sTf, sTmp);  // ends with __syncthreads
+    for (int i = threadIdx.x; i < CH * CH / 2; i += blockDim.x) {
+        const int r = i / (CH / 2), c = 2 * (i % (CH / 2));
+        const uint32_t w = pack_bf16(sTf[r * SM::LDF + c], sTf[r * SM::LDF + c + 1]);
+        *reinterpret_cast<uint32_t*>(sT.ptr(r, c)) = w;
+        *reinterpret_cast<uint32_t*>(p.Tm + tile_cc + r * CH + c) = w;
+    }
+    // beta kd -> X1, beta V -> X2 (kd' and ki' are no longer needed)
+    build_tile<F_KD, D, KDA, false>(sX1, sK, nullptr, p, ci, h, G, sInvK, sBeta, 1.f);
+    {
+        constexpr int CPR = D / 8;
+        for (int i = threadIdx.x; i < CH * CPR; i += blockDim.x) {
+            const int r = i / CPR, j = i % CPR;
+            uint4 v = *reinterpret_cast<const uint4*>(sV.chunk(r, j));
+            uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                float2 f = unpack_bf16(w[e]);
+                w[e] = pack_bf16(f.x * sBeta[r], f.y * sBeta[r]);
+            }
+            *reinterpret_cast<uint4*>(sX2.chunk(r, j)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    }
+    __syncthreads();
+
+    const int m0 = 16 * (warp & 3), n0 = (D / 2) * (warp >> 2);
+    {  // W = T (beta kd): to global and (bf16) to X3 for P W
+        float acc[1][NTD][4];
+        zero_acc(acc);
+        warp_mma<1, NTD, A_ROW, B_ROW>(acc, sT, sX1, m0, n0, 0, CH);
+        frag_foreach(acc, m0, n0, [&](int r, int c, float a0, float a1) {
+            const uint32_t w = pack_bf16(a0, a1);
+            *reinterpret_cast<uint32_t*>(sX3.ptr(r, c)) = w;
+            *reinterpret_cast<uint32_t*>(p.W + tile_cd + r * D + c) = w;
+        });
+    }
+    {  // U = T (beta V)
+        float acc[1][NTD][4];
+        zero_acc(acc);
+        warp_mma<1, NTD, A_ROW, B_ROW>(acc, sT, sX2, m0, n0, 0, CH);
+        frag_foreach(acc, m0, n0, [&](int r, int c, float a0, float a1) {
+            *reinterpret_cast<uint32_t*>(p.U + tile_cd + r * D + c) = pack_bf16(a0, a1);
+        });
+    }
+    __syncthreads();
+    {  // R = qd - P W
+        float acc[1][NTD][4];
+        zero_acc(acc);
+        warp_mma<1, NTD, A_ROW, B_ROW>(acc, sP, sX3, m0, n0, 0, CH);
+        frag_foreach(acc, m0, n0, [&](int r, int c, float a0, float a1) {
+            const float2 q = unpack_bf16(*reinterpret_cast<const uint32_t*>(sQ.ptr(r, c)));
+            const float s = p.scale * sInvQ[r];
+            const float qd0 = q.x * s * gate_factor<F_KD>(G, r, c);
+            const float qd1 = q.y * s * gate_factor<F_KD>(G, r, c + 1);
+            *reinterpret_cast<uint32_t*>(p.R + tile_cd + r * D + c) = pack_bf16(qd0 - a0, qd1 - a1);
+        });
+    }
+    // kr = kn e^{gT - gc}; gT
+    {
+        constexpr int CPR = D / 8;
+        for (int i = threadIdx.x; i < CH * CPR; i += blockDim.x) {
+            const int r = i / CPR, j = i % CPR;
+            uint4 v = *reinterpret_cast<const uint4*>(sK.chunk(r, j));
+            uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                float2 f = unpack_bf16(w[e]);
+                const int d = j * 8 + 2 * e;
+                w[e] = pack_bf16(f.x * sInvK[r] * gate_factor<F_KR>(G, r, d),
+                                 f.y * sInvK[r] * gate_factor<F_KR>(G, r, d + 1));
+            }
+            *reinterpret_cast<uint4*>(p.Kr + tile_cd + r * D + j * 8) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        float* gTo = p.gT + ((size_t)chunk * p.H + h) * D;
+        for (int d = threadIdx.x; d < D; d += blockDim.x) gTo[d] = G.gTv(d);
+    }
+}
+
+template <int D, bool KDA>
+static cudaError_t launch_prep_t(const Params& p, cudaStream_t s) {
+    const int bytes = PrepSmem<D, KDA>::bytes;
+    cudaError_t e = cudaFuncSetAttribute(k_prep<D, KDA>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    dim3 grid(p.max_chunks, p.H);
+    k_prep<D, KDA><<<grid, 256, bytes, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_prep(const Params& p, cudaStream_t s) {
+    if (p.max_chunks == 0) return cudaSuccess;
+    if (p.D == 128) return p.kda ? launch_prep_t<128, true>(p, s) : launch_prep_t<128, false>(p, s);
+    return p.kda ? launch_prep_t<64, true>(p, s) : launch_prep_t<64, false>(p, s);
+}
+
+}  // namespace gdr

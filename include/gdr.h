@@ -1,0 +1,145 @@
+/*
+ * gdr.h -- C ABI of the GB300 (sm_103a) chunked gated delta-rule backward.
+ *
+ * The method: linear attention with the gated delta rule, per (sequence, head)
+ *
+ *     qn = q / sqrt(|q|^2 + 1e-6),   kn = k / sqrt(|k|^2 + 1e-6),   beta = sigmoid(b)
+ *     S_t = (I - beta_t kn_t kn_t^T) diag(exp g_t) S_{t-1} + beta_t kn_t v_t^T
+ *     o_t = scale * S_t^T qn_t
+ *
+ * with a scalar log gate per token and head (GDN) or a per-channel log gate
+ * g = -exp(A_log[h]) * softplus(g_raw + dt_bias[h, :]) (KDA).  The decay is
+ * applied before the delta update; for a scalar gate the two orders agree.
+ * Sources: the FlashQLA GDN backward page ("FlashQLA ... GDN 反向", §一 for the
+ * backward's inputs and outputs: q, k, v, g, beta, h0, dO, optional dht ->
+ * dq, dk, dv (bf16), dg, dbeta, dh0 (fp32)) and "FlashKDA之backward（K1）" (the
+ * KDA gate parameters, the L2 norm with eps 1e-6, beta in logit space, the
+ * atomically reduced dA_log / ddt_bias, varlen through int64 cu_seqlens).
+ * The loss whose gradients are returned is  sum_t <dO_t, o_t> + sum <dht, S_T>.
+ *
+ * Conventions for every entry point
+ * ---------------------------------
+ *  * All tensor pointers are DEVICE pointers, 16-byte aligned, contiguous:
+ *      q, k, v, dO, dq, dk, dv, g_raw, dg_raw : bf16   [T_total, H, D]   (token-major)
+ *      beta_logit, dbeta                      : bf16   [T_total, H]
+ *      g, dg  (GDN natural-log gate)          : float  [T_total, H]
+ *      A_log, dA_log                          : float  [H]
+ *      dt_bias, ddt_bias                      : float  [H, D]
+ *      h0, dht, dh0                           : float  [N, H, D, D]  (row = key channel)
+ *  * cu_seqlens: device int64 [N + 1], 0 = cu[0] <= cu[1] <= ... <= cu[N] = T_total;
+ *    NULL means dense: N sequences of T_total / N tokens each.
+ *  * h0 and dht may be NULL (zero).  All outputs are written in full (rows of
+ *    every sequence); the library never writes outside the given tensors.
+ *  * Ownership: the caller allocates every buffer, including the workspace
+ *    (size from gdr_workspace_bytes) and the states buffer (gdr_states_bytes).
+ *    The library allocates no device memory and keeps no state besides a
+ *    thread-local error string and the optional instrumentation events of
+ *    gdr_profile_begin.
+ *  * Asynchrony: work is enqueued on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream) and the call returns without synchronising.  Argument
+ *    errors are detected on the host before anything is enqueued.  Conditions
+ *    only the device can see (inconsistent cu_seqlens, a gate range the
+ *    kernels cannot represent) set bits in the workspace status word; read
+ *    it with gdr_workspace_status after the work completes.
+ *  * Calls that share a workspace must not run concurrently.
+ */
+#ifndef GDR_H
+#define GDR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GDR_OK = 0,
+    GDR_ERR_INVALID = 1,      /* null / misaligned pointer, bad size or shape */
+    GDR_ERR_UNSUPPORTED = 2,  /* head_dim not in {64, 128} */
+    GDR_ERR_WORKSPACE = 3,    /* workspace or states buffer too small */
+    GDR_ERR_CUDA = 4          /* a CUDA runtime call or kernel launch failed */
+} gdr_status;
+
+/* Device-side status bits (gdr_workspace_status). */
+#define GDR_DEV_BAD_SEQLENS 1 /* cu_seqlens not non-decreasing from 0 to T_total */
+#define GDR_DEV_GATE_RANGE 2  /* a chunk's log-gate span exceeded 160 (or a cumulative gate > 80) */
+
+typedef struct {
+    int32_t num_seqs;          /* N >= 1 */
+    int64_t total_tokens;      /* T_total >= 0 */
+    int32_t num_heads;         /* H >= 1 */
+    int32_t head_dim;          /* D = dk = dv, 64 or 128 */
+    const int64_t* cu_seqlens; /* device int64 [N + 1], or NULL for dense */
+    float scale;               /* output scale, usually 1 / sqrt(D) */
+} gdr_shape;
+
+/* Bytes of the scratch workspace that gdr_fwd_states / gdr_bwd / kda_fwd_states /
+ * kda_bwd need for this shape (returns 0 for an invalid shape). */
+size_t gdr_workspace_bytes(const gdr_shape* shape);
+
+/* Bytes of the per-chunk state buffer written by gdr_fwd_states / kda_fwd_states:
+ * the bf16 chunk-start state of every 64-token chunk and head. */
+size_t gdr_states_bytes(const gdr_shape* shape);
+
+/* Forward chunk states for GDN (the "forward workspace" of the FlashKDA
+ * pipeline, here the chunk-start state S0 of each chunk, saved so the backward
+ * can skip its own recomputation).  Writes `states`. */
+gdr_status gdr_fwd_states(const gdr_shape* shape, const void* q, const void* k, const void* v,
+                          const float* g, const void* beta_logit, const float* h0,
+                          void* states, size_t states_bytes, void* workspace,
+                          size_t workspace_bytes, void* stream);
+
+/* Same for KDA (per-channel gate from g_raw, A_log, dt_bias). */
+gdr_status kda_fwd_states(const gdr_shape* shape, const void* q, const void* k, const void* v,
+                          const void* g_raw, const float* A_log, const float* dt_bias,
+                          const void* beta_logit, const float* h0, void* states,
+                          size_t states_bytes, void* workspace, size_t workspace_bytes,
+                          void* stream);
+
+/* GDN backward ("FlashQLA ... GDN 反向", §一-§二: one call returns dq, dk, dv, dg,
+ * dbeta, dh0).  `states` is the buffer from gdr_fwd_states for the same inputs,
+ * or NULL to recompute the chunk states inside the call.  dg is the gradient
+ * w.r.t. the per-token log gate g (the reverse cumsum is done inside); dbeta is
+ * w.r.t. the beta logit; dh0 is fp32 and always written. */
+gdr_status gdr_bwd(const gdr_shape* shape, const void* q, const void* k, const void* v,
+                   const float* g, const void* beta_logit, const float* h0, const void* dO,
+                   const float* dht, const void* states, void* workspace, size_t workspace_bytes,
+                   void* dq, void* dk, void* dv, float* dg, void* dbeta, float* dh0,
+                   void* stream);
+
+/* KDA backward ("FlashKDA之backward（K1）": gate chain per element, dA_log and
+ * ddt_bias reduced over all tokens).  dg_raw is w.r.t. g_raw (bf16).  dA_log and
+ * ddt_bias are overwritten (zeroed on the stream, then accumulated). */
+gdr_status kda_bwd(const gdr_shape* shape, const void* q, const void* k, const void* v,
+                   const void* g_raw, const float* A_log, const float* dt_bias,
+                   const void* beta_logit, const float* h0, const void* dO, const float* dht,
+                   const void* states, void* workspace, size_t workspace_bytes, void* dq,
+                   void* dk, void* dv, void* dg_raw, void* dbeta, float* dh0, float* dA_log,
+                   float* ddt_bias, void* stream);
+
+/* Waits for `stream`, then returns in *device_status the OR of the GDR_DEV_*
+ * bits raised by the last call that used `workspace` (0 = none). */
+gdr_status gdr_workspace_status(const void* workspace, void* stream, int* device_status);
+
+/* Message of the last error returned on the calling thread ("" if none). */
+const char* gdr_last_error(void);
+
+/* Instrumentation (not part of the method): per-kernel device timing.
+ * gdr_profile_begin(n) makes the next n kernel launches of this library (on
+ * any thread, not thread-safe) record a CUDA event pair on their stream;
+ * gdr_profile_end waits for them and writes, per kernel kind, the summed
+ * milliseconds and the number of launches (arrays of GDR_KERNEL_COUNT). */
+#define GDR_KERNEL_CHUNK_TABLE 0 /* varlen chunk table */
+#define GDR_KERNEL_PREP 1        /* chunk-parallel intra-chunk preparation */
+#define GDR_KERNEL_STATES 2      /* serial state / state-gradient recurrences */
+#define GDR_KERNEL_MAIN 3        /* chunk-parallel main backward */
+#define GDR_KERNEL_COUNT 4
+gdr_status gdr_profile_begin(int max_launches);
+gdr_status gdr_profile_end(double* total_ms, int* launches);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDR_H */

@@ -1,0 +1,89 @@
+"""Shared helpers of the parity tests: run the CUDA path (through the C ABI)
+and the float64 oracle on the same seeded inputs, and compare."""
+import numpy as np
+import torch
+
+# Tolerances (max relative L2 error per tensor): bf16-class gradients vs the
+# float64 oracle, and the fp32 state / parameter gradients.
+TOL_BF16 = 2e-2
+TOL_FP32 = 1e-3
+
+
+def rel_l2(a, b):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    den = np.linalg.norm(b)
+    num = np.linalg.norm(a - b)
+    if den == 0.0:
+        return 0.0 if num == 0.0 else float("inf")
+    return float(num / den)
+
+
+def f64(t):
+    return None if t is None else t.detach().to("cpu", torch.float64).numpy()
+
+
+def to_gpu(x):
+    return {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+
+
+def run_gpu(x, states=None, workspace=None):
+    """x: dict from inputs.make / inputs.custom (CPU tensors).  Returns CPU tensors."""
+    import chunked_gated_delta_bwd_gb300 as gdr
+    d = to_gpu(x)
+    N = d["cu_seqlens"].numel() - 1
+    common = dict(h0=d["h0"], dht=d["dht"], cu_seqlens=d["cu_seqlens"], num_seqs=N,
+                  scale=d["scale"], states=states, workspace=workspace)
+    if x["mode"] == "gdn":
+        out = gdr.gdr_bwd(d["q"], d["k"], d["v"], d["g"], d["beta_logit"], d["dO"], **common)
+    else:
+        out = gdr.kda_bwd(d["q"], d["k"], d["v"], d["g_raw"], d["A_log"], d["dt_bias"],
+                          d["beta_logit"], d["dO"], **common)
+    torch.cuda.synchronize()
+    return {k: v.cpu() for k, v in out.items()}
+
+
+def run_oracle(x, heads=None):
+    """Oracle on the bf16-rounded inputs (upcast to float64), optionally on a subset of heads."""
+    from oracle import oracle
+    sel = (lambda t: t) if heads is None else (lambda t: t[:, heads])
+    selh = (lambda t: t) if heads is None else (lambda t: t[heads])
+    q, k, v, dO = (sel(f64(x[n])) for n in ("q", "k", "v", "dO"))
+    b = sel(f64(x["beta_logit"]))
+    h0 = None if x["h0"] is None else (f64(x["h0"]) if heads is None else f64(x["h0"])[:, heads])
+    dht = None if x["dht"] is None else (f64(x["dht"]) if heads is None else f64(x["dht"])[:, heads])
+    cu = x["cu_seqlens"].numpy()
+    if x["mode"] == "gdn":
+        return oracle.gdn(q, k, v, sel(f64(x["g"])), b, x["scale"], cu, h0=h0, dO=dO, dht=dht)
+    return oracle.kda(q, k, v, sel(f64(x["g_raw"])), selh(f64(x["A_log"])), selh(f64(x["dt_bias"])),
+                      b, x["scale"], cu, h0=h0, dO=dO, dht=dht)
+
+
+def compare(gpu, ref, x, heads=None):
+    """Per-tensor relative L2 errors and their tolerances."""
+    sel = (lambda t: t) if heads is None else (lambda t: t[:, heads])
+    pairs = {"dq": ("dq", TOL_BF16), "dk": ("dk", TOL_BF16), "dv": ("dv", TOL_BF16),
+             "dbeta": ("dbeta", TOL_BF16), "dh0": ("dh0", TOL_FP32)}
+    if x["mode"] == "gdn":
+        pairs["dg"] = ("dg", TOL_BF16)
+    else:
+        pairs.update(dg_raw=("dg_raw", TOL_BF16), dA_log=("dA_log", TOL_FP32),
+                     ddt_bias=("ddt_bias", TOL_FP32))
+    res = {}
+    for name, (rname, tol) in pairs.items():
+        g = f64(gpu[name])
+        if name in ("dA_log", "ddt_bias"):
+            g = g if heads is None else g[heads]
+        elif name == "dh0":
+            g = g if heads is None else g[:, heads]
+        else:
+            g = sel(g)
+        res[name] = (rel_l2(g, ref[rname]), tol)
+    return res
+
+
+def assert_parity(res, label=""):
+    bad = {k: v for k, v in res.items() if not (v[0] <= v[1])}
+    msg = ", ".join("%s=%.2e(tol %.0e)" % (k, v[0], v[1]) for k, v in res.items())
+    assert not bad, "%s parity failed: %s" % (label, msg)
+    return msg

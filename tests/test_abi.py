@@ -1,0 +1,120 @@
+"""C-ABI checks that need no GPU: the library builds and loads, exports every
+function include/gdr.h declares, sizes its buffers, and rejects bad arguments
+on the host before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import chunked_gated_delta_bwd_gb300 as gdr
+from chunked_gated_delta_bwd_gb300 import api, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gdr.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    build.build()
+    return api.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdr_\w+|kda_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("gdr_fwd_states", "kda_fwd_states", "gdr_bwd", "kda_bwd", "gdr_workspace_bytes",
+              "gdr_states_bytes", "gdr_workspace_status", "gdr_last_error"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for n in declared_functions():
+        assert hasattr(L, n), n
+
+
+def test_workspace_sizes(L):
+    sh = gdr.make_shape(1, 32768, 16, 128)
+    chunks = 512
+    assert gdr.states_bytes(sh) == chunks * 16 * 128 * 128 * 2
+    ws = gdr.workspace_bytes(sh)
+    tiles = chunks * 16 * (4 * 64 * 128 * 2 + 64 * 64 * 2 + 128 * 4 + 2 * 128 * 128 * 2)
+    assert tiles <= ws <= tiles + 64 * 256
+    # varlen bound: sum ceil(len/64) <= (T + 63 N) / 64
+    fake_cu = ctypes.c_void_p(256)
+    sh2 = api.GdrShape(3, 130, 2, 64, fake_cu.value, 0.125)
+    assert gdr.states_bytes(sh2) == ((130 + 63 * 3) // 64) * 2 * 64 * 64 * 2
+
+
+@pytest.mark.parametrize("mutate,code", [
+    (dict(head_dim=96), 2),
+    (dict(num_heads=0), 1),
+    (dict(num_seqs=0), 1),
+    (dict(total_tokens=-1), 1),
+    (dict(total_tokens=100, num_seqs=3), 1),  # dense needs T % N == 0
+])
+def test_bad_shapes_rejected(L, mutate, code):
+    sh = gdr.make_shape(2, 128, 2, 64)
+    for k, v in mutate.items():
+        setattr(sh, k, v)
+    assert L.gdr_workspace_bytes(ctypes.byref(sh)) == 0
+    A = ctypes.c_void_p(4096)
+    rc = L.gdr_bwd(ctypes.byref(sh), *([A] * 6), A, None, None, A, 1 << 40, *([A] * 6), None)
+    assert rc == code
+    assert L.gdr_last_error()
+
+
+def _bwd_args(A, ws_bytes):
+    # q k v g beta h0 dO dht states ws ws_bytes dq dk dv dg dbeta dh0 stream
+    return [A, A, A, A, A, None, A, None, None, A, ws_bytes, A, A, A, A, A, A, None]
+
+
+def test_null_and_misaligned_pointers_rejected(L):
+    sh = gdr.make_shape(2, 128, 2, 64)
+    ws = gdr.workspace_bytes(sh)
+    A = ctypes.c_void_p(4096)
+    args = _bwd_args(A, ws)
+    for i in (0, 1, 2, 3, 4, 6, 9, 11, 12, 13, 14, 15, 16):
+        bad = list(args)
+        bad[i] = None
+        assert L.gdr_bwd(ctypes.byref(sh), *bad) == 1, i
+        bad[i] = ctypes.c_void_p(4096 + 8)
+        assert L.gdr_bwd(ctypes.byref(sh), *bad) == 1, i
+        assert b"aligned" in L.gdr_last_error()
+
+
+def test_small_workspace_rejected(L):
+    sh = gdr.make_shape(2, 128, 2, 64)
+    ws = gdr.workspace_bytes(sh)
+    A = ctypes.c_void_p(4096)
+    assert L.gdr_bwd(ctypes.byref(sh), *_bwd_args(A, ws - 1)) == 3
+    # KDA: A_log / dt_bias / dg_raw / dA_log / ddt_bias are required
+    kargs = [A] * 7 + [None, A, None, None, A, ws] + [A] * 8 + [None]
+    for i in (3, 4, 5):
+        bad = list(kargs)
+        bad[i] = None
+        assert L.kda_bwd(ctypes.byref(sh), *bad) == 1
+    bad = list(kargs)
+    bad[12] = ws - 1
+    assert L.kda_bwd(ctypes.byref(sh), *bad) == 3
+
+
+def test_states_buffer_too_small_rejected(L):
+    sh = gdr.make_shape(2, 128, 2, 64)
+    ws = gdr.workspace_bytes(sh)
+    st = gdr.states_bytes(sh)
+    A = ctypes.c_void_p(4096)
+    rc = L.gdr_fwd_states(ctypes.byref(sh), A, A, A, A, A, None, A, st - 1, A, ws, None)
+    assert rc == 3
+
+
+def test_product_path_fails_loudly_without_library(monkeypatch):
+    monkeypatch.setattr(api, "_LIB", None)
+    monkeypatch.setattr(build, "LIB", "/nonexistent/libgdr.so")
+    with pytest.raises(api.GdrError):
+        api.lib()

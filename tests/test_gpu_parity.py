@@ -1,0 +1,132 @@
+"""GPU parity: the CUDA path (through the C ABI) against the float64 oracle on
+the same seeded inputs.  Tolerances: relative L2 <= 2e-2 for each bf16-class
+gradient (dq, dk, dv, dg / dg_raw, dbeta) and <= 1e-3 for dh0, dA_log, ddt_bias.
+
+Small cases run the oracle on every head; the full-size workloads compare a
+sample of heads (the oracle runs per (sequence, head), so a sampled head is
+checked in full, including its dA_log / ddt_bias sums over all tokens)."""
+import pytest
+import torch
+
+from chunked_gated_delta_bwd_gb300 import inputs
+from tests import helpers as H
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from chunked_gated_delta_bwd_gb300 import build
+    build.build()
+
+
+def _check(x, heads=None, label=""):
+    gpu = H.run_gpu(x)
+    ref = H.run_oracle(x, heads)
+    res = H.compare(gpu, ref, x, heads)
+    print(label, H.assert_parity(res, label))
+    return gpu
+
+
+# -- small cases: several chunks, ragged tails, both head dims, both gates ----
+def test_gdn_tiny_config():
+    _check(inputs.make(inputs.CASES["gdn_tiny"]), label="gdn_tiny")
+
+
+@pytest.mark.parametrize("dim", [64, 128])
+def test_gdn_varlen_ragged(dim):
+    x = inputs.custom("gdn", [1, 63, 64, 65, 200, 130], heads=3, dim=dim, seed=101,
+                      with_h0=True, with_dht=True)
+    _check(x, label="gdn_ragged_d%d" % dim)
+
+
+@pytest.mark.parametrize("dim", [64, 128])
+def test_kda_varlen_ragged(dim):
+    x = inputs.custom("kda", [130, 70, 5], heads=2, dim=dim, seed=102, with_h0=True, with_dht=True)
+    _check(x, label="kda_ragged_d%d" % dim)
+
+
+def test_gdn_dense_layout():
+    # equal lengths passed without cu_seqlens (dense B x T)
+    import chunked_gated_delta_bwd_gb300 as gdr
+    x = inputs.custom("gdn", [300, 300], heads=2, dim=128, seed=103, with_h0=True, with_dht=True)
+    d = H.to_gpu(x)
+    B, T = 2, 300
+    rs = lambda t: t.reshape(B, T, *t.shape[1:])
+    out = gdr.gdr_bwd(rs(d["q"]), rs(d["k"]), rs(d["v"]), rs(d["g"]), rs(d["beta_logit"]),
+                      rs(d["dO"]), h0=d["h0"], dht=d["dht"], scale=d["scale"])
+    torch.cuda.synchronize()
+    gpu = {k: (v.reshape(B * T, *v.shape[2:]) if k != "dh0" else v).cpu() for k, v in out.items()}
+    res = H.compare(gpu, H.run_oracle(x), x)
+    print("dense", H.assert_parity(res, "dense"))
+
+
+def test_empty_and_single_token_sequences():
+    x = inputs.custom("gdn", [0, 1, 0, 64, 1], heads=2, dim=64, seed=104, with_h0=True, with_dht=True)
+    gpu = _check(x, label="empty")
+    # empty sequences pass dht straight through to dh0
+    torch.testing.assert_close(gpu["dh0"][0], x["dht"][0], rtol=0, atol=0)
+    torch.testing.assert_close(gpu["dh0"][2], x["dht"][2], rtol=0, atol=0)
+
+
+def test_saved_states_match_recompute():
+    import chunked_gated_delta_bwd_gb300 as gdr
+    for mode in ("gdn", "kda"):
+        x = inputs.custom(mode, [200, 77], heads=2, dim=128, seed=105, with_h0=True, with_dht=True)
+        d = H.to_gpu(x)
+        if mode == "gdn":
+            st = gdr.gdr_fwd_states(d["q"], d["k"], d["v"], d["g"], d["beta_logit"], h0=d["h0"],
+                                    cu_seqlens=d["cu_seqlens"], scale=d["scale"])
+        else:
+            st = gdr.gdr_fwd_states(d["q"], d["k"], d["v"], None, d["beta_logit"], h0=d["h0"],
+                                    cu_seqlens=d["cu_seqlens"], scale=d["scale"], gate="kda",
+                                    g_raw=d["g_raw"], A_log=d["A_log"], dt_bias=d["dt_bias"])
+        a = H.run_gpu(x, states=st)
+        b = H.run_gpu(x)
+        for k in a:
+            if k in ("dA_log", "ddt_bias"):  # atomically reduced: order may differ
+                torch.testing.assert_close(a[k], b[k], rtol=1e-5, atol=1e-6)
+            else:
+                assert torch.equal(a[k], b[k]), k
+
+
+def test_deterministic_outputs():
+    x = inputs.custom("gdn", [500, 3], heads=4, dim=128, seed=106, with_h0=True, with_dht=True)
+    a, b = H.run_gpu(x), H.run_gpu(x)
+    for k in a:
+        assert torch.equal(a[k], b[k]), k
+
+
+def test_gate_range_is_flagged_not_faulted():
+    import chunked_gated_delta_bwd_gb300 as gdr
+    x = inputs.custom("kda", [128], heads=1, dim=64, seed=107)
+    x["A_log"] = torch.full_like(x["A_log"], 4.0)  # ~55 nats of decay per token
+    ws = torch.empty(gdr.workspace_bytes(gdr.make_shape(1, 128, 1, 64, None)) + 4096,
+                     dtype=torch.uint8, device="cuda")
+    H.run_gpu(x, workspace=ws)
+    assert gdr.workspace_status(ws) & gdr.api.GDR_DEV_GATE_RANGE
+
+
+def test_bad_cu_seqlens_are_flagged_not_faulted():
+    import chunked_gated_delta_bwd_gb300 as gdr
+    x = inputs.custom("gdn", [100, 50], heads=1, dim=64, seed=108)
+    x["cu_seqlens"] = torch.tensor([0, 120, 100], dtype=torch.int64)  # not monotone
+    ws = torch.empty(gdr.workspace_bytes(gdr.make_shape(2, 150, 1, 64, x["cu_seqlens"])) + 4096,
+                     dtype=torch.uint8, device="cuda")
+    H.run_gpu(x, workspace=ws)
+    assert gdr.workspace_status(ws) & gdr.api.GDR_DEV_BAD_SEQLENS
+
+
+# -- the task's full-size workloads, sampled heads -------------------------------
+@pytest.mark.parametrize("name,heads", [
+    ("gdn_b2_h16_t4k", [0, 5, 10, 15]),
+    ("kda_b1_h16_t8k", [0, 5, 10, 15]),
+    ("gdn_varlen_h32", [0, 31]),
+    ("gdn_h16_t32k", [3, 12]),
+    ("kda_h16_t32k", [3, 12]),
+])
+def test_full_size_sampled_heads(name, heads):
+    x = inputs.make(inputs.CASES[name])
+    _check(x, heads=heads, label=name)
