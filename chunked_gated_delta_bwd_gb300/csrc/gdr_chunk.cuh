@@ -178,6 +178,14 @@ __device__ __forceinline__ float gate_factor(const Gates<D, KDA>& G, int r, int 
     return __expf(gate_exponent<KIND>(G, r, d));
 }
 
+// Element of a derived tile as the tensor cores see it: bf16(x * m * f) with
+// m = inv * mul * rowmul.  build_tile and the gate-gradient terms of the main
+// kernel both go through these two functions, so they agree bit for bit.
+__device__ __forceinline__ float derived_m(float inv, float mul, float rowmul) { return inv * mul * rowmul; }
+__device__ __forceinline__ float derived_val(float x, float m, float f) {
+    return __bfloat162float(__float2bfloat16_rn(x * m * f));
+}
+
 // dst[r][d] = src[r][d] * inv[r] * rowmul[r] * mul * e^{factor KIND}(r, d)
 // src: swizzled shared tile (SRC_GLOBAL = false) or the chunk rows of a
 // token-major global tensor (SRC_GLOBAL = true).  rowmul may be null.
@@ -198,7 +206,7 @@ __device__ __forceinline__ void build_tile(const Tile& dst, const Tile& src, con
         } else {
             v = *reinterpret_cast<const uint4*>(src.chunk(r, j));
         }
-        float m = inv[r] * mul * (rowmul ? rowmul[r] : 1.f);
+        const float m = derived_m(inv[r], mul, rowmul ? rowmul[r] : 1.f);
         uint32_t w[4] = {v.x, v.y, v.z, v.w};
         float fr = 0.f;
         if (!KDA) fr = gate_factor<KIND>(G, r, 0);
@@ -208,7 +216,7 @@ __device__ __forceinline__ void build_tile(const Tile& dst, const Tile& src, con
             const int d = j * 8 + 2 * e;
             float f0 = KDA ? gate_factor<KIND>(G, r, d) : fr;
             float f1 = KDA ? gate_factor<KIND>(G, r, d + 1) : fr;
-            w[e] = pack_bf16(f.x * m * f0, f.y * m * f1);
+            w[e] = pack_bf16(f.x * m * f0, f.y * m * f1);  // == derived_val(x, m, f) per element
         }
         *reinterpret_cast<uint4*>(dst.chunk(r, j)) = make_uint4(w[0], w[1], w[2], w[3]);
     }

@@ -27,7 +27,7 @@ struct Params {
 
     // workspace
     int* status;
-    __nv_bfloat16 *W, *U, *Kr, *R, *Tm;  // per chunk-head tiles: [C][D] x4, [C][C]
+    __nv_bfloat16 *W, *U, *Kr, *R, *Rlo, *Tm;  // per chunk-head tiles: [C][D] x5, [C][C]
     float* gT;                           // [chunk][H][D]
     __nv_bfloat16 *S0, *dS;              // per chunk-head states [D][D]
 

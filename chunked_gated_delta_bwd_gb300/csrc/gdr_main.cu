@@ -35,8 +35,9 @@ struct MainSmem {
     static constexpr int oK = 0, oV = oK + TCD, oDO = oV + TCD, oS0 = oDO + TCD, oDS = oS0 + TDD,
                          oT = oDS + TDD, oA = oT + TCC, oP = oA + TCC, oU = oP + TCC, oX1 = oU + TCD,
                          oX2 = oX1 + TCD, oG = oX2 + TCD, oSmall = oG + Gates<D, KDA>::floats() * 4;
-    // small arrays (floats): invQ, invK, beta, dbeta, fac[4][C], dgT[D], rowq[2][C], rowk[2][C], misc[64]
-    static constexpr int nSmall = CH * 4 + 4 * CH + D + 4 * CH + 64;
+    // small arrays (floats): invQ, invK, beta [C] each, fac[4][C], dgT partials [4][D] and [D],
+    // dbeta partials [4][C], rowq[2][C], rowk[2][C], misc[64]
+    static constexpr int nSmall = 3 * CH + 4 * CH + 5 * D + 4 * CH + 4 * CH + 64;
     static constexpr int bytes = oSmall + nSmall * 4;
     static_assert(2 * TDD >= CH * D * 4, "dgc scratch must fit in the state tiles");
 };
@@ -65,10 +66,14 @@ __global__ void __launch_bounds__(256, 1) k_main(const Params p) {
     float* sInvQ = reinterpret_cast<float*>(smem + SM::oSmall);
     float* sInvK = sInvQ + CH;
     float* sBeta = sInvK + CH;
-    float* sDbeta = sBeta + CH;
-    float* sFac = sDbeta + CH;      // GDN per-row factors [4][C]
-    float* sDgT = sFac + 4 * CH;    // [D]
-    float* sRowQ = sDgT + D;        // [2][C]
+    float* sFac = sBeta + CH;       // GDN per-row factors [4][C]
+    // Partial sums with one writer per slot, summed in a fixed order (bitwise
+    // reproducible): dgT from the kr product per 16-row band [4][D] and from the
+    // state term [D]; dbeta per column half of the dY and dA products [4][C].
+    float* sDgTp = sFac + 4 * CH;   // [4][D]
+    float* sDgTs = sDgTp + 4 * D;   // [D]
+    float* sDb = sDgTs + D;         // [4][C]
+    float* sRowQ = sDb + 4 * CH;    // [2][C]
     float* sRowK = sRowQ + 2 * CH;  // [2][C]
     float* sMisc = sRowK + 2 * CH;  // [64]
 
@@ -87,8 +92,6 @@ __global__ void __launch_bounds__(256, 1) k_main(const Params p) {
     load_gates<D, KDA>(p, ci, h, G, false);
     load_beta(p, ci, h, sBeta);
     row_inv_norms_global<D>(p.q, p, ci, h, sInvQ);
-    for (int i = threadIdx.x; i < CH; i += blockDim.x) sDbeta[i] = 0.f;
-    for (int i = threadIdx.x; i < D; i += blockDim.x) sDgT[i] = 0.f;
     cp_async_wait<0>();
     __syncthreads();
     row_inv_norms_smem<D>(sK, sInvK);
@@ -116,11 +119,22 @@ __global__ void __launch_bounds__(256, 1) k_main(const Params p) {
     const int mC = 16 * (warp & 3), nC = 32 * (warp >> 2);       // C x C outputs: 16 x 32 per warp
     const int mD = 16 * (warp & 3), nD = (D / 2) * (warp >> 2);  // C x D outputs: 16 x D/2 per warp
 
-    // gradients w.r.t. qn, and the two signed halves of the gradient w.r.t. kn
-    float dQn[1][NTD][4], dKp[1][NTD][4], dKm[1][NTD][4];
+    // Register accumulators over the C x D tile (same warp tiling for every
+    // C x D product): gradients w.r.t. qn and kn, and dgc, the gradient w.r.t.
+    // the cumulative gate.  dgc adds, for every derived tile X = base * e^{+-gc},
+    // +-X * dX with X the exact bf16 value the tensor-core product consumed, so
+    // the paired terms of each in-chunk product (row r, row s) cancel to fp32
+    // rounding in the reverse cumsum instead of to bf16 rounding.
+    float dQn[1][NTD][4], dKn[1][NTD][4], dGc[1][NTD][4];
     zero_acc(dQn);
-    zero_acc(dKp);
-    zero_acc(dKm);
+    zero_acc(dKn);
+    zero_acc(dGc);
+    auto qraw = [&](int r, int c) -> float {
+        return r < ci.len ? bf2f(p.q[((ci.t0 + r) * p.H + h) * D + c]) : 0.f;
+    };
+    auto kraw = [&](int r, int c) -> float {
+        return bf2f(*reinterpret_cast<const __nv_bfloat16*>(sK.ptr(r, c)));
+    };
 
     // ---- forward recompute ------------------------------------------------
     // kd' -> X1, ki' -> X2 ; A = strict_lower(beta kd' ki'^T)
@@ -168,7 +182,9 @@ __global__ void __launch_bounds__(256, 1) k_main(const Params p) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int r = mD + frag_g() + 8 * (e >> 1), c = nD + nt * 8 + 2 * frag_c() + (e & 1);
-                dQn[0][nt][e] += p.scale * acc[0][nt][e] * fac(F_KD, r, c);
+                const float t = p.scale * acc[0][nt][e] * fac(F_KD, r, c);
+                dQn[0][nt][e] += t;
+                dGc[0][nt][e] += qraw(r, c) * sInvQ[r] * t;
             }
     }
     __syncthreads();
@@ -216,8 +232,8 @@ __global__ void __launch_bounds__(256, 1) k_main(const Params p) {
             rs[i] += __shfl_xor_sync(0xffffffffu, rs[i], 2);
         }
         if (frag_c() == 0) {
-            atomicAdd(&sDbeta[mD + frag_g()], rs[0]);
-            atomicAdd(&sDbeta[mD + frag_g() + 8], rs[1]);
+            sDb[(warp >> 2) * CH + mD + frag_g()] = rs[0];
+            sDb[(warp >> 2) * CH + mD + frag_g() + 8] = rs[1];
         }
         __syncthreads();
         frag_foreach(acc, mD, nD, [&](int r, int c, float a0, float a1) {
@@ -235,7 +251,9 @@ __global__ void __launch_bounds__(256, 1) k_main(const Params p) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int r = mD + frag_g() + 8 * (e >> 1), c = nD + nt * 8 + 2 * frag_c() + (e & 1);
-                dKp[0][nt][e] -= sBeta[r] * acc[0][nt][e] * fac(F_KD, r, c);
+                const float t = -sBeta[r] * acc[0][nt][e] * fac(F_KD, r, c);
+                dKn[0][nt][e] += t;
+                dGc[0][nt][e] += kraw(r, c) * sInvK[r] * t;
             }
         zero_acc(acc);
         warp_mma<1, NTD, A_ROW, B_COL>(acc, sU, sDS, mD, nD, 0, D);
@@ -248,9 +266,10 @@ __global__ void __launch_bounds__(256, 1) k_main(const Params p) {
             for (int e = 0; e < 4; ++e) {
                 const int r = mD + frag_g() + 8 * (e >> 1), c = nD + nt * 8 + 2 * frag_c() + (e & 1);
                 const float t = acc[0][nt][e] * fac(F_KR, r, c);  // dkr e^{gT-gc}
-                dKm[0][nt][e] += t;
-                const float kn = bf2f(*reinterpret_cast<const __nv_bfloat16*>(sK.ptr(r, c))) * sInvK[r];
-                colsum[nt][e & 1] += t * kn;
+                dKn[0][nt][e] += t;
+                const float kt = kraw(r, c) * sInvK[r] * t;
+                dGc[0][nt][e] -= kt;
+                colsum[nt][e & 1] += kt;
             }
 #pragma unroll
         for (int nt = 0; nt < NTD; ++nt)
@@ -260,7 +279,7 @@ __global__ void __launch_bounds__(256, 1) k_main(const Params p) {
                 v += __shfl_xor_sync(0xffffffffu, v, 4);
                 v += __shfl_xor_sync(0xffffffffu, v, 8);
                 v += __shfl_xor_sync(0xffffffffu, v, 16);
-                if (frag_g() == 0) atomicAdd(&sDgT[nD + nt * 8 + 2 * frag_c() + j], v);
+                if (frag_g() == 0) sDgTp[(warp & 3) * D + nD + nt * 8 + 2 * frag_c() + j] = v;
             }
     }
     // dgT += e^{gT} rowsum(dS_C . S0)  (2 threads per state row for D = 128)
@@ -280,7 +299,7 @@ __global__ void __launch_bounds__(256, 1) k_main(const Params p) {
         }
 #pragma unroll
         for (int o = 1; o < TPR; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        if (part == 0) atomicAdd(&sDgT[r], s * __expf(G.gTv(r)));
+        if (part == 0) sDgTs[r] = s * __expf(G.gTv(r));
     }
     // dP = lower(dO u^T) -> P
     {
@@ -311,8 +330,8 @@ __global__ void __launch_bounds__(256, 1) k_main(const Params p) {
             rs[i] += __shfl_xor_sync(0xffffffffu, rs[i], 2);
         }
         if (frag_c() == 0) {
-            atomicAdd(&sDbeta[mC + frag_g()], rs[0]);
-            atomicAdd(&sDbeta[mC + frag_g() + 8], rs[1]);
+            sDb[(2 + (warp >> 2)) * CH + mC + frag_g()] = rs[0];
+            sDb[(2 + (warp >> 2)) * CH + mC + frag_g() + 8] = rs[1];
         }
     }
     // ki' -> X1
@@ -328,7 +347,9 @@ __global__ void __launch_bounds__(256, 1) k_main(const Params p) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int r = mD + frag_g() + 8 * (e >> 1), c = nD + nt * 8 + 2 * frag_c() + (e & 1);
-                dQn[0][nt][e] += p.scale * acc[0][nt][e] * fac(F_KDP, r, c);
+                const float f = fac(F_KDP, r, c);
+                dQn[0][nt][e] += p.scale * acc[0][nt][e] * f;
+                dGc[0][nt][e] += derived_val(qraw(r, c), derived_m(sInvQ[r], p.scale, 1.f), f) * acc[0][nt][e];
             }
         zero_acc(acc);
         warp_mma<1, NTD, A_ROW, B_ROW>(acc, sA, sX1, mD, nD, 0, CH);
@@ -337,7 +358,9 @@ __global__ void __launch_bounds__(256, 1) k_main(const Params p) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int r = mD + frag_g() + 8 * (e >> 1), c = nD + nt * 8 + 2 * frag_c() + (e & 1);
-                dKp[0][nt][e] += acc[0][nt][e] * fac(F_KDP, r, c);
+                const float f = fac(F_KDP, r, c);
+                dKn[0][nt][e] += acc[0][nt][e] * f;
+                dGc[0][nt][e] += derived_val(kraw(r, c), derived_m(sInvK[r], 1.f, 1.f), f) * acc[0][nt][e];
             }
     }
     __syncthreads();
@@ -355,7 +378,9 @@ __global__ void __launch_bounds__(256, 1) k_main(const Params p) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int r = mD + frag_g() + 8 * (e >> 1), c = nD + nt * 8 + 2 * frag_c() + (e & 1);
-                dKm[0][nt][e] += acc[0][nt][e] * fac(F_KIP, r, c);
+                const float f = fac(F_KIP, r, c);
+                dKn[0][nt][e] += acc[0][nt][e] * f;
+                dGc[0][nt][e] -= derived_val(kraw(r, c), derived_m(sInvK[r], 1.f, 1.f), f) * acc[0][nt][e];
             }
     }
 
@@ -381,7 +406,7 @@ __global__ void __launch_bounds__(256, 1) k_main(const Params p) {
                 for (int j = 0; j < 2; ++j) {
                     const int e = 2 * hf + j;
                     rq[hf] += dQn[0][nt][e] * qn[nt][e];
-                    rk[hf] += (dKp[0][nt][e] + dKm[0][nt][e]) * kn[nt][e];
+                    rk[hf] += dKn[0][nt][e] * kn[nt][e];
                 }
             }
 #pragma unroll
@@ -412,10 +437,9 @@ __global__ void __launch_bounds__(256, 1) k_main(const Params p) {
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
                 const int e = 2 * hf + j;
-                const float dk_full = dKp[0][nt][e] + dKm[0][nt][e];
                 oq[j] = (dQn[0][nt][e] - qn[nt][e] * tq) * sInvQ[r];
-                ok[j] = (dk_full - kn[nt][e] * tk) * sInvK[r];
-                og[j] = qn[nt][e] * dQn[0][nt][e] + kn[nt][e] * (dKp[0][nt][e] - dKm[0][nt][e]);
+                ok[j] = (dKn[0][nt][e] - kn[nt][e] * tk) * sInvK[r];
+                og[j] = dGc[0][nt][e];
             }
             if (r < ci.len) {
                 const size_t o = ((ci.t0 + r) * p.H + h) * D + c;
@@ -425,8 +449,13 @@ __global__ void __launch_bounds__(256, 1) k_main(const Params p) {
             *reinterpret_cast<float2*>(sDgc + r * D + c) = make_float2(og[0], og[1]);
         }
     // dbeta in logit space
-    for (int r = threadIdx.x; r < ci.len; r += blockDim.x)
-        p.dbeta[(ci.t0 + r) * p.H + h] = __float2bfloat16((1.f - sBeta[r]) * sDbeta[r]);
+    for (int r = threadIdx.x; r < ci.len; r += blockDim.x) {
+        const float db = ((sDb[r] + sDb[CH + r]) + sDb[2 * CH + r]) + sDb[3 * CH + r];
+        p.dbeta[(ci.t0 + r) * p.H + h] = __float2bfloat16((1.f - sBeta[r]) * db);
+    }
+    auto dgT_of = [&](int d) -> float {
+        return (((sDgTs[d] + sDgTp[d]) + sDgTp[D + d]) + sDgTp[2 * D + d]) + sDgTp[3 * D + d];
+    };
     __syncthreads();
 
     // reverse cumsum of dgc plus the chunk constant dgT, then the gate front end
@@ -443,7 +472,7 @@ __global__ void __launch_bounds__(256, 1) k_main(const Params p) {
         __syncthreads();
         if (warp == 0) {
             float t = 0.f;
-            for (int d = lane; d < D; d += 32) t += sDgT[d];
+            for (int d = lane; d < D; d += 32) t += dgT_of(d);
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
             // suffix sums over 64 rows: lane holds rows 2*lane, 2*lane+1
@@ -464,7 +493,7 @@ __global__ void __launch_bounds__(256, 1) k_main(const Params p) {
         float dA_acc = 0.f;
         for (int d = threadIdx.x; d < D; d += blockDim.x) {
             const float dt = p.dt_bias[h * D + d];
-            float acc = sDgT[d], ddt = 0.f;
+            float acc = dgT_of(d), ddt = 0.f;
             for (int r = CH - 1; r >= 0; --r) {
                 acc += sDgc[r * D + d];
                 if (r < ci.len) {

@@ -10,9 +10,11 @@
 //   U  = T diag(beta) V
 //   P  = lower(qd ki^T)                           (inclusive)
 //   R  = qd - P W                                 dS0 = e^{gT} dS_C + R^T dO - W^T (kr dS_C)
+//        (stored as a bf16 pair R = R_hi + R_lo: R^T dO feeds dh0, which is
+//        checked at 1e-3, and a single bf16 rounding of R alone costs ~1e-3)
 //   kr = kn e^{gT-gc}
 //
-// Outputs per (chunk, head): W, U, Kr, R as bf16 [C][D], T as bf16 [C][C],
+// Outputs per (chunk, head): W, U, Kr, R_hi, R_lo as bf16 [C][D], T as bf16 [C][C],
 // gT as fp32 [D].
 #include "gdr_chunk.cuh"
 
@@ -152,7 +154,11 @@ __global__ void __launch_bounds__(256, 1) k_prep(const Params p) {
             const float s = p.scale * sInvQ[r];
             const float qd0 = q.x * s * gate_factor<F_KD>(G, r, c);
             const float qd1 = q.y * s * gate_factor<F_KD>(G, r, c + 1);
-            *reinterpret_cast<uint32_t*>(p.R + tile_cd + r * D + c) = pack_bf16(qd0 - a0, qd1 - a1);
+            const float r0 = qd0 - a0, r1 = qd1 - a1;
+            const uint32_t hi = pack_bf16(r0, r1);
+            const float2 hf = unpack_bf16(hi);
+            *reinterpret_cast<uint32_t*>(p.R + tile_cd + r * D + c) = hi;
+            *reinterpret_cast<uint32_t*>(p.Rlo + tile_cd + r * D + c) = pack_bf16(r0 - hf.x, r1 - hf.y);
         });
     }
     // kr = kn e^{gT - gc}; gT

@@ -10,7 +10,7 @@
 //       X = W S0 ;  S_C = diag(e^{gT}) S0 + kr^T (U - X)
 //   role 1, backward (state gradient at each chunk end, saved bf16 per chunk;
 //       the FlashQLA dh recurrence, "FlashQLA ... GDN 反向", §三):
-//       Y = kr dS_C ;  dS0 = diag(e^{gT}) dS_C + R^T dO - W^T Y
+//       Y = kr dS_C ;  dS0 = diag(e^{gT}) dS_C + (R_hi + R_lo)^T dO - W^T Y
 //       and dh0 = dS0 of each sequence's first chunk (fp32).
 #include "gdr_chunk.cuh"
 
@@ -24,8 +24,8 @@ struct StateSmem {
     static constexpr int ROWB = 2 * D;
     static constexpr int TCD = CH * ROWB;
     static constexpr int TNV = CH * LDV * 2;  // C x BV narrow tile
-    // one stage: three C x D tiles, one narrow tile, gT
-    static constexpr int oT0 = 0, oT1 = TCD, oT2 = 2 * TCD, oN = 3 * TCD, oG = oN + TNV,
+    // one stage: four C x D tiles, one narrow tile, gT
+    static constexpr int oT0 = 0, oT1 = TCD, oT2 = 2 * TCD, oT3 = 3 * TCD, oN = 4 * TCD, oG = oN + TNV,
                          stage = oG + D * 4;
     static constexpr int oStage0 = 0, oStage1 = stage, oS = 2 * stage, oY = oS + D * LDV * 2,
                          bytes = oY + TNV;
@@ -75,7 +75,7 @@ __global__ void __launch_bounds__(128) k_states(const Params p, int role0) {
     auto issue = [&](int c, int b) {
         unsigned char* s = stage(b);
         const size_t tcd = ((size_t)c * p.H + h) * CH * D;
-        TileCD t0{s + SM::oT0}, t1{s + SM::oT1}, t2{s + SM::oT2};
+        TileCD t0{s + SM::oT0}, t1{s + SM::oT1}, t2{s + SM::oT2}, t3{s + SM::oT3};
         TileN tn{s + SM::oN};
         if (role == 0) {
             async_load_tile<CH, D>(t0, p.W + tcd);
@@ -88,6 +88,7 @@ __global__ void __launch_bounds__(128) k_states(const Params p, int role0) {
             async_load_tile<CH, D>(t0, p.Kr + tcd);
             async_load_tile<CH, D>(t1, p.R + tcd);
             async_load_tile<CH, D>(t2, p.W + tcd);
+            async_load_tile<CH, D>(t3, p.Rlo + tcd);
             const int local = c - cb;
             const int64_t t0r = bos + (int64_t)local * CH;
             const int64_t rem = eos - t0r;
@@ -110,7 +111,7 @@ __global__ void __launch_bounds__(128) k_states(const Params p, int role0) {
         const int c = role == 0 ? cb + it : ce - 1 - it;
         const int b = it & 1;
         unsigned char* s = stage(b);
-        TileCD t0{s + SM::oT0}, t1{s + SM::oT1}, t2{s + SM::oT2};
+        TileCD t0{s + SM::oT0}, t1{s + SM::oT1}, t2{s + SM::oT2}, t3{s + SM::oT3};
         TileN tn{s + SM::oN};
         const float* gs = reinterpret_cast<const float*>(s + SM::oG);
 
@@ -156,7 +157,8 @@ __global__ void __launch_bounds__(128) k_states(const Params p, int role0) {
         if (role == 0) {
             warp_mma<MT, 2, A_COL, B_ROW>(st, t1, sY, m0, 0, 0, CH);  // + kr^T Vn
         } else {
-            warp_mma<MT, 2, A_COL, B_ROW>(st, t1, tn, m0, 0, 0, CH);  // + R^T dO
+            warp_mma<MT, 2, A_COL, B_ROW>(st, t1, tn, m0, 0, 0, CH);  // + R_hi^T dO
+            warp_mma<MT, 2, A_COL, B_ROW>(st, t3, tn, m0, 0, 0, CH);  // + R_lo^T dO
             warp_mma<MT, 2, A_COL, B_ROW>(st, t2, sY, m0, 0, 0, CH);  // - W^T Y
         }
     }
