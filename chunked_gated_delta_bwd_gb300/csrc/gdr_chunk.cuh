@@ -193,7 +193,8 @@ template <int KIND, int D, bool KDA, bool SRC_GLOBAL, class Tile>
 __device__ __forceinline__ void build_tile(const Tile& dst, const Tile& src, const __nv_bfloat16* gsrc,
                                            const Params& p, const ChunkInfo& ci, int h,
                                            const Gates<D, KDA>& G, const float* inv,
-                                           const float* rowmul, float mul) {
+                                           const float* rowmul, float mul, const Tile* lo = nullptr) {
+    // With `lo`, the tile is stored as a bf16 pair: dst = bf16(v), lo = bf16(v - dst).
     constexpr int CPR = D / 8;
     for (int i = threadIdx.x; i < CH * CPR; i += blockDim.x) {
         const int r = i / CPR, j = i % CPR;
@@ -207,18 +208,36 @@ __device__ __forceinline__ void build_tile(const Tile& dst, const Tile& src, con
             v = *reinterpret_cast<const uint4*>(src.chunk(r, j));
         }
         const float m = derived_m(inv[r], mul, rowmul ? rowmul[r] : 1.f);
-        uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t w[4] = {v.x, v.y, v.z, v.w}, wl[4];
         float fr = 0.f;
         if (!KDA) fr = gate_factor<KIND>(G, r, 0);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             float2 f = unpack_bf16(w[e]);
             const int d = j * 8 + 2 * e;
-            float f0 = KDA ? gate_factor<KIND>(G, r, d) : fr;
-            float f1 = KDA ? gate_factor<KIND>(G, r, d + 1) : fr;
-            w[e] = pack_bf16(f.x * m * f0, f.y * m * f1);  // == derived_val(x, m, f) per element
+            const float f0 = KDA ? gate_factor<KIND>(G, r, d) : fr;
+            const float f1 = KDA ? gate_factor<KIND>(G, r, d + 1) : fr;
+            const float v0 = f.x * m * f0, v1 = f.y * m * f1;  // == derived_val(x, m, f) once rounded
+            w[e] = pack_bf16(v0, v1);
+            if (lo) {
+                const float2 hv = unpack_bf16(w[e]);
+                wl[e] = pack_bf16(v0 - hv.x, v1 - hv.y);
+            }
         }
         *reinterpret_cast<uint4*>(dst.chunk(r, j)) = make_uint4(w[0], w[1], w[2], w[3]);
+        if (lo) *reinterpret_cast<uint4*>(lo->chunk(r, j)) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+    }
+}
+
+// Stores two fp32 values at (r, c), (r, c+1) of a bf16 tile, and, with `lo`,
+// their bf16 residuals into a second tile.
+template <class Tile>
+__device__ __forceinline__ void store_pair(const Tile& hi, const Tile* lo, int r, int c, float v0, float v1) {
+    const uint32_t w = pack_bf16(v0, v1);
+    *reinterpret_cast<uint32_t*>(hi.ptr(r, c)) = w;
+    if (lo) {
+        const float2 hv = unpack_bf16(w);
+        *reinterpret_cast<uint32_t*>(lo->ptr(r, c)) = pack_bf16(v0 - hv.x, v1 - hv.y);
     }
 }
 

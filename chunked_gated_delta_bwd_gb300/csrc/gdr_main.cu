@@ -38,7 +38,14 @@ struct MainSmem {
     // small arrays (floats): invQ, invK, beta [C] each, fac[4][C], dgT partials [4][D] and [D],
     // dbeta partials [4][C], rowq[2][C], rowk[2][C], misc[64]
     static constexpr int nSmall = 3 * CH + 4 * CH + 5 * D + 4 * CH + 4 * CH + 64;
-    static constexpr int bytes = oSmall + nSmall * 4;
+    static constexpr int oEnd = (oSmall + nSmall * 4 + 127) / 128 * 128;
+    // Residual (lo) tiles of the precise mode.  They live on the state tiles once
+    // those are dead (D = 128: S0 holds dP_lo, (beta dA)_lo, ki'_lo; dS holds
+    // qd'_lo, kd'_lo); for D = 64 the last three get their own space.
+    static constexpr bool BIG = (D == 128);
+    static constexpr int oDPlo = oS0, oBDAlo = BIG ? oS0 + TCC : oDS, oKIlo = BIG ? oS0 + 2 * TCC : oEnd,
+                         oQDlo = BIG ? oDS : oEnd + TCD, oKDlo = BIG ? oDS + TCD : oEnd + 2 * TCD;
+    static constexpr int bytes = (BIG || !KDA) ? oEnd : oEnd + 3 * TCD;
     static_assert(2 * TDD >= CH * D * 4, "dgc scratch must fit in the state tiles");
 };
 
@@ -48,6 +55,11 @@ __global__ void __launch_bounds__(256, 1) k_main(const Params p) {
     using TileCD = SwzTile<SM::ROWB>;
     using TileCC = SwzTile<128>;
     constexpr int NTD = D / 16;
+    // KDA runs the precise mode: the operands that carry the per-channel gate
+    // gradient (u and beta E, dP and beta dA, and the in-chunk tiles qd', kd',
+    // ki' of the gradient products) are bf16 pairs hi + lo, each product
+    // hi*hi + lo*hi + hi*lo, because dA_log and ddt_bias sum dg over every token.
+    constexpr bool PREC = KDA;
     extern __shared__ __align__(1024) unsigned char smem[];
 
     const int chunk = blockIdx.x, h = blockIdx.y;
@@ -58,6 +70,8 @@ __global__ void __launch_bounds__(256, 1) k_main(const Params p) {
         sX1{smem + SM::oX1}, sX2{smem + SM::oX2};
     TileCD sS0{smem + SM::oS0}, sDS{smem + SM::oDS};  // D x D tiles, same row size
     TileCC sT{smem + SM::oT}, sA{smem + SM::oA}, sP{smem + SM::oP};
+    TileCC sDPlo{smem + SM::oDPlo}, sBDAlo{smem + SM::oBDAlo};
+    TileCD sKIlo{smem + SM::oKIlo}, sQDlo{smem + SM::oQDlo}, sKDlo{smem + SM::oKDlo};
     float* gbase = reinterpret_cast<float*>(smem + SM::oG);
     Gates<D, KDA> G;
     G.gc = gbase;
@@ -103,6 +117,25 @@ __global__ void __launch_bounds__(256, 1) k_main(const Params p) {
             sFac[3 * CH + r] = gate_factor<F_KR>(G, r, 0);
         }
     }
+    // dgT (state part) = e^{gT} rowsum(dS_C . S0)
+    {
+        constexpr int TPR = 256 / D;  // threads per state row
+        const int r = threadIdx.x / TPR, part = threadIdx.x % TPR;
+        float s = 0.f;
+        for (int j = part * (D / 8 / TPR); j < (part + 1) * (D / 8 / TPR); ++j) {
+            uint4 a = *reinterpret_cast<const uint4*>(sS0.chunk(r, j));
+            uint4 b = *reinterpret_cast<const uint4*>(sDS.chunk(r, j));
+            const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                float2 fa = unpack_bf16(wa[e]), fb = unpack_bf16(wb[e]);
+                s += fa.x * fb.x + fa.y * fb.y;
+            }
+        }
+#pragma unroll
+        for (int o = 1; o < TPR; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        if (part == 0) sDgTs[r] = s * __expf(G.gTv(r));
+    }
     __syncthreads();
 
     auto fac = [&](int kind, int r, int d) -> float {
@@ -114,6 +147,11 @@ __global__ void __launch_bounds__(256, 1) k_main(const Params p) {
             default: return gate_factor<F_KR>(G, r, d);
         }
     };
+    // value of a derived in-chunk tile element as the gradient products see it
+    // (exact bf16 operand, or the fp32 value the hi + lo pair represents)
+    auto tile_val = [&](float x, float m, float f) -> float {
+        return PREC ? x * m * f : derived_val(x, m, f);
+    };
 
     // warp tilings
     const int mC = 16 * (warp & 3), nC = 32 * (warp >> 2);       // C x C outputs: 16 x 32 per warp
@@ -122,9 +160,9 @@ __global__ void __launch_bounds__(256, 1) k_main(const Params p) {
     // Register accumulators over the C x D tile (same warp tiling for every
     // C x D product): gradients w.r.t. qn and kn, and dgc, the gradient w.r.t.
     // the cumulative gate.  dgc adds, for every derived tile X = base * e^{+-gc},
-    // +-X * dX with X the exact bf16 value the tensor-core product consumed, so
-    // the paired terms of each in-chunk product (row r, row s) cancel to fp32
-    // rounding in the reverse cumsum instead of to bf16 rounding.
+    // +-X * dX with X the value the tensor-core product consumed, so the paired
+    // terms of each in-chunk product (row r, row s) cancel to fp32 rounding in the
+    // reverse cumsum instead of to bf16 rounding.
     float dQn[1][NTD][4], dKn[1][NTD][4], dGc[1][NTD][4];
     zero_acc(dQn);
     zero_acc(dKn);
@@ -135,6 +173,11 @@ __global__ void __launch_bounds__(256, 1) k_main(const Params p) {
     auto kraw = [&](int r, int c) -> float {
         return bf2f(*reinterpret_cast<const __nv_bfloat16*>(sK.ptr(r, c)));
     };
+#define FRAG_LOOP(NT_)                                                                          \
+    _Pragma("unroll") for (int nt = 0; nt < NT_; ++nt) _Pragma("unroll") for (int e = 0; e < 4; ++e)
+#define FRAG_RC(M0_, N0_)                                                                       \
+    const int r = (M0_) + frag_g() + 8 * (e >> 1);                                              \
+    const int c = (N0_) + nt * 8 + 2 * frag_c() + (e & 1)
 
     // ---- forward recompute ------------------------------------------------
     // kd' -> X1, ki' -> X2 ; A = strict_lower(beta kd' ki'^T)
@@ -163,7 +206,7 @@ __global__ void __launch_bounds__(256, 1) k_main(const Params p) {
         });
     }
     __syncthreads();
-    // kd -> X1 ; X = kd S0 ; V <- beta (V - X) ; dqd = dO S0^T
+    // kd -> X1 ; X = kd S0 ; beta (V - X) -> V (hi) and U (lo) ; dqd = dO S0^T
     build_tile<F_KD, D, KDA, false>(sX1, sK, nullptr, p, ci, h, G, sInvK, nullptr, 1.f);
     __syncthreads();
     {
@@ -171,38 +214,22 @@ __global__ void __launch_bounds__(256, 1) k_main(const Params p) {
         zero_acc(acc);
         warp_mma<1, NTD, A_ROW, B_ROW>(acc, sX1, sS0, mD, nD, 0, D);
         frag_foreach(acc, mD, nD, [&](int r, int c, float a0, float a1) {
-            uint32_t* pv = reinterpret_cast<uint32_t*>(sV.ptr(r, c));
-            const float2 v = unpack_bf16(*pv);
-            *pv = pack_bf16(sBeta[r] * (v.x - a0), sBeta[r] * (v.y - a1));
+            const float2 v = unpack_bf16(*reinterpret_cast<const uint32_t*>(sV.ptr(r, c)));
+            store_pair(sV, PREC ? &sU : nullptr, r, c, sBeta[r] * (v.x - a0), sBeta[r] * (v.y - a1));
         });
         zero_acc(acc);
         warp_mma<1, NTD, A_ROW, B_COL>(acc, sDO, sS0, mD, nD, 0, D);
-#pragma unroll
-        for (int nt = 0; nt < NTD; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int r = mD + frag_g() + 8 * (e >> 1), c = nD + nt * 8 + 2 * frag_c() + (e & 1);
-                const float t = p.scale * acc[0][nt][e] * fac(F_KD, r, c);
-                dQn[0][nt][e] += t;
-                dGc[0][nt][e] += qraw(r, c) * sInvQ[r] * t;
-            }
+        FRAG_LOOP(NTD) {
+            FRAG_RC(mD, nD);
+            const float t = p.scale * acc[0][nt][e] * fac(F_KD, r, c);
+            dQn[0][nt][e] += t;
+            dGc[0][nt][e] += qraw(r, c) * sInvQ[r] * t;
+        }
     }
     __syncthreads();
-    // u = T (beta E) -> U
-    {
-        float acc[1][NTD][4];
-        zero_acc(acc);
-        warp_mma<1, NTD, A_ROW, B_ROW>(acc, sT, sV, mD, nD, 0, CH);
-        frag_foreach(acc, mD, nD, [&](int r, int c, float a0, float a1) {
-            *reinterpret_cast<uint32_t*>(sU.ptr(r, c)) = pack_bf16(a0, a1);
-        });
-    }
-    // kr -> X1 (X1's last reader was the X product, behind the barrier above)
+    // kr -> X1 ; du = P^T dO + kr dS_C -> X2
     build_tile<F_KR, D, KDA, false>(sX1, sK, nullptr, p, ci, h, G, sInvK, nullptr, 1.f);
     __syncthreads();
-
-    // ---- reverse pass -----------------------------------------------------
-    // du = P^T dO + kr dS_C -> X2
     {
         float acc[1][NTD][4];
         zero_acc(acc);
@@ -220,7 +247,12 @@ __global__ void __launch_bounds__(256, 1) k_main(const Params p) {
         warp_mma<1, NTD, A_COL, B_ROW>(acc, sT, sX2, mD, nD, 0, CH);
         float rs[2] = {0.f, 0.f};
         frag_foreach(acc, mD, nD, [&](int r, int c, float a0, float a1) {
-            const float2 be = unpack_bf16(*reinterpret_cast<const uint32_t*>(sV.ptr(r, c)));
+            float2 be = unpack_bf16(*reinterpret_cast<const uint32_t*>(sV.ptr(r, c)));
+            if (PREC) {
+                const float2 bl = unpack_bf16(*reinterpret_cast<const uint32_t*>(sU.ptr(r, c)));
+                be.x += bl.x;
+                be.y += bl.y;
+            }
             rs[(r - mD) >> 3] += a0 * be.x + a1 * be.y;
             if (r < ci.len)
                 *reinterpret_cast<uint32_t*>(p.dv + ((ci.t0 + r) * p.H + h) * D + c) =
@@ -241,36 +273,45 @@ __global__ void __launch_bounds__(256, 1) k_main(const Params p) {
         });
     }
     __syncthreads();
-    // dkd (from E) = -beta (dY S0^T) ; dkr = u dS_C^T
+    // dkd (from E) = -beta (dY S0^T) ; u = T (beta E) -> U (hi) and V (lo)
     {
         float acc[1][NTD][4];
         zero_acc(acc);
         warp_mma<1, NTD, A_ROW, B_COL>(acc, sX2, sS0, mD, nD, 0, D);
-#pragma unroll
-        for (int nt = 0; nt < NTD; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int r = mD + frag_g() + 8 * (e >> 1), c = nD + nt * 8 + 2 * frag_c() + (e & 1);
-                const float t = -sBeta[r] * acc[0][nt][e] * fac(F_KD, r, c);
-                dKn[0][nt][e] += t;
-                dGc[0][nt][e] += kraw(r, c) * sInvK[r] * t;
-            }
+        FRAG_LOOP(NTD) {
+            FRAG_RC(mD, nD);
+            const float t = -sBeta[r] * acc[0][nt][e] * fac(F_KD, r, c);
+            dKn[0][nt][e] += t;
+            dGc[0][nt][e] += kraw(r, c) * sInvK[r] * t;
+        }
+        zero_acc(acc);
+        warp_mma<1, NTD, A_ROW, B_ROW>(acc, sT, sV, mD, nD, 0, CH);
+        if (PREC) warp_mma<1, NTD, A_ROW, B_ROW>(acc, sT, sU, mD, nD, 0, CH);
+        __syncthreads();
+        frag_foreach(acc, mD, nD, [&](int r, int c, float a0, float a1) {
+            store_pair(sU, PREC ? &sV : nullptr, r, c, a0, a1);
+        });
+    }
+    __syncthreads();
+
+    // ---- reverse pass, state-free part -----------------------------------
+    // dkr = u dS_C^T ; dgT (kr part) = colsum(dkr . kr)
+    {
+        float acc[1][NTD][4];
         zero_acc(acc);
         warp_mma<1, NTD, A_ROW, B_COL>(acc, sU, sDS, mD, nD, 0, D);
+        if (PREC) warp_mma<1, NTD, A_ROW, B_COL>(acc, sV, sDS, mD, nD, 0, D);
         float colsum[NTD][2];
 #pragma unroll
         for (int nt = 0; nt < NTD; ++nt) colsum[nt][0] = colsum[nt][1] = 0.f;
-#pragma unroll
-        for (int nt = 0; nt < NTD; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int r = mD + frag_g() + 8 * (e >> 1), c = nD + nt * 8 + 2 * frag_c() + (e & 1);
-                const float t = acc[0][nt][e] * fac(F_KR, r, c);  // dkr e^{gT-gc}
-                dKn[0][nt][e] += t;
-                const float kt = kraw(r, c) * sInvK[r] * t;
-                dGc[0][nt][e] -= kt;
-                colsum[nt][e & 1] += kt;
-            }
+        FRAG_LOOP(NTD) {
+            FRAG_RC(mD, nD);
+            const float t = acc[0][nt][e] * fac(F_KR, r, c);  // dkr e^{gT-gc}
+            dKn[0][nt][e] += t;
+            const float kt = kraw(r, c) * sInvK[r] * t;
+            dGc[0][nt][e] -= kt;
+            colsum[nt][e & 1] += kt;
+        }
 #pragma unroll
         for (int nt = 0; nt < NTD; ++nt)
 #pragma unroll
@@ -282,47 +323,29 @@ __global__ void __launch_bounds__(256, 1) k_main(const Params p) {
                 if (frag_g() == 0) sDgTp[(warp & 3) * D + nD + nt * 8 + 2 * frag_c() + j] = v;
             }
     }
-    // dgT += e^{gT} rowsum(dS_C . S0)  (2 threads per state row for D = 128)
-    {
-        constexpr int TPR = 256 / D;  // threads per row
-        const int r = threadIdx.x / TPR, part = threadIdx.x % TPR;
-        float s = 0.f;
-        for (int j = part * (D / 8 / TPR); j < (part + 1) * (D / 8 / TPR); ++j) {
-            uint4 a = *reinterpret_cast<const uint4*>(sS0.chunk(r, j));
-            uint4 b = *reinterpret_cast<const uint4*>(sDS.chunk(r, j));
-            const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                float2 fa = unpack_bf16(wa[e]), fb = unpack_bf16(wb[e]);
-                s += fa.x * fb.x + fa.y * fb.y;
-            }
-        }
-#pragma unroll
-        for (int o = 1; o < TPR; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        if (part == 0) sDgTs[r] = s * __expf(G.gTv(r));
-    }
-    // dP = lower(dO u^T) -> P
+    // dP = lower(dO u^T) -> P (hi) and the S0 space (lo)
     {
         float acc[1][4][4];
         zero_acc(acc);
         warp_mma<1, 4, A_ROW, B_COL>(acc, sDO, sU, mC, nC, 0, D);
-        __syncthreads();  // all readers of P (du) are done long ago; readers of S0/dS finish here
+        if (PREC) warp_mma<1, 4, A_ROW, B_COL>(acc, sDO, sV, mC, nC, 0, D);
+        __syncthreads();  // every reader of P (du), S0 (Z) and dS_C (dkr) is done
         frag_foreach(acc, mC, nC, [&](int r, int c, float a0, float a1) {
-            *reinterpret_cast<uint32_t*>(sP.ptr(r, c)) = pack_bf16(c <= r ? a0 : 0.f, c + 1 <= r ? a1 : 0.f);
+            store_pair(sP, PREC ? &sDPlo : nullptr, r, c, c <= r ? a0 : 0.f, c + 1 <= r ? a1 : 0.f);
         });
     }
-    // dA = -strict_lower(dY u^T) ; dbeta += rowsum(dA . A) ; A <- beta dA
+    // dA = -strict_lower(dY u^T) ; dbeta += rowsum(dA . A) ; A <- beta dA (hi, lo)
     {
         float acc[1][4][4];
         zero_acc(acc);
         warp_mma<1, 4, A_ROW, B_COL>(acc, sX2, sU, mC, nC, 0, D);
+        if (PREC) warp_mma<1, 4, A_ROW, B_COL>(acc, sX2, sV, mC, nC, 0, D);
         float rs[2] = {0.f, 0.f};
         frag_foreach(acc, mC, nC, [&](int r, int c, float a0, float a1) {
-            uint32_t* pa = reinterpret_cast<uint32_t*>(sA.ptr(r, c));
-            const float2 av = unpack_bf16(*pa);
+            const float2 av = unpack_bf16(*reinterpret_cast<const uint32_t*>(sA.ptr(r, c)));
             const float d0 = c < r ? -a0 : 0.f, d1 = c + 1 < r ? -a1 : 0.f;
             rs[(r - mC) >> 3] += d0 * av.x + d1 * av.y;
-            *pa = pack_bf16(sBeta[r] * d0, sBeta[r] * d1);
+            store_pair(sA, PREC ? &sBDAlo : nullptr, r, c, sBeta[r] * d0, sBeta[r] * d1);
         });
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
@@ -334,55 +357,62 @@ __global__ void __launch_bounds__(256, 1) k_main(const Params p) {
             sDb[(2 + (warp >> 2)) * CH + mC + frag_g() + 8] = rs[1];
         }
     }
-    // ki' -> X1
-    build_tile<F_KIP, D, KDA, false>(sX1, sK, nullptr, p, ci, h, G, sInvK, nullptr, 1.f);
+    // ki' -> X1 (+ lo)
+    build_tile<F_KIP, D, KDA, false>(sX1, sK, nullptr, p, ci, h, G, sInvK, nullptr, 1.f, PREC ? &sKIlo : nullptr);
     __syncthreads();
     // dqd' = dP ki' ; dkd' = (beta dA) ki'
     {
         float acc[1][NTD][4];
         zero_acc(acc);
         warp_mma<1, NTD, A_ROW, B_ROW>(acc, sP, sX1, mD, nD, 0, CH);
-#pragma unroll
-        for (int nt = 0; nt < NTD; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int r = mD + frag_g() + 8 * (e >> 1), c = nD + nt * 8 + 2 * frag_c() + (e & 1);
-                const float f = fac(F_KDP, r, c);
-                dQn[0][nt][e] += p.scale * acc[0][nt][e] * f;
-                dGc[0][nt][e] += derived_val(qraw(r, c), derived_m(sInvQ[r], p.scale, 1.f), f) * acc[0][nt][e];
-            }
+        if (PREC) {
+            warp_mma<1, NTD, A_ROW, B_ROW>(acc, sDPlo, sX1, mD, nD, 0, CH);
+            warp_mma<1, NTD, A_ROW, B_ROW>(acc, sP, sKIlo, mD, nD, 0, CH);
+        }
+        FRAG_LOOP(NTD) {
+            FRAG_RC(mD, nD);
+            const float f = fac(F_KDP, r, c);
+            dQn[0][nt][e] += p.scale * acc[0][nt][e] * f;
+            dGc[0][nt][e] += tile_val(qraw(r, c), derived_m(sInvQ[r], p.scale, 1.f), f) * acc[0][nt][e];
+        }
         zero_acc(acc);
         warp_mma<1, NTD, A_ROW, B_ROW>(acc, sA, sX1, mD, nD, 0, CH);
-#pragma unroll
-        for (int nt = 0; nt < NTD; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int r = mD + frag_g() + 8 * (e >> 1), c = nD + nt * 8 + 2 * frag_c() + (e & 1);
-                const float f = fac(F_KDP, r, c);
-                dKn[0][nt][e] += acc[0][nt][e] * f;
-                dGc[0][nt][e] += derived_val(kraw(r, c), derived_m(sInvK[r], 1.f, 1.f), f) * acc[0][nt][e];
-            }
+        if (PREC) {
+            warp_mma<1, NTD, A_ROW, B_ROW>(acc, sBDAlo, sX1, mD, nD, 0, CH);
+            warp_mma<1, NTD, A_ROW, B_ROW>(acc, sA, sKIlo, mD, nD, 0, CH);
+        }
+        FRAG_LOOP(NTD) {
+            FRAG_RC(mD, nD);
+            const float f = fac(F_KDP, r, c);
+            dKn[0][nt][e] += acc[0][nt][e] * f;
+            dGc[0][nt][e] += tile_val(kraw(r, c), derived_m(sInvK[r], 1.f, 1.f), f) * acc[0][nt][e];
+        }
     }
     __syncthreads();
-    // qd' -> X1, kd' -> X2 ; dki' = dP^T qd' + (beta dA)^T kd'
-    build_tile<F_KDP, D, KDA, true>(sX1, sX1, p.q, p, ci, h, G, sInvQ, nullptr, p.scale);
-    build_tile<F_KDP, D, KDA, false>(sX2, sK, nullptr, p, ci, h, G, sInvK, nullptr, 1.f);
+    // qd' -> X1, kd' -> X2 (+ lo) ; dki' = dP^T qd' + (beta dA)^T kd'
+    build_tile<F_KDP, D, KDA, true>(sX1, sX1, p.q, p, ci, h, G, sInvQ, nullptr, p.scale, PREC ? &sQDlo : nullptr);
+    build_tile<F_KDP, D, KDA, false>(sX2, sK, nullptr, p, ci, h, G, sInvK, nullptr, 1.f, PREC ? &sKDlo : nullptr);
     __syncthreads();
     {
         float acc[1][NTD][4];
         zero_acc(acc);
         warp_mma<1, NTD, A_COL, B_ROW>(acc, sP, sX1, mD, nD, 0, CH);
         warp_mma<1, NTD, A_COL, B_ROW>(acc, sA, sX2, mD, nD, 0, CH);
-#pragma unroll
-        for (int nt = 0; nt < NTD; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int r = mD + frag_g() + 8 * (e >> 1), c = nD + nt * 8 + 2 * frag_c() + (e & 1);
-                const float f = fac(F_KIP, r, c);
-                dKn[0][nt][e] += acc[0][nt][e] * f;
-                dGc[0][nt][e] -= derived_val(kraw(r, c), derived_m(sInvK[r], 1.f, 1.f), f) * acc[0][nt][e];
-            }
+        if (PREC) {
+            warp_mma<1, NTD, A_COL, B_ROW>(acc, sDPlo, sX1, mD, nD, 0, CH);
+            warp_mma<1, NTD, A_COL, B_ROW>(acc, sP, sQDlo, mD, nD, 0, CH);
+            warp_mma<1, NTD, A_COL, B_ROW>(acc, sBDAlo, sX2, mD, nD, 0, CH);
+            warp_mma<1, NTD, A_COL, B_ROW>(acc, sA, sKDlo, mD, nD, 0, CH);
+        }
+        FRAG_LOOP(NTD) {
+            FRAG_RC(mD, nD);
+            const float f = fac(F_KIP, r, c);
+            dKn[0][nt][e] += acc[0][nt][e] * f;
+            dGc[0][nt][e] -= tile_val(kraw(r, c), derived_m(sInvK[r], 1.f, 1.f), f) * acc[0][nt][e];
+        }
     }
+#undef FRAG_LOOP
+#undef FRAG_RC
 
     // ---- epilogue -----------------------------------------------------------
     // row dots <dqn, qn>, <dkn, kn>
@@ -425,7 +455,8 @@ __global__ void __launch_bounds__(256, 1) k_main(const Params p) {
         }
     }
     __syncthreads();
-    // dq, dk stores; dgc -> fp32 scratch over the (now free) state tiles
+    // dq, dk stores; dgc -> fp32 scratch over the state tiles (their last
+    // readers, the residual tiles of the precise mode, are behind the barrier above)
     float* sDgc = reinterpret_cast<float*>(smem + SM::oS0);  // [C][D]
 #pragma unroll
     for (int nt = 0; nt < NTD; ++nt)

@@ -22,10 +22,10 @@ def _built():
     build.build()
 
 
-def _check(x, heads=None, label=""):
+def _check(x, heads=None, label="", conditioned=False):
     gpu = H.run_gpu(x)
     ref = H.run_oracle(x, heads)
-    res = H.compare(gpu, ref, x, heads)
+    res = H.compare(gpu, ref, x, heads, conditioned=conditioned)
     print(label, H.assert_parity(res, label))
     return gpu
 
@@ -44,8 +44,9 @@ def test_gdn_varlen_ragged(dim):
 
 @pytest.mark.parametrize("dim", [64, 128])
 def test_kda_varlen_ragged(dim):
+    # 205 tokens: dA_log / ddt_bias are short sums, judged against their term magnitudes
     x = inputs.custom("kda", [130, 70, 5], heads=2, dim=dim, seed=102, with_h0=True, with_dht=True)
-    _check(x, label="kda_ragged_d%d" % dim)
+    _check(x, label="kda_ragged_d%d" % dim, conditioned=True)
 
 
 def test_gdn_dense_layout():
