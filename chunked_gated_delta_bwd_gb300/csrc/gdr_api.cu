@@ -3,6 +3,8 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <mutex>
+
 #include "../../include/gdr.h"
 #include "gdr_common.cuh"
 #include "gdr_internal.h"
@@ -360,3 +362,60 @@ gdr_status gdr_profile_end(double* total_ms, int* launches) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// gdr_bwd_fixed: the GDN backward with its scratch in a static device array.
+//
+// Some callers cannot allocate device memory where they run the backward: a
+// plug-in whose host framework owns every device allocation and hands the
+// plug-in only tensors, or code on a path where a cudaMalloc (which may
+// synchronise the device or fail under memory pressure) is not allowed.  For
+// them this entry point needs no workspace argument: its scratch is the array
+// below, which every GPU that loads this library holds until the process exits.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) unsigned char g_fixed_ws[GDR_FIXED_WORKSPACE_BYTES];
+
+namespace gdr {
+static std::mutex g_fixed_mu;
+static void* g_fixed_addr[GDR_FIXED_MAX_DEVICES];
+
+// Device address of g_fixed_ws on the current device (resolved once per device).
+static gdr_status fixed_workspace(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= GDR_FIXED_MAX_DEVICES) return fail(GDR_ERR_UNSUPPORTED, "device index out of range%s");
+    std::lock_guard<std::mutex> lock(g_fixed_mu);
+    if (!g_fixed_addr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_fixed_ws);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(fixed workspace)");
+        g_fixed_addr[dev] = p;
+    }
+    *out = g_fixed_addr[dev];
+    return GDR_OK;
+}
+}  // namespace gdr
+
+extern "C" gdr_status gdr_bwd_fixed(const gdr_shape* shape, const void* q, const void* k, const void* v,
+                                    const float* g, const void* beta_logit, const float* h0, const void* dO,
+                                    const float* dht, const void* states, void* dq, void* dk, void* dv,
+                                    float* dg, void* dbeta, float* dh0, void* stream) {
+    if (gdr_status st0 = check_shape(shape)) return st0;
+    const size_t need = layout(shape).total;
+    if (need > (size_t)GDR_FIXED_WORKSPACE_BYTES) {
+        snprintf(g_err, sizeof(g_err),
+                 "gdr_bwd_fixed: this problem needs %zu bytes of scratch; the fixed workspace holds %zu "
+                 "(use gdr_bwd with a caller workspace)",
+                 need, (size_t)GDR_FIXED_WORKSPACE_BYTES);
+        return GDR_ERR_WORKSPACE;
+    }
+    void* ws = nullptr;
+    if (gdr_status st1 = fixed_workspace(&ws)) return st1;
+    // The status word is the only scratch that must start at zero; bwd_impl
+    // clears it on the stream before any kernel runs.  Everything else in the
+    // scratch is fully written before it is read within one call.
+    return bwd_impl(shape, q, k, v, g, nullptr, nullptr, nullptr, beta_logit, h0, dO, dht, states, ws,
+                    (size_t)GDR_FIXED_WORKSPACE_BYTES, dq, dk, dv, dg, nullptr, dbeta, dh0, nullptr, nullptr,
+                    stream, 0);
+}

@@ -118,6 +118,32 @@ gdr_status kda_bwd(const gdr_shape* shape, const void* q, const void* k, const v
                    void* dk, void* dv, void* dg_raw, void* dbeta, float* dh0, float* dA_log,
                    float* ddt_bias, void* stream);
 
+/* Allocation-free GDN backward (an addition of this library; the pages have no
+ * counterpart).  For callers that cannot allocate device memory where they run
+ * the backward: a plug-in whose host framework owns every device allocation,
+ * or code where a cudaMalloc (which may synchronise or fail) is not allowed.
+ *
+ * Same arguments and results as gdr_bwd, without the workspace: the scratch
+ * is a static device array of GDR_FIXED_WORKSPACE_BYTES inside this library,
+ * which every GPU that loads the library holds until the process exits.
+ *  * Problems whose gdr_workspace_bytes exceeds that size are rejected with
+ *    GDR_ERR_WORKSPACE (message in gdr_last_error) before anything is enqueued.
+ *  * The first call on a device (per process) resolves the array's device
+ *    address with cudaGetSymbolAddress, with that device current; make that
+ *    first call before any stream capture.
+ *  * Every call on a device shares the one array and leaves its contents
+ *    behind: calls that overlap on the GPU (different streams, or threads
+ *    without ordering) race; serialise them, e.g. on one stream.
+ *  * Device-side status bits (gdr_workspace_status) are not reported: the
+ *    caller has no handle on the scratch.
+ *  * Allocates nothing: no cudaMalloc / cudaFree or allocating library call. */
+#define GDR_FIXED_WORKSPACE_BYTES (64u << 20)
+#define GDR_FIXED_MAX_DEVICES 64
+gdr_status gdr_bwd_fixed(const gdr_shape* shape, const void* q, const void* k, const void* v,
+                         const float* g, const void* beta_logit, const float* h0, const void* dO,
+                         const float* dht, const void* states, void* dq, void* dk, void* dv,
+                         float* dg, void* dbeta, float* dh0, void* stream);
+
 /* Waits for `stream`, then returns in *device_status the OR of the GDR_DEV_*
  * bits raised by the last call that used `workspace` (0 = none). */
 gdr_status gdr_workspace_status(const void* workspace, void* stream, int* device_status);
