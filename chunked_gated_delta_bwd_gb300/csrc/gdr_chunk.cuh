@@ -29,20 +29,26 @@ struct Gates {
 };
 
 // Computes gc, gT and ref for one (chunk, head).  Rows >= len have g = 0.
+// Must be called by every thread of the block (it synchronises).
 template <int D, bool KDA>
 __device__ void load_gates(const Params& p, const ChunkInfo& ci, int h, const Gates<D, KDA>& G,
                            bool flag_range) {
     if constexpr (KDA) {
+        // per-element log gates (all threads, coalesced), then one thread per
+        // channel forms the inclusive cumsum in shared memory
         const float a = expf(p.A_log[h]);
+        for (int i = threadIdx.x; i < CH * D; i += blockDim.x) {
+            const int r = i / D, d = i % D;
+            float gv = 0.f;
+            if (r < ci.len) gv = -a * softplus_f(bf2f(p.g_raw[((ci.t0 + r) * p.H + h) * D + d]) + p.dt_bias[h * D + d]);
+            G.gc[r * G.LDG + d] = gv;
+        }
+        __syncthreads();
         for (int d = threadIdx.x; d < D; d += blockDim.x) {
-            const float dt = p.dt_bias[h * D + d];
             float acc = 0.f, mx = -3.0e38f, mn = 3.0e38f;
-            const __nv_bfloat16* src = p.g_raw + (ci.t0 * p.H + h) * D + d;
 #pragma unroll 8
             for (int r = 0; r < CH; ++r) {
-                float gv = 0.f;
-                if (r < ci.len) gv = -a * softplus_f(bf2f(src[(int64_t)r * p.H * D]) + dt);
-                acc += gv;
+                acc += G.gc[r * G.LDG + d];
                 G.gc[r * G.LDG + d] = acc;
                 mx = fmaxf(mx, acc);
                 mn = fminf(mn, acc);

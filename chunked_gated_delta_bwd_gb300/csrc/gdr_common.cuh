@@ -20,6 +20,7 @@ constexpr int CH = 64;  // chunk length
 // Status bits OR-ed into the workspace status word by device code.
 constexpr int ST_BAD_SEQLENS = 1;  // cu_seqlens not monotone / wrong total
 constexpr int ST_GATE_RANGE = 2;   // a chunk's gate span exceeds the exponent range handled
+constexpr int ST_MMA_TIMEOUT = 4;  // a bounded wait for the tensor cores ran out (the CTA gave up)
 
 // --------------------------------------------------------------------------
 // small utilities
@@ -197,8 +198,20 @@ __device__ __forceinline__ bool lookup_chunk(int gc, int N, const int* chunk_off
     return true;
 }
 
-// softplus and sigmoid in fp32 (CUDA math library calls)
-__device__ __forceinline__ float softplus_f(float x) { return x > 20.f ? x : log1pf(expf(x)); }
-__device__ __forceinline__ float sigmoid_f(float x) { return 1.f / (1.f + expf(-x)); }
+// softplus(x) = max(x, 0) + log(1 + e^{-|x|}).  With y = e^{-|x|} in (0, 1]:
+// y >= 1/16 takes the hardware logarithm of 1 + y (absolute error ~1e-7 on a
+// result >= 0.06); smaller y takes the alternating series of log(1 + y) to y^6
+// (truncation below 1e-9 relative).  Relative error of the result ~3e-6.
+__device__ __forceinline__ float softplus_f(float x) {
+    const float y = __expf(-fabsf(x));
+    float l;
+    if (y >= 0.0625f) {
+        l = __logf(1.f + y);
+    } else {
+        l = y * (1.f - y * (0.5f - y * (1.f / 3.f - y * (0.25f - y * (0.2f - y * (1.f / 6.f))))));
+    }
+    return fmaxf(x, 0.f) + l;
+}
+__device__ __forceinline__ float sigmoid_f(float x) { return __fdividef(1.f, 1.f + __expf(-x)); }
 
 }  // namespace gdr

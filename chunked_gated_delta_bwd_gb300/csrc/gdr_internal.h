@@ -42,5 +42,6 @@ cudaError_t launch_chunk_table(const Params& p, cudaStream_t s);
 cudaError_t launch_prep(const Params& p, cudaStream_t s);
 cudaError_t launch_states(const Params& p, bool fwd, bool bwd, cudaStream_t s);
 cudaError_t launch_main(const Params& p, cudaStream_t s);
+cudaError_t launch_main_tc(const Params& p, cudaStream_t s);  // GDN, D = 128, tcgen05
 
 }  // namespace gdr

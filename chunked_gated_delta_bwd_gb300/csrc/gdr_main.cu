@@ -520,33 +520,45 @@ __global__ void __launch_bounds__(256, 1) k_main(const Params p) {
             if (2 * lane + 1 < ci.len) p.dg[(ci.t0 + 2 * lane + 1) * p.H + h] = suf1;
         }
     } else {
-        const float ea = expf(p.A_log[h]);
-        float dA_acc = 0.f;
+        // suffix sums per channel in place (one thread per channel), then the gate
+        // chain elementwise over all threads with per-channel partial sums
         for (int d = threadIdx.x; d < D; d += blockDim.x) {
-            const float dt = p.dt_bias[h * D + d];
-            float acc = dgT_of(d), ddt = 0.f;
+            float acc = dgT_of(d);
             for (int r = CH - 1; r >= 0; --r) {
                 acc += sDgc[r * D + d];
-                if (r < ci.len) {
-                    const size_t o = ((ci.t0 + r) * p.H + h) * D + d;
-                    const float x = bf2f(p.g_raw[o]) + dt;
-                    const float gl = -ea * softplus_f(x);
-                    const float draw = acc * (-ea * sigmoid_f(x));
-                    p.dg_raw[o] = __float2bfloat16(draw);
-                    ddt += draw;
-                    dA_acc += acc * gl;
-                }
+                sDgc[r * D + d] = acc;
             }
-            atomicAdd(&p.ddt_bias[h * D + d], ddt);
         }
+        __syncthreads();
+        const float ea = expf(p.A_log[h]);
+        constexpr int RSTEP = 256 / D;  // rows handled per pass (threads per channel)
+        const int d = threadIdx.x % D, r0 = threadIdx.x / D;
+        const float dt = p.dt_bias[h * D + d];
+        float ddt = 0.f, dA_acc = 0.f;
+        for (int r = r0; r < ci.len; r += RSTEP) {
+            const size_t o = ((ci.t0 + r) * p.H + h) * D + d;
+            const float x = bf2f(p.g_raw[o]) + dt;
+            const float dgl = sDgc[r * D + d];
+            const float draw = dgl * (-ea * sigmoid_f(x));
+            p.dg_raw[o] = __float2bfloat16(draw);
+            ddt += draw;
+            dA_acc += dgl * (-ea * softplus_f(x));
+        }
+        __syncthreads();  // sDgc reads done; reuse the row-sum scratch for the partials
+        sRowQ[threadIdx.x] = ddt;  // [RSTEP][D] (256 floats: rowq and rowk are contiguous)
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) dA_acc += __shfl_xor_sync(0xffffffffu, dA_acc, o);
         if (lane == 0) sMisc[warp] = dA_acc;
         __syncthreads();
+        if (threadIdx.x < D) {
+            float t = 0.f;
+            for (int j = 0; j < RSTEP; ++j) t += sRowQ[j * D + threadIdx.x];
+            atomicAdd(&p.ddt_bias[h * D + threadIdx.x], t);
+        }
         if (threadIdx.x == 0) {
-            float s = 0.f;
-            for (int w = 0; w < 8; ++w) s += sMisc[w];
-            atomicAdd(&p.dA_log[h], s);
+            float t = 0.f;
+            for (int w = 0; w < 8; ++w) t += sMisc[w];
+            atomicAdd(&p.dA_log[h], t);
         }
     }
 }
@@ -563,6 +575,7 @@ static cudaError_t launch_main_t(const Params& p, cudaStream_t s) {
 
 cudaError_t launch_main(const Params& p, cudaStream_t s) {
     if (p.max_chunks == 0) return cudaSuccess;
+    if (p.D == 128 && !p.kda) return launch_main_tc(p, s);
     if (p.D == 128) return p.kda ? launch_main_t<128, true>(p, s) : launch_main_t<128, false>(p, s);
     return p.kda ? launch_main_t<64, true>(p, s) : launch_main_t<64, false>(p, s);
 }

@@ -1,8 +1,8 @@
 // The two serial chunk recurrences, one CTA per (sequence, head, value slice).
 //
 // The state S (dk x dv) and its gradient dS are independent across value
-// columns, so each CTA owns BV = 16 columns and carries them in fp32
-// registers through every chunk of its sequence.  Both recurrences use only
+// columns, so each CTA (8 warps) owns BV = 32 columns and carries them in
+// fp32 registers through every chunk of its sequence.  Both recurrences use only
 // the per-chunk tiles written by the prep kernel; neither depends on the
 // other, so one launch runs both (blockIdx.y selects the role).
 //
@@ -16,7 +16,7 @@
 
 namespace gdr {
 
-constexpr int BV = 16;        // value columns per CTA
+constexpr int BV = 32;        // value columns per CTA
 constexpr int LDV = BV + 8;   // padded row (elements) of the narrow tiles
 
 template <int D>
@@ -38,12 +38,12 @@ __device__ __forceinline__ int chunk_begin(const Params& p, int seq) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(128) k_states(const Params p, int role0) {
+__global__ void __launch_bounds__(256) k_states(const Params p, int role0) {
     using SM = StateSmem<D>;
     using TileCD = SwzTile<SM::ROWB>;
     using TileN = PadTile<LDV>;
     constexpr int SLICES = D / BV;
-    constexpr int MT = D / 64;  // 16-row tiles per warp over the dk rows (4 warps)
+    constexpr int MT = D / 64;  // 16-row tiles per warp over the dk rows (4 row bands x 2 column halves)
     extern __shared__ __align__(1024) unsigned char smem[];
 
     const int role = role0 + blockIdx.y;
@@ -59,13 +59,14 @@ __global__ void __launch_bounds__(128) k_states(const Params p, int role0) {
     TileN sS{smem + SM::oS}, sY{smem + SM::oY};
     auto stage = [&](int b) { return smem + (b ? SM::oStage1 : SM::oStage0); };
 
-    // state rows owned by this warp: d = 16*MT*warp + 16*mt + g (+8)
-    const int m0 = 16 * MT * warp;
+    // state fragment of this warp: rows 16*MT*(warp&3) .. (D/4 rows), columns 16*(warp>>2) .. +16
+    const int m0 = 16 * MT * (warp & 3), n0 = 16 * (warp >> 2);
+    const int mx = 16 * (warp & 3);  // rows of the C x BV product
     float st[MT][2][4];
     {
         const float* init = role == 0 ? p.h0 : p.dht;
         const size_t sb = ((size_t)seq * p.H + h) * D * D;
-        frag_foreach(st, m0, 0, [&](int r, int c, float& a0, float& a1) {
+        frag_foreach(st, m0, n0, [&](int r, int c, float& a0, float& a1) {
             a0 = init ? init[sb + (size_t)r * D + col0 + c] : 0.f;
             a1 = init ? init[sb + (size_t)r * D + col0 + c + 1] : 0.f;
         });
@@ -80,8 +81,8 @@ __global__ void __launch_bounds__(128) k_states(const Params p, int role0) {
         if (role == 0) {
             async_load_tile<CH, D>(t0, p.W + tcd);
             async_load_tile<CH, D>(t1, p.Kr + tcd);
-            for (int i = threadIdx.x; i < CH * 2; i += blockDim.x) {
-                const int r = i >> 1, j = i & 1;
+            for (int i = threadIdx.x; i < CH * (BV / 8); i += blockDim.x) {
+                const int r = i / (BV / 8), j = i % (BV / 8);
                 cp_async16(tn.chunk(r, j), p.U + tcd + r * D + col0 + j * 8, true);
             }
         } else {
@@ -93,8 +94,8 @@ __global__ void __launch_bounds__(128) k_states(const Params p, int role0) {
             const int64_t t0r = bos + (int64_t)local * CH;
             const int64_t rem = eos - t0r;
             const int len = (int)(rem < CH ? rem : CH);
-            for (int i = threadIdx.x; i < CH * 2; i += blockDim.x) {
-                const int r = i >> 1, j = i & 1;
+            for (int i = threadIdx.x; i < CH * (BV / 8); i += blockDim.x) {
+                const int r = i / (BV / 8), j = i % (BV / 8);
                 const bool ok = r < len;
                 cp_async16(tn.chunk(r, j), p.dO + ((t0r + (ok ? r : 0)) * p.H + h) * D + col0 + j * 8, ok);
             }
@@ -121,7 +122,7 @@ __global__ void __launch_bounds__(128) k_states(const Params p, int role0) {
 
         // save the state entering this step (S0 of chunk c, or dS_C of chunk c)
         __nv_bfloat16* dst = (role == 0 ? p.S0 : p.dS) + ((size_t)c * p.H + h) * D * D;
-        frag_foreach(st, m0, 0, [&](int r, int cc, float a0, float a1) {
+        frag_foreach(st, m0, n0, [&](int r, int cc, float a0, float a1) {
             const uint32_t w = pack_bf16(a0, a1);
             *reinterpret_cast<uint32_t*>(sS.ptr(r, cc)) = w;
             *reinterpret_cast<uint32_t*>(dst + (size_t)r * D + col0 + cc) = w;
@@ -132,8 +133,8 @@ __global__ void __launch_bounds__(128) k_states(const Params p, int role0) {
         {
             float x[1][2][4];
             zero_acc(x);
-            warp_mma<1, 2, A_ROW, B_ROW>(x, role == 0 ? t0 : t0, sS, 16 * warp, 0, 0, D);
-            frag_foreach(x, 16 * warp, 0, [&](int r, int cc, float a0, float a1) {
+            warp_mma<1, 2, A_ROW, B_ROW>(x, t0, sS, mx, n0, 0, D);
+            frag_foreach(x, mx, n0, [&](int r, int cc, float a0, float a1) {
                 float o0, o1;
                 if (role == 0) {
                     const float2 u = unpack_bf16(*reinterpret_cast<const uint32_t*>(tn.ptr(r, cc)));
@@ -149,22 +150,22 @@ __global__ void __launch_bounds__(128) k_states(const Params p, int role0) {
         __syncthreads();
 
         // decay the carried rows, then accumulate the chunk's contribution
-        frag_foreach(st, m0, 0, [&](int r, int, float& a0, float& a1) {
+        frag_foreach(st, m0, n0, [&](int r, int, float& a0, float& a1) {
             const float gam = __expf(gs[r]);
             a0 *= gam;
             a1 *= gam;
         });
         if (role == 0) {
-            warp_mma<MT, 2, A_COL, B_ROW>(st, t1, sY, m0, 0, 0, CH);  // + kr^T Vn
+            warp_mma<MT, 2, A_COL, B_ROW>(st, t1, sY, m0, n0, 0, CH);  // + kr^T Vn
         } else {
-            warp_mma<MT, 2, A_COL, B_ROW>(st, t1, tn, m0, 0, 0, CH);  // + R_hi^T dO
-            warp_mma<MT, 2, A_COL, B_ROW>(st, t3, tn, m0, 0, 0, CH);  // + R_lo^T dO
-            warp_mma<MT, 2, A_COL, B_ROW>(st, t2, sY, m0, 0, 0, CH);  // - W^T Y
+            warp_mma<MT, 2, A_COL, B_ROW>(st, t1, tn, m0, n0, 0, CH);  // + R_hi^T dO
+            warp_mma<MT, 2, A_COL, B_ROW>(st, t3, tn, m0, n0, 0, CH);  // + R_lo^T dO
+            warp_mma<MT, 2, A_COL, B_ROW>(st, t2, sY, m0, n0, 0, CH);  // - W^T Y
         }
     }
     if (role == 1) {
         const size_t sb = ((size_t)seq * p.H + h) * D * D;
-        frag_foreach(st, m0, 0, [&](int r, int c, float a0, float a1) {
+        frag_foreach(st, m0, n0, [&](int r, int c, float a0, float a1) {
             p.dh0[sb + (size_t)r * D + col0 + c] = a0;
             p.dh0[sb + (size_t)r * D + col0 + c + 1] = a1;
         });
@@ -177,7 +178,7 @@ static cudaError_t launch_states_t(const Params& p, int role0, int nroles, cudaS
     cudaError_t e = cudaFuncSetAttribute(k_states<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess) return e;
     dim3 grid(p.N * p.H * (D / BV), nroles);
-    k_states<D><<<grid, 128, bytes, s>>>(p, role0);
+    k_states<D><<<grid, 256, bytes, s>>>(p, role0);
     return cudaGetLastError();
 }
 

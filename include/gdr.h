@@ -64,6 +64,7 @@ typedef enum {
 /* Device-side status bits (gdr_workspace_status). */
 #define GDR_DEV_BAD_SEQLENS 1 /* cu_seqlens not non-decreasing from 0 to T_total */
 #define GDR_DEV_GATE_RANGE 2  /* a chunk's log-gate span exceeded 160 (or a cumulative gate > 80) */
+#define GDR_DEV_TIMEOUT 4     /* a bounded wait for the tensor cores ran out; that CTA's outputs are missing */
 
 typedef struct {
     int32_t num_seqs;          /* N >= 1 */
