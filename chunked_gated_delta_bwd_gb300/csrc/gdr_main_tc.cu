@@ -39,18 +39,12 @@ constexpr int oSmall = 204800;
 // small arrays (floats)
 constexpr int NCOL = 16;  // columns per thread (16 warps: 4 lane quarters x 4 column quarters)
 constexpr int nInvQ = 64, nInvK = 64, nBeta = 64, nFac = 256, nGate = 128, nDgTs = 128, nDgTp = 512,
-              nDbP = 256, nDbA = 256, nRow = 256 * 3, nMisc = 64;
+              nDbP = 64, nDbA = 256, nRow = 256 * 3, nMisc = 64;
 constexpr int SMALL_FLOATS = nInvQ + nInvK + nBeta + nFac + nGate + nDgTs + nDgTp + nDbP + nDbA + nRow + nMisc;
 constexpr int SMEM_BYTES = oSmall + SMALL_FLOATS * 4 + 64 + 1024;  // + mbarrier/tmem slot + alignment
 // tensor-memory columns
-constexpr uint32_t R_A = 0, R_B = 128, R_C = 192, R_D = 256;
+constexpr uint32_t R_A = 0, R_B = 128, R_C = 192, R_D = 256, R_Q = 320, R_K = 384;
 
-__device__ __forceinline__ float bf_at(const unsigned char* base, int r, int c, int rows) {
-    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(base + tc::sw_off(r, c, rows)));
-}
-__device__ __forceinline__ void bf_put(unsigned char* base, int r, int c, int rows, float v) {
-    *reinterpret_cast<__nv_bfloat16*>(base + tc::sw_off(r, c, rows)) = __float2bfloat16(v);
-}
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
@@ -128,7 +122,7 @@ __global__ void __launch_bounds__(512, 1) k_main_tc(const Params p) {
     float* sGate = sFac + nFac;      // gc[64], ref, gT
     float* sDgTs = sGate + nGate;    // [128] state part of dgT
     float* sDgTp = sDgTs + nDgTs;    // [4][128] kr part of dgT per column quarter
-    float* sDbP = sDgTp + nDgTp;     // [4][64] <dY, beta E> per lane quarter
+    float* sDbP = sDgTp + nDgTp;     // [64] <dY, beta E> per row
     float* sDbA = sDbP + nDbP;       // [4][64] rowsum(dA . A) per column quarter
     float* sRow = sDbA + nDbA;       // [3][4][64] row reductions
     float* sMisc = sRow + nRow;      // [64]
@@ -237,12 +231,30 @@ __global__ void __launch_bounds__(512, 1) k_main_tc(const Params p) {
     const float* facKR = sFac + 3 * CH;
 
     // per-thread accumulators (feature L, rows c0 .. c0+15)
-    float dQn[NCOL], dKn[NCOL], dGc[NCOL], v[NCOL];
+    float dQn[NCOL], dKn[NCOL], dGc[NCOL], v[NCOL], qk[NCOL];
 #pragma unroll
     for (int i = 0; i < NCOL; ++i) dQn[i] = dKn[i] = dGc[i] = 0.f;
-    auto qraw = [&](int r, int d) -> float {
-        return r < ci.len ? bf2f(p.q[((ci.t0 + r) * p.H + h) * TC_D + d]) : 0.f;
+    // byte offset of element (row c0 + i, column L) in a token-major SW128 tile with `rows` rows;
+    // c0 is a multiple of 16, so (row & 7) == (i & 7) is known at compile time
+    const int lch = (L & 63) >> 3, lsub = (L & 7) << 1;
+    auto tok = [&](int rows, int i) -> uint32_t {
+        return (uint32_t)((L >> 6) * rows * 128 + (c0 + i) * 128 + ((lch ^ (i & 7)) << 4) + lsub);
     };
+    auto tok_bf = [&](const unsigned char* base, int rows, int i) -> float {
+        return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(base + tok(rows, i)));
+    };
+    // raw q and k of this thread's feature and rows, staged once in tensor memory
+    {
+#pragma unroll
+        for (int i = 0; i < NCOL; ++i) {
+            const int r = c0 + i;
+            qk[i] = r < ci.len ? bf2f(p.q[((ci.t0 + r) * p.H + h) * TC_D + L]) : 0.f;
+        }
+        tc::st16(tl(R_Q + c0), qk);
+#pragma unroll
+        for (int i = 0; i < NCOL; ++i) qk[i] = tok_bf(sK, 64, i);
+        tc::st16(tl(R_K + c0), qk);
+    }
 
     // ---- G1: [A_raw; P] = [kd'; qd'] ki'^T ----------------------------------------
     build_sw<false>(sW0, 128, 0, sK, nullptr, p, ci, h, facKDP, sInvK, 1.f);        // kd'
@@ -298,15 +310,17 @@ __global__ void __launch_bounds__(512, 1) k_main_tc(const Params p) {
 #pragma unroll
     for (int i = 0; i < NCOL; ++i) {  // beta E = beta (V - X), in place of V (lane = value channel)
         const int r = c0 + i;
-        bf_put(sV, r, L, 64, sBeta[r] * (bf_at(sV, r, L, 64) - v[i]));
+        __nv_bfloat16* pv = reinterpret_cast<__nv_bfloat16*>(sV + tok(64, i));
+        *pv = __float2bfloat16(sBeta[r] * (__bfloat162float(*pv) - v[i]));
     }
     tc::ld16(tl(R_D + c0), v);
+    tc::ld16(tl(R_Q + c0), qk);
 #pragma unroll
     for (int i = 0; i < NCOL; ++i) {  // dqd (lane = key channel)
         const int r = c0 + i;
         const float t = p.scale * v[i] * facKD[r];
         dQn[i] += t;
-        dGc[i] += qraw(r, L) * sInvQ[r] * t;
+        dGc[i] += qk[i] * sInvQ[r] * t;
     }
     build_sw<false>(sW2, 64, 0, sK, nullptr, p, ci, h, facKR, sInvK, 1.f);   // kr (ki' is dead)
     sync_all();
@@ -324,19 +338,27 @@ __global__ void __launch_bounds__(512, 1) k_main_tc(const Params p) {
         tc::commit(mb);
     }
     if (!wait_mma()) return;
+    // u^T and du^T are stored feature-major ([j][r], 128 rows x 64 columns): 16-byte row stores
+    auto store_fm = [&](unsigned char* dst) {
+#pragma unroll
+        for (int jc = 0; jc < NCOL / 8; ++jc) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) w[e] = pack_bf16(v[jc * 8 + 2 * e], v[jc * 8 + 2 * e + 1]);
+            *reinterpret_cast<uint4*>(dst + tc::sw_chunk(L, (c0 >> 3) + jc, 128)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    };
     tc::ld16(tl(R_B + c0), v);
-#pragma unroll
-    for (int i = 0; i < NCOL; ++i) bf_put(sW1, c0 + i, L, 64, v[i]);  // u [r][j]
+    store_fm(sW1);  // u^T
     tc::ld16(tl(R_C + c0), v);
-#pragma unroll
-    for (int i = 0; i < NCOL; ++i) bf_put(sW2, c0 + i, L, 64, v[i]);  // du [r][j] over kr
+    store_fm(sW2);  // du^T over kr
     sync_all();
 
     // ---- G6: dY^T = du^T T ------------------------------------------------------------
     if (tid == 0) {
-        constexpr uint32_t id6 = tc::idesc(128, 64, 1, 1);
+        constexpr uint32_t id6 = tc::idesc(128, 64, 0, 1);
         for (int k = 0; k < CH; k += 16)
-            tc::mma(tmem + R_D, tc::mdesc(sb + oW2, 64, 0, k), tc::mdesc(sb + oT, 64, 0, k), id6, k > 0);
+            tc::mma(tmem + R_D, tc::kdesc(sb + oW2, 128, 0, k), tc::mdesc(sb + oT, 64, 0, k), id6, k > 0);
         tc::commit(mb);
     }
     if (!wait_mma()) return;
@@ -344,33 +366,49 @@ __global__ void __launch_bounds__(512, 1) k_main_tc(const Params p) {
 #pragma unroll
     for (int i = 0; i < NCOL; ++i) {
         const int r = c0 + i;
-        if (r < ci.len)
-            p.dv[((ci.t0 + r) * p.H + h) * TC_D + L] = __float2bfloat16(sBeta[r] * v[i]);
-        const float db = warp_sum(v[i] * bf_at(sV, r, L, 64));  // <dY, beta E> over this warp's 32 channels
-        if (lane == 0) sDbP[q4 * CH + r] = db;
-        bf_put(sDOY, 64 + r, L, 128, v[i]);  // dY [r][j] below dO
+        if (r < ci.len) p.dv[((ci.t0 + r) * p.H + h) * TC_D + L] = __float2bfloat16(sBeta[r] * v[i]);
+        *reinterpret_cast<__nv_bfloat16*>(sDOY + tok(128, i) + 64 * 128) = __float2bfloat16(v[i]);  // dY below dO
     }
     sync_all();
 
     // ---- G7: Z^T = S0 dY^T ; G8: dkr^T = dS u^T ; G9: [dP; dA]_raw = [dO; dY] u^T ------------
     if (tid == 0) {
-        constexpr uint32_t id = tc::idesc(128, 64, 0, 0);
+        constexpr uint32_t id7 = tc::idesc(128, 64, 0, 0), id89 = tc::idesc(128, 64, 0, 1);
         for (int k = 0; k < TC_D; k += 16)
-            tc::mma(tmem + R_B, tc::kdesc(sb + oS0, 128, 0, k), tc::kdesc(sb + oDOY, 128, 64, k), id, k > 0);
+            tc::mma(tmem + R_B, tc::kdesc(sb + oS0, 128, 0, k), tc::kdesc(sb + oDOY, 128, 64, k), id7, k > 0);
         for (int k = 0; k < TC_D; k += 16)
-            tc::mma(tmem + R_C, tc::kdesc(sb + oDS, 128, 0, k), tc::kdesc(sb + oW1, 64, 0, k), id, k > 0);
+            tc::mma(tmem + R_C, tc::kdesc(sb + oDS, 128, 0, k), tc::mdesc(sb + oW1, 128, 0, k), id89, k > 0);
         for (int k = 0; k < TC_D; k += 16)
-            tc::mma(tmem + R_D, tc::kdesc(sb + oDOY, 128, 0, k), tc::kdesc(sb + oW1, 64, 0, k), id, k > 0);
+            tc::mma(tmem + R_D, tc::kdesc(sb + oDOY, 128, 0, k), tc::mdesc(sb + oW1, 128, 0, k), id89, k > 0);
         tc::commit(mb);
     }
+    // while the tensor cores run: <dY, beta E> per row (token-major, 4 threads per row)
+    if (tid < 4 * CH) {
+        const int r = tid >> 2, part = tid & 3;
+        float s2 = 0.f;
+        for (int j = part * 4; j < part * 4 + 4; ++j) {
+            uint4 a = *reinterpret_cast<const uint4*>(sDOY + tc::sw_chunk(64 + r, j, 128));
+            uint4 b = *reinterpret_cast<const uint4*>(sV + tc::sw_chunk(r, j, 64));
+            const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 fa = unpack_bf16(wa[e]), fb = unpack_bf16(wb[e]);
+                s2 += fa.x * fb.x + fa.y * fb.y;
+            }
+        }
+        s2 += __shfl_xor_sync(0xffffffffu, s2, 1);
+        s2 += __shfl_xor_sync(0xffffffffu, s2, 2);
+        if (part == 0) sDbP[r] = s2;
+    }
     if (!wait_mma()) return;
+    tc::ld16(tl(R_K + c0), qk);  // raw k
     tc::ld16(tl(R_B + c0), v);
 #pragma unroll
     for (int i = 0; i < NCOL; ++i) {  // dkd (from E) = -beta Z
         const int r = c0 + i;
         const float t = -sBeta[r] * v[i] * facKD[r];
         dKn[i] += t;
-        dGc[i] += bf_at(sK, r, L, 64) * sInvK[r] * t;
+        dGc[i] += qk[i] * sInvK[r] * t;
     }
     tc::ld16(tl(R_C + c0), v);
     {
@@ -380,7 +418,7 @@ __global__ void __launch_bounds__(512, 1) k_main_tc(const Params p) {
             const int r = c0 + i;
             const float t = v[i] * facKR[r];
             dKn[i] += t;
-            const float kt = bf_at(sK, r, L, 64) * sInvK[r] * t;
+            const float kt = qk[i] * sInvK[r] * t;
             dGc[i] -= kt;
             dgt += kt;
         }
@@ -395,6 +433,8 @@ __global__ void __launch_bounds__(512, 1) k_main_tc(const Params p) {
 #pragma unroll
         for (int jc = 0; jc < NCOL / 8; ++jc) {
             uint32_t w[4];
+            const uint4 av = *reinterpret_cast<const uint4*>(sA + tc::sw_chunk(r, (c0 >> 3) + jc, 64));
+            const uint32_t wa[4] = {av.x, av.y, av.z, av.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int s0 = c0 + jc * 8 + 2 * e;
@@ -405,7 +445,8 @@ __global__ void __launch_bounds__(512, 1) k_main_tc(const Params p) {
                 } else {
                     a0 = s0 < r ? -a0 : 0.f;
                     a1 = s0 + 1 < r ? -a1 : 0.f;
-                    dbs += a0 * bf_at(sA, r, s0, 64) + a1 * bf_at(sA, r, s0 + 1, 64);
+                    const float2 aa = unpack_bf16(wa[e]);
+                    dbs += a0 * aa.x + a1 * aa.y;
                     a0 *= sBeta[r];
                     a1 *= sBeta[r];
                 }
@@ -433,21 +474,23 @@ __global__ void __launch_bounds__(512, 1) k_main_tc(const Params p) {
         tc::commit(mb);
     }
     if (!wait_mma()) return;
+    tc::ld16(tl(R_Q + c0), qk);  // raw q
     tc::ld16(tl(R_A + c0), v);
 #pragma unroll
     for (int i = 0; i < NCOL; ++i) {  // dqd'
         const int r = c0 + i;
         const float f = facKDP[r];
         dQn[i] += p.scale * v[i] * f;
-        dGc[i] += derived_val(qraw(r, L), derived_m(sInvQ[r], p.scale, 1.f), f) * v[i];
+        dGc[i] += derived_val(qk[i], derived_m(sInvQ[r], p.scale, 1.f), f) * v[i];
     }
+    tc::ld16(tl(R_K + c0), qk);  // raw k
     tc::ld16(tl(R_A + 64 + c0), v);
 #pragma unroll
     for (int i = 0; i < NCOL; ++i) {  // dkd'
         const int r = c0 + i;
         const float f = facKDP[r];
         dKn[i] += v[i] * f;
-        dGc[i] += derived_val(bf_at(sK, r, L, 64), derived_m(sInvK[r], 1.f, 1.f), f) * v[i];
+        dGc[i] += derived_val(qk[i], derived_m(sInvK[r], 1.f, 1.f), f) * v[i];
     }
     tc::ld16(tl(R_B + c0), v);
 #pragma unroll
@@ -455,19 +498,20 @@ __global__ void __launch_bounds__(512, 1) k_main_tc(const Params p) {
         const int r = c0 + i;
         const float f = facKIP[r];
         dKn[i] += v[i] * f;
-        dGc[i] -= derived_val(bf_at(sK, r, L, 64), derived_m(sInvK[r], 1.f, 1.f), f) * v[i];
+        dGc[i] -= derived_val(qk[i], derived_m(sInvK[r], 1.f, 1.f), f) * v[i];
     }
 
     // ---- epilogue: L2 backward, dq / dk, dbeta, dg ---------------------------------------
     float* sRowQ = sRow;            // [4][64]
     float* sRowK = sRow + 256;      // [4][64]
     float* sRowG = sRow + 512;      // [4][64]
+    tc::ld16(tl(R_Q + c0), v);      // raw q (k is in qk)
 #pragma unroll
     for (int i = 0; i < NCOL; ++i) {
         const int r = c0 + i;
-        const float qn = qraw(r, L) * sInvQ[r];
-        const float kn = bf_at(sK, r, L, 64) * sInvK[r];
-        const float a = warp_sum(dQn[i] * qn), b = warp_sum(dKn[i] * kn), g = warp_sum(dGc[i]);
+        const float a = warp_sum(dQn[i] * v[i] * sInvQ[r]);
+        const float b = warp_sum(dKn[i] * qk[i] * sInvK[r]);
+        const float g = warp_sum(dGc[i]);
         if (lane == 0) {
             sRowQ[q4 * CH + r] = a;
             sRowK[q4 * CH + r] = b;
@@ -481,8 +525,8 @@ __global__ void __launch_bounds__(512, 1) k_main_tc(const Params p) {
         if (r < ci.len) {
             const float tq = ((sRowQ[r] + sRowQ[CH + r]) + sRowQ[2 * CH + r]) + sRowQ[3 * CH + r];
             const float tk = ((sRowK[r] + sRowK[CH + r]) + sRowK[2 * CH + r]) + sRowK[3 * CH + r];
-            const float qn = qraw(r, L) * sInvQ[r];
-            const float kn = bf_at(sK, r, L, 64) * sInvK[r];
+            const float qn = v[i] * sInvQ[r];
+            const float kn = qk[i] * sInvK[r];
             const size_t o = ((ci.t0 + r) * p.H + h) * TC_D + L;
             p.dq[o] = __float2bfloat16((dQn[i] - qn * tq) * sInvQ[r]);
             p.dk[o] = __float2bfloat16((dKn[i] - kn * tk) * sInvK[r]);
@@ -490,9 +534,8 @@ __global__ void __launch_bounds__(512, 1) k_main_tc(const Params p) {
     }
     // dbeta (logit space)
     for (int r = tid; r < ci.len; r += blockDim.x) {
-        const float dY_E = ((sDbP[r] + sDbP[CH + r]) + sDbP[2 * CH + r]) + sDbP[3 * CH + r];
         const float dA_A = ((sDbA[r] + sDbA[CH + r]) + sDbA[2 * CH + r]) + sDbA[3 * CH + r];
-        p.dbeta[(ci.t0 + r) * p.H + h] = __float2bfloat16((1.f - sBeta[r]) * (dY_E + dA_A));
+        p.dbeta[(ci.t0 + r) * p.H + h] = __float2bfloat16((1.f - sBeta[r]) * (sDbP[r] + dA_A));
     }
     // dg: channel sums of dgc (per row), suffix sums over the rows, plus the chunk constant dgT
     if (warp == 0) {
