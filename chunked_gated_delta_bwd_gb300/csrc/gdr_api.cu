@@ -75,7 +75,7 @@ cudaError_t launch_chunk_table(const Params& p, cudaStream_t s) {
 // ---------------------------------------------------------------------------
 struct Layout {
     int64_t max_chunks;
-    size_t status, chunk_off, W, U, Kr, R, Rlo, T, gT, S0, dS, total;
+    size_t status, chunk_off, W, U, Kr, R, Rlo, T, gT, egT, S0, dS, total;
 };
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -112,6 +112,7 @@ static Layout layout(const gdr_shape* sh) {
     L.Rlo = o; o = align256(o + mc * H * CH * D * 2);
     L.T = o; o = align256(o + mc * H * CH * CH * 2);
     L.gT = o; o = align256(o + mc * H * D * 4);
+    L.egT = o; o = align256(o + mc * H * D * 4);
     L.S0 = o; o = align256(o + mc * H * D * D * 2);
     L.dS = o; o = align256(o + mc * H * D * D * 2);
     L.total = o;
@@ -151,6 +152,7 @@ static void base_params(Params& p, const gdr_shape* sh, const Layout& L, void* w
     p.Rlo = reinterpret_cast<__nv_bfloat16*>(w + L.Rlo);
     p.Tm = reinterpret_cast<__nv_bfloat16*>(w + L.T);
     p.gT = reinterpret_cast<float*>(w + L.gT);
+    p.egT = reinterpret_cast<float*>(w + L.egT);
     p.S0 = reinterpret_cast<__nv_bfloat16*>(w + L.S0);
     p.dS = reinterpret_cast<__nv_bfloat16*>(w + L.dS);
 }

@@ -27,9 +27,11 @@ struct Params {
 
     // workspace
     int* status;
-    __nv_bfloat16 *W, *U, *Kr, *R, *Rlo, *Tm;  // per chunk-head tiles: [C][D] x5, [C][C]
-    float* gT;                           // [chunk][H][D]
-    __nv_bfloat16 *S0, *dS;              // per chunk-head states [D][D]
+    // per chunk-head tiles: W, Kr, R, Rlo [C][D]; U [C][D] (D = 64) or value-major [D][C]
+    // (D = 128); T [C][C]
+    __nv_bfloat16 *W, *U, *Kr, *R, *Rlo, *Tm;
+    float *gT, *egT;                     // [chunk][H][D]: chunk gate total and its exponential
+    __nv_bfloat16 *S0, *dS;              // per chunk-head states, value-major [dv][dk]
 
     // outputs
     __nv_bfloat16 *dq, *dk, *dv, *dbeta;
@@ -41,6 +43,7 @@ struct Params {
 cudaError_t launch_chunk_table(const Params& p, cudaStream_t s);
 cudaError_t launch_prep(const Params& p, cudaStream_t s);
 cudaError_t launch_states(const Params& p, bool fwd, bool bwd, cudaStream_t s);
+cudaError_t launch_states_tc(const Params& p, bool fwd, bool bwd, cudaStream_t s);  // D = 128, tcgen05 + TMA
 cudaError_t launch_main(const Params& p, cudaStream_t s);
 cudaError_t launch_main_tc(const Params& p, cudaStream_t s);  // GDN, D = 128, tcgen05
 

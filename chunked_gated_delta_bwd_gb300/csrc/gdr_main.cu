@@ -117,24 +117,27 @@ __global__ void __launch_bounds__(256, 1) k_main(const Params p) {
             sFac[3 * CH + r] = gate_factor<F_KR>(G, r, 0);
         }
     }
-    // dgT (state part) = e^{gT} rowsum(dS_C . S0)
+    // dgT (state part) = e^{gT} rowsum(dS_C . S0): the saved states are value-major
+    // ([dv][dk]), so for each key channel d it is a column sum over the value rows
     {
-        constexpr int TPR = 256 / D;  // threads per state row
-        const int r = threadIdx.x / TPR, part = threadIdx.x % TPR;
-        float s = 0.f;
-        for (int j = part * (D / 8 / TPR); j < (part + 1) * (D / 8 / TPR); ++j) {
-            uint4 a = *reinterpret_cast<const uint4*>(sS0.chunk(r, j));
-            uint4 b = *reinterpret_cast<const uint4*>(sDS.chunk(r, j));
-            const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                float2 fa = unpack_bf16(wa[e]), fb = unpack_bf16(wb[e]);
-                s += fa.x * fb.x + fa.y * fb.y;
-            }
+        constexpr int NG = 256 / (D / 2);  // row groups per column pair
+        const int cp = threadIdx.x / NG, g = threadIdx.x % NG;
+        float s0 = 0.f, s1 = 0.f;
+        for (int j = g; j < D; j += NG) {
+            const float2 a = unpack_bf16(*reinterpret_cast<const uint32_t*>(sS0.ptr(j, 2 * cp)));
+            const float2 b = unpack_bf16(*reinterpret_cast<const uint32_t*>(sDS.ptr(j, 2 * cp)));
+            s0 += a.x * b.x;
+            s1 += a.y * b.y;
         }
 #pragma unroll
-        for (int o = 1; o < TPR; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        if (part == 0) sDgTs[r] = s * __expf(G.gTv(r));
+        for (int o = 1; o < NG; o <<= 1) {
+            s0 += __shfl_xor_sync(0xffffffffu, s0, o);
+            s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+        }
+        if (g == 0) {
+            sDgTs[2 * cp] = s0 * __expf(G.gTv(2 * cp));
+            sDgTs[2 * cp + 1] = s1 * __expf(G.gTv(2 * cp + 1));
+        }
     }
     __syncthreads();
 
@@ -212,13 +215,13 @@ __global__ void __launch_bounds__(256, 1) k_main(const Params p) {
     {
         float acc[1][NTD][4];
         zero_acc(acc);
-        warp_mma<1, NTD, A_ROW, B_ROW>(acc, sX1, sS0, mD, nD, 0, D);
+        warp_mma<1, NTD, A_ROW, B_COL>(acc, sX1, sS0, mD, nD, 0, D);
         frag_foreach(acc, mD, nD, [&](int r, int c, float a0, float a1) {
             const float2 v = unpack_bf16(*reinterpret_cast<const uint32_t*>(sV.ptr(r, c)));
             store_pair(sV, PREC ? &sU : nullptr, r, c, sBeta[r] * (v.x - a0), sBeta[r] * (v.y - a1));
         });
         zero_acc(acc);
-        warp_mma<1, NTD, A_ROW, B_COL>(acc, sDO, sS0, mD, nD, 0, D);
+        warp_mma<1, NTD, A_ROW, B_ROW>(acc, sDO, sS0, mD, nD, 0, D);
         FRAG_LOOP(NTD) {
             FRAG_RC(mD, nD);
             const float t = p.scale * acc[0][nt][e] * fac(F_KD, r, c);
@@ -234,7 +237,7 @@ __global__ void __launch_bounds__(256, 1) k_main(const Params p) {
         float acc[1][NTD][4];
         zero_acc(acc);
         warp_mma<1, NTD, A_COL, B_ROW>(acc, sP, sDO, mD, nD, 0, CH);
-        warp_mma<1, NTD, A_ROW, B_ROW>(acc, sX1, sDS, mD, nD, 0, D);
+        warp_mma<1, NTD, A_ROW, B_COL>(acc, sX1, sDS, mD, nD, 0, D);
         frag_foreach(acc, mD, nD, [&](int r, int c, float a0, float a1) {
             *reinterpret_cast<uint32_t*>(sX2.ptr(r, c)) = pack_bf16(a0, a1);
         });
@@ -277,7 +280,7 @@ __global__ void __launch_bounds__(256, 1) k_main(const Params p) {
     {
         float acc[1][NTD][4];
         zero_acc(acc);
-        warp_mma<1, NTD, A_ROW, B_COL>(acc, sX2, sS0, mD, nD, 0, D);
+        warp_mma<1, NTD, A_ROW, B_ROW>(acc, sX2, sS0, mD, nD, 0, D);
         FRAG_LOOP(NTD) {
             FRAG_RC(mD, nD);
             const float t = -sBeta[r] * acc[0][nt][e] * fac(F_KD, r, c);
@@ -299,8 +302,8 @@ __global__ void __launch_bounds__(256, 1) k_main(const Params p) {
     {
         float acc[1][NTD][4];
         zero_acc(acc);
-        warp_mma<1, NTD, A_ROW, B_COL>(acc, sU, sDS, mD, nD, 0, D);
-        if (PREC) warp_mma<1, NTD, A_ROW, B_COL>(acc, sV, sDS, mD, nD, 0, D);
+        warp_mma<1, NTD, A_ROW, B_ROW>(acc, sU, sDS, mD, nD, 0, D);
+        if (PREC) warp_mma<1, NTD, A_ROW, B_ROW>(acc, sV, sDS, mD, nD, 0, D);
         float colsum[NTD][2];
 #pragma unroll
         for (int nt = 0; nt < NTD; ++nt) colsum[nt][0] = colsum[nt][1] = 0.f;

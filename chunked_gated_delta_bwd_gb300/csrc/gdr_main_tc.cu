@@ -7,7 +7,8 @@
 // row r), so a thread owns one feature for 16 rows and the per-row gate
 // factors are per-thread scalars.  C x C products stack two 64-row operands
 // into one 128-row operand ([kd'; qd'] ki'^T gives A and P; [dO; dY] u^T gives
-// dP and dA).  With S0 = chunk-start state, dS = state gradient at the chunk end:
+// dP and dA).  With S0 = chunk-start state, dS = state gradient at the chunk end (both
+// saved value-major, [dv][dk], so the operand major-ness below reads them transposed):
 //   G1  [A_raw; P]   = [kd'; qd'] ki'^T                 G7  Z^T    = S0 dY^T
 //   G2  X^T          = S0^T kd^T                        G8  dkr^T  = dS u^T
 //   G3  dqd^T        = S0 dO^T                          G9  [dP; dA] = [dO; dY] u^T
@@ -207,22 +208,25 @@ __global__ void __launch_bounds__(512, 1) k_main_tc(const Params p) {
         sFac[2 * CH + r] = gate_factor<F_KIP>(G, r, 0);
         sFac[3 * CH + r] = gate_factor<F_KR>(G, r, 0);
     }
-    {  // e^{gT} rowsum(dS . S0): four threads per state row
-        const int r = tid >> 2, part = tid & 3;
-        float s = 0.f;
-        for (int j = part * 4; j < part * 4 + 4; ++j) {
-            uint4 a = *reinterpret_cast<const uint4*>(sS0 + tc::sw_chunk(r, j, 128));
-            uint4 b = *reinterpret_cast<const uint4*>(sDS + tc::sw_chunk(r, j, 128));
-            const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float2 fa = unpack_bf16(wa[e]), fb = unpack_bf16(wb[e]);
-                s += fa.x * fb.x + fa.y * fb.y;
-            }
+    {  // e^{gT} rowsum(dS . S0) per key channel: a column sum of the value-major tiles
+        const int cp = tid >> 3, g = tid & 7;  // column pair, row group
+        float s0 = 0.f, s1 = 0.f;
+        for (int j = g; j < TC_D; j += 8) {
+            const float2 a = unpack_bf16(*reinterpret_cast<const uint32_t*>(sS0 + tc::sw_off(j, 2 * cp, 128)));
+            const float2 b = unpack_bf16(*reinterpret_cast<const uint32_t*>(sDS + tc::sw_off(j, 2 * cp, 128)));
+            s0 += a.x * b.x;
+            s1 += a.y * b.y;
         }
-        s += __shfl_xor_sync(0xffffffffu, s, 1);
-        s += __shfl_xor_sync(0xffffffffu, s, 2);
-        if (part == 0) sDgTs[r] = s * __expf(G.gTv(r));
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) {
+            s0 += __shfl_xor_sync(0xffffffffu, s0, o);
+            s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+        }
+        if (g == 0) {
+            const float eg = __expf(G.gTv(0));
+            sDgTs[2 * cp] = s0 * eg;
+            sDgTs[2 * cp + 1] = s1 * eg;
+        }
     }
     __syncthreads();
     const float* facKD = sFac;
@@ -298,11 +302,11 @@ __global__ void __launch_bounds__(512, 1) k_main_tc(const Params p) {
 
     // ---- G2: X^T = S0^T kd^T ; G3: dqd^T = S0 dO^T -----------------------------------
     if (tid == 0) {
-        constexpr uint32_t id2 = tc::idesc(128, 64, 1, 0), id3 = tc::idesc(128, 64, 0, 0);
+        constexpr uint32_t id2 = tc::idesc(128, 64, 0, 0), id3 = tc::idesc(128, 64, 1, 0);
         for (int k = 0; k < TC_D; k += 16)
-            tc::mma(tmem + R_C, tc::mdesc(sb + oS0, 128, 0, k), tc::kdesc(sb + oW0, 64, 0, k), id2, k > 0);
+            tc::mma(tmem + R_C, tc::kdesc(sb + oS0, 128, 0, k), tc::kdesc(sb + oW0, 64, 0, k), id2, k > 0);
         for (int k = 0; k < TC_D; k += 16)
-            tc::mma(tmem + R_D, tc::kdesc(sb + oS0, 128, 0, k), tc::kdesc(sb + oDOY, 128, 0, k), id3, k > 0);
+            tc::mma(tmem + R_D, tc::mdesc(sb + oS0, 128, 0, k), tc::kdesc(sb + oDOY, 128, 0, k), id3, k > 0);
         tc::commit(mb);
     }
     if (!wait_mma()) return;
@@ -328,13 +332,13 @@ __global__ void __launch_bounds__(512, 1) k_main_tc(const Params p) {
     // ---- G4: u^T = (beta E)^T T^T ; G5: du^T = dO^T P + dS^T kr^T -----------------------
     if (tid == 0) {
         constexpr uint32_t id4 = tc::idesc(128, 64, 1, 0), id5a = tc::idesc(128, 64, 1, 1),
-                           id5b = tc::idesc(128, 64, 1, 0);
+                           id5b = tc::idesc(128, 64, 0, 0);
         for (int k = 0; k < CH; k += 16)
             tc::mma(tmem + R_B, tc::mdesc(sb + oV, 64, 0, k), tc::kdesc(sb + oT, 64, 0, k), id4, k > 0);
         for (int k = 0; k < CH; k += 16)
             tc::mma(tmem + R_C, tc::mdesc(sb + oDOY, 128, 0, k), tc::mdesc(sb + oP, 64, 0, k), id5a, k > 0);
         for (int k = 0; k < TC_D; k += 16)
-            tc::mma(tmem + R_C, tc::mdesc(sb + oDS, 128, 0, k), tc::kdesc(sb + oW2, 64, 0, k), id5b, 1);
+            tc::mma(tmem + R_C, tc::kdesc(sb + oDS, 128, 0, k), tc::kdesc(sb + oW2, 64, 0, k), id5b, 1);
         tc::commit(mb);
     }
     if (!wait_mma()) return;
@@ -373,13 +377,14 @@ __global__ void __launch_bounds__(512, 1) k_main_tc(const Params p) {
 
     // ---- G7: Z^T = S0 dY^T ; G8: dkr^T = dS u^T ; G9: [dP; dA]_raw = [dO; dY] u^T ------------
     if (tid == 0) {
-        constexpr uint32_t id7 = tc::idesc(128, 64, 0, 0), id89 = tc::idesc(128, 64, 0, 1);
+        constexpr uint32_t id7 = tc::idesc(128, 64, 1, 0), id8 = tc::idesc(128, 64, 1, 1),
+                           id9 = tc::idesc(128, 64, 0, 1);
         for (int k = 0; k < TC_D; k += 16)
-            tc::mma(tmem + R_B, tc::kdesc(sb + oS0, 128, 0, k), tc::kdesc(sb + oDOY, 128, 64, k), id7, k > 0);
+            tc::mma(tmem + R_B, tc::mdesc(sb + oS0, 128, 0, k), tc::kdesc(sb + oDOY, 128, 64, k), id7, k > 0);
         for (int k = 0; k < TC_D; k += 16)
-            tc::mma(tmem + R_C, tc::kdesc(sb + oDS, 128, 0, k), tc::mdesc(sb + oW1, 128, 0, k), id89, k > 0);
+            tc::mma(tmem + R_C, tc::mdesc(sb + oDS, 128, 0, k), tc::mdesc(sb + oW1, 128, 0, k), id8, k > 0);
         for (int k = 0; k < TC_D; k += 16)
-            tc::mma(tmem + R_D, tc::kdesc(sb + oDOY, 128, 0, k), tc::mdesc(sb + oW1, 128, 0, k), id89, k > 0);
+            tc::mma(tmem + R_D, tc::kdesc(sb + oDOY, 128, 0, k), tc::mdesc(sb + oW1, 128, 0, k), id9, k > 0);
         tc::commit(mb);
     }
     // while the tensor cores run: <dY, beta E> per row (token-major, 4 threads per row)

@@ -14,8 +14,8 @@
 //        checked at 1e-3, and a single bf16 rounding of R alone costs ~1e-3)
 //   kr = kn e^{gT-gc}
 //
-// Outputs per (chunk, head): W, U, Kr, R_hi, R_lo as bf16 [C][D], T as bf16 [C][C],
-// gT as fp32 [D].
+// Outputs per (chunk, head): W, Kr, R_hi, R_lo as bf16 [C][D], U as bf16 [C][D] (D = 64)
+// or value-major [D][C] (D = 128), T as bf16 [C][C], gT and e^{gT} as fp32 [D].
 #include "gdr_chunk.cuh"
 
 namespace gdr {
@@ -141,7 +141,12 @@ __global__ void __launch_bounds__(256, 1) k_prep(const Params p) {
         zero_acc(acc);
         warp_mma<1, NTD, A_ROW, B_ROW>(acc, sT, sX2, m0, n0, 0, CH);
         frag_foreach(acc, m0, n0, [&](int r, int c, float a0, float a1) {
-            *reinterpret_cast<uint32_t*>(p.U + tile_cd + r * D + c) = pack_bf16(a0, a1);
+            if (D == 128) {  // value-major [D][C], the layout the D = 128 state recurrence reads
+                p.U[tile_cd + c * CH + r] = __float2bfloat16(a0);
+                p.U[tile_cd + (c + 1) * CH + r] = __float2bfloat16(a1);
+            } else {
+                *reinterpret_cast<uint32_t*>(p.U + tile_cd + r * D + c) = pack_bf16(a0, a1);
+            }
         });
     }
     __syncthreads();
@@ -178,7 +183,11 @@ __global__ void __launch_bounds__(256, 1) k_prep(const Params p) {
             *reinterpret_cast<uint4*>(p.Kr + tile_cd + r * D + j * 8) = make_uint4(w[0], w[1], w[2], w[3]);
         }
         float* gTo = p.gT + ((size_t)chunk * p.H + h) * D;
-        for (int d = threadIdx.x; d < D; d += blockDim.x) gTo[d] = G.gTv(d);
+        float* egTo = p.egT + ((size_t)chunk * p.H + h) * D;
+        for (int d = threadIdx.x; d < D; d += blockDim.x) {
+            gTo[d] = G.gTv(d);
+            egTo[d] = __expf(G.gTv(d));
+        }
     }
 }
 

@@ -6,7 +6,7 @@
 // the per-chunk tiles written by the prep kernel; neither depends on the
 // other, so one launch runs both (blockIdx.y selects the role).
 //
-//   role 0, forward  (chunk-start states, saved bf16 per chunk):
+//   role 0, forward  (chunk-start states, saved bf16 per chunk, value-major):
 //       X = W S0 ;  S_C = diag(e^{gT}) S0 + kr^T (U - X)
 //   role 1, backward (state gradient at each chunk end, saved bf16 per chunk;
 //       the FlashQLA dh recurrence, "FlashQLA ... GDN 反向", §三):
@@ -125,7 +125,8 @@ __global__ void __launch_bounds__(256) k_states(const Params p, int role0) {
         frag_foreach(st, m0, n0, [&](int r, int cc, float a0, float a1) {
             const uint32_t w = pack_bf16(a0, a1);
             *reinterpret_cast<uint32_t*>(sS.ptr(r, cc)) = w;
-            *reinterpret_cast<uint32_t*>(dst + (size_t)r * D + col0 + cc) = w;
+            dst[(size_t)(col0 + cc) * D + r] = __float2bfloat16(a0);  // saved value-major [dv][dk]
+            dst[(size_t)(col0 + cc + 1) * D + r] = __float2bfloat16(a1);
         });
         __syncthreads();
 
@@ -184,8 +185,9 @@ static cudaError_t launch_states_t(const Params& p, int role0, int nroles, cudaS
 
 cudaError_t launch_states(const Params& p, bool fwd, bool bwd, cudaStream_t s) {
     if (!fwd && !bwd) return cudaSuccess;
+    if (p.D == 128) return launch_states_tc(p, fwd, bwd, s);
     const int role0 = fwd ? 0 : 1, nroles = (fwd && bwd) ? 2 : 1;
-    return p.D == 128 ? launch_states_t<128>(p, role0, nroles, s) : launch_states_t<64>(p, role0, nroles, s);
+    return launch_states_t<64>(p, role0, nroles, s);
 }
 
 }  // namespace gdr

@@ -1,0 +1,308 @@
+// The two serial chunk recurrences on tcgen05 (D = 128), carried value-major:
+// one CTA per (sequence, head, role) holds the whole transposed state S^T
+// (128 value rows j x 128 key columns d) in fp32 registers of 8 consumer warps
+// (thread = row j, 64 of the 128 columns) through every chunk of its sequence.
+//
+//   role 0, forward (chunk-start states, saved bf16 per chunk):
+//       X^T = S0^T W^T ;  S_C^T = S0^T e^{gT} + (U - X)^T kr
+//   role 1, backward (state gradient at each chunk end, saved bf16 per chunk; the
+//       dh recurrence of "FlashQLA ... GDN 反向", §三, here transposed):
+//       Y^T = dS_C^T kr^T ;  dS0^T = dS_C^T e^{gT} + dO^T (R_hi + R_lo) - Y^T W ;
+//       dh0 = dS0 of the first chunk.
+//
+// Every product has M = 128 (the value rows), so every tensor-memory lane holds a
+// useful row and the element-wise steps spread over all four SM sub-partitions.
+// Per chunk: consumers write bf16 S^T (the saved state, copied out by a TMA
+// store); the MMA warp issues X^T (or Y^T) = S^T [C x D tile]^T; consumers
+// write bf16 (U - X)^T (or -Y^T); the MMA warp issues the update product (role 1
+// also the state-independent dO^T R terms), which consumers add to the decayed
+// state.  A separate TMA warp streams each chunk's tiles (and its e^{gT} row) two
+// chunks ahead and stores the saved states, so that neither issuing thread waits
+// behind the other's instructions.  All waits are bounded; a wait that runs out
+// sets a flag that turns every later wait and issue into a no-op, so all warps
+// still meet every barrier and the CTA ends with its copies drained and its
+// tensor memory released.
+#include "gdr_chunk.cuh"
+#include "gdr_tc.cuh"
+#include "gdr_tma.h"
+
+namespace gdr {
+
+namespace {
+
+constexpr int SD = 128;
+constexpr int TILE = CH * SD * 2;       // one C x D bf16 tile, 16 KB
+constexpr int oEG = 5 * TILE;           // within a stage: e^{gT} row (fp32 [D])
+constexpr int STAGE = 5 * TILE + 1024;  // role 0: W, kr, U^T ; role 1: kr, W, R_hi, R_lo, dO
+constexpr int oBS = 2 * STAGE;          // bf16 S^T   [128 rows j][128 cols d]
+constexpr int oBY = oBS + 2 * TILE;     // bf16 (U - X)^T or -Y^T [128 rows j][64 cols t]
+constexpr int oBar = oBY + TILE;        // full[2], y, z mbarriers; tmem slot; abort flag
+constexpr int SMEM_BYTES = oBar + 64 + 1024;
+constexpr int NCONS = 256, NTHREADS = NCONS + 64;  // 8 consumer warps, the MMA warp, the TMA warp
+constexpr int MMA_WARP = NCONS / 32, TMA_WARP = MMA_WARP + 1;
+constexpr int N_BS_READY = NTHREADS, N_BY_READY = NCONS + 32, N_BS_FREE = NCONS + 32;  // barrier sizes
+constexpr uint32_t R_Y = 0, R_Z0 = 128, R_Z1 = 256;  // tensor-memory columns
+constexpr int BAR_BS_READY = 1, BAR_BY_READY = 2, BAR_BS_FREE = 3;
+
+struct StateMaps {
+    CUtensorMap W, Kr, Ut, R, Rlo, dO, S0, dS;
+};
+
+__device__ __forceinline__ int seq_chunk_begin(const Params& p, int seq) {
+    if (p.chunk_off) return p.chunk_off[seq];
+    return seq * (int)((p.seq_len + CH - 1) / CH);
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(NTHREADS, 1) k_states_tc(const Params p, int role0,
+                                                           const __grid_constant__ StateMaps m) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    const uint32_t sb = smem_u32(smem);
+
+    const int role = role0 + blockIdx.y;
+    const int seq = blockIdx.x / p.H, h = blockIdx.x % p.H;
+    const int cb = seq_chunk_begin(p, seq), ce = seq_chunk_begin(p, seq + 1);
+    const int n = ce - cb;
+    const int64_t bos = p.cu_seqlens ? p.cu_seqlens[seq] : (int64_t)seq * p.seq_len;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + oBar);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 4);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 4) + 1;
+    const uint32_t full0 = smem_u32(bars), mby = smem_u32(bars + 2), mbz = smem_u32(bars + 3);
+
+    if (warp == 0) tc::alloc(smem_u32(tslot), 512);
+    if (tid == 0) {
+        tc::mbar_init(full0, 1);
+        tc::mbar_init(full0 + 8, 1);
+        tc::mbar_init(mby, 1);
+        tc::mbar_init(mbz, 1);
+        *abort_flag = 0;
+    }
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tmem = *tslot;
+
+    auto failed = [&]() { return *abort_flag != 0; };
+    auto wait = [&](uint32_t bar, uint32_t parity) {
+        if (!failed() && !tc::mbar_wait(bar, parity)) {
+            *abort_flag = 1;
+            atomicOr(p.status, ST_MMA_TIMEOUT);
+        }
+    };
+    auto chunk_of = [&](int it) { return role == 0 ? cb + it : ce - 1 - it; };
+    auto full_bar = [&](int it) { return full0 + 8 * (it & 1); };
+    auto full_par = [&](int it) { return (uint32_t)((it >> 1) & 1); };
+
+    if (warp == TMA_WARP) {
+        // ---------------- TMA warp: tile loads two chunks ahead, saved-state stores ----------------
+        int issued = 0;
+        auto issue = [&](int it) {
+            const int c = chunk_of(it);
+            const uint32_t st = sb + (it & 1) * STAGE, bar = full_bar(it);
+            const int row = (c * p.H + h) * CH;
+            tc::mbar_expect_tx(bar, (role == 0 ? 3 : 5) * TILE + SD * 4);
+            if (role == 0) {
+                tc::tma_load_3d(st, &m.W, 0, row, 0, bar);
+                tc::tma_load_3d(st + TILE, &m.Kr, 0, row, 0, bar);
+                tc::tma_load_2d(st + 2 * TILE, &m.Ut, 0, 2 * row, bar);  // U^T: 128 rows x 64 columns
+            } else {
+                tc::tma_load_3d(st, &m.Kr, 0, row, 0, bar);
+                tc::tma_load_3d(st + TILE, &m.W, 0, row, 0, bar);
+                tc::tma_load_3d(st + 2 * TILE, &m.R, 0, row, 0, bar);
+                tc::tma_load_3d(st + 3 * TILE, &m.Rlo, 0, row, 0, bar);
+                // rows past the sequence end are read too: they meet zero rows of R_hi / R_lo
+                const int t0 = (int)(bos + (int64_t)(c - cb) * CH);
+                tc::tma_load_4d(st + 4 * TILE, &m.dO, 0, h, t0, 0, bar);
+            }
+            tc::bulk_load(st + oEG, p.egT + ((size_t)c * p.H + h) * SD, SD * 4, bar);
+            issued = it + 1;
+        };
+        if (lane == 0) {
+            tc::prefetch_map(&m.W);
+            tc::prefetch_map(&m.Kr);
+            tc::prefetch_map(role == 0 ? &m.Ut : &m.R);
+            tc::prefetch_map(role == 0 ? &m.S0 : &m.Rlo);
+            if (role == 1) {
+                tc::prefetch_map(&m.dO);
+                tc::prefetch_map(&m.dS);
+            }
+            if (n > 0) issue(0);
+            if (n > 1) issue(1);
+        }
+        __syncwarp();
+        if (n > 0) tc::named_arrive(BAR_BS_FREE, N_BS_FREE);
+        for (int it = 0; it < n; ++it) {
+            const int c = chunk_of(it);
+            tc::named_sync(BAR_BS_READY, N_BS_READY);
+            if (lane == 0) {
+                if (!failed()) {  // save the state entering this step (S0 of chunk c, or dS_C of chunk c)
+                    tc::tma_store_3d(role == 0 ? &m.S0 : &m.dS, 0, (c * p.H + h) * SD, 0, sb + oBS);
+                    tc::bulk_commit();
+                }
+                tc::bulk_wait_read();  // the state tile may be rewritten
+            }
+            __syncwarp();
+            if (it + 1 < n) tc::named_arrive(BAR_BS_FREE, N_BS_FREE);
+            if (lane == 0) {
+                wait(mbz, it & 1);  // every product reading stage it & 1 has completed
+                if (!failed() && it + 2 < n) issue(it + 2);
+            }
+            __syncwarp();
+        }
+        if (lane == 0) {
+            // the last two loads issued are the newest phases of their barriers (drained on the failure path)
+            for (int i = issued > 2 ? issued - 2 : 0; i < issued; ++i) tc::mbar_wait(full_bar(i), full_par(i));
+            tc::bulk_wait_all();
+        }
+    } else if (warp == MMA_WARP) {
+        // ---------------- MMA warp: every tcgen05.mma is issued by lane 0 ----------------
+        for (int it = 0; it < n; ++it) {
+            const uint32_t st = sb + (it & 1) * STAGE;
+            const uint32_t z = tmem + ((it & 1) ? R_Z1 : R_Z0);
+            tc::named_sync(BAR_BS_READY, N_BS_READY);
+            tc::fence_after();
+            if (lane == 0) {
+                wait(full_bar(it), full_par(it));
+                if (!failed()) {
+                    // X^T = S^T W^T (role 0) or Y^T = dS^T kr^T (role 1): B = the stage's first tile
+                    constexpr uint32_t idy = tc::idesc(128, 64, 0, 0);
+                    for (int k = 0; k < SD; k += 16)
+                        tc::mma(tmem + R_Y, tc::kdesc(sb + oBS, SD, 0, k), tc::kdesc(st, CH, 0, k), idy, k > 0);
+                    tc::commit(mby);
+                    if (role == 1) {  // dO^T R_hi + dO^T R_lo (independent of the state)
+                        constexpr uint32_t idr = tc::idesc(128, 128, 1, 1);
+                        for (int k = 0; k < CH; k += 16)
+                            tc::mma(z, tc::mdesc(st + 4 * TILE, CH, 0, k), tc::mdesc(st + 2 * TILE, CH, 0, k), idr,
+                                    k > 0);
+                        for (int k = 0; k < CH; k += 16)
+                            tc::mma(z, tc::mdesc(st + 4 * TILE, CH, 0, k), tc::mdesc(st + 3 * TILE, CH, 0, k), idr, 1);
+                    }
+                }
+            }
+            __syncwarp();
+            tc::named_sync(BAR_BY_READY, N_BY_READY);
+            tc::fence_after();
+            if (lane == 0 && !failed()) {
+                // role 0: Z = (U - X)^T kr ; role 1: Z += (-Y^T) W   (B = the stage's second tile)
+                constexpr uint32_t idz = tc::idesc(128, 128, 0, 1);
+                for (int k = 0; k < CH; k += 16)
+                    tc::mma(z, tc::kdesc(sb + oBY, SD, 0, k), tc::mdesc(st + TILE, CH, 0, k), idz, role == 1 || k > 0);
+                tc::commit(mbz);
+            }
+            __syncwarp();
+        }
+    } else {
+        // ---------------- consumer warps: the state and the element-wise steps ----------------
+        const int q4 = warp & 3, cg = warp >> 2;
+        const int j = 32 * q4 + lane;  // tensor-memory lane = value row of S^T
+        auto tl = [&](uint32_t col) { return tmem + ((uint32_t)(32 * q4) << 16) + col; };
+        float S[64];  // S^T[j][64 cg + i]
+        {
+            const float* init = role == 0 ? p.h0 : p.dht;
+            const size_t o = ((size_t)seq * p.H + h) * SD * SD + j;
+#pragma unroll
+            for (int i = 0; i < 64; ++i) S[i] = init ? init[o + (size_t)(64 * cg + i) * SD] : 0.f;
+        }
+        for (int it = 0; it < n; ++it) {
+            const unsigned char* stp = smem + (it & 1) * STAGE;
+            const uint32_t z = (it & 1) ? R_Z1 : R_Z0;
+            tc::named_sync(BAR_BS_FREE, N_BS_FREE);
+#pragma unroll
+            for (int jc = 0; jc < 8; ++jc) {
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) w[e] = pack_bf16(S[8 * jc + 2 * e], S[8 * jc + 2 * e + 1]);
+                *reinterpret_cast<uint4*>(smem + oBS + tc::sw_chunk(j, 8 * cg + jc, SD)) =
+                    make_uint4(w[0], w[1], w[2], w[3]);
+            }
+            tc::fence_async_smem();
+            tc::fence_before();
+            tc::named_arrive(BAR_BS_READY, N_BS_READY);
+
+            // this chunk's decay of the 64 columns (read before the stage can be refilled)
+            wait(full_bar(it), full_par(it));
+            float eg[64];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const float4 v = *reinterpret_cast<const float4*>(stp + oEG + 4 * (64 * cg + 4 * i));
+                eg[4 * i] = v.x;
+                eg[4 * i + 1] = v.y;
+                eg[4 * i + 2] = v.z;
+                eg[4 * i + 3] = v.w;
+            }
+            wait(mby, it & 1);
+            tc::fence_after();
+#pragma unroll
+            for (int qq = 0; qq < 2; ++qq) {  // tokens 32 cg + 16 qq .. +15
+                float y[16];
+                tc::ld16(tl(R_Y + 32 * cg + 16 * qq), y);
+                const int jc = 4 * cg + 2 * qq;
+                uint32_t w[8];
+                if (role == 0) {  // (U - X)^T
+                    const uint4 u0 = *reinterpret_cast<const uint4*>(stp + 2 * TILE + tc::sw_chunk(j, jc, SD));
+                    const uint4 u1 = *reinterpret_cast<const uint4*>(stp + 2 * TILE + tc::sw_chunk(j, jc + 1, SD));
+                    const uint32_t uw[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float2 u = unpack_bf16(uw[e]);
+                        w[e] = pack_bf16(u.x - y[2 * e], u.y - y[2 * e + 1]);
+                    }
+                } else {  // -Y^T
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) w[e] = pack_bf16(-y[2 * e], -y[2 * e + 1]);
+                }
+                *reinterpret_cast<uint4*>(smem + oBY + tc::sw_chunk(j, jc, SD)) = make_uint4(w[0], w[1], w[2], w[3]);
+                *reinterpret_cast<uint4*>(smem + oBY + tc::sw_chunk(j, jc + 1, SD)) = make_uint4(w[4], w[5], w[6], w[7]);
+            }
+            tc::fence_async_smem();
+            tc::fence_before();
+            tc::named_arrive(BAR_BY_READY, N_BY_READY);
+
+            wait(mbz, it & 1);
+            tc::fence_after();
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) {
+                float zz[16];
+                tc::ld16(tl(z + 64 * cg + 16 * qq), zz);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) S[16 * qq + e] = fmaf(eg[16 * qq + e], S[16 * qq + e], zz[e]);
+            }
+            tc::fence_before();
+        }
+        if (role == 1) {  // dh0 [D][D] = dS0 of the first chunk (key-major, like dht)
+            const size_t o = ((size_t)seq * p.H + h) * SD * SD + j;
+#pragma unroll
+            for (int i = 0; i < 64; ++i) p.dh0[o + (size_t)(64 * cg + i) * SD] = S[i];
+        }
+    }
+    tc::fence_before();
+    __syncthreads();
+    if (warp == 0) tc::dealloc(tmem, 512);
+}
+
+cudaError_t launch_states_tc(const Params& p, bool fwd, bool bwd, cudaStream_t s) {
+    if (!fwd && !bwd) return cudaSuccess;
+    StateMaps m;
+    const uint64_t rows = (uint64_t)p.max_chunks * p.H * CH;  // C x D tiles
+    const uint64_t srows = (uint64_t)p.max_chunks * p.H * SD;  // D x D states
+    bool ok = encode_blocked_rows_map(&m.W, p.W, rows, CH) && encode_blocked_rows_map(&m.Kr, p.Kr, rows, CH) &&
+              encode_rows_map(&m.Ut, fwd ? p.U : nullptr, srows, CH, SD) &&
+              encode_blocked_rows_map(&m.R, bwd ? p.R : nullptr, rows, CH) &&
+              encode_blocked_rows_map(&m.Rlo, bwd ? p.Rlo : nullptr, rows, CH) &&
+              encode_blocked_tokens_map(&m.dO, bwd ? p.dO : nullptr, (uint64_t)p.T_total, p.H) &&
+              encode_blocked_rows_map(&m.S0, fwd ? p.S0 : nullptr, srows, SD) &&
+              encode_blocked_rows_map(&m.dS, bwd ? p.dS : nullptr, srows, SD);
+    if (!ok) return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(k_states_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    const int role0 = fwd ? 0 : 1, nroles = (fwd && bwd) ? 2 : 1;
+    dim3 grid(p.N * p.H, nroles);
+    k_states_tc<<<grid, NTHREADS, SMEM_BYTES, s>>>(p, role0, m);
+    return cudaGetLastError();
+}
+
+}  // namespace gdr

@@ -80,7 +80,9 @@ typedef struct {
 size_t gdr_workspace_bytes(const gdr_shape* shape);
 
 /* Bytes of the per-chunk state buffer written by gdr_fwd_states / kda_fwd_states:
- * the bf16 chunk-start state of every 64-token chunk and head. */
+ * the bf16 chunk-start state of every 64-token chunk and head, stored value-major
+ * ([chunk][head][dv][dk], i.e. S^T, the layout the tensor-core products read), with
+ * chunks numbered sequence after sequence. */
 size_t gdr_states_bytes(const gdr_shape* shape);
 
 /* Forward chunk states for GDN (the "forward workspace" of the FlashKDA

@@ -43,7 +43,7 @@ def test_workspace_sizes(L):
     chunks = 512
     assert gdr.states_bytes(sh) == chunks * 16 * 128 * 128 * 2
     ws = gdr.workspace_bytes(sh)
-    tiles = chunks * 16 * (5 * 64 * 128 * 2 + 64 * 64 * 2 + 128 * 4 + 2 * 128 * 128 * 2)
+    tiles = chunks * 16 * (5 * 64 * 128 * 2 + 64 * 64 * 2 + 2 * 128 * 4 + 2 * 128 * 128 * 2)
     assert tiles <= ws <= tiles + 64 * 256
     # varlen bound: sum ceil(len/64) <= (T + 63 N) / 64
     fake_cu = ctypes.c_void_p(256)
