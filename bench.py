@@ -245,16 +245,20 @@ def main_gpu(args):
     launches = sum(n for _, n in prof.values())
 
     # per-variant step times (informational, separate short loops)
-    def time_loop(fn, n=max(3, args.steps // 2)):
+    per_variant = {}
+
+    def time_loop(name, fn, n=max(3, args.steps // 2)):
         torch.cuda.synchronize()
+        api.profile_begin(8 * n)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         for _ in range(n):
             fn()
         b.record(stream)
         torch.cuda.synchronize()
+        per_variant[name] = {k: round(v[0] / n, 4) for k, v in api.profile_end().items() if v[1]}
         return a.elapsed_time(b) / n
-    ms_g, ms_k = time_loop(step_g), time_loop(step_k)
+    ms_g, ms_k = time_loop("gdn", step_g), time_loop("kda", step_k)
 
     # ---- end to end: pinned host inputs -> device -> backward -> host gradients ----
     def pinned(x):
@@ -336,6 +340,7 @@ def main_gpu(args):
                    "l2": "inputs larger than L2 (no flush)", "parallelism": "replicas" if world > 1 else "1 GPU"},
         "roofline": roof,
         "kernels_ms_per_step": {k: v[0] / args.steps for k, v in prof.items()},
+        "kernels_ms_per_variant": per_variant,
         "gpu_launches": launches,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms},

@@ -29,32 +29,50 @@ struct Gates {
 };
 
 // Computes gc, gT and ref for one (chunk, head).  Rows >= len have g = 0.
-// Must be called by every thread of the block (it synchronises).
-template <int D, bool KDA>
+// Must be called by every thread of the block (it synchronises); NT = blockDim.x.
+template <int D, bool KDA, int NT = 256>
 __device__ void load_gates(const Params& p, const ChunkInfo& ci, int h, const Gates<D, KDA>& G,
                            bool flag_range) {
     if constexpr (KDA) {
-        // per-element log gates (all threads, coalesced), then one thread per
-        // channel forms the inclusive cumsum in shared memory
+        // thread = (channel d, segment of RS rows): the raw gates of its rows come from
+        // global memory in one batch of independent loads, g = -e^{A_log} softplus(raw +
+        // dt_bias) and the inclusive scan run in registers, then the earlier segments'
+        // totals (the last row of each segment's local scan) are added as a prefix
+        constexpr int NSEG = NT / D, RS = CH / NSEG;
+        static_assert(NSEG * D == NT && NSEG * RS == CH, "thread count must tile the C x D gate block");
         const float a = expf(p.A_log[h]);
-        for (int i = threadIdx.x; i < CH * D; i += blockDim.x) {
-            const int r = i / D, d = i % D;
-            float gv = 0.f;
-            if (r < ci.len) gv = -a * softplus_f(bf2f(p.g_raw[((ci.t0 + r) * p.H + h) * D + d]) + p.dt_bias[h * D + d]);
-            G.gc[r * G.LDG + d] = gv;
+        const int d = threadIdx.x % D, sg = threadIdx.x / D;
+        const float bias = p.dt_bias[h * D + d];
+        float v[RS];
+#pragma unroll
+        for (int i = 0; i < RS; ++i) {
+            const int r = sg * RS + i;
+            v[i] = r < ci.len ? bf2f(p.g_raw[((ci.t0 + r) * p.H + h) * D + d]) : 0.f;
         }
+        float acc = 0.f;
+#pragma unroll
+        for (int i = 0; i < RS; ++i) {
+            if (sg * RS + i < ci.len) acc += -a * softplus_f(v[i] + bias);
+            v[i] = acc;
+        }
+        if (sg < NSEG - 1) G.gc[(sg * RS + RS - 1) * G.LDG + d] = acc;
         __syncthreads();
-        for (int d = threadIdx.x; d < D; d += blockDim.x) {
-            float acc = 0.f, mx = -3.0e38f, mn = 3.0e38f;
-#pragma unroll 8
+        float pre = 0.f;
+        for (int s2 = 0; s2 < sg; ++s2) pre += G.gc[(s2 * RS + RS - 1) * G.LDG + d];
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < RS; ++i) G.gc[(sg * RS + i) * G.LDG + d] = v[i] + pre;
+        __syncthreads();
+        for (int dd = threadIdx.x; dd < D; dd += NT) {
+            float mx = -3.0e38f, mn = 3.0e38f;
+#pragma unroll 16
             for (int r = 0; r < CH; ++r) {
-                acc += G.gc[r * G.LDG + d];
-                G.gc[r * G.LDG + d] = acc;
-                mx = fmaxf(mx, acc);
-                mn = fminf(mn, acc);
+                const float x = G.gc[r * G.LDG + dd];
+                mx = fmaxf(mx, x);
+                mn = fminf(mn, x);
             }
-            G.gT[d] = acc;
-            G.ref[d] = 0.5f * (mx + mn);
+            G.gT[dd] = G.gc[(CH - 1) * G.LDG + dd];
+            G.ref[dd] = 0.5f * (mx + mn);
             if (flag_range && (0.5f * (mx - mn) > 80.f || mx > 80.f)) atomicOr(p.status, ST_GATE_RANGE);
         }
     } else {
