@@ -20,17 +20,25 @@
 
 namespace gdr {
 
+// For GDN, q is not kept in shared memory (it is read from global memory, L2-resident,
+// where needed) and for D = 128 the fp32 inversion scratch lives on the work tiles X1..X3,
+// which are dead between the A / P products and the W / U operands: the D = 128 GDN kernel
+// fits two CTAs per SM.  KDA's per-channel gates keep it at one CTA per SM, so it keeps q
+// in shared memory.
 template <int D, bool KDA>
 struct PrepSmem {
     static constexpr int ROWB = 2 * D;
     static constexpr int TCD = CH * ROWB;   // C x D bf16 tile
     static constexpr int TCC = CH * 128;    // C x C bf16 tile
     static constexpr int LDF = 65;
-    static constexpr int oK = 0, oQ = oK + TCD, oV = oQ + TCD, oX1 = oV + TCD, oX2 = oX1 + TCD,
-                         oX3 = oX2 + TCD, oT = oX3 + TCD, oP = oT + TCC, oA = oP + TCC,
-                         oTf = oA + CH * LDF * 4, oTmp = oTf + CH * LDF * 4, oG = oTmp + 768 * 4,
-                         oSmall = oG + Gates<D, KDA>::floats() * 4,
-                         bytes = oSmall + 3 * CH * 4;
+    static constexpr int SCRATCH = 2 * CH * LDF * 4 + 768 * 4;  // fp32 A and T, inversion temporaries
+    static constexpr bool ALIAS = 3 * TCD >= SCRATCH;             // D = 128: on X1..X3
+    static constexpr bool QS = KDA;  // q tile in shared memory
+    static constexpr int oK = 0, oQ = oK + TCD, oV = oQ + (QS ? TCD : 0), oX1 = oV + TCD, oX2 = oX1 + TCD,
+                         oX3 = oX2 + TCD,
+                         oT = oX3 + TCD, oP = oT + TCC, oScr = oP + TCC, oG = oScr + (ALIAS ? 0 : SCRATCH),
+                         oSmall = oG + Gates<D, KDA>::floats() * 4, bytes = oSmall + 3 * CH * 4;
+    static constexpr int oA = ALIAS ? oX1 : oScr, oTf = oA + CH * LDF * 4, oTmp = oTf + CH * LDF * 4;
 };
 
 template <int D, bool KDA>
@@ -64,37 +72,43 @@ __global__ void __launch_bounds__(256, 1) k_prep(const Params p) {
     const size_t tile_cd = ((size_t)chunk * p.H + h) * CH * D;
     const size_t tile_cc = ((size_t)chunk * p.H + h) * CH * CH;
 
-    async_load_rows<D>(sQ, p.q, p, ci, h);
+    if (SM::QS) async_load_rows<D>(sQ, p.q, p, ci, h);
     async_load_rows<D>(sK, p.k, p, ci, h);
     async_load_rows<D>(sV, p.v, p, ci, h);
     cp_async_commit();
     load_gates<D, KDA>(p, ci, h, G, true);
     load_beta(p, ci, h, sBeta);
+    if (!SM::QS) row_inv_norms_global<D>(p.q, p, ci, h, sInvQ);
     cp_async_wait<0>();
     __syncthreads();
 
-    row_inv_norms_smem<D>(sQ, sInvQ);
+    if (SM::QS) row_inv_norms_smem<D>(sQ, sInvQ);
     row_inv_norms_smem<D>(sK, sInvK);
     __syncthreads();
 
     build_tile<F_KDP, D, KDA, false>(sX1, sK, nullptr, p, ci, h, G, sInvK, nullptr, 1.f);
     build_tile<F_KIP, D, KDA, false>(sX2, sK, nullptr, p, ci, h, G, sInvK, nullptr, 1.f);
-    build_tile<F_KDP, D, KDA, false>(sX3, sQ, nullptr, p, ci, h, G, sInvQ, nullptr, p.scale);
+    if (SM::QS)
+        build_tile<F_KDP, D, KDA, false>(sX3, sQ, nullptr, p, ci, h, G, sInvQ, nullptr, p.scale);
+    else
+        build_tile<F_KDP, D, KDA, true>(sX3, sX3, p.q, p, ci, h, G, sInvQ, nullptr, p.scale);
     __syncthreads();
 
-    // A = strict_lower(diag(beta) kd' ki'^T) (fp32), P = lower(qd' ki'^T) (bf16)
+    // A = strict_lower(diag(beta) kd' ki'^T) (fp32), P = lower(qd' ki'^T) (bf16); A is written
+    // over X1..X3, so both products finish in every warp before it is stored
     {
         const int m0 = 16 * (warp & 3), n0 = 32 * (warp >> 2);
-        float acc[1][4][4];
+        float acc[1][4][4], accp[1][4][4];
         zero_acc(acc);
+        zero_acc(accp);
         warp_mma<1, 4, A_ROW, B_COL>(acc, sX1, sX2, m0, n0, 0, D);
+        warp_mma<1, 4, A_ROW, B_COL>(accp, sX3, sX2, m0, n0, 0, D);
+        __syncthreads();
         frag_foreach(acc, m0, n0, [&](int r, int c, float a0, float a1) {
             sA[r * SM::LDF + c] = c < r ? sBeta[r] * a0 : 0.f;
             sA[r * SM::LDF + c + 1] = c + 1 < r ? sBeta[r] * a1 : 0.f;
         });
-        zero_acc(acc);
-        warp_mma<1, 4, A_ROW, B_COL>(acc, sX3, sX2, m0, n0, 0, D);
-        frag_foreach(acc, m0, n0, [&](int r, int c, float a0, float a1) {
+        frag_foreach(accp, m0, n0, [&](int r, int c, float a0, float a1) {
             *reinterpret_cast<uint32_t*>(sP.ptr(r, c)) = pack_bf16(c <= r ? a0 : 0.f, c + 1 <= r ? a1 : 0.f);
         });
     }
@@ -107,7 +121,8 @@ __global__ void __launch_bounds__(256, 1) k_prep(const Params p) {
         *reinterpret_cast<uint32_t*>(sT.ptr(r, c)) = w;
         *reinterpret_cast<uint32_t*>(p.Tm + tile_cc + r * CH + c) = w;
     }
-    // beta kd -> X1, beta V -> X2 (kd' and ki' are no longer needed)
+    __syncthreads();  // the inversion scratch on X1..X3 is dead
+    // beta kd -> X1, beta V -> X2
     build_tile<F_KD, D, KDA, false>(sX1, sK, nullptr, p, ci, h, G, sInvK, sBeta, 1.f);
     {
         constexpr int CPR = D / 8;
@@ -155,7 +170,10 @@ __global__ void __launch_bounds__(256, 1) k_prep(const Params p) {
         zero_acc(acc);
         warp_mma<1, NTD, A_ROW, B_ROW>(acc, sP, sX3, m0, n0, 0, CH);
         frag_foreach(acc, m0, n0, [&](int r, int c, float a0, float a1) {
-            const float2 q = unpack_bf16(*reinterpret_cast<const uint32_t*>(sQ.ptr(r, c)));
+            const float2 q =
+                SM::QS ? unpack_bf16(*reinterpret_cast<const uint32_t*>(sQ.ptr(r, c)))
+                : r < ci.len ? unpack_bf16(*reinterpret_cast<const uint32_t*>(p.q + ((ci.t0 + r) * p.H + h) * D + c))
+                             : make_float2(0.f, 0.f);
             const float s = p.scale * sInvQ[r];
             const float qd0 = q.x * s * gate_factor<F_KD>(G, r, c);
             const float qd1 = q.y * s * gate_factor<F_KD>(G, r, c + 1);
@@ -195,6 +213,8 @@ template <int D, bool KDA>
 static cudaError_t launch_prep_t(const Params& p, cudaStream_t s) {
     const int bytes = PrepSmem<D, KDA>::bytes;
     cudaError_t e = cudaFuncSetAttribute(k_prep<D, KDA>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess)  // let two CTAs share an SM where their shared memory allows it
+        e = cudaFuncSetAttribute(k_prep<D, KDA>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return e;
     dim3 grid(p.max_chunks, p.H);
     k_prep<D, KDA><<<grid, 256, bytes, s>>>(p);
