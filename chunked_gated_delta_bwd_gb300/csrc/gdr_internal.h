@@ -45,6 +45,6 @@ cudaError_t launch_prep(const Params& p, cudaStream_t s);
 cudaError_t launch_states(const Params& p, bool fwd, bool bwd, cudaStream_t s);
 cudaError_t launch_states_tc(const Params& p, bool fwd, bool bwd, cudaStream_t s);  // D = 128, tcgen05 + TMA
 cudaError_t launch_main(const Params& p, cudaStream_t s);
-cudaError_t launch_main_tc(const Params& p, cudaStream_t s);  // GDN, D = 128, tcgen05
+cudaError_t launch_main_tc2(const Params& p, cudaStream_t s);  // GDN and KDA, D = 128, tcgen05 + TMA
 
 }  // namespace gdr

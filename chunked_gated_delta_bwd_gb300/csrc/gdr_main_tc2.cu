@@ -1,0 +1,860 @@
+// Chunk-parallel main backward on tcgen05 for D = 128, GDN and KDA: one CTA (16
+// warps) per (chunk, head).  Same algebra as the warp-level kernel in gdr_main.cu;
+// every product is a 128-row tcgen05 MMA into tensor memory, written feature-major
+// where the natural output is C x D: the accumulator holds X^T (lane = key channel d
+// or value channel j, column = token row r), so a thread owns one channel for 16
+// rows.  The raw q and k rows and (KDA) the per-channel cumulative gate gc are staged
+// in tensor memory in that layout once, and every derived tile (kd', ki', qd', kd,
+// kr) is built from registers, channel-major ([d][r]), with 16-byte stores.
+//
+// With S0 = chunk-start state, dS = state gradient at the chunk end (both value-major
+// [j][d]) and [X; Y] a 128-row operand stacked from two 64-row tiles:
+//   G1  [A_raw; P]   = [kd'; qd'] ki'^T                 G7  Z^T    = S0 dY^T
+//   G2  X^T          = S0^T kd^T                        G8  dkr^T  = dS u^T
+//   G3  dqd^T        = S0 dO^T                          G9  [dP; dA] = [dO; dY] u^T
+//   G4  u^T          = (beta E)^T T^T                   G10 [dqd', dkd']^T = ki'^T [dP; beta dA]^T
+//   G5  du^T         = dO^T P + dS^T kr^T               G11 dki'^T = qd'^T dP + kd'^T (beta dA)
+//   G6  dY^T         = du^T T
+// followed by the elementwise assembly of "FlashKDA之backward（K1）" (§3.2-§3.3, §5).
+//
+// KDA runs the precise mode of the warp-level kernel: the operands that carry the
+// per-channel gate gradient (beta E, u, dP and beta dA, and ki', qd', kd' of G10 / G11)
+// are bf16 pairs hi + lo and each of those products is hi*hi + lo*hi + hi*lo, because
+// dA_log and ddt_bias sum dg over every token of a head.
+#include "gdr_chunk.cuh"
+#include "gdr_tc.cuh"
+#include "gdr_tma.h"
+
+namespace gdr {
+
+namespace {
+
+constexpr int MD = 128;
+constexpr int TILE = CH * MD * 2;  // 16 KB: a C x D token-major or a D x C channel-major bf16 tile
+// shared-memory map (bytes from the 1024-aligned base); later tenants after the arrows
+constexpr int oK = 0;           // k (token-major)     -> (KDA) beta E lo  -> (KDA) qd' lo
+constexpr int oV = 16384;       // v -> beta E (token-major)
+constexpr int oDOY = 32768;     // [dO; dY] token-major, 128 rows
+constexpr int oS0 = 65536;      // S0 [j][d]          -> kd' [d][r] (+ lo at +16 KB)
+constexpr int oDS = 98304;      // dS [j][d]          -> [dP; beta dA] [m][s] (+ lo at +16 KB)
+constexpr int oT = 131072;      // T  [r][s]
+constexpr int oA = 139264;      // beta A_raw, strict lower [r][s]
+constexpr int oP = 147456;      // P, lower [r][s]
+constexpr int oW0 = 155648;     // kd' [d][r] (G1, A block 0) -> kd [d][r] -> (KDA) u^T lo -> ki' [d][r]
+constexpr int oW1 = 172032;     // qd' [d][r] (G1, A block 1) -> u^T [j][r] -> (KDA) ki' lo
+constexpr int oW2 = 188416;     // q (token-major) -> ki' [d][r] -> kr [d][r] -> du^T -> qd' [d][r]
+constexpr int oSmall = 204800;
+// small arrays (floats)
+constexpr int NCOL = 16;  // rows per thread (16 warps: 4 lane quarters x 4 row quarters)
+constexpr int nInvQ = 64, nInvK = 64, nBeta = 64, nFac = 256, nGate = 128, nRef = 128, nGT = 128,
+              nScan = 512, nDgTs = 128, nDgTp = 512, nDbP = 64, nDbA = 256, nRow = 256 * 3, nMisc = 64;
+constexpr int SMALL_FLOATS =
+    nInvQ + nInvK + nBeta + nFac + nGate + nRef + nGT + nScan + nDgTs + nDgTp + nDbP + nDbA + nRow + nMisc;
+constexpr int SMEM_BYTES = oSmall + SMALL_FLOATS * 4 + 64 + 1024;  // + mbarriers / tmem slot + alignment
+// tensor-memory columns
+constexpr uint32_t R_A = 0, R_B = 128, R_C = 192, R_D = 256, R_Q = 320, R_K = 384, R_G = 448;
+
+struct MainMaps {
+    CUtensorMap q, k, v, dO, S0, dS, T;
+};
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+// Sum over the warp of each of 32 per-lane values: lane l returns the total of v[l]
+// (recursive halving: 31 exchanges instead of 32 x 5).
+__device__ __forceinline__ float warp_transpose_sum32(float (&v)[32]) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < o; ++i) {
+            const float send = up ? v[i] : v[i + o];
+            const float keep = up ? v[i + o] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+    }
+    return v[0];
+}
+// Same for 16 values: lanes l and l ^ 1 return the total of v[l >> 1].
+__device__ __forceinline__ float warp_transpose_sum16(float (&v)[16]) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 16; o >= 2; o >>= 1) {
+        const int n = o >> 1;  // values kept after this step
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < n; ++i) {
+            const float send = up ? v[i] : v[i + n];
+            const float keep = up ? v[i + n] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+    }
+    return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
+}
+
+}  // namespace
+
+template <bool KDA>
+__global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __grid_constant__ MainMaps m) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    const uint32_t sb = smem_u32(smem);
+
+    const int chunk = blockIdx.x, h = blockIdx.y;
+    ChunkInfo ci;
+    if (!lookup_chunk(chunk, p.N, p.chunk_off, p.cu_seqlens, p.seq_len, ci)) return;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int q4 = warp & 3, hc = warp >> 2;  // tensor-memory lane quarter, row quarter
+    const int L = 32 * q4 + lane;             // this thread's lane: a channel, or a stacked row
+    const int c0 = NCOL * hc;                 // first of this thread's 16 rows
+
+    unsigned char *sK = smem + oK, *sV = smem + oV, *sDOY = smem + oDOY, *sS0 = smem + oS0, *sDS = smem + oDS,
+                  *sA = smem + oA, *sP = smem + oP, *sW0 = smem + oW0, *sW1 = smem + oW1, *sW2 = smem + oW2;
+    float* fsm = reinterpret_cast<float*>(smem + oSmall);
+    float* sInvQ = fsm;
+    float* sInvK = sInvQ + nInvQ;
+    float* sBeta = sInvK + nInvK;
+    float* sFac = sBeta + nBeta;     // GDN [4][64]: e^{gc}, e^{gc-ref}, e^{ref-gc}, e^{gT-gc}
+    float* sGate = sFac + nFac;      // GDN gc[64], ref, gT
+    float* sRef = sGate + nGate;     // KDA ref[d]
+    float* sGT = sRef + nRef;        // KDA gT[d]
+    float* sScan = sGT + nGT;        // KDA [4][128] per-quarter gate totals / extrema / suffix totals
+    float* sDgTs = sScan + nScan;    // [128] state part of dgT
+    float* sDgTp = sDgTs + nDgTs;    // [4][128] kr part of dgT per row quarter
+    float* sDbP = sDgTp + nDgTp;     // [64] <dY, beta E> per row
+    float* sDbA = sDbP + nDbP;       // [4][64] rowsum(dA . A) per column quarter
+    float* sRow = sDbA + nDbA;       // [3][4][64] row reductions (and KDA partials)
+    float* sMisc = sRow + nRow;      // [64]
+    uint64_t* mbars = reinterpret_cast<uint64_t*>(sMisc + nMisc);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbars + 2);
+    const uint32_t mb = smem_u32(mbars), mload = smem_u32(mbars + 1);
+
+    Gates<MD, false> G;  // GDN scalar gates
+    G.gc = sGate;
+    G.ref = sGate + CH;
+    G.gT = sGate + CH + 1;
+
+    const int row_cd = (chunk * p.H + h) * CH, row_dd = (chunk * p.H + h) * MD;
+
+    // ---- set-up: tensor memory, barriers, TMA loads of every operand tile ----------
+    if (warp == 0) tc::alloc(smem_u32(tslot), 512);
+    if (tid == 0) {
+        tc::mbar_init(mb, 1);
+        tc::mbar_init(mload, 1);
+        tc::mbar_expect_tx(mload, 4 * TILE + 2 * 2 * TILE + CH * CH * 2);
+        const int t0 = (int)ci.t0;
+        tc::tma_load_4d(sb + oK, &m.k, 0, h, t0, 0, mload);
+        tc::tma_load_4d(sb + oV, &m.v, 0, h, t0, 0, mload);
+        tc::tma_load_4d(sb + oW2, &m.q, 0, h, t0, 0, mload);
+        tc::tma_load_3d(sb + oDOY, &m.dO, 0, h, t0, mload);  // rows 0..63 of a 128-row tile
+        tc::tma_load_3d(sb + oDOY + 128 * 128, &m.dO, 64, h, t0, mload);
+        tc::tma_load_3d(sb + oS0, &m.S0, 0, row_dd, 0, mload);
+        tc::tma_load_3d(sb + oDS, &m.dS, 0, row_dd, 0, mload);
+        tc::tma_load_2d(sb + oT, &m.T, 0, row_cd, mload);
+    }
+    if constexpr (!KDA) load_gates<MD, false, 512>(p, ci, h, G, false);
+    load_beta(p, ci, h, sBeta);
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tmem = *tslot;
+    uint32_t phase = 0;
+    auto sync_all = [&]() {  // make smem writes visible to the tensor cores and order TMEM use
+        tc::fence_async_smem();
+        tc::fence_before();
+        __syncthreads();
+        tc::fence_after();
+    };
+    // Waits for the last commit.  If the tensor cores do not answer within the
+    // bounded spin, every thread learns it from the vote, the status word records
+    // it, the tensor memory is released and the CTA returns.
+    auto wait_mma = [&]() -> bool {
+        const bool ok = tc::mbar_wait(mb, phase);
+        phase ^= 1;
+        tc::fence_after();
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) atomicOr(p.status, ST_MMA_TIMEOUT);
+            tc::fence_before();
+            __syncthreads();
+            if (warp == 0) tc::dealloc(tmem, 512);
+            return false;
+        }
+        return true;
+    };
+    auto tl = [&](uint32_t col) { return tmem + ((uint32_t)(32 * q4) << 16) + col; };
+    auto rows16 = [&](const float* a, float (&o)[16]) {  // a[c0 .. c0+15]
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float4 v = *reinterpret_cast<const float4*>(a + c0 + 4 * i);
+            o[4 * i] = v.x;
+            o[4 * i + 1] = v.y;
+            o[4 * i + 2] = v.z;
+            o[4 * i + 3] = v.w;
+        }
+    };
+    // row L of a channel-major [128][64] tile, columns c0 .. c0+15, from 16 fp32 values
+    auto store_cm = [&](unsigned char* tile, const float (&v)[16]) {
+        uint32_t w[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) w[e] = pack_bf16(v[2 * e], v[2 * e + 1]);
+        *reinterpret_cast<uint4*>(tile + tc::sw_chunk(L, c0 >> 3, 128)) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(tile + tc::sw_chunk(L, (c0 >> 3) + 1, 128)) = make_uint4(w[4], w[5], w[6], w[7]);
+    };
+    // the same as a bf16 pair: hi to `tile`, the residual v - hi to `lo`
+    auto store_cm_pair = [&](unsigned char* tile, unsigned char* lo, const float (&v)[16]) {
+        uint32_t w[8], wl[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            w[e] = pack_bf16(v[2 * e], v[2 * e + 1]);
+            const float2 hf = unpack_bf16(w[e]);
+            wl[e] = pack_bf16(v[2 * e] - hf.x, v[2 * e + 1] - hf.y);
+        }
+        *reinterpret_cast<uint4*>(tile + tc::sw_chunk(L, c0 >> 3, 128)) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(tile + tc::sw_chunk(L, (c0 >> 3) + 1, 128)) = make_uint4(w[4], w[5], w[6], w[7]);
+        *reinterpret_cast<uint4*>(lo + tc::sw_chunk(L, c0 >> 3, 128)) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+        *reinterpret_cast<uint4*>(lo + tc::sw_chunk(L, (c0 >> 3) + 1, 128)) = make_uint4(wl[4], wl[5], wl[6], wl[7]);
+    };
+
+    // KDA: per-channel log gates of this thread's channel and rows, scanned across the four
+    // row quarters, staged in tensor memory (lane = channel, column = row)
+    float refL = 0.f, gTL = 0.f;
+    if constexpr (KDA) {
+        const float a = expf(p.A_log[h]);
+        const float bias = p.dt_bias[h * MD + L];
+        float g[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int r = c0 + i;
+            g[i] = r < ci.len ? bf2f(p.g_raw[((ci.t0 + r) * p.H + h) * MD + L]) : 0.f;
+        }
+        float acc = 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            if (c0 + i < ci.len) acc += -a * softplus_f(g[i] + bias);
+            g[i] = acc;
+        }
+        sScan[hc * MD + L] = acc;  // this quarter's total
+        __syncthreads();
+        float pre = 0.f, tot = 0.f;
+#pragma unroll
+        for (int h2 = 0; h2 < 4; ++h2) {
+            const float t = sScan[h2 * MD + L];
+            if (h2 < hc) pre += t;
+            tot += t;
+        }
+        float mx = -3.0e38f, mn = 3.0e38f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            g[i] += pre;
+            mx = fmaxf(mx, g[i]);
+            mn = fminf(mn, g[i]);
+        }
+        tc::st16(tl(R_G + c0), g);
+        __syncthreads();  // totals read
+        sScan[hc * MD + L] = mx;
+        sRow[hc * MD + L] = mn;
+        __syncthreads();
+        if (hc == 0) {
+            float M = sScan[L], N = sRow[L];
+#pragma unroll
+            for (int h2 = 1; h2 < 4; ++h2) {
+                M = fmaxf(M, sScan[h2 * MD + L]);
+                N = fminf(N, sRow[h2 * MD + L]);
+            }
+            sRef[L] = 0.5f * (M + N);
+            sGT[L] = tot;
+        }
+    }
+
+    // wait for the operand tiles; rows past the chunk's end read as zero
+    {
+        const bool ok = tc::mbar_wait(mload, 0);
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) atomicOr(p.status, ST_MMA_TIMEOUT);
+            tc::fence_before();
+            __syncthreads();
+            if (warp == 0) tc::dealloc(tmem, 512);
+            return;
+        }
+    }
+    if (ci.len < CH) {
+        const int nz = (CH - ci.len) * 16;  // 16-byte chunks per 64-row tile (2 blocks x 8)
+        for (int i = tid; i < 4 * nz; i += 512) {
+            const int t = i / nz, rem = i % nz, r = ci.len + rem / 16, jc = rem % 16;
+            unsigned char* base = t == 0 ? sK : t == 1 ? sV : t == 2 ? sW2 : sDOY;
+            const int rows = t == 3 ? 128 : 64;
+            *reinterpret_cast<uint4*>(base + tc::sw_chunk(r, jc, rows)) = make_uint4(0, 0, 0, 0);
+        }
+    }
+    __syncthreads();
+    if constexpr (KDA) {
+        refL = sRef[L];
+        gTL = sGT[L];
+    }
+
+    // inverse row norms of q (from W2) and k, 4 threads per row; GDN gate factor table;
+    // dgT state part (column sums of the value-major dS . S0)
+    {
+        const int r = (tid >> 2) & 63, part = tid & 3;
+        const unsigned char* src = tid < 256 ? sW2 : sK;
+        float s = 0.f;
+        for (int j = part * 4; j < part * 4 + 4; ++j) {
+            const uint4 v = *reinterpret_cast<const uint4*>(src + tc::sw_chunk(r, j, 64));
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 f = unpack_bf16(w[e]);
+                s += f.x * f.x + f.y * f.y;
+            }
+        }
+        s += __shfl_xor_sync(0xffffffffu, s, 1);
+        s += __shfl_xor_sync(0xffffffffu, s, 2);
+        if (part == 0) (tid < 256 ? sInvQ : sInvK)[r] = rsqrtf(s + 1e-6f);
+    }
+    if constexpr (!KDA) {
+        for (int r = tid; r < CH; r += 512) {
+            sFac[0 * CH + r] = gate_factor<F_KD>(G, r, 0);
+            sFac[1 * CH + r] = gate_factor<F_KDP>(G, r, 0);
+            sFac[2 * CH + r] = gate_factor<F_KIP>(G, r, 0);
+            sFac[3 * CH + r] = gate_factor<F_KR>(G, r, 0);
+        }
+    }
+    {
+        const int cp = tid >> 3, g = tid & 7;  // column pair, row group
+        float s0 = 0.f, s1 = 0.f;
+        for (int j = g; j < MD; j += 8) {
+            const float2 a = unpack_bf16(*reinterpret_cast<const uint32_t*>(sS0 + tc::sw_off(j, 2 * cp, 128)));
+            const float2 b = unpack_bf16(*reinterpret_cast<const uint32_t*>(sDS + tc::sw_off(j, 2 * cp, 128)));
+            s0 += a.x * b.x;
+            s1 += a.y * b.y;
+        }
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) {
+            s0 += __shfl_xor_sync(0xffffffffu, s0, o);
+            s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+        }
+        if (g == 0) {
+            if constexpr (KDA) {
+                sDgTs[2 * cp] = s0 * __expf(sGT[2 * cp]);
+                sDgTs[2 * cp + 1] = s1 * __expf(sGT[2 * cp + 1]);
+            } else {
+                const float eg = __expf(G.gTv(0));
+                sDgTs[2 * cp] = s0 * eg;
+                sDgTs[2 * cp + 1] = s1 * eg;
+            }
+        }
+    }
+    // raw q and k of this thread's channel and rows into tensor memory
+    {
+        const int lch = (L & 63) >> 3, lsub = (L & 7) << 1;
+        float qs[NCOL], ks[NCOL];
+#pragma unroll
+        for (int i = 0; i < NCOL; ++i) {
+            const uint32_t off = (uint32_t)((L >> 6) * 64 * 128 + (c0 + i) * 128 + ((lch ^ (i & 7)) << 4) + lsub);
+            qs[i] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(sW2 + off));
+            ks[i] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(sK + off));
+        }
+        tc::st16(tl(R_Q + c0), qs);
+        tc::st16(tl(R_K + c0), ks);
+    }
+    __syncthreads();  // norms, factors and the q tile reads are done
+
+    // per-element factors of this thread's channel and rows
+    auto factors = [&](int kind, float (&f)[16]) {
+        if constexpr (KDA) {
+            float g[16];
+            tc::ld16(tl(R_G + c0), g);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const float e = kind == F_KD ? g[i] : kind == F_KDP ? g[i] - refL : kind == F_KIP ? refL - g[i] : gTL - g[i];
+                f[i] = __expf(e);
+            }
+        } else {
+            rows16(sFac + kind * CH, f);
+        }
+    };
+    // raw q (or k) of this thread's channel and rows, and the rows' inverse norms
+    auto load_x = [&](bool isq, float (&x)[16], float (&inv)[16]) {
+        tc::ld16(tl((isq ? R_Q : R_K) + c0), x);
+        rows16(isq ? sInvQ : sInvK, inv);
+    };
+    // a derived tile, channel-major: bf16(x * m_r * f), m_r = inv_r * mul (hi + lo if lo)
+    auto build = [&](unsigned char* tile, unsigned char* lo, bool isq, float mul, int kind) {
+        float f[16], x[16], inv[16];
+        factors(kind, f);
+        load_x(isq, x, inv);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) x[i] = x[i] * derived_m(inv[i], mul, 1.f) * f[i];
+        if (lo)
+            store_cm_pair(tile, lo, x);
+        else
+            store_cm(tile, x);
+    };
+
+    // per-thread accumulators (channel L, rows c0 .. c0+15)
+    float dQn[NCOL], dKn[NCOL], dGc[NCOL], v[NCOL];
+#pragma unroll
+    for (int i = 0; i < NCOL; ++i) dQn[i] = dKn[i] = dGc[i] = 0.f;
+    // byte offset of element (row c0 + i, column L) in a token-major SW128 tile with `rows` rows
+    const int lch = (L & 63) >> 3, lsub = (L & 7) << 1;
+    auto tok = [&](int rows, int i) -> uint32_t {
+        return (uint32_t)((L >> 6) * rows * 128 + (c0 + i) * 128 + ((lch ^ (i & 7)) << 4) + lsub);
+    };
+
+    // ---- G1: [A_raw; P] = [kd'; qd'] ki'^T ----------------------------------------
+    build(sW0, nullptr, false, 1.f, F_KDP);    // kd'
+    build(sW1, nullptr, true, p.scale, F_KDP);  // qd'
+    build(sW2, nullptr, false, 1.f, F_KIP);     // ki' (the q tile is dead)
+    sync_all();
+    if (tid == 0) {
+        constexpr uint32_t id = tc::idesc(128, 64, 1, 1);
+        for (int k = 0; k < MD; k += 16)
+            tc::mma(tmem + R_B, tc::mdesc(sb + oW0, 128, 0, k), tc::mdesc(sb + oW2, 128, 0, k), id, k > 0);
+        tc::commit(mb);
+    }
+    if (!wait_mma()) return;
+    tc::ld16(tl(R_B + c0), v);
+    {
+        const bool isA = L < 64;
+        const int r = isA ? L : L - 64;
+        unsigned char* dst = isA ? sA : sP;
+        const float br = sBeta[r];
+#pragma unroll
+        for (int jc = 0; jc < NCOL / 8; ++jc) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int s0 = c0 + jc * 8 + 2 * e;
+                float a0 = v[jc * 8 + 2 * e], a1 = v[jc * 8 + 2 * e + 1];
+                if (isA) {
+                    a0 = s0 < r ? br * a0 : 0.f;
+                    a1 = s0 + 1 < r ? br * a1 : 0.f;
+                } else {
+                    a0 = s0 <= r ? a0 : 0.f;
+                    a1 = s0 + 1 <= r ? a1 : 0.f;
+                }
+                w[e] = pack_bf16(a0, a1);
+            }
+            *reinterpret_cast<uint4*>(dst + tc::sw_chunk(r, (c0 >> 3) + jc, 64)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    }
+    build(sW0, nullptr, false, 1.f, F_KD);  // kd (G1 has completed: kd' is dead)
+    build(sW2, nullptr, false, 1.f, F_KR);  // kr (ki' is dead)
+    sync_all();
+
+    // ---- G2: X^T = S0^T kd^T ; G3: dqd^T = S0 dO^T ; G5b: dS^T kr^T ----------------------
+    if (tid == 0) {
+        constexpr uint32_t id2 = tc::idesc(128, 64, 0, 1), id3 = tc::idesc(128, 64, 1, 0),
+                           id5 = tc::idesc(128, 64, 0, 1);
+        for (int k = 0; k < MD; k += 16)
+            tc::mma(tmem + R_C, tc::kdesc(sb + oS0, 128, 0, k), tc::mdesc(sb + oW0, 128, 0, k), id2, k > 0);
+        for (int k = 0; k < MD; k += 16)
+            tc::mma(tmem + R_D, tc::mdesc(sb + oS0, 128, 0, k), tc::kdesc(sb + oDOY, 128, 0, k), id3, k > 0);
+        // second half of G5 (independent of beta E): du^T = dS^T kr^T (+ dO^T P later)
+        for (int k = 0; k < MD; k += 16)
+            tc::mma(tmem + R_A, tc::kdesc(sb + oDS, 128, 0, k), tc::mdesc(sb + oW2, 128, 0, k), id5, k > 0);
+        tc::commit(mb);
+    }
+    if (!wait_mma()) return;
+    tc::ld16(tl(R_C + c0), v);
+    {
+        float bt[16];
+        rows16(sBeta, bt);
+#pragma unroll
+        for (int i = 0; i < NCOL; ++i) {  // beta E = beta (V - X), in place of V (lane = value channel)
+            __nv_bfloat16* pv = reinterpret_cast<__nv_bfloat16*>(sV + tok(64, i));
+            const float be = bt[i] * (__bfloat162float(*pv) - v[i]);
+            const __nv_bfloat16 hi = __float2bfloat16(be);
+            *pv = hi;
+            if (KDA) *reinterpret_cast<__nv_bfloat16*>(sK + tok(64, i)) = __float2bfloat16(be - __bfloat162float(hi));
+        }
+    }
+    tc::ld16(tl(R_D + c0), v);
+    {
+        float f[16], x[16], inv[16];
+        factors(F_KD, f);
+        load_x(true, x, inv);
+#pragma unroll
+        for (int i = 0; i < NCOL; ++i) {  // dqd (lane = key channel)
+            const float t = p.scale * v[i] * f[i];
+            dQn[i] += t;
+            dGc[i] += x[i] * inv[i] * t;
+        }
+    }
+    sync_all();
+
+    // ---- G4: u^T = (beta E)^T T^T ; G5a: du^T += dO^T P ------------------------------
+    if (tid == 0) {
+        constexpr uint32_t id4 = tc::idesc(128, 64, 1, 0), id5 = tc::idesc(128, 64, 1, 1);
+        for (int k = 0; k < CH; k += 16)
+            tc::mma(tmem + R_B, tc::mdesc(sb + oV, 64, 0, k), tc::kdesc(sb + oT, 64, 0, k), id4, k > 0);
+        if (KDA)
+            for (int k = 0; k < CH; k += 16)
+                tc::mma(tmem + R_B, tc::mdesc(sb + oK, 64, 0, k), tc::kdesc(sb + oT, 64, 0, k), id4, 1);
+        for (int k = 0; k < CH; k += 16)
+            tc::mma(tmem + R_A, tc::mdesc(sb + oDOY, 128, 0, k), tc::mdesc(sb + oP, 64, 0, k), id5, 1);
+        tc::commit(mb);
+    }
+    if (!wait_mma()) return;
+    tc::ld16(tl(R_B + c0), v);
+    if (KDA)
+        store_cm_pair(sW1, sW0, v);  // u^T (hi) and its residual (kd is dead)
+    else
+        store_cm(sW1, v);
+    tc::ld16(tl(R_A + c0), v);
+    store_cm(sW2, v);  // du^T over kr
+    sync_all();
+
+    // ---- G6: dY^T = du^T T ------------------------------------------------------------
+    if (tid == 0) {
+        constexpr uint32_t id6 = tc::idesc(128, 64, 0, 1);
+        for (int k = 0; k < CH; k += 16)
+            tc::mma(tmem + R_D, tc::kdesc(sb + oW2, 128, 0, k), tc::mdesc(sb + oT, 64, 0, k), id6, k > 0);
+        tc::commit(mb);
+    }
+    if (!wait_mma()) return;
+    tc::ld16(tl(R_D + c0), v);
+    {
+        float bt[16];
+        rows16(sBeta, bt);
+#pragma unroll
+        for (int i = 0; i < NCOL; ++i) {
+            const int r = c0 + i;
+            if (r < ci.len) p.dv[((ci.t0 + r) * p.H + h) * MD + L] = __float2bfloat16(bt[i] * v[i]);
+            *reinterpret_cast<__nv_bfloat16*>(sDOY + tok(128, i) + 64 * 128) = __float2bfloat16(v[i]);  // dY
+        }
+    }
+    sync_all();
+
+    // ---- G7: Z^T = S0 dY^T ; G8: dkr^T = dS u^T ; G9: [dP; dA]_raw = [dO; dY] u^T ------------
+    if (tid == 0) {
+        constexpr uint32_t id7 = tc::idesc(128, 64, 1, 0), id8 = tc::idesc(128, 64, 1, 1),
+                           id9 = tc::idesc(128, 64, 0, 1);
+        for (int k = 0; k < MD; k += 16)
+            tc::mma(tmem + R_B, tc::mdesc(sb + oS0, 128, 0, k), tc::kdesc(sb + oDOY, 128, 64, k), id7, k > 0);
+        for (int k = 0; k < MD; k += 16)
+            tc::mma(tmem + R_C, tc::mdesc(sb + oDS, 128, 0, k), tc::mdesc(sb + oW1, 128, 0, k), id8, k > 0);
+        for (int k = 0; k < MD; k += 16)
+            tc::mma(tmem + R_D, tc::kdesc(sb + oDOY, 128, 0, k), tc::mdesc(sb + oW1, 128, 0, k), id9, k > 0);
+        if (KDA) {  // u lo
+            for (int k = 0; k < MD; k += 16)
+                tc::mma(tmem + R_C, tc::mdesc(sb + oDS, 128, 0, k), tc::mdesc(sb + oW0, 128, 0, k), id8, 1);
+            for (int k = 0; k < MD; k += 16)
+                tc::mma(tmem + R_D, tc::kdesc(sb + oDOY, 128, 0, k), tc::mdesc(sb + oW0, 128, 0, k), id9, 1);
+        }
+        tc::commit(mb);
+    }
+    // while the tensor cores run: <dY, beta E> per row (token-major, 4 threads per row)
+    if (tid < 4 * CH) {
+        const int r = tid >> 2, part = tid & 3;
+        float s2 = 0.f;
+        for (int j = part * 4; j < part * 4 + 4; ++j) {
+            const uint4 a = *reinterpret_cast<const uint4*>(sDOY + tc::sw_chunk(64 + r, j, 128));
+            const uint4 b = *reinterpret_cast<const uint4*>(sV + tc::sw_chunk(r, j, 64));
+            const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};
+            uint32_t wl[4] = {0, 0, 0, 0};
+            if (KDA) {
+                const uint4 l = *reinterpret_cast<const uint4*>(sK + tc::sw_chunk(r, j, 64));
+                wl[0] = l.x;
+                wl[1] = l.y;
+                wl[2] = l.z;
+                wl[3] = l.w;
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 fa = unpack_bf16(wa[e]);
+                float2 fb = unpack_bf16(wb[e]);
+                if (KDA) {
+                    const float2 fl = unpack_bf16(wl[e]);
+                    fb.x += fl.x;
+                    fb.y += fl.y;
+                }
+                s2 += fa.x * fb.x + fa.y * fb.y;
+            }
+        }
+        s2 += __shfl_xor_sync(0xffffffffu, s2, 1);
+        s2 += __shfl_xor_sync(0xffffffffu, s2, 2);
+        if (part == 0) sDbP[r] = s2;
+    }
+    if (!wait_mma()) return;
+    tc::ld16(tl(R_B + c0), v);
+    {
+        float f[16], x[16], inv[16];
+        factors(F_KD, f);
+        load_x(false, x, inv);
+        float bt[16];
+        rows16(sBeta, bt);
+#pragma unroll
+        for (int i = 0; i < NCOL; ++i) {  // dkd (from E) = -beta Z
+            const float t = -bt[i] * v[i] * f[i];
+            dKn[i] += t;
+            dGc[i] += x[i] * inv[i] * t;
+        }
+        tc::ld16(tl(R_C + c0), v);
+        factors(F_KR, f);
+        float dgt = 0.f;
+#pragma unroll
+        for (int i = 0; i < NCOL; ++i) {  // dkr
+            const float t = v[i] * f[i];
+            dKn[i] += t;
+            const float kt = x[i] * inv[i] * t;
+            dGc[i] -= kt;
+            dgt += kt;
+        }
+        sDgTp[hc * MD + L] = dgt;
+    }
+    tc::ld16(tl(R_D + c0), v);
+    {
+        // lanes 0..63: dP rows, lanes 64..127: dA rows ; [dP; beta dA] -> the dS space [128][64]
+        const bool isP = L < 64;
+        const int r = isP ? L : L - 64;
+        const float br = sBeta[r];
+        float dbs = 0.f;
+        float o[16];
+#pragma unroll
+        for (int jc = 0; jc < NCOL / 8; ++jc) {
+            const uint4 av = *reinterpret_cast<const uint4*>(sA + tc::sw_chunk(r, (c0 >> 3) + jc, 64));
+            const uint32_t wa[4] = {av.x, av.y, av.z, av.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int i0 = jc * 8 + 2 * e, s0 = c0 + i0;
+                float a0 = v[i0], a1 = v[i0 + 1];
+                if (isP) {
+                    a0 = s0 <= r ? a0 : 0.f;
+                    a1 = s0 + 1 <= r ? a1 : 0.f;
+                } else {
+                    a0 = s0 < r ? -a0 : 0.f;
+                    a1 = s0 + 1 < r ? -a1 : 0.f;
+                    const float2 aa = unpack_bf16(wa[e]);
+                    dbs += a0 * aa.x + a1 * aa.y;
+                    a0 *= br;
+                    a1 *= br;
+                }
+                o[i0] = a0;
+                o[i0 + 1] = a1;
+            }
+        }
+        if (!isP) sDbA[hc * CH + r] = dbs;
+        __syncthreads();  // every reader of S0, dS (and the u lo tile) is done
+        if (KDA)
+            store_cm_pair(sDS, sDS + TILE, o);
+        else
+            store_cm(sDS, o);
+    }
+    // rebuilds for G10 / G11: ki' -> W0 (lo W1), qd' -> W2 (lo K), kd' -> S0 (lo S0 + 16 KB)
+    build(sW0, KDA ? sW1 : nullptr, false, 1.f, F_KIP);
+    build(sW2, KDA ? sK : nullptr, true, p.scale, F_KDP);
+    build(sS0, KDA ? sS0 + TILE : nullptr, false, 1.f, F_KDP);
+    sync_all();
+
+    // ---- G10: [dqd', dkd']^T = ki'^T [dP; beta dA]^T ; G11: dki'^T = qd'^T dP + kd'^T (beta dA) --
+    if (tid == 0) {
+        constexpr uint32_t id10 = tc::idesc(128, 128, 0, 0), id11 = tc::idesc(128, 64, 0, 1);
+        const uint32_t kiH = sb + oW0, kiL = sb + oW1, qdH = sb + oW2, qdL = sb + oK, kdH = sb + oS0,
+                       kdL = sb + oS0 + TILE, xH = sb + oDS, xL = sb + oDS + TILE;
+        for (int k = 0; k < CH; k += 16)
+            tc::mma(tmem + R_A, tc::kdesc(kiH, 128, 0, k), tc::kdesc(xH, 128, 0, k), id10, k > 0);
+        if (KDA) {
+            for (int k = 0; k < CH; k += 16)
+                tc::mma(tmem + R_A, tc::kdesc(kiH, 128, 0, k), tc::kdesc(xL, 128, 0, k), id10, 1);
+            for (int k = 0; k < CH; k += 16)
+                tc::mma(tmem + R_A, tc::kdesc(kiL, 128, 0, k), tc::kdesc(xH, 128, 0, k), id10, 1);
+        }
+        for (int k = 0; k < CH; k += 16)
+            tc::mma(tmem + R_B, tc::kdesc(qdH, 128, 0, k), tc::mdesc(xH, 128, 0, k), id11, k > 0);
+        for (int k = 0; k < CH; k += 16)
+            tc::mma(tmem + R_B, tc::kdesc(kdH, 128, 0, k), tc::mdesc(xH, 128, 64, k), id11, 1);
+        if (KDA) {
+            for (int k = 0; k < CH; k += 16) {
+                tc::mma(tmem + R_B, tc::kdesc(qdH, 128, 0, k), tc::mdesc(xL, 128, 0, k), id11, 1);
+                tc::mma(tmem + R_B, tc::kdesc(qdL, 128, 0, k), tc::mdesc(xH, 128, 0, k), id11, 1);
+                tc::mma(tmem + R_B, tc::kdesc(kdH, 128, 0, k), tc::mdesc(xL, 128, 64, k), id11, 1);
+                tc::mma(tmem + R_B, tc::kdesc(kdL, 128, 0, k), tc::mdesc(xH, 128, 64, k), id11, 1);
+            }
+        }
+        tc::commit(mb);
+    }
+    if (!wait_mma()) return;
+    // the gate-gradient term takes the derived-tile value the products consumed: the bf16
+    // element (GDN) or the fp32 value of the hi + lo pair (KDA)
+    auto tile_val = [&](float x, float mm, float f) -> float { return KDA ? x * mm * f : derived_val(x, mm, f); };
+    {
+        float f[16], x[16], inv[16];
+        factors(F_KDP, f);
+        load_x(true, x, inv);
+        tc::ld16(tl(R_A + c0), v);
+#pragma unroll
+        for (int i = 0; i < NCOL; ++i) {  // dqd'
+            dQn[i] += p.scale * v[i] * f[i];
+            dGc[i] += tile_val(x[i], derived_m(inv[i], p.scale, 1.f), f[i]) * v[i];
+        }
+        load_x(false, x, inv);
+        tc::ld16(tl(R_A + 64 + c0), v);
+#pragma unroll
+        for (int i = 0; i < NCOL; ++i) {  // dkd'
+            dKn[i] += v[i] * f[i];
+            dGc[i] += tile_val(x[i], derived_m(inv[i], 1.f, 1.f), f[i]) * v[i];
+        }
+        factors(F_KIP, f);
+        tc::ld16(tl(R_B + c0), v);
+#pragma unroll
+        for (int i = 0; i < NCOL; ++i) {  // dki'
+            dKn[i] += v[i] * f[i];
+            dGc[i] -= tile_val(x[i], derived_m(inv[i], 1.f, 1.f), f[i]) * v[i];
+        }
+    }
+
+    // ---- epilogue: L2-norm backward, dq / dk, dbeta, the gate gradient ----------------------
+    float* sRowQ = sRow;        // [4][64] per lane quarter
+    float* sRowK = sRow + 256;  // [4][64]
+    float* sRowG = sRow + 512;  // [4][64] (GDN)
+    if constexpr (!KDA) {  // channel sums of dgc per row (dGc is dead afterwards)
+        const float sg = warp_transpose_sum16(dGc);  // lanes 2i, 2i+1: row c0 + i
+        if ((lane & 1) == 0) sRowG[q4 * CH + c0 + (lane >> 1)] = sg;
+    }
+    {
+        // per-row dots over this warp's 32 channels: lane l gets row c0 + (l & 15)
+        float t[32];
+        {
+            float x[16], inv[16];
+            load_x(true, x, inv);
+#pragma unroll
+            for (int i = 0; i < NCOL; ++i) t[i] = dQn[i] * x[i] * inv[i];
+            load_x(false, x, inv);
+#pragma unroll
+            for (int i = 0; i < NCOL; ++i) t[16 + i] = dKn[i] * x[i] * inv[i];
+        }
+        const float s = warp_transpose_sum32(t);  // lane l: value l (l < 16: q row c0+l, else k row c0+l-16)
+        (lane < 16 ? sRowQ : sRowK)[q4 * CH + c0 + (lane & 15)] = s;
+    }
+    __syncthreads();
+    {
+        float x[16], inv[16];
+        load_x(true, x, inv);
+#pragma unroll
+        for (int i = 0; i < NCOL; ++i) {
+            const int r = c0 + i;
+            const float tq = ((sRowQ[r] + sRowQ[CH + r]) + sRowQ[2 * CH + r]) + sRowQ[3 * CH + r];
+            if (r < ci.len)
+                p.dq[((ci.t0 + r) * p.H + h) * MD + L] = __float2bfloat16((dQn[i] - x[i] * inv[i] * tq) * inv[i]);
+        }
+        load_x(false, x, inv);
+#pragma unroll
+        for (int i = 0; i < NCOL; ++i) {
+            const int r = c0 + i;
+            const float tk = ((sRowK[r] + sRowK[CH + r]) + sRowK[2 * CH + r]) + sRowK[3 * CH + r];
+            if (r < ci.len)
+                p.dk[((ci.t0 + r) * p.H + h) * MD + L] = __float2bfloat16((dKn[i] - x[i] * inv[i] * tk) * inv[i]);
+        }
+    }
+    // dbeta (logit space)
+    for (int r = tid; r < ci.len; r += 512) {
+        const float dA_A = ((sDbA[r] + sDbA[CH + r]) + sDbA[2 * CH + r]) + sDbA[3 * CH + r];
+        p.dbeta[(ci.t0 + r) * p.H + h] = __float2bfloat16((1.f - sBeta[r]) * (sDbP[r] + dA_A));
+    }
+    auto dgT_of = [&](int d) -> float {
+        return (((sDgTs[d] + sDgTp[d]) + sDgTp[MD + d]) + sDgTp[2 * MD + d]) + sDgTp[3 * MD + d];
+    };
+    if constexpr (!KDA) {
+        // dg: channel sums of dgc (per row), suffix sums over the rows, plus the chunk constant dgT
+        if (warp == 0) {
+            float t = 0.f;
+            for (int d = lane; d < MD; d += 32) t += dgT_of(d);
+            t = warp_sum(t);
+            const int r0 = 2 * lane;
+            const float a = ((sRowG[r0] + sRowG[CH + r0]) + sRowG[2 * CH + r0]) + sRowG[3 * CH + r0];
+            const float b = ((sRowG[r0 + 1] + sRowG[CH + r0 + 1]) + sRowG[2 * CH + r0 + 1]) + sRowG[3 * CH + r0 + 1];
+            float incl = a + b;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float y = __shfl_down_sync(0xffffffffu, incl, o);
+                if (lane + o < 32) incl += y;
+            }
+            if (r0 < ci.len) p.dg[(ci.t0 + r0) * p.H + h] = incl + t;
+            if (r0 + 1 < ci.len) p.dg[(ci.t0 + r0 + 1) * p.H + h] = incl - a + t;
+        }
+    } else {
+        // reverse cumsum of dgc over the rows per channel: this thread's 16 rows in registers,
+        // the later row quarters' totals and the chunk constant dgT as the suffix; then the
+        // gate chain rule per element, with per-channel partial sums
+        float xr[16];
+        const float bias = p.dt_bias[h * MD + L];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int r = c0 + i;
+            xr[i] = r < ci.len ? bf2f(p.g_raw[((ci.t0 + r) * p.H + h) * MD + L]) + bias : 0.f;
+        }
+        float acc = 0.f;
+#pragma unroll
+        for (int i = 15; i >= 0; --i) {
+            acc += dGc[i];
+            dGc[i] = acc;
+        }
+        sScan[hc * MD + L] = acc;
+        __syncthreads();
+        float post = dgT_of(L);
+#pragma unroll
+        for (int h2 = 3; h2 >= 0; --h2)
+            if (h2 > hc) post += sScan[h2 * MD + L];
+        const float ea = expf(p.A_log[h]);
+        float ddt = 0.f, dA_acc = 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int r = c0 + i;
+            if (r < ci.len) {
+                const float dgl = dGc[i] + post;
+                const float draw = dgl * (-ea * sigmoid_f(xr[i]));
+                p.dg_raw[((ci.t0 + r) * p.H + h) * MD + L] = __float2bfloat16(draw);
+                ddt += draw;
+                dA_acc += dgl * (-ea * softplus_f(xr[i]));
+            }
+        }
+        __syncthreads();  // suffix totals read
+        sScan[hc * MD + L] = ddt;
+        dA_acc = warp_sum(dA_acc);
+        if (lane == 0) sMisc[warp] = dA_acc;
+        __syncthreads();
+        if (tid < MD) {
+            const float t = ((sScan[tid] + sScan[MD + tid]) + sScan[2 * MD + tid]) + sScan[3 * MD + tid];
+            atomicAdd(&p.ddt_bias[h * MD + tid], t);
+        }
+        if (tid == 0) {
+            float t = 0.f;
+            for (int w = 0; w < 16; ++w) t += sMisc[w];
+            atomicAdd(&p.dA_log[h], t);
+        }
+    }
+    tc::fence_before();
+    __syncthreads();
+    if (warp == 0) tc::dealloc(tmem, 512);
+}
+
+template <bool KDA>
+static cudaError_t launch_main_tc2_t(const Params& p, cudaStream_t s) {
+    MainMaps m;
+    const uint64_t rows_cc = (uint64_t)p.max_chunks * p.H * CH;
+    const uint64_t rows_dd = (uint64_t)p.max_chunks * p.H * MD;
+    const uint64_t T = (uint64_t)p.T_total;
+    bool ok = encode_blocked_tokens_map(&m.q, p.q, T, p.H) && encode_blocked_tokens_map(&m.k, p.k, T, p.H) &&
+              encode_blocked_tokens_map(&m.v, p.v, T, p.H) && encode_tokens_map(&m.dO, p.dO, T, p.H, MD) &&
+              encode_blocked_rows_map(&m.S0, p.S0, rows_dd, MD) && encode_blocked_rows_map(&m.dS, p.dS, rows_dd, MD) &&
+              encode_rows_map(&m.T, p.Tm, rows_cc, CH, CH);
+    if (!ok) return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(k_main_tc2<KDA>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    dim3 grid(p.max_chunks, p.H);
+    k_main_tc2<KDA><<<grid, 512, SMEM_BYTES, s>>>(p, m);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_main_tc2(const Params& p, cudaStream_t s) {
+    return p.kda ? launch_main_tc2_t<true>(p, s) : launch_main_tc2_t<false>(p, s);
+}
+
+}  // namespace gdr
