@@ -284,11 +284,13 @@ __device__ __forceinline__ void frag_foreach(float (&acc)[MT][NT][4], int m0, in
 // T = (I + A)^-1 for a strictly lower 64x64 fp32 matrix A (row stride 65).
 // Blocked: 16x16 diagonal blocks by forward substitution, then the off-diagonal
 // blocks T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj by increasing i - j.
-// tmp: 3 * 256 floats.  Needs blockDim.x == 256.  Tf gets the full lower T.
+// tmp: 3 * 256 floats.  NT = blockDim.x (a multiple of 256 or 256 exactly); threads
+// beyond the first 256 only help clear Tf.  Tf gets the full lower T.
+template <int NT = 256>
 __device__ inline void invert_unit_lower64(const float* A, float* Tf, float* tmp) {
     constexpr int LD = 65;
     const int t = threadIdx.x;
-    for (int i = t; i < 64 * LD; i += 256) Tf[i] = 0.f;
+    for (int i = t; i < 64 * LD; i += NT) Tf[i] = 0.f;
     __syncthreads();
     if (t < 64) {
         const int b = t >> 4, j = t & 15;
@@ -307,7 +309,7 @@ __device__ inline void invert_unit_lower64(const float* A, float* Tf, float* tmp
     __syncthreads();
     for (int L = 1; L < 4; ++L) {
         const int nb = 4 - L;
-        for (int e = t; e < nb * 256; e += 256) {
+        for (int e = t; e < nb * 256 && t < 256; e += 256) {
             const int j = e >> 8, i = j + L, r = (e >> 4) & 15, c = e & 15;
             float acc = 0.f;
             for (int k = j; k < i; ++k) {
@@ -319,7 +321,7 @@ __device__ inline void invert_unit_lower64(const float* A, float* Tf, float* tmp
             tmp[e] = acc;
         }
         __syncthreads();
-        for (int e = t; e < nb * 256; e += 256) {
+        for (int e = t; e < nb * 256 && t < 256; e += 256) {
             const int j = e >> 8, i = j + L, r = (e >> 4) & 15, c = e & 15;
             const float* Tr = Tf + (16 * i + r) * LD + 16 * i;
             const float* M = tmp + (j << 8) + c;

@@ -27,8 +27,8 @@ struct Params {
 
     // workspace
     int* status;
-    // per chunk-head tiles: W, Kr, R, Rlo [C][D]; U [C][D] (D = 64) or value-major [D][C]
-    // (D = 128); T [C][C]
+    // per chunk-head tiles: W, U, Kr, R, Rlo [C][D] (D = 64) or channel-major [D][C]
+    // (D = 128, the layout the tcgen05 state recurrence reads); T [C][C]
     __nv_bfloat16 *W, *U, *Kr, *R, *Rlo, *Tm;
     float *gT, *egT;                     // [chunk][H][D]: chunk gate total and its exponential
     __nv_bfloat16 *S0, *dS;              // per chunk-head states, value-major [dv][dk]
@@ -40,8 +40,22 @@ struct Params {
     float *dh0, *dA_log, *ddt_bias;
 };
 
+// multiprocessors of the current device (cached per device)
+inline int num_sms() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+    if (cache[dev] == 0) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        cache[dev] = n > 0 ? n : 1;
+    }
+    return cache[dev];
+}
+
 cudaError_t launch_chunk_table(const Params& p, cudaStream_t s);
 cudaError_t launch_prep(const Params& p, cudaStream_t s);
+cudaError_t launch_prep_tc(const Params& p, cudaStream_t s);  // D = 128, tcgen05 + TMA
 cudaError_t launch_states(const Params& p, bool fwd, bool bwd, cudaStream_t s);
 cudaError_t launch_states_tc(const Params& p, bool fwd, bool bwd, cudaStream_t s);  // D = 128, tcgen05 + TMA
 cudaError_t launch_main(const Params& p, cudaStream_t s);

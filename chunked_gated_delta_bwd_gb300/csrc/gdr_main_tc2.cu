@@ -1,5 +1,8 @@
-// Chunk-parallel main backward on tcgen05 for D = 128, GDN and KDA: one CTA (16
-// warps) per (chunk, head).  Same algebra as the warp-level kernel in gdr_main.cu;
+// Chunk-parallel main backward on tcgen05 for D = 128, GDN and KDA: persistent CTAs
+// of 16 warps, one per SM, each looping over (chunk, head) items; the next item's
+// operand tiles arrive by TMA while the current item's epilogue runs (every large
+// shared tile is dead after the last product group).  Same algebra as the warp-level
+// kernel in gdr_main.cu;
 // every product is a 128-row tcgen05 MMA into tensor memory, written feature-major
 // where the natural output is C x D: the accumulator holds X^T (lane = key channel d
 // or value channel j, column = token row r), so a thread owns one channel for 16
@@ -105,11 +108,10 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
     unsigned char* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     const uint32_t sb = smem_u32(smem);
 
-    const int chunk = blockIdx.x, h = blockIdx.y;
-    ChunkInfo ci;
-    if (!lookup_chunk(chunk, p.N, p.chunk_off, p.cu_seqlens, p.seq_len, ci)) return;
-
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // items (chunk, head) = chunk * H + h over the chunks that exist
+    const int total_chunks = p.chunk_off ? p.chunk_off[p.N] : p.N * (int)((p.seq_len + CH - 1) / CH);
+    const int n_items = total_chunks * p.H;
     const int q4 = warp & 3, hc = warp >> 2;  // tensor-memory lane quarter, row quarter
     const int L = 32 * q4 + lane;             // this thread's lane: a channel, or a stacked row
     const int c0 = NCOL * hc;                 // first of this thread's 16 rows
@@ -140,31 +142,36 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
     G.ref = sGate + CH;
     G.gT = sGate + CH + 1;
 
-    const int row_cd = (chunk * p.H + h) * CH, row_dd = (chunk * p.H + h) * MD;
+    // every operand tile of an item (thread 0)
+    auto issue_loads = [&](int item) {
+        ChunkInfo cj;
+        lookup_chunk(item / p.H, p.N, p.chunk_off, p.cu_seqlens, p.seq_len, cj);
+        const int hh = item % p.H, t0 = (int)cj.t0, rcd = item * CH, rdd = item * MD;
+        tc::mbar_expect_tx(mload, 4 * TILE + 2 * 2 * TILE + CH * CH * 2);
+        tc::tma_load_4d(sb + oK, &m.k, 0, hh, t0, 0, mload);
+        tc::tma_load_4d(sb + oV, &m.v, 0, hh, t0, 0, mload);
+        tc::tma_load_4d(sb + oW2, &m.q, 0, hh, t0, 0, mload);
+        tc::tma_load_3d(sb + oDOY, &m.dO, 0, hh, t0, mload);  // rows 0..63 of a 128-row tile
+        tc::tma_load_3d(sb + oDOY + 128 * 128, &m.dO, 64, hh, t0, mload);
+        tc::tma_load_3d(sb + oS0, &m.S0, 0, rdd, 0, mload);
+        tc::tma_load_3d(sb + oDS, &m.dS, 0, rdd, 0, mload);
+        tc::tma_load_2d(sb + oT, &m.T, 0, rcd, mload);
+    };
 
-    // ---- set-up: tensor memory, barriers, TMA loads of every operand tile ----------
+    // ---- set-up: tensor memory, barriers, the first item's loads ----------------------
     if (warp == 0) tc::alloc(smem_u32(tslot), 512);
     if (tid == 0) {
         tc::mbar_init(mb, 1);
         tc::mbar_init(mload, 1);
-        tc::mbar_expect_tx(mload, 4 * TILE + 2 * 2 * TILE + CH * CH * 2);
-        const int t0 = (int)ci.t0;
-        tc::tma_load_4d(sb + oK, &m.k, 0, h, t0, 0, mload);
-        tc::tma_load_4d(sb + oV, &m.v, 0, h, t0, 0, mload);
-        tc::tma_load_4d(sb + oW2, &m.q, 0, h, t0, 0, mload);
-        tc::tma_load_3d(sb + oDOY, &m.dO, 0, h, t0, mload);  // rows 0..63 of a 128-row tile
-        tc::tma_load_3d(sb + oDOY + 128 * 128, &m.dO, 64, h, t0, mload);
-        tc::tma_load_3d(sb + oS0, &m.S0, 0, row_dd, 0, mload);
-        tc::tma_load_3d(sb + oDS, &m.dS, 0, row_dd, 0, mload);
-        tc::tma_load_2d(sb + oT, &m.T, 0, row_cd, mload);
+        if ((int)blockIdx.x < n_items) issue_loads(blockIdx.x);
     }
-    if constexpr (!KDA) load_gates<MD, false, 512>(p, ci, h, G, false);
-    load_beta(p, ci, h, sBeta);
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
     const uint32_t tmem = *tslot;
     uint32_t phase = 0;
+    int it = 0;              // this CTA's item count (the load barrier's phase)
+    bool pending = (int)blockIdx.x < n_items;  // a load batch is in flight
     auto sync_all = [&]() {  // make smem writes visible to the tensor cores and order TMEM use
         tc::fence_async_smem();
         tc::fence_before();
@@ -174,15 +181,21 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
     // Waits for the last commit.  If the tensor cores do not answer within the
     // bounded spin, every thread learns it from the vote, the status word records
     // it, the tensor memory is released and the CTA returns.
+    auto bail = [&]() {
+        if (tid == 0) {
+            atomicOr(p.status, ST_MMA_TIMEOUT);
+            if (pending) tc::mbar_wait(mload, (uint32_t)(it & 1));  // bounded drain of the loads in flight
+        }
+        tc::fence_before();
+        __syncthreads();
+        if (warp == 0) tc::dealloc(tmem, 512);
+    };
     auto wait_mma = [&]() -> bool {
         const bool ok = tc::mbar_wait(mb, phase);
         phase ^= 1;
         tc::fence_after();
         if (__syncthreads_or(!ok)) {
-            if (tid == 0) atomicOr(p.status, ST_MMA_TIMEOUT);
-            tc::fence_before();
-            __syncthreads();
-            if (warp == 0) tc::dealloc(tmem, 512);
+            bail();
             return false;
         }
         return true;
@@ -220,6 +233,13 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
         *reinterpret_cast<uint4*>(lo + tc::sw_chunk(L, c0 >> 3, 128)) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
         *reinterpret_cast<uint4*>(lo + tc::sw_chunk(L, (c0 >> 3) + 1, 128)) = make_uint4(wl[4], wl[5], wl[6], wl[7]);
     };
+
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++it) {
+    const int chunk = item / p.H, h = item % p.H;
+    ChunkInfo ci;
+    lookup_chunk(chunk, p.N, p.chunk_off, p.cu_seqlens, p.seq_len, ci);
+    if constexpr (!KDA) load_gates<MD, false, 512>(p, ci, h, G, false);
+    load_beta(p, ci, h, sBeta);
 
     // KDA: per-channel log gates of this thread's channel and rows, scanned across the four
     // row quarters, staged in tensor memory (lane = channel, column = row)
@@ -274,14 +294,9 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
 
     // wait for the operand tiles; rows past the chunk's end read as zero
     {
-        const bool ok = tc::mbar_wait(mload, 0);
-        if (__syncthreads_or(!ok)) {
-            if (tid == 0) atomicOr(p.status, ST_MMA_TIMEOUT);
-            tc::fence_before();
-            __syncthreads();
-            if (warp == 0) tc::dealloc(tmem, 512);
-            return;
-        }
+        const bool ok = tc::mbar_wait(mload, (uint32_t)(it & 1));
+        if (__syncthreads_or(!ok)) return bail();
+        pending = false;
     }
     if (ci.len < CH) {
         const int nz = (CH - ci.len) * 16;  // 16-byte chunks per 64-row tile (2 blocks x 8)
@@ -681,6 +696,11 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
         tc::commit(mb);
     }
     if (!wait_mma()) return;
+    // every large shared tile is dead: the next item's operands may land while this epilogue runs
+    if (item + (int)gridDim.x < n_items) {
+        if (tid == 0) issue_loads(item + gridDim.x);
+        pending = true;
+    }
     // the gate-gradient term takes the derived-tile value the products consumed: the bf16
     // element (GDN) or the fp32 value of the hi + lo pair (KDA)
     auto tile_val = [&](float x, float mm, float f) -> float { return KDA ? x * mm * f : derived_val(x, mm, f); };
@@ -831,6 +851,10 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
         }
     }
     tc::fence_before();
+    __syncthreads();  // this item's small arrays and tensor memory are free
+    tc::fence_after();
+    }
+    tc::fence_before();
     __syncthreads();
     if (warp == 0) tc::dealloc(tmem, 512);
 }
@@ -848,8 +872,9 @@ static cudaError_t launch_main_tc2_t(const Params& p, cudaStream_t s) {
     if (!ok) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(k_main_tc2<KDA>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    dim3 grid(p.max_chunks, p.H);
-    k_main_tc2<KDA><<<grid, 512, SMEM_BYTES, s>>>(p, m);
+    const int items = p.max_chunks * p.H;
+    const int ctas = items < num_sms() ? items : num_sms();
+    k_main_tc2<KDA><<<ctas, 512, SMEM_BYTES, s>>>(p, m);
     return cudaGetLastError();
 }
 

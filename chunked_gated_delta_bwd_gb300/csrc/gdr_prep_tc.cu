@@ -1,0 +1,473 @@
+// Chunk-parallel preparation on tcgen05 for D = 128, GDN and KDA: persistent CTAs of
+// 16 warps, one per SM, each looping over (chunk, head) items; the q, k, v tiles of the
+// next item arrive by TMA into a second buffer while the current item is computed.
+// Same quantities as the warp-level kernel in gdr_prep.cu (the X/R form of the FlashQLA
+// dh kernel, "FlashQLA ... GDN 反向", §三):
+//
+//   [A_raw; P] = [kd'; qd'] ki'^T       A = strict_lower(diag(beta) A_raw) (fp32), P = lower(.)
+//   T   = (I + A)^-1                     (fp32 blocked inverse on CUDA cores)
+//   W^T = (beta kd)^T T^T                U^T = (beta V)^T T^T
+//   R^T = qd^T - W^T P^T                 (a bf16 pair R_hi + R_lo)
+//   kr  = kn e^{gT-gc}
+//
+// Products whose natural output is C x D are computed transposed (lane = channel), so
+// a thread owns one channel for 16 rows; W, U, Kr, R_hi and R_lo are written
+// channel-major ([D][C], 32 contiguous bytes per thread and row), the layout the
+// D = 128 state recurrence reads; T is written [C][C].  The raw q and k rows and (KDA)
+// the per-channel cumulative gate are staged in tensor memory once.
+#include "gdr_chunk.cuh"
+#include "gdr_tc.cuh"
+#include "gdr_tma.h"
+
+namespace gdr {
+
+namespace {
+
+constexpr int PD = 128;
+constexpr int TILE = CH * PD * 2;  // 16 KB
+constexpr int LDF = 65;            // row stride of the fp32 64 x 64 matrices of the inversion
+// shared-memory map (bytes from the 1024-aligned base); two input stages of q, k, v
+constexpr int STAGE = 3 * TILE;
+constexpr int oQ = 0;         // q (token-major) -> (beta kd)^T [d][s]   (+ STAGE for the other stage)
+constexpr int oK = 16384;     // k (token-major) -> (beta V)^T [j][s]
+constexpr int oV = 32768;     // v (token-major)
+constexpr int oW0 = 2 * STAGE;  // kd'^T [d][r] (G1, A block 0)
+constexpr int oW1 = oW0 + TILE; // qd'^T [d][r] (G1, A block 1)
+constexpr int oW2 = oW1 + TILE; // ki'^T [d][s] (G1, B) -> W^T bf16 [d][s]
+constexpr int oP = oW2 + TILE;  // P [r][s] bf16
+constexpr int oT = oP + 8192;   // T [r][s] bf16
+constexpr int oA = oT + 8192;   // A fp32 [64][65]
+constexpr int oTf = oA + CH * LDF * 4;
+constexpr int oTmp = oTf + CH * LDF * 4;
+constexpr int oSmall = (oTmp + 768 * 4 + 1023) / 1024 * 1024;
+static_assert(oTmp + 768 * 4 <= oSmall, "inversion scratch overlaps the small arrays");
+constexpr int nInvQ = 64, nInvK = 64, nBeta = 64, nFac = 256, nGate = 128, nRef = 128, nGT = 128, nScan = 512;
+constexpr int SMALL_FLOATS = nInvQ + nInvK + nBeta + nFac + nGate + nRef + nGT + nScan;
+constexpr int SMEM_BYTES = oSmall + SMALL_FLOATS * 4 + 64 + 1024;
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+constexpr uint32_t R_G1 = 0, R_W = 64, R_U = 128, R_R = 192, R_Q = 256, R_K = 320, R_G = 384;
+
+struct PrepMaps {
+    CUtensorMap q, k, v;
+};
+
+}  // namespace
+
+template <bool KDA>
+__global__ void __launch_bounds__(512, 1) k_prep_tc(const Params p, const __grid_constant__ PrepMaps m) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    const uint32_t sb = smem_u32(smem);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // items (chunk, head) = chunk * H + h over the chunks that exist
+    const int total_chunks = p.chunk_off ? p.chunk_off[p.N] : p.N * (int)((p.seq_len + CH - 1) / CH);
+    const int n_items = total_chunks * p.H;
+    const int q4 = warp & 3, hc = warp >> 2;
+    const int L = 32 * q4 + lane;  // this thread's lane: a channel, or a stacked row of G1
+    const int c0 = 16 * hc;        // first of this thread's 16 rows
+
+    unsigned char *sW0 = smem + oW0, *sW1 = smem + oW1, *sW2 = smem + oW2, *sP = smem + oP, *sT = smem + oT;
+    float* sA = reinterpret_cast<float*>(smem + oA);
+    float* sTf = reinterpret_cast<float*>(smem + oTf);
+    float* sTmp = reinterpret_cast<float*>(smem + oTmp);
+    float* fsm = reinterpret_cast<float*>(smem + oSmall);
+    float* sInvQ = fsm;
+    float* sInvK = sInvQ + nInvQ;
+    float* sBeta = sInvK + nInvK;
+    float* sFac = sBeta + nBeta;  // GDN [4][64]
+    float* sGate = sFac + nFac;   // GDN gc[64], ref, gT
+    float* sRef = sGate + nGate;  // KDA ref[d]
+    float* sGT = sRef + nRef;     // KDA gT[d]
+    float* sScan = sGT + nGT;     // KDA [4][128]
+    uint64_t* mbars = reinterpret_cast<uint64_t*>(sScan + nScan);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbars + 3);
+    const uint32_t mb = smem_u32(mbars), mload0 = smem_u32(mbars + 1);  // load barriers: one per stage
+
+    Gates<PD, false> G;
+    G.gc = sGate;
+    G.ref = sGate + CH;
+    G.gT = sGate + CH + 1;
+
+    // q, k, v of item `it` into stage s (thread 0)
+    auto issue_loads = [&](int item, int stg) {
+        ChunkInfo cj;
+        lookup_chunk(item / p.H, p.N, p.chunk_off, p.cu_seqlens, p.seq_len, cj);
+        const int hh = item % p.H, t0 = (int)cj.t0;
+        const uint32_t bar = mload0 + 8 * stg, st = sb + stg * STAGE;
+        tc::mbar_expect_tx(bar, 3 * TILE);
+        tc::tma_load_4d(st + oQ, &m.q, 0, hh, t0, 0, bar);
+        tc::tma_load_4d(st + oK, &m.k, 0, hh, t0, 0, bar);
+        tc::tma_load_4d(st + oV, &m.v, 0, hh, t0, 0, bar);
+    };
+    if (warp == 0) tc::alloc(smem_u32(tslot), 512);
+    if (tid == 0) {
+        tc::mbar_init(mb, 1);
+        tc::mbar_init(mload0, 1);
+        tc::mbar_init(mload0 + 8, 1);
+        if ((int)blockIdx.x < n_items) issue_loads(blockIdx.x, 0);
+    }
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tmem = *tslot;
+    uint32_t phase = 0;
+    int it = 0;  // this CTA's item count (selects the stage)
+    auto tl = [&](uint32_t col) { return tmem + ((uint32_t)(32 * q4) << 16) + col; };
+    auto sync_all = [&]() {
+        tc::fence_async_smem();
+        tc::fence_before();
+        __syncthreads();
+        tc::fence_after();
+    };
+    int pending = -1;  // stage with a load in flight that this item does not consume, or -1
+    uint32_t pending_par = 0;
+    auto bail = [&]() {
+        if (tid == 0) {
+            atomicOr(p.status, ST_MMA_TIMEOUT);
+            if (pending >= 0) tc::mbar_wait(mload0 + 8 * pending, pending_par);  // bounded drain
+        }
+        tc::fence_before();
+        __syncthreads();
+        if (warp == 0) tc::dealloc(tmem, 512);
+    };
+    auto wait_mma = [&]() -> bool {
+        const bool ok = tc::mbar_wait(mb, phase);
+        phase ^= 1;
+        tc::fence_after();
+        if (__syncthreads_or(!ok)) {
+            bail();
+            return false;
+        }
+        return true;
+    };
+    auto rows16 = [&](const float* a, float (&o)[16]) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float4 v = *reinterpret_cast<const float4*>(a + c0 + 4 * i);
+            o[4 * i] = v.x;
+            o[4 * i + 1] = v.y;
+            o[4 * i + 2] = v.z;
+            o[4 * i + 3] = v.w;
+        }
+    };
+    auto pack8 = [&](const float (&v)[16], uint32_t (&w)[8]) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) w[e] = pack_bf16(v[2 * e], v[2 * e + 1]);
+    };
+    // row L, columns c0 .. c0+15 of a channel-major [128][64] shared tile
+    auto store_cm = [&](unsigned char* tile, const uint32_t (&w)[8]) {
+        *reinterpret_cast<uint4*>(tile + tc::sw_chunk(L, c0 >> 3, 128)) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(tile + tc::sw_chunk(L, (c0 >> 3) + 1, 128)) = make_uint4(w[4], w[5], w[6], w[7]);
+    };
+    // row L, columns c0 .. c0+15 of a chunk-head's channel-major [128][64] global tile
+    auto store_global_cm = [&](__nv_bfloat16* tile, const uint32_t (&w)[8]) {
+        uint4* g = reinterpret_cast<uint4*>(tile + (size_t)L * CH + c0);
+        g[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        g[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    };
+
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++it) {
+    const int chunk = item / p.H, h = item % p.H;
+    ChunkInfo ci;
+    lookup_chunk(chunk, p.N, p.chunk_off, p.cu_seqlens, p.seq_len, ci);
+    const int stg = it & 1;
+    unsigned char *sQ = smem + stg * STAGE + oQ, *sK = smem + stg * STAGE + oK, *sV = smem + stg * STAGE + oV;
+    const uint32_t sQa = sb + stg * STAGE + oQ, sKa = sb + stg * STAGE + oK;
+    const size_t tile_cd = ((size_t)chunk * p.H + h) * CH * PD;
+    const size_t tile_cc = ((size_t)chunk * p.H + h) * CH * CH;
+    // the next item's tiles into the other stage (its previous tenant finished last iteration)
+    pending = -1;
+    if (item + (int)gridDim.x < n_items) {
+        if (tid == 0) issue_loads(item + gridDim.x, stg ^ 1);
+        pending = stg ^ 1;
+        pending_par = (uint32_t)(((it + 1) >> 1) & 1);
+    }
+    if constexpr (!KDA) load_gates<PD, false, 512>(p, ci, h, G, true);
+    load_beta(p, ci, h, sBeta);
+
+    // KDA: per-channel log gates of this thread's channel and rows, scanned across the four
+    // row quarters, staged in tensor memory; the gate-range check of the chunk
+    float refL = 0.f, gTL = 0.f;
+    if constexpr (KDA) {
+        const float a = expf(p.A_log[h]);
+        const float bias = p.dt_bias[h * PD + L];
+        float g[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int r = c0 + i;
+            g[i] = r < ci.len ? bf2f(p.g_raw[((ci.t0 + r) * p.H + h) * PD + L]) : 0.f;
+        }
+        float acc = 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            if (c0 + i < ci.len) acc += -a * softplus_f(g[i] + bias);
+            g[i] = acc;
+        }
+        sScan[hc * PD + L] = acc;
+        __syncthreads();
+        float pre = 0.f, tot = 0.f;
+#pragma unroll
+        for (int h2 = 0; h2 < 4; ++h2) {
+            const float t = sScan[h2 * PD + L];
+            if (h2 < hc) pre += t;
+            tot += t;
+        }
+        float mx = -3.0e38f, mn = 3.0e38f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            g[i] += pre;
+            mx = fmaxf(mx, g[i]);
+            mn = fminf(mn, g[i]);
+        }
+        tc::st16(tl(R_G + c0), g);
+        __syncthreads();
+        sScan[hc * PD + L] = mx;
+        sTmp[hc * PD + L] = mn;  // the inversion scratch is not in use yet
+        __syncthreads();
+        if (hc == 0) {
+            float M = sScan[L], N = sTmp[L];
+#pragma unroll
+            for (int h2 = 1; h2 < 4; ++h2) {
+                M = fmaxf(M, sScan[h2 * PD + L]);
+                N = fminf(N, sTmp[h2 * PD + L]);
+            }
+            sRef[L] = 0.5f * (M + N);
+            sGT[L] = tot;
+            if (0.5f * (M - N) > 80.f || M > 80.f) atomicOr(p.status, ST_GATE_RANGE);
+        }
+    }
+
+    // operand tiles; rows past the chunk's end read as zero
+    {
+        const bool ok = tc::mbar_wait(mload0 + 8 * stg, (uint32_t)((it >> 1) & 1));
+        if (__syncthreads_or(!ok)) return bail();
+    }
+    if (ci.len < CH) {
+        const int nz = (CH - ci.len) * 16;
+        for (int i = tid; i < 3 * nz; i += 512) {
+            const int t = i / nz, rem = i % nz, r = ci.len + rem / 16, jc = rem % 16;
+            unsigned char* base = t == 0 ? sQ : t == 1 ? sK : sV;
+            *reinterpret_cast<uint4*>(base + tc::sw_chunk(r, jc, 64)) = make_uint4(0, 0, 0, 0);
+        }
+    }
+    __syncthreads();
+    if constexpr (KDA) {
+        refL = sRef[L];
+        gTL = sGT[L];
+    }
+    {  // inverse row norms of q and k, 4 threads per row
+        const int r = (tid >> 2) & 63, part = tid & 3;
+        const unsigned char* src = tid < 256 ? sQ : sK;
+        float s = 0.f;
+        for (int j = part * 4; j < part * 4 + 4; ++j) {
+            const uint4 v = *reinterpret_cast<const uint4*>(src + tc::sw_chunk(r, j, 64));
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 f = unpack_bf16(w[e]);
+                s += f.x * f.x + f.y * f.y;
+            }
+        }
+        s += __shfl_xor_sync(0xffffffffu, s, 1);
+        s += __shfl_xor_sync(0xffffffffu, s, 2);
+        if (part == 0) (tid < 256 ? sInvQ : sInvK)[r] = rsqrtf(s + 1e-6f);
+    }
+    if constexpr (!KDA) {
+        for (int r = tid; r < CH; r += 512) {
+            sFac[0 * CH + r] = gate_factor<F_KD>(G, r, 0);
+            sFac[1 * CH + r] = gate_factor<F_KDP>(G, r, 0);
+            sFac[2 * CH + r] = gate_factor<F_KIP>(G, r, 0);
+            sFac[3 * CH + r] = gate_factor<F_KR>(G, r, 0);
+        }
+    }
+    {  // raw q and k of this thread's channel and rows into tensor memory
+        const int lch = (L & 63) >> 3, lsub = (L & 7) << 1;
+        float qs[16], ks[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const uint32_t off = (uint32_t)((L >> 6) * 64 * 128 + (c0 + i) * 128 + ((lch ^ (i & 7)) << 4) + lsub);
+            qs[i] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(sQ + off));
+            ks[i] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(sK + off));
+        }
+        tc::st16(tl(R_Q + c0), qs);
+        tc::st16(tl(R_K + c0), ks);
+    }
+    __syncthreads();  // norms, factors and the q / k tile reads are done
+
+    auto factors = [&](int kind, float (&f)[16]) {
+        if constexpr (KDA) {
+            float g[16];
+            tc::ld16(tl(R_G + c0), g);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const float e = kind == F_KD ? g[i] : kind == F_KDP ? g[i] - refL : kind == F_KIP ? refL - g[i] : gTL - g[i];
+                f[i] = __expf(e);
+            }
+        } else {
+            rows16(sFac + kind * CH, f);
+        }
+    };
+    // x (raw q or k of this channel and rows) * m_r * f, m_r = inv_r * mul * rowmul_r
+    auto derived = [&](bool isq, float mul, const float* rowmul, int kind, float (&o)[16]) {
+        float f[16], inv[16], rm[16];
+        factors(kind, f);
+        tc::ld16(tl((isq ? R_Q : R_K) + c0), o);
+        rows16(isq ? sInvQ : sInvK, inv);
+        if (rowmul) rows16(rowmul, rm);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) o[i] = o[i] * derived_m(inv[i], mul, rowmul ? rm[i] : 1.f) * f[i];
+    };
+    auto build = [&](unsigned char* tile, bool isq, float mul, const float* rowmul, int kind) {
+        float v[16];
+        uint32_t w[8];
+        derived(isq, mul, rowmul, kind, v);
+        pack8(v, w);
+        store_cm(tile, w);
+    };
+
+    // ---- G1: [A_raw; P] = [kd'; qd'] ki'^T ----------------------------------------------
+    build(sW0, false, 1.f, nullptr, F_KDP);
+    build(sW1, true, p.scale, nullptr, F_KDP);
+    build(sW2, false, 1.f, nullptr, F_KIP);
+    sync_all();
+    if (tid == 0) {
+        constexpr uint32_t id = tc::idesc(128, 64, 1, 1);
+        for (int k = 0; k < PD; k += 16)
+            tc::mma(tmem + R_G1, tc::mdesc(sb + oW0, 128, 0, k), tc::mdesc(sb + oW2, 128, 0, k), id, k > 0);
+        tc::commit(mb);
+    }
+    if (!wait_mma()) return;
+    {
+        float v[16];
+        tc::ld16(tl(R_G1 + c0), v);
+        if (L < 64) {  // A = strict_lower(beta A_raw), fp32 for the inversion
+            const int r = L;
+            const float br = sBeta[r];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) sA[r * LDF + c0 + i] = c0 + i < r ? br * v[i] : 0.f;
+        } else {  // P = lower(qd' ki'^T), bf16 [r][s]
+            const int r = L - 64;
+            uint32_t w[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int s0 = c0 + 2 * e;
+                w[e] = pack_bf16(s0 <= r ? v[2 * e] : 0.f, s0 + 1 <= r ? v[2 * e + 1] : 0.f);
+            }
+            *reinterpret_cast<uint4*>(sP + tc::sw_chunk(r, c0 >> 3, 64)) = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4*>(sP + tc::sw_chunk(r, (c0 >> 3) + 1, 64)) = make_uint4(w[4], w[5], w[6], w[7]);
+        }
+    }
+    __syncthreads();
+    invert_unit_lower64<512>(sA, sTf, sTmp);  // ends with __syncthreads
+    for (int i = tid; i < CH * CH / 2; i += 512) {
+        const int r = i / (CH / 2), c = 2 * (i % (CH / 2));
+        const uint32_t w = pack_bf16(sTf[r * LDF + c], sTf[r * LDF + c + 1]);
+        *reinterpret_cast<uint32_t*>(sT + tc::sw_off(r, c, 64)) = w;
+        *reinterpret_cast<uint32_t*>(p.Tm + tile_cc + r * CH + c) = w;
+    }
+    // (beta kd)^T -> the q tile's space ; (beta V)^T -> the k tile's space
+    build(sQ, false, 1.f, sBeta, F_KD);
+    {
+        float v[16], bt[16];
+        uint32_t w[8];
+        rows16(sBeta, bt);
+        const int lch = (L & 63) >> 3, lsub = (L & 7) << 1;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const uint32_t off = (uint32_t)((L >> 6) * 64 * 128 + (c0 + i) * 128 + ((lch ^ (i & 7)) << 4) + lsub);
+            v[i] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(sV + off)) * bt[i];
+        }
+        pack8(v, w);
+        store_cm(sK, w);
+    }
+    sync_all();
+
+    // ---- W^T = (beta kd)^T T^T ; U^T = (beta V)^T T^T --------------------------------------
+    if (tid == 0) {
+        constexpr uint32_t id = tc::idesc(128, 64, 0, 0);
+        for (int k = 0; k < CH; k += 16)
+            tc::mma(tmem + R_W, tc::kdesc(sQa, 128, 0, k), tc::kdesc(sb + oT, 64, 0, k), id, k > 0);
+        for (int k = 0; k < CH; k += 16)
+            tc::mma(tmem + R_U, tc::kdesc(sKa, 128, 0, k), tc::kdesc(sb + oT, 64, 0, k), id, k > 0);
+        tc::commit(mb);
+    }
+    if (!wait_mma()) return;
+    {
+        float v[16];
+        uint32_t w[8];
+        tc::ld16(tl(R_W + c0), v);
+        pack8(v, w);
+        store_global_cm(p.W + tile_cd, w);
+        store_cm(sW2, w);  // bf16 W^T, the A operand of W^T P^T (ki' is dead)
+        tc::ld16(tl(R_U + c0), v);
+        pack8(v, w);
+        store_global_cm(p.U + tile_cd, w);
+    }
+    sync_all();
+
+    // ---- R^T = qd^T - W^T P^T ----------------------------------------------------------------
+    if (tid == 0) {
+        constexpr uint32_t id = tc::idesc(128, 64, 0, 0);
+        for (int k = 0; k < CH; k += 16)
+            tc::mma(tmem + R_R, tc::kdesc(sb + oW2, 128, 0, k), tc::kdesc(sb + oP, 64, 0, k), id, k > 0);
+        tc::commit(mb);
+    }
+    // while the tensor cores run: kr = kn e^{gT-gc} ; gT, e^{gT}
+    {
+        float v[16];
+        uint32_t w[8];
+        derived(false, 1.f, nullptr, F_KR, v);
+        pack8(v, w);
+        store_global_cm(p.Kr + tile_cd, w);
+        if (hc == 0) {
+            const float gt = KDA ? gTL : G.gTv(0);
+            p.gT[((size_t)chunk * p.H + h) * PD + L] = gt;
+            p.egT[((size_t)chunk * p.H + h) * PD + L] = __expf(gt);
+        }
+    }
+    if (!wait_mma()) return;
+    {
+        float acc[16], qd[16];
+        uint32_t w[8], wl[8];
+        tc::ld16(tl(R_R + c0), acc);
+        derived(true, p.scale, nullptr, F_KD, qd);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float r0 = qd[2 * e] - acc[2 * e], r1 = qd[2 * e + 1] - acc[2 * e + 1];
+            w[e] = pack_bf16(r0, r1);
+            const float2 hf = unpack_bf16(w[e]);
+            wl[e] = pack_bf16(r0 - hf.x, r1 - hf.y);
+        }
+        store_global_cm(p.R + tile_cd, w);
+        store_global_cm(p.Rlo + tile_cd, wl);
+    }
+    tc::fence_before();
+    __syncthreads();  // this item's shared tiles and tensor memory are free
+    tc::fence_after();
+    }
+    tc::fence_before();
+    __syncthreads();
+    if (warp == 0) tc::dealloc(tmem, 512);
+}
+
+template <bool KDA>
+static cudaError_t launch_prep_tc_t(const Params& p, cudaStream_t s) {
+    PrepMaps m;
+    const uint64_t T = (uint64_t)p.T_total;
+    if (!(encode_blocked_tokens_map(&m.q, p.q, T, p.H) && encode_blocked_tokens_map(&m.k, p.k, T, p.H) &&
+          encode_blocked_tokens_map(&m.v, p.v, T, p.H)))
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(k_prep_tc<KDA>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    const int items = p.max_chunks * p.H;
+    const int ctas = items < num_sms() ? items : num_sms();
+    k_prep_tc<KDA><<<ctas, 512, SMEM_BYTES, s>>>(p, m);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_prep_tc(const Params& p, cudaStream_t s) {
+    return p.kda ? launch_prep_tc_t<true>(p, s) : launch_prep_tc_t<false>(p, s);
+}
+
+}  // namespace gdr

@@ -33,7 +33,8 @@ namespace {
 constexpr int SD = 128;
 constexpr int TILE = CH * SD * 2;       // one C x D bf16 tile, 16 KB
 constexpr int oEG = 5 * TILE;           // within a stage: e^{gT} row (fp32 [D])
-constexpr int STAGE = 5 * TILE + 1024;  // role 0: W, kr, U^T ; role 1: kr, W, R_hi, R_lo, dO
+constexpr int STAGE = 5 * TILE + 1024;  // role 0: W^T, kr^T, U^T ; role 1: kr^T, W^T, R_hi^T, R_lo^T, dO
+// (the per-chunk tiles of the prep kernel are channel-major [D][C]; dO is token-major)
 constexpr int oBS = 2 * STAGE;          // bf16 S^T   [128 rows j][128 cols d]
 constexpr int oBY = oBS + 2 * TILE;     // bf16 (U - X)^T or -Y^T [128 rows j][64 cols t]
 constexpr int oBar = oBY + TILE;        // full[2], y, z mbarriers; tmem slot; abort flag
@@ -105,15 +106,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_states_tc(const Params p, int r
             const uint32_t st = sb + (it & 1) * STAGE, bar = full_bar(it);
             const int row = (c * p.H + h) * CH;
             tc::mbar_expect_tx(bar, (role == 0 ? 3 : 5) * TILE + SD * 4);
+            // channel-major tiles: 128 rows x 64 columns, one box each
             if (role == 0) {
-                tc::tma_load_3d(st, &m.W, 0, row, 0, bar);
-                tc::tma_load_3d(st + TILE, &m.Kr, 0, row, 0, bar);
-                tc::tma_load_2d(st + 2 * TILE, &m.Ut, 0, 2 * row, bar);  // U^T: 128 rows x 64 columns
+                tc::tma_load_2d(st, &m.W, 0, 2 * row, bar);
+                tc::tma_load_2d(st + TILE, &m.Kr, 0, 2 * row, bar);
+                tc::tma_load_2d(st + 2 * TILE, &m.Ut, 0, 2 * row, bar);
             } else {
-                tc::tma_load_3d(st, &m.Kr, 0, row, 0, bar);
-                tc::tma_load_3d(st + TILE, &m.W, 0, row, 0, bar);
-                tc::tma_load_3d(st + 2 * TILE, &m.R, 0, row, 0, bar);
-                tc::tma_load_3d(st + 3 * TILE, &m.Rlo, 0, row, 0, bar);
+                tc::tma_load_2d(st, &m.Kr, 0, 2 * row, bar);
+                tc::tma_load_2d(st + TILE, &m.W, 0, 2 * row, bar);
+                tc::tma_load_2d(st + 2 * TILE, &m.R, 0, 2 * row, bar);
+                tc::tma_load_2d(st + 3 * TILE, &m.Rlo, 0, 2 * row, bar);
                 // rows past the sequence end are read too: they meet zero rows of R_hi / R_lo
                 const int t0 = (int)(bos + (int64_t)(c - cb) * CH);
                 tc::tma_load_4d(st + 4 * TILE, &m.dO, 0, h, t0, 0, bar);
@@ -160,6 +162,21 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_states_tc(const Params p, int r
         }
     } else if (warp == MMA_WARP) {
         // ---------------- MMA warp: every tcgen05.mma is issued by lane 0 ----------------
+        // Role 1's state-independent products dO^T R_hi and dO^T R_lo fill the tensor pipe
+        // while the consumers work: R_hi of a chunk right after its Y^T product (during the
+        // element-wise step on Y), R_lo of the next chunk right after the update product
+        // (during the state update); R_lo initialises the chunk's accumulator.
+        constexpr uint32_t idr = tc::idesc(128, 128, 1, 0);
+        auto r_part = [&](int j, int tile, uint32_t acc) {
+            const uint32_t stj = sb + (j & 1) * STAGE, zj = tmem + ((j & 1) ? R_Z1 : R_Z0);
+            for (int k = 0; k < CH; k += 16)
+                tc::mma(zj, tc::mdesc(stj + 4 * TILE, CH, 0, k), tc::kdesc(stj + tile * TILE, SD, 0, k), idr,
+                        acc || k > 0);
+        };
+        if (role == 1 && lane == 0 && n > 0) {
+            wait(full_bar(0), full_par(0));
+            if (!failed()) r_part(0, 3, 0);
+        }
         for (int it = 0; it < n; ++it) {
             const uint32_t st = sb + (it & 1) * STAGE;
             const uint32_t z = tmem + ((it & 1) ? R_Z1 : R_Z0);
@@ -169,18 +186,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_states_tc(const Params p, int r
                 wait(full_bar(it), full_par(it));
                 if (!failed()) {
                     // X^T = S^T W^T (role 0) or Y^T = dS^T kr^T (role 1): B = the stage's first tile
-                    constexpr uint32_t idy = tc::idesc(128, 64, 0, 0);
+                    constexpr uint32_t idy = tc::idesc(128, 64, 0, 1);
                     for (int k = 0; k < SD; k += 16)
-                        tc::mma(tmem + R_Y, tc::kdesc(sb + oBS, SD, 0, k), tc::kdesc(st, CH, 0, k), idy, k > 0);
+                        tc::mma(tmem + R_Y, tc::kdesc(sb + oBS, SD, 0, k), tc::mdesc(st, SD, 0, k), idy, k > 0);
                     tc::commit(mby);
-                    if (role == 1) {  // dO^T R_hi + dO^T R_lo (independent of the state)
-                        constexpr uint32_t idr = tc::idesc(128, 128, 1, 1);
-                        for (int k = 0; k < CH; k += 16)
-                            tc::mma(z, tc::mdesc(st + 4 * TILE, CH, 0, k), tc::mdesc(st + 2 * TILE, CH, 0, k), idr,
-                                    k > 0);
-                        for (int k = 0; k < CH; k += 16)
-                            tc::mma(z, tc::mdesc(st + 4 * TILE, CH, 0, k), tc::mdesc(st + 3 * TILE, CH, 0, k), idr, 1);
-                    }
+                    if (role == 1) r_part(it, 2, 1);  // + dO^T R_hi
                 }
             }
             __syncwarp();
@@ -188,10 +198,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_states_tc(const Params p, int r
             tc::fence_after();
             if (lane == 0 && !failed()) {
                 // role 0: Z = (U - X)^T kr ; role 1: Z += (-Y^T) W   (B = the stage's second tile)
-                constexpr uint32_t idz = tc::idesc(128, 128, 0, 1);
+                constexpr uint32_t idz = tc::idesc(128, 128, 0, 0);
                 for (int k = 0; k < CH; k += 16)
-                    tc::mma(z, tc::kdesc(sb + oBY, SD, 0, k), tc::mdesc(st + TILE, CH, 0, k), idz, role == 1 || k > 0);
+                    tc::mma(z, tc::kdesc(sb + oBY, SD, 0, k), tc::kdesc(st + TILE, SD, 0, k), idz, role == 1 || k > 0);
                 tc::commit(mbz);
+                if (role == 1 && it + 1 < n) {  // the next chunk's dO^T R_lo (its consumers read that buffer last step)
+                    wait(full_bar(it + 1), full_par(it + 1));
+                    if (!failed()) r_part(it + 1, 3, 0);
+                }
             }
             __syncwarp();
         }
@@ -289,10 +303,10 @@ cudaError_t launch_states_tc(const Params& p, bool fwd, bool bwd, cudaStream_t s
     StateMaps m;
     const uint64_t rows = (uint64_t)p.max_chunks * p.H * CH;  // C x D tiles
     const uint64_t srows = (uint64_t)p.max_chunks * p.H * SD;  // D x D states
-    bool ok = encode_blocked_rows_map(&m.W, p.W, rows, CH) && encode_blocked_rows_map(&m.Kr, p.Kr, rows, CH) &&
+    bool ok = encode_rows_map(&m.W, p.W, srows, CH, SD) && encode_rows_map(&m.Kr, p.Kr, srows, CH, SD) &&
               encode_rows_map(&m.Ut, fwd ? p.U : nullptr, srows, CH, SD) &&
-              encode_blocked_rows_map(&m.R, bwd ? p.R : nullptr, rows, CH) &&
-              encode_blocked_rows_map(&m.Rlo, bwd ? p.Rlo : nullptr, rows, CH) &&
+              encode_rows_map(&m.R, bwd ? p.R : nullptr, srows, CH, SD) &&
+              encode_rows_map(&m.Rlo, bwd ? p.Rlo : nullptr, srows, CH, SD) &&
               encode_blocked_tokens_map(&m.dO, bwd ? p.dO : nullptr, (uint64_t)p.T_total, p.H) &&
               encode_blocked_rows_map(&m.S0, fwd ? p.S0 : nullptr, srows, SD) &&
               encode_blocked_rows_map(&m.dS, bwd ? p.dS : nullptr, srows, SD);
