@@ -28,6 +28,36 @@ struct Gates {
     static constexpr int floats() { return KDA ? CH * LDG + 2 * D : CH + 2; }
 };
 
+// GDN gate of one chunk by the first warp: lane l holds g of rows 2l and 2l + 1 (0 past
+// the chunk's end); writes gc (inclusive cumsum), gT and ref = (max gc + min gc) / 2.
+template <int D>
+__device__ __forceinline__ void gdn_gate_scan(float g0, float g1, const Gates<D, false>& G, bool flag_range,
+                                              const Params& p) {
+    const int lane = threadIdx.x & 31, r0 = 2 * lane;
+    const float s = g0 + g1;
+    float incl = s;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    const float excl = incl - s;
+    G.gc[r0] = excl + g0;
+    G.gc[r0 + 1] = incl;
+    float mx = fmaxf(excl + g0, incl), mn = fminf(excl + g0, incl);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    }
+    const float gT = __shfl_sync(0xffffffffu, incl, 31);
+    if (lane == 0) {
+        G.gT[0] = gT;
+        G.ref[0] = 0.5f * (mx + mn);
+        if (flag_range && (0.5f * (mx - mn) > 80.f || mx > 80.f)) atomicOr(p.status, ST_GATE_RANGE);
+    }
+}
+
 // Computes gc, gT and ref for one (chunk, head).  Rows >= len have g = 0.
 // Must be called by every thread of the block (it synchronises); NT = blockDim.x.
 template <int D, bool KDA, int NT = 256>
@@ -77,32 +107,10 @@ __device__ void load_gates(const Params& p, const ChunkInfo& ci, int h, const Ga
         }
     } else {
         if (threadIdx.x < 32) {
-            const int lane = threadIdx.x;
-            const int r0 = 2 * lane;
+            const int r0 = 2 * threadIdx.x;
             const float g0 = r0 < ci.len ? p.g[(ci.t0 + r0) * p.H + h] : 0.f;
             const float g1 = r0 + 1 < ci.len ? p.g[(ci.t0 + r0 + 1) * p.H + h] : 0.f;
-            const float s = g0 + g1;
-            float incl = s;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                float t = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += t;
-            }
-            const float excl = incl - s;
-            G.gc[r0] = excl + g0;
-            G.gc[r0 + 1] = incl;
-            float mx = fmaxf(excl + g0, incl), mn = fminf(excl + g0, incl);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-                mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-            }
-            const float gT = __shfl_sync(0xffffffffu, incl, 31);
-            if (lane == 0) {
-                G.gT[0] = gT;
-                G.ref[0] = 0.5f * (mx + mn);
-                if (flag_range && (0.5f * (mx - mn) > 80.f || mx > 80.f)) atomicOr(p.status, ST_GATE_RANGE);
-            }
+            gdn_gate_scan(g0, g1, G, flag_range, p);
         }
     }
 }

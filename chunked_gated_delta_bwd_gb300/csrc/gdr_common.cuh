@@ -213,5 +213,19 @@ __device__ __forceinline__ float softplus_f(float x) {
     return fmaxf(x, 0.f) + l;
 }
 __device__ __forceinline__ float sigmoid_f(float x) { return __fdividef(1.f, 1.f + __expf(-x)); }
+// softplus(x) (as softplus_f) and sigmoid(x) from one exponential y = e^{-|x|}:
+// sigmoid = 1 / (1 + y) for x >= 0, y / (1 + y) otherwise.
+__device__ __forceinline__ void softplus_sigmoid(float x, float& sp, float& sg) {
+    const float y = __expf(-fabsf(x));
+    float l;
+    if (y >= 0.0625f) {
+        l = __logf(1.f + y);
+    } else {
+        l = y * (1.f - y * (0.5f - y * (1.f / 3.f - y * (0.25f - y * (0.2f - y * (1.f / 6.f))))));
+    }
+    sp = fmaxf(x, 0.f) + l;
+    const float inv = __fdividef(1.f, 1.f + y);
+    sg = x >= 0.f ? inv : y * inv;
+}
 
 }  // namespace gdr

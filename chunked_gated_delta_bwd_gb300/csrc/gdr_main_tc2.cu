@@ -41,24 +41,25 @@ constexpr int oDOY = 32768;     // [dO; dY] token-major, 128 rows
 constexpr int oS0 = 65536;      // S0 [j][d]          -> kd' [d][r] (+ lo at +16 KB)
 constexpr int oDS = 98304;      // dS [j][d]          -> [dP; beta dA] [m][s] (+ lo at +16 KB)
 constexpr int oT = 131072;      // T  [r][s]
-constexpr int oA = 139264;      // beta A_raw, strict lower [r][s]
+constexpr int oA = 139264;      // beta A_raw, strict lower [r][s]   -> (KDA) raw gate tile, with P's space
 constexpr int oP = 147456;      // P, lower [r][s]
-constexpr int oW0 = 155648;     // kd' [d][r] (G1, A block 0) -> kd [d][r] -> (KDA) u^T lo -> ki' [d][r]
+constexpr int oW0 = 155648;     // (KDA) raw gate tile -> kd' [d][r] (G1, A block 0) -> kd [d][r]
+                                //   -> (KDA) u^T lo -> ki' [d][r]
 constexpr int oW1 = 172032;     // qd' [d][r] (G1, A block 1) -> u^T [j][r] -> (KDA) ki' lo
 constexpr int oW2 = 188416;     // q (token-major) -> ki' [d][r] -> kr [d][r] -> du^T -> qd' [d][r]
 constexpr int oSmall = 204800;
 // small arrays (floats)
 constexpr int NCOL = 16;  // rows per thread (16 warps: 4 lane quarters x 4 row quarters)
 constexpr int nInvQ = 64, nInvK = 64, nBeta = 64, nFac = 256, nGate = 128, nRef = 128, nGT = 128,
-              nScan = 512, nDgTs = 128, nDgTp = 512, nDbP = 64, nDbA = 256, nRow = 256 * 3, nMisc = 64;
+              nScan = 512, nDgTs = 128, nDgTp = 512, nDbP = 64, nDbA = 256, nRow = 256 * 3, nMisc = 64, nTot = 128;
 constexpr int SMALL_FLOATS =
-    nInvQ + nInvK + nBeta + nFac + nGate + nRef + nGT + nScan + nDgTs + nDgTp + nDbP + nDbA + nRow + nMisc;
+    nInvQ + nInvK + nBeta + nFac + nGate + nRef + nGT + nScan + nDgTs + nDgTp + nDbP + nDbA + nRow + nMisc + nTot;
 constexpr int SMEM_BYTES = oSmall + SMALL_FLOATS * 4 + 64 + 1024;  // + mbarriers / tmem slot + alignment
 // tensor-memory columns
 constexpr uint32_t R_A = 0, R_B = 128, R_C = 192, R_D = 256, R_Q = 320, R_K = 384, R_G = 448;
 
 struct MainMaps {
-    CUtensorMap q, k, v, dO, S0, dS, T;
+    CUtensorMap q, k, v, dO, S0, dS, T, graw;
 };
 
 __device__ __forceinline__ float warp_sum(float x) {
@@ -133,9 +134,11 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
     float* sDbA = sDbP + nDbP;       // [4][64] rowsum(dA . A) per column quarter
     float* sRow = sDbA + nDbA;       // [3][4][64] row reductions (and KDA partials)
     float* sMisc = sRow + nRow;      // [64]
-    uint64_t* mbars = reinterpret_cast<uint64_t*>(sMisc + nMisc);
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbars + 2);
-    const uint32_t mb = smem_u32(mbars), mload = smem_u32(mbars + 1);
+    float* sTot = sMisc + nMisc;     // [2][64] row dots summed over the lane quarters (q, k)
+    uint64_t* mbars = reinterpret_cast<uint64_t*>(sTot + nTot);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbars + 3);
+    // MMA completion; operand tiles of an item; (KDA) the raw gate tile for the gate chain rule
+    const uint32_t mb = smem_u32(mbars), mload = smem_u32(mbars + 1), mgr = smem_u32(mbars + 2);
 
     Gates<MD, false> G;  // GDN scalar gates
     G.gc = sGate;
@@ -147,7 +150,8 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
         ChunkInfo cj;
         lookup_chunk(item / p.H, p.N, p.chunk_off, p.cu_seqlens, p.seq_len, cj);
         const int hh = item % p.H, t0 = (int)cj.t0, rcd = item * CH, rdd = item * MD;
-        tc::mbar_expect_tx(mload, 4 * TILE + 2 * 2 * TILE + CH * CH * 2);
+        tc::mbar_expect_tx(mload, 4 * TILE + 2 * 2 * TILE + CH * CH * 2 + (KDA ? TILE : 0));
+        if (KDA) tc::tma_load_4d(sb + oW0, &m.graw, 0, hh, t0, 0, mload);  // raw gates (token-major)
         tc::tma_load_4d(sb + oK, &m.k, 0, hh, t0, 0, mload);
         tc::tma_load_4d(sb + oV, &m.v, 0, hh, t0, 0, mload);
         tc::tma_load_4d(sb + oW2, &m.q, 0, hh, t0, 0, mload);
@@ -163,6 +167,7 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
     if (tid == 0) {
         tc::mbar_init(mb, 1);
         tc::mbar_init(mload, 1);
+        tc::mbar_init(mgr, 1);
         if ((int)blockIdx.x < n_items) issue_loads(blockIdx.x);
     }
     tc::fence_before();
@@ -172,6 +177,23 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
     uint32_t phase = 0;
     int it = 0;              // this CTA's item count (the load barrier's phase)
     bool pending = (int)blockIdx.x < n_items;  // a load batch is in flight
+    bool pending_g = false;                    // (KDA) a raw gate tile is in flight
+    // the next item's GDN gate (first warp, rows 2 lane and 2 lane + 1) and beta logit
+    // (thread r < 64), loaded one item ahead
+    float pg0 = 0.f, pg1 = 0.f, pb = 0.f;
+    auto prefetch_small = [&](int item) {
+        if (tid >= CH) return;
+        ChunkInfo cj;
+        lookup_chunk(item / p.H, p.N, p.chunk_off, p.cu_seqlens, p.seq_len, cj);
+        const int hh = item % p.H;
+        pb = tid < cj.len ? bf2f(p.beta_logit[(cj.t0 + tid) * p.H + hh]) : 0.f;
+        if (!KDA && tid < 32) {
+            const int r0 = 2 * tid;
+            pg0 = r0 < cj.len ? p.g[(cj.t0 + r0) * p.H + hh] : 0.f;
+            pg1 = r0 + 1 < cj.len ? p.g[(cj.t0 + r0 + 1) * p.H + hh] : 0.f;
+        }
+    };
+    if ((int)blockIdx.x < n_items) prefetch_small(blockIdx.x);
     auto sync_all = [&]() {  // make smem writes visible to the tensor cores and order TMEM use
         tc::fence_async_smem();
         tc::fence_before();
@@ -185,6 +207,7 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
         if (tid == 0) {
             atomicOr(p.status, ST_MMA_TIMEOUT);
             if (pending) tc::mbar_wait(mload, (uint32_t)(it & 1));  // bounded drain of the loads in flight
+            if (pending_g) tc::mbar_wait(mgr, (uint32_t)(it & 1));
         }
         tc::fence_before();
         __syncthreads();
@@ -238,20 +261,30 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
     const int chunk = item / p.H, h = item % p.H;
     ChunkInfo ci;
     lookup_chunk(chunk, p.N, p.chunk_off, p.cu_seqlens, p.seq_len, ci);
-    if constexpr (!KDA) load_gates<MD, false, 512>(p, ci, h, G, false);
-    load_beta(p, ci, h, sBeta);
+    if constexpr (!KDA)
+        if (tid < 32) gdn_gate_scan(pg0, pg1, G, false, p);
+    if (tid < CH) sBeta[tid] = tid < ci.len ? sigmoid_f(pb) : 0.f;
 
+    // wait for the operand tiles; rows past the chunk's end read as zero
+    {
+        const bool ok = tc::mbar_wait(mload, (uint32_t)(it & 1));
+        if (__syncthreads_or(!ok)) return bail();
+        pending = false;
+    }
     // KDA: per-channel log gates of this thread's channel and rows, scanned across the four
     // row quarters, staged in tensor memory (lane = channel, column = row)
     float refL = 0.f, gTL = 0.f;
     if constexpr (KDA) {
         const float a = expf(p.A_log[h]);
         const float bias = p.dt_bias[h * MD + L];
-        float g[16];
+        float g[16];  // raw gates of this channel and rows, from the token-major tile in W0
+        {
+            const int lch = (L & 63) >> 3, lsub = (L & 7) << 1;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const int r = c0 + i;
-            g[i] = r < ci.len ? bf2f(p.g_raw[((ci.t0 + r) * p.H + h) * MD + L]) : 0.f;
+            for (int i = 0; i < 16; ++i) {
+                const uint32_t off = (uint32_t)((L >> 6) * 64 * 128 + (c0 + i) * 128 + ((lch ^ (i & 7)) << 4) + lsub);
+                g[i] = c0 + i < ci.len ? __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(sW0 + off)) : 0.f;
+            }
         }
         float acc = 0.f;
 #pragma unroll
@@ -292,12 +325,6 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
         }
     }
 
-    // wait for the operand tiles; rows past the chunk's end read as zero
-    {
-        const bool ok = tc::mbar_wait(mload, (uint32_t)(it & 1));
-        if (__syncthreads_or(!ok)) return bail();
-        pending = false;
-    }
     if (ci.len < CH) {
         const int nz = (CH - ci.len) * 16;  // 16-byte chunks per 64-row tile (2 blocks x 8)
         for (int i = tid; i < 4 * nz; i += 512) {
@@ -667,6 +694,13 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
     build(sW2, KDA ? sK : nullptr, true, p.scale, F_KDP);
     build(sS0, KDA ? sS0 + TILE : nullptr, false, 1.f, F_KDP);
     sync_all();
+    if (KDA) {  // the raw gates again, for the gate chain rule, into the dead A and P tiles
+        if (tid == 0) {
+            tc::mbar_expect_tx(mgr, TILE);
+            tc::tma_load_4d(sb + oA, &m.graw, 0, h, (int)ci.t0, 0, mgr);
+        }
+        pending_g = true;
+    }
 
     // ---- G10: [dqd', dkd']^T = ki'^T [dP; beta dA]^T ; G11: dki'^T = qd'^T dP + kd'^T (beta dA) --
     if (tid == 0) {
@@ -700,6 +734,7 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
     if (item + (int)gridDim.x < n_items) {
         if (tid == 0) issue_loads(item + gridDim.x);
         pending = true;
+        prefetch_small(item + gridDim.x);
     }
     // the gate-gradient term takes the derived-tile value the products consumed: the bf16
     // element (GDN) or the fp32 value of the hi + lo pair (KDA)
@@ -754,23 +789,29 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
         (lane < 16 ? sRowQ : sRowK)[q4 * CH + c0 + (lane & 15)] = s;
     }
     __syncthreads();
+    if (tid < 2 * CH) {  // sums over the four lane quarters, once per row
+        const float* part = tid < CH ? sRowQ : sRowK;
+        const int r = tid & (CH - 1);
+        sTot[tid] = ((part[r] + part[CH + r]) + part[2 * CH + r]) + part[3 * CH + r];
+    }
+    __syncthreads();
     {
-        float x[16], inv[16];
+        float x[16], inv[16], tt[16];
         load_x(true, x, inv);
+        rows16(sTot, tt);
 #pragma unroll
         for (int i = 0; i < NCOL; ++i) {
             const int r = c0 + i;
-            const float tq = ((sRowQ[r] + sRowQ[CH + r]) + sRowQ[2 * CH + r]) + sRowQ[3 * CH + r];
             if (r < ci.len)
-                p.dq[((ci.t0 + r) * p.H + h) * MD + L] = __float2bfloat16((dQn[i] - x[i] * inv[i] * tq) * inv[i]);
+                p.dq[((ci.t0 + r) * p.H + h) * MD + L] = __float2bfloat16((dQn[i] - x[i] * inv[i] * tt[i]) * inv[i]);
         }
         load_x(false, x, inv);
+        rows16(sTot + CH, tt);
 #pragma unroll
         for (int i = 0; i < NCOL; ++i) {
             const int r = c0 + i;
-            const float tk = ((sRowK[r] + sRowK[CH + r]) + sRowK[2 * CH + r]) + sRowK[3 * CH + r];
             if (r < ci.len)
-                p.dk[((ci.t0 + r) * p.H + h) * MD + L] = __float2bfloat16((dKn[i] - x[i] * inv[i] * tk) * inv[i]);
+                p.dk[((ci.t0 + r) * p.H + h) * MD + L] = __float2bfloat16((dKn[i] - x[i] * inv[i] * tt[i]) * inv[i]);
         }
     }
     // dbeta (logit space)
@@ -805,10 +846,17 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
         // gate chain rule per element, with per-channel partial sums
         float xr[16];
         const float bias = p.dt_bias[h * MD + L];
+        {
+            const bool ok = tc::mbar_wait(mgr, (uint32_t)(it & 1));
+            if (__syncthreads_or(!ok)) return bail();
+            pending_g = false;
+            const unsigned char* gt = smem + oA;  // token-major raw gates (A and P spaces)
+            const int lch = (L & 63) >> 3, lsub = (L & 7) << 1;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const int r = c0 + i;
-            xr[i] = r < ci.len ? bf2f(p.g_raw[((ci.t0 + r) * p.H + h) * MD + L]) + bias : 0.f;
+            for (int i = 0; i < 16; ++i) {
+                const uint32_t off = (uint32_t)((L >> 6) * 64 * 128 + (c0 + i) * 128 + ((lch ^ (i & 7)) << 4) + lsub);
+                xr[i] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(gt + off)) + bias;
+            }
         }
         float acc = 0.f;
 #pragma unroll
@@ -828,11 +876,13 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
         for (int i = 0; i < 16; ++i) {
             const int r = c0 + i;
             if (r < ci.len) {
+                float sp, sg;
+                softplus_sigmoid(xr[i], sp, sg);
                 const float dgl = dGc[i] + post;
-                const float draw = dgl * (-ea * sigmoid_f(xr[i]));
+                const float draw = dgl * (-ea * sg);
                 p.dg_raw[((ci.t0 + r) * p.H + h) * MD + L] = __float2bfloat16(draw);
                 ddt += draw;
-                dA_acc += dgl * (-ea * softplus_f(xr[i]));
+                dA_acc += dgl * (-ea * sp);
             }
         }
         __syncthreads();  // suffix totals read
@@ -868,7 +918,8 @@ static cudaError_t launch_main_tc2_t(const Params& p, cudaStream_t s) {
     bool ok = encode_blocked_tokens_map(&m.q, p.q, T, p.H) && encode_blocked_tokens_map(&m.k, p.k, T, p.H) &&
               encode_blocked_tokens_map(&m.v, p.v, T, p.H) && encode_tokens_map(&m.dO, p.dO, T, p.H, MD) &&
               encode_blocked_rows_map(&m.S0, p.S0, rows_dd, MD) && encode_blocked_rows_map(&m.dS, p.dS, rows_dd, MD) &&
-              encode_rows_map(&m.T, p.Tm, rows_cc, CH, CH);
+              encode_rows_map(&m.T, p.Tm, rows_cc, CH, CH) &&
+              encode_blocked_tokens_map(&m.graw, KDA ? p.g_raw : nullptr, T, p.H);
     if (!ok) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(k_main_tc2<KDA>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
