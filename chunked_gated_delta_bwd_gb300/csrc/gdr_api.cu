@@ -75,7 +75,8 @@ cudaError_t launch_chunk_table(const Params& p, cudaStream_t s) {
 // ---------------------------------------------------------------------------
 struct Layout {
     int64_t max_chunks;
-    size_t status, chunk_off, W, U, Kr, R, Rlo, T, gT, egT, S0, dS, total;
+    size_t status, chunk_off, W, U, Kr, R, Rlo, T, gT, egT, S0, dS, segL, segLb, segP, segS, total;
+    int seg_G;
 };
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -94,6 +95,19 @@ static gdr_status check_shape(const gdr_shape* sh) {
     if (mc > (int64_t)1 << 30 || N * sh->num_heads * (sh->head_dim / 16) > ((int64_t)1 << 31) - 1)
         return fail(GDR_ERR_INVALID, "problem too large for one call");
     return GDR_OK;
+}
+
+// Segments of the time-parallel state passing (1 = the serial chains).  A function of the
+// shape only, sized for one wave of about 150 SMs: phase 1 runs 3G - 4 CTAs and phase 3
+// 2G CTAs per (sequence, head); each segment keeps at least 32 chunks.
+static int seg_count(const gdr_shape* sh, int64_t max_chunks) {
+    if (sh->head_dim != 128) return 1;
+    const int64_t pairs = (int64_t)sh->num_seqs * sh->num_heads;
+    const int64_t per_seq = max_chunks / sh->num_seqs;
+    int G = 1;
+    for (int g = 2; g <= 4; ++g)
+        if ((3 * g - 4) * pairs <= 148 && 2 * g * pairs <= 148 && per_seq >= 32 * g) G = g;
+    return G;
 }
 
 static Layout layout(const gdr_shape* sh) {
@@ -115,6 +129,12 @@ static Layout layout(const gdr_shape* sh) {
     L.egT = o; o = align256(o + mc * H * D * 4);
     L.S0 = o; o = align256(o + mc * H * D * D * 2);
     L.dS = o; o = align256(o + mc * H * D * D * 2);
+    L.seg_G = seg_count(sh, L.max_chunks);
+    const size_t segb = L.seg_G > 1 ? (size_t)N * H * L.seg_G * D * D * 4 : 0;  // fp32 [pair][G][D][D]
+    L.segL = o; o = align256(o + segb);
+    L.segLb = o; o = align256(o + segb);
+    L.segP = o; o = align256(o + segb);
+    L.segS = o; o = align256(o + 2 * segb);
     L.total = o;
     return L;
 }
@@ -155,6 +175,11 @@ static void base_params(Params& p, const gdr_shape* sh, const Layout& L, void* w
     p.egT = reinterpret_cast<float*>(w + L.egT);
     p.S0 = reinterpret_cast<__nv_bfloat16*>(w + L.S0);
     p.dS = reinterpret_cast<__nv_bfloat16*>(w + L.dS);
+    p.seg_G = L.seg_G;
+    p.segL = reinterpret_cast<float*>(w + L.segL);
+    p.segLb = reinterpret_cast<float*>(w + L.segLb);
+    p.segP = reinterpret_cast<float*>(w + L.segP);
+    p.segS = reinterpret_cast<float*>(w + L.segS);
 }
 
 // ---------------------------------------------------------------------------

@@ -32,6 +32,10 @@ struct Params {
     __nv_bfloat16 *W, *U, *Kr, *R, *Rlo, *Tm;
     float *gT, *egT;                     // [chunk][H][D]: chunk gate total and its exponential
     __nv_bfloat16 *S0, *dS;              // per chunk-head states, value-major [dv][dk]
+    // time-parallel state passing (seg_G > 1): per (sequence, head) and segment, fp32 key-major
+    // [D][D]: segment results from zero (role 0 / role 1), segment transitions, segment starts
+    int seg_G;
+    float *segL, *segLb, *segP, *segS;
 
     // outputs
     __nv_bfloat16 *dq, *dk, *dv, *dbeta;

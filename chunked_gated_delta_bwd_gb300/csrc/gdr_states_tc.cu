@@ -54,18 +54,89 @@ __device__ __forceinline__ int seq_chunk_begin(const Params& p, int seq) {
     return seq * (int)((p.seq_len + CH - 1) / CH);
 }
 
+// What one CTA runs: a chain over chunks [cb, ce) of one (sequence, head), walked upward
+// (role 0) or downward (role 1), from a start state (zero, the identity, or a key-major
+// [D][D] fp32 matrix), optionally saving the state entering each chunk, optionally with
+// the chunks' input terms (U, or R^T dO) -- without them the chain multiplies the
+// start state by the chunks' transitions -- and writing its final state key-major.
+struct StateTask {
+    int seq, h, role, cb, ce, input, save, identity;
+    const float* init;
+    float* out;
+};
+
+// Launch modes:
+//   0  one chain per (sequence, head, role) over the whole sequence (blockIdx.y = role)
+//   1  segment phase 1, 3G - 4 CTAs per (sequence, head): role 0 from segments 0 .. G-2
+//      (segment 0 from h0, the others from zero), role 1 from segments 1 .. G-1 (segment
+//      G-1 from dht, the others from zero), and the transitions of segments 1 .. G-2
+//   3  segment phase 3, 2G CTAs per (sequence, head): every segment of both roles from
+//      its true start state, saving the per-chunk states (and dh0)
+__device__ __forceinline__ StateTask decode_task(const Params& p, int mode, int role0) {
+    StateTask t;
+    const int G = p.seg_G, DD = 128 * 128;
+    int pair, g = 0, kind = 0;  // kind: 0 data chain, 1 transition chain
+    if (mode == 0) {
+        pair = blockIdx.x;
+        t.role = role0 + blockIdx.y;
+    } else if (mode == 1) {
+        const int K = 3 * G - 4, k = blockIdx.x % K;
+        pair = blockIdx.x / K;
+        if (k < G - 1) {
+            t.role = 0, g = k;
+        } else if (k < 2 * G - 2) {
+            t.role = 1, g = k - (G - 1) + 1;
+        } else {
+            t.role = 0, g = k - (2 * G - 2) + 1, kind = 1;
+        }
+    } else {
+        pair = blockIdx.x / (2 * G);
+        const int rem = blockIdx.x % (2 * G);
+        t.role = rem / G, g = rem % G;
+    }
+    t.seq = pair / p.H, t.h = pair % p.H;
+    const int cb = seq_chunk_begin(p, t.seq), ce = seq_chunk_begin(p, t.seq + 1);
+    const size_t pd = (size_t)pair * G;
+    t.input = kind == 0;
+    t.identity = kind == 1;
+    t.save = mode != 1;
+    t.out = nullptr;
+    if (mode == 0) {
+        t.cb = cb, t.ce = ce;
+        t.init = t.role == 0 ? (p.h0 ? p.h0 + (size_t)pair * DD : nullptr) : (p.dht ? p.dht + (size_t)pair * DD : nullptr);
+        if (t.role == 1) t.out = p.dh0 + (size_t)pair * DD;
+    } else {
+        const int len = (ce - cb + G - 1) / G;
+        t.cb = min(cb + g * len, ce), t.ce = min(cb + (g + 1) * len, ce);
+        const float* h0 = p.h0 ? p.h0 + (size_t)pair * DD : nullptr;
+        const float* dht = p.dht ? p.dht + (size_t)pair * DD : nullptr;
+        if (mode == 1) {
+            t.init = kind == 1 ? nullptr : t.role == 0 ? (g == 0 ? h0 : nullptr) : (g == G - 1 ? dht : nullptr);
+            t.out = (kind == 1 ? p.segP : t.role == 0 ? p.segL : p.segLb) + (pd + g) * DD;
+        } else {
+            if (t.role == 0)
+                t.init = g == 0 ? h0 : p.segS + ((pd + g) * 2 + 0) * DD;
+            else
+                t.init = g == G - 1 ? dht : p.segS + ((pd + g) * 2 + 1) * DD;
+            if (t.role == 1 && g == 0) t.out = p.dh0 + (size_t)pair * DD;
+        }
+    }
+    return t;
+}
+
 }  // namespace
 
-__global__ void __launch_bounds__(NTHREADS, 1) k_states_tc(const Params p, int role0,
+__global__ void __launch_bounds__(NTHREADS, 1) k_states_tc(const Params p, int mode, int role0,
                                                            const __grid_constant__ StateMaps m) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     const uint32_t sb = smem_u32(smem);
 
-    const int role = role0 + blockIdx.y;
-    const int seq = blockIdx.x / p.H, h = blockIdx.x % p.H;
-    const int cb = seq_chunk_begin(p, seq), ce = seq_chunk_begin(p, seq + 1);
+    const StateTask task = decode_task(p, mode, role0);
+    const int role = task.role, seq = task.seq, h = task.h;
+    const int cb = task.cb, ce = task.ce;
     const int n = ce - cb;
+    const int seq_cb = seq_chunk_begin(p, seq);  // the sequence's first chunk (token offsets)
     const int64_t bos = p.cu_seqlens ? p.cu_seqlens[seq] : (int64_t)seq * p.seq_len;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -105,19 +176,19 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_states_tc(const Params p, int r
             const int c = chunk_of(it);
             const uint32_t st = sb + (it & 1) * STAGE, bar = full_bar(it);
             const int row = (c * p.H + h) * CH;
-            tc::mbar_expect_tx(bar, (role == 0 ? 3 : 5) * TILE + SD * 4);
+            tc::mbar_expect_tx(bar, (task.input ? (role == 0 ? 3 : 5) : 2) * TILE + SD * 4);
             // channel-major tiles: 128 rows x 64 columns, one box each
             if (role == 0) {
                 tc::tma_load_2d(st, &m.W, 0, 2 * row, bar);
                 tc::tma_load_2d(st + TILE, &m.Kr, 0, 2 * row, bar);
-                tc::tma_load_2d(st + 2 * TILE, &m.Ut, 0, 2 * row, bar);
+                if (task.input) tc::tma_load_2d(st + 2 * TILE, &m.Ut, 0, 2 * row, bar);
             } else {
                 tc::tma_load_2d(st, &m.Kr, 0, 2 * row, bar);
                 tc::tma_load_2d(st + TILE, &m.W, 0, 2 * row, bar);
                 tc::tma_load_2d(st + 2 * TILE, &m.R, 0, 2 * row, bar);
                 tc::tma_load_2d(st + 3 * TILE, &m.Rlo, 0, 2 * row, bar);
                 // rows past the sequence end are read too: they meet zero rows of R_hi / R_lo
-                const int t0 = (int)(bos + (int64_t)(c - cb) * CH);
+                const int t0 = (int)(bos + (int64_t)(c - seq_cb) * CH);
                 tc::tma_load_4d(st + 4 * TILE, &m.dO, 0, h, t0, 0, bar);
             }
             tc::bulk_load(st + oEG, p.egT + ((size_t)c * p.H + h) * SD, SD * 4, bar);
@@ -141,7 +212,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_states_tc(const Params p, int r
             const int c = chunk_of(it);
             tc::named_sync(BAR_BS_READY, N_BS_READY);
             if (lane == 0) {
-                if (!failed()) {  // save the state entering this step (S0 of chunk c, or dS_C of chunk c)
+                if (task.save && !failed()) {  // save the state entering this step (S0 of chunk c, or dS_C of chunk c)
                     tc::tma_store_3d(role == 0 ? &m.S0 : &m.dS, 0, (c * p.H + h) * SD, 0, sb + oBS);
                     tc::bulk_commit();
                 }
@@ -214,13 +285,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_states_tc(const Params p, int r
         const int q4 = warp & 3, cg = warp >> 2;
         const int j = 32 * q4 + lane;  // tensor-memory lane = value row of S^T
         auto tl = [&](uint32_t col) { return tmem + ((uint32_t)(32 * q4) << 16) + col; };
-        float S[64];  // S^T[j][64 cg + i]
-        {
-            const float* init = role == 0 ? p.h0 : p.dht;
-            const size_t o = ((size_t)seq * p.H + h) * SD * SD + j;
+        float S[64];  // S^T[j][64 cg + i], from the key-major start state (or zero, or the identity)
 #pragma unroll
-            for (int i = 0; i < 64; ++i) S[i] = init ? init[o + (size_t)(64 * cg + i) * SD] : 0.f;
-        }
+        for (int i = 0; i < 64; ++i)
+            S[i] = task.init ? task.init[(size_t)(64 * cg + i) * SD + j] : (task.identity && 64 * cg + i == j ? 1.f : 0.f);
         for (int it = 0; it < n; ++it) {
             const unsigned char* stp = smem + (it & 1) * STAGE;
             const uint32_t z = (it & 1) ? R_Z1 : R_Z0;
@@ -256,7 +324,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_states_tc(const Params p, int r
                 tc::ld16(tl(R_Y + 32 * cg + 16 * qq), y);
                 const int jc = 4 * cg + 2 * qq;
                 uint32_t w[8];
-                if (role == 0) {  // (U - X)^T
+                if (role == 0 && task.input) {  // (U - X)^T
                     const uint4 u0 = *reinterpret_cast<const uint4*>(stp + 2 * TILE + tc::sw_chunk(j, jc, SD));
                     const uint4 u1 = *reinterpret_cast<const uint4*>(stp + 2 * TILE + tc::sw_chunk(j, jc + 1, SD));
                     const uint32_t uw[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
@@ -265,7 +333,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_states_tc(const Params p, int r
                         const float2 u = unpack_bf16(uw[e]);
                         w[e] = pack_bf16(u.x - y[2 * e], u.y - y[2 * e + 1]);
                     }
-                } else {  // -Y^T
+                } else {  // -Y^T (or -X^T of a transition chain)
 #pragma unroll
                     for (int e = 0; e < 8; ++e) w[e] = pack_bf16(-y[2 * e], -y[2 * e + 1]);
                 }
@@ -287,15 +355,71 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_states_tc(const Params p, int r
             }
             tc::fence_before();
         }
-        if (role == 1) {  // dh0 [D][D] = dS0 of the first chunk (key-major, like dht)
-            const size_t o = ((size_t)seq * p.H + h) * SD * SD + j;
+        if (task.out) {  // the final state, key-major [D][D] (dh0, or a segment's result)
 #pragma unroll
-            for (int i = 0; i < 64; ++i) p.dh0[o + (size_t)(64 * cg + i) * SD] = S[i];
+            for (int i = 0; i < 64; ++i) task.out[(size_t)(64 * cg + i) * SD + j] = S[i];
         }
     }
     tc::fence_before();
     __syncthreads();
     if (warp == 0) tc::dealloc(tmem, 512);
+}
+
+// Segment boundaries (phase 2), fp32 on CUDA cores: one CTA per (sequence, head, role).
+// Key-major states S [d][j]; a segment maps S_start to P^T S_start + L (role 0, the
+// transition chain stores P^T key-major) and dS_enter to P dS_enter + L' (role 1).  Each
+// thread owns a 4 x 8 block of the 128 x 128 result (rows 4 rb .., columns 8 cb ..).
+__global__ void __launch_bounds__(512) k_seg_combine(const Params p) {
+    extern __shared__ float sm[];
+    float* cur = sm;              // [128][128] the state crossing the boundary
+    float* tr = sm + 128 * 128;   // [128][128] the segment's transition (P^T, key-major)
+    const int pair = blockIdx.x, role = blockIdx.y, G = p.seg_G, DD = 128 * 128;
+    const size_t pd = (size_t)pair * G;
+    const int tid = threadIdx.x, rb = tid >> 4, cb = tid & 15;
+    const float* first = role == 0 ? p.segL + (pd + 0) * DD : p.segLb + (pd + G - 1) * DD;
+    for (int i = tid; i < DD / 4; i += 512) reinterpret_cast<float4*>(cur)[i] = reinterpret_cast<const float4*>(first)[i];
+    __syncthreads();
+    for (int step = 0; step < G - 1; ++step) {
+        const int g = role == 0 ? step + 1 : G - 2 - step;  // the segment that starts from `cur`
+        float4* dst = reinterpret_cast<float4*>(p.segS + ((pd + g) * 2 + role) * DD);
+        for (int i = tid; i < DD / 4; i += 512) dst[i] = reinterpret_cast<const float4*>(cur)[i];
+        if (step == G - 2) break;  // the last segment's start is all phase 3 needs
+        const float* P = p.segP + (pd + g) * DD;
+        const float* L = (role == 0 ? p.segL : p.segLb) + (pd + g) * DD;
+        for (int i = tid; i < DD / 4; i += 512) reinterpret_cast<float4*>(tr)[i] = reinterpret_cast<const float4*>(P)[i];
+        __syncthreads();
+        float acc[4][8];
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int c = 0; c < 8; ++c) acc[r][c] = L[(size_t)(4 * rb + r) * 128 + 8 * cb + c];
+#pragma unroll 4
+        for (int e = 0; e < 128; ++e) {
+            const float4 s0 = *reinterpret_cast<const float4*>(cur + e * 128 + 8 * cb);
+            const float4 s1 = *reinterpret_cast<const float4*>(cur + e * 128 + 8 * cb + 4);
+            const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+            float a[4];
+            if (role == 0) {  // (P^T S)[d][j] = sum_e P^T[d][e] S[e][j]
+#pragma unroll
+                for (int r = 0; r < 4; ++r) a[r] = tr[(4 * rb + r) * 128 + e];
+            } else {          // (P dS)[d][j] = sum_e P^T[e][d] dS[e][j]
+                const float4 t4 = *reinterpret_cast<const float4*>(tr + e * 128 + 4 * rb);
+                a[0] = t4.x, a[1] = t4.y, a[2] = t4.z, a[3] = t4.w;
+            }
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                for (int c = 0; c < 8; ++c) acc[r][c] = fmaf(a[r], sv[c], acc[r][c]);
+        }
+        __syncthreads();  // every read of cur is done
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            float4* o = reinterpret_cast<float4*>(cur + (4 * rb + r) * 128 + 8 * cb);
+            o[0] = make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+            o[1] = make_float4(acc[r][4], acc[r][5], acc[r][6], acc[r][7]);
+        }
+        __syncthreads();
+    }
 }
 
 cudaError_t launch_states_tc(const Params& p, bool fwd, bool bwd, cudaStream_t s) {
@@ -310,12 +434,26 @@ cudaError_t launch_states_tc(const Params& p, bool fwd, bool bwd, cudaStream_t s
               encode_blocked_tokens_map(&m.dO, bwd ? p.dO : nullptr, (uint64_t)p.T_total, p.H) &&
               encode_blocked_rows_map(&m.S0, fwd ? p.S0 : nullptr, srows, SD) &&
               encode_blocked_rows_map(&m.dS, bwd ? p.dS : nullptr, srows, SD);
+    (void)rows;
     if (!ok) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(k_states_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
+    const int pairs = p.N * p.H;
+    if (p.seg_G >= 2 && fwd && bwd) {
+        // time-parallel segments: phase 1 chains, the boundaries, phase 3 chains
+        k_states_tc<<<pairs * (3 * p.seg_G - 4), NTHREADS, SMEM_BYTES, s>>>(p, 1, 0, m);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        const int cbytes = 2 * 128 * 128 * 4;
+        e = cudaFuncSetAttribute(k_seg_combine, cudaFuncAttributeMaxDynamicSharedMemorySize, cbytes);
+        if (e != cudaSuccess) return e;
+        k_seg_combine<<<dim3(pairs, 2), 512, cbytes, s>>>(p);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        k_states_tc<<<pairs * 2 * p.seg_G, NTHREADS, SMEM_BYTES, s>>>(p, 3, 0, m);
+        return cudaGetLastError();
+    }
     const int role0 = fwd ? 0 : 1, nroles = (fwd && bwd) ? 2 : 1;
-    dim3 grid(p.N * p.H, nroles);
-    k_states_tc<<<grid, NTHREADS, SMEM_BYTES, s>>>(p, role0, m);
+    dim3 grid(pairs, nroles);
+    k_states_tc<<<grid, NTHREADS, SMEM_BYTES, s>>>(p, 0, role0, m);
     return cudaGetLastError();
 }
 
