@@ -49,6 +49,14 @@ def test_kda_varlen_ragged(dim):
     _check(x, label="kda_ragged_d%d" % dim, conditioned=True)
 
 
+@pytest.mark.parametrize("mode", ["gdn", "kda"])
+def test_segmented_state_passing_varlen(mode):
+    # few (sequence, head) pairs and long sequences: the state chains run as time-parallel
+    # segments (3 here); the 64-token sequence leaves two of its three segments empty
+    x = inputs.custom(mode, [16000, 64], heads=2, dim=128, seed=109, with_h0=True, with_dht=True)
+    _check(x, label="segments_%s" % mode, conditioned=(mode == "kda"))
+
+
 def test_gdn_dense_layout():
     # equal lengths passed without cu_seqlens (dense B x T)
     import chunked_gated_delta_bwd_gb300 as gdr
