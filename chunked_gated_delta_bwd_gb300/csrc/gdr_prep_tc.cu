@@ -5,7 +5,7 @@
 // dh kernel, "FlashQLA ... GDN 反向", §三):
 //
 //   [A_raw; P] = [kd'; qd'] ki'^T       A = strict_lower(diag(beta) A_raw) (fp32), P = lower(.)
-//   T   = (I + A)^-1                     (fp32 blocked inverse on CUDA cores)
+//   T   = (I + A)^-1                     (blocked inverse to fp32 accuracy, below)
 //   W^T = (beta kd)^T T^T                U^T = (beta V)^T T^T
 //   R^T = qd^T - W^T P^T                 (a bf16 pair R_hi + R_lo)
 //   kr  = kn e^{gT-gc}
@@ -15,6 +15,15 @@
 // channel-major ([D][C], 32 contiguous bytes per thread and row), the layout the
 // D = 128 state recurrence reads; T is written [C][C].  The raw q and k rows and (KDA)
 // the per-channel cumulative gate are staged in tensor memory once.
+//
+// The inverse runs on warps 0-7 while warps 8-15 build the T-independent operands of the
+// next products: the 16 x 16 diagonal blocks by forward substitution (one thread per
+// column), then every 8-column strip of the block rows below its diagonal block by block
+// forward substitution, T_i = -T_ii sum_k A_ik T_k, with the 16 x 8 products on warp-level
+// tf32 tensor-core instructions (m16n8k8) in a three-term split (hi hi + hi lo + lo hi of
+// a = hi + lo), which keeps fp32 accuracy.  The shapes are too small for tcgen05 (M >= 64).
+// The next item's gates and beta logits are read one item ahead (KDA: the raw-gate tile
+// by TMA into the space of the dead fp32 matrices).
 #include "gdr_chunk.cuh"
 #include "gdr_tc.cuh"
 #include "gdr_tma.h"
@@ -25,7 +34,8 @@ namespace {
 
 constexpr int PD = 128;
 constexpr int TILE = CH * PD * 2;  // 16 KB
-constexpr int LDF = 65;            // row stride of the fp32 64 x 64 matrices of the inversion
+constexpr int LDF = 68;            // row stride of the fp32 64 x 64 matrices of the inversion
+constexpr int XLD = 20;            // row stride of a warp's 16 x 8 transfer tile (stored [col][row])
 // shared-memory map (bytes from the 1024-aligned base); two input stages of q, k, v
 constexpr int STAGE = 3 * TILE;
 constexpr int oQ = 0;         // q (token-major) -> (beta kd)^T [d][s]   (+ STAGE for the other stage)
@@ -36,11 +46,14 @@ constexpr int oW1 = oW0 + TILE; // qd'^T [d][r] (G1, A block 1)
 constexpr int oW2 = oW1 + TILE; // ki'^T [d][s] (G1, B) -> W^T bf16 [d][s]
 constexpr int oP = oW2 + TILE;  // P [r][s] bf16
 constexpr int oT = oP + 8192;   // T [r][s] bf16
-constexpr int oA = oT + 8192;   // A fp32 [64][65]
-constexpr int oTf = oA + CH * LDF * 4;
-constexpr int oTmp = oTf + CH * LDF * 4;
-constexpr int oSmall = (oTmp + 768 * 4 + 1023) / 1024 * 1024;
-static_assert(oTmp + 768 * 4 <= oSmall, "inversion scratch overlaps the small arrays");
+constexpr int oA = oT + 8192;   // A fp32 [64][LDF] row-major; (KDA) the next item's raw gates before
+constexpr int oTf = oA + CH * LDF * 4;  // T fp32, transposed [c][r], stride LDF
+constexpr int oTmp = oTf + CH * LDF * 4;  // 8 warps' transfer tiles [8][XLD]
+constexpr int nTmp = 8 * 8 * XLD;
+constexpr int oSmall = (oTmp + nTmp * 4 + 1023) / 1024 * 1024;
+static_assert(oTmp + nTmp * 4 <= oSmall, "inversion scratch overlaps the small arrays");
+static_assert(CH * LDF * 4 >= TILE, "the raw-gate tile fits the space of A");
+static_assert(nTmp >= 4 * PD, "the KDA gate scan's minima fit the transfer tiles");
 constexpr int nInvQ = 64, nInvK = 64, nBeta = 64, nFac = 256, nGate = 128, nRef = 128, nGT = 128, nScan = 512;
 constexpr int SMALL_FLOATS = nInvQ + nInvK + nBeta + nFac + nGate + nRef + nGT + nScan;
 constexpr int SMEM_BYTES = oSmall + SMALL_FLOATS * 4 + 64 + 1024;
@@ -48,8 +61,124 @@ static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 constexpr uint32_t R_G1 = 0, R_W = 64, R_U = 128, R_R = 192, R_Q = 256, R_K = 320, R_G = 384;
 
 struct PrepMaps {
-    CUtensorMap q, k, v;
+    CUtensorMap q, k, v, graw;
 };
+
+// tf32 split of an fp32 value: hi keeps the top 10 mantissa bits, lo the rest (the tensor
+// cores read the top 19 bits of each operand register)
+__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
+    hi = __float_as_uint(x) & 0xffffe000u;
+    lo = __float_as_uint(x - __uint_as_float(hi)) & 0xffffe000u;
+}
+// d += a b for a 16 x 8 (k) A fragment and an 8 (k) x 8 B fragment, tf32 in, fp32 out
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+// d += a b to fp32 accuracy: three accumulators for hi hi, hi lo and lo hi
+__device__ __forceinline__ void mma_3xtf32(float (&d)[3][4], const float (&a)[4], const float (&b)[2]) {
+    uint32_t ah[4], al[4], bh[2], bl[2];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) split_tf32(a[i], ah[i], al[i]);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) split_tf32(b[i], bh[i], bl[i]);
+    mma_tf32(d[0], ah, bh);
+    mma_tf32(d[1], ah, bl);
+    mma_tf32(d[2], al, bh);
+}
+
+// T = (I + A)^-1 for a strictly lower 64 x 64 fp32 A (row-major, stride LDF), by warps 0-7
+// (the first 256 threads; named barrier 1).  Writes T in fp32 transposed (tT[c][r], the
+// operand copy), and in bf16 [r][c] into the swizzled tile sT and the global tile gT; the
+// blocks above the diagonal are not written.
+__device__ __forceinline__ void invert_tc(const float* sA, float* tT, float* xfer, unsigned char* sT,
+                                          __nv_bfloat16* gT) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid < 64) {  // diagonal block b, column j: forward substitution down the block
+        const int b = tid >> 4, j = tid & 15;
+        const float* Ab = sA + 16 * b * LDF + 16 * b;
+        float x[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            float a[16];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (4 * q < i) {
+                    const float4 v = *reinterpret_cast<const float4*>(Ab + i * LDF + 4 * q);
+                    a[4 * q] = v.x;
+                    a[4 * q + 1] = v.y;
+                    a[4 * q + 2] = v.z;
+                    a[4 * q + 3] = v.w;
+                }
+            float acc = i == j ? 1.f : 0.f;
+#pragma unroll
+            for (int s = 0; s < i; ++s) acc = fmaf(-a[s], x[s], acc);
+            x[i] = acc;
+        }
+        float* dst = tT + (16 * b + j) * LDF + 16 * b;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<float4*>(dst + 4 * q) = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int r = 16 * b + i, c = 16 * b + j;
+            const __nv_bfloat16 y = __float2bfloat16(x[i]);
+            *reinterpret_cast<__nv_bfloat16*>(sT + tc::sw_off(r, c, 64)) = y;
+            gT[r * CH + c] = y;
+        }
+    }
+    tc::named_sync(1, 256);
+    // strip of columns n0 .. n0+7 (block column jb), block rows jb+1 .. 3
+    const int n0 = 8 * warp, jb = warp >> 1, gid = lane >> 2, tig = lane & 3;
+    float* xf = xfer + warp * 8 * XLD;
+    for (int i = jb + 1; i < 4; ++i) {
+        float acc[3][4] = {};
+        for (int k = jb; k < i; ++k) {  // M = sum_k A_ik T_k
+#pragma unroll
+            for (int ks = 0; ks < 2; ++ks) {
+                const int kk = 16 * k + 8 * ks;
+                const float* Ar = sA + (16 * i + gid) * LDF + kk + tig;
+                const float* Br = tT + (n0 + gid) * LDF + kk + tig;
+                const float a[4] = {Ar[0], Ar[8 * LDF], Ar[4], Ar[8 * LDF + 4]};
+                const float bb[2] = {Br[0], Br[4]};
+                mma_3xtf32(acc, a, bb);
+            }
+        }
+        // M (accumulator layout: rows gid, gid + 8; columns 2 tig, 2 tig + 1) -> xf[col][row]
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float mval = acc[0][e] + (acc[1][e] + acc[2][e]);
+            xf[(2 * tig + (e & 1)) * XLD + gid + 8 * (e >> 1)] = mval;
+        }
+        __syncwarp();
+        float out[3][4] = {};
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks) {  // T_i = -T_ii M
+            const int cc = 16 * i + 8 * ks + tig, rr = 16 * i + gid;
+            const float a[4] = {tT[cc * LDF + rr], tT[cc * LDF + rr + 8], tT[(cc + 4) * LDF + rr],
+                                tT[(cc + 4) * LDF + rr + 8]};
+            const float bb[2] = {xf[gid * XLD + 8 * ks + tig], xf[gid * XLD + 8 * ks + tig + 4]};
+            mma_3xtf32(out, a, bb);
+        }
+        float t[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            t[e] = -(out[0][e] + (out[1][e] + out[2][e]));
+            tT[(n0 + 2 * tig + (e & 1)) * LDF + 16 * i + gid + 8 * (e >> 1)] = t[e];
+        }
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+            const int r = 16 * i + gid + 8 * h2, c = n0 + 2 * tig;
+            const uint32_t w = pack_bf16(t[2 * h2], t[2 * h2 + 1]);
+            *reinterpret_cast<uint32_t*>(sT + tc::sw_off(r, c, 64)) = w;
+            *reinterpret_cast<uint32_t*>(gT + r * CH + c) = w;
+        }
+        __syncwarp();
+    }
+}
 
 }  // namespace
 
@@ -81,8 +210,9 @@ __global__ void __launch_bounds__(512, 1) k_prep_tc(const Params p, const __grid
     float* sGT = sRef + nRef;     // KDA gT[d]
     float* sScan = sGT + nGT;     // KDA [4][128]
     uint64_t* mbars = reinterpret_cast<uint64_t*>(sScan + nScan);
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbars + 3);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbars + 4);
     const uint32_t mb = smem_u32(mbars), mload0 = smem_u32(mbars + 1);  // load barriers: one per stage
+    const uint32_t mgr = smem_u32(mbars + 3);                            // (KDA) the raw-gate tile
 
     Gates<PD, false> G;
     G.gc = sGate;
@@ -100,13 +230,28 @@ __global__ void __launch_bounds__(512, 1) k_prep_tc(const Params p, const __grid
         tc::tma_load_4d(st + oK, &m.k, 0, hh, t0, 0, bar);
         tc::tma_load_4d(st + oV, &m.v, 0, hh, t0, 0, bar);
     };
+    // (KDA) raw gates of `item`, token-major, into the space of A (dead from the end of the
+    // inversion to the next item's G1)
+    auto issue_gate_load = [&](int item) {
+        ChunkInfo cj;
+        lookup_chunk(item / p.H, p.N, p.chunk_off, p.cu_seqlens, p.seq_len, cj);
+        tc::mbar_expect_tx(mgr, TILE);
+        tc::tma_load_4d(sb + oA, &m.graw, 0, item % p.H, (int)cj.t0, 0, mgr);
+    };
     if (warp == 0) tc::alloc(smem_u32(tslot), 512);
     if (tid == 0) {
         tc::mbar_init(mb, 1);
         tc::mbar_init(mload0, 1);
         tc::mbar_init(mload0 + 8, 1);
-        if ((int)blockIdx.x < n_items) issue_loads(blockIdx.x, 0);
+        tc::mbar_init(mgr, 1);
+        if ((int)blockIdx.x < n_items) {
+            issue_loads(blockIdx.x, 0);
+            if (KDA) issue_gate_load(blockIdx.x);
+        }
     }
+    // T's blocks above the diagonal stay zero in the shared tile
+    for (int i = tid; i < CH * CH * 2 / 16; i += 512)
+        *reinterpret_cast<uint4*>(smem + oT + 16 * i) = make_uint4(0, 0, 0, 0);
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
@@ -122,10 +267,12 @@ __global__ void __launch_bounds__(512, 1) k_prep_tc(const Params p, const __grid
     };
     int pending = -1;  // stage with a load in flight that this item does not consume, or -1
     uint32_t pending_par = 0;
+    bool pending_g = KDA && (int)blockIdx.x < n_items;  // (KDA) a raw-gate tile is in flight
     auto bail = [&]() {
         if (tid == 0) {
             atomicOr(p.status, ST_MMA_TIMEOUT);
             if (pending >= 0) tc::mbar_wait(mload0 + 8 * pending, pending_par);  // bounded drain
+            if (pending_g) tc::mbar_wait(mgr, (uint32_t)(it & 1));
         }
         tc::fence_before();
         __syncthreads();
@@ -141,10 +288,30 @@ __global__ void __launch_bounds__(512, 1) k_prep_tc(const Params p, const __grid
         }
         return true;
     };
-    auto rows16 = [&](const float* a, float (&o)[16]) {
+    // the next item's beta logit (thread r < 64), GDN gates (first warp, rows 2 lane and
+    // 2 lane + 1) and KDA gate parameters (every thread: its channel), read one item ahead
+    float pb = 0.f, pg0 = 0.f, pg1 = 0.f, pbias = 0.f, palog = 0.f;
+    auto prefetch_small = [&](int item) {
+        ChunkInfo cj;
+        lookup_chunk(item / p.H, p.N, p.chunk_off, p.cu_seqlens, p.seq_len, cj);
+        const int hh = item % p.H;
+        if (tid < CH) pb = tid < cj.len ? bf2f(p.beta_logit[(cj.t0 + tid) * p.H + hh]) : 0.f;
+        if (!KDA && tid < 32) {
+            const int r0 = 2 * tid;
+            pg0 = r0 < cj.len ? p.g[(cj.t0 + r0) * p.H + hh] : 0.f;
+            pg1 = r0 + 1 < cj.len ? p.g[(cj.t0 + r0 + 1) * p.H + hh] : 0.f;
+        }
+        if (KDA) {
+            pbias = p.dt_bias[hh * PD + L];
+            palog = p.A_log[hh];
+        }
+    };
+    if ((int)blockIdx.x < n_items) prefetch_small(blockIdx.x);
+    // a[cq .. cq+15]
+    auto rows16 = [&](const float* a, float (&o)[16], int cq) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const float4 v = *reinterpret_cast<const float4*>(a + c0 + 4 * i);
+            const float4 v = *reinterpret_cast<const float4*>(a + cq + 4 * i);
             o[4 * i] = v.x;
             o[4 * i + 1] = v.y;
             o[4 * i + 2] = v.z;
@@ -155,10 +322,10 @@ __global__ void __launch_bounds__(512, 1) k_prep_tc(const Params p, const __grid
 #pragma unroll
         for (int e = 0; e < 8; ++e) w[e] = pack_bf16(v[2 * e], v[2 * e + 1]);
     };
-    // row L, columns c0 .. c0+15 of a channel-major [128][64] shared tile
-    auto store_cm = [&](unsigned char* tile, const uint32_t (&w)[8]) {
-        *reinterpret_cast<uint4*>(tile + tc::sw_chunk(L, c0 >> 3, 128)) = make_uint4(w[0], w[1], w[2], w[3]);
-        *reinterpret_cast<uint4*>(tile + tc::sw_chunk(L, (c0 >> 3) + 1, 128)) = make_uint4(w[4], w[5], w[6], w[7]);
+    // row L, columns cq .. cq+15 of a channel-major [128][64] shared tile
+    auto store_cm = [&](unsigned char* tile, const uint32_t (&w)[8], int cq) {
+        *reinterpret_cast<uint4*>(tile + tc::sw_chunk(L, cq >> 3, 128)) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(tile + tc::sw_chunk(L, (cq >> 3) + 1, 128)) = make_uint4(w[4], w[5], w[6], w[7]);
     };
     // row L, columns c0 .. c0+15 of a chunk-head's channel-major [128][64] global tile
     auto store_global_cm = [&](__nv_bfloat16* tile, const uint32_t (&w)[8]) {
@@ -176,27 +343,39 @@ __global__ void __launch_bounds__(512, 1) k_prep_tc(const Params p, const __grid
     const uint32_t sQa = sb + stg * STAGE + oQ, sKa = sb + stg * STAGE + oK;
     const size_t tile_cd = ((size_t)chunk * p.H + h) * CH * PD;
     const size_t tile_cc = ((size_t)chunk * p.H + h) * CH * CH;
+    const bool has_next = item + (int)gridDim.x < n_items;
     // the next item's tiles into the other stage (its previous tenant finished last iteration)
     pending = -1;
-    if (item + (int)gridDim.x < n_items) {
+    if (has_next) {
         if (tid == 0) issue_loads(item + gridDim.x, stg ^ 1);
         pending = stg ^ 1;
         pending_par = (uint32_t)(((it + 1) >> 1) & 1);
     }
-    if constexpr (!KDA) load_gates<PD, false, 512>(p, ci, h, G, true);
-    load_beta(p, ci, h, sBeta);
+    if constexpr (!KDA)
+        if (tid < 32) gdn_gate_scan(pg0, pg1, G, true, p);
+    if (tid < CH) sBeta[tid] = tid < ci.len ? sigmoid_f(pb) : 0.f;
 
-    // KDA: per-channel log gates of this thread's channel and rows, scanned across the four
-    // row quarters, staged in tensor memory; the gate-range check of the chunk
+    // KDA: per-channel log gates of this thread's channel and rows (raw gates from the
+    // token-major tile in the space of A), scanned across the four row quarters, staged in
+    // tensor memory; the gate-range check of the chunk
     float refL = 0.f, gTL = 0.f;
     if constexpr (KDA) {
-        const float a = expf(p.A_log[h]);
-        const float bias = p.dt_bias[h * PD + L];
+        const float a = expf(palog);
+        const float bias = pbias;
+        {
+            const bool ok = tc::mbar_wait(mgr, (uint32_t)(it & 1));
+            if (__syncthreads_or(!ok)) return bail();
+            pending_g = false;
+        }
         float g[16];
+        {
+            const unsigned char* gt = smem + oA;
+            const int lch = (L & 63) >> 3, lsub = (L & 7) << 1;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const int r = c0 + i;
-            g[i] = r < ci.len ? bf2f(p.g_raw[((ci.t0 + r) * p.H + h) * PD + L]) : 0.f;
+            for (int i = 0; i < 16; ++i) {
+                const uint32_t off = (uint32_t)((L >> 6) * 64 * 128 + (c0 + i) * 128 + ((lch ^ (i & 7)) << 4) + lsub);
+                g[i] = c0 + i < ci.len ? __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(gt + off)) : 0.f;
+            }
         }
         float acc = 0.f;
 #pragma unroll
@@ -295,41 +474,42 @@ __global__ void __launch_bounds__(512, 1) k_prep_tc(const Params p, const __grid
     }
     __syncthreads();  // norms, factors and the q / k tile reads are done
 
-    auto factors = [&](int kind, float (&f)[16]) {
+    // gate factors of this thread's channel and rows cq .. cq+15
+    auto factors = [&](int kind, float (&f)[16], int cq) {
         if constexpr (KDA) {
             float g[16];
-            tc::ld16(tl(R_G + c0), g);
+            tc::ld16(tl(R_G + cq), g);
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 const float e = kind == F_KD ? g[i] : kind == F_KDP ? g[i] - refL : kind == F_KIP ? refL - g[i] : gTL - g[i];
                 f[i] = __expf(e);
             }
         } else {
-            rows16(sFac + kind * CH, f);
+            rows16(sFac + kind * CH, f, cq);
         }
     };
-    // x (raw q or k of this channel and rows) * m_r * f, m_r = inv_r * mul * rowmul_r
-    auto derived = [&](bool isq, float mul, const float* rowmul, int kind, float (&o)[16]) {
+    // x (raw q or k of this channel and rows cq ..) * m_r * f, m_r = inv_r * mul * rowmul_r
+    auto derived = [&](bool isq, float mul, const float* rowmul, int kind, float (&o)[16], int cq) {
         float f[16], inv[16], rm[16];
-        factors(kind, f);
-        tc::ld16(tl((isq ? R_Q : R_K) + c0), o);
-        rows16(isq ? sInvQ : sInvK, inv);
-        if (rowmul) rows16(rowmul, rm);
+        factors(kind, f, cq);
+        tc::ld16(tl((isq ? R_Q : R_K) + cq), o);
+        rows16(isq ? sInvQ : sInvK, inv, cq);
+        if (rowmul) rows16(rowmul, rm, cq);
 #pragma unroll
         for (int i = 0; i < 16; ++i) o[i] = o[i] * derived_m(inv[i], mul, rowmul ? rm[i] : 1.f) * f[i];
     };
-    auto build = [&](unsigned char* tile, bool isq, float mul, const float* rowmul, int kind) {
+    auto build = [&](unsigned char* tile, bool isq, float mul, const float* rowmul, int kind, int cq) {
         float v[16];
         uint32_t w[8];
-        derived(isq, mul, rowmul, kind, v);
+        derived(isq, mul, rowmul, kind, v, cq);
         pack8(v, w);
-        store_cm(tile, w);
+        store_cm(tile, w, cq);
     };
 
     // ---- G1: [A_raw; P] = [kd'; qd'] ki'^T ----------------------------------------------
-    build(sW0, false, 1.f, nullptr, F_KDP);
-    build(sW1, true, p.scale, nullptr, F_KDP);
-    build(sW2, false, 1.f, nullptr, F_KIP);
+    build(sW0, false, 1.f, nullptr, F_KDP, c0);
+    build(sW1, true, p.scale, nullptr, F_KDP, c0);
+    build(sW2, false, 1.f, nullptr, F_KIP, c0);
     sync_all();
     if (tid == 0) {
         constexpr uint32_t id = tc::idesc(128, 64, 1, 1);
@@ -345,7 +525,10 @@ __global__ void __launch_bounds__(512, 1) k_prep_tc(const Params p, const __grid
             const int r = L;
             const float br = sBeta[r];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) sA[r * LDF + c0 + i] = c0 + i < r ? br * v[i] : 0.f;
+            for (int i = 0; i < 16; i += 4)
+                *reinterpret_cast<float4*>(sA + r * LDF + c0 + i) =
+                    make_float4(c0 + i < r ? br * v[i] : 0.f, c0 + i + 1 < r ? br * v[i + 1] : 0.f,
+                                c0 + i + 2 < r ? br * v[i + 2] : 0.f, c0 + i + 3 < r ? br * v[i + 3] : 0.f);
         } else {  // P = lower(qd' ki'^T), bf16 [r][s]
             const int r = L - 64;
             uint32_t w[8];
@@ -359,29 +542,42 @@ __global__ void __launch_bounds__(512, 1) k_prep_tc(const Params p, const __grid
         }
     }
     __syncthreads();
-    invert_unit_lower64<512>(sA, sTf, sTmp);  // ends with __syncthreads
-    for (int i = tid; i < CH * CH / 2; i += 512) {
-        const int r = i / (CH / 2), c = 2 * (i % (CH / 2));
-        const uint32_t w = pack_bf16(sTf[r * LDF + c], sTf[r * LDF + c + 1]);
-        *reinterpret_cast<uint32_t*>(sT + tc::sw_off(r, c, 64)) = w;
-        *reinterpret_cast<uint32_t*>(p.Tm + tile_cc + r * CH + c) = w;
-    }
-    // (beta kd)^T -> the q tile's space ; (beta V)^T -> the k tile's space
-    build(sQ, false, 1.f, sBeta, F_KD);
-    {
-        float v[16], bt[16];
-        uint32_t w[8];
-        rows16(sBeta, bt);
-        const int lch = (L & 63) >> 3, lsub = (L & 7) << 1;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const uint32_t off = (uint32_t)((L >> 6) * 64 * 128 + (c0 + i) * 128 + ((lch ^ (i & 7)) << 4) + lsub);
-            v[i] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(sV + off)) * bt[i];
+    if (warp < 8) {
+        invert_tc(sA, sTf, sTmp, sT, p.Tm + tile_cc);
+    } else {
+        // T's zero blocks above the diagonal in the global tile: rows 16 b .. 16 b + 15,
+        // columns from 16 (b + 1), 16-byte pieces (6 + 4 + 2 per row of block rows 0, 1, 2)
+        const int t2 = tid - 256;
+        if (t2 < 192) {
+            const int b = t2 < 96 ? 0 : t2 < 160 ? 1 : 2;
+            const int base = b == 0 ? 0 : b == 1 ? 96 : 160, per = 6 - 2 * b;
+            const int r = 16 * b + (t2 - base) / per, piece = (t2 - base) % per;
+            *reinterpret_cast<uint4*>(p.Tm + tile_cc + r * CH + 16 * (b + 1) + 8 * piece) = make_uint4(0, 0, 0, 0);
         }
-        pack8(v, w);
-        store_cm(sK, w);
+        // (beta kd)^T -> the q tile's space ; (beta V)^T -> the k tile's space; this warp's
+        // lanes for row quarters (hc - 2) and hc
+        for (int pass = 0; pass < 2; ++pass) {
+            const int cq = 16 * (hc - 2 + 2 * pass);
+            build(sQ, false, 1.f, sBeta, F_KD, cq);
+            float v[16], bt[16];
+            uint32_t w[8];
+            rows16(sBeta, bt, cq);
+            const int lch = (L & 63) >> 3, lsub = (L & 7) << 1;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const uint32_t off = (uint32_t)((L >> 6) * 64 * 128 + (cq + i) * 128 + ((lch ^ (i & 7)) << 4) + lsub);
+                v[i] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(sV + off)) * bt[i];
+            }
+            pack8(v, w);
+            store_cm(sK, w, cq);
+        }
     }
     sync_all();
+    if (has_next) {  // the space of A is free: the next item's small inputs and (KDA) raw gates
+        if (KDA && tid == 0) issue_gate_load(item + gridDim.x);
+        pending_g = KDA;
+        prefetch_small(item + gridDim.x);
+    }
 
     // ---- W^T = (beta kd)^T T^T ; U^T = (beta V)^T T^T --------------------------------------
     if (tid == 0) {
@@ -399,7 +595,7 @@ __global__ void __launch_bounds__(512, 1) k_prep_tc(const Params p, const __grid
         tc::ld16(tl(R_W + c0), v);
         pack8(v, w);
         store_global_cm(p.W + tile_cd, w);
-        store_cm(sW2, w);  // bf16 W^T, the A operand of W^T P^T (ki' is dead)
+        store_cm(sW2, w, c0);  // bf16 W^T, the A operand of W^T P^T (ki' is dead)
         tc::ld16(tl(R_U + c0), v);
         pack8(v, w);
         store_global_cm(p.U + tile_cd, w);
@@ -417,7 +613,7 @@ __global__ void __launch_bounds__(512, 1) k_prep_tc(const Params p, const __grid
     {
         float v[16];
         uint32_t w[8];
-        derived(false, 1.f, nullptr, F_KR, v);
+        derived(false, 1.f, nullptr, F_KR, v, c0);
         pack8(v, w);
         store_global_cm(p.Kr + tile_cd, w);
         if (hc == 0) {
@@ -431,7 +627,7 @@ __global__ void __launch_bounds__(512, 1) k_prep_tc(const Params p, const __grid
         float acc[16], qd[16];
         uint32_t w[8], wl[8];
         tc::ld16(tl(R_R + c0), acc);
-        derived(true, p.scale, nullptr, F_KD, qd);
+        derived(true, p.scale, nullptr, F_KD, qd, c0);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             const float r0 = qd[2 * e] - acc[2 * e], r1 = qd[2 * e + 1] - acc[2 * e + 1];
@@ -456,7 +652,8 @@ static cudaError_t launch_prep_tc_t(const Params& p, cudaStream_t s) {
     PrepMaps m;
     const uint64_t T = (uint64_t)p.T_total;
     if (!(encode_blocked_tokens_map(&m.q, p.q, T, p.H) && encode_blocked_tokens_map(&m.k, p.k, T, p.H) &&
-          encode_blocked_tokens_map(&m.v, p.v, T, p.H)))
+          encode_blocked_tokens_map(&m.v, p.v, T, p.H) &&
+          encode_blocked_tokens_map(&m.graw, KDA ? p.g_raw : nullptr, T, p.H)))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(k_prep_tc<KDA>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
