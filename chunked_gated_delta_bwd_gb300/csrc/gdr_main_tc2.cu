@@ -124,7 +124,7 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
     float* sInvK = sInvQ + nInvQ;
     float* sBeta = sInvK + nInvK;
     float* sFac = sBeta + nBeta;     // GDN [4][64]: e^{gc}, e^{gc-ref}, e^{ref-gc}, e^{gT-gc}
-    float* sGate = sFac + nFac;      // GDN gc[64], ref, gT
+    float* sGate = sFac + nFac;      // GDN gc[64], ref, gT; KDA dt_bias[d]
     float* sRef = sGate + nGate;     // KDA ref[d]
     float* sGT = sRef + nRef;        // KDA gT[d]
     float* sScan = sGT + nGT;        // KDA [4][128] per-quarter gate totals / extrema / suffix totals
@@ -133,7 +133,7 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
     float* sDbP = sDgTp + nDgTp;     // [64] <dY, beta E> per row
     float* sDbA = sDbP + nDbP;       // [4][64] rowsum(dA . A) per column quarter
     float* sRow = sDbA + nDbA;       // [3][4][64] row reductions (and KDA partials)
-    float* sMisc = sRow + nRow;      // [64]
+    float* sMisc = sRow + nRow;      // [64]: per-warp partials [0, 16); KDA e^{A_log} at [32]
     float* sTot = sMisc + nMisc;     // [2][64] row dots summed over the lane quarters (q, k)
     uint64_t* mbars = reinterpret_cast<uint64_t*>(sTot + nTot);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(mbars + 3);
@@ -264,6 +264,12 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
     if constexpr (!KDA)
         if (tid < 32) gdn_gate_scan(pg0, pg1, G, false, p);
     if (tid < CH) sBeta[tid] = tid < ci.len ? sigmoid_f(pb) : 0.f;
+    // KDA gate parameters, read while the operand tiles land
+    float alog = 0.f, bias = 0.f;
+    if constexpr (KDA) {
+        alog = p.A_log[h];
+        bias = p.dt_bias[h * MD + L];
+    }
 
     // wait for the operand tiles; rows past the chunk's end read as zero
     {
@@ -275,8 +281,9 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
     // row quarters, staged in tensor memory (lane = channel, column = row)
     float refL = 0.f, gTL = 0.f;
     if constexpr (KDA) {
-        const float a = expf(p.A_log[h]);
-        const float bias = p.dt_bias[h * MD + L];
+        const float a = expf(alog);
+        if (hc == 0) sGate[L] = bias;  // for the gate chain rule at the end of the item
+        if (tid == 0) sMisc[32] = a;
         float g[16];  // raw gates of this channel and rows, from the token-major tile in W0
         {
             const int lch = (L & 63) >> 3, lsub = (L & 7) << 1;
@@ -845,7 +852,7 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
         // the later row quarters' totals and the chunk constant dgT as the suffix; then the
         // gate chain rule per element, with per-channel partial sums
         float xr[16];
-        const float bias = p.dt_bias[h * MD + L];
+        const float bias = sGate[L];
         {
             const bool ok = tc::mbar_wait(mgr, (uint32_t)(it & 1));
             if (__syncthreads_or(!ok)) return bail();
@@ -870,7 +877,7 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
 #pragma unroll
         for (int h2 = 3; h2 >= 0; --h2)
             if (h2 > hc) post += sScan[h2 * MD + L];
-        const float ea = expf(p.A_log[h]);
+        const float ea = sMisc[32];
         float ddt = 0.f, dA_acc = 0.f;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {

@@ -90,6 +90,61 @@ __device__ __forceinline__ void mma_3xtf32(float (&d)[3][4], const float (&a)[4]
     mma_tf32(d[2], al, bh);
 }
 
+// Block rows JB+1 .. 3 of the 8-column strip n0 of T (one warp), given the diagonal blocks:
+// T_i = -T_ii M_i, M_i = sum_{k=JB}^{i-1} A_ik T_k; every loop has compile-time bounds so
+// that the operand loads of a product are issued together.
+template <int JB>
+__device__ __forceinline__ void invert_strip(const float* sA, float* tT, float* xf, unsigned char* sT,
+                                             __nv_bfloat16* gT, int n0, int lane) {
+    const int gid = lane >> 2, tig = lane & 3;
+#pragma unroll
+    for (int i = JB + 1; i < 4; ++i) {
+        float acc[3][4] = {};
+#pragma unroll
+        for (int k = JB; k < i; ++k) {  // M = sum_k A_ik T_k
+#pragma unroll
+            for (int ks = 0; ks < 2; ++ks) {
+                const int kk = 16 * k + 8 * ks;
+                const float* Ar = sA + (16 * i + gid) * LDF + kk + tig;
+                const float* Br = tT + (n0 + gid) * LDF + kk + tig;
+                const float a[4] = {Ar[0], Ar[8 * LDF], Ar[4], Ar[8 * LDF + 4]};
+                const float bb[2] = {Br[0], Br[4]};
+                mma_3xtf32(acc, a, bb);
+            }
+        }
+        // M (accumulator layout: rows gid, gid + 8; columns 2 tig, 2 tig + 1) -> xf[col][row]
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float mval = acc[0][e] + (acc[1][e] + acc[2][e]);
+            xf[(2 * tig + (e & 1)) * XLD + gid + 8 * (e >> 1)] = mval;
+        }
+        __syncwarp();
+        float out[3][4] = {};
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks) {  // T_i = -T_ii M
+            const int cc = 16 * i + 8 * ks + tig, rr = 16 * i + gid;
+            const float a[4] = {tT[cc * LDF + rr], tT[cc * LDF + rr + 8], tT[(cc + 4) * LDF + rr],
+                                tT[(cc + 4) * LDF + rr + 8]};
+            const float bb[2] = {xf[gid * XLD + 8 * ks + tig], xf[gid * XLD + 8 * ks + tig + 4]};
+            mma_3xtf32(out, a, bb);
+        }
+        float t[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            t[e] = -(out[0][e] + (out[1][e] + out[2][e]));
+            tT[(n0 + 2 * tig + (e & 1)) * LDF + 16 * i + gid + 8 * (e >> 1)] = t[e];
+        }
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+            const int r = 16 * i + gid + 8 * h2, c = n0 + 2 * tig;
+            const uint32_t w = pack_bf16(t[2 * h2], t[2 * h2 + 1]);
+            *reinterpret_cast<uint32_t*>(sT + tc::sw_off(r, c, 64)) = w;
+            *reinterpret_cast<uint32_t*>(gT + r * CH + c) = w;
+        }
+        __syncwarp();
+    }
+}
+
 // T = (I + A)^-1 for a strictly lower 64 x 64 fp32 A (row-major, stride LDF), by warps 0-7
 // (the first 256 threads; named barrier 1).  Writes T in fp32 transposed (tT[c][r], the
 // operand copy), and in bf16 [r][c] into the swizzled tile sT and the global tile gT; the
@@ -132,51 +187,13 @@ __device__ __forceinline__ void invert_tc(const float* sA, float* tT, float* xfe
     }
     tc::named_sync(1, 256);
     // strip of columns n0 .. n0+7 (block column jb), block rows jb+1 .. 3
-    const int n0 = 8 * warp, jb = warp >> 1, gid = lane >> 2, tig = lane & 3;
+    const int n0 = 8 * warp, jb = warp >> 1;
     float* xf = xfer + warp * 8 * XLD;
-    for (int i = jb + 1; i < 4; ++i) {
-        float acc[3][4] = {};
-        for (int k = jb; k < i; ++k) {  // M = sum_k A_ik T_k
-#pragma unroll
-            for (int ks = 0; ks < 2; ++ks) {
-                const int kk = 16 * k + 8 * ks;
-                const float* Ar = sA + (16 * i + gid) * LDF + kk + tig;
-                const float* Br = tT + (n0 + gid) * LDF + kk + tig;
-                const float a[4] = {Ar[0], Ar[8 * LDF], Ar[4], Ar[8 * LDF + 4]};
-                const float bb[2] = {Br[0], Br[4]};
-                mma_3xtf32(acc, a, bb);
-            }
-        }
-        // M (accumulator layout: rows gid, gid + 8; columns 2 tig, 2 tig + 1) -> xf[col][row]
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float mval = acc[0][e] + (acc[1][e] + acc[2][e]);
-            xf[(2 * tig + (e & 1)) * XLD + gid + 8 * (e >> 1)] = mval;
-        }
-        __syncwarp();
-        float out[3][4] = {};
-#pragma unroll
-        for (int ks = 0; ks < 2; ++ks) {  // T_i = -T_ii M
-            const int cc = 16 * i + 8 * ks + tig, rr = 16 * i + gid;
-            const float a[4] = {tT[cc * LDF + rr], tT[cc * LDF + rr + 8], tT[(cc + 4) * LDF + rr],
-                                tT[(cc + 4) * LDF + rr + 8]};
-            const float bb[2] = {xf[gid * XLD + 8 * ks + tig], xf[gid * XLD + 8 * ks + tig + 4]};
-            mma_3xtf32(out, a, bb);
-        }
-        float t[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            t[e] = -(out[0][e] + (out[1][e] + out[2][e]));
-            tT[(n0 + 2 * tig + (e & 1)) * LDF + 16 * i + gid + 8 * (e >> 1)] = t[e];
-        }
-#pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-            const int r = 16 * i + gid + 8 * h2, c = n0 + 2 * tig;
-            const uint32_t w = pack_bf16(t[2 * h2], t[2 * h2 + 1]);
-            *reinterpret_cast<uint32_t*>(sT + tc::sw_off(r, c, 64)) = w;
-            *reinterpret_cast<uint32_t*>(gT + r * CH + c) = w;
-        }
-        __syncwarp();
+    switch (jb) {
+        case 0: invert_strip<0>(sA, tT, xf, sT, gT, n0, lane); break;
+        case 1: invert_strip<1>(sA, tT, xf, sT, gT, n0, lane); break;
+        case 2: invert_strip<2>(sA, tT, xf, sT, gT, n0, lane); break;
+        default: break;
     }
 }
 
