@@ -42,6 +42,10 @@ D_, C_ = 128, 64
 MAIN_FLOP_PER_TH = 10 * D_ * D_ + 22 * C_ * D_
 MAIN_BYTES_PER_TH = {"gdn": 4 * 2 * D_ + 2 + 4 + 2 * (2 * D_ * D_ // C_) + 2 * C_ + 3 * 2 * D_ + 2 + 4,
                      "kda": 4 * 2 * D_ + 2 + 2 * D_ + 2 * (2 * D_ * D_ // C_) + 2 * C_ + 3 * 2 * D_ + 2 + 2 * D_}
+# Forward output kernel (o = R S0 + P U per chunk) per token-head: reads S0 (2 D^2 / C), R^T and
+# U^T (2 D each), P (2 C); writes o (2 D).  Flops: 2 (D^2 + C D).
+OUT_BYTES_PER_TH = 2 * D_ * D_ // C_ + 2 * D_ + 2 * D_ + 2 * C_ + 2 * D_
+OUT_FLOP_PER_TH = 2 * (D_ * D_ + C_ * D_)
 
 
 def peaks():
@@ -260,6 +264,39 @@ def main_gpu(args):
         return a.elapsed_time(b) / n
     ms_g, ms_k = time_loop("gdn", step_g), time_loop("kda", step_k)
 
+    # ---- the forward (o, ht) on the same inputs: informational, one loop per variant ----
+    fwd_kernels = {}
+
+    def fwd_loop(name, fn, n=max(3, args.steps // 2)):
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize()
+        api.profile_begin(8 * n)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        fwd_kernels[name] = {k: round(v[0] / n, 4) for k, v in api.profile_end().items() if v[1]}
+        return a.elapsed_time(b) / n
+    fms_g = fwd_loop("gdn", lambda A=G: gdr.gdr_fwd(A["q"], A["k"], A["v"], A["g"], A["beta_logit"], h0=A["h0"],
+                                                   num_seqs=N, scale=A["scale"], workspace=ws_g))
+    fms_k = fwd_loop("kda", lambda A=K: gdr.kda_fwd(A["q"], A["k"], A["v"], A["g_raw"], A["A_log"], A["dt_bias"],
+                                                   A["beta_logit"], h0=A["h0"], num_seqs=N, scale=A["scale"],
+                                                   workspace=ws_k))
+    th_v = CASE_G.seq_len * CASE_G.heads
+    out_ms = (fwd_kernels["gdn"].get("out", 0.0) + fwd_kernels["kda"].get("out", 0.0)) / 2
+    forward = {
+        "ms_per_variant": {"gdn": fms_g, "kda": fms_k},
+        "mtokens_per_s": (CASE_G.seq_len + CASE_K.seq_len) / ((fms_g + fms_k) * 1e-3) / 1e6,
+        "kernels_ms_per_variant": fwd_kernels,
+        "out_roofline": ({"kernel": "k_out (forward output)", "bound": "hbm",
+                          "achieved": th_v * OUT_BYTES_PER_TH / (out_ms * 1e-3) / 1e9, "unit": "GB/s",
+                          "tensor_tflops": th_v * OUT_FLOP_PER_TH / (out_ms * 1e-3) / 1e12}
+                         if out_ms > 0 else None),
+    }
+
     # ---- end to end: pinned host inputs -> device -> backward -> host gradients ----
     def pinned(x):
         return {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
@@ -306,6 +343,9 @@ def main_gpu(args):
 
     # ---- roofline of the dominant kernel ----
     hbm, tf_burst, tf_sus, src = peaks()
+    if forward["out_roofline"]:
+        fr = forward["out_roofline"]
+        fr.update(peak=hbm, frac=fr["achieved"] / hbm, peak_source=src + " (hbm_gbs)")
     dom = max(prof, key=lambda k: prof[k][0])
     th = CASE_G.seq_len * CASE_G.heads  # token-heads per variant
     roof = None
@@ -341,6 +381,7 @@ def main_gpu(args):
         "roofline": roof,
         "kernels_ms_per_step": {k: v[0] / args.steps for k, v in prof.items()},
         "kernels_ms_per_variant": per_variant,
+        "forward": forward,
         "gpu_launches": launches,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms},

@@ -51,6 +51,10 @@ def lib():
         L.gdr_fwd_states.argtypes = [sp] + [vp] * 7 + [sz, vp, sz, vp]
         L.kda_fwd_states.restype = ctypes.c_int
         L.kda_fwd_states.argtypes = [sp] + [vp] * 9 + [sz, vp, sz, vp]
+        L.gdr_fwd.restype = ctypes.c_int
+        L.gdr_fwd.argtypes = [sp] + [vp] * 9 + [sz, vp, sz, vp]
+        L.kda_fwd.restype = ctypes.c_int
+        L.kda_fwd.argtypes = [sp] + [vp] * 11 + [sz, vp, sz, vp]
         L.gdr_bwd.restype = ctypes.c_int
         L.gdr_bwd.argtypes = [sp] + [vp] * 10 + [sz] + [vp] * 7
         L.kda_bwd.restype = ctypes.c_int
@@ -175,6 +179,51 @@ def gdr_fwd_states(q, k, v, g, beta_logit, h0=None, cu_seqlens=None, num_seqs=No
     return states
 
 
+def _fwd(gate, q, k, v, beta_logit, h0, cu_seqlens, num_seqs, scale, states, workspace, want_ht,
+         g=None, g_raw=None, A_log=None, dt_bias=None):
+    P = _Problem(q, cu_seqlens, num_seqs, scale)
+    T, H, D, N = P.T, P.H, P.D, P.N
+    q, k, v = (_need(P.flat(x), torch.bfloat16, (T, H, D), n) for x, n in ((q, "q"), (k, "k"), (v, "v")))
+    beta_logit = _need(P.flat(beta_logit), torch.bfloat16, (T, H), "beta_logit")
+    h0 = _opt(h0, torch.float32, (N, H, D, D), "h0")
+    ws = P.workspace(workspace)
+    o = torch.empty(T, H, D, dtype=torch.bfloat16, device="cuda")
+    ht = torch.empty(N, H, D, D, dtype=torch.float32, device="cuda") if want_ht else None
+    if states is True:
+        states = torch.empty(max(states_bytes(P.shape), 16), dtype=torch.uint8, device="cuda")
+    nst = 0 if states is None else states.numel()
+    if gate == "gdn":
+        g = _need(P.flat(g), torch.float32, (T, H), "g")
+        rc = lib().gdr_fwd(ctypes.byref(P.shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta_logit),
+                           _ptr(h0), _ptr(o), _ptr(ht), _ptr(states), nst, _ptr(ws), ws.numel(), _stream())
+    else:
+        g_raw = _need(P.flat(g_raw), torch.bfloat16, (T, H, D), "g_raw")
+        A_log = _need(A_log, torch.float32, (H,), "A_log")
+        dt_bias = _need(dt_bias, torch.float32, (H, D), "dt_bias")
+        rc = lib().kda_fwd(ctypes.byref(P.shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g_raw), _ptr(A_log),
+                           _ptr(dt_bias), _ptr(beta_logit), _ptr(h0), _ptr(o), _ptr(ht), _ptr(states), nst,
+                           _ptr(ws), ws.numel(), _stream())
+    _check(rc, "gdr_fwd" if gate == "gdn" else "kda_fwd")
+    out = {"o": P.unflat(o), "ht": ht}
+    if states is not None:
+        out["states"] = states
+    return out
+
+
+def gdr_fwd(q, k, v, g, beta_logit, h0=None, cu_seqlens=None, num_seqs=None, scale=None, states=None,
+            workspace=None, want_ht=True):
+    """GDN forward.  Returns dict(o, ht[, states]); ``states=True`` allocates and returns the
+    chunk-start states for a later gdr_bwd (or pass a uint8 buffer of states_bytes)."""
+    return _fwd("gdn", q, k, v, beta_logit, h0, cu_seqlens, num_seqs, scale, states, workspace, want_ht, g=g)
+
+
+def kda_fwd(q, k, v, g_raw, A_log, dt_bias, beta_logit, h0=None, cu_seqlens=None, num_seqs=None, scale=None,
+            states=None, workspace=None, want_ht=True):
+    """KDA forward.  Returns dict(o, ht[, states]) as gdr_fwd."""
+    return _fwd("kda", q, k, v, beta_logit, h0, cu_seqlens, num_seqs, scale, states, workspace, want_ht,
+                g_raw=g_raw, A_log=A_log, dt_bias=dt_bias)
+
+
 def gdr_bwd(q, k, v, g, beta_logit, dO, h0=None, dht=None, cu_seqlens=None, num_seqs=None,
             scale=None, states=None, workspace=None, out=None):
     """GDN backward.  Returns dict(dq, dk, dv, dg, dbeta, dh0)."""
@@ -240,7 +289,7 @@ def workspace_status(workspace) -> int:
     return st.value
 
 
-KERNEL_NAMES = ("chunk_table", "prep", "states", "main")
+KERNEL_NAMES = ("chunk_table", "prep", "states", "main", "out")
 
 
 def profile_begin(max_launches: int):

@@ -245,6 +245,38 @@ static gdr_status fwd_states_impl(const gdr_shape* sh, const void* q, const void
     return GDR_OK;
 }
 
+// forward: chunk tiles (with P), the chunk-start states and final states, the output
+static gdr_status fwd_impl(const gdr_shape* sh, const void* q, const void* k, const void* v, const float* g,
+                           const void* g_raw, const float* A_log, const float* dt_bias, const void* beta,
+                           const float* h0, void* o, float* ht, void* states, size_t states_bytes, void* ws,
+                           size_t ws_bytes, void* stream, int kda) {
+    if (gdr_status st0 = check_shape(sh)) return st0;
+    NEED(q); NEED(k); NEED(v); NEED(beta); NEED(ws); NEED(o); OPT(h0); OPT(ht); OPT(states);
+    if (kda) { NEED(g_raw); NEED(A_log); NEED(dt_bias); } else { NEED(g); }
+    const Layout L = layout(sh);
+    if (ws_bytes < L.total) return fail(GDR_ERR_WORKSPACE, "workspace too small%s");
+    if (states && states_bytes < gdr_states_bytes(sh)) return fail(GDR_ERR_WORKSPACE, "states buffer too small%s");
+    Params p;
+    base_params(p, sh, L, ws, kda);
+    p.q = (const __nv_bfloat16*)q; p.k = (const __nv_bfloat16*)k; p.v = (const __nv_bfloat16*)v;
+    p.beta_logit = (const __nv_bfloat16*)beta;
+    p.g = g; p.g_raw = (const __nv_bfloat16*)g_raw; p.A_log = A_log; p.dt_bias = dt_bias;
+    p.h0 = h0;
+    p.o = (__nv_bfloat16*)o;
+    p.ht = ht;
+    if (states) p.S0 = (__nv_bfloat16*)states;
+    p.Pm = p.dS;  // the state-gradient tiles of the backward are free in a forward call
+    cudaStream_t s = (cudaStream_t)stream;
+    gdr_status st = common_front(p, s);
+    if (st != GDR_OK) return st;
+    cudaError_t e = timed(GDR_KERNEL_STATES, s, [&] { return launch_states(p, true, false, s); });
+    if (e != cudaSuccess) return cuda_fail(e, "state recurrence launch");
+    e = timed(GDR_KERNEL_OUT, s, [&] { return launch_out(p, s); });
+    if (e != cudaSuccess) return cuda_fail(e, "output launch");
+    g_err[0] = 0;
+    return GDR_OK;
+}
+
 static gdr_status bwd_impl(const gdr_shape* sh, const void* q, const void* k, const void* v,
                            const float* g, const void* g_raw, const float* A_log, const float* dt_bias,
                            const void* beta, const float* h0, const void* dO, const float* dht,
@@ -315,6 +347,21 @@ gdr_status kda_fwd_states(const gdr_shape* shape, const void* q, const void* k, 
                           void* workspace, size_t workspace_bytes, void* stream) {
     return fwd_states_impl(shape, q, k, v, nullptr, g_raw, A_log, dt_bias, beta_logit, h0, states,
                            states_bytes, workspace, workspace_bytes, stream, 1);
+}
+
+gdr_status gdr_fwd(const gdr_shape* shape, const void* q, const void* k, const void* v, const float* g,
+                   const void* beta_logit, const float* h0, void* o, float* ht, void* states,
+                   size_t states_bytes, void* workspace, size_t workspace_bytes, void* stream) {
+    return fwd_impl(shape, q, k, v, g, nullptr, nullptr, nullptr, beta_logit, h0, o, ht, states, states_bytes,
+                    workspace, workspace_bytes, stream, 0);
+}
+
+gdr_status kda_fwd(const gdr_shape* shape, const void* q, const void* k, const void* v, const void* g_raw,
+                   const float* A_log, const float* dt_bias, const void* beta_logit, const float* h0, void* o,
+                   float* ht, void* states, size_t states_bytes, void* workspace, size_t workspace_bytes,
+                   void* stream) {
+    return fwd_impl(shape, q, k, v, nullptr, g_raw, A_log, dt_bias, beta_logit, h0, o, ht, states, states_bytes,
+                    workspace, workspace_bytes, stream, 1);
 }
 
 gdr_status gdr_bwd(const gdr_shape* shape, const void* q, const void* k, const void* v, const float* g,

@@ -30,6 +30,7 @@ struct Params {
     // per chunk-head tiles: W, U, Kr, R, Rlo [C][D] (D = 64) or channel-major [D][C]
     // (D = 128, the layout the tcgen05 state recurrence reads); T [C][C]
     __nv_bfloat16 *W, *U, *Kr, *R, *Rlo, *Tm;
+    __nv_bfloat16* Pm;                   // forward only: P = lower(qd ki^T) [C][C] per chunk-head, or nullptr
     float *gT, *egT;                     // [chunk][H][D]: chunk gate total and its exponential
     __nv_bfloat16 *S0, *dS;              // per chunk-head states, value-major [dv][dk]
     // time-parallel state passing (seg_G > 1): per (sequence, head) and segment, fp32 key-major
@@ -38,6 +39,8 @@ struct Params {
     float *segL, *segLb, *segP, *segS;
 
     // outputs
+    __nv_bfloat16* o;               // forward output [T,H,D]
+    float* ht;                      // forward final state [N,H,D,D] (key-major), or nullptr
     __nv_bfloat16 *dq, *dk, *dv, *dbeta;
     float* dg;                      // GDN [T,H]
     __nv_bfloat16* dg_raw;          // KDA [T,H,D]
@@ -64,5 +67,6 @@ cudaError_t launch_states(const Params& p, bool fwd, bool bwd, cudaStream_t s);
 cudaError_t launch_states_tc(const Params& p, bool fwd, bool bwd, cudaStream_t s);  // D = 128, tcgen05 + TMA
 cudaError_t launch_main(const Params& p, cudaStream_t s);
 cudaError_t launch_main_tc2(const Params& p, cudaStream_t s);  // GDN and KDA, D = 128, tcgen05 + TMA
+cudaError_t launch_out(const Params& p, cudaStream_t s);       // forward output o = R S0 + P U
 
 }  // namespace gdr

@@ -109,7 +109,9 @@ __global__ void __launch_bounds__(256, 1) k_prep(const Params p) {
             sA[r * SM::LDF + c + 1] = c + 1 < r ? sBeta[r] * a1 : 0.f;
         });
         frag_foreach(accp, m0, n0, [&](int r, int c, float a0, float a1) {
-            *reinterpret_cast<uint32_t*>(sP.ptr(r, c)) = pack_bf16(c <= r ? a0 : 0.f, c + 1 <= r ? a1 : 0.f);
+            const uint32_t w = pack_bf16(c <= r ? a0 : 0.f, c + 1 <= r ? a1 : 0.f);
+            *reinterpret_cast<uint32_t*>(sP.ptr(r, c)) = w;
+            if (p.Pm) *reinterpret_cast<uint32_t*>(p.Pm + tile_cc + r * CH + c) = w;  // forward output
         });
     }
     __syncthreads();

@@ -556,6 +556,11 @@ __global__ void __launch_bounds__(512, 1) k_prep_tc(const Params p, const __grid
             }
             *reinterpret_cast<uint4*>(sP + tc::sw_chunk(r, c0 >> 3, 64)) = make_uint4(w[0], w[1], w[2], w[3]);
             *reinterpret_cast<uint4*>(sP + tc::sw_chunk(r, (c0 >> 3) + 1, 64)) = make_uint4(w[4], w[5], w[6], w[7]);
+            if (p.Pm) {  // forward output: P [r][s] per chunk-head
+                uint4* g = reinterpret_cast<uint4*>(p.Pm + tile_cc + r * CH + c0);
+                g[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                g[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            }
         }
     }
     __syncthreads();

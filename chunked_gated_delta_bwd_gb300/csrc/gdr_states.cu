@@ -164,11 +164,12 @@ __global__ void __launch_bounds__(256) k_states(const Params p, int role0) {
             warp_mma<MT, 2, A_COL, B_ROW>(st, t2, sY, m0, n0, 0, CH);  // - W^T Y
         }
     }
-    if (role == 1) {
+    float* out = role == 1 ? p.dh0 : p.ht;  // dh0, or the forward's final state (if asked)
+    if (out) {
         const size_t sb = ((size_t)seq * p.H + h) * D * D;
         frag_foreach(st, m0, n0, [&](int r, int c, float a0, float a1) {
-            p.dh0[sb + (size_t)r * D + col0 + c] = a0;
-            p.dh0[sb + (size_t)r * D + col0 + c + 1] = a1;
+            out[sb + (size_t)r * D + col0 + c] = a0;
+            out[sb + (size_t)r * D + col0 + c + 1] = a1;
         });
     }
 }

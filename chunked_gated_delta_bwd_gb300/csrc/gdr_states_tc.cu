@@ -105,6 +105,7 @@ __device__ __forceinline__ StateTask decode_task(const Params& p, int mode, int 
         t.cb = cb, t.ce = ce;
         t.init = t.role == 0 ? (p.h0 ? p.h0 + (size_t)pair * DD : nullptr) : (p.dht ? p.dht + (size_t)pair * DD : nullptr);
         if (t.role == 1) t.out = p.dh0 + (size_t)pair * DD;
+        else if (p.ht) t.out = p.ht + (size_t)pair * DD;  // the forward's final state
     } else {
         const int len = (ce - cb + G - 1) / G;
         t.cb = min(cb + g * len, ce), t.ce = min(cb + (g + 1) * len, ce);

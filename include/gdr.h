@@ -100,6 +100,22 @@ gdr_status kda_fwd_states(const gdr_shape* shape, const void* q, const void* k, 
                           size_t states_bytes, void* workspace, size_t workspace_bytes,
                           void* stream);
 
+/* GDN forward: the output o (bf16 [T_total, H, D]) and, if ht is not NULL, the final
+ * state of every sequence and head (fp32 [N, H, D, D], row = key channel), from the
+ * chunked form of the recurrence ("FlashKDA之backward（K1）" §2: per chunk
+ * o = qd S0 + P u with the WY/UT factors).  If `states` is not NULL it also receives
+ * the chunk-start states (the buffer of gdr_fwd_states; states_bytes >=
+ * gdr_states_bytes), so a following gdr_bwd can skip their recomputation.  Uses the
+ * same workspace as gdr_bwd (gdr_workspace_bytes). */
+gdr_status gdr_fwd(const gdr_shape* shape, const void* q, const void* k, const void* v,
+                   const float* g, const void* beta_logit, const float* h0, void* o, float* ht,
+                   void* states, size_t states_bytes, void* workspace, size_t workspace_bytes,
+                   void* stream);
+/* KDA forward (per-channel gate from g_raw, A_log, dt_bias); as gdr_fwd. */
+gdr_status kda_fwd(const gdr_shape* shape, const void* q, const void* k, const void* v,
+                   const void* g_raw, const float* A_log, const float* dt_bias,
+                   const void* beta_logit, const float* h0, void* o, float* ht, void* states,
+                   size_t states_bytes, void* workspace, size_t workspace_bytes, void* stream);
 /* GDN backward ("FlashQLA ... GDN 反向", §一-§二: one call returns dq, dk, dv, dg,
  * dbeta, dh0).  `states` is the buffer from gdr_fwd_states for the same inputs,
  * or NULL to recompute the chunk states inside the call.  dg is the gradient
@@ -163,7 +179,8 @@ const char* gdr_last_error(void);
 #define GDR_KERNEL_PREP 1        /* chunk-parallel intra-chunk preparation */
 #define GDR_KERNEL_STATES 2      /* serial state / state-gradient recurrences */
 #define GDR_KERNEL_MAIN 3        /* chunk-parallel main backward */
-#define GDR_KERNEL_COUNT 4
+#define GDR_KERNEL_OUT 4         /* chunk-parallel forward output (gdr_fwd / kda_fwd) */
+#define GDR_KERNEL_COUNT 5
 gdr_status gdr_profile_begin(int max_launches);
 gdr_status gdr_profile_end(double* total_ms, int* launches);
 

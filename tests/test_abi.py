@@ -28,7 +28,7 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for n in ("gdr_fwd_states", "kda_fwd_states", "gdr_bwd", "kda_bwd", "gdr_workspace_bytes",
+    for n in ("gdr_fwd_states", "kda_fwd_states", "gdr_fwd", "kda_fwd", "gdr_bwd", "kda_bwd", "gdr_workspace_bytes",
               "gdr_states_bytes", "gdr_workspace_status", "gdr_last_error"):
         assert n in names
 
@@ -112,6 +112,41 @@ def test_states_buffer_too_small_rejected(L):
     A = ctypes.c_void_p(4096)
     rc = L.gdr_fwd_states(ctypes.byref(sh), A, A, A, A, A, None, A, st - 1, A, ws, None)
     assert rc == 3
+
+
+def test_forward_arguments_rejected(L):
+    # gdr_fwd(shape, q, k, v, g, beta, h0, o, ht, states, states_bytes, ws, ws_bytes, stream)
+    sh = gdr.make_shape(2, 128, 2, 64)
+    ws = gdr.workspace_bytes(sh)
+    st = gdr.states_bytes(sh)
+    A = ctypes.c_void_p(4096)
+    args = [A, A, A, A, A, None, A, None, None, 0, A, ws, None]
+    for i in (0, 1, 2, 3, 4, 6, 10):  # q, k, v, g, beta, o, workspace are required
+        bad = list(args)
+        bad[i] = None
+        assert L.gdr_fwd(ctypes.byref(sh), *bad) == 1, i
+        bad[i] = ctypes.c_void_p(4096 + 8)
+        assert L.gdr_fwd(ctypes.byref(sh), *bad) == 1, i
+    for i in (5, 7, 8):  # h0, ht, states are optional but must be aligned
+        bad = list(args)
+        bad[i] = ctypes.c_void_p(4096 + 8)
+        if i == 8:
+            bad[9] = st
+        assert L.gdr_fwd(ctypes.byref(sh), *bad) == 1, i
+    small = list(args)
+    small[11] = ws - 1
+    assert L.gdr_fwd(ctypes.byref(sh), *small) == 3
+    small = list(args)
+    small[8], small[9] = A, st - 1
+    assert L.gdr_fwd(ctypes.byref(sh), *small) == 3
+    # kda_fwd: g_raw, A_log, dt_bias are required
+    kargs = [A, A, A, A, A, A, A, None, A, None, None, 0, A, ws, None]
+    for i in (3, 4, 5):
+        bad = list(kargs)
+        bad[i] = None
+        assert L.kda_fwd(ctypes.byref(sh), *bad) == 1, i
+    sh_bad = gdr.make_shape(2, 128, 2, 96)
+    assert L.kda_fwd(ctypes.byref(sh_bad), *kargs) == 2
 
 
 def test_product_path_fails_loudly_without_library(monkeypatch):

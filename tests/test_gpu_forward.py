@@ -1,0 +1,88 @@
+"""GPU parity of the forward (gdr_fwd / kda_fwd: output o and final state ht) against
+the float64 oracle's forward on the same seeded inputs.  Tolerances: relative L2
+<= 2e-2 for o (a bf16 output, like the gradients) and <= 5e-3 for ht (fp32, built
+from bf16 chunk tiles; the derivation is beside TOL_HT in tests/helpers.py)."""
+import pytest
+import torch
+
+from chunked_gated_delta_bwd_gb300 import inputs
+from tests import helpers as H
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from chunked_gated_delta_bwd_gb300 import build
+    build.build()
+
+
+def _check(x, heads=None, label=""):
+    gpu = H.run_gpu_fwd(x)
+    ref = H.run_oracle_fwd(x, heads)
+    print(label, H.assert_parity(H.compare_fwd(gpu, ref, heads), label))
+    return gpu
+
+
+def test_gdn_tiny_config():
+    _check(inputs.make(inputs.CASES["gdn_tiny"]), label="fwd_gdn_tiny")
+
+
+@pytest.mark.parametrize("mode", ["gdn", "kda"])
+@pytest.mark.parametrize("dim", [64, 128])
+def test_varlen_ragged_with_h0(mode, dim):
+    x = inputs.custom(mode, [1, 63, 64, 65, 200, 130], heads=3, dim=dim, seed=111, with_h0=True)
+    _check(x, label="fwd_%s_ragged_d%d" % (mode, dim))
+
+
+@pytest.mark.parametrize("dim", [64, 128])
+def test_empty_and_single_token_sequences(dim):
+    x = inputs.custom("kda", [0, 1, 0, 64, 1], heads=2, dim=dim, seed=112, with_h0=True)
+    gpu = _check(x, label="fwd_empty_d%d" % dim)
+    # an empty sequence leaves its initial state unchanged
+    torch.testing.assert_close(gpu["ht"][0], x["h0"][0], rtol=0, atol=0)
+    torch.testing.assert_close(gpu["ht"][2], x["h0"][2], rtol=0, atol=0)
+
+
+@pytest.mark.parametrize("mode", ["gdn", "kda"])
+def test_forward_states_feed_the_backward(mode):
+    # the chunk-start states kept by the forward equal gdr_fwd_states's, and a backward from
+    # them equals the backward that recomputes them
+    import chunked_gated_delta_bwd_gb300 as gdr
+    x = inputs.custom(mode, [200, 77], heads=2, dim=128, seed=113, with_h0=True, with_dht=True)
+    d = H.to_gpu(x)
+    kw = dict(h0=d["h0"], cu_seqlens=d["cu_seqlens"], scale=d["scale"])
+    if mode == "gdn":
+        ref_states = gdr.gdr_fwd_states(d["q"], d["k"], d["v"], d["g"], d["beta_logit"], **kw)
+    else:
+        ref_states = gdr.gdr_fwd_states(d["q"], d["k"], d["v"], None, d["beta_logit"], gate="kda",
+                                        g_raw=d["g_raw"], A_log=d["A_log"], dt_bias=d["dt_bias"], **kw)
+    fwd = H.run_gpu_fwd(x, states=True)
+    assert torch.equal(fwd["states"], ref_states.cpu())
+    a = H.run_gpu(x, states=fwd["states"].cuda())
+    b = H.run_gpu(x)
+    for k in a:
+        if k in ("dA_log", "ddt_bias"):
+            torch.testing.assert_close(a[k], b[k], rtol=1e-5, atol=1e-6)
+        else:
+            assert torch.equal(a[k], b[k]), k
+
+
+def test_forward_is_deterministic():
+    x = inputs.custom("gdn", [500, 3], heads=4, dim=128, seed=114, with_h0=True)
+    a, b = H.run_gpu_fwd(x), H.run_gpu_fwd(x)
+    for k in a:
+        assert torch.equal(a[k], b[k]), k
+
+
+@pytest.mark.parametrize("name,heads", [
+    ("gdn_b2_h16_t4k", [0, 15]),
+    ("kda_b1_h16_t8k", [0, 15]),
+    ("gdn_varlen_h32", [0, 31]),
+    ("gdn_h16_t32k", [3]),
+    ("kda_h16_t32k", [12]),
+])
+def test_full_size_sampled_heads(name, heads):
+    _check(inputs.make(inputs.CASES[name]), heads=heads, label="fwd_" + name)
