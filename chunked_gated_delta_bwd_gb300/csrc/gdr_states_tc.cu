@@ -70,8 +70,12 @@ struct StateTask {
 //   1  segment phase 1, 3G - 4 CTAs per (sequence, head): role 0 from segments 0 .. G-2
 //      (segment 0 from h0, the others from zero), role 1 from segments 1 .. G-1 (segment
 //      G-1 from dht, the others from zero), and the transitions of segments 1 .. G-2
+//   2  segment phase 1 of a forward-only call, 2G - 3 CTAs per (sequence, head): the role-0
+//      chains and the transitions of mode 1
 //   3  segment phase 3, 2G CTAs per (sequence, head): every segment of both roles from
 //      its true start state, saving the per-chunk states (and dh0)
+//   4  segment phase 3 of a forward-only call, G CTAs per (sequence, head): role 0 (and the
+//      final state of the last segment, if asked)
 __device__ __forceinline__ StateTask decode_task(const Params& p, int mode, int role0) {
     StateTask t;
     const int G = p.seg_G, DD = 128 * 128;
@@ -79,19 +83,20 @@ __device__ __forceinline__ StateTask decode_task(const Params& p, int mode, int 
     if (mode == 0) {
         pair = blockIdx.x;
         t.role = role0 + blockIdx.y;
-    } else if (mode == 1) {
-        const int K = 3 * G - 4, k = blockIdx.x % K;
+    } else if (mode == 1 || mode == 2) {
+        const int K = mode == 1 ? 3 * G - 4 : 2 * G - 3, k = blockIdx.x % K;
         pair = blockIdx.x / K;
         if (k < G - 1) {
             t.role = 0, g = k;
-        } else if (k < 2 * G - 2) {
+        } else if (mode == 1 && k < 2 * G - 2) {
             t.role = 1, g = k - (G - 1) + 1;
         } else {
-            t.role = 0, g = k - (2 * G - 2) + 1, kind = 1;
+            t.role = 0, g = k - (mode == 1 ? 2 * G - 2 : G - 1) + 1, kind = 1;
         }
     } else {
-        pair = blockIdx.x / (2 * G);
-        const int rem = blockIdx.x % (2 * G);
+        const int per = mode == 3 ? 2 * G : G;
+        pair = blockIdx.x / per;
+        const int rem = blockIdx.x % per;
         t.role = rem / G, g = rem % G;
     }
     t.seq = pair / p.H, t.h = pair % p.H;
@@ -99,7 +104,7 @@ __device__ __forceinline__ StateTask decode_task(const Params& p, int mode, int 
     const size_t pd = (size_t)pair * G;
     t.input = kind == 0;
     t.identity = kind == 1;
-    t.save = mode != 1;
+    t.save = mode != 1 && mode != 2;
     t.out = nullptr;
     if (mode == 0) {
         t.cb = cb, t.ce = ce;
@@ -111,7 +116,7 @@ __device__ __forceinline__ StateTask decode_task(const Params& p, int mode, int 
         t.cb = min(cb + g * len, ce), t.ce = min(cb + (g + 1) * len, ce);
         const float* h0 = p.h0 ? p.h0 + (size_t)pair * DD : nullptr;
         const float* dht = p.dht ? p.dht + (size_t)pair * DD : nullptr;
-        if (mode == 1) {
+        if (mode == 1 || mode == 2) {
             t.init = kind == 1 ? nullptr : t.role == 0 ? (g == 0 ? h0 : nullptr) : (g == G - 1 ? dht : nullptr);
             t.out = (kind == 1 ? p.segP : t.role == 0 ? p.segL : p.segLb) + (pd + g) * DD;
         } else {
@@ -120,6 +125,7 @@ __device__ __forceinline__ StateTask decode_task(const Params& p, int mode, int 
             else
                 t.init = g == G - 1 ? dht : p.segS + ((pd + g) * 2 + 1) * DD;
             if (t.role == 1 && g == 0) t.out = p.dh0 + (size_t)pair * DD;
+            if (t.role == 0 && g == G - 1 && p.ht) t.out = p.ht + (size_t)pair * DD;
         }
     }
     return t;
@@ -440,16 +446,18 @@ cudaError_t launch_states_tc(const Params& p, bool fwd, bool bwd, cudaStream_t s
     cudaError_t e = cudaFuncSetAttribute(k_states_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int pairs = p.N * p.H;
-    if (p.seg_G >= 2 && fwd && bwd) {
-        // time-parallel segments: phase 1 chains, the boundaries, phase 3 chains
-        k_states_tc<<<pairs * (3 * p.seg_G - 4), NTHREADS, SMEM_BYTES, s>>>(p, 1, 0, m);
+    if (p.seg_G >= 2 && fwd) {
+        // time-parallel segments: phase 1 chains, the boundaries, phase 3 chains (both roles,
+        // or role 0 alone in a forward-only call)
+        const int G = p.seg_G;
+        k_states_tc<<<pairs * (bwd ? 3 * G - 4 : 2 * G - 3), NTHREADS, SMEM_BYTES, s>>>(p, bwd ? 1 : 2, 0, m);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         const int cbytes = 2 * 128 * 128 * 4;
         e = cudaFuncSetAttribute(k_seg_combine, cudaFuncAttributeMaxDynamicSharedMemorySize, cbytes);
         if (e != cudaSuccess) return e;
-        k_seg_combine<<<dim3(pairs, 2), 512, cbytes, s>>>(p);
+        k_seg_combine<<<dim3(pairs, bwd ? 2 : 1), 512, cbytes, s>>>(p);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        k_states_tc<<<pairs * 2 * p.seg_G, NTHREADS, SMEM_BYTES, s>>>(p, 3, 0, m);
+        k_states_tc<<<pairs * (bwd ? 2 * G : G), NTHREADS, SMEM_BYTES, s>>>(p, bwd ? 3 : 4, 0, m);
         return cudaGetLastError();
     }
     const int role0 = fwd ? 0 : 1, nroles = (fwd && bwd) ? 2 : 1;

@@ -70,6 +70,14 @@ def test_forward_states_feed_the_backward(mode):
             assert torch.equal(a[k], b[k]), k
 
 
+@pytest.mark.parametrize("mode", ["gdn", "kda"])
+def test_segmented_forward_varlen(mode):
+    # few (sequence, head) pairs and a long sequence: the forward's state chains run as
+    # time-parallel segments (3 here); the 64-token sequence leaves two segments empty
+    x = inputs.custom(mode, [16000, 64], heads=2, dim=128, seed=115, with_h0=True)
+    _check(x, label="fwd_segments_%s" % mode)
+
+
 def test_forward_is_deterministic():
     x = inputs.custom("gdn", [500, 3], heads=4, dim=128, seed=114, with_h0=True)
     a, b = H.run_gpu_fwd(x), H.run_gpu_fwd(x)
