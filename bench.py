@@ -396,24 +396,31 @@ def main_gpu(args):
 
 
 def run_profile_case(args):
-    """Small case for ncu captures: a few GDN or KDA backwards at B=1 H=16 T=8192 D=128
-    (inputs ~150 MB, larger than L2); no timing line."""
+    """Small case for ncu captures: a few GDN or KDA backwards (or, with the _fwd cases,
+    forwards) at B=1 H=16 T=8192 D=128 (inputs ~150 MB, larger than L2); no timing line."""
     import chunked_gated_delta_bwd_gb300 as gdr
     from chunked_gated_delta_bwd_gb300 import build
     build.build()
-    mode = args.profile_case
+    mode = args.profile_case.replace("_fwd", "")
+    fwd = args.profile_case.endswith("_fwd")
     case = inputs.Case("profile_" + mode, mode, 1, 8192, 16, 128, seed=5, with_h0=True, with_dht=True)
     x = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inputs.make(case).items()}
     ws = torch.empty(gdr.workspace_bytes(gdr.make_shape(1, 8192, 16, 128)), dtype=torch.uint8, device="cuda")
     for _ in range(args.steps):
-        if mode == "gdn":
+        if fwd and mode == "gdn":
+            gdr.gdr_fwd(x["q"], x["k"], x["v"], x["g"], x["beta_logit"], h0=x["h0"], num_seqs=1,
+                        scale=x["scale"], workspace=ws)
+        elif fwd:
+            gdr.kda_fwd(x["q"], x["k"], x["v"], x["g_raw"], x["A_log"], x["dt_bias"], x["beta_logit"],
+                        h0=x["h0"], num_seqs=1, scale=x["scale"], workspace=ws)
+        elif mode == "gdn":
             gdr.gdr_bwd(x["q"], x["k"], x["v"], x["g"], x["beta_logit"], x["dO"], h0=x["h0"], dht=x["dht"],
                         num_seqs=1, scale=x["scale"], workspace=ws)
         else:
             gdr.kda_bwd(x["q"], x["k"], x["v"], x["g_raw"], x["A_log"], x["dt_bias"], x["beta_logit"],
                         x["dO"], h0=x["h0"], dht=x["dht"], num_seqs=1, scale=x["scale"], workspace=ws)
     torch.cuda.synchronize()
-    print("profile case %s: %d backward calls done" % (mode, args.steps))
+    print("profile case %s: %d calls done" % (args.profile_case, args.steps))
 
 
 def build_sha():
@@ -434,7 +441,7 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=8192)
     ap.add_argument("--ref-tokens", type=int, default=1024)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile-case", choices=["gdn", "kda"], default=None,
+    ap.add_argument("--profile-case", choices=["gdn", "kda", "gdn_fwd", "kda_fwd"], default=None,
                     help="run a small case (B=1 H=16 T=8192) for ncu captures instead of the benchmark")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
