@@ -285,6 +285,35 @@ def main_gpu(args):
     fms_k = fwd_loop("kda", lambda A=K: gdr.kda_fwd(A["q"], A["k"], A["v"], A["g_raw"], A["A_log"], A["dt_bias"],
                                                    A["beta_logit"], h0=A["h0"], num_seqs=N, scale=A["scale"],
                                                    workspace=ws_k))
+    # the backward from saved chunk states (the forward kept them): no forward recurrence
+    saved = {}
+    st_g = gdr.gdr_fwd_states(G["q"], G["k"], G["v"], G["g"], G["beta_logit"], h0=G["h0"], num_seqs=N,
+                              scale=G["scale"], workspace=ws_g)
+    st_k = gdr.gdr_fwd_states(K["q"], K["k"], K["v"], None, K["beta_logit"], h0=K["h0"], num_seqs=N,
+                              scale=K["scale"], workspace=ws_k, gate="kda", g_raw=K["g_raw"], A_log=K["A_log"],
+                              dt_bias=K["dt_bias"])
+    saved_kernels = {}
+
+    def saved_loop(name, fn, n=max(3, args.steps // 2)):
+        fn()
+        torch.cuda.synchronize()
+        api.profile_begin(8 * n)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        saved_kernels[name] = {k: round(v[0] / n, 4) for k, v in api.profile_end().items() if v[1]}
+        saved[name] = a.elapsed_time(b) / n
+    saved_loop("gdn", lambda A=G, o=out_g: gdr.gdr_bwd(A["q"], A["k"], A["v"], A["g"], A["beta_logit"], A["dO"],
+                                                       h0=A["h0"], dht=A["dht"], num_seqs=N, scale=A["scale"],
+                                                       states=st_g, workspace=ws_g, out=o))
+    saved_loop("kda", lambda A=K, o=out_k: gdr.kda_bwd(A["q"], A["k"], A["v"], A["g_raw"], A["A_log"],
+                                                       A["dt_bias"], A["beta_logit"], A["dO"], h0=A["h0"],
+                                                       dht=A["dht"], num_seqs=N, scale=A["scale"], states=st_k,
+                                                       workspace=ws_k, out=o))
+    del st_g, st_k
     th_v = CASE_G.seq_len * CASE_G.heads
     out_ms = (fwd_kernels["gdn"].get("out", 0.0) + fwd_kernels["kda"].get("out", 0.0)) / 2
     forward = {
@@ -382,6 +411,7 @@ def main_gpu(args):
         "kernels_ms_per_step": {k: v[0] / args.steps for k, v in prof.items()},
         "kernels_ms_per_variant": per_variant,
         "forward": forward,
+        "bwd_from_saved_states": {"ms_per_variant": saved, "kernels_ms_per_variant": saved_kernels},
         "gpu_launches": launches,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms},
@@ -423,11 +453,16 @@ def run_profile_case(args):
     print("profile case %s: %d calls done" % (args.profile_case, args.steps))
 
 
+# the sources that define the main kernel (its .cu file and the headers it includes)
+MAIN_SOURCES = ("gdr_main_tc2.cu", "gdr_chunk.cuh", "gdr_common.cuh", "gdr_tc.cuh", "gdr_tma.h", "gdr_internal.h")
+
+
 def build_sha():
+    """Hash of the main kernel's sources: the stored DRAM traffic is reported only while it matches."""
     import hashlib
     h = hashlib.sha1()
     csrc = os.path.join(ROOT, "chunked_gated_delta_bwd_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in MAIN_SOURCES:
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:12]
 

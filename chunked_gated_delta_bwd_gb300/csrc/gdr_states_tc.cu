@@ -65,48 +65,50 @@ struct StateTask {
     float* out;
 };
 
-// Launch modes:
-//   0  one chain per (sequence, head, role) over the whole sequence (blockIdx.y = role)
-//   1  segment phase 1, 3G - 4 CTAs per (sequence, head): role 0 from segments 0 .. G-2
-//      (segment 0 from h0, the others from zero), role 1 from segments 1 .. G-1 (segment
-//      G-1 from dht, the others from zero), and the transitions of segments 1 .. G-2
-//   2  segment phase 1 of a forward-only call, 2G - 3 CTAs per (sequence, head): the role-0
-//      chains and the transitions of mode 1
-//   3  segment phase 3, 2G CTAs per (sequence, head): every segment of both roles from
-//      its true start state, saving the per-chunk states (and dh0)
-//   4  segment phase 3 of a forward-only call, G CTAs per (sequence, head): role 0 (and the
-//      final state of the last segment, if asked)
-__device__ __forceinline__ StateTask decode_task(const Params& p, int mode, int role0) {
+// Launch forms (phase, roles; roles: 1 = role 0, 2 = role 1, 3 = both):
+//   phase 0  one chain per (sequence, head, asked role) over the whole sequence
+//            (blockIdx.y picks the role when both are asked)
+//   phase 1  segment phase 1, per (sequence, head): the role-0 chains of segments 0 .. G-2
+//            (segment 0 from h0, the others from zero) and the role-1 chains of segments
+//            1 .. G-1 (segment G-1 from dht, the others from zero), each if its role is
+//            asked, and the transition chains of segments 1 .. G-2
+//   phase 3  segment phase 3, per (sequence, head): every segment of each asked role from
+//            its true start state, saving the per-chunk states (and dh0 / ht)
+__host__ __device__ inline int phase1_tasks(int G, int roles) {
+    return ((roles & 1) ? G - 1 : 0) + ((roles & 2) ? G - 1 : 0) + G - 2;
+}
+__device__ __forceinline__ StateTask decode_task(const Params& p, int phase, int roles) {
     StateTask t;
     const int G = p.seg_G, DD = 128 * 128;
     int pair, g = 0, kind = 0;  // kind: 0 data chain, 1 transition chain
-    if (mode == 0) {
+    if (phase == 0) {
         pair = blockIdx.x;
-        t.role = role0 + blockIdx.y;
-    } else if (mode == 1 || mode == 2) {
-        const int K = mode == 1 ? 3 * G - 4 : 2 * G - 3, k = blockIdx.x % K;
+        t.role = roles == 2 ? 1 : (int)blockIdx.y;
+    } else if (phase == 1) {
+        const int n0 = (roles & 1) ? G - 1 : 0, n1 = (roles & 2) ? G - 1 : 0;
+        const int K = phase1_tasks(G, roles), k = blockIdx.x % K;
         pair = blockIdx.x / K;
-        if (k < G - 1) {
+        if (k < n0) {
             t.role = 0, g = k;
-        } else if (mode == 1 && k < 2 * G - 2) {
-            t.role = 1, g = k - (G - 1) + 1;
+        } else if (k < n0 + n1) {
+            t.role = 1, g = k - n0 + 1;
         } else {
-            t.role = 0, g = k - (mode == 1 ? 2 * G - 2 : G - 1) + 1, kind = 1;
+            t.role = 0, g = k - n0 - n1 + 1, kind = 1;
         }
     } else {
-        const int per = mode == 3 ? 2 * G : G;
+        const int per = (roles == 3 ? 2 : 1) * G;
         pair = blockIdx.x / per;
         const int rem = blockIdx.x % per;
-        t.role = rem / G, g = rem % G;
+        t.role = roles == 3 ? rem / G : (roles == 1 ? 0 : 1), g = rem % G;
     }
     t.seq = pair / p.H, t.h = pair % p.H;
     const int cb = seq_chunk_begin(p, t.seq), ce = seq_chunk_begin(p, t.seq + 1);
     const size_t pd = (size_t)pair * G;
     t.input = kind == 0;
     t.identity = kind == 1;
-    t.save = mode != 1 && mode != 2;
+    t.save = phase != 1;
     t.out = nullptr;
-    if (mode == 0) {
+    if (phase == 0) {
         t.cb = cb, t.ce = ce;
         t.init = t.role == 0 ? (p.h0 ? p.h0 + (size_t)pair * DD : nullptr) : (p.dht ? p.dht + (size_t)pair * DD : nullptr);
         if (t.role == 1) t.out = p.dh0 + (size_t)pair * DD;
@@ -116,7 +118,7 @@ __device__ __forceinline__ StateTask decode_task(const Params& p, int mode, int 
         t.cb = min(cb + g * len, ce), t.ce = min(cb + (g + 1) * len, ce);
         const float* h0 = p.h0 ? p.h0 + (size_t)pair * DD : nullptr;
         const float* dht = p.dht ? p.dht + (size_t)pair * DD : nullptr;
-        if (mode == 1 || mode == 2) {
+        if (phase == 1) {
             t.init = kind == 1 ? nullptr : t.role == 0 ? (g == 0 ? h0 : nullptr) : (g == G - 1 ? dht : nullptr);
             t.out = (kind == 1 ? p.segP : t.role == 0 ? p.segL : p.segLb) + (pd + g) * DD;
         } else {
@@ -133,13 +135,13 @@ __device__ __forceinline__ StateTask decode_task(const Params& p, int mode, int 
 
 }  // namespace
 
-__global__ void __launch_bounds__(NTHREADS, 1) k_states_tc(const Params p, int mode, int role0,
+__global__ void __launch_bounds__(NTHREADS, 1) k_states_tc(const Params p, int phase, int roles,
                                                            const __grid_constant__ StateMaps m) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     const uint32_t sb = smem_u32(smem);
 
-    const StateTask task = decode_task(p, mode, role0);
+    const StateTask task = decode_task(p, phase, roles);
     const int role = task.role, seq = task.seq, h = task.h;
     const int cb = task.cb, ce = task.ce;
     const int n = ce - cb;
@@ -376,11 +378,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_states_tc(const Params p, int m
 // Key-major states S [d][j]; a segment maps S_start to P^T S_start + L (role 0, the
 // transition chain stores P^T key-major) and dS_enter to P dS_enter + L' (role 1).  Each
 // thread owns a 4 x 8 block of the 128 x 128 result (rows 4 rb .., columns 8 cb ..).
-__global__ void __launch_bounds__(512) k_seg_combine(const Params p) {
+__global__ void __launch_bounds__(512) k_seg_combine(const Params p, int roles) {
     extern __shared__ float sm[];
     float* cur = sm;              // [128][128] the state crossing the boundary
     float* tr = sm + 128 * 128;   // [128][128] the segment's transition (P^T, key-major)
-    const int pair = blockIdx.x, role = blockIdx.y, G = p.seg_G, DD = 128 * 128;
+    const int pair = blockIdx.x, role = roles == 3 ? (int)blockIdx.y : (roles == 1 ? 0 : 1), G = p.seg_G,
+              DD = 128 * 128;
     const size_t pd = (size_t)pair * G;
     const int tid = threadIdx.x, rb = tid >> 4, cb = tid & 15;
     const float* first = role == 0 ? p.segL + (pd + 0) * DD : p.segLb + (pd + G - 1) * DD;
@@ -446,23 +449,21 @@ cudaError_t launch_states_tc(const Params& p, bool fwd, bool bwd, cudaStream_t s
     cudaError_t e = cudaFuncSetAttribute(k_states_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int pairs = p.N * p.H;
-    if (p.seg_G >= 2 && fwd) {
-        // time-parallel segments: phase 1 chains, the boundaries, phase 3 chains (both roles,
-        // or role 0 alone in a forward-only call)
+    const int roles = (fwd ? 1 : 0) | (bwd ? 2 : 0), nroles = roles == 3 ? 2 : 1;
+    if (p.seg_G >= 2) {
+        // time-parallel segments: phase 1 chains, the boundaries, phase 3 chains
         const int G = p.seg_G;
-        k_states_tc<<<pairs * (bwd ? 3 * G - 4 : 2 * G - 3), NTHREADS, SMEM_BYTES, s>>>(p, bwd ? 1 : 2, 0, m);
+        k_states_tc<<<pairs * phase1_tasks(G, roles), NTHREADS, SMEM_BYTES, s>>>(p, 1, roles, m);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         const int cbytes = 2 * 128 * 128 * 4;
         e = cudaFuncSetAttribute(k_seg_combine, cudaFuncAttributeMaxDynamicSharedMemorySize, cbytes);
         if (e != cudaSuccess) return e;
-        k_seg_combine<<<dim3(pairs, bwd ? 2 : 1), 512, cbytes, s>>>(p);
+        k_seg_combine<<<dim3(pairs, nroles), 512, cbytes, s>>>(p, roles);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        k_states_tc<<<pairs * (bwd ? 2 * G : G), NTHREADS, SMEM_BYTES, s>>>(p, bwd ? 3 : 4, 0, m);
+        k_states_tc<<<pairs * nroles * G, NTHREADS, SMEM_BYTES, s>>>(p, 3, roles, m);
         return cudaGetLastError();
     }
-    const int role0 = fwd ? 0 : 1, nroles = (fwd && bwd) ? 2 : 1;
-    dim3 grid(pairs, nroles);
-    k_states_tc<<<grid, NTHREADS, SMEM_BYTES, s>>>(p, 0, role0, m);
+    k_states_tc<<<dim3(pairs, nroles), NTHREADS, SMEM_BYTES, s>>>(p, 0, roles, m);
     return cudaGetLastError();
 }
 
