@@ -124,21 +124,50 @@ def kda_gate(g_raw, A_log, dt_bias):
     return -np.exp(A_log)[None, :, None] * softplus(g_raw + dt_bias[None, :, :])
 
 
+LN2 = np.log(2.0)
+
+
+def kda_sigmoid_gate(g_raw, A_log, dt_bias, gate_scale):
+    """Sigmoid-bounded per-channel log gate of the FlashKDA kernels ("FlashKDA之backward（K1）",
+    §5.2: the base-2 log gate is gate_scale * sigmoid(e^{A_log[h]} (g_raw + dt_bias[h, d]))),
+    written as a natural-log gate: ln 2 * gate_scale * sigmoid(e^{A_log} (g_raw + dt_bias))."""
+    g_raw, A_log, dt_bias = map(_f64, (g_raw, A_log, dt_bias))
+    z = np.exp(A_log)[None, :, None] * (g_raw + dt_bias[None, :, :])
+    return LN2 * float(gate_scale) * sigmoid(z)
+
+
 def kda(q, k, v, g_raw, A_log, dt_bias, beta_logit, scale, cu_seqlens, h0=None, dO=None,
-        dht=None, nthreads=0):
+        dht=None, nthreads=0, gate="softplus", gate_scale=None):
     """KDA: per-channel gate from ``g_raw`` [T,H,D], ``A_log`` [H], ``dt_bias`` [H,D].
 
-    Backward returns ``dg_raw`` [T,H,D], ``dA_log`` [H] and ``ddt_bias`` [H,D]
-    in place of ``dg``.
+    ``gate="softplus"``: g = -e^{A_log} softplus(g_raw + dt_bias); ``gate="sigmoid"``: the
+    sigmoid-bounded gate of ``kda_sigmoid_gate`` with ``gate_scale``.  Backward returns
+    ``dg_raw`` [T,H,D], ``dA_log`` [H] and ``ddt_bias`` [H,D] in place of ``dg``.
     """
     g_raw, A_log, dt_bias = map(_f64, (g_raw, A_log, dt_bias))
-    glog = kda_gate(g_raw, A_log, dt_bias)
+    if gate == "softplus":
+        glog = kda_gate(g_raw, A_log, dt_bias)
+    elif gate == "sigmoid":
+        glog = kda_sigmoid_gate(g_raw, A_log, dt_bias, gate_scale)
+    else:
+        raise ValueError("gate must be 'softplus' or 'sigmoid'")
     out = gated_delta(q, k, v, glog, beta_logit, scale, cu_seqlens, h0, dO, dht, nthreads)
     if "dglog" in out:
         dglog = out.pop("dglog")
+        a = np.exp(A_log)[None, :, None]
         x = g_raw + dt_bias[None, :, :]
-        dg_raw = dglog * (-np.exp(A_log)[None, :, None] * sigmoid(x))
+        if gate == "softplus":
+            # g = -a softplus(x): dg/dx = -a sigmoid(x), dg/dA_log = g
+            dg_raw = dglog * (-a * sigmoid(x))
+            dA = dglog * glog
+        else:
+            # g = ln2 gs sigmoid(z), z = a x: dg/dz = ln2 gs s (1 - s); dz/dx = a, dz/dA_log = a x
+            s = sigmoid(a * x)
+            dz = dglog * LN2 * float(gate_scale) * s * (1.0 - s)
+            dg_raw = dz * a
+            dA = dz * a * x
         out["dg_raw"] = dg_raw
         out["ddt_bias"] = dg_raw.sum(axis=0)
-        out["dA_log"] = (dglog * glog).sum(axis=(0, 2))
+        out["dA_log"] = dA.sum(axis=(0, 2))
+        out["dA_terms"] = dA  # per-element terms of dA_log (their magnitudes condition short sums)
     return out

@@ -51,9 +51,9 @@ def _loss_gdn(c):
     return L
 
 
-def _loss_kda(c):
+def _loss_kda(c, gate="softplus", gate_scale=None):
     r = oracle.kda(c["q"], c["k"], c["v"], c["g_raw"], c["A_log"], c["dt_bias"], c["b"],
-                   c["scale"], c["cu"], h0=c["h0"])
+                   c["scale"], c["cu"], h0=c["h0"], gate=gate, gate_scale=gate_scale)
     L = (r["o"] * c["dO"]).sum()
     if c["dht"] is not None:
         L += (r["ht"] * c["dht"]).sum()
@@ -106,16 +106,37 @@ def test_gdn_backward_matches_fd(lens, D, sample):
         _check(fd, ref, name)
 
 
-def test_kda_backward_matches_fd():
+@pytest.mark.parametrize("gate,gate_scale", [("softplus", None), ("sigmoid", -2.0)])
+def test_kda_backward_matches_fd(gate, gate_scale):
     rng = np.random.default_rng(12)
     c = _rand_case(rng, (4, 3), 2, 4, "kda")
     an = oracle.kda(c["q"], c["k"], c["v"], c["g_raw"], c["A_log"], c["dt_bias"], c["b"],
-                    c["scale"], c["cu"], h0=c["h0"], dO=c["dO"], dht=c["dht"])
+                    c["scale"], c["cu"], h0=c["h0"], dO=c["dO"], dht=c["dht"], gate=gate, gate_scale=gate_scale)
     for name, key in (("q", "dq"), ("k", "dk"), ("v", "dv"), ("g_raw", "dg_raw"),
                       ("A_log", "dA_log"), ("dt_bias", "ddt_bias"), ("b", "dbeta"),
                       ("h0", "dh0")):
-        fd = central_grad(lambda: _loss_kda(c), c[name])
+        fd = central_grad(lambda: _loss_kda(c, gate, gate_scale), c[name])
         _check(fd, an[key].reshape(-1), name)
+
+
+def test_sigmoid_gate_value_at_vanishing_slope():
+    # with e^{A_log} -> 0 the sigmoid-bounded gate is ln2 * gate_scale * sigmoid(0) = ln2 * gate_scale / 2
+    # for every token and channel, so the KDA path equals the plain recurrence with that constant
+    # log gate, and no gradient reaches g_raw
+    rng = np.random.default_rng(21)
+    c = _rand_case(rng, (9, 5), 2, 4, "kda")
+    c["A_log"] = np.full(2, -60.0)
+    gs = -3.0
+    a = oracle.kda(c["q"], c["k"], c["v"], c["g_raw"], c["A_log"], c["dt_bias"], c["b"], c["scale"], c["cu"],
+                   h0=c["h0"], dO=c["dO"], dht=c["dht"], gate="sigmoid", gate_scale=gs)
+    glog = np.full(c["q"].shape, np.log(2.0) * gs / 2)
+    b = oracle.gated_delta(c["q"], c["k"], c["v"], glog, c["b"], c["scale"], c["cu"], h0=c["h0"], dO=c["dO"],
+                           dht=c["dht"])
+    for key in ("o", "ht", "dq", "dk", "dv", "dbeta", "dh0"):
+        np.testing.assert_allclose(a[key], b[key], rtol=1e-12, atol=1e-12, err_msg=key)
+    assert np.abs(a["dg_raw"]).max() < 1e-20
+    # and the gate parameters' gradients are the chain-rule sums of the per-element terms
+    np.testing.assert_allclose(a["ddt_bias"], a["dg_raw"].sum(axis=0), rtol=1e-12, atol=0)
 
 
 def test_dht_gradient_is_the_final_state():
