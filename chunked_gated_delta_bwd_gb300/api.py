@@ -27,7 +27,10 @@ GDR_DEV_GATE_RANGE = 2
 class GdrShape(ctypes.Structure):
     _fields_ = [("num_seqs", ctypes.c_int32), ("total_tokens", ctypes.c_int64),
                 ("num_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
-                ("cu_seqlens", ctypes.c_void_p), ("scale", ctypes.c_float)]
+                ("cu_seqlens", ctypes.c_void_p), ("scale", ctypes.c_float),
+                ("kda_gate", ctypes.c_int32), ("gate_scale", ctypes.c_float)]
+
+KDA_GATES = {"softplus": 0, "sigmoid": 1}  # GDR_KDA_GATE_SOFTPLUS / GDR_KDA_GATE_SIGMOID
 
 
 class GdrError(RuntimeError):
@@ -84,7 +87,11 @@ def _stream():
     return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
 
 
-def make_shape(num_seqs, total_tokens, heads, dim, cu_seqlens=None, scale=None):
+def make_shape(num_seqs, total_tokens, heads, dim, cu_seqlens=None, scale=None, kda_gate="softplus",
+               gate_scale=0.0):
+    """The problem shape.  ``kda_gate`` selects the KDA gate function ("softplus":
+    g = -e^{A_log} softplus(g_raw + dt_bias); "sigmoid": g = ln2 gate_scale sigmoid(e^{A_log} (g_raw +
+    dt_bias)) with gate_scale <= 0); the GDN calls ignore it."""
     sh = GdrShape()
     sh.num_seqs = int(num_seqs)
     sh.total_tokens = int(total_tokens)
@@ -92,6 +99,10 @@ def make_shape(num_seqs, total_tokens, heads, dim, cu_seqlens=None, scale=None):
     sh.head_dim = int(dim)
     sh.cu_seqlens = None if cu_seqlens is None else cu_seqlens.data_ptr()
     sh.scale = float(dim ** -0.5 if scale is None else scale)
+    if kda_gate not in KDA_GATES:
+        raise ValueError("kda_gate must be one of %s" % sorted(KDA_GATES))
+    sh.kda_gate = KDA_GATES[kda_gate]
+    sh.gate_scale = float(0.0 if gate_scale is None else gate_scale)
     return sh
 
 
@@ -117,7 +128,7 @@ def _opt(t, dtype, shape, name):
 
 
 class _Problem:
-    def __init__(self, q, cu_seqlens, num_seqs, scale):
+    def __init__(self, q, cu_seqlens, num_seqs, scale, kda_gate="softplus", gate_scale=0.0):
         if q.dim() == 4:
             B, T, H, D = q.shape
             self.dense_shape = (B, T)
@@ -132,7 +143,7 @@ class _Problem:
             _need(cu_seqlens, torch.int64, (N + 1,), "cu_seqlens")
         self.N, self.T, self.H, self.D = int(N), int(Tt), int(H), int(D)
         self.cu = cu_seqlens
-        self.shape = make_shape(N, Tt, H, D, cu_seqlens, scale)
+        self.shape = make_shape(N, Tt, H, D, cu_seqlens, scale, kda_gate, gate_scale)
 
     def flat(self, t):
         if t is None or self.dense_shape is None:
@@ -154,9 +165,10 @@ class _Problem:
 
 
 def gdr_fwd_states(q, k, v, g, beta_logit, h0=None, cu_seqlens=None, num_seqs=None, scale=None,
-                   workspace=None, gate="gdn", g_raw=None, A_log=None, dt_bias=None):
+                   workspace=None, gate="gdn", g_raw=None, A_log=None, dt_bias=None, kda_gate="softplus",
+                   gate_scale=0.0):
     """Chunk-start states of every 64-token chunk (bf16), for gdr_bwd / kda_bwd."""
-    P = _Problem(q, cu_seqlens, num_seqs, scale)
+    P = _Problem(q, cu_seqlens, num_seqs, scale, kda_gate, gate_scale)
     T, H, D, N = P.T, P.H, P.D, P.N
     q, k, v = (_need(P.flat(x), torch.bfloat16, (T, H, D), n) for x, n in ((q, "q"), (k, "k"), (v, "v")))
     beta_logit = _need(P.flat(beta_logit), torch.bfloat16, (T, H), "beta_logit")
@@ -180,8 +192,8 @@ def gdr_fwd_states(q, k, v, g, beta_logit, h0=None, cu_seqlens=None, num_seqs=No
 
 
 def _fwd(gate, q, k, v, beta_logit, h0, cu_seqlens, num_seqs, scale, states, workspace, want_ht,
-         g=None, g_raw=None, A_log=None, dt_bias=None):
-    P = _Problem(q, cu_seqlens, num_seqs, scale)
+         g=None, g_raw=None, A_log=None, dt_bias=None, kda_gate="softplus", gate_scale=0.0):
+    P = _Problem(q, cu_seqlens, num_seqs, scale, kda_gate, gate_scale)
     T, H, D, N = P.T, P.H, P.D, P.N
     q, k, v = (_need(P.flat(x), torch.bfloat16, (T, H, D), n) for x, n in ((q, "q"), (k, "k"), (v, "v")))
     beta_logit = _need(P.flat(beta_logit), torch.bfloat16, (T, H), "beta_logit")
@@ -218,10 +230,10 @@ def gdr_fwd(q, k, v, g, beta_logit, h0=None, cu_seqlens=None, num_seqs=None, sca
 
 
 def kda_fwd(q, k, v, g_raw, A_log, dt_bias, beta_logit, h0=None, cu_seqlens=None, num_seqs=None, scale=None,
-            states=None, workspace=None, want_ht=True):
-    """KDA forward.  Returns dict(o, ht[, states]) as gdr_fwd."""
+            states=None, workspace=None, want_ht=True, kda_gate="softplus", gate_scale=0.0):
+    """KDA forward.  Returns dict(o, ht[, states]) as gdr_fwd; ``kda_gate`` / ``gate_scale`` as make_shape."""
     return _fwd("kda", q, k, v, beta_logit, h0, cu_seqlens, num_seqs, scale, states, workspace, want_ht,
-                g_raw=g_raw, A_log=A_log, dt_bias=dt_bias)
+                g_raw=g_raw, A_log=A_log, dt_bias=dt_bias, kda_gate=kda_gate, gate_scale=gate_scale)
 
 
 def gdr_bwd(q, k, v, g, beta_logit, dO, h0=None, dht=None, cu_seqlens=None, num_seqs=None,
@@ -246,9 +258,10 @@ def gdr_bwd(q, k, v, g, beta_logit, dO, h0=None, dht=None, cu_seqlens=None, num_
 
 
 def kda_bwd(q, k, v, g_raw, A_log, dt_bias, beta_logit, dO, h0=None, dht=None, cu_seqlens=None,
-            num_seqs=None, scale=None, states=None, workspace=None, out=None):
-    """KDA backward.  Returns dict(dq, dk, dv, dg_raw, dbeta, dh0, dA_log, ddt_bias)."""
-    P = _Problem(q, cu_seqlens, num_seqs, scale)
+            num_seqs=None, scale=None, states=None, workspace=None, out=None, kda_gate="softplus", gate_scale=0.0):
+    """KDA backward.  Returns dict(dq, dk, dv, dg_raw, dbeta, dh0, dA_log, ddt_bias); ``kda_gate`` /
+    ``gate_scale`` as make_shape."""
+    P = _Problem(q, cu_seqlens, num_seqs, scale, kda_gate, gate_scale)
     T, H, D, N = P.T, P.H, P.D, P.N
     q, k, v, dO, g_raw = (_need(P.flat(x), torch.bfloat16, (T, H, D), n)
                           for x, n in ((q, "q"), (k, "k"), (v, "v"), (dO, "dO"), (g_raw, "g_raw")))

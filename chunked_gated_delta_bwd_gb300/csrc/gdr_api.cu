@@ -90,6 +90,10 @@ static gdr_status check_shape(const gdr_shape* sh) {
     if (!sh->cu_seqlens && sh->total_tokens % sh->num_seqs != 0)
         return fail(GDR_ERR_INVALID, "dense layout needs total_tokens divisible by num_seqs");
     if (sh->num_heads > 65535) return fail(GDR_ERR_INVALID, "num_heads must be <= 65535");
+    if (sh->kda_gate != GDR_KDA_GATE_SOFTPLUS && sh->kda_gate != GDR_KDA_GATE_SIGMOID)
+        return fail(GDR_ERR_INVALID, "kda_gate must be GDR_KDA_GATE_SOFTPLUS or GDR_KDA_GATE_SIGMOID");
+    if (sh->kda_gate == GDR_KDA_GATE_SIGMOID && !(sh->gate_scale <= 0.f && sh->gate_scale > -1e30f))
+        return fail(GDR_ERR_INVALID, "gate_scale must be finite and <= 0 (a decaying gate)");
     const int64_t N = sh->num_seqs, T = sh->total_tokens;
     const int64_t mc = sh->cu_seqlens ? (T + (CH - 1) * N) / CH : N * ((T / N + CH - 1) / CH);
     if (mc > (int64_t)1 << 30 || N * sh->num_heads * (sh->head_dim / 16) > ((int64_t)1 << 31) - 1)
@@ -162,6 +166,8 @@ static void base_params(Params& p, const gdr_shape* sh, const Layout& L, void* w
     p.cu_seqlens = sh->cu_seqlens;
     p.scale = sh->scale;
     p.kda = kda;
+    p.kda_gate = sh->kda_gate;
+    p.gate_scale = sh->gate_scale;
     unsigned char* w = static_cast<unsigned char*>(ws);
     p.status = reinterpret_cast<int*>(w + L.status);
     p.chunk_off = sh->cu_seqlens ? reinterpret_cast<int*>(w + L.chunk_off) : nullptr;

@@ -82,7 +82,7 @@ __device__ void load_gates(const Params& p, const ChunkInfo& ci, int h, const Ga
         float acc = 0.f;
 #pragma unroll
         for (int i = 0; i < RS; ++i) {
-            if (sg * RS + i < ci.len) acc += -a * softplus_f(v[i] + bias);
+            if (sg * RS + i < ci.len) acc += kda_gate_fn(p.kda_gate, p.gate_scale, a, v[i] + bias);
             v[i] = acc;
         }
         if (sg < NSEG - 1) G.gc[(sg * RS + RS - 1) * G.LDG + d] = acc;

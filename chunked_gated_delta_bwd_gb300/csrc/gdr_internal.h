@@ -17,6 +17,8 @@ struct Params {
     const int* chunk_off;   // device [N+1] chunk prefix sums, or nullptr (dense)
     float scale;
     int kda;                // 0: scalar GDN gate, 1: per-channel KDA gate
+    int kda_gate;           // KDA gate function: 0 softplus, 1 sigmoid-bounded (gdr.h)
+    float gate_scale;       // sigmoid-bounded gate: g = ln2 gate_scale sigmoid(e^{A_log} x)
 
     // inputs
     const __nv_bfloat16 *q, *k, *v, *dO, *beta_logit;

@@ -542,10 +542,11 @@ __global__ void __launch_bounds__(256, 1) k_main(const Params p) {
             const size_t o = ((ci.t0 + r) * p.H + h) * D + d;
             const float x = bf2f(p.g_raw[o]) + dt;
             const float dgl = sDgc[r * D + d];
-            const float draw = dgl * (-ea * sigmoid_f(x));
+            float dA;
+            const float draw = kda_gate_bwd(p.kda_gate, p.gate_scale, ea, x, dgl, dA);
             p.dg_raw[o] = __float2bfloat16(draw);
             ddt += draw;
-            dA_acc += dgl * (-ea * softplus_f(x));
+            dA_acc += dA;
         }
         __syncthreads();  // sDgc reads done; reuse the row-sum scratch for the partials
         sRowQ[threadIdx.x] = ddt;  // [RSTEP][D] (256 floats: rowq and rowk are contiguous)

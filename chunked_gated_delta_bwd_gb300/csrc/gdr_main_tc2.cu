@@ -296,7 +296,7 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
         float acc = 0.f;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-            if (c0 + i < ci.len) acc += -a * softplus_f(g[i] + bias);
+            if (c0 + i < ci.len) acc += kda_gate_fn(p.kda_gate, p.gate_scale, a, g[i] + bias);
             g[i] = acc;
         }
         sScan[hc * MD + L] = acc;  // this quarter's total
@@ -883,13 +883,11 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
         for (int i = 0; i < 16; ++i) {
             const int r = c0 + i;
             if (r < ci.len) {
-                float sp, sg;
-                softplus_sigmoid(xr[i], sp, sg);
-                const float dgl = dGc[i] + post;
-                const float draw = dgl * (-ea * sg);
+                float dA;
+                const float draw = kda_gate_bwd(p.kda_gate, p.gate_scale, ea, xr[i], dGc[i] + post, dA);
                 p.dg_raw[((ci.t0 + r) * p.H + h) * MD + L] = __float2bfloat16(draw);
                 ddt += draw;
-                dA_acc += dgl * (-ea * sp);
+                dA_acc += dA;
             }
         }
         __syncthreads();  // suffix totals read

@@ -397,7 +397,7 @@ __global__ void __launch_bounds__(512, 1) k_prep_tc(const Params p, const __grid
         float acc = 0.f;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-            if (c0 + i < ci.len) acc += -a * softplus_f(g[i] + bias);
+            if (c0 + i < ci.len) acc += kda_gate_fn(p.kda_gate, p.gate_scale, a, g[i] + bias);
             g[i] = acc;
         }
         sScan[hc * PD + L] = acc;

@@ -13,7 +13,10 @@ Value recipes (the workloads the pages benchmark and the benchmark's configs):
 * beta logits ~ N(0, 1), bf16 [T_total, H];
 * GDN gate: g = -softplus(a), a ~ N(0, 1), float32 [T_total, H] (natural log);
 * KDA gate inputs: g_raw ~ N(0, 1) bf16 [T_total, H, D], A_log ~ U(-1, 0) float32
-  [H], dt_bias ~ N(0, 0.1) float32 [H, D];
+  [H], dt_bias ~ N(0, 0.1) float32 [H, D]; the gate function is an API parameter
+  carried along (``kda_gate``: "softplus", or "sigmoid" with ``gate_scale``; the pages
+  print no value for gate_scale, the sigmoid cases use -2, a per-token decay of the
+  same order as the softplus gate's);
 * h0, dht ~ N(0, 0.1) float32 [N, H, D, D] where the case asks for them;
 * varlen: N lengths ~ U[1, max_len] (integers), cu_seqlens int64 [N + 1].
 """
@@ -36,6 +39,8 @@ class Case:
     with_h0: bool = False
     with_dht: bool = False
     lengths: Optional[tuple] = None  # explicit lengths (overrides the dense / random ones)
+    kda_gate: str = "softplus"        # KDA gate function ("softplus" or "sigmoid")
+    gate_scale: float = 0.0           # the sigmoid gate's scale
     note: str = field(default="", compare=False)
 
 
@@ -49,6 +54,9 @@ CASES = {
                            note="KDA bwd: B=1 H=16 T=8192 D=128, h0=0, no dht"),
     "gdn_varlen_h32": Case("gdn_varlen_h32", "gdn", 16, 0, 32, 128, seed=3, varlen_max=4096,
                            note="GDN varlen bwd: 16 packed sequences, lengths U[1,4096], H=32"),
+    "kda_sigmoid_b1_h16_t8k": Case("kda_sigmoid_b1_h16_t8k", "kda", 1, 8192, 16, 128, seed=5, with_h0=True,
+                                   with_dht=True, kda_gate="sigmoid", gate_scale=-2.0,
+                                   note="KDA with the sigmoid-bounded gate: B=1 H=16 T=8192 D=128"),
     "gdn_h16_t32k": Case("gdn_h16_t32k", "gdn", 1, 32768, 16, 128, seed=4, with_h0=True,
                          with_dht=True, note="long-sequence GDN bwd: B=1 H=16 T=32768 D=128"),
     "kda_h16_t32k": Case("kda_h16_t32k", "kda", 1, 32768, 16, 128, seed=4, with_h0=True,
@@ -87,13 +95,14 @@ def make(case: Case):
         x["g_raw"] = normal(T, H, D)
         x["A_log"] = (torch.rand(H, generator=gen) - 1.0).to(torch.float32)
         x["dt_bias"] = normal(H, D, std=0.1, dtype=torch.float32)
+        x["kda_gate"], x["gate_scale"] = case.kda_gate, case.gate_scale
     x["h0"] = normal(N, H, D, D, std=0.1, dtype=torch.float32) if case.with_h0 else None
     x["dht"] = normal(N, H, D, D, std=0.1, dtype=torch.float32) if case.with_dht else None
     x["dO"] = normal(T, H, D)
     return x
 
 
-def custom(mode, lengths, heads, dim, seed, with_h0=False, with_dht=False):
+def custom(mode, lengths, heads, dim, seed, with_h0=False, with_dht=False, kda_gate="softplus", gate_scale=0.0):
     """A case with explicit sequence lengths (ragged tails, empty sequences, ...)."""
     return make(Case("custom", mode, len(lengths), 0, heads, dim, seed, with_h0=with_h0,
-                     with_dht=with_dht, lengths=tuple(lengths)))
+                     with_dht=with_dht, lengths=tuple(lengths), kda_gate=kda_gate, gate_scale=gate_scale))

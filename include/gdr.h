@@ -73,7 +73,17 @@ typedef struct {
     int32_t head_dim;          /* D = dk = dv, 64 or 128 */
     const int64_t* cu_seqlens; /* device int64 [N + 1], or NULL for dense */
     float scale;               /* output scale, usually 1 / sqrt(D) */
+    /* KDA only (ignored by the GDN calls): the per-channel gate function, with
+     * x = g_raw + dt_bias[h, :] and a = exp(A_log[h]):
+     *   GDR_KDA_GATE_SOFTPLUS (0): g = -a * softplus(x)
+     *   GDR_KDA_GATE_SIGMOID  (1): g = ln(2) * gate_scale * sigmoid(a * x), the
+     *     sigmoid-bounded gate of "FlashKDA之backward（K1）" §5.2 (whose base-2 log
+     *     gate is gate_scale * sigmoid(a x)); gate_scale must be finite and <= 0. */
+    int32_t kda_gate;
+    float gate_scale;
 } gdr_shape;
+#define GDR_KDA_GATE_SOFTPLUS 0
+#define GDR_KDA_GATE_SIGMOID 1
 
 /* Bytes of the scratch workspace that gdr_fwd_states / gdr_bwd / kda_fwd_states /
  * kda_bwd need for this shape (returns 0 for an invalid shape). */

@@ -38,7 +38,7 @@ def run_gpu(x, states=None, workspace=None):
         out = gdr.gdr_bwd(d["q"], d["k"], d["v"], d["g"], d["beta_logit"], d["dO"], **common)
     else:
         out = gdr.kda_bwd(d["q"], d["k"], d["v"], d["g_raw"], d["A_log"], d["dt_bias"],
-                          d["beta_logit"], d["dO"], **common)
+                          d["beta_logit"], d["dO"], kda_gate=x["kda_gate"], gate_scale=x["gate_scale"], **common)
     torch.cuda.synchronize()
     return {k: v.cpu() for k, v in out.items()}
 
@@ -56,7 +56,7 @@ def run_oracle(x, heads=None):
     if x["mode"] == "gdn":
         return oracle.gdn(q, k, v, sel(f64(x["g"])), b, x["scale"], cu, h0=h0, dO=dO, dht=dht)
     return oracle.kda(q, k, v, sel(f64(x["g_raw"])), selh(f64(x["A_log"])), selh(f64(x["dt_bias"])),
-                      b, x["scale"], cu, h0=h0, dO=dO, dht=dht)
+                      b, x["scale"], cu, h0=h0, dO=dO, dht=dht, gate=x["kda_gate"], gate_scale=x["gate_scale"])
 
 
 def compare(gpu, ref, x, heads=None, conditioned=False):
@@ -91,17 +91,10 @@ def compare(gpu, ref, x, heads=None, conditioned=False):
 
 def conditioned_error(g, ref, x, name, heads=None):
     """|sum error| / sum of |terms|, as an L2 ratio over the reduced entries."""
-    from oracle import oracle
-    sel = (lambda t: t) if heads is None else (lambda t: t[:, heads])
-    selh = (lambda t: t) if heads is None else (lambda t: t[heads])
-    glog = oracle.kda_gate(sel(f64(x["g_raw"])), selh(f64(x["A_log"])), selh(f64(x["dt_bias"])))
-    z = sel(f64(x["g_raw"])) + selh(f64(x["dt_bias"]))[None]
-    chain = -np.exp(selh(f64(x["A_log"])))[None, :, None] / (1.0 + np.exp(-z))
-    dglog = ref["dg_raw"] / chain
     if name == "ddt_bias":
         mag = np.abs(ref["dg_raw"]).sum(axis=0)
     else:
-        mag = np.abs(dglog * glog).sum(axis=(0, 2))
+        mag = np.abs(ref["dA_terms"]).sum(axis=(0, 2))
     return float(np.linalg.norm(g - ref[name]) / np.linalg.norm(mag))
 
 
@@ -122,7 +115,8 @@ def run_gpu_fwd(x, states=None, workspace=None):
     if x["mode"] == "gdn":
         out = gdr.gdr_fwd(d["q"], d["k"], d["v"], d["g"], d["beta_logit"], **common)
     else:
-        out = gdr.kda_fwd(d["q"], d["k"], d["v"], d["g_raw"], d["A_log"], d["dt_bias"], d["beta_logit"], **common)
+        out = gdr.kda_fwd(d["q"], d["k"], d["v"], d["g_raw"], d["A_log"], d["dt_bias"], d["beta_logit"],
+                          kda_gate=x["kda_gate"], gate_scale=x["gate_scale"], **common)
     torch.cuda.synchronize()
     return {k: v.cpu() for k, v in out.items()}
 
@@ -139,7 +133,7 @@ def run_oracle_fwd(x, heads=None):
     if x["mode"] == "gdn":
         return oracle.gdn(q, k, v, sel(f64(x["g"])), b, x["scale"], cu, h0=h0)
     return oracle.kda(q, k, v, sel(f64(x["g_raw"])), selh(f64(x["A_log"])), selh(f64(x["dt_bias"])),
-                      b, x["scale"], cu, h0=h0)
+                      b, x["scale"], cu, h0=h0, gate=x["kda_gate"], gate_scale=x["gate_scale"])
 
 
 # Forward final state ht: the chunk tiles it is built from are bf16 (U, kr and the

@@ -114,6 +114,21 @@ def test_states_buffer_too_small_rejected(L):
     assert rc == 3
 
 
+def test_kda_gate_choice_checked(L):
+    sh = gdr.make_shape(2, 128, 2, 64)
+    ws = gdr.workspace_bytes(sh)
+    assert ws > 0
+    sh.kda_gate = 2
+    assert gdr.workspace_bytes(sh) == 0
+    sh.kda_gate = 1
+    sh.gate_scale = 0.5  # a growing gate
+    assert gdr.workspace_bytes(sh) == 0
+    sh.gate_scale = -2.0
+    assert gdr.workspace_bytes(sh) == ws
+    with pytest.raises(ValueError):
+        gdr.make_shape(2, 128, 2, 64, kda_gate="tanh")
+
+
 def test_forward_arguments_rejected(L):
     # gdr_fwd(shape, q, k, v, g, beta, h0, o, ht, states, states_bytes, ws, ws_bytes, stream)
     sh = gdr.make_shape(2, 128, 2, 64)

@@ -30,10 +30,12 @@ def test_gdn_tiny_config():
     _check(inputs.make(inputs.CASES["gdn_tiny"]), label="fwd_gdn_tiny")
 
 
-@pytest.mark.parametrize("mode", ["gdn", "kda"])
+@pytest.mark.parametrize("mode", ["gdn", "kda", "kda_sigmoid"])
 @pytest.mark.parametrize("dim", [64, 128])
 def test_varlen_ragged_with_h0(mode, dim):
-    x = inputs.custom(mode, [1, 63, 64, 65, 200, 130], heads=3, dim=dim, seed=111, with_h0=True)
+    gate = "sigmoid" if mode == "kda_sigmoid" else "softplus"
+    x = inputs.custom(mode.split("_")[0], [1, 63, 64, 65, 200, 130], heads=3, dim=dim, seed=111, with_h0=True,
+                      kda_gate=gate, gate_scale=-2.0)
     _check(x, label="fwd_%s_ragged_d%d" % (mode, dim))
 
 

@@ -42,11 +42,13 @@ def test_gdn_varlen_ragged(dim):
     _check(x, label="gdn_ragged_d%d" % dim)
 
 
+@pytest.mark.parametrize("gate", ["softplus", "sigmoid"])
 @pytest.mark.parametrize("dim", [64, 128])
-def test_kda_varlen_ragged(dim):
+def test_kda_varlen_ragged(dim, gate):
     # 205 tokens: dA_log / ddt_bias are short sums, judged against their term magnitudes
-    x = inputs.custom("kda", [130, 70, 5], heads=2, dim=dim, seed=102, with_h0=True, with_dht=True)
-    _check(x, label="kda_ragged_d%d" % dim, conditioned=True)
+    x = inputs.custom("kda", [130, 70, 5], heads=2, dim=dim, seed=102, with_h0=True, with_dht=True,
+                      kda_gate=gate, gate_scale=-2.0)
+    _check(x, label="kda_%s_ragged_d%d" % (gate, dim), conditioned=True)
 
 
 @pytest.mark.parametrize("mode", ["gdn", "kda"])
@@ -132,6 +134,7 @@ def test_bad_cu_seqlens_are_flagged_not_faulted():
 @pytest.mark.parametrize("name,heads", [
     ("gdn_b2_h16_t4k", [0, 5, 10, 15]),
     ("kda_b1_h16_t8k", [0, 5, 10, 15]),
+    ("kda_sigmoid_b1_h16_t8k", [0, 15]),
     ("gdn_varlen_h32", [0, 31]),
     ("gdn_h16_t32k", [3, 12]),
     ("kda_h16_t32k", [3, 12]),
