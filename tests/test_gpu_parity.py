@@ -141,4 +141,7 @@ def test_bad_cu_seqlens_are_flagged_not_faulted():
 ])
 def test_full_size_sampled_heads(name, heads):
     x = inputs.make(inputs.CASES[name])
-    _check(x, heads=heads, label=name)
+    # the sigmoid-gate workload is not one of the pages' (no tolerance is stated for it): its
+    # dA_log sums cancel to ~1/3000 of the magnitude of their terms (~1/1400 for the softplus
+    # gate), so they are judged against their term magnitudes, as the short cases are
+    _check(x, heads=heads, label=name, conditioned=(x.get("kda_gate") == "sigmoid"))
