@@ -314,6 +314,27 @@ def main_gpu(args):
                                                        dht=A["dht"], num_seqs=N, scale=A["scale"], states=st_k,
                                                        workspace=ws_k, out=o))
     del st_g, st_k
+
+    # the KDA backward and forward with the sigmoid-bounded gate (gate_scale -2), same inputs
+    sig = {}
+
+    def sig_loop(name, fn, n=max(3, args.steps // 2)):
+        fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        sig[name] = a.elapsed_time(b) / n
+    sig_loop("bwd_ms", lambda A=K, o=out_k: gdr.kda_bwd(A["q"], A["k"], A["v"], A["g_raw"], A["A_log"], A["dt_bias"],
+                                                        A["beta_logit"], A["dO"], h0=A["h0"], dht=A["dht"],
+                                                        num_seqs=N, scale=A["scale"], workspace=ws_k, out=o,
+                                                        kda_gate="sigmoid", gate_scale=-2.0))
+    sig_loop("fwd_ms", lambda A=K: gdr.kda_fwd(A["q"], A["k"], A["v"], A["g_raw"], A["A_log"], A["dt_bias"],
+                                               A["beta_logit"], h0=A["h0"], num_seqs=N, scale=A["scale"],
+                                               workspace=ws_k, kda_gate="sigmoid", gate_scale=-2.0))
     th_v = CASE_G.seq_len * CASE_G.heads
     out_ms = (fwd_kernels["gdn"].get("out", 0.0) + fwd_kernels["kda"].get("out", 0.0)) / 2
     forward = {
@@ -412,6 +433,7 @@ def main_gpu(args):
         "kernels_ms_per_variant": per_variant,
         "forward": forward,
         "bwd_from_saved_states": {"ms_per_variant": saved, "kernels_ms_per_variant": saved_kernels},
+        "kda_sigmoid_gate": sig,
         "gpu_launches": launches,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms},
