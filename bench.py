@@ -335,6 +335,26 @@ def main_gpu(args):
     sig_loop("fwd_ms", lambda A=K: gdr.kda_fwd(A["q"], A["k"], A["v"], A["g_raw"], A["A_log"], A["dt_bias"],
                                                A["beta_logit"], h0=A["h0"], num_seqs=N, scale=A["scale"],
                                                workspace=ws_k, kda_gate="sigmoid", gate_scale=-2.0))
+    # the causal conv1d (+ SiLU) backward feeding q, k, v of this layer: C = 3 H D channels, K = 4
+    conv = None
+    cc = inputs.conv_case([CASE_G.seq_len], 3 * CASE_G.heads * CASE_G.dim, 4, seed=230)
+    cx = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in cc.items()}
+    conv_fn = lambda: gdr.conv1d_bwd(cx["x"], cx["weight"], cx["bias"], cx["dy"], silu=True)
+    for _ in range(2):
+        conv_fn()
+    torch.cuda.synchronize()
+    n_conv = max(3, args.steps // 2)
+    api.profile_begin(2 * n_conv)
+    for _ in range(n_conv):
+        conv_fn()
+    torch.cuda.synchronize()
+    conv_prof = api.profile_end()
+    if conv_prof["conv"][1]:
+        conv_ms = conv_prof["conv"][0] / conv_prof["conv"][1]
+        conv_bytes = CASE_G.seq_len * cc["x"].shape[1] * 6  # x, dy read, dx written (bf16)
+        conv = {"kernel": "k_conv1d_bwd", "ms": conv_ms, "tokens": CASE_G.seq_len, "channels": cc["x"].shape[1],
+                "width": 4, "bound": "hbm", "achieved": conv_bytes / (conv_ms * 1e-3) / 1e9, "unit": "GB/s"}
+    del cx
     th_v = CASE_G.seq_len * CASE_G.heads
     out_ms = (fwd_kernels["gdn"].get("out", 0.0) + fwd_kernels["kda"].get("out", 0.0)) / 2
     forward = {
@@ -393,6 +413,8 @@ def main_gpu(args):
 
     # ---- roofline of the dominant kernel ----
     hbm, tf_burst, tf_sus, src = peaks()
+    if conv:
+        conv.update(peak=hbm, frac=conv["achieved"] / hbm, peak_source=src + " (hbm_gbs)")
     if forward["out_roofline"]:
         fr = forward["out_roofline"]
         fr.update(peak=hbm, frac=fr["achieved"] / hbm, peak_source=src + " (hbm_gbs)")
@@ -434,6 +456,7 @@ def main_gpu(args):
         "forward": forward,
         "bwd_from_saved_states": {"ms_per_variant": saved, "kernels_ms_per_variant": saved_kernels},
         "kda_sigmoid_gate": sig,
+        "conv1d_bwd": conv,
         "gpu_launches": launches,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms},

@@ -62,6 +62,9 @@ def lib():
         L.gdr_bwd.argtypes = [sp] + [vp] * 10 + [sz] + [vp] * 7
         L.kda_bwd.restype = ctypes.c_int
         L.kda_bwd.argtypes = [sp] + [vp] * 12 + [sz] + [vp] * 9
+        L.gdr_conv1d_bwd.restype = ctypes.c_int
+        L.gdr_conv1d_bwd.argtypes = [ctypes.c_int32, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32] + [vp] * 5 + \
+            [ctypes.c_int32] + [vp] * 4
         L.gdr_workspace_status.restype = ctypes.c_int
         L.gdr_workspace_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int)]
         L.gdr_last_error.restype = ctypes.c_char_p
@@ -281,6 +284,35 @@ def kda_bwd(q, k, v, g_raw, A_log, dt_bias, beta_logit, dO, h0=None, dht=None, c
     return {k_: (P.unflat(t) if k_ not in ("dh0", "dA_log", "ddt_bias") else t) for k_, t in o.items()}
 
 
+def conv1d_bwd(x, weight, bias, dy, cu_seqlens=None, num_seqs=None, silu=True):
+    """Backward of the causal depthwise conv1d (+ SiLU): x, dy bf16 [T, C] (or [B, T, C]),
+    weight float32 [C, K], bias float32 [C] or None.  Returns dict(dx, dweight, dbias)."""
+    dense = None
+    if x.dim() == 3:
+        B, T, C = x.shape
+        dense = (B, T)
+        N, Tt = B, B * T
+        x, dy = x.reshape(Tt, C), dy.reshape(Tt, C)
+    else:
+        Tt, C = x.shape
+        N = num_seqs if cu_seqlens is None else cu_seqlens.numel() - 1
+        N = 1 if N is None else N
+    K = weight.shape[1] if weight.dim() == 2 else -1
+    _need(x, torch.bfloat16, (Tt, C), "x")
+    _need(dy, torch.bfloat16, (Tt, C), "dy")
+    _need(weight, torch.float32, (C, K), "weight")
+    _opt(bias, torch.float32, (C,), "bias")
+    if cu_seqlens is not None:
+        _need(cu_seqlens, torch.int64, (N + 1,), "cu_seqlens")
+    dx = torch.empty(Tt, C, dtype=torch.bfloat16, device="cuda")
+    dw = torch.empty(C, K, dtype=torch.float32, device="cuda")
+    db = torch.empty(C, dtype=torch.float32, device="cuda") if bias is not None else None
+    rc = lib().gdr_conv1d_bwd(int(N), int(Tt), int(C), int(K), _ptr(cu_seqlens), _ptr(x), _ptr(weight), _ptr(bias),
+                              _ptr(dy), 1 if silu else 0, _ptr(dx), _ptr(dw), _ptr(db), _stream())
+    _check(rc, "gdr_conv1d_bwd")
+    return {"dx": dx if dense is None else dx.reshape(*dense, C), "dweight": dw, "dbias": db}
+
+
 def alloc_outputs(T, H, D, N, gate, device="cuda"):
     bf = dict(dtype=torch.bfloat16, device=device)
     o = {"dq": torch.empty(T, H, D, **bf), "dk": torch.empty(T, H, D, **bf),
@@ -302,7 +334,7 @@ def workspace_status(workspace) -> int:
     return st.value
 
 
-KERNEL_NAMES = ("chunk_table", "prep", "states", "main", "out")
+KERNEL_NAMES = ("chunk_table", "prep", "states", "main", "out", "conv")
 
 
 def profile_begin(max_launches: int):

@@ -389,6 +389,41 @@ gdr_status kda_bwd(const gdr_shape* shape, const void* q, const void* k, const v
                     stream, 1);
 }
 
+gdr_status gdr_conv1d_bwd(int32_t num_seqs, int64_t total_tokens, int32_t channels, int32_t width,
+                          const int64_t* cu_seqlens, const void* x, const float* weight, const float* bias,
+                          const void* dy, int32_t silu, void* dx, float* dweight, float* dbias, void* stream) {
+    if (num_seqs < 1 || total_tokens < 0 || channels < 1)
+        return fail(GDR_ERR_INVALID, "num_seqs and channels must be >= 1, total_tokens >= 0%s");
+    if (width < 1 || width > 4) return fail(GDR_ERR_UNSUPPORTED, "width must be 1 to 4%s");
+    if (channels % 2 != 0) return fail(GDR_ERR_INVALID, "channels must be even%s");
+    if (!cu_seqlens && total_tokens % num_seqs != 0)
+        return fail(GDR_ERR_INVALID, "dense layout needs total_tokens divisible by num_seqs%s");
+    if ((int64_t)channels * total_tokens > ((int64_t)1 << 40)) return fail(GDR_ERR_INVALID, "problem too large%s");
+    NEED(x); NEED(weight); NEED(dy); NEED(dx); NEED(dweight); OPT(bias); OPT(dbias);
+    ConvParams p;
+    p.N = num_seqs;
+    p.T = total_tokens;
+    p.C = channels;
+    p.K = width;
+    p.silu = silu != 0;
+    p.cu_seqlens = cu_seqlens;
+    p.x = (const __nv_bfloat16*)x;
+    p.dy = (const __nv_bfloat16*)dy;
+    p.w = weight;
+    p.bias = bias;
+    p.dx = (__nv_bfloat16*)dx;
+    p.dw = dweight;
+    p.dbias = dbias;
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = cudaMemsetAsync(dweight, 0, sizeof(float) * channels * width, s);
+    if (e == cudaSuccess && dbias) e = cudaMemsetAsync(dbias, 0, sizeof(float) * channels, s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(dweight/dbias)");
+    e = timed(GDR_KERNEL_CONV, s, [&] { return launch_conv1d_bwd(p, s); });
+    if (e != cudaSuccess) return cuda_fail(e, "conv1d backward launch");
+    g_err[0] = 0;
+    return GDR_OK;
+}
+
 gdr_status gdr_workspace_status(const void* workspace, void* stream, int* device_status) {
     if (!workspace || !device_status) return fail(GDR_ERR_INVALID, "workspace and device_status must be non-NULL%s");
     cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);

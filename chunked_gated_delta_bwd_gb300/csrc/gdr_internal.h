@@ -62,6 +62,19 @@ inline int num_sms() {
     return cache[dev];
 }
 
+// causal depthwise conv1d backward (gdr_conv1d_bwd)
+struct ConvParams {
+    int N;                        // sequences
+    int64_t T;                    // tokens
+    int C, K, silu;               // channels, taps, SiLU after the conv
+    const int64_t* cu_seqlens;    // device [N+1] or nullptr (dense)
+    const __nv_bfloat16 *x, *dy;  // [T][C]
+    const float *w, *bias;        // [C][K], [C] or nullptr
+    __nv_bfloat16* dx;            // [T][C]
+    float *dw, *dbias;            // [C][K], [C] or nullptr (accumulated: zeroed by the caller)
+};
+cudaError_t launch_conv1d_bwd(const ConvParams& p, cudaStream_t s);
+
 cudaError_t launch_chunk_table(const Params& p, cudaStream_t s);
 cudaError_t launch_prep(const Params& p, cudaStream_t s);
 cudaError_t launch_prep_tc(const Params& p, cudaStream_t s);  // D = 128, tcgen05 + TMA

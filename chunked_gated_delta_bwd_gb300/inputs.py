@@ -102,6 +102,21 @@ def make(case: Case):
     return x
 
 
+def conv_case(lengths, channels, width, seed, with_bias=True, silu=True):
+    """Inputs of the causal conv1d backward: x, dy ~ N(0, 1) bf16 [T_total, C] (token-major;
+    in a GDN layer C = the q, k and v channels), weight ~ N(0, 0.25) float32 [C, K], bias ~
+    N(0, 0.1) float32 [C] (or None), packed sequences of the given lengths."""
+    gen = torch.Generator().manual_seed(seed)
+    cu = torch.zeros(len(lengths) + 1, dtype=torch.int64)
+    cu[1:] = torch.cumsum(torch.tensor(lengths, dtype=torch.int64), 0)
+    T = int(cu[-1])
+    x = torch.randn(T, channels, generator=gen).to(torch.bfloat16)
+    w = (torch.randn(channels, width, generator=gen) * 0.5).to(torch.float32)
+    b = (torch.randn(channels, generator=gen) * 0.1).to(torch.float32) if with_bias else None
+    dy = torch.randn(T, channels, generator=gen).to(torch.bfloat16)
+    return {"cu_seqlens": cu, "x": x, "weight": w, "bias": b, "dy": dy, "silu": silu}
+
+
 def custom(mode, lengths, heads, dim, seed, with_h0=False, with_dht=False, kda_gate="softplus", gate_scale=0.0):
     """A case with explicit sequence lengths (ragged tails, empty sequences, ...)."""
     return make(Case("custom", mode, len(lengths), 0, heads, dim, seed, with_h0=with_h0,

@@ -173,6 +173,24 @@ gdr_status gdr_bwd_fixed(const gdr_shape* shape, const void* q, const void* k, c
                          const float* dht, const void* states, void* dq, void* dk, void* dv,
                          float* dg, void* dbeta, float* dh0, void* stream);
 
+/* Backward of the causal depthwise conv1d (optionally followed by SiLU) that produces
+ * q, k and v in a gated delta-rule layer ("第三章 反向传播的完整推导", the
+ * causal-convolution page): per channel c with `width` K taps and zero state before
+ * each sequence's first token,
+ *     z_t = bias[c] + sum_k weight[c, k] x[t-K+1+k, c],   y = silu ? z sigmoid(z) : z.
+ * Given dy = dL/dy it writes dx (bf16), dweight (fp32 [C, K]) and, if dbias is not
+ * NULL, dbias (fp32 [C]); the pre-activation z is recomputed from x.
+ *  * x, dy, dx: bf16 [T_total, C] token-major (C = channels, even);
+ *    weight fp32 [C, K], 1 <= K <= 4; bias fp32 [C] or NULL (zero).
+ *  * cu_seqlens: device int64 [N + 1] or NULL (dense: N sequences of T_total / N
+ *    tokens); no sum crosses a sequence boundary.  Inconsistent cu_seqlens give
+ *    meaningless gradients but no access outside the tensors.
+ *  * dweight and dbias are overwritten (zeroed on the stream, then accumulated
+ *    with atomics, so their last bits depend on the order of the additions). */
+gdr_status gdr_conv1d_bwd(int32_t num_seqs, int64_t total_tokens, int32_t channels, int32_t width,
+                          const int64_t* cu_seqlens, const void* x, const float* weight,
+                          const float* bias, const void* dy, int32_t silu, void* dx,
+                          float* dweight, float* dbias, void* stream);
 /* Waits for `stream`, then returns in *device_status the OR of the GDR_DEV_*
  * bits raised by the last call that used `workspace` (0 = none). */
 gdr_status gdr_workspace_status(const void* workspace, void* stream, int* device_status);
@@ -190,7 +208,8 @@ const char* gdr_last_error(void);
 #define GDR_KERNEL_STATES 2      /* serial state / state-gradient recurrences */
 #define GDR_KERNEL_MAIN 3        /* chunk-parallel main backward */
 #define GDR_KERNEL_OUT 4         /* chunk-parallel forward output (gdr_fwd / kda_fwd) */
-#define GDR_KERNEL_COUNT 5
+#define GDR_KERNEL_CONV 5        /* causal conv1d backward (gdr_conv1d_bwd) */
+#define GDR_KERNEL_COUNT 6
 gdr_status gdr_profile_begin(int max_launches);
 gdr_status gdr_profile_end(double* total_ms, int* launches);
 

@@ -164,6 +164,25 @@ def test_forward_arguments_rejected(L):
     assert L.kda_fwd(ctypes.byref(sh_bad), *kargs) == 2
 
 
+def test_conv1d_arguments_rejected(L):
+    A = ctypes.c_void_p(4096)
+    ok = [2, 256, 8, 4, None, A, A, A, A, 1, A, A, A, None]
+    def call(args):
+        return L.gdr_conv1d_bwd(*args)
+    for i, v, code in ((3, 5, 2), (3, 0, 2), (2, 6, 1), (0, 0, 1), (1, 255, 1)):  # width, channels, N, dense T
+        bad = list(ok)
+        bad[i] = v
+        assert call(bad) == code, (i, v)
+    for i in (5, 6, 8, 10, 11):  # x, weight, dy, dx, dweight required
+        bad = list(ok)
+        bad[i] = None
+        assert call(bad) == 1, i
+    for i in (7, 12):  # bias, dbias optional but aligned
+        bad = list(ok)
+        bad[i] = ctypes.c_void_p(4096 + 4)
+        assert call(bad) == 1, i
+
+
 def test_product_path_fails_loudly_without_library(monkeypatch):
     monkeypatch.setattr(api, "_LIB", None)
     monkeypatch.setattr(build, "LIB", "/nonexistent/libgdr.so")
