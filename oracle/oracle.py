@@ -69,7 +69,24 @@ def gated_delta(q, k, v, glog, beta_logit, scale, cu_seqlens, h0=None, dO=None, 
 
     Returns a dict with ``o`` [T,H,D], ``ht`` [N,H,D,D] and, with ``dO``,
     ``dq, dk, dv, dglog`` [T,H,D], ``dbeta`` [T,H] (logit space), ``dh0`` [N,H,D,D].
+
+    Grouped heads (GQA: q, k with Hk heads, v and everything else with H = r Hk heads):
+    value head h reads q / k head h // r, i.e. each q / k head is shared by r consecutive
+    value heads (the grouped-query layout of the FlashQLA page's GQA tests); the shared
+    q / k is the same as r copies of it, so dq and dk are the sums over each group.
     """
+    q, k = _f64(q), _f64(k)
+    if q.shape[1] != np.shape(v)[1]:
+        Hk, H = q.shape[1], np.shape(v)[1]
+        assert H % Hk == 0 and k.shape == q.shape
+        r = H // Hk
+        out = gated_delta(np.repeat(q, r, axis=1), np.repeat(k, r, axis=1), v, glog, beta_logit, scale,
+                          cu_seqlens, h0, dO, dht, nthreads)
+        for name in ("dq", "dk"):
+            if name in out:
+                T, _, D = out[name].shape
+                out[name] = out[name].reshape(T, Hk, r, D).sum(axis=2)
+        return out
     q, k, v, glog, beta_logit = map(_f64, (q, k, v, glog, beta_logit))
     h0, dO, dht = _f64(h0), _f64(dO), _f64(dht)
     cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int64))
@@ -101,7 +118,7 @@ def gated_delta(q, k, v, glog, beta_logit, scale, cu_seqlens, h0=None, dO=None, 
 def gdn(q, k, v, g, beta_logit, scale, cu_seqlens, h0=None, dO=None, dht=None, nthreads=0):
     """GDN: scalar natural-log gate ``g`` [T,H].  Backward returns ``dg`` [T,H]."""
     g = _f64(g)
-    T, H, D = np.shape(q)
+    T, H, D = np.shape(v)
     assert g.shape == (T, H)
     glog = np.ascontiguousarray(np.broadcast_to(g[:, :, None], (T, H, D)))
     out = gated_delta(q, k, v, glog, beta_logit, scale, cu_seqlens, h0, dO, dht, nthreads)

@@ -139,6 +139,31 @@ def test_sigmoid_gate_value_at_vanishing_slope():
     np.testing.assert_allclose(a["ddt_bias"], a["dg_raw"].sum(axis=0), rtol=1e-12, atol=0)
 
 
+@pytest.mark.parametrize("mode", ["gdn", "kda"])
+def test_grouped_heads_backward_matches_fd(mode):
+    # GQA: 2 q / k heads shared by 4 value heads (value head h reads q / k head h // 2)
+    rng = np.random.default_rng(14)
+    c = _rand_case(rng, (5, 3), 4, 3, mode)
+    c["q"], c["k"] = c["q"][:, :2].copy(), c["k"][:, :2].copy()
+    if mode == "gdn":
+        an = oracle.gdn(c["q"], c["k"], c["v"], c["g"], c["b"], c["scale"], c["cu"], h0=c["h0"], dO=c["dO"],
+                        dht=c["dht"])
+        loss = lambda: _loss_gdn(c)
+    else:
+        an = oracle.kda(c["q"], c["k"], c["v"], c["g_raw"], c["A_log"], c["dt_bias"], c["b"], c["scale"],
+                        c["cu"], h0=c["h0"], dO=c["dO"], dht=c["dht"])
+        loss = lambda: _loss_kda(c)
+    assert an["dq"].shape == c["q"].shape and an["dv"].shape == c["v"].shape
+    for name, key in (("q", "dq"), ("k", "dk"), ("v", "dv"), ("b", "dbeta"), ("h0", "dh0")):
+        fd = central_grad(loss, c[name])
+        _check(fd, an[key].reshape(-1), name)
+    # the group's value heads see the same q / k: the output equals the run on expanded q / k
+    ex = oracle.gated_delta(np.repeat(c["q"], 2, axis=1), np.repeat(c["k"], 2, axis=1), c["v"],
+                            oracle.kda_gate(c["g_raw"], c["A_log"], c["dt_bias"]) if mode == "kda"
+                            else np.repeat(c["g"][:, :, None], 3, axis=2), c["b"], c["scale"], c["cu"], h0=c["h0"])
+    np.testing.assert_allclose(an["o"], ex["o"], rtol=1e-13, atol=1e-13)
+
+
 def test_dht_gradient_is_the_final_state():
     # d L / d dht = ht, so FD in dht is the forward's final state; and the
     # gradient w.r.t. dO is o.  This pins which output each cotangent pairs with.
