@@ -335,6 +335,27 @@ def main_gpu(args):
     sig_loop("fwd_ms", lambda A=K: gdr.kda_fwd(A["q"], A["k"], A["v"], A["g_raw"], A["A_log"], A["dt_bias"],
                                                A["beta_logit"], h0=A["h0"], num_seqs=N, scale=A["scale"],
                                                workspace=ws_k, kda_gate="sigmoid", gate_scale=-2.0))
+    # GDN with grouped q / k heads: 16 q / k heads shared by 32 value heads, T = 32768
+    gqa = None
+    gq_case = inputs.Case("gqa", "gdn", 1, CASE_G.seq_len, 2 * CASE_G.heads, CASE_G.dim, seed=231, with_h0=True,
+                          with_dht=True, k_heads=CASE_G.heads)
+    gx = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inputs.make(gq_case).items()}
+    ws_q = torch.empty(gdr.workspace_bytes(gdr.make_shape(N, T, 2 * Hh, D, k_heads=Hh)), dtype=torch.uint8,
+                       device="cuda")
+    gqa_fn = lambda A=gx: gdr.gdr_bwd(A["q"], A["k"], A["v"], A["g"], A["beta_logit"], A["dO"], h0=A["h0"],
+                                      dht=A["dht"], num_seqs=N, scale=A["scale"], workspace=ws_q)
+    gqa_fn()
+    torch.cuda.synchronize()
+    ga, gb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n_gqa = max(3, args.steps // 2)
+    ga.record(stream)
+    for _ in range(n_gqa):
+        gqa_fn()
+    gb.record(stream)
+    torch.cuda.synchronize()
+    gqa = {"workload": "GDN bwd, 16 q/k heads, 32 v heads, T=32768 D=128", "ms": ga.elapsed_time(gb) / n_gqa}
+    del gx, ws_q
+
     # the causal conv1d (+ SiLU) backward feeding q, k, v of this layer: C = 3 H D channels, K = 4
     conv = None
     cc = inputs.conv_case([CASE_G.seq_len], 3 * CASE_G.heads * CASE_G.dim, 4, seed=230)
@@ -457,6 +478,7 @@ def main_gpu(args):
         "bwd_from_saved_states": {"ms_per_variant": saved, "kernels_ms_per_variant": saved_kernels},
         "kda_sigmoid_gate": sig,
         "conv1d_bwd": conv,
+        "gqa": gqa,
         "gpu_launches": launches,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms},

@@ -28,7 +28,8 @@ class GdrShape(ctypes.Structure):
     _fields_ = [("num_seqs", ctypes.c_int32), ("total_tokens", ctypes.c_int64),
                 ("num_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("cu_seqlens", ctypes.c_void_p), ("scale", ctypes.c_float),
-                ("kda_gate", ctypes.c_int32), ("gate_scale", ctypes.c_float)]
+                ("kda_gate", ctypes.c_int32), ("gate_scale", ctypes.c_float),
+                ("num_k_heads", ctypes.c_int32)]
 
 KDA_GATES = {"softplus": 0, "sigmoid": 1}  # GDR_KDA_GATE_SOFTPLUS / GDR_KDA_GATE_SIGMOID
 
@@ -91,7 +92,7 @@ def _stream():
 
 
 def make_shape(num_seqs, total_tokens, heads, dim, cu_seqlens=None, scale=None, kda_gate="softplus",
-               gate_scale=0.0):
+               gate_scale=0.0, k_heads=None):
     """The problem shape.  ``kda_gate`` selects the KDA gate function ("softplus":
     g = -e^{A_log} softplus(g_raw + dt_bias); "sigmoid": g = ln2 gate_scale sigmoid(e^{A_log} (g_raw +
     dt_bias)) with gate_scale <= 0); the GDN calls ignore it."""
@@ -106,6 +107,7 @@ def make_shape(num_seqs, total_tokens, heads, dim, cu_seqlens=None, scale=None, 
         raise ValueError("kda_gate must be one of %s" % sorted(KDA_GATES))
     sh.kda_gate = KDA_GATES[kda_gate]
     sh.gate_scale = float(0.0 if gate_scale is None else gate_scale)
+    sh.num_k_heads = 0 if k_heads is None or int(k_heads) == int(heads) else int(k_heads)
     return sh
 
 
@@ -131,22 +133,27 @@ def _opt(t, dtype, shape, name):
 
 
 class _Problem:
-    def __init__(self, q, cu_seqlens, num_seqs, scale, kda_gate="softplus", gate_scale=0.0):
+    """Shape of one call: value heads H from v, q / k heads Hk from q (GQA when Hk < H)."""
+
+    def __init__(self, q, cu_seqlens, num_seqs, scale, kda_gate="softplus", gate_scale=0.0, v=None):
+        v = q if v is None else v
         if q.dim() == 4:
-            B, T, H, D = q.shape
+            B, T, Hk, D = q.shape
+            H = v.shape[2]
             self.dense_shape = (B, T)
             N, Tt = B, B * T
         else:
-            Tt, H, D = q.shape
+            Tt, Hk, D = q.shape
+            H = v.shape[1]
             self.dense_shape = None
             N = num_seqs if cu_seqlens is None else cu_seqlens.numel() - 1
             if N is None:
                 N = 1
         if cu_seqlens is not None:
             _need(cu_seqlens, torch.int64, (N + 1,), "cu_seqlens")
-        self.N, self.T, self.H, self.D = int(N), int(Tt), int(H), int(D)
+        self.N, self.T, self.H, self.D, self.Hk = int(N), int(Tt), int(H), int(D), int(Hk)
         self.cu = cu_seqlens
-        self.shape = make_shape(N, Tt, H, D, cu_seqlens, scale, kda_gate, gate_scale)
+        self.shape = make_shape(N, Tt, H, D, cu_seqlens, scale, kda_gate, gate_scale, k_heads=Hk)
 
     def flat(self, t):
         if t is None or self.dense_shape is None:
@@ -171,9 +178,10 @@ def gdr_fwd_states(q, k, v, g, beta_logit, h0=None, cu_seqlens=None, num_seqs=No
                    workspace=None, gate="gdn", g_raw=None, A_log=None, dt_bias=None, kda_gate="softplus",
                    gate_scale=0.0):
     """Chunk-start states of every 64-token chunk (bf16), for gdr_bwd / kda_bwd."""
-    P = _Problem(q, cu_seqlens, num_seqs, scale, kda_gate, gate_scale)
-    T, H, D, N = P.T, P.H, P.D, P.N
-    q, k, v = (_need(P.flat(x), torch.bfloat16, (T, H, D), n) for x, n in ((q, "q"), (k, "k"), (v, "v")))
+    P = _Problem(q, cu_seqlens, num_seqs, scale, kda_gate, gate_scale, v=v)
+    T, H, D, N, Hk = P.T, P.H, P.D, P.N, P.Hk
+    q, k = (_need(P.flat(x), torch.bfloat16, (T, Hk, D), n) for x, n in ((q, "q"), (k, "k")))
+    v = _need(P.flat(v), torch.bfloat16, (T, H, D), "v")
     beta_logit = _need(P.flat(beta_logit), torch.bfloat16, (T, H), "beta_logit")
     h0 = _opt(h0, torch.float32, (N, H, D, D), "h0")
     states = torch.empty(max(states_bytes(P.shape), 16), dtype=torch.uint8, device="cuda")
@@ -196,9 +204,10 @@ def gdr_fwd_states(q, k, v, g, beta_logit, h0=None, cu_seqlens=None, num_seqs=No
 
 def _fwd(gate, q, k, v, beta_logit, h0, cu_seqlens, num_seqs, scale, states, workspace, want_ht,
          g=None, g_raw=None, A_log=None, dt_bias=None, kda_gate="softplus", gate_scale=0.0):
-    P = _Problem(q, cu_seqlens, num_seqs, scale, kda_gate, gate_scale)
-    T, H, D, N = P.T, P.H, P.D, P.N
-    q, k, v = (_need(P.flat(x), torch.bfloat16, (T, H, D), n) for x, n in ((q, "q"), (k, "k"), (v, "v")))
+    P = _Problem(q, cu_seqlens, num_seqs, scale, kda_gate, gate_scale, v=v)
+    T, H, D, N, Hk = P.T, P.H, P.D, P.N, P.Hk
+    q, k = (_need(P.flat(x), torch.bfloat16, (T, Hk, D), n) for x, n in ((q, "q"), (k, "k")))
+    v = _need(P.flat(v), torch.bfloat16, (T, H, D), "v")
     beta_logit = _need(P.flat(beta_logit), torch.bfloat16, (T, H), "beta_logit")
     h0 = _opt(h0, torch.float32, (N, H, D, D), "h0")
     ws = P.workspace(workspace)
@@ -242,16 +251,16 @@ def kda_fwd(q, k, v, g_raw, A_log, dt_bias, beta_logit, h0=None, cu_seqlens=None
 def gdr_bwd(q, k, v, g, beta_logit, dO, h0=None, dht=None, cu_seqlens=None, num_seqs=None,
             scale=None, states=None, workspace=None, out=None):
     """GDN backward.  Returns dict(dq, dk, dv, dg, dbeta, dh0)."""
-    P = _Problem(q, cu_seqlens, num_seqs, scale)
-    T, H, D, N = P.T, P.H, P.D, P.N
-    q, k, v, dO = (_need(P.flat(x), torch.bfloat16, (T, H, D), n)
-                   for x, n in ((q, "q"), (k, "k"), (v, "v"), (dO, "dO")))
+    P = _Problem(q, cu_seqlens, num_seqs, scale, v=v)
+    T, H, D, N, Hk = P.T, P.H, P.D, P.N, P.Hk
+    q, k = (_need(P.flat(x), torch.bfloat16, (T, Hk, D), n) for x, n in ((q, "q"), (k, "k")))
+    v, dO = (_need(P.flat(x), torch.bfloat16, (T, H, D), n) for x, n in ((v, "v"), (dO, "dO")))
     g = _need(P.flat(g), torch.float32, (T, H), "g")
     beta_logit = _need(P.flat(beta_logit), torch.bfloat16, (T, H), "beta_logit")
     h0 = _opt(h0, torch.float32, (N, H, D, D), "h0")
     dht = _opt(dht, torch.float32, (N, H, D, D), "dht")
     ws = P.workspace(workspace)
-    o = out if out is not None else alloc_outputs(T, H, D, N, "gdn")
+    o = out if out is not None else alloc_outputs(T, H, D, N, "gdn", k_heads=Hk)
     rc = lib().gdr_bwd(ctypes.byref(P.shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta_logit),
                        _ptr(h0), _ptr(dO), _ptr(dht), _ptr(states), _ptr(ws), ws.numel(),
                        _ptr(o["dq"]), _ptr(o["dk"]), _ptr(o["dv"]), _ptr(o["dg"]), _ptr(o["dbeta"]),
@@ -264,17 +273,18 @@ def kda_bwd(q, k, v, g_raw, A_log, dt_bias, beta_logit, dO, h0=None, dht=None, c
             num_seqs=None, scale=None, states=None, workspace=None, out=None, kda_gate="softplus", gate_scale=0.0):
     """KDA backward.  Returns dict(dq, dk, dv, dg_raw, dbeta, dh0, dA_log, ddt_bias); ``kda_gate`` /
     ``gate_scale`` as make_shape."""
-    P = _Problem(q, cu_seqlens, num_seqs, scale, kda_gate, gate_scale)
-    T, H, D, N = P.T, P.H, P.D, P.N
-    q, k, v, dO, g_raw = (_need(P.flat(x), torch.bfloat16, (T, H, D), n)
-                          for x, n in ((q, "q"), (k, "k"), (v, "v"), (dO, "dO"), (g_raw, "g_raw")))
+    P = _Problem(q, cu_seqlens, num_seqs, scale, kda_gate, gate_scale, v=v)
+    T, H, D, N, Hk = P.T, P.H, P.D, P.N, P.Hk
+    q, k = (_need(P.flat(x), torch.bfloat16, (T, Hk, D), n) for x, n in ((q, "q"), (k, "k")))
+    v, dO, g_raw = (_need(P.flat(x), torch.bfloat16, (T, H, D), n)
+                    for x, n in ((v, "v"), (dO, "dO"), (g_raw, "g_raw")))
     A_log = _need(A_log, torch.float32, (H,), "A_log")
     dt_bias = _need(dt_bias, torch.float32, (H, D), "dt_bias")
     beta_logit = _need(P.flat(beta_logit), torch.bfloat16, (T, H), "beta_logit")
     h0 = _opt(h0, torch.float32, (N, H, D, D), "h0")
     dht = _opt(dht, torch.float32, (N, H, D, D), "dht")
     ws = P.workspace(workspace)
-    o = out if out is not None else alloc_outputs(T, H, D, N, "kda")
+    o = out if out is not None else alloc_outputs(T, H, D, N, "kda", k_heads=Hk)
     rc = lib().kda_bwd(ctypes.byref(P.shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g_raw), _ptr(A_log),
                        _ptr(dt_bias), _ptr(beta_logit), _ptr(h0), _ptr(dO), _ptr(dht), _ptr(states),
                        _ptr(ws), ws.numel(), _ptr(o["dq"]), _ptr(o["dk"]), _ptr(o["dv"]),
@@ -313,9 +323,10 @@ def conv1d_bwd(x, weight, bias, dy, cu_seqlens=None, num_seqs=None, silu=True):
     return {"dx": dx if dense is None else dx.reshape(*dense, C), "dweight": dw, "dbias": db}
 
 
-def alloc_outputs(T, H, D, N, gate, device="cuda"):
+def alloc_outputs(T, H, D, N, gate, device="cuda", k_heads=None):
     bf = dict(dtype=torch.bfloat16, device=device)
-    o = {"dq": torch.empty(T, H, D, **bf), "dk": torch.empty(T, H, D, **bf),
+    Hk = H if k_heads is None else k_heads
+    o = {"dq": torch.empty(T, Hk, D, **bf), "dk": torch.empty(T, Hk, D, **bf),
          "dv": torch.empty(T, H, D, **bf), "dbeta": torch.empty(T, H, **bf),
          "dh0": torch.empty(N, H, D, D, dtype=torch.float32, device=device)}
     if gate == "gdn":

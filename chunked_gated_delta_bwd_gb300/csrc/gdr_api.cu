@@ -65,6 +65,45 @@ __global__ void __launch_bounds__(1024) k_chunk_table(const int64_t* cu, int N, 
     if (t == 1023) chunk_off[N] = s_tot[1023];
 }
 
+// GQA: dq and dk of each q / k head are the sums of the terms of its value heads
+// (bf16 [T][H][D] in the workspace, summed in fp32); eight channels per thread, both tensors.
+__global__ void __launch_bounds__(256) k_group_sum(const __nv_bfloat16* __restrict__ pq,
+                                                   const __nv_bfloat16* __restrict__ pk, __nv_bfloat16* oq,
+                                                   __nv_bfloat16* ok, int64_t T, int H, int Hk, int D) {
+    const int r = H / Hk;
+    const int64_t n8 = T * Hk * D / 8;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < 2 * n8; i += (int64_t)gridDim.x * blockDim.x) {
+        const bool second = i >= n8;
+        const int64_t e = (second ? i - n8 : i) * 8;
+        const int64_t t = e / ((int64_t)Hk * D);
+        const int rem = (int)(e % ((int64_t)Hk * D)), hk = rem / D, d = rem % D;
+        const __nv_bfloat16* src = (second ? pk : pq) + ((t * H + (int64_t)hk * r) * D + d);
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int j = 0; j < r; ++j) {
+            const uint4 v = *reinterpret_cast<const uint4*>(src + (int64_t)j * D);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float2 f = unpack_bf16(w[q]);
+                acc[2 * q] += f.x;
+                acc[2 * q + 1] += f.y;
+            }
+        }
+        uint4 o;
+        o.x = pack_bf16(acc[0], acc[1]);
+        o.y = pack_bf16(acc[2], acc[3]);
+        o.z = pack_bf16(acc[4], acc[5]);
+        o.w = pack_bf16(acc[6], acc[7]);
+        *reinterpret_cast<uint4*>((second ? ok : oq) + e) = o;
+    }
+}
+
+cudaError_t launch_group_sum(const Params& p, cudaStream_t s) {
+    if (p.T_total == 0) return cudaSuccess;
+    k_group_sum<<<8 * num_sms(), 256, 0, s>>>(p.dq, p.dk, p.dq_out, p.dk_out, p.T_total, p.H, p.Hk, p.D);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_chunk_table(const Params& p, cudaStream_t s) {
     k_chunk_table<<<1, 1024, 0, s>>>(p.cu_seqlens, p.N, p.T_total, const_cast<int*>(p.chunk_off), p.status);
     return cudaGetLastError();
@@ -75,7 +114,7 @@ cudaError_t launch_chunk_table(const Params& p, cudaStream_t s) {
 // ---------------------------------------------------------------------------
 struct Layout {
     int64_t max_chunks;
-    size_t status, chunk_off, W, U, Kr, R, Rlo, T, gT, egT, S0, dS, segL, segLb, segP, segS, total;
+    size_t status, chunk_off, W, U, Kr, R, Rlo, T, gT, egT, S0, dS, segL, segLb, segP, segS, dqk, total;
     int seg_G;
 };
 
@@ -90,6 +129,8 @@ static gdr_status check_shape(const gdr_shape* sh) {
     if (!sh->cu_seqlens && sh->total_tokens % sh->num_seqs != 0)
         return fail(GDR_ERR_INVALID, "dense layout needs total_tokens divisible by num_seqs");
     if (sh->num_heads > 65535) return fail(GDR_ERR_INVALID, "num_heads must be <= 65535");
+    if (sh->num_k_heads < 0 || (sh->num_k_heads > 0 && sh->num_heads % sh->num_k_heads != 0))
+        return fail(GDR_ERR_INVALID, "num_heads must be a multiple of num_k_heads (or num_k_heads 0)");
     if (sh->kda_gate != GDR_KDA_GATE_SOFTPLUS && sh->kda_gate != GDR_KDA_GATE_SIGMOID)
         return fail(GDR_ERR_INVALID, "kda_gate must be GDR_KDA_GATE_SOFTPLUS or GDR_KDA_GATE_SIGMOID");
     if (sh->kda_gate == GDR_KDA_GATE_SIGMOID && !(sh->gate_scale <= 0.f && sh->gate_scale > -1e30f))
@@ -139,6 +180,9 @@ static Layout layout(const gdr_shape* sh) {
     L.segLb = o; o = align256(o + segb);
     L.segP = o; o = align256(o + segb);
     L.segS = o; o = align256(o + 2 * segb);
+    // GQA: per-value-head dq, dk terms (bf16 [T, H, D] each) before the group sums
+    const bool gqa = sh->num_k_heads > 0 && sh->num_k_heads < sh->num_heads;
+    L.dqk = o; o = align256(o + (gqa ? 2 * (size_t)T * H * D * 2 : 0));
     L.total = o;
     return L;
 }
@@ -159,6 +203,7 @@ static void base_params(Params& p, const gdr_shape* sh, const Layout& L, void* w
     memset(&p, 0, sizeof(p));
     p.N = sh->num_seqs;
     p.H = sh->num_heads;
+    p.Hk = sh->num_k_heads > 0 ? sh->num_k_heads : sh->num_heads;
     p.D = sh->head_dim;
     p.T_total = sh->total_tokens;
     p.seq_len = sh->cu_seqlens ? 0 : sh->total_tokens / sh->num_seqs;
@@ -305,6 +350,12 @@ static gdr_status bwd_impl(const gdr_shape* sh, const void* q, const void* k, co
     p.h0 = h0; p.dht = dht;
     if (states) p.S0 = (__nv_bfloat16*)states;
     p.dq = (__nv_bfloat16*)dq; p.dk = (__nv_bfloat16*)dk; p.dv = (__nv_bfloat16*)dv;
+    if (p.Hk < p.H) {  // GQA: per-value-head terms in the workspace, summed over each group at the end
+        p.dq_out = p.dq;
+        p.dk_out = p.dk;
+        p.dq = reinterpret_cast<__nv_bfloat16*>(static_cast<unsigned char*>(ws) + L.dqk);
+        p.dk = p.dq + (size_t)p.T_total * p.H * p.D;
+    }
     p.dbeta = (__nv_bfloat16*)dbeta; p.dg = dg; p.dg_raw = (__nv_bfloat16*)dg_raw;
     p.dh0 = dh0; p.dA_log = dA_log; p.ddt_bias = ddt_bias;
     cudaStream_t s = (cudaStream_t)stream;
@@ -319,6 +370,10 @@ static gdr_status bwd_impl(const gdr_shape* sh, const void* q, const void* k, co
     if (e != cudaSuccess) return cuda_fail(e, "state recurrence launch");
     e = timed(GDR_KERNEL_MAIN, s, [&] { return launch_main(p, s); });
     if (e != cudaSuccess) return cuda_fail(e, "main backward launch");
+    if (p.Hk < p.H) {
+        e = timed(GDR_KERNEL_MAIN, s, [&] { return launch_group_sum(p, s); });
+        if (e != cudaSuccess) return cuda_fail(e, "group sum launch");
+    }
     g_err[0] = 0;
     return GDR_OK;
 }

@@ -121,16 +121,17 @@ __device__ __forceinline__ void load_beta(const Params& p, const ChunkInfo& ci, 
         sBeta[r] = r < ci.len ? sigmoid_f(bf2f(p.beta_logit[(ci.t0 + r) * p.H + h])) : 0.f;
 }
 
-// Issues cp.async copies of the chunk's rows of a token-major [T,H,D] tensor
-// into a swizzled C x D tile (rows >= len are zero-filled).
+// Issues cp.async copies of the chunk's rows of a token-major [T,heads,D] tensor
+// into a swizzled C x D tile (rows >= len are zero-filled); heads < 0 means p.H.
 template <int D, class Tile>
 __device__ __forceinline__ void async_load_rows(const Tile& t, const __nv_bfloat16* src, const Params& p,
-                                                const ChunkInfo& ci, int h) {
+                                                const ChunkInfo& ci, int h, int heads = -1) {
     constexpr int CPR = D / 8;  // 16-byte chunks per row
+    const int nh = heads < 0 ? p.H : heads;
     for (int i = threadIdx.x; i < CH * CPR; i += blockDim.x) {
         const int r = i / CPR, j = i % CPR;
         const bool ok = r < ci.len;
-        const __nv_bfloat16* g = src + ((ci.t0 + (ok ? r : 0)) * p.H + h) * D + j * 8;
+        const __nv_bfloat16* g = src + ((ci.t0 + (ok ? r : 0)) * nh + h) * D + j * 8;
         cp_async16(t.chunk(r, j), g, ok);
     }
 }
@@ -172,11 +173,11 @@ __device__ __forceinline__ void row_inv_norms_smem(const Tile& t, float* out) {
 // Same, reading the chunk's rows of a token-major global tensor.
 template <int D>
 __device__ __forceinline__ void row_inv_norms_global(const __nv_bfloat16* src, const Params& p,
-                                                     const ChunkInfo& ci, int h, float* out) {
+                                                     const ChunkInfo& ci, int h, float* out, int heads = -1) {
     const int r = threadIdx.x >> 2, part = threadIdx.x & 3;
     float s = 0.f;
     if (r < ci.len) {
-        const uint4* g = reinterpret_cast<const uint4*>(src + ((ci.t0 + r) * p.H + h) * D);
+        const uint4* g = reinterpret_cast<const uint4*>(src + ((ci.t0 + r) * (heads < 0 ? p.H : heads) + h) * D);
 #pragma unroll
         for (int j = part * (D / 32); j < (part + 1) * (D / 32); ++j) {
             uint4 v = g[j];
@@ -225,15 +226,17 @@ template <int KIND, int D, bool KDA, bool SRC_GLOBAL, class Tile>
 __device__ __forceinline__ void build_tile(const Tile& dst, const Tile& src, const __nv_bfloat16* gsrc,
                                            const Params& p, const ChunkInfo& ci, int h,
                                            const Gates<D, KDA>& G, const float* inv,
-                                           const float* rowmul, float mul, const Tile* lo = nullptr) {
-    // With `lo`, the tile is stored as a bf16 pair: dst = bf16(v), lo = bf16(v - dst).
+                                           const float* rowmul, float mul, const Tile* lo = nullptr,
+                                           int heads = -1) {
+    // With `lo`, the tile is stored as a bf16 pair: dst = bf16(v), lo = bf16(v - dst).  A
+    // global source has `heads` heads per token (heads < 0 means p.H); h indexes them.
     constexpr int CPR = D / 8;
     for (int i = threadIdx.x; i < CH * CPR; i += blockDim.x) {
         const int r = i / CPR, j = i % CPR;
         uint4 v;
         if (SRC_GLOBAL) {
             if (r < ci.len)
-                v = *reinterpret_cast<const uint4*>(gsrc + ((ci.t0 + r) * p.H + h) * D + j * 8);
+                v = *reinterpret_cast<const uint4*>(gsrc + ((ci.t0 + r) * (heads < 0 ? p.H : heads) + h) * D + j * 8);
             else
                 v = make_uint4(0, 0, 0, 0);
         } else {

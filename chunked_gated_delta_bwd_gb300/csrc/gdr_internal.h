@@ -10,6 +10,8 @@ namespace gdr {
 struct Params {
     // shape
     int N, H, D;
+    int Hk;                 // q / k heads (GQA: H is a multiple; value head h reads q / k head h / (H / Hk))
+    __nv_bfloat16 *dq_out, *dk_out;  // GQA: the caller's dq / dk [T,Hk,D] (dq / dk hold per-value-head terms)
     int64_t T_total;
     int64_t seq_len;        // dense layout: tokens per sequence (T_total / N)
     int max_chunks;         // upper bound on the number of chunks (grid size)
@@ -49,6 +51,9 @@ struct Params {
     float *dh0, *dA_log, *ddt_bias;
 };
 
+// q / k head of value head h
+__host__ __device__ __forceinline__ int qk_head(const Params& p, int h) { return h / (p.H / p.Hk); }
+
 // multiprocessors of the current device (cached per device)
 inline int num_sms() {
     static int cache[64] = {0};
@@ -83,5 +88,6 @@ cudaError_t launch_states_tc(const Params& p, bool fwd, bool bwd, cudaStream_t s
 cudaError_t launch_main(const Params& p, cudaStream_t s);
 cudaError_t launch_main_tc2(const Params& p, cudaStream_t s);  // GDN and KDA, D = 128, tcgen05 + TMA
 cudaError_t launch_out(const Params& p, cudaStream_t s);       // forward output o = R S0 + P U
+cudaError_t launch_group_sum(const Params& p, cudaStream_t s);  // GQA: dq, dk summed over each head group
 
 }  // namespace gdr

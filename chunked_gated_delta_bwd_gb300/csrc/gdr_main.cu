@@ -96,7 +96,8 @@ __global__ void __launch_bounds__(256, 1) k_main(const Params p) {
     const size_t tcc = ((size_t)chunk * p.H + h) * CH * CH;
 
     // ---- loads -------------------------------------------------------------
-    async_load_rows<D>(sK, p.k, p, ci, h);
+    const int hq = qk_head(p, h);  // q / k head of this value head
+    async_load_rows<D>(sK, p.k, p, ci, hq, p.Hk);
     async_load_rows<D>(sV, p.v, p, ci, h);
     async_load_rows<D>(sDO, p.dO, p, ci, h);
     async_load_tile<D, D>(sS0, p.S0 + tdd);
@@ -105,7 +106,7 @@ __global__ void __launch_bounds__(256, 1) k_main(const Params p) {
     cp_async_commit();
     load_gates<D, KDA>(p, ci, h, G, false);
     load_beta(p, ci, h, sBeta);
-    row_inv_norms_global<D>(p.q, p, ci, h, sInvQ);
+    row_inv_norms_global<D>(p.q, p, ci, hq, sInvQ, p.Hk);
     cp_async_wait<0>();
     __syncthreads();
     row_inv_norms_smem<D>(sK, sInvK);
@@ -171,7 +172,7 @@ __global__ void __launch_bounds__(256, 1) k_main(const Params p) {
     zero_acc(dKn);
     zero_acc(dGc);
     auto qraw = [&](int r, int c) -> float {
-        return r < ci.len ? bf2f(p.q[((ci.t0 + r) * p.H + h) * D + c]) : 0.f;
+        return r < ci.len ? bf2f(p.q[((ci.t0 + r) * p.Hk + hq) * D + c]) : 0.f;
     };
     auto kraw = [&](int r, int c) -> float {
         return bf2f(*reinterpret_cast<const __nv_bfloat16*>(sK.ptr(r, c)));
@@ -198,7 +199,8 @@ __global__ void __launch_bounds__(256, 1) k_main(const Params p) {
     }
     __syncthreads();
     // qd' -> X1 ; P = lower(qd' ki'^T)
-    build_tile<F_KDP, D, KDA, true>(sX1, sX1, p.q, p, ci, h, G, sInvQ, nullptr, p.scale);
+    build_tile<F_KDP, D, KDA, true>(sX1, sX1, p.q, p, ci, hq, G, sInvQ, nullptr, p.scale,
+                                    static_cast<const decltype(sX1)*>(nullptr), p.Hk);
     __syncthreads();
     {
         float acc[1][4][4];
@@ -393,7 +395,8 @@ __global__ void __launch_bounds__(256, 1) k_main(const Params p) {
     }
     __syncthreads();
     // qd' -> X1, kd' -> X2 (+ lo) ; dki' = dP^T qd' + (beta dA)^T kd'
-    build_tile<F_KDP, D, KDA, true>(sX1, sX1, p.q, p, ci, h, G, sInvQ, nullptr, p.scale, PREC ? &sQDlo : nullptr);
+    build_tile<F_KDP, D, KDA, true>(sX1, sX1, p.q, p, ci, hq, G, sInvQ, nullptr, p.scale, PREC ? &sQDlo : nullptr,
+                                    p.Hk);
     build_tile<F_KDP, D, KDA, false>(sX2, sK, nullptr, p, ci, h, G, sInvK, nullptr, 1.f, PREC ? &sKDlo : nullptr);
     __syncthreads();
     {
@@ -429,7 +432,7 @@ __global__ void __launch_bounds__(256, 1) k_main(const Params p) {
                 const int r = mD + frag_g() + 8 * hf, c = nD + nt * 8 + 2 * frag_c();
                 float2 qv = make_float2(0.f, 0.f);
                 if (r < ci.len)
-                    qv = unpack_bf16(*reinterpret_cast<const uint32_t*>(p.q + ((ci.t0 + r) * p.H + h) * D + c));
+                    qv = unpack_bf16(*reinterpret_cast<const uint32_t*>(p.q + ((ci.t0 + r) * p.Hk + hq) * D + c));
                 const float2 kv = unpack_bf16(*reinterpret_cast<const uint32_t*>(sK.ptr(r, c)));
                 qn[nt][2 * hf] = qv.x * sInvQ[r];
                 qn[nt][2 * hf + 1] = qv.y * sInvQ[r];

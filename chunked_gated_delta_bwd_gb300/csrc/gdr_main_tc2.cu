@@ -152,9 +152,9 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
         const int hh = item % p.H, t0 = (int)cj.t0, rcd = item * CH, rdd = item * MD;
         tc::mbar_expect_tx(mload, 4 * TILE + 2 * 2 * TILE + CH * CH * 2 + (KDA ? TILE : 0));
         if (KDA) tc::tma_load_4d(sb + oW0, &m.graw, 0, hh, t0, 0, mload);  // raw gates (token-major)
-        tc::tma_load_4d(sb + oK, &m.k, 0, hh, t0, 0, mload);
+        tc::tma_load_4d(sb + oK, &m.k, 0, qk_head(p, hh), t0, 0, mload);
         tc::tma_load_4d(sb + oV, &m.v, 0, hh, t0, 0, mload);
-        tc::tma_load_4d(sb + oW2, &m.q, 0, hh, t0, 0, mload);
+        tc::tma_load_4d(sb + oW2, &m.q, 0, qk_head(p, hh), t0, 0, mload);
         tc::tma_load_3d(sb + oDOY, &m.dO, 0, hh, t0, mload);  // rows 0..63 of a 128-row tile
         tc::tma_load_3d(sb + oDOY + 128 * 128, &m.dO, 64, hh, t0, mload);
         tc::tma_load_3d(sb + oS0, &m.S0, 0, rdd, 0, mload);
@@ -920,7 +920,7 @@ static cudaError_t launch_main_tc2_t(const Params& p, cudaStream_t s) {
     const uint64_t rows_cc = (uint64_t)p.max_chunks * p.H * CH;
     const uint64_t rows_dd = (uint64_t)p.max_chunks * p.H * MD;
     const uint64_t T = (uint64_t)p.T_total;
-    bool ok = encode_blocked_tokens_map(&m.q, p.q, T, p.H) && encode_blocked_tokens_map(&m.k, p.k, T, p.H) &&
+    bool ok = encode_blocked_tokens_map(&m.q, p.q, T, p.Hk) && encode_blocked_tokens_map(&m.k, p.k, T, p.Hk) &&
               encode_blocked_tokens_map(&m.v, p.v, T, p.H) && encode_tokens_map(&m.dO, p.dO, T, p.H, MD) &&
               encode_blocked_rows_map(&m.S0, p.S0, rows_dd, MD) && encode_blocked_rows_map(&m.dS, p.dS, rows_dd, MD) &&
               encode_rows_map(&m.T, p.Tm, rows_cc, CH, CH) &&

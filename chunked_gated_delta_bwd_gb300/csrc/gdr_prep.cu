@@ -72,13 +72,14 @@ __global__ void __launch_bounds__(256, 1) k_prep(const Params p) {
     const size_t tile_cd = ((size_t)chunk * p.H + h) * CH * D;
     const size_t tile_cc = ((size_t)chunk * p.H + h) * CH * CH;
 
-    if (SM::QS) async_load_rows<D>(sQ, p.q, p, ci, h);
-    async_load_rows<D>(sK, p.k, p, ci, h);
+    const int hq = qk_head(p, h);  // q / k head of this value head
+    if (SM::QS) async_load_rows<D>(sQ, p.q, p, ci, hq, p.Hk);
+    async_load_rows<D>(sK, p.k, p, ci, hq, p.Hk);
     async_load_rows<D>(sV, p.v, p, ci, h);
     cp_async_commit();
     load_gates<D, KDA>(p, ci, h, G, true);
     load_beta(p, ci, h, sBeta);
-    if (!SM::QS) row_inv_norms_global<D>(p.q, p, ci, h, sInvQ);
+    if (!SM::QS) row_inv_norms_global<D>(p.q, p, ci, hq, sInvQ, p.Hk);
     cp_async_wait<0>();
     __syncthreads();
 
@@ -91,7 +92,8 @@ __global__ void __launch_bounds__(256, 1) k_prep(const Params p) {
     if (SM::QS)
         build_tile<F_KDP, D, KDA, false>(sX3, sQ, nullptr, p, ci, h, G, sInvQ, nullptr, p.scale);
     else
-        build_tile<F_KDP, D, KDA, true>(sX3, sX3, p.q, p, ci, h, G, sInvQ, nullptr, p.scale);
+        build_tile<F_KDP, D, KDA, true>(sX3, sX3, p.q, p, ci, hq, G, sInvQ, nullptr, p.scale,
+                                        static_cast<const decltype(sX3)*>(nullptr), p.Hk);
     __syncthreads();
 
     // A = strict_lower(diag(beta) kd' ki'^T) (fp32), P = lower(qd' ki'^T) (bf16); A is written
@@ -174,7 +176,7 @@ __global__ void __launch_bounds__(256, 1) k_prep(const Params p) {
         frag_foreach(acc, m0, n0, [&](int r, int c, float a0, float a1) {
             const float2 q =
                 SM::QS ? unpack_bf16(*reinterpret_cast<const uint32_t*>(sQ.ptr(r, c)))
-                : r < ci.len ? unpack_bf16(*reinterpret_cast<const uint32_t*>(p.q + ((ci.t0 + r) * p.H + h) * D + c))
+                : r < ci.len ? unpack_bf16(*reinterpret_cast<const uint32_t*>(p.q + ((ci.t0 + r) * p.Hk + hq) * D + c))
                              : make_float2(0.f, 0.f);
             const float s = p.scale * sInvQ[r];
             const float qd0 = q.x * s * gate_factor<F_KD>(G, r, c);

@@ -243,8 +243,8 @@ __global__ void __launch_bounds__(512, 1) k_prep_tc(const Params p, const __grid
         const int hh = item % p.H, t0 = (int)cj.t0;
         const uint32_t bar = mload0 + 8 * stg, st = sb + stg * STAGE;
         tc::mbar_expect_tx(bar, 3 * TILE);
-        tc::tma_load_4d(st + oQ, &m.q, 0, hh, t0, 0, bar);
-        tc::tma_load_4d(st + oK, &m.k, 0, hh, t0, 0, bar);
+        tc::tma_load_4d(st + oQ, &m.q, 0, qk_head(p, hh), t0, 0, bar);
+        tc::tma_load_4d(st + oK, &m.k, 0, qk_head(p, hh), t0, 0, bar);
         tc::tma_load_4d(st + oV, &m.v, 0, hh, t0, 0, bar);
     };
     // (KDA) raw gates of `item`, token-major, into the space of A (dead from the end of the
@@ -673,7 +673,7 @@ template <bool KDA>
 static cudaError_t launch_prep_tc_t(const Params& p, cudaStream_t s) {
     PrepMaps m;
     const uint64_t T = (uint64_t)p.T_total;
-    if (!(encode_blocked_tokens_map(&m.q, p.q, T, p.H) && encode_blocked_tokens_map(&m.k, p.k, T, p.H) &&
+    if (!(encode_blocked_tokens_map(&m.q, p.q, T, p.Hk) && encode_blocked_tokens_map(&m.k, p.k, T, p.Hk) &&
           encode_blocked_tokens_map(&m.v, p.v, T, p.H) &&
           encode_blocked_tokens_map(&m.graw, KDA ? p.g_raw : nullptr, T, p.H)))
         return cudaErrorInvalidValue;

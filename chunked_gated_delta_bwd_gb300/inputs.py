@@ -39,6 +39,7 @@ class Case:
     with_h0: bool = False
     with_dht: bool = False
     lengths: Optional[tuple] = None  # explicit lengths (overrides the dense / random ones)
+    k_heads: Optional[int] = None     # q / k heads (GQA: fewer than `heads`, which counts v heads)
     kda_gate: str = "softplus"        # KDA gate function ("softplus" or "sigmoid")
     gate_scale: float = 0.0           # the sigmoid gate's scale
     note: str = field(default="", compare=False)
@@ -57,6 +58,9 @@ CASES = {
     "kda_sigmoid_b1_h16_t8k": Case("kda_sigmoid_b1_h16_t8k", "kda", 1, 8192, 16, 128, seed=5, with_h0=True,
                                    with_dht=True, kda_gate="sigmoid", gate_scale=-2.0,
                                    note="KDA with the sigmoid-bounded gate: B=1 H=16 T=8192 D=128"),
+    "gdn_gqa_hk16_hv32_t4k": Case("gdn_gqa_hk16_hv32_t4k", "gdn", 1, 4096, 32, 128, seed=6, with_h0=True,
+                                  with_dht=True, k_heads=16,
+                                  note="GDN with grouped q/k heads: 16 q/k heads, 32 v heads, T=4096"),
     "gdn_h16_t32k": Case("gdn_h16_t32k", "gdn", 1, 32768, 16, 128, seed=4, with_h0=True,
                          with_dht=True, note="long-sequence GDN bwd: B=1 H=16 T=32768 D=128"),
     "kda_h16_t32k": Case("kda_h16_t32k", "kda", 1, 32768, 16, 128, seed=4, with_h0=True,
@@ -84,8 +88,9 @@ def make(case: Case):
         return (torch.randn(*shape, generator=gen) * std).to(dtype)
 
     x = {"cu_seqlens": cu, "scale": D ** -0.5, "mode": case.mode}
-    x["q"] = normal(T, H, D)
-    x["k"] = normal(T, H, D)
+    Hk = H if case.k_heads is None else case.k_heads
+    x["q"] = normal(T, Hk, D)
+    x["k"] = normal(T, Hk, D)
     x["v"] = normal(T, H, D)
     x["beta_logit"] = normal(T, H)
     if case.mode == "gdn":
@@ -117,7 +122,9 @@ def conv_case(lengths, channels, width, seed, with_bias=True, silu=True):
     return {"cu_seqlens": cu, "x": x, "weight": w, "bias": b, "dy": dy, "silu": silu}
 
 
-def custom(mode, lengths, heads, dim, seed, with_h0=False, with_dht=False, kda_gate="softplus", gate_scale=0.0):
+def custom(mode, lengths, heads, dim, seed, with_h0=False, with_dht=False, kda_gate="softplus", gate_scale=0.0,
+           k_heads=None):
     """A case with explicit sequence lengths (ragged tails, empty sequences, ...)."""
     return make(Case("custom", mode, len(lengths), 0, heads, dim, seed, with_h0=with_h0,
-                     with_dht=with_dht, lengths=tuple(lengths), kda_gate=kda_gate, gate_scale=gate_scale))
+                     with_dht=with_dht, lengths=tuple(lengths), kda_gate=kda_gate, gate_scale=gate_scale,
+                     k_heads=k_heads))

@@ -20,7 +20,8 @@
  * Conventions for every entry point
  * ---------------------------------
  *  * All tensor pointers are DEVICE pointers, 16-byte aligned, contiguous:
- *      q, k, v, dO, dq, dk, dv, g_raw, dg_raw : bf16   [T_total, H, D]   (token-major)
+ *      q, k, v, dO, dq, dk, dv, g_raw, dg_raw : bf16   [T_total, H, D]   (token-major;
+ *                                               q, k, dq, dk [T_total, Hk, D] with GQA)
  *      beta_logit, dbeta                      : bf16   [T_total, H]
  *      g, dg  (GDN natural-log gate)          : float  [T_total, H]
  *      A_log, dA_log                          : float  [H]
@@ -81,6 +82,11 @@ typedef struct {
      *     gate is gate_scale * sigmoid(a x)); gate_scale must be finite and <= 0. */
     int32_t kda_gate;
     float gate_scale;
+    /* Grouped q / k heads (GQA): the number Hk of q and k heads, 0 meaning num_heads.
+     * num_heads (H) counts the heads of everything else (v, gates, beta, states, o, dO);
+     * H must be a multiple of Hk, and value head h reads q / k head h / (H / Hk).  q, k,
+     * dq and dk are then [T_total, Hk, D]; dq and dk sum over each group. */
+    int32_t num_k_heads;
 } gdr_shape;
 #define GDR_KDA_GATE_SOFTPLUS 0
 #define GDR_KDA_GATE_SIGMOID 1

@@ -43,12 +43,25 @@ def run_gpu(x, states=None, workspace=None):
     return {k: v.cpu() for k, v in out.items()}
 
 
+def k_heads_of(x, heads):
+    """The q / k heads that the value heads `heads` read (GQA: whole groups expected)."""
+    r = x["v"].shape[1] // x["q"].shape[1]
+    if heads is None or r == 1:
+        return heads
+    groups = sorted({h // r for h in heads})
+    assert sorted(heads) == [g * r + j for g in groups for j in range(r)], "sample whole head groups"
+    return groups
+
+
 def run_oracle(x, heads=None):
     """Oracle on the bf16-rounded inputs (upcast to float64), optionally on a subset of heads."""
     from oracle import oracle
     sel = (lambda t: t) if heads is None else (lambda t: t[:, heads])
     selh = (lambda t: t) if heads is None else (lambda t: t[heads])
-    q, k, v, dO = (sel(f64(x[n])) for n in ("q", "k", "v", "dO"))
+    kh = k_heads_of(x, heads)
+    selk = (lambda t: t) if kh is None else (lambda t: t[:, kh])
+    q, k = (selk(f64(x[n])) for n in ("q", "k"))
+    v, dO = (sel(f64(x[n])) for n in ("v", "dO"))
     b = sel(f64(x["beta_logit"]))
     h0 = None if x["h0"] is None else (f64(x["h0"]) if heads is None else f64(x["h0"])[:, heads])
     dht = None if x["dht"] is None else (f64(x["dht"]) if heads is None else f64(x["dht"])[:, heads])
@@ -67,6 +80,8 @@ def compare(gpu, ref, x, heads=None, conditioned=False):
     signs -- are judged relative to the sum of the magnitudes of their terms
     instead of to the (possibly near-cancelling) sum itself."""
     sel = (lambda t: t) if heads is None else (lambda t: t[:, heads])
+    kh = k_heads_of(x, heads)
+    selk = (lambda t: t) if kh is None else (lambda t: t[:, kh])
     pairs = {"dq": ("dq", TOL_BF16), "dk": ("dk", TOL_BF16), "dv": ("dv", TOL_BF16),
              "dbeta": ("dbeta", TOL_BF16), "dh0": ("dh0", TOL_FP32)}
     if x["mode"] == "gdn":
@@ -81,6 +96,8 @@ def compare(gpu, ref, x, heads=None, conditioned=False):
             g = g if heads is None else g[heads]
         elif name == "dh0":
             g = g if heads is None else g[:, heads]
+        elif name in ("dq", "dk"):
+            g = selk(g)
         else:
             g = sel(g)
         res[name] = (rel_l2(g, ref[rname]), tol)
@@ -126,7 +143,10 @@ def run_oracle_fwd(x, heads=None):
     from oracle import oracle
     sel = (lambda t: t) if heads is None else (lambda t: t[:, heads])
     selh = (lambda t: t) if heads is None else (lambda t: t[heads])
-    q, k, v = (sel(f64(x[n])) for n in ("q", "k", "v"))
+    kh = k_heads_of(x, heads)
+    selk = (lambda t: t) if kh is None else (lambda t: t[:, kh])
+    q, k = (selk(f64(x[n])) for n in ("q", "k"))
+    v = sel(f64(x["v"]))
     b = sel(f64(x["beta_logit"]))
     h0 = None if x["h0"] is None else (f64(x["h0"]) if heads is None else f64(x["h0"])[:, heads])
     cu = x["cu_seqlens"].numpy()

@@ -169,7 +169,8 @@ def test_conv1d_arguments_rejected(L):
     ok = [2, 256, 8, 4, None, A, A, A, A, 1, A, A, A, None]
     def call(args):
         return L.gdr_conv1d_bwd(*args)
-    for i, v, code in ((3, 5, 2), (3, 0, 2), (2, 6, 1), (0, 0, 1), (1, 255, 1)):  # width, channels, N, dense T
+    # every call here must be rejected on the host (the pointers are not device memory)
+    for i, v, code in ((3, 5, 2), (3, 0, 2), (2, 7, 1), (0, 0, 1), (1, 255, 1)):  # width, channels, N, dense T
         bad = list(ok)
         bad[i] = v
         assert call(bad) == code, (i, v)

@@ -40,6 +40,12 @@ def test_varlen_ragged_with_h0(mode, dim):
 
 
 @pytest.mark.parametrize("dim", [64, 128])
+def test_grouped_qk_heads(dim):
+    x = inputs.custom("gdn", [1, 63, 200, 130], heads=4, dim=dim, seed=117, with_h0=True, k_heads=2)
+    _check(x, label="fwd_gqa_d%d" % dim)
+
+
+@pytest.mark.parametrize("dim", [64, 128])
 def test_empty_and_single_token_sequences(dim):
     x = inputs.custom("kda", [0, 1, 0, 64, 1], heads=2, dim=dim, seed=112, with_h0=True)
     gpu = _check(x, label="fwd_empty_d%d" % dim)

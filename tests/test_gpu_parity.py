@@ -59,6 +59,16 @@ def test_segmented_state_passing_varlen(mode):
     _check(x, label="segments_%s" % mode, conditioned=(mode == "kda"))
 
 
+@pytest.mark.parametrize("mode", ["gdn", "kda"])
+@pytest.mark.parametrize("dim", [64, 128])
+def test_grouped_qk_heads_varlen(mode, dim):
+    # GQA: 2 q / k heads shared by 6 value heads (3 per group)
+    x = inputs.custom(mode, [1, 63, 200, 130], heads=6, dim=dim, seed=116, with_h0=True, with_dht=True,
+                      k_heads=2)
+    gpu = _check(x, label="gqa_%s_d%d" % (mode, dim), conditioned=(mode == "kda"))
+    assert tuple(gpu["dq"].shape) == (x["q"].shape[0], 2, dim)
+
+
 def test_gdn_dense_layout():
     # equal lengths passed without cu_seqlens (dense B x T)
     import chunked_gated_delta_bwd_gb300 as gdr
@@ -135,6 +145,7 @@ def test_bad_cu_seqlens_are_flagged_not_faulted():
     ("gdn_b2_h16_t4k", [0, 5, 10, 15]),
     ("kda_b1_h16_t8k", [0, 5, 10, 15]),
     ("kda_sigmoid_b1_h16_t8k", [0, 15]),
+    ("gdn_gqa_hk16_hv32_t4k", [0, 1, 30, 31]),
     ("gdn_varlen_h32", [0, 31]),
     ("gdn_h16_t32k", [3, 12]),
     ("kda_h16_t32k", [3, 12]),
