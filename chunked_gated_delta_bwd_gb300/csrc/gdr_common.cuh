@@ -233,24 +233,34 @@ __device__ __forceinline__ void softplus_sigmoid(float x, float& sp, float& sg) 
 //   mode 1 (sigmoid-bounded):  g = ln2 gs sigmoid(a x)  ("FlashKDA之backward（K1）" §5.2: the
 //                              base-2 log gate gs sigmoid(a x), written in natural log)
 constexpr float kLn2f = 0.6931471805599453f;
+template <int MODE>
+__device__ __forceinline__ float kda_gate_fn(float gs, float a, float x) {
+    if constexpr (MODE == 0) return -a * softplus_f(x);
+    else return kLn2f * gs * sigmoid_f(a * x);
+}
 __device__ __forceinline__ float kda_gate_fn(int mode, float gs, float a, float x) {
-    return mode == 0 ? -a * softplus_f(x) : kLn2f * gs * sigmoid_f(a * x);
+    return mode == 0 ? kda_gate_fn<0>(gs, a, x) : kda_gate_fn<1>(gs, a, x);
 }
 // Its chain rule for one element: dgl = dL/dg.  Returns dL/dg_raw (which is also the
 // element's dt_bias term) and sets dA, the element's term of dL/dA_log.
 //   mode 0: dg/dx = -a sigmoid(x), dg/dA_log = g
 //   mode 1: dg/dz = ln2 gs s (1 - s) with z = a x, s = sigmoid(z); dz/dx = a, dz/dA_log = a x
-__device__ __forceinline__ float kda_gate_bwd(int mode, float gs, float a, float x, float dgl, float& dA) {
-    if (mode == 0) {
+template <int MODE>
+__device__ __forceinline__ float kda_gate_bwd(float gs, float a, float x, float dgl, float& dA) {
+    if constexpr (MODE == 0) {
         float sp, sg;
         softplus_sigmoid(x, sp, sg);
         dA = dgl * (-a * sp);
         return dgl * (-a * sg);
+    } else {
+        const float s = sigmoid_f(a * x);
+        const float dz = dgl * (kLn2f * gs) * (s * (1.f - s));
+        dA = dz * a * x;
+        return dz * a;
     }
-    const float s = sigmoid_f(a * x);
-    const float dz = dgl * (kLn2f * gs) * (s * (1.f - s));
-    dA = dz * a * x;
-    return dz * a;
+}
+__device__ __forceinline__ float kda_gate_bwd(int mode, float gs, float a, float x, float dgl, float& dA) {
+    return mode == 0 ? kda_gate_bwd<0>(gs, a, x, dgl, dA) : kda_gate_bwd<1>(gs, a, x, dgl, dA);
 }
 
 }  // namespace gdr

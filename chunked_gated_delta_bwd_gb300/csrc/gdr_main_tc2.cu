@@ -35,7 +35,7 @@ namespace {
 constexpr int MD = 128;
 constexpr int TILE = CH * MD * 2;  // 16 KB: a C x D token-major or a D x C channel-major bf16 tile
 // shared-memory map (bytes from the 1024-aligned base); later tenants after the arrows
-constexpr int oK = 0;           // k (token-major)     -> (KDA) beta E lo  -> (KDA) qd' lo
+constexpr int oK = 0;           // k (token-major)     -> kr [d][r] -> (KDA) beta E lo -> (KDA) qd' lo
 constexpr int oV = 16384;       // v -> beta E (token-major)
 constexpr int oDOY = 32768;     // [dO; dY] token-major, 128 rows
 constexpr int oS0 = 65536;      // S0 [j][d]          -> kd' [d][r] (+ lo at +16 KB)
@@ -46,7 +46,7 @@ constexpr int oP = 147456;      // P, lower [r][s]
 constexpr int oW0 = 155648;     // (KDA) raw gate tile -> kd' [d][r] (G1, A block 0) -> kd [d][r]
                                 //   -> (KDA) u^T lo -> ki' [d][r]
 constexpr int oW1 = 172032;     // qd' [d][r] (G1, A block 1) -> u^T [j][r] -> (KDA) ki' lo
-constexpr int oW2 = 188416;     // q (token-major) -> ki' [d][r] -> kr [d][r] -> du^T -> qd' [d][r]
+constexpr int oW2 = 188416;     // q (token-major) -> ki' [d][r] -> du^T -> qd' [d][r]
 constexpr int oSmall = 204800;
 // small arrays (floats)
 constexpr int NCOL = 16;  // rows per thread (16 warps: 4 lane quarters x 4 row quarters)
@@ -103,7 +103,7 @@ __device__ __forceinline__ float warp_transpose_sum16(float (&v)[16]) {
 
 }  // namespace
 
-template <bool KDA>
+template <bool KDA, int GATE>
 __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __grid_constant__ MainMaps m) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -145,21 +145,25 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
     G.ref = sGate + CH;
     G.gT = sGate + CH + 1;
 
-    // every operand tile of an item (thread 0)
-    auto issue_loads = [&](int item) {
+    // the operand tiles of an item: copy `which` (0 .. 8), or all of them (which < 0).  The
+    // copies may be issued by different threads and in any order: the transaction count of
+    // the barrier can run ahead of the expectation that copy 0's thread registers.
+    auto issue_loads = [&](int item, int which) {
         ChunkInfo cj;
         lookup_chunk(item / p.H, p.N, p.chunk_off, p.cu_seqlens, p.seq_len, cj);
         const int hh = item % p.H, t0 = (int)cj.t0, rcd = item * CH, rdd = item * MD;
-        tc::mbar_expect_tx(mload, 4 * TILE + 2 * 2 * TILE + CH * CH * 2 + (KDA ? TILE : 0));
-        if (KDA) tc::tma_load_4d(sb + oW0, &m.graw, 0, hh, t0, 0, mload);  // raw gates (token-major)
-        tc::tma_load_4d(sb + oK, &m.k, 0, qk_head(p, hh), t0, 0, mload);
-        tc::tma_load_4d(sb + oV, &m.v, 0, hh, t0, 0, mload);
-        tc::tma_load_4d(sb + oW2, &m.q, 0, qk_head(p, hh), t0, 0, mload);
-        tc::tma_load_3d(sb + oDOY, &m.dO, 0, hh, t0, mload);  // rows 0..63 of a 128-row tile
-        tc::tma_load_3d(sb + oDOY + 128 * 128, &m.dO, 64, hh, t0, mload);
-        tc::tma_load_3d(sb + oS0, &m.S0, 0, rdd, 0, mload);
-        tc::tma_load_3d(sb + oDS, &m.dS, 0, rdd, 0, mload);
-        tc::tma_load_2d(sb + oT, &m.T, 0, rcd, mload);
+        if (which <= 0) tc::mbar_expect_tx(mload, 4 * TILE + 2 * 2 * TILE + CH * CH * 2 + (KDA ? TILE : 0));
+        if (KDA && (which < 0 || which == 0))
+            tc::tma_load_4d(sb + oW0, &m.graw, 0, hh, t0, 0, mload);  // raw gates (token-major)
+        if (which < 0 || which == 1) tc::tma_load_4d(sb + oK, &m.k, 0, qk_head(p, hh), t0, 0, mload);
+        if (which < 0 || which == 2) tc::tma_load_4d(sb + oV, &m.v, 0, hh, t0, 0, mload);
+        if (which < 0 || which == 3) tc::tma_load_4d(sb + oW2, &m.q, 0, qk_head(p, hh), t0, 0, mload);
+        if (which < 0 || which == 4)  // rows 0..63 of a 128-row tile
+            tc::tma_load_3d(sb + oDOY, &m.dO, 0, hh, t0, mload);
+        if (which < 0 || which == 5) tc::tma_load_3d(sb + oDOY + 128 * 128, &m.dO, 64, hh, t0, mload);
+        if (which < 0 || which == 6) tc::tma_load_3d(sb + oS0, &m.S0, 0, rdd, 0, mload);
+        if (which < 0 || which == 7) tc::tma_load_3d(sb + oDS, &m.dS, 0, rdd, 0, mload);
+        if (which < 0 || which == 8) tc::tma_load_2d(sb + oT, &m.T, 0, rcd, mload);
     };
 
     // ---- set-up: tensor memory, barriers, the first item's loads ----------------------
@@ -168,7 +172,7 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
         tc::mbar_init(mb, 1);
         tc::mbar_init(mload, 1);
         tc::mbar_init(mgr, 1);
-        if ((int)blockIdx.x < n_items) issue_loads(blockIdx.x);
+        if ((int)blockIdx.x < n_items) issue_loads(blockIdx.x, -1);
     }
     tc::fence_before();
     __syncthreads();
@@ -296,7 +300,7 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
         float acc = 0.f;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-            if (c0 + i < ci.len) acc += kda_gate_fn(p.kda_gate, p.gate_scale, a, g[i] + bias);
+            if (c0 + i < ci.len) acc += kda_gate_fn<GATE>(p.gate_scale, a, g[i] + bias);
             g[i] = acc;
         }
         sScan[hc * MD + L] = acc;  // this quarter's total
@@ -456,16 +460,25 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
         return (uint32_t)((L >> 6) * rows * 128 + (c0 + i) * 128 + ((lch ^ (i & 7)) << 4) + lsub);
     };
 
-    // ---- G1: [A_raw; P] = [kd'; qd'] ki'^T ----------------------------------------
+    // ---- G1: [A_raw; P] = [kd'; qd'] ki'^T ; then G3: dqd^T = S0 dO^T, G5b: dS^T kr^T --------
+    // (G3 and G5b need no G1 result: they run while the G1 epilogue does)
     build(sW0, nullptr, false, 1.f, F_KDP);    // kd'
     build(sW1, nullptr, true, p.scale, F_KDP);  // qd'
     build(sW2, nullptr, false, 1.f, F_KIP);     // ki' (the q tile is dead)
+    build(sK, nullptr, false, 1.f, F_KR);       // kr (the k tile is dead: staged in tensor memory)
     sync_all();
     if (tid == 0) {
         constexpr uint32_t id = tc::idesc(128, 64, 1, 1);
         for (int k = 0; k < MD; k += 16)
             tc::mma(tmem + R_B, tc::mdesc(sb + oW0, 128, 0, k), tc::mdesc(sb + oW2, 128, 0, k), id, k > 0);
         tc::commit(mb);
+        constexpr uint32_t id3 = tc::idesc(128, 64, 1, 0), id5 = tc::idesc(128, 64, 0, 1);
+        for (int k = 0; k < MD; k += 16)
+            tc::mma(tmem + R_D, tc::mdesc(sb + oS0, 128, 0, k), tc::kdesc(sb + oDOY, 128, 0, k), id3, k > 0);
+        // second half of G5 (independent of beta E): du^T = dS^T kr^T (+ dO^T P later); the
+        // next commit (after G2) covers these two groups
+        for (int k = 0; k < MD; k += 16)
+            tc::mma(tmem + R_A, tc::kdesc(sb + oDS, 128, 0, k), tc::mdesc(sb + oK, 128, 0, k), id5, k > 0);
     }
     if (!wait_mma()) return;
     tc::ld16(tl(R_B + c0), v);
@@ -494,20 +507,13 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
         }
     }
     build(sW0, nullptr, false, 1.f, F_KD);  // kd (G1 has completed: kd' is dead)
-    build(sW2, nullptr, false, 1.f, F_KR);  // kr (ki' is dead)
     sync_all();
 
-    // ---- G2: X^T = S0^T kd^T ; G3: dqd^T = S0 dO^T ; G5b: dS^T kr^T ----------------------
+    // ---- G2: X^T = S0^T kd^T (its commit also covers G3 and G5b) ---------------------------
     if (tid == 0) {
-        constexpr uint32_t id2 = tc::idesc(128, 64, 0, 1), id3 = tc::idesc(128, 64, 1, 0),
-                           id5 = tc::idesc(128, 64, 0, 1);
+        constexpr uint32_t id2 = tc::idesc(128, 64, 0, 1);
         for (int k = 0; k < MD; k += 16)
             tc::mma(tmem + R_C, tc::kdesc(sb + oS0, 128, 0, k), tc::mdesc(sb + oW0, 128, 0, k), id2, k > 0);
-        for (int k = 0; k < MD; k += 16)
-            tc::mma(tmem + R_D, tc::mdesc(sb + oS0, 128, 0, k), tc::kdesc(sb + oDOY, 128, 0, k), id3, k > 0);
-        // second half of G5 (independent of beta E): du^T = dS^T kr^T (+ dO^T P later)
-        for (int k = 0; k < MD; k += 16)
-            tc::mma(tmem + R_A, tc::kdesc(sb + oDS, 128, 0, k), tc::mdesc(sb + oW2, 128, 0, k), id5, k > 0);
         tc::commit(mb);
     }
     if (!wait_mma()) return;
@@ -557,7 +563,7 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
     else
         store_cm(sW1, v);
     tc::ld16(tl(R_A + c0), v);
-    store_cm(sW2, v);  // du^T over kr
+    store_cm(sW2, v);  // du^T over ki'
     sync_all();
 
     // ---- G6: dY^T = du^T T ------------------------------------------------------------
@@ -739,7 +745,7 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
     if (!wait_mma()) return;
     // every large shared tile is dead: the next item's operands may land while this epilogue runs
     if (item + (int)gridDim.x < n_items) {
-        if (tid == 0) issue_loads(item + gridDim.x);
+        if (lane == 0 && warp < 9) issue_loads(item + gridDim.x, warp);  // one copy per warp
         pending = true;
         prefetch_small(item + gridDim.x);
     }
@@ -884,7 +890,7 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
             const int r = c0 + i;
             if (r < ci.len) {
                 float dA;
-                const float draw = kda_gate_bwd(p.kda_gate, p.gate_scale, ea, xr[i], dGc[i] + post, dA);
+                const float draw = kda_gate_bwd<GATE>(p.gate_scale, ea, xr[i], dGc[i] + post, dA);
                 p.dg_raw[((ci.t0 + r) * p.H + h) * MD + L] = __float2bfloat16(draw);
                 ddt += draw;
                 dA_acc += dA;
@@ -914,7 +920,7 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
     if (warp == 0) tc::dealloc(tmem, 512);
 }
 
-template <bool KDA>
+template <bool KDA, int GATE>
 static cudaError_t launch_main_tc2_t(const Params& p, cudaStream_t s) {
     MainMaps m;
     const uint64_t rows_cc = (uint64_t)p.max_chunks * p.H * CH;
@@ -926,16 +932,18 @@ static cudaError_t launch_main_tc2_t(const Params& p, cudaStream_t s) {
               encode_rows_map(&m.T, p.Tm, rows_cc, CH, CH) &&
               encode_blocked_tokens_map(&m.graw, KDA ? p.g_raw : nullptr, T, p.H);
     if (!ok) return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(k_main_tc2<KDA>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(k_main_tc2<KDA, GATE>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int items = p.max_chunks * p.H;
     const int ctas = items < num_sms() ? items : num_sms();
-    k_main_tc2<KDA><<<ctas, 512, SMEM_BYTES, s>>>(p, m);
+    k_main_tc2<KDA, GATE><<<ctas, 512, SMEM_BYTES, s>>>(p, m);
     return cudaGetLastError();
 }
 
 cudaError_t launch_main_tc2(const Params& p, cudaStream_t s) {
-    return p.kda ? launch_main_tc2_t<true>(p, s) : launch_main_tc2_t<false>(p, s);
+    // the KDA gate function is a template parameter: each instance carries only its own code
+    if (!p.kda) return launch_main_tc2_t<false, 0>(p, s);
+    return p.kda_gate == 0 ? launch_main_tc2_t<true, 0>(p, s) : launch_main_tc2_t<true, 1>(p, s);
 }
 
 }  // namespace gdr

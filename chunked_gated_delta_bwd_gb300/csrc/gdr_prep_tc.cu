@@ -199,7 +199,7 @@ __device__ __forceinline__ void invert_tc(const float* sA, float* tT, float* xfe
 
 }  // namespace
 
-template <bool KDA>
+template <bool KDA, int GATE>
 __global__ void __launch_bounds__(512, 1) k_prep_tc(const Params p, const __grid_constant__ PrepMaps m) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -236,16 +236,20 @@ __global__ void __launch_bounds__(512, 1) k_prep_tc(const Params p, const __grid
     G.ref = sGate + CH;
     G.gT = sGate + CH + 1;
 
-    // q, k, v of item `it` into stage s (thread 0)
-    auto issue_loads = [&](int item, int stg) {
+    // q, k, v of item `it` into stage s: copy `which` (0 q, 1 k, 2 v) or all (which < 0); the
+    // copies may be issued by different threads in any order (the barrier's transaction
+    // count can run ahead of the expectation registered with copy 0)
+    auto issue_loads = [&](int item, int stg, int which) {
         ChunkInfo cj;
         lookup_chunk(item / p.H, p.N, p.chunk_off, p.cu_seqlens, p.seq_len, cj);
         const int hh = item % p.H, t0 = (int)cj.t0;
         const uint32_t bar = mload0 + 8 * stg, st = sb + stg * STAGE;
-        tc::mbar_expect_tx(bar, 3 * TILE);
-        tc::tma_load_4d(st + oQ, &m.q, 0, qk_head(p, hh), t0, 0, bar);
-        tc::tma_load_4d(st + oK, &m.k, 0, qk_head(p, hh), t0, 0, bar);
-        tc::tma_load_4d(st + oV, &m.v, 0, hh, t0, 0, bar);
+        if (which <= 0) {
+            tc::mbar_expect_tx(bar, 3 * TILE);
+            tc::tma_load_4d(st + oQ, &m.q, 0, qk_head(p, hh), t0, 0, bar);
+        }
+        if (which < 0 || which == 1) tc::tma_load_4d(st + oK, &m.k, 0, qk_head(p, hh), t0, 0, bar);
+        if (which < 0 || which == 2) tc::tma_load_4d(st + oV, &m.v, 0, hh, t0, 0, bar);
     };
     // (KDA) raw gates of `item`, token-major, into the space of A (dead from the end of the
     // inversion to the next item's G1)
@@ -262,7 +266,7 @@ __global__ void __launch_bounds__(512, 1) k_prep_tc(const Params p, const __grid
         tc::mbar_init(mload0 + 8, 1);
         tc::mbar_init(mgr, 1);
         if ((int)blockIdx.x < n_items) {
-            issue_loads(blockIdx.x, 0);
+            issue_loads(blockIdx.x, 0, -1);
             if (KDA) issue_gate_load(blockIdx.x);
         }
     }
@@ -364,7 +368,7 @@ __global__ void __launch_bounds__(512, 1) k_prep_tc(const Params p, const __grid
     // the next item's tiles into the other stage (its previous tenant finished last iteration)
     pending = -1;
     if (has_next) {
-        if (tid == 0) issue_loads(item + gridDim.x, stg ^ 1);
+        if (lane == 0 && warp >= 13) issue_loads(item + gridDim.x, stg ^ 1, warp - 13);  // one copy per warp
         pending = stg ^ 1;
         pending_par = (uint32_t)(((it + 1) >> 1) & 1);
     }
@@ -397,7 +401,7 @@ __global__ void __launch_bounds__(512, 1) k_prep_tc(const Params p, const __grid
         float acc = 0.f;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-            if (c0 + i < ci.len) acc += kda_gate_fn(p.kda_gate, p.gate_scale, a, g[i] + bias);
+            if (c0 + i < ci.len) acc += kda_gate_fn<GATE>(p.gate_scale, a, g[i] + bias);
             g[i] = acc;
         }
         sScan[hc * PD + L] = acc;
@@ -669,7 +673,7 @@ __global__ void __launch_bounds__(512, 1) k_prep_tc(const Params p, const __grid
     if (warp == 0) tc::dealloc(tmem, 512);
 }
 
-template <bool KDA>
+template <bool KDA, int GATE>
 static cudaError_t launch_prep_tc_t(const Params& p, cudaStream_t s) {
     PrepMaps m;
     const uint64_t T = (uint64_t)p.T_total;
@@ -677,16 +681,17 @@ static cudaError_t launch_prep_tc_t(const Params& p, cudaStream_t s) {
           encode_blocked_tokens_map(&m.v, p.v, T, p.H) &&
           encode_blocked_tokens_map(&m.graw, KDA ? p.g_raw : nullptr, T, p.H)))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(k_prep_tc<KDA>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(k_prep_tc<KDA, GATE>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int items = p.max_chunks * p.H;
     const int ctas = items < num_sms() ? items : num_sms();
-    k_prep_tc<KDA><<<ctas, 512, SMEM_BYTES, s>>>(p, m);
+    k_prep_tc<KDA, GATE><<<ctas, 512, SMEM_BYTES, s>>>(p, m);
     return cudaGetLastError();
 }
 
 cudaError_t launch_prep_tc(const Params& p, cudaStream_t s) {
-    return p.kda ? launch_prep_tc_t<true>(p, s) : launch_prep_tc_t<false>(p, s);
+    if (!p.kda) return launch_prep_tc_t<false, 0>(p, s);
+    return p.kda_gate == 0 ? launch_prep_tc_t<true, 0>(p, s) : launch_prep_tc_t<true, 1>(p, s);
 }
 
 }  // namespace gdr
