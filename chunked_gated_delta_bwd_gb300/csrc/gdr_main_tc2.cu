@@ -123,7 +123,7 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
     float* sInvQ = fsm;
     float* sInvK = sInvQ + nInvQ;
     float* sBeta = sInvK + nInvK;
-    float* sFac = sBeta + nBeta;     // GDN [4][64]: e^{gc}, e^{gc-ref}, e^{ref-gc}, e^{gT-gc}
+    float* sFac = sBeta + nBeta;     // GDN [4][64]: e^{gc}, e^{gc-ref}, e^{ref-gc}, e^{gT-gc}; KDA [2][128]: e^{ref}, e^{gT-ref}
     float* sGate = sFac + nFac;      // GDN gc[64], ref, gT; KDA dt_bias[d]
     float* sRef = sGate + nGate;     // KDA ref[d]
     float* sGT = sRef + nRef;        // KDA gT[d]
@@ -282,13 +282,13 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
         pending = false;
     }
     // KDA: per-channel log gates of this thread's channel and rows, scanned across the four
-    // row quarters, staged in tensor memory (lane = channel, column = row)
-    float refL = 0.f, gTL = 0.f;
+    // row quarters; once the chunk's reference is known, e^{gc - ref} is staged in tensor
+    // memory (lane = channel, column = row) and the other gate factors derive from it
+    float g[16];  // (KDA) cumulative gates of this thread's rows
     if constexpr (KDA) {
         const float a = expf(alog);
         if (hc == 0) sGate[L] = bias;  // for the gate chain rule at the end of the item
         if (tid == 0) sMisc[32] = a;
-        float g[16];  // raw gates of this channel and rows, from the token-major tile in W0
         {
             const int lch = (L & 63) >> 3, lsub = (L & 7) << 1;
 #pragma unroll
@@ -333,6 +333,8 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
             }
             sRef[L] = 0.5f * (M + N);
             sGT[L] = tot;
+            sFac[L] = __expf(0.5f * (M + N));              // e^{ref}
+            sFac[MD + L] = __expf(tot - 0.5f * (M + N));   // e^{gT - ref}
         }
     }
 
@@ -347,8 +349,11 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
     }
     __syncthreads();
     if constexpr (KDA) {
-        refL = sRef[L];
-        gTL = sGT[L];
+        const float refL = sRef[L];
+        float f[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) f[i] = __expf(g[i] - refL);
+        tc::st16(tl(R_G + c0), f);
     }
 
     // inverse row norms of q (from W2) and k, 4 threads per row; GDN gate factor table;
@@ -421,12 +426,17 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
     // per-element factors of this thread's channel and rows
     auto factors = [&](int kind, float (&f)[16]) {
         if constexpr (KDA) {
-            float g[16];
-            tc::ld16(tl(R_G + c0), g);
+            // e^{gc-ref} from tensor memory; e^{gc} = e^{gc-ref} e^{ref}, e^{ref-gc} = 1 / e^{gc-ref},
+            // e^{gT-gc} = e^{gT-ref} / e^{gc-ref} (|gc - ref| <= 80: no overflow)
+            const float eRef = sFac[L], eGTref = sFac[MD + L];
+            float e[16];
+            tc::ld16(tl(R_G + c0), e);
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-                const float e = kind == F_KD ? g[i] : kind == F_KDP ? g[i] - refL : kind == F_KIP ? refL - g[i] : gTL - g[i];
-                f[i] = __expf(e);
+                if (kind == F_KDP) f[i] = e[i];
+                else if (kind == F_KD) f[i] = e[i] * eRef;
+                else if (kind == F_KIP) f[i] = __fdividef(1.f, e[i]);
+                else f[i] = __fdividef(eGTref, e[i]);
             }
         } else {
             rows16(sFac + kind * CH, f);
