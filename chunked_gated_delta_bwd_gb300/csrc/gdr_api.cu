@@ -115,7 +115,7 @@ cudaError_t launch_chunk_table(const Params& p, cudaStream_t s) {
 struct Layout {
     int64_t max_chunks;
     size_t status, chunk_off, W, U, Kr, R, Rlo, T, gT, egT, S0, dS, segL, segLb, segP, segS, dqk, total;
-    int seg_G;
+    int seg_G, seg_G1;  // segments for calls that run both state directions / one
 };
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -142,16 +142,20 @@ static gdr_status check_shape(const gdr_shape* sh) {
     return GDR_OK;
 }
 
-// Segments of the time-parallel state passing (1 = the serial chains).  A function of the
-// shape only, sized for one wave of about 150 SMs: phase 1 runs 3G - 4 CTAs and phase 3
-// 2G CTAs per (sequence, head); each segment keeps at least 32 chunks.
-static int seg_count(const gdr_shape* sh, int64_t max_chunks) {
+// Segments of the time-parallel state passing (1 = the serial chains), for calls that run
+// both directions or one.  A function of the shape only, sized for one wave of about 150
+// SMs: phase 1 runs 3G - 4 CTAs per (sequence, head) for both directions and 2G - 3 for
+// one, phase 3 runs G per direction; each segment keeps at least 32 chunks, and G <= 8
+// keeps the serial boundary composition short.
+static int seg_count(const gdr_shape* sh, int64_t max_chunks, bool two_dirs) {
     if (sh->head_dim != 128) return 1;
     const int64_t pairs = (int64_t)sh->num_seqs * sh->num_heads;
     const int64_t per_seq = max_chunks / sh->num_seqs;
     int G = 1;
-    for (int g = 2; g <= 4; ++g)
-        if ((3 * g - 4) * pairs <= 148 && 2 * g * pairs <= 148 && per_seq >= 32 * g) G = g;
+    for (int g = 2; g <= 8; ++g) {
+        const int64_t p1 = two_dirs ? 3 * g - 4 : 2 * g - 3, p3 = two_dirs ? 2 * g : g;
+        if (p1 * pairs <= 148 && p3 * pairs <= 148 && per_seq >= 32 * g) G = g;
+    }
     return G;
 }
 
@@ -174,8 +178,10 @@ static Layout layout(const gdr_shape* sh) {
     L.egT = o; o = align256(o + mc * H * D * 4);
     L.S0 = o; o = align256(o + mc * H * D * D * 2);
     L.dS = o; o = align256(o + mc * H * D * D * 2);
-    L.seg_G = seg_count(sh, L.max_chunks);
-    const size_t segb = L.seg_G > 1 ? (size_t)N * H * L.seg_G * D * D * 4 : 0;  // fp32 [pair][G][D][D]
+    L.seg_G = seg_count(sh, L.max_chunks, true);
+    L.seg_G1 = seg_count(sh, L.max_chunks, false);
+    const int64_t Gmax = L.seg_G > L.seg_G1 ? L.seg_G : L.seg_G1;
+    const size_t segb = Gmax > 1 ? (size_t)N * H * Gmax * D * D * 4 : 0;  // fp32 [pair][G][D][D]
     L.segL = o; o = align256(o + segb);
     L.segLb = o; o = align256(o + segb);
     L.segP = o; o = align256(o + segb);
@@ -227,6 +233,7 @@ static void base_params(Params& p, const gdr_shape* sh, const Layout& L, void* w
     p.S0 = reinterpret_cast<__nv_bfloat16*>(w + L.S0);
     p.dS = reinterpret_cast<__nv_bfloat16*>(w + L.dS);
     p.seg_G = L.seg_G;
+    p.seg_G1 = L.seg_G1;
     p.segL = reinterpret_cast<float*>(w + L.segL);
     p.segLb = reinterpret_cast<float*>(w + L.segLb);
     p.segP = reinterpret_cast<float*>(w + L.segP);

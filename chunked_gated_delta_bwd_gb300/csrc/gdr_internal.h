@@ -38,8 +38,10 @@ struct Params {
     float *gT, *egT;                     // [chunk][H][D]: chunk gate total and its exponential
     __nv_bfloat16 *S0, *dS;              // per chunk-head states, value-major [dv][dk]
     // time-parallel state passing (seg_G > 1): per (sequence, head) and segment, fp32 key-major
-    // [D][D]: segment results from zero (role 0 / role 1), segment transitions, segment starts
-    int seg_G;
+    // [D][D]: segment results from zero (role 0 / role 1), segment transitions, segment starts.
+    // seg_G serves calls that run both state directions, seg_G1 calls that run one; the
+    // kernels read seg_G, which the state launcher sets to the count of the call
+    int seg_G, seg_G1;
     float *segL, *segLb, *segP, *segS;
 
     // outputs

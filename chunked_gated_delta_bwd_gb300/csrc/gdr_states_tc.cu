@@ -374,60 +374,77 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_states_tc(const Params p, int p
     if (warp == 0) tc::dealloc(tmem, 512);
 }
 
-// Segment boundaries (phase 2), fp32 on CUDA cores: one CTA per (sequence, head, role).
-// Key-major states S [d][j]; a segment maps S_start to P^T S_start + L (role 0, the
-// transition chain stores P^T key-major) and dS_enter to P dS_enter + L' (role 1).  Each
-// thread owns a 4 x 8 block of the 128 x 128 result (rows 4 rb .., columns 8 cb ..).
-__global__ void __launch_bounds__(512) k_seg_combine(const Params p, int roles) {
+// Segment boundaries (phase 2), fp32 on CUDA cores: one CTA per (sequence, head, role,
+// 16-column slice).  The columns of the state crossing a boundary are independent
+// (S_end = P^T S_start + L acts on each column alone), so every slice walks the G - 1
+// boundaries by itself; each output is summed over the key index in ascending order.
+constexpr int CMB_COLS = 16, CMB_SLICES = 128 / CMB_COLS;
+__global__ void __launch_bounds__(256) k_seg_combine(const Params p, int roles) {
     extern __shared__ float sm[];
-    float* cur = sm;              // [128][128] the state crossing the boundary
-    float* tr = sm + 128 * 128;   // [128][128] the segment's transition (P^T, key-major)
+    float* tr = sm;               // [128][128] the segment's transition (P^T, key-major)
+    float* cur = sm + 128 * 128;  // [128][16] this slice of the state crossing the boundary
     const int pair = blockIdx.x, role = roles == 3 ? (int)blockIdx.y : (roles == 1 ? 0 : 1), G = p.seg_G,
-              DD = 128 * 128;
+              DD = 128 * 128, j0 = CMB_COLS * (int)blockIdx.z;
     const size_t pd = (size_t)pair * G;
-    const int tid = threadIdx.x, rb = tid >> 4, cb = tid & 15;
+    // thread: rows 4 rb .. 4 rb + 3 and columns j0 + 2 cb, j0 + 2 cb + 1 of the slice; the
+    // eight threads of a quarter warp share rb (their row reads are one broadcast)
+    const int tid = threadIdx.x, rb = tid >> 3, cb = tid & 7;
     const float* first = role == 0 ? p.segL + (pd + 0) * DD : p.segLb + (pd + G - 1) * DD;
-    for (int i = tid; i < DD / 4; i += 512) reinterpret_cast<float4*>(cur)[i] = reinterpret_cast<const float4*>(first)[i];
+    for (int i = tid; i < 128 * CMB_COLS / 4; i += 256) {
+        const int e = i / (CMB_COLS / 4), q = i % (CMB_COLS / 4);
+        reinterpret_cast<float4*>(cur)[i] = *reinterpret_cast<const float4*>(first + e * 128 + j0 + 4 * q);
+    }
     __syncthreads();
     for (int step = 0; step < G - 1; ++step) {
         const int g = role == 0 ? step + 1 : G - 2 - step;  // the segment that starts from `cur`
-        float4* dst = reinterpret_cast<float4*>(p.segS + ((pd + g) * 2 + role) * DD);
-        for (int i = tid; i < DD / 4; i += 512) dst[i] = reinterpret_cast<const float4*>(cur)[i];
+        float* dst = p.segS + ((pd + g) * 2 + role) * DD;
+        for (int i = tid; i < 128 * CMB_COLS / 4; i += 256) {
+            const int e = i / (CMB_COLS / 4), q = i % (CMB_COLS / 4);
+            *reinterpret_cast<float4*>(dst + e * 128 + j0 + 4 * q) = reinterpret_cast<const float4*>(cur)[i];
+        }
         if (step == G - 2) break;  // the last segment's start is all phase 3 needs
         const float* P = p.segP + (pd + g) * DD;
         const float* L = (role == 0 ? p.segL : p.segLb) + (pd + g) * DD;
-        for (int i = tid; i < DD / 4; i += 512) reinterpret_cast<float4*>(tr)[i] = reinterpret_cast<const float4*>(P)[i];
+        for (int i = tid; i < DD / 4; i += 256) reinterpret_cast<float4*>(tr)[i] = reinterpret_cast<const float4*>(P)[i];
         __syncthreads();
-        float acc[4][8];
+        float acc[4][2];
 #pragma unroll
         for (int r = 0; r < 4; ++r)
 #pragma unroll
-            for (int c = 0; c < 8; ++c) acc[r][c] = L[(size_t)(4 * rb + r) * 128 + 8 * cb + c];
-#pragma unroll 4
-        for (int e = 0; e < 128; ++e) {
-            const float4 s0 = *reinterpret_cast<const float4*>(cur + e * 128 + 8 * cb);
-            const float4 s1 = *reinterpret_cast<const float4*>(cur + e * 128 + 8 * cb + 4);
-            const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-            float a[4];
+            for (int c = 0; c < 2; ++c) acc[r][c] = L[(size_t)(4 * rb + r) * 128 + j0 + 2 * cb + c];
+#pragma unroll 2
+        for (int e = 0; e < 128; e += 4) {
+            float2 s[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) s[u] = *reinterpret_cast<const float2*>(cur + (e + u) * CMB_COLS + 2 * cb);
             if (role == 0) {  // (P^T S)[d][j] = sum_e P^T[d][e] S[e][j]
 #pragma unroll
-                for (int r = 0; r < 4; ++r) a[r] = tr[(4 * rb + r) * 128 + e];
+                for (int r = 0; r < 4; ++r) {
+                    const float4 a = *reinterpret_cast<const float4*>(tr + (4 * rb + r) * 128 + e);
+                    const float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        acc[r][0] = fmaf(av[u], s[u].x, acc[r][0]);
+                        acc[r][1] = fmaf(av[u], s[u].y, acc[r][1]);
+                    }
+                }
             } else {          // (P dS)[d][j] = sum_e P^T[e][d] dS[e][j]
-                const float4 t4 = *reinterpret_cast<const float4*>(tr + e * 128 + 4 * rb);
-                a[0] = t4.x, a[1] = t4.y, a[2] = t4.z, a[3] = t4.w;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float4 a = *reinterpret_cast<const float4*>(tr + (e + u) * 128 + 4 * rb);
+                    const float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        acc[r][0] = fmaf(av[r], s[u].x, acc[r][0]);
+                        acc[r][1] = fmaf(av[r], s[u].y, acc[r][1]);
+                    }
+                }
             }
-#pragma unroll
-            for (int r = 0; r < 4; ++r)
-#pragma unroll
-                for (int c = 0; c < 8; ++c) acc[r][c] = fmaf(a[r], sv[c], acc[r][c]);
         }
-        __syncthreads();  // every read of cur is done
+        __syncthreads();  // every read of cur and tr is done
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            float4* o = reinterpret_cast<float4*>(cur + (4 * rb + r) * 128 + 8 * cb);
-            o[0] = make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
-            o[1] = make_float4(acc[r][4], acc[r][5], acc[r][6], acc[r][7]);
-        }
+        for (int r = 0; r < 4; ++r)
+            *reinterpret_cast<float2*>(cur + (4 * rb + r) * CMB_COLS + 2 * cb) = make_float2(acc[r][0], acc[r][1]);
         __syncthreads();
     }
 }
@@ -450,20 +467,22 @@ cudaError_t launch_states_tc(const Params& p, bool fwd, bool bwd, cudaStream_t s
     if (e != cudaSuccess) return e;
     const int pairs = p.N * p.H;
     const int roles = (fwd ? 1 : 0) | (bwd ? 2 : 0), nroles = roles == 3 ? 2 : 1;
-    if (p.seg_G >= 2) {
+    Params q = p;
+    q.seg_G = roles == 3 ? p.seg_G : p.seg_G1;  // the segment count of this call's directions
+    if (q.seg_G >= 2) {
         // time-parallel segments: phase 1 chains, the boundaries, phase 3 chains
-        const int G = p.seg_G;
-        k_states_tc<<<pairs * phase1_tasks(G, roles), NTHREADS, SMEM_BYTES, s>>>(p, 1, roles, m);
+        const int G = q.seg_G;
+        k_states_tc<<<pairs * phase1_tasks(G, roles), NTHREADS, SMEM_BYTES, s>>>(q, 1, roles, m);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        const int cbytes = 2 * 128 * 128 * 4;
+        const int cbytes = (128 * 128 + 128 * CMB_COLS) * 4;
         e = cudaFuncSetAttribute(k_seg_combine, cudaFuncAttributeMaxDynamicSharedMemorySize, cbytes);
         if (e != cudaSuccess) return e;
-        k_seg_combine<<<dim3(pairs, nroles), 512, cbytes, s>>>(p, roles);
+        k_seg_combine<<<dim3(pairs, nroles, CMB_SLICES), 256, cbytes, s>>>(q, roles);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        k_states_tc<<<pairs * nroles * G, NTHREADS, SMEM_BYTES, s>>>(p, 3, roles, m);
+        k_states_tc<<<pairs * nroles * G, NTHREADS, SMEM_BYTES, s>>>(q, 3, roles, m);
         return cudaGetLastError();
     }
-    k_states_tc<<<dim3(pairs, nroles), NTHREADS, SMEM_BYTES, s>>>(p, 0, roles, m);
+    k_states_tc<<<dim3(pairs, nroles), NTHREADS, SMEM_BYTES, s>>>(q, 0, roles, m);
     return cudaGetLastError();
 }
 
