@@ -62,45 +62,6 @@ struct MainMaps {
     CUtensorMap q, k, v, dO, S0, dS, T, graw;
 };
 
-__device__ __forceinline__ float warp_sum(float x) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-    return x;
-}
-
-// Sum over the warp of each of 32 per-lane values: lane l returns the total of v[l]
-// (recursive halving: 31 exchanges instead of 32 x 5).
-__device__ __forceinline__ float warp_transpose_sum32(float (&v)[32]) {
-    const int lane = threadIdx.x & 31;
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) {
-        const bool up = (lane & o) != 0;
-#pragma unroll
-        for (int i = 0; i < o; ++i) {
-            const float send = up ? v[i] : v[i + o];
-            const float keep = up ? v[i + o] : v[i];
-            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-        }
-    }
-    return v[0];
-}
-// Same for 16 values: lanes l and l ^ 1 return the total of v[l >> 1].
-__device__ __forceinline__ float warp_transpose_sum16(float (&v)[16]) {
-    const int lane = threadIdx.x & 31;
-#pragma unroll
-    for (int o = 16; o >= 2; o >>= 1) {
-        const int n = o >> 1;  // values kept after this step
-        const bool up = (lane & o) != 0;
-#pragma unroll
-        for (int i = 0; i < n; ++i) {
-            const float send = up ? v[i] : v[i + n];
-            const float keep = up ? v[i + n] : v[i];
-            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-        }
-    }
-    return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
-}
-
 }  // namespace
 
 template <bool KDA, int GATE>
@@ -952,7 +913,7 @@ static cudaError_t launch_main_tc2_t(const Params& p, cudaStream_t s) {
 
 cudaError_t launch_main_tc2(const Params& p, cudaStream_t s) {
     // the KDA gate function is a template parameter: each instance carries only its own code
-    if (!p.kda) return launch_main_tc2_t<false, 0>(p, s);
+    if (!p.kda) return launch_main_gdn(p, s);
     return p.kda_gate == 0 ? launch_main_tc2_t<true, 0>(p, s) : launch_main_tc2_t<true, 1>(p, s);
 }
 
