@@ -8,12 +8,14 @@
 // kr = diag(invk e^{gT-gc}) k.  So the tensor cores read the raw bf16 q and k tiles as
 // they arrive (no derived tile is built) and the row factors are applied in fp32 where
 // a product's result is read or where the next operand is written:
-//   B1  G1  [A; P]_raw = [k; q] k^T       G2  X^T_raw = S0^T k^T
-//       G3  dqd^T      = S0 dO^T          G5b du^T_raw = dS^T k^T
+//   B1  G1  [A; P]_raw = [k; q] k^T       G2  X^T_raw = S0^T k^T    G5b du^T_raw = dS^T k^T
 //   B2  G4  u^T  = (beta E)^T T^T         G5a du^T = dO^T P      (+ G5b x invk e^{gT-gc})
 //   B3  G6  dY^T = du^T T
-//   B4  G7  Z^T  = S0 dY^T   G8 dkr^T = dS u^T   G9 [dP; dA]_raw = [dO; dY] u^T
+//   B4  G3/G7 [dqd^T, Z^T] = S0 [dO; dY]^T   G8 dkr^T = dS u^T   G9 [dP; dA]_raw = [dO; dY] u^T
 //   B5  G10 [dqd', dkd']^T = k^T X10^T    G11 dki'^T = q^T X11_P + k^T X11_A
+// A tcgen05.mma takes tens of cycles to issue whatever its size, so the groups of a batch
+// are issued by lane 0 of different warps (one per SM sub-partition), each committing to
+// the batch's barrier, and G3 waits for dY to run as one N = 128 product with G7.
 // with X10 = [dP; beta dA] scaled by the column factor invk_s e^{ref-gc_s} (ki' folded
 // in) and X11 = [dP; beta dA] scaled by the row factors of qd' and kd'.  B1 needs no
 // per-item preparation, so it is issued as soon as the tiles land and runs under the
@@ -88,6 +90,8 @@ __global__ void __launch_bounds__(512, 1) k_main_gdn(const Params p, const __gri
     float* sFac = sBeta + nBeta;          // [4][64] e^{gc}, e^{gc-ref}, e^{ref-gc}, e^{gT-gc} (Fac order)
     float* sTab = sFac + nFac;            // [6][64] combined row factors (Tab order)
     float* sGate = sTab + nTab;           // gc[64], ref, gT
+    // chunk of the current and of the next item, by item parity (seq, local, t0 lo / hi, len)
+    int* sCI = reinterpret_cast<int*>(sGate + nGate + 2);
     float* sDgTs = sGate + nGate + nPad;  // [128] state part of dgT
     float* sDgTp = sDgTs + nDgTs;         // [4][128] kr part of dgT per row quarter
     float* sDbP = sDgTp + nDgTp;          // [64] <dY, beta E> per row
@@ -98,9 +102,10 @@ __global__ void __launch_bounds__(512, 1) k_main_gdn(const Params p, const __gri
     float* sRowK = sRowQ + 256;           // [4][64] row dots <dk^, k^>
     float* sTot = sRowQ + nRow;           // [2][64] row dots summed over the lane quarters (q, k)
     uint64_t* mbars = reinterpret_cast<uint64_t*>(sTot + nTot);
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbars + 2);
-    // MMA completion; operand tiles of an item
-    const uint32_t mb = smem_u32(mbars), mload = smem_u32(mbars + 1);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbars + 4);
+    // operand tiles of an item; MMA completion of the batches with 1, 2 and 3 issuing threads
+    const uint32_t mload = smem_u32(mbars), mb1 = smem_u32(mbars + 1), mb2 = smem_u32(mbars + 2),
+                   mb3 = smem_u32(mbars + 3);
 
     Gates<MD, false> G;
     G.gc = sGate;
@@ -109,13 +114,22 @@ __global__ void __launch_bounds__(512, 1) k_main_gdn(const Params p, const __gri
 
     // the operand tiles of an item: copy `which` (0 .. 9), or all of them (which < 0); k and
     // q are stacked into one 128-row tile, one 64-column box at a time.  The copies may be
-    // issued by different threads and in any order: the barrier's phase cannot complete
-    // before copy 0's thread has registered the expectation.
-    auto issue_loads = [&](int item, int which) {
-        ChunkInfo cj;
-        lookup_chunk(item / p.H, p.N, p.chunk_off, p.cu_seqlens, p.seq_len, cj);
+    // issued by different threads, at different times and in any order: the barrier's phase
+    // cannot complete before the thread of copy 4 (the first one issued) has registered the
+    // expectation.
+    auto put_ci = [&](int slot, const ChunkInfo& c) {
+        int* d = sCI + 8 * slot;
+        d[0] = c.seq, d[1] = c.local, d[2] = (int)(c.t0 & 0xffffffff), d[3] = (int)(c.t0 >> 32), d[4] = c.len;
+    };
+    auto get_ci = [&](int slot) {
+        const int* d = sCI + 8 * slot;
+        ChunkInfo c;
+        c.seq = d[0], c.local = d[1], c.t0 = (int64_t)(((uint64_t)(uint32_t)d[3] << 32) | (uint32_t)d[2]), c.len = d[4];
+        return c;
+    };
+    auto issue_loads = [&](int item, const ChunkInfo& cj, int which) {
         const int hh = item % p.H, hk = qk_head(p, hh), t0 = (int)cj.t0, rcd = item * CH, rdd = item * MD;
-        if (which <= 0) tc::mbar_expect_tx(mload, 8 * TILE + CH * CH * 2);
+        if (which < 0 || which == 4) tc::mbar_expect_tx(mload, 8 * TILE + CH * CH * 2);
         if (which < 0 || which == 0) tc::tma_load_3d(sb + oKQ, &m.k, 0, hk, t0, mload);
         if (which < 0 || which == 1) tc::tma_load_3d(sb + oKQ + 2 * 8192, &m.k, 64, hk, t0, mload);
         if (which < 0 || which == 2) tc::tma_load_3d(sb + oKQ + 8192, &m.q, 0, hk, t0, mload);
@@ -131,33 +145,40 @@ __global__ void __launch_bounds__(512, 1) k_main_gdn(const Params p, const __gri
     // ---- set-up: tensor memory, barriers, the first item's loads ----------------------
     if (warp == 0) tc::alloc(smem_u32(tslot), 512);
     if (tid == 0) {
-        tc::mbar_init(mb, 1);
         tc::mbar_init(mload, 1);
-        if ((int)blockIdx.x < n_items) issue_loads(blockIdx.x, -1);
+        tc::mbar_init(mb1, 1);
+        tc::mbar_init(mb2, 2);
+        tc::mbar_init(mb3, 3);
+        if ((int)blockIdx.x < n_items) {
+            ChunkInfo c0i;
+            lookup_chunk((int)blockIdx.x / p.H, p.N, p.chunk_off, p.cu_seqlens, p.seq_len, c0i);
+            put_ci(0, c0i);
+            issue_loads(blockIdx.x, c0i, -1);
+        }
     }
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
     const uint32_t tmem = *tslot;
-    uint32_t phase = 0;
+    uint32_t phases = 0;  // bit n: the next phase of the barrier with n issuing threads
     int it = 0;                                // this CTA's item count (the load barrier's phase)
     bool pending = (int)blockIdx.x < n_items;  // a load batch is in flight
+    uint32_t pend_par = 0;                     // ... on this phase parity of the load barrier
     // the next item's gate (first warp, rows 2 lane and 2 lane + 1) and beta logit (thread
-    // r < 64), loaded one item ahead
-    float pg0 = 0.f, pg1 = 0.f, pb = 0.f;
-    auto prefetch_small = [&](int item) {
+    // r < 64), loaded one item ahead as raw values (rows clamped into the chunk) that are
+    // first read at the next item's top, so no thread waits for them
+    float pg0 = 0.f, pg1 = 0.f;
+    unsigned short pb = 0;
+    auto prefetch_small = [&](int item, const ChunkInfo& cj) {
         if (tid >= CH) return;
-        ChunkInfo cj;
-        lookup_chunk(item / p.H, p.N, p.chunk_off, p.cu_seqlens, p.seq_len, cj);
         const int hh = item % p.H;
-        pb = tid < cj.len ? bf2f(p.beta_logit[(cj.t0 + tid) * p.H + hh]) : 0.f;
+        pb = reinterpret_cast<const unsigned short*>(p.beta_logit)[(cj.t0 + min(tid, cj.len - 1)) * p.H + hh];
         if (tid < 32) {
-            const int r0 = 2 * tid;
-            pg0 = r0 < cj.len ? p.g[(cj.t0 + r0) * p.H + hh] : 0.f;
-            pg1 = r0 + 1 < cj.len ? p.g[(cj.t0 + r0 + 1) * p.H + hh] : 0.f;
+            pg0 = p.g[(cj.t0 + min(2 * tid, cj.len - 1)) * p.H + hh];
+            pg1 = p.g[(cj.t0 + min(2 * tid + 1, cj.len - 1)) * p.H + hh];
         }
     };
-    if ((int)blockIdx.x < n_items) prefetch_small(blockIdx.x);
+    if ((int)blockIdx.x < n_items) prefetch_small(blockIdx.x, get_ci(0));
     auto sync_all = [&]() {  // make smem writes visible to the tensor cores and order TMEM use
         tc::fence_async_smem();
         tc::fence_before();
@@ -170,15 +191,16 @@ __global__ void __launch_bounds__(512, 1) k_main_gdn(const Params p, const __gri
     auto bail = [&]() {
         if (tid == 0) {
             atomicOr(p.status, ST_MMA_TIMEOUT);
-            if (pending) tc::mbar_wait(mload, (uint32_t)(it & 1));
+            if (pending) tc::mbar_wait(mload, pend_par);
         }
         tc::fence_before();
         __syncthreads();
         if (warp == 0) tc::dealloc(tmem, 512);
     };
-    auto wait_mma = [&]() -> bool {
-        const bool ok = tc::mbar_wait(mb, phase);
-        phase ^= 1;
+    auto wait_mma = [&](int n) -> bool {
+        const uint32_t bar = n == 1 ? mb1 : n == 2 ? mb2 : mb3;
+        const bool ok = tc::mbar_wait(bar, (phases >> n) & 1);
+        phases ^= 1u << n;
         tc::fence_after();
         if (__syncthreads_or(!ok)) {
             bail();
@@ -218,11 +240,16 @@ __global__ void __launch_bounds__(512, 1) k_main_gdn(const Params p, const __gri
     };
 
     for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++it) {
-    const int chunk = item / p.H, h = item % p.H;
-    ChunkInfo ci;
-    lookup_chunk(chunk, p.N, p.chunk_off, p.cu_seqlens, p.seq_len, ci);
-    if (tid < 32) gdn_gate_scan(pg0, pg1, G, false, p);
-    if (tid < CH) sBeta[tid] = tid < ci.len ? sigmoid_f(pb) : 0.f;
+    const int h = item % p.H;
+    const ChunkInfo ci = get_ci(it & 1);
+    const int next = item + (int)gridDim.x;
+    if (tid == 32 && next < n_items) {  // the next item's chunk, for its loads and small values
+        ChunkInfo cn;
+        lookup_chunk(next / p.H, p.N, p.chunk_off, p.cu_seqlens, p.seq_len, cn);
+        put_ci((it + 1) & 1, cn);
+    }
+    if (tid < 32) gdn_gate_scan(2 * tid < ci.len ? pg0 : 0.f, 2 * tid + 1 < ci.len ? pg1 : 0.f, G, false, p);
+    if (tid < CH) sBeta[tid] = tid < ci.len ? sigmoid_f(__bfloat162float(__ushort_as_bfloat16(pb))) : 0.f;
 
     // wait for the operand tiles; rows past the chunk's end are zeroed before any product
     {
@@ -230,6 +257,7 @@ __global__ void __launch_bounds__(512, 1) k_main_gdn(const Params p, const __gri
         if (__syncthreads_or(!ok)) return bail();
         pending = false;
     }
+    if (next < n_items) prefetch_small(next, get_ci((it + 1) & 1));  // first read at the next item's top
     if (ci.len < CH) {
         const int nz = (CH - ci.len) * 16;  // 16-byte chunks per 128-column row
         for (int i = tid; i < 4 * nz; i += 512) {
@@ -241,19 +269,16 @@ __global__ void __launch_bounds__(512, 1) k_main_gdn(const Params p, const __gri
         sync_all();
     }
 
-    // ---- B1: G1 [A; P]_raw = [k; q] k^T, G2 X^T_raw = S0^T k^T, G3 dqd^T = S0 dO^T,
-    //      G5b du^T_raw = dS^T k^T: all on the tiles as loaded, under the prologue below
-    if (tid == 0) {
-        constexpr uint32_t id1 = tc::idesc(128, 64, 0, 0), id3 = tc::idesc(128, 64, 1, 0);
+    // ---- B1: G1 [A; P]_raw = [k; q] k^T, G2 X^T_raw = S0^T k^T, G5b du^T_raw = dS^T k^T:
+    //      all on the tiles as loaded, under the prologue below (three issuing threads)
+    if (lane == 0 && warp < 3) {
+        constexpr uint32_t id1 = tc::idesc(128, 64, 0, 0);
+        const uint32_t dst = tmem + (warp == 0 ? R_B : warp == 1 ? R_C : R_G5);
+        const uint32_t a = sb + (warp == 0 ? oKQ : warp == 1 ? oS0 : oDS);
+#pragma unroll
         for (int k = 0; k < MD; k += 16)
-            tc::mma(tmem + R_B, tc::kdesc(sb + oKQ, 128, 0, k), tc::kdesc(sb + oKQ, 128, 0, k), id1, k > 0);
-        for (int k = 0; k < MD; k += 16)
-            tc::mma(tmem + R_C, tc::kdesc(sb + oS0, 128, 0, k), tc::kdesc(sb + oKQ, 128, 0, k), id1, k > 0);
-        for (int k = 0; k < MD; k += 16)
-            tc::mma(tmem + R_D, tc::mdesc(sb + oS0, 128, 0, k), tc::kdesc(sb + oDOY, 128, 0, k), id3, k > 0);
-        for (int k = 0; k < MD; k += 16)
-            tc::mma(tmem + R_G5, tc::kdesc(sb + oDS, 128, 0, k), tc::kdesc(sb + oKQ, 128, 0, k), id1, k > 0);
-        tc::commit(mb);
+            tc::mma(dst, tc::kdesc(a, 128, 0, k), tc::kdesc(sb + oKQ, 128, 0, k), id1, k > 0);
+        tc::commit(mb3);
     }
 
     // ---- prologue, while B1 runs: inverse row norms of q and k (4 threads per row), the
@@ -329,8 +354,8 @@ __global__ void __launch_bounds__(512, 1) k_main_gdn(const Params p, const __gri
 #pragma unroll
     for (int i = 0; i < NCOL; ++i) dQn[i] = dKn[i] = dGc[i] = 0.f;
 
-    // ---- E1: A and P (scaled, masked, bf16), beta E in place of v, the dqd terms -------
-    if (!wait_mma()) return;
+    // ---- E1: A and P (scaled, masked, bf16), beta E in place of v ----------------------
+    if (!wait_mma(3)) return;
     {
         float v[16], cf[16];
         tc::ld16(tl(R_B + c0), v);
@@ -369,30 +394,23 @@ __global__ void __launch_bounds__(512, 1) k_main_gdn(const Params p, const __gri
             *pv = __float2bfloat16(bt[i] * (__bfloat162float(*pv) - v[i] * kf[i]));
         }
     }
-    {
-        float v[16], f[16], x[16], inv[16];
-        tc::ld16(tl(R_D + c0), v);  // dqd^T (lane = key channel)
-        rows16(sFac + F_KD * CH, f);
-        load_x(true, x, inv);
-#pragma unroll
-        for (int i = 0; i < NCOL; ++i) {
-            const float t = p.scale * v[i] * f[i];
-            dQn[i] += t;
-            dGc[i] += x[i] * inv[i] * t;
-        }
-    }
     sync_all();
 
     // ---- B2: G4 u^T = (beta E)^T T^T ; G5a du^T = dO^T P ------------------------------
-    if (tid == 0) {
+    if (lane == 0 && warp < 2) {
         constexpr uint32_t id4 = tc::idesc(128, 64, 1, 0), id5 = tc::idesc(128, 64, 1, 1);
-        for (int k = 0; k < CH; k += 16)
-            tc::mma(tmem + R_B, tc::mdesc(sb + oV, 64, 0, k), tc::kdesc(sb + oT, 64, 0, k), id4, k > 0);
-        for (int k = 0; k < CH; k += 16)
-            tc::mma(tmem + R_A, tc::mdesc(sb + oDOY, 128, 0, k), tc::mdesc(sb + oP, 64, 0, k), id5, k > 0);
-        tc::commit(mb);
+        if (warp == 0) {
+#pragma unroll
+            for (int k = 0; k < CH; k += 16)
+                tc::mma(tmem + R_B, tc::mdesc(sb + oV, 64, 0, k), tc::kdesc(sb + oT, 64, 0, k), id4, k > 0);
+        } else {
+#pragma unroll
+            for (int k = 0; k < CH; k += 16)
+                tc::mma(tmem + R_A, tc::mdesc(sb + oDOY, 128, 0, k), tc::mdesc(sb + oP, 64, 0, k), id5, k > 0);
+        }
+        tc::commit(mb2);
     }
-    if (!wait_mma()) return;
+    if (!wait_mma(2)) return;
     {
         float v[16], w[16], kf[16];
         tc::ld16(tl(R_B + c0), v);
@@ -409,11 +427,12 @@ __global__ void __launch_bounds__(512, 1) k_main_gdn(const Params p, const __gri
     // ---- B3: G6 dY^T = du^T T ; dv = beta dY, dY into the lower half of [dO; dY] ---------
     if (tid == 0) {
         constexpr uint32_t id6 = tc::idesc(128, 64, 0, 1);
+#pragma unroll
         for (int k = 0; k < CH; k += 16)
             tc::mma(tmem + R_D, tc::kdesc(sb + oDU, 128, 0, k), tc::mdesc(sb + oT, 64, 0, k), id6, k > 0);
-        tc::commit(mb);
+        tc::commit(mb1);
     }
-    if (!wait_mma()) return;
+    if (!wait_mma(1)) return;
     {
         float v[16], bt[16];
         tc::ld16(tl(R_D + c0), v);
@@ -427,17 +446,26 @@ __global__ void __launch_bounds__(512, 1) k_main_gdn(const Params p, const __gri
     }
     sync_all();
 
-    // ---- B4: G7 Z^T = S0 dY^T ; G8 dkr^T = dS u^T ; G9 [dP; dA]_raw = [dO; dY] u^T --------
-    if (tid == 0) {
-        constexpr uint32_t id7 = tc::idesc(128, 64, 1, 0), id8 = tc::idesc(128, 64, 1, 1),
-                           id9 = tc::idesc(128, 64, 0, 1);
-        for (int k = 0; k < MD; k += 16)
-            tc::mma(tmem + R_B, tc::mdesc(sb + oS0, 128, 0, k), tc::kdesc(sb + oDOY, 128, 64, k), id7, k > 0);
-        for (int k = 0; k < MD; k += 16)
-            tc::mma(tmem + R_C, tc::mdesc(sb + oDS, 128, 0, k), tc::mdesc(sb + oU, 128, 0, k), id8, k > 0);
-        for (int k = 0; k < MD; k += 16)
-            tc::mma(tmem + R_D, tc::kdesc(sb + oDOY, 128, 0, k), tc::mdesc(sb + oU, 128, 0, k), id9, k > 0);
-        tc::commit(mb);
+    // ---- B4: G3/G7 [dqd^T, Z^T] = S0 [dO; dY]^T ; G8 dkr^T = dS u^T ; G9 [dP; dA]_raw =
+    //      [dO; dY] u^T (three issuing threads)
+    if (lane == 0 && warp < 3) {
+        if (warp == 0) {
+            constexpr uint32_t id37 = tc::idesc(128, 128, 1, 0);
+#pragma unroll
+            for (int k = 0; k < MD; k += 16)
+                tc::mma(tmem + R_A, tc::mdesc(sb + oS0, 128, 0, k), tc::kdesc(sb + oDOY, 128, 0, k), id37, k > 0);
+        } else if (warp == 1) {
+            constexpr uint32_t id8 = tc::idesc(128, 64, 1, 1);
+#pragma unroll
+            for (int k = 0; k < MD; k += 16)
+                tc::mma(tmem + R_C, tc::mdesc(sb + oDS, 128, 0, k), tc::mdesc(sb + oU, 128, 0, k), id8, k > 0);
+        } else {
+            constexpr uint32_t id9 = tc::idesc(128, 64, 0, 1);
+#pragma unroll
+            for (int k = 0; k < MD; k += 16)
+                tc::mma(tmem + R_D, tc::kdesc(sb + oDOY, 128, 0, k), tc::mdesc(sb + oU, 128, 0, k), id9, k > 0);
+        }
+        tc::commit(mb3);
     }
     // while the tensor cores run: <dY, beta E> per row (token-major, 4 threads per row)
     if (tid < 4 * CH) {
@@ -457,11 +485,25 @@ __global__ void __launch_bounds__(512, 1) k_main_gdn(const Params p, const __gri
         s2 += __shfl_xor_sync(0xffffffffu, s2, 2);
         if (part == 0) sDbP[r] = s2;
     }
-    if (!wait_mma()) return;
+    if (!wait_mma(3)) return;
+    // v, dO, S0 and T are dead: the next item's copies of them start now (k, q, dS after B5)
+    if (next < n_items) {
+        if (lane == 0 && warp < 5) issue_loads(next, get_ci((it + 1) & 1), warp == 0 ? 4 : warp == 4 ? 9 : warp + 4);
+        pending = true;
+        pend_par = (uint32_t)((it + 1) & 1);
+    }
     {
         float v[16], f[16], x[16], inv[16], bt[16];
-        tc::ld16(tl(R_B + c0), v);
         rows16(sFac + F_KD * CH, f);
+        tc::ld16(tl(R_A + c0), v);  // dqd^T (lane = key channel)
+        load_x(true, x, inv);
+#pragma unroll
+        for (int i = 0; i < NCOL; ++i) {  // dqd
+            const float t = p.scale * v[i] * f[i];
+            dQn[i] += t;
+            dGc[i] += x[i] * inv[i] * t;
+        }
+        tc::ld16(tl(R_A + 64 + c0), v);  // Z^T
         load_x(false, x, inv);
         rows16(sBeta, bt);
 #pragma unroll
@@ -534,23 +576,27 @@ __global__ void __launch_bounds__(512, 1) k_main_gdn(const Params p, const __gri
     sync_all();
 
     // ---- B5: G10 [dqd', dkd']^T = k^T X10^T ; G11 dki'^T = q^T X11_P + k^T X11_A ----------
-    if (tid == 0) {
-        constexpr uint32_t id10 = tc::idesc(128, 128, 1, 0), id11 = tc::idesc(128, 64, 1, 1);
-        for (int k = 0; k < CH; k += 16)
-            tc::mma(tmem + R_A, tc::mdesc(sb + oKQ, 128, 0, k), tc::kdesc(sb + oDS, 128, 0, k), id10, k > 0);
-        for (int k = 0; k < CH; k += 16)
-            tc::mma(tmem + R_B, tc::mdesc(sb + oKQ, 128, 64, k), tc::mdesc(sb + oDS + TILE, 128, 0, k), id11, k > 0);
-        for (int k = 0; k < CH; k += 16)
-            tc::mma(tmem + R_B, tc::mdesc(sb + oKQ, 128, 0, k), tc::mdesc(sb + oDS + TILE, 128, 64, k), id11, 1);
-        tc::commit(mb);
+    if (lane == 0 && warp < 2) {
+        if (warp == 0) {
+            constexpr uint32_t id10 = tc::idesc(128, 128, 1, 0);
+#pragma unroll
+            for (int k = 0; k < CH; k += 16)
+                tc::mma(tmem + R_A, tc::mdesc(sb + oKQ, 128, 0, k), tc::kdesc(sb + oDS, 128, 0, k), id10, k > 0);
+        } else {
+            constexpr uint32_t id11 = tc::idesc(128, 64, 1, 1);
+#pragma unroll
+            for (int k = 0; k < CH; k += 16)
+                tc::mma(tmem + R_B, tc::mdesc(sb + oKQ, 128, 64, k), tc::mdesc(sb + oDS + TILE, 128, 0, k), id11, k > 0);
+#pragma unroll
+            for (int k = 0; k < CH; k += 16)
+                tc::mma(tmem + R_B, tc::mdesc(sb + oKQ, 128, 0, k), tc::mdesc(sb + oDS + TILE, 128, 64, k), id11, 1);
+        }
+        tc::commit(mb2);
     }
-    if (!wait_mma()) return;
-    // every large shared tile is dead: the next item's operands may land while this epilogue runs
-    if (item + (int)gridDim.x < n_items) {
-        if (lane == 0 && warp < 10) issue_loads(item + gridDim.x, warp);  // one copy per warp
-        pending = true;
-        prefetch_small(item + gridDim.x);
-    }
+    if (!wait_mma(2)) return;
+    // every large shared tile is dead: the rest of the next item's operands
+    if (next < n_items && lane == 0 && warp < 5)
+        issue_loads(next, get_ci((it + 1) & 1), warp == 4 ? 8 : warp);
     {
         float f[16], v[16];
         rows16(sFac + F_KDP * CH, f);

@@ -142,6 +142,7 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
     uint32_t phase = 0;
     int it = 0;              // this CTA's item count (the load barrier's phase)
     bool pending = (int)blockIdx.x < n_items;  // a load batch is in flight
+    uint32_t pend_par = 0;                     // ... on this phase parity of the load barrier
     bool pending_g = false;                    // (KDA) a raw gate tile is in flight
     // the next item's GDN gate (first warp, rows 2 lane and 2 lane + 1) and beta logit
     // (thread r < 64), loaded one item ahead
@@ -171,7 +172,7 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
     auto bail = [&]() {
         if (tid == 0) {
             atomicOr(p.status, ST_MMA_TIMEOUT);
-            if (pending) tc::mbar_wait(mload, (uint32_t)(it & 1));  // bounded drain of the loads in flight
+            if (pending) tc::mbar_wait(mload, pend_par);  // bounded drain of the loads in flight
             if (pending_g) tc::mbar_wait(mgr, (uint32_t)(it & 1));
         }
         tc::fence_before();
@@ -440,14 +441,17 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
     sync_all();
     if (tid == 0) {
         constexpr uint32_t id = tc::idesc(128, 64, 1, 1);
+#pragma unroll
         for (int k = 0; k < MD; k += 16)
             tc::mma(tmem + R_B, tc::mdesc(sb + oW0, 128, 0, k), tc::mdesc(sb + oW2, 128, 0, k), id, k > 0);
         tc::commit(mb);
         constexpr uint32_t id3 = tc::idesc(128, 64, 1, 0), id5 = tc::idesc(128, 64, 0, 1);
+#pragma unroll
         for (int k = 0; k < MD; k += 16)
             tc::mma(tmem + R_D, tc::mdesc(sb + oS0, 128, 0, k), tc::kdesc(sb + oDOY, 128, 0, k), id3, k > 0);
         // second half of G5 (independent of beta E): du^T = dS^T kr^T (+ dO^T P later); the
         // next commit (after G2) covers these two groups
+#pragma unroll
         for (int k = 0; k < MD; k += 16)
             tc::mma(tmem + R_A, tc::kdesc(sb + oDS, 128, 0, k), tc::mdesc(sb + oK, 128, 0, k), id5, k > 0);
     }
@@ -483,6 +487,7 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
     // ---- G2: X^T = S0^T kd^T (its commit also covers G3 and G5b) ---------------------------
     if (tid == 0) {
         constexpr uint32_t id2 = tc::idesc(128, 64, 0, 1);
+#pragma unroll
         for (int k = 0; k < MD; k += 16)
             tc::mma(tmem + R_C, tc::kdesc(sb + oS0, 128, 0, k), tc::mdesc(sb + oW0, 128, 0, k), id2, k > 0);
         tc::commit(mb);
@@ -518,11 +523,14 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
     // ---- G4: u^T = (beta E)^T T^T ; G5a: du^T += dO^T P ------------------------------
     if (tid == 0) {
         constexpr uint32_t id4 = tc::idesc(128, 64, 1, 0), id5 = tc::idesc(128, 64, 1, 1);
+#pragma unroll
         for (int k = 0; k < CH; k += 16)
             tc::mma(tmem + R_B, tc::mdesc(sb + oV, 64, 0, k), tc::kdesc(sb + oT, 64, 0, k), id4, k > 0);
         if (KDA)
+#pragma unroll
             for (int k = 0; k < CH; k += 16)
                 tc::mma(tmem + R_B, tc::mdesc(sb + oK, 64, 0, k), tc::kdesc(sb + oT, 64, 0, k), id4, 1);
+#pragma unroll
         for (int k = 0; k < CH; k += 16)
             tc::mma(tmem + R_A, tc::mdesc(sb + oDOY, 128, 0, k), tc::mdesc(sb + oP, 64, 0, k), id5, 1);
         tc::commit(mb);
@@ -540,6 +548,7 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
     // ---- G6: dY^T = du^T T ------------------------------------------------------------
     if (tid == 0) {
         constexpr uint32_t id6 = tc::idesc(128, 64, 0, 1);
+#pragma unroll
         for (int k = 0; k < CH; k += 16)
             tc::mma(tmem + R_D, tc::kdesc(sb + oW2, 128, 0, k), tc::mdesc(sb + oT, 64, 0, k), id6, k > 0);
         tc::commit(mb);
@@ -562,15 +571,20 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
     if (tid == 0) {
         constexpr uint32_t id7 = tc::idesc(128, 64, 1, 0), id8 = tc::idesc(128, 64, 1, 1),
                            id9 = tc::idesc(128, 64, 0, 1);
+#pragma unroll
         for (int k = 0; k < MD; k += 16)
             tc::mma(tmem + R_B, tc::mdesc(sb + oS0, 128, 0, k), tc::kdesc(sb + oDOY, 128, 64, k), id7, k > 0);
+#pragma unroll
         for (int k = 0; k < MD; k += 16)
             tc::mma(tmem + R_C, tc::mdesc(sb + oDS, 128, 0, k), tc::mdesc(sb + oW1, 128, 0, k), id8, k > 0);
+#pragma unroll
         for (int k = 0; k < MD; k += 16)
             tc::mma(tmem + R_D, tc::kdesc(sb + oDOY, 128, 0, k), tc::mdesc(sb + oW1, 128, 0, k), id9, k > 0);
         if (KDA) {  // u lo
+#pragma unroll
             for (int k = 0; k < MD; k += 16)
                 tc::mma(tmem + R_C, tc::mdesc(sb + oDS, 128, 0, k), tc::mdesc(sb + oW0, 128, 0, k), id8, 1);
+#pragma unroll
             for (int k = 0; k < MD; k += 16)
                 tc::mma(tmem + R_D, tc::kdesc(sb + oDOY, 128, 0, k), tc::mdesc(sb + oW0, 128, 0, k), id9, 1);
         }
@@ -691,19 +705,25 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
         constexpr uint32_t id10 = tc::idesc(128, 128, 0, 0), id11 = tc::idesc(128, 64, 0, 1);
         const uint32_t kiH = sb + oW0, kiL = sb + oW1, qdH = sb + oW2, qdL = sb + oK, kdH = sb + oS0,
                        kdL = sb + oS0 + TILE, xH = sb + oDS, xL = sb + oDS + TILE;
+#pragma unroll
         for (int k = 0; k < CH; k += 16)
             tc::mma(tmem + R_A, tc::kdesc(kiH, 128, 0, k), tc::kdesc(xH, 128, 0, k), id10, k > 0);
         if (KDA) {
+#pragma unroll
             for (int k = 0; k < CH; k += 16)
                 tc::mma(tmem + R_A, tc::kdesc(kiH, 128, 0, k), tc::kdesc(xL, 128, 0, k), id10, 1);
+#pragma unroll
             for (int k = 0; k < CH; k += 16)
                 tc::mma(tmem + R_A, tc::kdesc(kiL, 128, 0, k), tc::kdesc(xH, 128, 0, k), id10, 1);
         }
+#pragma unroll
         for (int k = 0; k < CH; k += 16)
             tc::mma(tmem + R_B, tc::kdesc(qdH, 128, 0, k), tc::mdesc(xH, 128, 0, k), id11, k > 0);
+#pragma unroll
         for (int k = 0; k < CH; k += 16)
             tc::mma(tmem + R_B, tc::kdesc(kdH, 128, 0, k), tc::mdesc(xH, 128, 64, k), id11, 1);
         if (KDA) {
+#pragma unroll
             for (int k = 0; k < CH; k += 16) {
                 tc::mma(tmem + R_B, tc::kdesc(qdH, 128, 0, k), tc::mdesc(xL, 128, 0, k), id11, 1);
                 tc::mma(tmem + R_B, tc::kdesc(qdL, 128, 0, k), tc::mdesc(xH, 128, 0, k), id11, 1);
@@ -718,6 +738,7 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
     if (item + (int)gridDim.x < n_items) {
         if (lane == 0 && warp < 9) issue_loads(item + gridDim.x, warp);  // one copy per warp
         pending = true;
+        pend_par = (uint32_t)((it + 1) & 1);
         prefetch_small(item + gridDim.x);
     }
     // the gate-gradient term takes the derived-tile value the products consumed: the bf16

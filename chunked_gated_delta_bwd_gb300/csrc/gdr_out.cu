@@ -73,8 +73,10 @@ __global__ void __launch_bounds__(128) k_out_tc(const Params p, const __grid_con
         if (tid == 0) {
             tc::fence_after();
             constexpr uint32_t id_r = tc::idesc(128, 64, 0, 1), id_p = tc::idesc(128, 64, 0, 0);
+#pragma unroll
             for (int k = 0; k < OD; k += 16)  // o^T = S0^T R^T
                 tc::mma(tmem, tc::kdesc(sb + oS0, OD, 0, k), tc::mdesc(sb + oR, OD, 0, k), id_r, k > 0);
+#pragma unroll
             for (int k = 0; k < CH; k += 16)  // + U^T P^T
                 tc::mma(tmem, tc::kdesc(sb + oU, OD, 0, k), tc::kdesc(sb + oP, CH, 0, k), id_p, 1);
             tc::commit(mb);

@@ -534,6 +534,7 @@ __global__ void __launch_bounds__(512, 1) k_prep_tc(const Params p, const __grid
     sync_all();
     if (tid == 0) {
         constexpr uint32_t id = tc::idesc(128, 64, 1, 1);
+#pragma unroll
         for (int k = 0; k < PD; k += 16)
             tc::mma(tmem + R_G1, tc::mdesc(sb + oW0, 128, 0, k), tc::mdesc(sb + oW2, 128, 0, k), id, k > 0);
         tc::commit(mb);
@@ -608,8 +609,10 @@ __global__ void __launch_bounds__(512, 1) k_prep_tc(const Params p, const __grid
     // ---- W^T = (beta kd)^T T^T ; U^T = (beta V)^T T^T --------------------------------------
     if (tid == 0) {
         constexpr uint32_t id = tc::idesc(128, 64, 0, 0);
+#pragma unroll
         for (int k = 0; k < CH; k += 16)
             tc::mma(tmem + R_W, tc::kdesc(sQa, 128, 0, k), tc::kdesc(sb + oT, 64, 0, k), id, k > 0);
+#pragma unroll
         for (int k = 0; k < CH; k += 16)
             tc::mma(tmem + R_U, tc::kdesc(sKa, 128, 0, k), tc::kdesc(sb + oT, 64, 0, k), id, k > 0);
         tc::commit(mb);
@@ -631,6 +634,7 @@ __global__ void __launch_bounds__(512, 1) k_prep_tc(const Params p, const __grid
     // ---- R^T = qd^T - W^T P^T ----------------------------------------------------------------
     if (tid == 0) {
         constexpr uint32_t id = tc::idesc(128, 64, 0, 0);
+#pragma unroll
         for (int k = 0; k < CH; k += 16)
             tc::mma(tmem + R_R, tc::kdesc(sb + oW2, 128, 0, k), tc::kdesc(sb + oP, 64, 0, k), id, k > 0);
         tc::commit(mb);

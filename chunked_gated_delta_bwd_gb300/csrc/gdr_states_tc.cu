@@ -249,6 +249,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_states_tc(const Params p, int p
         constexpr uint32_t idr = tc::idesc(128, 128, 1, 0);
         auto r_part = [&](int j, int tile, uint32_t acc) {
             const uint32_t stj = sb + (j & 1) * STAGE, zj = tmem + ((j & 1) ? R_Z1 : R_Z0);
+#pragma unroll
             for (int k = 0; k < CH; k += 16)
                 tc::mma(zj, tc::mdesc(stj + 4 * TILE, CH, 0, k), tc::kdesc(stj + tile * TILE, SD, 0, k), idr,
                         acc || k > 0);
@@ -267,6 +268,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_states_tc(const Params p, int p
                 if (!failed()) {
                     // X^T = S^T W^T (role 0) or Y^T = dS^T kr^T (role 1): B = the stage's first tile
                     constexpr uint32_t idy = tc::idesc(128, 64, 0, 1);
+#pragma unroll
                     for (int k = 0; k < SD; k += 16)
                         tc::mma(tmem + R_Y, tc::kdesc(sb + oBS, SD, 0, k), tc::mdesc(st, SD, 0, k), idy, k > 0);
                     tc::commit(mby);
@@ -279,6 +281,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_states_tc(const Params p, int p
             if (lane == 0 && !failed()) {
                 // role 0: Z = (U - X)^T kr ; role 1: Z += (-Y^T) W   (B = the stage's second tile)
                 constexpr uint32_t idz = tc::idesc(128, 128, 0, 0);
+#pragma unroll
                 for (int k = 0; k < CH; k += 16)
                     tc::mma(z, tc::kdesc(sb + oBY, SD, 0, k), tc::kdesc(st + TILE, SD, 0, k), idz, role == 1 || k > 0);
                 tc::commit(mbz);

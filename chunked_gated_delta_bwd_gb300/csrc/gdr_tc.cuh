@@ -31,12 +31,15 @@ __device__ __forceinline__ uint64_t desc(uint32_t saddr, uint32_t lbo, uint32_t 
 }
 
 // K-major operand: rows row0.. of a tile with `rows` rows, K step k (multiple of 16)
+// (the descriptor of the tile base plus the step's offset in 16-byte units: the base part
+// is loop-invariant and the offset a constant in unrolled K loops; exact because both are
+// multiples of 16 bytes and shared addresses stay below 2^18)
 __device__ __forceinline__ uint64_t kdesc(uint32_t base, int rows, int row0, int k) {
-    return desc(base + (k >> 6) * rows * 128 + row0 * 128 + (k & 63) * 2, 16, 1024);
+    return desc(base, 16, 1024) + (uint64_t)((uint32_t)((k >> 6) * rows * 128 + row0 * 128 + (k & 63) * 2) >> 4);
 }
 // MN-major operand: K rows start at row0 (rows of the tile are K), MN in 64-wide column blocks
 __device__ __forceinline__ uint64_t mdesc(uint32_t base, int rows, int row0, int k) {
-    return desc(base + (row0 + k) * 128, rows * 128, 1024);
+    return desc(base, rows * 128, 1024) + (uint64_t)((uint32_t)((row0 + k) * 128) >> 4);
 }
 
 // kind::f16 instruction descriptor: bf16 A and B, fp32 D, M x N, major-ness of A and B
