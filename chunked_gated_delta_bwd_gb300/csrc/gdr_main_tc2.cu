@@ -146,17 +146,19 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
     bool pending_g = false;                    // (KDA) a raw gate tile is in flight
     // the next item's GDN gate (first warp, rows 2 lane and 2 lane + 1) and beta logit
     // (thread r < 64), loaded one item ahead
-    float pg0 = 0.f, pg1 = 0.f, pb = 0.f;
+    // (raw values, rows clamped into the chunk, first read at the next item's top, so no
+    // thread waits for them)
+    float pg0 = 0.f, pg1 = 0.f;
+    unsigned short pb = 0;
     auto prefetch_small = [&](int item) {
         if (tid >= CH) return;
         ChunkInfo cj;
         lookup_chunk(item / p.H, p.N, p.chunk_off, p.cu_seqlens, p.seq_len, cj);
         const int hh = item % p.H;
-        pb = tid < cj.len ? bf2f(p.beta_logit[(cj.t0 + tid) * p.H + hh]) : 0.f;
+        pb = reinterpret_cast<const unsigned short*>(p.beta_logit)[(cj.t0 + min(tid, cj.len - 1)) * p.H + hh];
         if (!KDA && tid < 32) {
-            const int r0 = 2 * tid;
-            pg0 = r0 < cj.len ? p.g[(cj.t0 + r0) * p.H + hh] : 0.f;
-            pg1 = r0 + 1 < cj.len ? p.g[(cj.t0 + r0 + 1) * p.H + hh] : 0.f;
+            pg0 = p.g[(cj.t0 + min(2 * tid, cj.len - 1)) * p.H + hh];
+            pg1 = p.g[(cj.t0 + min(2 * tid + 1, cj.len - 1)) * p.H + hh];
         }
     };
     if ((int)blockIdx.x < n_items) prefetch_small(blockIdx.x);
@@ -228,8 +230,8 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
     ChunkInfo ci;
     lookup_chunk(chunk, p.N, p.chunk_off, p.cu_seqlens, p.seq_len, ci);
     if constexpr (!KDA)
-        if (tid < 32) gdn_gate_scan(pg0, pg1, G, false, p);
-    if (tid < CH) sBeta[tid] = tid < ci.len ? sigmoid_f(pb) : 0.f;
+        if (tid < 32) gdn_gate_scan(2 * tid < ci.len ? pg0 : 0.f, 2 * tid + 1 < ci.len ? pg1 : 0.f, G, false, p);
+    if (tid < CH) sBeta[tid] = tid < ci.len ? sigmoid_f(__bfloat162float(__ushort_as_bfloat16(pb))) : 0.f;
     // KDA gate parameters, read while the operand tiles land
     float alog = 0.f, bias = 0.f;
     if constexpr (KDA) {

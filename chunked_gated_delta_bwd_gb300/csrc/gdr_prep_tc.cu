@@ -311,16 +311,19 @@ __global__ void __launch_bounds__(512, 1) k_prep_tc(const Params p, const __grid
     };
     // the next item's beta logit (thread r < 64), GDN gates (first warp, rows 2 lane and
     // 2 lane + 1) and KDA gate parameters (every thread: its channel), read one item ahead
-    float pb = 0.f, pg0 = 0.f, pg1 = 0.f, pbias = 0.f, palog = 0.f;
+    // as raw values (rows clamped into the chunk) that are first read at the next item's
+    // top, so no thread waits for them
+    float pg0 = 0.f, pg1 = 0.f, pbias = 0.f, palog = 0.f;
+    unsigned short pb = 0;
     auto prefetch_small = [&](int item) {
         ChunkInfo cj;
         lookup_chunk(item / p.H, p.N, p.chunk_off, p.cu_seqlens, p.seq_len, cj);
         const int hh = item % p.H;
-        if (tid < CH) pb = tid < cj.len ? bf2f(p.beta_logit[(cj.t0 + tid) * p.H + hh]) : 0.f;
+        if (tid < CH)
+            pb = reinterpret_cast<const unsigned short*>(p.beta_logit)[(cj.t0 + min(tid, cj.len - 1)) * p.H + hh];
         if (!KDA && tid < 32) {
-            const int r0 = 2 * tid;
-            pg0 = r0 < cj.len ? p.g[(cj.t0 + r0) * p.H + hh] : 0.f;
-            pg1 = r0 + 1 < cj.len ? p.g[(cj.t0 + r0 + 1) * p.H + hh] : 0.f;
+            pg0 = p.g[(cj.t0 + min(2 * tid, cj.len - 1)) * p.H + hh];
+            pg1 = p.g[(cj.t0 + min(2 * tid + 1, cj.len - 1)) * p.H + hh];
         }
         if (KDA) {
             pbias = p.dt_bias[hh * PD + L];
@@ -373,8 +376,8 @@ __global__ void __launch_bounds__(512, 1) k_prep_tc(const Params p, const __grid
         pending_par = (uint32_t)(((it + 1) >> 1) & 1);
     }
     if constexpr (!KDA)
-        if (tid < 32) gdn_gate_scan(pg0, pg1, G, true, p);
-    if (tid < CH) sBeta[tid] = tid < ci.len ? sigmoid_f(pb) : 0.f;
+        if (tid < 32) gdn_gate_scan(2 * tid < ci.len ? pg0 : 0.f, 2 * tid + 1 < ci.len ? pg1 : 0.f, G, true, p);
+    if (tid < CH) sBeta[tid] = tid < ci.len ? sigmoid_f(__bfloat162float(__ushort_as_bfloat16(pb))) : 0.f;
 
     // KDA: per-channel log gates of this thread's channel and rows (raw gates from the
     // token-major tile in the space of A), scanned across the four row quarters, staged in
