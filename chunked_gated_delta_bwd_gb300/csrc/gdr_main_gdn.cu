@@ -16,6 +16,9 @@
 // A tcgen05.mma takes tens of cycles to issue whatever its size, so the groups of a batch
 // are issued by lane 0 of different warps (one per SM sub-partition), each committing to
 // the batch's barrier, and G3 waits for dY to run as one N = 128 product with G7.
+// dv, dq and dk of a full chunk are staged token-major in shared tiles that are dead by
+// then (du^T, u^T, A and P) and written by TMA stores; a chunk cut by its sequence's end
+// writes its rows one element at a time.
 // with X10 = [dP; beta dA] scaled by the column factor invk_s e^{ref-gc_s} (ki' folded
 // in) and X11 = [dP; beta dA] scaled by the row factors of qd' and kd'.  B1 needs no
 // per-item preparation, so it is issued as soon as the tiles land and runs under the
@@ -63,8 +66,9 @@ constexpr uint32_t R_A = 0, R_B = 128, R_C = 192, R_D = 256, R_Q = 320, R_K = 38
 enum Tab { T_CF = 0, T_KDF = 1, T_KRF = 2, T_RA = 3, T_RP = 4, T_RK = 5 };
 
 struct GdnMaps {
-    CUtensorMap q, k, v, dO, S0, dS, T;
+    CUtensorMap q, k, v, dO, S0, dS, T, dq, dk, dv;
 };
+constexpr int STORE_TID = 96;  // the thread that issues the TMA stores of dq, dk and dv
 
 }  // namespace
 
@@ -193,6 +197,7 @@ __global__ void __launch_bounds__(512, 1) k_main_gdn(const Params p, const __gri
             atomicOr(p.status, ST_MMA_TIMEOUT);
             if (pending) tc::mbar_wait(mload, pend_par);
         }
+        if (tid == STORE_TID) tc::bulk_wait_all();
         tc::fence_before();
         __syncthreads();
         if (warp == 0) tc::dealloc(tmem, 512);
@@ -355,6 +360,7 @@ __global__ void __launch_bounds__(512, 1) k_main_gdn(const Params p, const __gri
     for (int i = 0; i < NCOL; ++i) dQn[i] = dKn[i] = dGc[i] = 0.f;
 
     // ---- E1: A and P (scaled, masked, bf16), beta E in place of v ----------------------
+    if (tid == STORE_TID) tc::bulk_wait_read();  // the last item's dq / dk / dv tiles were read
     if (!wait_mma(3)) return;
     {
         float v[16], cf[16];
@@ -433,18 +439,26 @@ __global__ void __launch_bounds__(512, 1) k_main_gdn(const Params p, const __gri
         tc::commit(mb1);
     }
     if (!wait_mma(1)) return;
+    const bool full = ci.len == CH;
     {
         float v[16], bt[16];
         tc::ld16(tl(R_D + c0), v);
         rows16(sBeta, bt);
 #pragma unroll
         for (int i = 0; i < NCOL; ++i) {
-            const int r = c0 + i;
-            if (r < ci.len) p.dv[((ci.t0 + r) * p.H + h) * MD + L] = __float2bfloat16(bt[i] * v[i]);
+            const __nv_bfloat16 dv = __float2bfloat16(bt[i] * v[i]);
+            if (full)  // dv staged token-major in the dead du^T tile
+                *reinterpret_cast<__nv_bfloat16*>(sDU + tok(64, i)) = dv;
+            else if (c0 + i < ci.len)
+                p.dv[((ci.t0 + c0 + i) * p.H + h) * MD + L] = dv;
             *reinterpret_cast<__nv_bfloat16*>(sDOY + tok(128, i) + 64 * 128) = __float2bfloat16(v[i]);  // dY
         }
     }
     sync_all();
+    if (full && tid == STORE_TID) {
+        tc::tma_store_4d(&m.dv, 0, h, (int)ci.t0, 0, sb + oDU);
+        tc::bulk_commit();
+    }
 
     // ---- B4: G3/G7 [dqd^T, Z^T] = S0 [dO; dY]^T ; G8 dkr^T = dS u^T ; G9 [dP; dA]_raw =
     //      [dO; dY] u^T (three issuing threads)
@@ -640,24 +654,31 @@ __global__ void __launch_bounds__(512, 1) k_main_gdn(const Params p, const __gri
     }
     __syncthreads();
     {
+        // dq into the dead u^T tile, dk into the dead A and P tiles (one 16 KB token-major
+        // tile), or row by row for a chunk cut by its sequence's end
         float x[16], inv[16], tt[16];
         load_x(true, x, inv);
         rows16(sTot, tt);
 #pragma unroll
         for (int i = 0; i < NCOL; ++i) {
-            const int r = c0 + i;
-            if (r < ci.len)
-                p.dq[((ci.t0 + r) * p.H + h) * MD + L] = __float2bfloat16((dQn[i] - x[i] * inv[i] * tt[i]) * inv[i]);
+            const __nv_bfloat16 d = __float2bfloat16((dQn[i] - x[i] * inv[i] * tt[i]) * inv[i]);
+            if (full)
+                *reinterpret_cast<__nv_bfloat16*>(sU + tok(64, i)) = d;
+            else if (c0 + i < ci.len)
+                p.dq[((ci.t0 + c0 + i) * p.H + h) * MD + L] = d;
         }
         load_x(false, x, inv);
         rows16(sTot + CH, tt);
 #pragma unroll
         for (int i = 0; i < NCOL; ++i) {
-            const int r = c0 + i;
-            if (r < ci.len)
-                p.dk[((ci.t0 + r) * p.H + h) * MD + L] = __float2bfloat16((dKn[i] - x[i] * inv[i] * tt[i]) * inv[i]);
+            const __nv_bfloat16 d = __float2bfloat16((dKn[i] - x[i] * inv[i] * tt[i]) * inv[i]);
+            if (full)
+                *reinterpret_cast<__nv_bfloat16*>(sA + tok(64, i)) = d;
+            else if (c0 + i < ci.len)
+                p.dk[((ci.t0 + c0 + i) * p.H + h) * MD + L] = d;
         }
     }
+    tc::fence_async_smem();  // the staged dq / dk reach the copy engine after the next barrier
     // dbeta (logit space): <dY, beta E> + rowsum(dA . A)
     for (int r = tid; r < ci.len; r += 512) {
         const float dA_A = ((sPairR[CH + r] + sPairR[128 + CH + r]) + sPairR[256 + CH + r]) + sPairR[384 + CH + r];
@@ -693,7 +714,13 @@ __global__ void __launch_bounds__(512, 1) k_main_gdn(const Params p, const __gri
     tc::fence_before();
     __syncthreads();  // this item's small arrays and tensor memory are free
     tc::fence_after();
+    if (full && tid == STORE_TID) {
+        tc::tma_store_4d(&m.dq, 0, h, (int)ci.t0, 0, sb + oU);
+        tc::tma_store_4d(&m.dk, 0, h, (int)ci.t0, 0, sb + oA);
+        tc::bulk_commit();
     }
+    }
+    if (tid == STORE_TID) tc::bulk_wait_all();
     tc::fence_before();
     __syncthreads();
     if (warp == 0) tc::dealloc(tmem, 512);
@@ -707,7 +734,8 @@ cudaError_t launch_main_gdn(const Params& p, cudaStream_t s) {
     bool ok = encode_tokens_map(&m.q, p.q, T, p.Hk, MD) && encode_tokens_map(&m.k, p.k, T, p.Hk, MD) &&
               encode_blocked_tokens_map(&m.v, p.v, T, p.H) && encode_tokens_map(&m.dO, p.dO, T, p.H, MD) &&
               encode_blocked_rows_map(&m.S0, p.S0, rows_dd, MD) && encode_blocked_rows_map(&m.dS, p.dS, rows_dd, MD) &&
-              encode_rows_map(&m.T, p.Tm, rows_cc, CH, CH);
+              encode_rows_map(&m.T, p.Tm, rows_cc, CH, CH) && encode_blocked_tokens_map(&m.dq, p.dq, T, p.H) &&
+              encode_blocked_tokens_map(&m.dk, p.dk, T, p.H) && encode_blocked_tokens_map(&m.dv, p.dv, T, p.H);
     if (!ok) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(k_main_gdn, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;

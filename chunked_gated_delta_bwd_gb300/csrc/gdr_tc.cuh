@@ -180,6 +180,12 @@ __device__ __forceinline__ void tma_store_2d(const void* map, int x, int y, uint
                  "r"(x), "r"(y), "r"(src)
                  : "memory");
 }
+__device__ __forceinline__ void tma_store_4d(const void* map, int x, int y, int z, int w, uint32_t src) {
+    asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3, %4}], [%5];\n" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(z), "r"(w), "r"(src)
+                 : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
 // the source shared memory of every committed store may be reused
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory"); }
