@@ -23,7 +23,8 @@
 // tf32 tensor-core instructions (m16n8k8) in a three-term split (hi hi + hi lo + lo hi of
 // a = hi + lo), which keeps fp32 accuracy.  The shapes are too small for tcgen05 (M >= 64).
 // The next item's gates and beta logits are read one item ahead (KDA: the raw-gate tile
-// by TMA into the space of the dead fp32 matrices).
+// by TMA into the space of the dead fp32 matrices).  W, U, Kr, R_hi and R_lo are staged in
+// shared tiles that are dead by then and written by TMA stores.
 #include "gdr_chunk.cuh"
 #include "gdr_tc.cuh"
 #include "gdr_tma.h"
@@ -61,8 +62,12 @@ static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 constexpr uint32_t R_G1 = 0, R_W = 64, R_U = 128, R_R = 192, R_Q = 256, R_K = 320, R_G = 384;
 
 struct PrepMaps {
-    CUtensorMap q, k, v, graw;
+    CUtensorMap q, k, v, graw, W, U, Kr, R, Rlo;
 };
+// The thread that issues the TMA stores of W, U, Kr, R_hi and R_lo and the copies of the
+// next item's q, k and v: its stores read the stage that those copies overwrite, and a
+// bulk store's completion is visible only to the thread that issued it.
+constexpr int STORE_TID = 416;
 
 // tf32 split of an fp32 value: hi keeps the top 10 mantissa bits, lo the rest (the tensor
 // cores read the top 19 bits of each operand register)
@@ -295,6 +300,7 @@ __global__ void __launch_bounds__(512, 1) k_prep_tc(const Params p, const __grid
             if (pending >= 0) tc::mbar_wait(mload0 + 8 * pending, pending_par);  // bounded drain
             if (pending_g) tc::mbar_wait(mgr, (uint32_t)(it & 1));
         }
+        if (tid == STORE_TID) tc::bulk_wait_all();
         tc::fence_before();
         __syncthreads();
         if (warp == 0) tc::dealloc(tmem, 512);
@@ -351,12 +357,6 @@ __global__ void __launch_bounds__(512, 1) k_prep_tc(const Params p, const __grid
         *reinterpret_cast<uint4*>(tile + tc::sw_chunk(L, cq >> 3, 128)) = make_uint4(w[0], w[1], w[2], w[3]);
         *reinterpret_cast<uint4*>(tile + tc::sw_chunk(L, (cq >> 3) + 1, 128)) = make_uint4(w[4], w[5], w[6], w[7]);
     };
-    // row L, columns c0 .. c0+15 of a chunk-head's channel-major [128][64] global tile
-    auto store_global_cm = [&](__nv_bfloat16* tile, const uint32_t (&w)[8]) {
-        uint4* g = reinterpret_cast<uint4*>(tile + (size_t)L * CH + c0);
-        g[0] = make_uint4(w[0], w[1], w[2], w[3]);
-        g[1] = make_uint4(w[4], w[5], w[6], w[7]);
-    };
 
     for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++it) {
     const int chunk = item / p.H, h = item % p.H;
@@ -365,13 +365,15 @@ __global__ void __launch_bounds__(512, 1) k_prep_tc(const Params p, const __grid
     const int stg = it & 1;
     unsigned char *sQ = smem + stg * STAGE + oQ, *sK = smem + stg * STAGE + oK, *sV = smem + stg * STAGE + oV;
     const uint32_t sQa = sb + stg * STAGE + oQ, sKa = sb + stg * STAGE + oK;
-    const size_t tile_cd = ((size_t)chunk * p.H + h) * CH * PD;
     const size_t tile_cc = ((size_t)chunk * p.H + h) * CH * CH;
     const bool has_next = item + (int)gridDim.x < n_items;
     // the next item's tiles into the other stage (its previous tenant finished last iteration)
     pending = -1;
     if (has_next) {
-        if (lane == 0 && warp >= 13) issue_loads(item + gridDim.x, stg ^ 1, warp - 13);  // one copy per warp
+        if (tid == STORE_TID) {  // the last item's stores have read the stage these copies fill
+            tc::bulk_wait_read();
+            issue_loads(item + gridDim.x, stg ^ 1, -1);
+        }
         pending = stg ^ 1;
         pending_par = (uint32_t)(((it + 1) >> 1) & 1);
     }
@@ -621,18 +623,23 @@ __global__ void __launch_bounds__(512, 1) k_prep_tc(const Params p, const __grid
         tc::commit(mb);
     }
     if (!wait_mma()) return;
+    const int trow = (chunk * p.H + h) * PD;  // the chunk-head's first row in the [D][C] tile maps
     {
         float v[16];
         uint32_t w[8];
         tc::ld16(tl(R_W + c0), v);
         pack8(v, w);
-        store_global_cm(p.W + tile_cd, w);
-        store_cm(sW2, w, c0);  // bf16 W^T, the A operand of W^T P^T (ki' is dead)
+        store_cm(sW2, w, c0);  // bf16 W^T, the A operand of W^T P^T (ki' is dead) and W's store
         tc::ld16(tl(R_U + c0), v);
         pack8(v, w);
-        store_global_cm(p.U + tile_cd, w);
+        store_cm(sK, w, c0);  // U^T over the dead (beta V)^T
     }
     sync_all();
+    if (tid == STORE_TID) {
+        tc::tma_store_2d(&m.W, 0, trow, sb + oW2);
+        tc::tma_store_2d(&m.U, 0, trow, sKa);
+        tc::bulk_commit();
+    }
 
     // ---- R^T = qd^T - W^T P^T ----------------------------------------------------------------
     if (tid == 0) {
@@ -642,13 +649,14 @@ __global__ void __launch_bounds__(512, 1) k_prep_tc(const Params p, const __grid
             tc::mma(tmem + R_R, tc::kdesc(sb + oW2, 128, 0, k), tc::kdesc(sb + oP, 64, 0, k), id, k > 0);
         tc::commit(mb);
     }
-    // while the tensor cores run: kr = kn e^{gT-gc} ; gT, e^{gT}
+    // while the tensor cores run: kr = kn e^{gT-gc} (over the dead v tile) ; gT, e^{gT}
     {
         float v[16];
         uint32_t w[8];
         derived(false, 1.f, nullptr, F_KR, v, c0);
         pack8(v, w);
-        store_global_cm(p.Kr + tile_cd, w);
+        store_cm(sV, w, c0);
+        tc::fence_async_smem();
         if (hc == 0) {
             const float gt = KDA ? gTL : G.gTv(0);
             p.gT[((size_t)chunk * p.H + h) * PD + L] = gt;
@@ -656,6 +664,10 @@ __global__ void __launch_bounds__(512, 1) k_prep_tc(const Params p, const __grid
         }
     }
     if (!wait_mma()) return;
+    if (tid == STORE_TID) {
+        tc::tma_store_2d(&m.Kr, 0, trow, sb + stg * STAGE + oV);
+        tc::bulk_commit();
+    }
     {
         float acc[16], qd[16];
         uint32_t w[8], wl[8];
@@ -668,13 +680,20 @@ __global__ void __launch_bounds__(512, 1) k_prep_tc(const Params p, const __grid
             const float2 hf = unpack_bf16(w[e]);
             wl[e] = pack_bf16(r0 - hf.x, r1 - hf.y);
         }
-        store_global_cm(p.R + tile_cd, w);
-        store_global_cm(p.Rlo + tile_cd, wl);
+        store_cm(sQ, w, c0);   // R_hi over the dead (beta kd)^T
+        store_cm(sW0, wl, c0);  // R_lo over the dead kd'^T
+        tc::fence_async_smem();
     }
     tc::fence_before();
     __syncthreads();  // this item's shared tiles and tensor memory are free
     tc::fence_after();
+    if (tid == STORE_TID) {
+        tc::tma_store_2d(&m.R, 0, trow, sQa);
+        tc::tma_store_2d(&m.Rlo, 0, trow, sb + oW0);
+        tc::bulk_commit();
     }
+    }
+    if (tid == STORE_TID) tc::bulk_wait_all();
     tc::fence_before();
     __syncthreads();
     if (warp == 0) tc::dealloc(tmem, 512);
@@ -684,9 +703,13 @@ template <bool KDA, int GATE>
 static cudaError_t launch_prep_tc_t(const Params& p, cudaStream_t s) {
     PrepMaps m;
     const uint64_t T = (uint64_t)p.T_total;
+    const uint64_t trows = (uint64_t)p.max_chunks * p.H * PD;  // rows of the [D][C] per chunk-head tiles
     if (!(encode_blocked_tokens_map(&m.q, p.q, T, p.Hk) && encode_blocked_tokens_map(&m.k, p.k, T, p.Hk) &&
           encode_blocked_tokens_map(&m.v, p.v, T, p.H) &&
-          encode_blocked_tokens_map(&m.graw, KDA ? p.g_raw : nullptr, T, p.H)))
+          encode_blocked_tokens_map(&m.graw, KDA ? p.g_raw : nullptr, T, p.H) &&
+          encode_rows_map(&m.W, p.W, trows, CH, PD) && encode_rows_map(&m.U, p.U, trows, CH, PD) &&
+          encode_rows_map(&m.Kr, p.Kr, trows, CH, PD) && encode_rows_map(&m.R, p.R, trows, CH, PD) &&
+          encode_rows_map(&m.Rlo, p.Rlo, trows, CH, PD)))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(k_prep_tc<KDA, GATE>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
