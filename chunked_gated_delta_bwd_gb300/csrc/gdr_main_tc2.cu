@@ -20,6 +20,10 @@
 //   G6  dY^T         = du^T T
 // followed by the elementwise assembly of "FlashKDA之backward（K1）" (§3.2-§3.3, §5).
 //
+// dv, dq, dk and dg_raw are staged token-major in shared tiles that are dead by then
+// (du^T, ki' lo, the dY rows of [dO; dY], the raw-gate tile) and written by TMA stores; a
+// chunk cut by its sequence's end copies its valid rows from the staged tile instead.
+//
 // KDA runs the precise mode of the warp-level kernel: the operands that carry the
 // per-channel gate gradient (beta E, u, dP and beta dA, and ki', qd', kd' of G10 / G11)
 // are bf16 pairs hi + lo and each of those products is hi*hi + lo*hi + hi*lo, because
@@ -59,8 +63,9 @@ constexpr int SMEM_BYTES = oSmall + SMALL_FLOATS * 4 + 64 + 1024;  // + mbarrier
 constexpr uint32_t R_A = 0, R_B = 128, R_C = 192, R_D = 256, R_Q = 320, R_K = 384, R_G = 448;
 
 struct MainMaps {
-    CUtensorMap q, k, v, dO, S0, dS, T, graw;
+    CUtensorMap q, k, v, dO, S0, dS, T, graw, dq, dk, dv, dgr;
 };
+constexpr int STORE_TID = 96;  // the thread that issues the TMA stores of dq, dk, dv and dg_raw
 
 }  // namespace
 
@@ -177,6 +182,7 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
             if (pending) tc::mbar_wait(mload, pend_par);  // bounded drain of the loads in flight
             if (pending_g) tc::mbar_wait(mgr, (uint32_t)(it & 1));
         }
+        if (tid == STORE_TID) tc::bulk_wait_all();
         tc::fence_before();
         __syncthreads();
         if (warp == 0) tc::dealloc(tmem, 512);
@@ -223,6 +229,31 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
         *reinterpret_cast<uint4*>(tile + tc::sw_chunk(L, (c0 >> 3) + 1, 128)) = make_uint4(w[4], w[5], w[6], w[7]);
         *reinterpret_cast<uint4*>(lo + tc::sw_chunk(L, c0 >> 3, 128)) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
         *reinterpret_cast<uint4*>(lo + tc::sw_chunk(L, (c0 >> 3) + 1, 128)) = make_uint4(wl[4], wl[5], wl[6], wl[7]);
+    };
+
+    // a staged token-major output tile (64 rows x 128 channels; the column blocks `bstride`
+    // bytes apart) to global memory: one TMA store (4D map: blocks 8 KB apart; 3D map: one
+    // store per block) for a full chunk, else the chunk's valid rows in 16-byte pieces
+    auto put_tile = [&](const CUtensorMap* map, bool blocked, uint32_t tile_off, int bstride, __nv_bfloat16* dst,
+                        const ChunkInfo& c, int hh) {
+        if (c.len == CH) {
+            if (tid == STORE_TID) {
+                if (blocked) {
+                    tc::tma_store_4d(map, 0, hh, (int)c.t0, 0, sb + tile_off);
+                } else {
+                    tc::tma_store_3d(map, 0, hh, (int)c.t0, sb + tile_off);
+                    tc::tma_store_3d(map, 64, hh, (int)c.t0, sb + tile_off + bstride);
+                }
+                tc::bulk_commit();
+            }
+        } else {
+            for (int i = tid; i < c.len * 16; i += 512) {
+                const int r = i >> 4, j = i & 15;
+                const uint4 v = *reinterpret_cast<const uint4*>(smem + tile_off + (j >> 3) * bstride + r * 128 +
+                                                                (((j & 7) ^ (r & 7)) << 4));
+                *reinterpret_cast<uint4*>(dst + ((c.t0 + r) * p.H + hh) * MD + j * 8) = v;
+            }
+        }
     };
 
     for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++it) {
@@ -385,6 +416,7 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
         tc::st16(tl(R_Q + c0), qs);
         tc::st16(tl(R_K + c0), ks);
     }
+    if (tid == STORE_TID) tc::bulk_wait_read();  // the last item's staged outputs were read
     __syncthreads();  // norms, factors and the q tile reads are done
 
     // per-element factors of this thread's channel and rows
@@ -562,12 +594,12 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
         rows16(sBeta, bt);
 #pragma unroll
         for (int i = 0; i < NCOL; ++i) {
-            const int r = c0 + i;
-            if (r < ci.len) p.dv[((ci.t0 + r) * p.H + h) * MD + L] = __float2bfloat16(bt[i] * v[i]);
+            *reinterpret_cast<__nv_bfloat16*>(sW2 + tok(64, i)) = __float2bfloat16(bt[i] * v[i]);  // dv, staged
             *reinterpret_cast<__nv_bfloat16*>(sDOY + tok(128, i) + 64 * 128) = __float2bfloat16(v[i]);  // dY
         }
     }
     sync_all();
+    put_tile(&m.dv, true, oW2, 8192, p.dv, ci, h);
 
     // ---- G7: Z^T = S0 dY^T ; G8: dkr^T = dS u^T ; G9: [dP; dA]_raw = [dO; dY] u^T ------------
     if (tid == 0) {
@@ -683,6 +715,7 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
             }
         }
         if (!isP) sDbA[hc * CH + r] = dbs;
+        if (tid == STORE_TID) tc::bulk_wait_read();  // dv's tile is read before qd' takes its space
         __syncthreads();  // every reader of S0, dS (and the u lo tile) is done
         if (KDA)
             store_cm_pair(sDS, sDS + TILE, o);
@@ -807,20 +840,19 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
         load_x(true, x, inv);
         rows16(sTot, tt);
 #pragma unroll
-        for (int i = 0; i < NCOL; ++i) {
-            const int r = c0 + i;
-            if (r < ci.len)
-                p.dq[((ci.t0 + r) * p.H + h) * MD + L] = __float2bfloat16((dQn[i] - x[i] * inv[i] * tt[i]) * inv[i]);
-        }
+        for (int i = 0; i < NCOL; ++i)  // dq into the dead ki' lo tile
+            *reinterpret_cast<__nv_bfloat16*>(sW1 + tok(64, i)) =
+                __float2bfloat16((dQn[i] - x[i] * inv[i] * tt[i]) * inv[i]);
         load_x(false, x, inv);
         rows16(sTot + CH, tt);
 #pragma unroll
-        for (int i = 0; i < NCOL; ++i) {
-            const int r = c0 + i;
-            if (r < ci.len)
-                p.dk[((ci.t0 + r) * p.H + h) * MD + L] = __float2bfloat16((dKn[i] - x[i] * inv[i] * tt[i]) * inv[i]);
-        }
+        for (int i = 0; i < NCOL; ++i)  // dk into the dead dY rows (the next item's dO fills rows 0..63)
+            *reinterpret_cast<__nv_bfloat16*>(sDOY + tok(128, i) + 64 * 128) =
+                __float2bfloat16((dKn[i] - x[i] * inv[i] * tt[i]) * inv[i]);
     }
+    sync_all();
+    put_tile(&m.dq, true, oW1, 8192, p.dq, ci, h);
+    put_tile(&m.dk, false, oDOY + 64 * 128, 128 * 128, p.dk, ci, h);
     // dbeta (logit space)
     for (int r = tid; r < ci.len; r += 512) {
         const float dA_A = ((sDbA[r] + sDbA[CH + r]) + sDbA[2 * CH + r]) + sDbA[3 * CH + r];
@@ -882,15 +914,17 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             const int r = c0 + i;
+            float dA;
+            const float draw = kda_gate_bwd<GATE>(p.gate_scale, ea, xr[i], dGc[i] + post, dA);
+            // staged in the raw-gate tile (read into xr above); rows past the end add nothing
+            *reinterpret_cast<__nv_bfloat16*>(smem + oA + tok(64, i)) = __float2bfloat16(draw);
             if (r < ci.len) {
-                float dA;
-                const float draw = kda_gate_bwd<GATE>(p.gate_scale, ea, xr[i], dGc[i] + post, dA);
-                p.dg_raw[((ci.t0 + r) * p.H + h) * MD + L] = __float2bfloat16(draw);
                 ddt += draw;
                 dA_acc += dA;
             }
         }
-        __syncthreads();  // suffix totals read
+        sync_all();  // suffix totals read; dg_raw staged
+        put_tile(&m.dgr, true, oA, 8192, p.dg_raw, ci, h);
         sScan[hc * MD + L] = ddt;
         dA_acc = warp_sum(dA_acc);
         if (lane == 0) sMisc[warp] = dA_acc;
@@ -909,6 +943,7 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
     __syncthreads();  // this item's small arrays and tensor memory are free
     tc::fence_after();
     }
+    if (tid == STORE_TID) tc::bulk_wait_all();
     tc::fence_before();
     __syncthreads();
     if (warp == 0) tc::dealloc(tmem, 512);
@@ -924,7 +959,10 @@ static cudaError_t launch_main_tc2_t(const Params& p, cudaStream_t s) {
               encode_blocked_tokens_map(&m.v, p.v, T, p.H) && encode_tokens_map(&m.dO, p.dO, T, p.H, MD) &&
               encode_blocked_rows_map(&m.S0, p.S0, rows_dd, MD) && encode_blocked_rows_map(&m.dS, p.dS, rows_dd, MD) &&
               encode_rows_map(&m.T, p.Tm, rows_cc, CH, CH) &&
-              encode_blocked_tokens_map(&m.graw, KDA ? p.g_raw : nullptr, T, p.H);
+              encode_blocked_tokens_map(&m.graw, KDA ? p.g_raw : nullptr, T, p.H) &&
+              encode_blocked_tokens_map(&m.dq, p.dq, T, p.H) && encode_tokens_map(&m.dk, p.dk, T, p.H, MD) &&
+              encode_blocked_tokens_map(&m.dv, p.dv, T, p.H) &&
+              encode_blocked_tokens_map(&m.dgr, KDA ? p.dg_raw : nullptr, T, p.H);
     if (!ok) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(k_main_tc2<KDA, GATE>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
