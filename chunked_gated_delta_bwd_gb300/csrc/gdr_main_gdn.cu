@@ -16,9 +16,9 @@
 // A tcgen05.mma takes tens of cycles to issue whatever its size, so the groups of a batch
 // are issued by lane 0 of different warps (one per SM sub-partition), each committing to
 // the batch's barrier, and G3 waits for dY to run as one N = 128 product with G7.
-// dv, dq and dk of a full chunk are staged token-major in shared tiles that are dead by
-// then (du^T, u^T, A and P) and written by TMA stores; a chunk cut by its sequence's end
-// writes its rows one element at a time.
+// dv, dq and dk are staged token-major in shared tiles that are dead by then (du^T, u^T,
+// A and P) and written by TMA stores; a chunk cut by its sequence's end copies its valid
+// rows from the staged tile instead.
 // with X10 = [dP; beta dA] scaled by the column factor invk_s e^{ref-gc_s} (ki' folded
 // in) and X11 = [dP; beta dA] scaled by the row factors of qd' and kd'.  B1 needs no
 // per-item preparation, so it is issued as soon as the tiles land and runs under the
@@ -244,6 +244,25 @@ __global__ void __launch_bounds__(512, 1) k_main_gdn(const Params p, const __gri
         rows16(isq ? sInvQ : sInvK, inv);
     };
 
+    // a staged token-major output tile (64 rows x 128 channels, column blocks 8 KB apart) to
+    // global memory: one TMA store for a full chunk, else the chunk's valid rows in 16-byte
+    // pieces (after a barrier that follows the staging)
+    auto put_tile = [&](const CUtensorMap* map, uint32_t tile_off, __nv_bfloat16* dst, const ChunkInfo& c, int hh) {
+        if (c.len == CH) {
+            if (tid == STORE_TID) {
+                tc::tma_store_4d(map, 0, hh, (int)c.t0, 0, sb + tile_off);
+                tc::bulk_commit();
+            }
+        } else {
+            for (int i = tid; i < c.len * 16; i += 512) {
+                const int r = i >> 4, j = i & 15;
+                const uint4 v = *reinterpret_cast<const uint4*>(smem + tile_off + (j >> 3) * 8192 + r * 128 +
+                                                                (((j & 7) ^ (r & 7)) << 4));
+                *reinterpret_cast<uint4*>(dst + ((c.t0 + r) * p.H + hh) * MD + j * 8) = v;
+            }
+        }
+    };
+
     for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++it) {
     const int h = item % p.H;
     const ChunkInfo ci = get_ci(it & 1);
@@ -439,26 +458,18 @@ __global__ void __launch_bounds__(512, 1) k_main_gdn(const Params p, const __gri
         tc::commit(mb1);
     }
     if (!wait_mma(1)) return;
-    const bool full = ci.len == CH;
     {
         float v[16], bt[16];
         tc::ld16(tl(R_D + c0), v);
         rows16(sBeta, bt);
 #pragma unroll
         for (int i = 0; i < NCOL; ++i) {
-            const __nv_bfloat16 dv = __float2bfloat16(bt[i] * v[i]);
-            if (full)  // dv staged token-major in the dead du^T tile
-                *reinterpret_cast<__nv_bfloat16*>(sDU + tok(64, i)) = dv;
-            else if (c0 + i < ci.len)
-                p.dv[((ci.t0 + c0 + i) * p.H + h) * MD + L] = dv;
+            *reinterpret_cast<__nv_bfloat16*>(sDU + tok(64, i)) = __float2bfloat16(bt[i] * v[i]);  // dv, staged
             *reinterpret_cast<__nv_bfloat16*>(sDOY + tok(128, i) + 64 * 128) = __float2bfloat16(v[i]);  // dY
         }
     }
     sync_all();
-    if (full && tid == STORE_TID) {
-        tc::tma_store_4d(&m.dv, 0, h, (int)ci.t0, 0, sb + oDU);
-        tc::bulk_commit();
-    }
+    put_tile(&m.dv, oDU, p.dv, ci, h);
 
     // ---- B4: G3/G7 [dqd^T, Z^T] = S0 [dO; dY]^T ; G8 dkr^T = dS u^T ; G9 [dP; dA]_raw =
     //      [dO; dY] u^T (three issuing threads)
@@ -660,23 +671,15 @@ __global__ void __launch_bounds__(512, 1) k_main_gdn(const Params p, const __gri
         load_x(true, x, inv);
         rows16(sTot, tt);
 #pragma unroll
-        for (int i = 0; i < NCOL; ++i) {
-            const __nv_bfloat16 d = __float2bfloat16((dQn[i] - x[i] * inv[i] * tt[i]) * inv[i]);
-            if (full)
-                *reinterpret_cast<__nv_bfloat16*>(sU + tok(64, i)) = d;
-            else if (c0 + i < ci.len)
-                p.dq[((ci.t0 + c0 + i) * p.H + h) * MD + L] = d;
-        }
+        for (int i = 0; i < NCOL; ++i)
+            *reinterpret_cast<__nv_bfloat16*>(sU + tok(64, i)) =
+                __float2bfloat16((dQn[i] - x[i] * inv[i] * tt[i]) * inv[i]);
         load_x(false, x, inv);
         rows16(sTot + CH, tt);
 #pragma unroll
-        for (int i = 0; i < NCOL; ++i) {
-            const __nv_bfloat16 d = __float2bfloat16((dKn[i] - x[i] * inv[i] * tt[i]) * inv[i]);
-            if (full)
-                *reinterpret_cast<__nv_bfloat16*>(sA + tok(64, i)) = d;
-            else if (c0 + i < ci.len)
-                p.dk[((ci.t0 + c0 + i) * p.H + h) * MD + L] = d;
-        }
+        for (int i = 0; i < NCOL; ++i)
+            *reinterpret_cast<__nv_bfloat16*>(sA + tok(64, i)) =
+                __float2bfloat16((dKn[i] - x[i] * inv[i] * tt[i]) * inv[i]);
     }
     tc::fence_async_smem();  // the staged dq / dk reach the copy engine after the next barrier
     // dbeta (logit space): <dY, beta E> + rowsum(dA . A)
@@ -714,11 +717,8 @@ __global__ void __launch_bounds__(512, 1) k_main_gdn(const Params p, const __gri
     tc::fence_before();
     __syncthreads();  // this item's small arrays and tensor memory are free
     tc::fence_after();
-    if (full && tid == STORE_TID) {
-        tc::tma_store_4d(&m.dq, 0, h, (int)ci.t0, 0, sb + oU);
-        tc::tma_store_4d(&m.dk, 0, h, (int)ci.t0, 0, sb + oA);
-        tc::bulk_commit();
-    }
+    put_tile(&m.dq, oU, p.dq, ci, h);
+    put_tile(&m.dk, oA, p.dk, ci, h);
     }
     if (tid == STORE_TID) tc::bulk_wait_all();
     tc::fence_before();
