@@ -521,7 +521,7 @@ def run_profile_case(args):
 
 
 # the sources that define the main kernel (its .cu file and the headers it includes)
-MAIN_SOURCES = ("gdr_main_tc2.cu", "gdr_chunk.cuh", "gdr_common.cuh", "gdr_tc.cuh", "gdr_tma.h", "gdr_internal.h")
+MAIN_SOURCES = ("gdr_main_kda.cu", "gdr_main_gdn.cu", "gdr_chunk.cuh", "gdr_common.cuh", "gdr_tc.cuh", "gdr_tma.h", "gdr_internal.h")
 
 
 def build_sha():

@@ -88,7 +88,7 @@ cudaError_t launch_prep_tc(const Params& p, cudaStream_t s);  // D = 128, tcgen0
 cudaError_t launch_states(const Params& p, bool fwd, bool bwd, cudaStream_t s);
 cudaError_t launch_states_tc(const Params& p, bool fwd, bool bwd, cudaStream_t s);  // D = 128, tcgen05 + TMA
 cudaError_t launch_main(const Params& p, cudaStream_t s);
-cudaError_t launch_main_tc2(const Params& p, cudaStream_t s);  // KDA (and GDN through launch_main_gdn), D = 128
+cudaError_t launch_main_kda(const Params& p, cudaStream_t s);  // KDA, D = 128, tcgen05 + TMA
 cudaError_t launch_main_gdn(const Params& p, cudaStream_t s);  // GDN, D = 128, tcgen05 + TMA on the raw q, k tiles
 cudaError_t launch_out(const Params& p, cudaStream_t s);       // forward output o = R S0 + P U
 cudaError_t launch_group_sum(const Params& p, cudaStream_t s);  // GQA: dq, dk summed over each head group

@@ -582,7 +582,7 @@ static cudaError_t launch_main_t(const Params& p, cudaStream_t s) {
 
 cudaError_t launch_main(const Params& p, cudaStream_t s) {
     if (p.max_chunks == 0) return cudaSuccess;
-    if (p.D == 128) return launch_main_tc2(p, s);
+    if (p.D == 128) return p.kda ? launch_main_kda(p, s) : launch_main_gdn(p, s);
     if (p.D == 128) return p.kda ? launch_main_t<128, true>(p, s) : launch_main_t<128, false>(p, s);
     return p.kda ? launch_main_t<64, true>(p, s) : launch_main_t<64, false>(p, s);
 }

@@ -1,14 +1,14 @@
-// Chunk-parallel main backward on tcgen05 for D = 128, GDN and KDA: persistent CTAs
-// of 16 warps, one per SM, each looping over (chunk, head) items; the next item's
-// operand tiles arrive by TMA while the current item's epilogue runs (every large
-// shared tile is dead after the last product group).  Same algebra as the warp-level
-// kernel in gdr_main.cu;
+// Chunk-parallel main backward on tcgen05 for D = 128 with the per-channel (KDA) gate:
+// persistent CTAs of 16 warps, one per SM, each looping over (chunk, head) items; the
+// next item's operand tiles arrive by TMA while the current item's epilogue runs (every
+// large shared tile is dead after the last product group).  Same algebra as the
+// warp-level kernel in gdr_main.cu (the scalar gate has its own kernel, gdr_main_gdn.cu);
 // every product is a 128-row tcgen05 MMA into tensor memory, written feature-major
 // where the natural output is C x D: the accumulator holds X^T (lane = key channel d
 // or value channel j, column = token row r), so a thread owns one channel for 16
-// rows.  The raw q and k rows and (KDA) the per-channel cumulative gate gc are staged
-// in tensor memory in that layout once, and every derived tile (kd', ki', qd', kd,
-// kr) is built from registers, channel-major ([d][r]), with 16-byte stores.
+// rows.  The raw q and k rows and e^{gc - ref} of the per-channel cumulative gate gc
+// are staged in tensor memory in that layout once, and every derived tile (kd', ki',
+// qd', kd, kr) is built from registers, channel-major ([d][r]), with 16-byte stores.
 //
 // With S0 = chunk-start state, dS = state gradient at the chunk end (both value-major
 // [j][d]) and [X; Y] a 128-row operand stacked from two 64-row tiles:
@@ -39,23 +39,23 @@ namespace {
 constexpr int MD = 128;
 constexpr int TILE = CH * MD * 2;  // 16 KB: a C x D token-major or a D x C channel-major bf16 tile
 // shared-memory map (bytes from the 1024-aligned base); later tenants after the arrows
-constexpr int oK = 0;           // k (token-major)     -> kr [d][r] -> (KDA) beta E lo -> (KDA) qd' lo
+constexpr int oK = 0;           // k (token-major)     -> kr [d][r] -> beta E lo -> qd' lo
 constexpr int oV = 16384;       // v -> beta E (token-major)
 constexpr int oDOY = 32768;     // [dO; dY] token-major, 128 rows
 constexpr int oS0 = 65536;      // S0 [j][d]          -> kd' [d][r] (+ lo at +16 KB)
 constexpr int oDS = 98304;      // dS [j][d]          -> [dP; beta dA] [m][s] (+ lo at +16 KB)
 constexpr int oT = 131072;      // T  [r][s]
-constexpr int oA = 139264;      // beta A_raw, strict lower [r][s]   -> (KDA) raw gate tile, with P's space
+constexpr int oA = 139264;      // beta A_raw, strict lower [r][s]   -> raw gate tile, with P's space
 constexpr int oP = 147456;      // P, lower [r][s]
-constexpr int oW0 = 155648;     // (KDA) raw gate tile -> kd' [d][r] (G1, A block 0) -> kd [d][r]
-                                //   -> (KDA) u^T lo -> ki' [d][r]
-constexpr int oW1 = 172032;     // qd' [d][r] (G1, A block 1) -> u^T [j][r] -> (KDA) ki' lo
+constexpr int oW0 = 155648;     // raw gate tile -> kd' [d][r] (G1, A block 0) -> kd [d][r]
+                                //   -> u^T lo -> ki' [d][r]
+constexpr int oW1 = 172032;     // qd' [d][r] (G1, A block 1) -> u^T [j][r] -> ki' lo
 constexpr int oW2 = 188416;     // q (token-major) -> ki' [d][r] -> du^T -> qd' [d][r]
 constexpr int oSmall = 204800;
 // small arrays (floats)
 constexpr int NCOL = 16;  // rows per thread (16 warps: 4 lane quarters x 4 row quarters)
 constexpr int nInvQ = 64, nInvK = 64, nBeta = 64, nFac = 256, nGate = 128, nRef = 128, nGT = 128,
-              nScan = 512, nDgTs = 128, nDgTp = 512, nDbP = 64, nDbA = 256, nRow = 256 * 3, nMisc = 64, nTot = 128;
+              nScan = 512, nDgTs = 128, nDgTp = 512, nDbP = 64, nDbA = 256, nRow = 512, nMisc = 64, nTot = 128;
 constexpr int SMALL_FLOATS =
     nInvQ + nInvK + nBeta + nFac + nGate + nRef + nGT + nScan + nDgTs + nDgTp + nDbP + nDbA + nRow + nMisc + nTot;
 constexpr int SMEM_BYTES = oSmall + SMALL_FLOATS * 4 + 64 + 1024;  // + mbarriers / tmem slot + alignment
@@ -69,8 +69,8 @@ constexpr int STORE_TID = 96;  // the thread that issues the TMA stores of dq, d
 
 }  // namespace
 
-template <bool KDA, int GATE>
-__global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __grid_constant__ MainMaps m) {
+template <int GATE>
+__global__ void __launch_bounds__(512, 1) k_main_kda(const Params p, const __grid_constant__ MainMaps m) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     const uint32_t sb = smem_u32(smem);
@@ -89,27 +89,22 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
     float* sInvQ = fsm;
     float* sInvK = sInvQ + nInvQ;
     float* sBeta = sInvK + nInvK;
-    float* sFac = sBeta + nBeta;     // GDN [4][64]: e^{gc}, e^{gc-ref}, e^{ref-gc}, e^{gT-gc}; KDA [2][128]: e^{ref}, e^{gT-ref}
-    float* sGate = sFac + nFac;      // GDN gc[64], ref, gT; KDA dt_bias[d]
-    float* sRef = sGate + nGate;     // KDA ref[d]
-    float* sGT = sRef + nRef;        // KDA gT[d]
-    float* sScan = sGT + nGT;        // KDA [4][128] per-quarter gate totals / extrema / suffix totals
+    float* sFac = sBeta + nBeta;     // [2][128]: e^{ref}, e^{gT-ref} per channel
+    float* sGate = sFac + nFac;      // dt_bias[d]
+    float* sRef = sGate + nGate;     // ref[d]
+    float* sGT = sRef + nRef;        // gT[d]
+    float* sScan = sGT + nGT;        // [4][128] per-quarter gate totals / extrema / suffix totals
     float* sDgTs = sScan + nScan;    // [128] state part of dgT
     float* sDgTp = sDgTs + nDgTs;    // [4][128] kr part of dgT per row quarter
     float* sDbP = sDgTp + nDgTp;     // [64] <dY, beta E> per row
     float* sDbA = sDbP + nDbP;       // [4][64] rowsum(dA . A) per column quarter
-    float* sRow = sDbA + nDbA;       // [3][4][64] row reductions (and KDA partials)
-    float* sMisc = sRow + nRow;      // [64]: per-warp partials [0, 16); KDA e^{A_log} at [32]
+    float* sRow = sDbA + nDbA;       // [2][4][64] row dots; earlier the [4][128] per-quarter gate minima
+    float* sMisc = sRow + nRow;      // [64]: per-warp partials [0, 16); e^{A_log} at [32]
     float* sTot = sMisc + nMisc;     // [2][64] row dots summed over the lane quarters (q, k)
     uint64_t* mbars = reinterpret_cast<uint64_t*>(sTot + nTot);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(mbars + 3);
-    // MMA completion; operand tiles of an item; (KDA) the raw gate tile for the gate chain rule
+    // MMA completion; operand tiles of an item; the raw gate tile for the gate chain rule
     const uint32_t mb = smem_u32(mbars), mload = smem_u32(mbars + 1), mgr = smem_u32(mbars + 2);
-
-    Gates<MD, false> G;  // GDN scalar gates
-    G.gc = sGate;
-    G.ref = sGate + CH;
-    G.gT = sGate + CH + 1;
 
     // the operand tiles of an item: copy `which` (0 .. 8), or all of them (which < 0).  The
     // copies may be issued by different threads and in any order: the transaction count of
@@ -118,8 +113,8 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
         ChunkInfo cj;
         lookup_chunk(item / p.H, p.N, p.chunk_off, p.cu_seqlens, p.seq_len, cj);
         const int hh = item % p.H, t0 = (int)cj.t0, rcd = item * CH, rdd = item * MD;
-        if (which <= 0) tc::mbar_expect_tx(mload, 4 * TILE + 2 * 2 * TILE + CH * CH * 2 + (KDA ? TILE : 0));
-        if (KDA && (which < 0 || which == 0))
+        if (which <= 0) tc::mbar_expect_tx(mload, 4 * TILE + 2 * 2 * TILE + CH * CH * 2 + TILE);
+        if (which < 0 || which == 0)
             tc::tma_load_4d(sb + oW0, &m.graw, 0, hh, t0, 0, mload);  // raw gates (token-major)
         if (which < 0 || which == 1) tc::tma_load_4d(sb + oK, &m.k, 0, qk_head(p, hh), t0, 0, mload);
         if (which < 0 || which == 2) tc::tma_load_4d(sb + oV, &m.v, 0, hh, t0, 0, mload);
@@ -148,12 +143,9 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
     int it = 0;              // this CTA's item count (the load barrier's phase)
     bool pending = (int)blockIdx.x < n_items;  // a load batch is in flight
     uint32_t pend_par = 0;                     // ... on this phase parity of the load barrier
-    bool pending_g = false;                    // (KDA) a raw gate tile is in flight
-    // the next item's GDN gate (first warp, rows 2 lane and 2 lane + 1) and beta logit
-    // (thread r < 64), loaded one item ahead
-    // (raw values, rows clamped into the chunk, first read at the next item's top, so no
-    // thread waits for them)
-    float pg0 = 0.f, pg1 = 0.f;
+    bool pending_g = false;                    // a raw gate tile is in flight
+    // the next item's beta logit (thread r < 64), loaded one item ahead as a raw value (row
+    // clamped into the chunk) first read at the next item's top, so no thread waits for it
     unsigned short pb = 0;
     auto prefetch_small = [&](int item) {
         if (tid >= CH) return;
@@ -161,10 +153,6 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
         lookup_chunk(item / p.H, p.N, p.chunk_off, p.cu_seqlens, p.seq_len, cj);
         const int hh = item % p.H;
         pb = reinterpret_cast<const unsigned short*>(p.beta_logit)[(cj.t0 + min(tid, cj.len - 1)) * p.H + hh];
-        if (!KDA && tid < 32) {
-            pg0 = p.g[(cj.t0 + min(2 * tid, cj.len - 1)) * p.H + hh];
-            pg1 = p.g[(cj.t0 + min(2 * tid + 1, cj.len - 1)) * p.H + hh];
-        }
     };
     if ((int)blockIdx.x < n_items) prefetch_small(blockIdx.x);
     auto sync_all = [&]() {  // make smem writes visible to the tensor cores and order TMEM use
@@ -260,15 +248,9 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
     const int chunk = item / p.H, h = item % p.H;
     ChunkInfo ci;
     lookup_chunk(chunk, p.N, p.chunk_off, p.cu_seqlens, p.seq_len, ci);
-    if constexpr (!KDA)
-        if (tid < 32) gdn_gate_scan(2 * tid < ci.len ? pg0 : 0.f, 2 * tid + 1 < ci.len ? pg1 : 0.f, G, false, p);
     if (tid < CH) sBeta[tid] = tid < ci.len ? sigmoid_f(__bfloat162float(__ushort_as_bfloat16(pb))) : 0.f;
-    // KDA gate parameters, read while the operand tiles land
-    float alog = 0.f, bias = 0.f;
-    if constexpr (KDA) {
-        alog = p.A_log[h];
-        bias = p.dt_bias[h * MD + L];
-    }
+    // gate parameters, read while the operand tiles land
+    const float alog = p.A_log[h], bias = p.dt_bias[h * MD + L];
 
     // wait for the operand tiles; rows past the chunk's end read as zero
     {
@@ -276,61 +258,59 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
         if (__syncthreads_or(!ok)) return bail();
         pending = false;
     }
-    // KDA: per-channel log gates of this thread's channel and rows, scanned across the four
+    // per-channel log gates of this thread's channel and rows, scanned across the four
     // row quarters; once the chunk's reference is known, e^{gc - ref} is staged in tensor
     // memory (lane = channel, column = row) and the other gate factors derive from it
-    float g[16];  // (KDA) cumulative gates of this thread's rows
-    if constexpr (KDA) {
-        const float a = expf(alog);
-        if (hc == 0) sGate[L] = bias;  // for the gate chain rule at the end of the item
-        if (tid == 0) sMisc[32] = a;
-        {
-            const int lch = (L & 63) >> 3, lsub = (L & 7) << 1;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const uint32_t off = (uint32_t)((L >> 6) * 64 * 128 + (c0 + i) * 128 + ((lch ^ (i & 7)) << 4) + lsub);
-                g[i] = c0 + i < ci.len ? __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(sW0 + off)) : 0.f;
-            }
-        }
-        float acc = 0.f;
+    float g[16];  // cumulative gates of this thread's rows
+    const float a = expf(alog);
+    if (hc == 0) sGate[L] = bias;  // for the gate chain rule at the end of the item
+    if (tid == 0) sMisc[32] = a;
+    {
+        const int lch = (L & 63) >> 3, lsub = (L & 7) << 1;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-            if (c0 + i < ci.len) acc += kda_gate_fn<GATE>(p.gate_scale, a, g[i] + bias);
-            g[i] = acc;
+            const uint32_t off = (uint32_t)((L >> 6) * 64 * 128 + (c0 + i) * 128 + ((lch ^ (i & 7)) << 4) + lsub);
+            g[i] = c0 + i < ci.len ? __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(sW0 + off)) : 0.f;
         }
-        sScan[hc * MD + L] = acc;  // this quarter's total
-        __syncthreads();
-        float pre = 0.f, tot = 0.f;
+    }
+    float acc = 0.f;
 #pragma unroll
-        for (int h2 = 0; h2 < 4; ++h2) {
-            const float t = sScan[h2 * MD + L];
-            if (h2 < hc) pre += t;
-            tot += t;
-        }
-        float mx = -3.0e38f, mn = 3.0e38f;
+    for (int i = 0; i < 16; ++i) {
+        if (c0 + i < ci.len) acc += kda_gate_fn<GATE>(p.gate_scale, a, g[i] + bias);
+        g[i] = acc;
+    }
+    sScan[hc * MD + L] = acc;  // this quarter's total
+    __syncthreads();
+    float pre = 0.f, tot = 0.f;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            g[i] += pre;
-            mx = fmaxf(mx, g[i]);
-            mn = fminf(mn, g[i]);
-        }
-        tc::st16(tl(R_G + c0), g);
-        __syncthreads();  // totals read
-        sScan[hc * MD + L] = mx;
-        sRow[hc * MD + L] = mn;
-        __syncthreads();
-        if (hc == 0) {
-            float M = sScan[L], N = sRow[L];
+    for (int h2 = 0; h2 < 4; ++h2) {
+        const float t = sScan[h2 * MD + L];
+        if (h2 < hc) pre += t;
+        tot += t;
+    }
+    float mx = -3.0e38f, mn = 3.0e38f;
 #pragma unroll
-            for (int h2 = 1; h2 < 4; ++h2) {
-                M = fmaxf(M, sScan[h2 * MD + L]);
-                N = fminf(N, sRow[h2 * MD + L]);
-            }
-            sRef[L] = 0.5f * (M + N);
-            sGT[L] = tot;
-            sFac[L] = __expf(0.5f * (M + N));              // e^{ref}
-            sFac[MD + L] = __expf(tot - 0.5f * (M + N));   // e^{gT - ref}
+    for (int i = 0; i < 16; ++i) {
+        g[i] += pre;
+        mx = fmaxf(mx, g[i]);
+        mn = fminf(mn, g[i]);
+    }
+    tc::st16(tl(R_G + c0), g);
+    __syncthreads();  // totals read
+    sScan[hc * MD + L] = mx;
+    sRow[hc * MD + L] = mn;
+    __syncthreads();
+    if (hc == 0) {
+        float M = sScan[L], N = sRow[L];
+#pragma unroll
+        for (int h2 = 1; h2 < 4; ++h2) {
+            M = fmaxf(M, sScan[h2 * MD + L]);
+            N = fminf(N, sRow[h2 * MD + L]);
         }
+        sRef[L] = 0.5f * (M + N);
+        sGT[L] = tot;
+        sFac[L] = __expf(0.5f * (M + N));              // e^{ref}
+        sFac[MD + L] = __expf(tot - 0.5f * (M + N));   // e^{gT - ref}
     }
 
     if (ci.len < CH) {
@@ -343,15 +323,13 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
         }
     }
     __syncthreads();
-    if constexpr (KDA) {
-        const float refL = sRef[L];
-        float f[16];
+    const float refL = sRef[L];
+    float f[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) f[i] = __expf(g[i] - refL);
-        tc::st16(tl(R_G + c0), f);
-    }
+    for (int i = 0; i < 16; ++i) f[i] = __expf(g[i] - refL);
+    tc::st16(tl(R_G + c0), f);
 
-    // inverse row norms of q (from W2) and k, 4 threads per row; GDN gate factor table;
+    // inverse row norms of q (from W2) and k, 4 threads per row;
     // dgT state part (column sums of the value-major dS . S0)
     {
         const int r = (tid >> 2) & 63, part = tid & 3;
@@ -370,14 +348,6 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
         s += __shfl_xor_sync(0xffffffffu, s, 2);
         if (part == 0) (tid < 256 ? sInvQ : sInvK)[r] = rsqrtf(s + 1e-6f);
     }
-    if constexpr (!KDA) {
-        for (int r = tid; r < CH; r += 512) {
-            sFac[0 * CH + r] = gate_factor<F_KD>(G, r, 0);
-            sFac[1 * CH + r] = gate_factor<F_KDP>(G, r, 0);
-            sFac[2 * CH + r] = gate_factor<F_KIP>(G, r, 0);
-            sFac[3 * CH + r] = gate_factor<F_KR>(G, r, 0);
-        }
-    }
     {
         const int cp = tid >> 3, g = tid & 7;  // column pair, row group
         float s0 = 0.f, s1 = 0.f;
@@ -393,14 +363,9 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
             s1 += __shfl_xor_sync(0xffffffffu, s1, o);
         }
         if (g == 0) {
-            if constexpr (KDA) {
-                sDgTs[2 * cp] = s0 * __expf(sGT[2 * cp]);
-                sDgTs[2 * cp + 1] = s1 * __expf(sGT[2 * cp + 1]);
-            } else {
-                const float eg = __expf(G.gTv(0));
-                sDgTs[2 * cp] = s0 * eg;
-                sDgTs[2 * cp + 1] = s1 * eg;
-            }
+            sDgTs[2 * cp] = s0 * __expf(sGT[2 * cp]);
+            sDgTs[2 * cp + 1] = s1 * __expf(sGT[2 * cp + 1]);
+        
         }
     }
     // raw q and k of this thread's channel and rows into tensor memory
@@ -421,22 +386,19 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
 
     // per-element factors of this thread's channel and rows
     auto factors = [&](int kind, float (&f)[16]) {
-        if constexpr (KDA) {
-            // e^{gc-ref} from tensor memory; e^{gc} = e^{gc-ref} e^{ref}, e^{ref-gc} = 1 / e^{gc-ref},
-            // e^{gT-gc} = e^{gT-ref} / e^{gc-ref} (|gc - ref| <= 80: no overflow)
-            const float eRef = sFac[L], eGTref = sFac[MD + L];
-            float e[16];
-            tc::ld16(tl(R_G + c0), e);
+        // e^{gc-ref} from tensor memory; e^{gc} = e^{gc-ref} e^{ref}, e^{ref-gc} = 1 / e^{gc-ref},
+        // e^{gT-gc} = e^{gT-ref} / e^{gc-ref} (|gc - ref| <= 80: no overflow)
+        const float eRef = sFac[L], eGTref = sFac[MD + L];
+        float e[16];
+        tc::ld16(tl(R_G + c0), e);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                if (kind == F_KDP) f[i] = e[i];
-                else if (kind == F_KD) f[i] = e[i] * eRef;
-                else if (kind == F_KIP) f[i] = __fdividef(1.f, e[i]);
-                else f[i] = __fdividef(eGTref, e[i]);
-            }
-        } else {
-            rows16(sFac + kind * CH, f);
+        for (int i = 0; i < 16; ++i) {
+            if (kind == F_KDP) f[i] = e[i];
+            else if (kind == F_KD) f[i] = e[i] * eRef;
+            else if (kind == F_KIP) f[i] = __fdividef(1.f, e[i]);
+            else f[i] = __fdividef(eGTref, e[i]);
         }
+    
     };
     // raw q (or k) of this thread's channel and rows, and the rows' inverse norms
     auto load_x = [&](bool isq, float (&x)[16], float (&inv)[16]) {
@@ -537,7 +499,7 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
             const float be = bt[i] * (__bfloat162float(*pv) - v[i]);
             const __nv_bfloat16 hi = __float2bfloat16(be);
             *pv = hi;
-            if (KDA) *reinterpret_cast<__nv_bfloat16*>(sK + tok(64, i)) = __float2bfloat16(be - __bfloat162float(hi));
+            *reinterpret_cast<__nv_bfloat16*>(sK + tok(64, i)) = __float2bfloat16(be - __bfloat162float(hi));
         }
     }
     tc::ld16(tl(R_D + c0), v);
@@ -560,10 +522,9 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
 #pragma unroll
         for (int k = 0; k < CH; k += 16)
             tc::mma(tmem + R_B, tc::mdesc(sb + oV, 64, 0, k), tc::kdesc(sb + oT, 64, 0, k), id4, k > 0);
-        if (KDA)
 #pragma unroll
-            for (int k = 0; k < CH; k += 16)
-                tc::mma(tmem + R_B, tc::mdesc(sb + oK, 64, 0, k), tc::kdesc(sb + oT, 64, 0, k), id4, 1);
+        for (int k = 0; k < CH; k += 16)  // + (beta E lo)^T T^T
+            tc::mma(tmem + R_B, tc::mdesc(sb + oK, 64, 0, k), tc::kdesc(sb + oT, 64, 0, k), id4, 1);
 #pragma unroll
         for (int k = 0; k < CH; k += 16)
             tc::mma(tmem + R_A, tc::mdesc(sb + oDOY, 128, 0, k), tc::mdesc(sb + oP, 64, 0, k), id5, 1);
@@ -571,10 +532,7 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
     }
     if (!wait_mma()) return;
     tc::ld16(tl(R_B + c0), v);
-    if (KDA)
-        store_cm_pair(sW1, sW0, v);  // u^T (hi) and its residual (kd is dead)
-    else
-        store_cm(sW1, v);
+    store_cm_pair(sW1, sW0, v);  // u^T (hi) and its residual (kd is dead)
     tc::ld16(tl(R_A + c0), v);
     store_cm(sW2, v);  // du^T over ki'
     sync_all();
@@ -614,14 +572,14 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
 #pragma unroll
         for (int k = 0; k < MD; k += 16)
             tc::mma(tmem + R_D, tc::kdesc(sb + oDOY, 128, 0, k), tc::mdesc(sb + oW1, 128, 0, k), id9, k > 0);
-        if (KDA) {  // u lo
+  // u lo
 #pragma unroll
-            for (int k = 0; k < MD; k += 16)
-                tc::mma(tmem + R_C, tc::mdesc(sb + oDS, 128, 0, k), tc::mdesc(sb + oW0, 128, 0, k), id8, 1);
+        for (int k = 0; k < MD; k += 16)
+            tc::mma(tmem + R_C, tc::mdesc(sb + oDS, 128, 0, k), tc::mdesc(sb + oW0, 128, 0, k), id8, 1);
 #pragma unroll
-            for (int k = 0; k < MD; k += 16)
-                tc::mma(tmem + R_D, tc::kdesc(sb + oDOY, 128, 0, k), tc::mdesc(sb + oW0, 128, 0, k), id9, 1);
-        }
+        for (int k = 0; k < MD; k += 16)
+            tc::mma(tmem + R_D, tc::kdesc(sb + oDOY, 128, 0, k), tc::mdesc(sb + oW0, 128, 0, k), id9, 1);
+    
         tc::commit(mb);
     }
     // while the tensor cores run: <dY, beta E> per row (token-major, 4 threads per row)
@@ -632,23 +590,15 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
             const uint4 a = *reinterpret_cast<const uint4*>(sDOY + tc::sw_chunk(64 + r, j, 128));
             const uint4 b = *reinterpret_cast<const uint4*>(sV + tc::sw_chunk(r, j, 64));
             const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};
-            uint32_t wl[4] = {0, 0, 0, 0};
-            if (KDA) {
-                const uint4 l = *reinterpret_cast<const uint4*>(sK + tc::sw_chunk(r, j, 64));
-                wl[0] = l.x;
-                wl[1] = l.y;
-                wl[2] = l.z;
-                wl[3] = l.w;
-            }
+            const uint4 l = *reinterpret_cast<const uint4*>(sK + tc::sw_chunk(r, j, 64));  // beta E lo
+            const uint32_t wl[4] = {l.x, l.y, l.z, l.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const float2 fa = unpack_bf16(wa[e]);
                 float2 fb = unpack_bf16(wb[e]);
-                if (KDA) {
-                    const float2 fl = unpack_bf16(wl[e]);
-                    fb.x += fl.x;
-                    fb.y += fl.y;
-                }
+                const float2 fl = unpack_bf16(wl[e]);
+                fb.x += fl.x;
+                fb.y += fl.y;
                 s2 += fa.x * fb.x + fa.y * fb.y;
             }
         }
@@ -717,23 +667,19 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
         if (!isP) sDbA[hc * CH + r] = dbs;
         if (tid == STORE_TID) tc::bulk_wait_read();  // dv's tile is read before qd' takes its space
         __syncthreads();  // every reader of S0, dS (and the u lo tile) is done
-        if (KDA)
-            store_cm_pair(sDS, sDS + TILE, o);
-        else
-            store_cm(sDS, o);
+        store_cm_pair(sDS, sDS + TILE, o);
     }
     // rebuilds for G10 / G11: ki' -> W0 (lo W1), qd' -> W2 (lo K), kd' -> S0 (lo S0 + 16 KB)
-    build(sW0, KDA ? sW1 : nullptr, false, 1.f, F_KIP);
-    build(sW2, KDA ? sK : nullptr, true, p.scale, F_KDP);
-    build(sS0, KDA ? sS0 + TILE : nullptr, false, 1.f, F_KDP);
+    build(sW0, sW1, false, 1.f, F_KIP);
+    build(sW2, sK, true, p.scale, F_KDP);
+    build(sS0, sS0 + TILE, false, 1.f, F_KDP);
     sync_all();
-    if (KDA) {  // the raw gates again, for the gate chain rule, into the dead A and P tiles
-        if (tid == 0) {
-            tc::mbar_expect_tx(mgr, TILE);
-            tc::tma_load_4d(sb + oA, &m.graw, 0, h, (int)ci.t0, 0, mgr);
-        }
-        pending_g = true;
+  // the raw gates again, for the gate chain rule, into the dead A and P tiles
+    if (tid == 0) {
+        tc::mbar_expect_tx(mgr, TILE);
+        tc::tma_load_4d(sb + oA, &m.graw, 0, h, (int)ci.t0, 0, mgr);
     }
+    pending_g = true;
 
     // ---- G10: [dqd', dkd']^T = ki'^T [dP; beta dA]^T ; G11: dki'^T = qd'^T dP + kd'^T (beta dA) --
     if (tid == 0) {
@@ -743,29 +689,27 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
 #pragma unroll
         for (int k = 0; k < CH; k += 16)
             tc::mma(tmem + R_A, tc::kdesc(kiH, 128, 0, k), tc::kdesc(xH, 128, 0, k), id10, k > 0);
-        if (KDA) {
 #pragma unroll
-            for (int k = 0; k < CH; k += 16)
-                tc::mma(tmem + R_A, tc::kdesc(kiH, 128, 0, k), tc::kdesc(xL, 128, 0, k), id10, 1);
+        for (int k = 0; k < CH; k += 16)
+            tc::mma(tmem + R_A, tc::kdesc(kiH, 128, 0, k), tc::kdesc(xL, 128, 0, k), id10, 1);
 #pragma unroll
-            for (int k = 0; k < CH; k += 16)
-                tc::mma(tmem + R_A, tc::kdesc(kiL, 128, 0, k), tc::kdesc(xH, 128, 0, k), id10, 1);
-        }
+        for (int k = 0; k < CH; k += 16)
+            tc::mma(tmem + R_A, tc::kdesc(kiL, 128, 0, k), tc::kdesc(xH, 128, 0, k), id10, 1);
+    
 #pragma unroll
         for (int k = 0; k < CH; k += 16)
             tc::mma(tmem + R_B, tc::kdesc(qdH, 128, 0, k), tc::mdesc(xH, 128, 0, k), id11, k > 0);
 #pragma unroll
         for (int k = 0; k < CH; k += 16)
             tc::mma(tmem + R_B, tc::kdesc(kdH, 128, 0, k), tc::mdesc(xH, 128, 64, k), id11, 1);
-        if (KDA) {
 #pragma unroll
-            for (int k = 0; k < CH; k += 16) {
-                tc::mma(tmem + R_B, tc::kdesc(qdH, 128, 0, k), tc::mdesc(xL, 128, 0, k), id11, 1);
-                tc::mma(tmem + R_B, tc::kdesc(qdL, 128, 0, k), tc::mdesc(xH, 128, 0, k), id11, 1);
-                tc::mma(tmem + R_B, tc::kdesc(kdH, 128, 0, k), tc::mdesc(xL, 128, 64, k), id11, 1);
-                tc::mma(tmem + R_B, tc::kdesc(kdL, 128, 0, k), tc::mdesc(xH, 128, 64, k), id11, 1);
-            }
+        for (int k = 0; k < CH; k += 16) {
+            tc::mma(tmem + R_B, tc::kdesc(qdH, 128, 0, k), tc::mdesc(xL, 128, 0, k), id11, 1);
+            tc::mma(tmem + R_B, tc::kdesc(qdL, 128, 0, k), tc::mdesc(xH, 128, 0, k), id11, 1);
+            tc::mma(tmem + R_B, tc::kdesc(kdH, 128, 0, k), tc::mdesc(xL, 128, 64, k), id11, 1);
+            tc::mma(tmem + R_B, tc::kdesc(kdL, 128, 0, k), tc::mdesc(xH, 128, 64, k), id11, 1);
         }
+    
         tc::commit(mb);
     }
     if (!wait_mma()) return;
@@ -776,9 +720,9 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
         pend_par = (uint32_t)((it + 1) & 1);
         prefetch_small(item + gridDim.x);
     }
-    // the gate-gradient term takes the derived-tile value the products consumed: the bf16
-    // element (GDN) or the fp32 value of the hi + lo pair (KDA)
-    auto tile_val = [&](float x, float mm, float f) -> float { return KDA ? x * mm * f : derived_val(x, mm, f); };
+    // the gate-gradient term takes the derived-tile value the products consumed: the fp32
+    // value of the hi + lo pair
+    auto tile_val = [&](float x, float mm, float f) -> float { return x * mm * f; };
     {
         float f[16], x[16], inv[16];
         factors(F_KDP, f);
@@ -808,11 +752,6 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
     // ---- epilogue: L2-norm backward, dq / dk, dbeta, the gate gradient ----------------------
     float* sRowQ = sRow;        // [4][64] per lane quarter
     float* sRowK = sRow + 256;  // [4][64]
-    float* sRowG = sRow + 512;  // [4][64] (GDN)
-    if constexpr (!KDA) {  // channel sums of dgc per row (dGc is dead afterwards)
-        const float sg = warp_transpose_sum16(dGc);  // lanes 2i, 2i+1: row c0 + i
-        if ((lane & 1) == 0) sRowG[q4 * CH + c0 + (lane >> 1)] = sg;
-    }
     {
         // per-row dots over this warp's 32 channels: lane l gets row c0 + (l & 15)
         float t[32];
@@ -861,83 +800,63 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
     auto dgT_of = [&](int d) -> float {
         return (((sDgTs[d] + sDgTp[d]) + sDgTp[MD + d]) + sDgTp[2 * MD + d]) + sDgTp[3 * MD + d];
     };
-    if constexpr (!KDA) {
-        // dg: channel sums of dgc (per row), suffix sums over the rows, plus the chunk constant dgT
-        if (warp == 0) {
-            float t = 0.f;
-            for (int d = lane; d < MD; d += 32) t += dgT_of(d);
-            t = warp_sum(t);
-            const int r0 = 2 * lane;
-            const float a = ((sRowG[r0] + sRowG[CH + r0]) + sRowG[2 * CH + r0]) + sRowG[3 * CH + r0];
-            const float b = ((sRowG[r0 + 1] + sRowG[CH + r0 + 1]) + sRowG[2 * CH + r0 + 1]) + sRowG[3 * CH + r0 + 1];
-            float incl = a + b;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float y = __shfl_down_sync(0xffffffffu, incl, o);
-                if (lane + o < 32) incl += y;
-            }
-            if (r0 < ci.len) p.dg[(ci.t0 + r0) * p.H + h] = incl + t;
-            if (r0 + 1 < ci.len) p.dg[(ci.t0 + r0 + 1) * p.H + h] = incl - a + t;
-        }
-    } else {
-        // reverse cumsum of dgc over the rows per channel: this thread's 16 rows in registers,
-        // the later row quarters' totals and the chunk constant dgT as the suffix; then the
-        // gate chain rule per element, with per-channel partial sums
-        float xr[16];
-        const float bias = sGate[L];
-        {
-            const bool ok = tc::mbar_wait(mgr, (uint32_t)(it & 1));
-            if (__syncthreads_or(!ok)) return bail();
-            pending_g = false;
-            const unsigned char* gt = smem + oA;  // token-major raw gates (A and P spaces)
-            const int lch = (L & 63) >> 3, lsub = (L & 7) << 1;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const uint32_t off = (uint32_t)((L >> 6) * 64 * 128 + (c0 + i) * 128 + ((lch ^ (i & 7)) << 4) + lsub);
-                xr[i] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(gt + off)) + bias;
-            }
-        }
-        float acc = 0.f;
-#pragma unroll
-        for (int i = 15; i >= 0; --i) {
-            acc += dGc[i];
-            dGc[i] = acc;
-        }
-        sScan[hc * MD + L] = acc;
-        __syncthreads();
-        float post = dgT_of(L);
-#pragma unroll
-        for (int h2 = 3; h2 >= 0; --h2)
-            if (h2 > hc) post += sScan[h2 * MD + L];
-        const float ea = sMisc[32];
-        float ddt = 0.f, dA_acc = 0.f;
+    // reverse cumsum of dgc over the rows per channel: this thread's 16 rows in registers,
+    // the later row quarters' totals and the chunk constant dgT as the suffix; then the
+    // gate chain rule per element, with per-channel partial sums
+    float xr[16];
+    const float dtb = sGate[L];
+    {
+        const bool ok = tc::mbar_wait(mgr, (uint32_t)(it & 1));
+        if (__syncthreads_or(!ok)) return bail();
+        pending_g = false;
+        const unsigned char* gt = smem + oA;  // token-major raw gates (A and P spaces)
+        const int lch = (L & 63) >> 3, lsub = (L & 7) << 1;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-            const int r = c0 + i;
-            float dA;
-            const float draw = kda_gate_bwd<GATE>(p.gate_scale, ea, xr[i], dGc[i] + post, dA);
-            // staged in the raw-gate tile (read into xr above); rows past the end add nothing
-            *reinterpret_cast<__nv_bfloat16*>(smem + oA + tok(64, i)) = __float2bfloat16(draw);
-            if (r < ci.len) {
-                ddt += draw;
-                dA_acc += dA;
-            }
+            const uint32_t off = (uint32_t)((L >> 6) * 64 * 128 + (c0 + i) * 128 + ((lch ^ (i & 7)) << 4) + lsub);
+            xr[i] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(gt + off)) + dtb;
         }
-        sync_all();  // suffix totals read; dg_raw staged
-        put_tile(&m.dgr, true, oA, 8192, p.dg_raw, ci, h);
-        sScan[hc * MD + L] = ddt;
-        dA_acc = warp_sum(dA_acc);
-        if (lane == 0) sMisc[warp] = dA_acc;
-        __syncthreads();
-        if (tid < MD) {
-            const float t = ((sScan[tid] + sScan[MD + tid]) + sScan[2 * MD + tid]) + sScan[3 * MD + tid];
-            atomicAdd(&p.ddt_bias[h * MD + tid], t);
+    }
+    float sfx = 0.f;
+#pragma unroll
+    for (int i = 15; i >= 0; --i) {
+        sfx += dGc[i];
+        dGc[i] = sfx;
+    }
+    sScan[hc * MD + L] = sfx;
+    __syncthreads();
+    float post = dgT_of(L);
+#pragma unroll
+    for (int h2 = 3; h2 >= 0; --h2)
+        if (h2 > hc) post += sScan[h2 * MD + L];
+    const float ea = sMisc[32];
+    float ddt = 0.f, dA_acc = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const int r = c0 + i;
+        float dA;
+        const float draw = kda_gate_bwd<GATE>(p.gate_scale, ea, xr[i], dGc[i] + post, dA);
+        // staged in the raw-gate tile (read into xr above); rows past the end add nothing
+        *reinterpret_cast<__nv_bfloat16*>(smem + oA + tok(64, i)) = __float2bfloat16(draw);
+        if (r < ci.len) {
+            ddt += draw;
+            dA_acc += dA;
         }
-        if (tid == 0) {
-            float t = 0.f;
-            for (int w = 0; w < 16; ++w) t += sMisc[w];
-            atomicAdd(&p.dA_log[h], t);
-        }
+    }
+    sync_all();  // suffix totals read; dg_raw staged
+    put_tile(&m.dgr, true, oA, 8192, p.dg_raw, ci, h);
+    sScan[hc * MD + L] = ddt;
+    dA_acc = warp_sum(dA_acc);
+    if (lane == 0) sMisc[warp] = dA_acc;
+    __syncthreads();
+    if (tid < MD) {
+        const float t = ((sScan[tid] + sScan[MD + tid]) + sScan[2 * MD + tid]) + sScan[3 * MD + tid];
+        atomicAdd(&p.ddt_bias[h * MD + tid], t);
+    }
+    if (tid == 0) {
+        float t = 0.f;
+        for (int w = 0; w < 16; ++w) t += sMisc[w];
+        atomicAdd(&p.dA_log[h], t);
     }
     tc::fence_before();
     __syncthreads();  // this item's small arrays and tensor memory are free
@@ -949,8 +868,8 @@ __global__ void __launch_bounds__(512, 1) k_main_tc2(const Params p, const __gri
     if (warp == 0) tc::dealloc(tmem, 512);
 }
 
-template <bool KDA, int GATE>
-static cudaError_t launch_main_tc2_t(const Params& p, cudaStream_t s) {
+template <int GATE>
+static cudaError_t launch_main_kda_t(const Params& p, cudaStream_t s) {
     MainMaps m;
     const uint64_t rows_cc = (uint64_t)p.max_chunks * p.H * CH;
     const uint64_t rows_dd = (uint64_t)p.max_chunks * p.H * MD;
@@ -959,23 +878,22 @@ static cudaError_t launch_main_tc2_t(const Params& p, cudaStream_t s) {
               encode_blocked_tokens_map(&m.v, p.v, T, p.H) && encode_tokens_map(&m.dO, p.dO, T, p.H, MD) &&
               encode_blocked_rows_map(&m.S0, p.S0, rows_dd, MD) && encode_blocked_rows_map(&m.dS, p.dS, rows_dd, MD) &&
               encode_rows_map(&m.T, p.Tm, rows_cc, CH, CH) &&
-              encode_blocked_tokens_map(&m.graw, KDA ? p.g_raw : nullptr, T, p.H) &&
+              encode_blocked_tokens_map(&m.graw, p.g_raw, T, p.H) &&
               encode_blocked_tokens_map(&m.dq, p.dq, T, p.H) && encode_tokens_map(&m.dk, p.dk, T, p.H, MD) &&
               encode_blocked_tokens_map(&m.dv, p.dv, T, p.H) &&
-              encode_blocked_tokens_map(&m.dgr, KDA ? p.dg_raw : nullptr, T, p.H);
+              encode_blocked_tokens_map(&m.dgr, p.dg_raw, T, p.H);
     if (!ok) return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(k_main_tc2<KDA, GATE>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(k_main_kda<GATE>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int items = p.max_chunks * p.H;
     const int ctas = items < num_sms() ? items : num_sms();
-    k_main_tc2<KDA, GATE><<<ctas, 512, SMEM_BYTES, s>>>(p, m);
+    k_main_kda<GATE><<<ctas, 512, SMEM_BYTES, s>>>(p, m);
     return cudaGetLastError();
 }
 
-cudaError_t launch_main_tc2(const Params& p, cudaStream_t s) {
+cudaError_t launch_main_kda(const Params& p, cudaStream_t s) {
     // the KDA gate function is a template parameter: each instance carries only its own code
-    if (!p.kda) return launch_main_gdn(p, s);
-    return p.kda_gate == 0 ? launch_main_tc2_t<true, 0>(p, s) : launch_main_tc2_t<true, 1>(p, s);
+    return p.kda_gate == 0 ? launch_main_kda_t<0>(p, s) : launch_main_kda_t<1>(p, s);
 }
 
 }  // namespace gdr
