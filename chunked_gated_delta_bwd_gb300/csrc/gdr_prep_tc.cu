@@ -226,7 +226,7 @@ __global__ void __launch_bounds__(512, 1) k_prep_tc(const Params p, const __grid
     float* sInvQ = fsm;
     float* sInvK = sInvQ + nInvQ;
     float* sBeta = sInvK + nInvK;
-    float* sFac = sBeta + nBeta;  // GDN [4][64]
+    float* sFac = sBeta + nBeta;  // GDN [4][64]; KDA [2][128] e^{ref}, e^{gT-ref} per channel
     float* sGate = sFac + nFac;   // GDN gc[64], ref, gT
     float* sRef = sGate + nGate;  // KDA ref[d]
     float* sGT = sRef + nRef;     // KDA gT[d]
@@ -439,6 +439,8 @@ __global__ void __launch_bounds__(512, 1) k_prep_tc(const Params p, const __grid
             }
             sRef[L] = 0.5f * (M + N);
             sGT[L] = tot;
+            sFac[L] = __expf(0.5f * (M + N));             // e^{ref}
+            sFac[PD + L] = __expf(tot - 0.5f * (M + N));  // e^{gT - ref}
             if (0.5f * (M - N) > 80.f || M > 80.f) atomicOr(p.status, ST_GATE_RANGE);
         }
     }
@@ -457,9 +459,14 @@ __global__ void __launch_bounds__(512, 1) k_prep_tc(const Params p, const __grid
         }
     }
     __syncthreads();
-    if constexpr (KDA) {
+    if constexpr (KDA) {  // e^{gc - ref} of this thread's channel and rows replaces gc in tensor memory
         refL = sRef[L];
         gTL = sGT[L];
+        float g[16];
+        tc::ld16(tl(R_G + c0), g);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) g[i] = __expf(g[i] - refL);
+        tc::st16(tl(R_G + c0), g);
     }
     {  // inverse row norms of q and k, 4 threads per row
         const int r = (tid >> 2) & 63, part = tid & 3;
@@ -503,12 +510,17 @@ __global__ void __launch_bounds__(512, 1) k_prep_tc(const Params p, const __grid
     // gate factors of this thread's channel and rows cq .. cq+15
     auto factors = [&](int kind, float (&f)[16], int cq) {
         if constexpr (KDA) {
-            float g[16];
-            tc::ld16(tl(R_G + cq), g);
+            // e^{gc-ref} from tensor memory; e^{gc} = e^{gc-ref} e^{ref}, e^{ref-gc} = 1 / e^{gc-ref},
+            // e^{gT-gc} = e^{gT-ref} / e^{gc-ref} (|gc - ref| <= 80: no overflow)
+            const float eRef = sFac[L], eGTref = sFac[PD + L];
+            float e[16];
+            tc::ld16(tl(R_G + cq), e);
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-                const float e = kind == F_KD ? g[i] : kind == F_KDP ? g[i] - refL : kind == F_KIP ? refL - g[i] : gTL - g[i];
-                f[i] = __expf(e);
+                if (kind == F_KDP) f[i] = e[i];
+                else if (kind == F_KD) f[i] = e[i] * eRef;
+                else if (kind == F_KIP) f[i] = __fdividef(1.f, e[i]);
+                else f[i] = __fdividef(eGTref, e[i]);
             }
         } else {
             rows16(sFac + kind * CH, f, cq);
