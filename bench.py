@@ -389,38 +389,74 @@ def main_gpu(args):
     }
 
     # ---- end to end: pinned host inputs -> device -> backward -> host gradients ----
+    # Pipelined as a training loop runs it: two device sets of inputs and gradients; step i's
+    # inputs upload on one copy stream while step i - 1 computes, and step i's gradients
+    # download on another while step i + 1 computes.  Every step still moves all of its
+    # inputs in and all of its gradients out inside the timed region.
     def pinned(x):
         return {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
     hg, hk = pinned(xg), pinned(xk)
     hout_g = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in out_g.items()}
     hout_k = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in out_k.items()}
-    keys_g = [k for k, v in hg.items() if isinstance(v, torch.Tensor)]
-    keys_k = [k for k, v in hk.items() if isinstance(v, torch.Tensor)]
-    h2d = sum(hg[k].numel() * hg[k].element_size() for k in keys_g if k != "cu_seqlens") + \
-        sum(hk[k].numel() * hk[k].element_size() for k in keys_k if k != "cu_seqlens")
+    keys_g = [k for k, v in hg.items() if isinstance(v, torch.Tensor) and k != "cu_seqlens"]
+    keys_k = [k for k, v in hk.items() if isinstance(v, torch.Tensor) and k != "cu_seqlens"]
+    h2d = sum(hg[k].numel() * hg[k].element_size() for k in keys_g) + \
+        sum(hk[k].numel() * hk[k].element_size() for k in keys_k)
     d2h = sum(v.numel() * v.element_size() for v in out_g.values()) + \
         sum(v.numel() * v.element_size() for v in out_k.values())
+    sets = [(G, K, out_g, out_k),
+            (dev(xg), dev(xk), gdr.alloc_outputs(T, Hh, D, N, "gdn"), gdr.alloc_outputs(T, Hh, D, N, "kda"))]
+    up_s, down_s = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: [torch.cuda.Event(), torch.cuda.Event()]
+    ev_up, ev_comp, ev_down = ev(), ev(), ev()
 
-    def e2e_step():
-        for k in keys_g:
-            if k != "cu_seqlens":
-                G[k].copy_(hg[k], non_blocking=True)
-        for k in keys_k:
-            if k != "cu_seqlens":
-                K[k].copy_(hk[k], non_blocking=True)
-        step()
-        for k, v in out_g.items():
-            hout_g[k].copy_(v, non_blocking=True)
-        for k, v in out_k.items():
-            hout_k[k].copy_(v, non_blocking=True)
+    def e2e_steps(n):
+        # the first upload, then per step: compute (after its upload and the previous download
+        # from the same set), the next upload (after the compute that last read that set) and
+        # this step's download
+        up_s.wait_stream(stream)
+        down_s.wait_stream(stream)
+        with torch.cuda.stream(up_s):
+            for k in keys_g:
+                sets[0][0][k].copy_(hg[k], non_blocking=True)
+            for k in keys_k:
+                sets[0][1][k].copy_(hk[k], non_blocking=True)
+            ev_up[0].record(up_s)
+        for i in range(n):
+            b = i & 1
+            Gb, Kb, og, ok = sets[b]
+            stream.wait_event(ev_up[b])
+            if i >= 2:
+                stream.wait_event(ev_down[b])
+            step_g(A=Gb, o=og)
+            step_k(A=Kb, o=ok)
+            ev_comp[b].record(stream)
+            if i + 1 < n:
+                nb = b ^ 1
+                with torch.cuda.stream(up_s):
+                    if i >= 1:
+                        up_s.wait_event(ev_comp[nb])
+                    for k in keys_g:
+                        sets[nb][0][k].copy_(hg[k], non_blocking=True)
+                    for k in keys_k:
+                        sets[nb][1][k].copy_(hk[k], non_blocking=True)
+                    ev_up[nb].record(up_s)
+            with torch.cuda.stream(down_s):
+                down_s.wait_event(ev_comp[b])
+                for k, v in og.items():
+                    hout_g[k].copy_(v, non_blocking=True)
+                for k, v in ok.items():
+                    hout_k[k].copy_(v, non_blocking=True)
+                ev_down[b].record(down_s)
+        stream.wait_stream(up_s)
+        stream.wait_stream(down_s)
 
-    e2e_step()
+    e2e_steps(2)
     torch.cuda.synchronize()
     barrier(world)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
+    e2e_steps(args.steps)
     b.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(a.elapsed_time(b) / args.steps, world)
