@@ -79,8 +79,9 @@ def barrier(world):
 
 
 class Clocks:
-    """Samples SM clocks and throttle reasons with nvidia-smi during the timed region."""
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """Samples SM clocks and throttle reasons with nvidia-smi (every 10 ms, time-stamped); the
+    summary keeps the samples taken inside the timed region [t0, t1] (host wall-clock)."""
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -91,7 +92,7 @@ class Clocks:
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "10"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -108,23 +109,27 @@ class Clocks:
                 out, _ = self.proc.communicate()
             self.lines = [l for l in out.splitlines() if l.strip()]
 
-    def summary(self):
-        sm, mx, reasons = [], 0.0, set()
+    def summary(self, t0=None, t1=None):
+        import datetime
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        rows = []
         for l in getattr(self, "lines", []):
             f = [x.strip() for x in l.split(",")]
-            if len(f) < 9:
+            if len(f) < 10:
                 continue
             try:
-                sm.append(float(f[1]))
-                mx = max(mx, float(f[2]))
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(f[2]), float(f[3]), f[6:10]))
             except ValueError:
                 continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx or None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        inside = [r for r in rows if t0 is not None and t0 - 0.005 <= r[0] <= t1 + 0.005]
+        use = inside if inside else rows
+        sm = [r[1] for r in use]
+        reasons = {n for r in use for n, v in zip(names, r[3]) if v.lower() == "active"}
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max((r[2] for r in use), default=None),
+                "reasons": sorted(reasons), "samples": len(sm),
+                "window": "timed region" if inside else "whole sampler run"}
 
 
 # ---------------------------------------------------------------------------
@@ -231,16 +236,25 @@ def main_gpu(args):
             raise RuntimeError("device status %d raised by the warm-up steps" % st)
 
     # ---- timed region (device-resident inputs) ----
-    api.profile_begin(16 * args.steps)
     barrier(world)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with Clocks(local) as clk:
+        # untimed steps while the sampler starts (about half a second), then the timed steps
+        t_settle = time.time()
+        while time.time() - t_settle < 0.5:
+            step()
+            torch.cuda.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        api.profile_begin(16 * args.steps)
+        t_clk0 = time.time()
         e0.record(stream)
         for _ in range(args.steps):
             step()
         e1.record(stream)
         torch.cuda.synchronize()
+        t_clk1 = time.time()
     barrier(world)
     prof = api.profile_end()
     ms_local = e0.elapsed_time(e1) / args.steps
@@ -500,7 +514,7 @@ def main_gpu(args):
         roof = {"kernel": k, "bound": "hbm", "achieved": None, "peak": hbm, "unit": "GB/s", "frac": None,
                 "traffic": None, "note": "dominant kernel has no algorithmic figure yet"}
 
-    csum = clk.summary()
+    csum = clk.summary(t_clk0, t_clk1)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
