@@ -1,0 +1,459 @@
+// Chunk-parallel preparation on tcgen05 for D = 128 with the scalar (GDN) gate:
+// persistent CTAs of 16 warps, one per SM, each looping over (chunk, head) items; the
+// q, k, v tiles of the next item arrive by TMA into a second stage while the current item
+// is computed.  The quantities of the X/R form of the FlashQLA dh kernel ("FlashQLA ...
+// GDN 反向", §三), as the per-channel kernel in gdr_prep_tc.cu computes them:
+//
+//   [A; P] = [kd'; qd'] ki'^T        A = strict_lower(diag(beta) .) (fp32), P = lower(.)
+//   T   = (I + A)^-1                  W^T = (beta kd)^T T^T       U^T = (beta V)^T T^T
+//   R^T = qd^T - W^T P^T (a bf16 pair R_hi + R_lo)                kr  = kn e^{gT-gc}
+//
+// With one log gate per token every gated tile is a row scaling of the raw q or k tile,
+// so, as in the scalar-gate main kernel, the products read the raw bf16 tiles as loaded
+// (k and q stacked into one 128-row tile) and the row factors are applied in fp32:
+//   G1  [A; P]_raw = [k; q] k^T, issued as soon as the tiles land (under the norms and
+//       the gate factors), then A = G1 x beta_r invk_r e^{gc_r-ref} x invk_s e^{ref-gc_s}
+//       and P = G1 x scale invq_r e^{gc_r-ref} x invk_s e^{ref-gc_s};
+//   W^T = k^T (T diag(beta invk e^{gc}))^T and U^T = v^T (T diag(beta))^T: the column
+//       factors go into two bf16 copies of T, no (beta kd)^T or (beta V)^T tile is built.
+// W, U, Kr, R_hi, R_lo and T are staged in shared tiles that are dead by then and written
+// by TMA stores; one thread issues those stores and the next item's copies.
+#include "gdr_chunk.cuh"
+#include "gdr_invert.cuh"
+#include "gdr_tc.cuh"
+#include "gdr_tma.h"
+
+namespace gdr {
+
+namespace {
+
+using inv::LDF;
+using inv::XLD;
+constexpr int PD = 128;
+constexpr int TILE = CH * PD * 2;  // 16 KB
+// shared-memory map (bytes from the 1024-aligned base); two input stages
+constexpr int STAGE = 3 * TILE;
+constexpr int oKQ = 0;            // [k; q] token-major, 128 rows -> U^T staged [j][s] (+16 KB: R_hi^T [d][r])
+constexpr int oV = 2 * TILE;      // v token-major -> kr staged [d][r]
+constexpr int oW2 = 2 * STAGE;    // W^T bf16 [d][s] (R's operand, W's store)
+constexpr int oP = oW2 + TILE;    // P [r][s] bf16
+constexpr int oT = oP + 8192;     // T [r][s] bf16 (blocks above the diagonal stay zero)
+constexpr int oT1 = oT + 8192;    // T diag(beta invk e^{gc}) [r][s] bf16 -> (with T2's space) R_lo^T staged
+constexpr int oT2 = oT1 + 8192;   // T diag(beta) [r][s] bf16
+constexpr int oA = oT2 + 8192;    // A fp32 [64][LDF] row-major
+constexpr int oTf = oA + CH * LDF * 4;    // T fp32, transposed [c][r], stride LDF
+constexpr int oTmp = oTf + CH * LDF * 4;  // 8 warps' transfer tiles [8][XLD]
+constexpr int nTmp = 8 * 8 * XLD;
+constexpr int oSmall = (oTmp + nTmp * 4 + 1023) / 1024 * 1024;
+constexpr int nInvQ = 64, nInvK = 64, nBeta = 64, nFac = 4 * 64, nTab = 4 * 64, nGate = 66, nPad = 62;
+constexpr int SMALL_FLOATS = nInvQ + nInvK + nBeta + nFac + nTab + nGate + nPad;
+constexpr int SMEM_BYTES = oSmall + SMALL_FLOATS * 4 + 64 + 1024;
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+constexpr uint32_t R_G1 = 0, R_W = 64, R_U = 128, R_R = 192, R_Q = 256, R_K = 320;
+// combined row-factor tables (each [64])
+enum Tab { T_CF = 0, T_RA = 1, T_RP = 2, T_CW = 3 };
+// The thread that issues the TMA stores of W, U, Kr, R_hi, R_lo and T and the copies of the
+// next item's q, k and v: its stores read the stage that those copies overwrite, and a bulk
+// store's completion is visible only to the thread that issued it.
+constexpr int STORE_TID = 416;
+
+struct PrepGdnMaps {
+    CUtensorMap q, k, v, W, U, Kr, R, Rlo, T;
+};
+
+}  // namespace
+
+__global__ void __launch_bounds__(512, 1) k_prep_gdn(const Params p, const __grid_constant__ PrepGdnMaps m) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    const uint32_t sb = smem_u32(smem);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // items (chunk, head) = chunk * H + h over the chunks that exist
+    const int total_chunks = p.chunk_off ? p.chunk_off[p.N] : p.N * (int)((p.seq_len + CH - 1) / CH);
+    const int n_items = total_chunks * p.H;
+    const int q4 = warp & 3, hc = warp >> 2;
+    const int L = 32 * q4 + lane;  // this thread's lane: a channel, or a stacked row of G1
+    const int c0 = 16 * hc;        // first of this thread's 16 rows (or columns)
+
+    unsigned char *sW2 = smem + oW2, *sP = smem + oP, *sT = smem + oT, *sT1 = smem + oT1, *sT2 = smem + oT2;
+    float* sA = reinterpret_cast<float*>(smem + oA);
+    float* sTf = reinterpret_cast<float*>(smem + oTf);
+    float* sTmp = reinterpret_cast<float*>(smem + oTmp);
+    float* fsm = reinterpret_cast<float*>(smem + oSmall);
+    float* sInvQ = fsm;
+    float* sInvK = sInvQ + nInvQ;
+    float* sBeta = sInvK + nInvK;
+    float* sFac = sBeta + nBeta;  // [4][64] e^{gc}, e^{gc-ref}, e^{ref-gc}, e^{gT-gc} (Fac order)
+    float* sTab = sFac + nFac;    // [4][64] combined row factors (Tab order)
+    float* sGate = sTab + nTab;   // gc[64], ref, gT
+    uint64_t* mbars = reinterpret_cast<uint64_t*>(sGate + nGate + nPad);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbars + 3);
+    const uint32_t mb = smem_u32(mbars), mload0 = smem_u32(mbars + 1);  // load barriers: one per stage
+
+    Gates<PD, false> G;
+    G.gc = sGate;
+    G.ref = sGate + CH;
+    G.gT = sGate + CH + 1;
+
+    // q, k, v of `item` into stage `stg`: k and q stacked into one 128-row tile, one 64-column
+    // box at a time, v as two column blocks
+    auto issue_loads = [&](int item, int stg) {
+        ChunkInfo cj;
+        lookup_chunk(item / p.H, p.N, p.chunk_off, p.cu_seqlens, p.seq_len, cj);
+        const int hh = item % p.H, hk = qk_head(p, hh), t0 = (int)cj.t0;
+        const uint32_t bar = mload0 + 8 * stg, st = sb + stg * STAGE;
+        tc::mbar_expect_tx(bar, 3 * TILE);
+        tc::tma_load_3d(st + oKQ, &m.k, 0, hk, t0, bar);
+        tc::tma_load_3d(st + oKQ + 2 * 8192, &m.k, 64, hk, t0, bar);
+        tc::tma_load_3d(st + oKQ + 8192, &m.q, 0, hk, t0, bar);
+        tc::tma_load_3d(st + oKQ + 3 * 8192, &m.q, 64, hk, t0, bar);
+        tc::tma_load_4d(st + oV, &m.v, 0, hh, t0, 0, bar);
+    };
+    if (warp == 0) tc::alloc(smem_u32(tslot), 512);
+    if (tid == 0) {
+        tc::mbar_init(mb, 1);
+        tc::mbar_init(mload0, 1);
+        tc::mbar_init(mload0 + 8, 1);
+    }
+    // T's blocks above the diagonal stay zero in the shared tile
+    for (int i = tid; i < CH * CH * 2 / 16; i += 512)
+        *reinterpret_cast<uint4*>(smem + oT + 16 * i) = make_uint4(0, 0, 0, 0);
+    tc::fence_async_smem();
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    if (tid == STORE_TID && (int)blockIdx.x < n_items) issue_loads(blockIdx.x, 0);
+    const uint32_t tmem = *tslot;
+    uint32_t phase = 0;
+    int it = 0;  // this CTA's item count (selects the stage)
+    auto tl = [&](uint32_t col) { return tmem + ((uint32_t)(32 * q4) << 16) + col; };
+    auto sync_all = [&]() {
+        tc::fence_async_smem();
+        tc::fence_before();
+        __syncthreads();
+        tc::fence_after();
+    };
+    int pending = (int)blockIdx.x < n_items ? 0 : -1;  // stage with a load in flight, or -1
+    uint32_t pending_par = 0;
+    auto bail = [&]() {
+        if (tid == STORE_TID) {
+            if (pending >= 0) tc::mbar_wait(mload0 + 8 * pending, pending_par);  // bounded drain
+            tc::bulk_wait_all();
+        }
+        if (tid == 0) atomicOr(p.status, ST_MMA_TIMEOUT);
+        tc::fence_before();
+        __syncthreads();
+        if (warp == 0) tc::dealloc(tmem, 512);
+    };
+    auto wait_mma = [&]() -> bool {
+        const bool ok = tc::mbar_wait(mb, phase);
+        phase ^= 1;
+        tc::fence_after();
+        if (__syncthreads_or(!ok)) {
+            bail();
+            return false;
+        }
+        return true;
+    };
+    // the next item's beta logit (thread r < 64) and gates (first warp, rows 2 lane and
+    // 2 lane + 1), read one item ahead as raw values (rows clamped into the chunk) that are
+    // first read at the next item's top, so no thread waits for them
+    float pg0 = 0.f, pg1 = 0.f;
+    unsigned short pb = 0;
+    auto prefetch_small = [&](int item) {
+        if (tid >= CH) return;
+        ChunkInfo cj;
+        lookup_chunk(item / p.H, p.N, p.chunk_off, p.cu_seqlens, p.seq_len, cj);
+        const int hh = item % p.H;
+        pb = reinterpret_cast<const unsigned short*>(p.beta_logit)[(cj.t0 + min(tid, cj.len - 1)) * p.H + hh];
+        if (tid < 32) {
+            pg0 = p.g[(cj.t0 + min(2 * tid, cj.len - 1)) * p.H + hh];
+            pg1 = p.g[(cj.t0 + min(2 * tid + 1, cj.len - 1)) * p.H + hh];
+        }
+    };
+    if ((int)blockIdx.x < n_items) prefetch_small(blockIdx.x);
+    auto rows16 = [&](const float* a, float (&o)[16], int cq) {  // a[cq .. cq+15]
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float4 v = *reinterpret_cast<const float4*>(a + cq + 4 * i);
+            o[4 * i] = v.x;
+            o[4 * i + 1] = v.y;
+            o[4 * i + 2] = v.z;
+            o[4 * i + 3] = v.w;
+        }
+    };
+    auto pack8 = [&](const float (&v)[16], uint32_t (&w)[8]) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) w[e] = pack_bf16(v[2 * e], v[2 * e + 1]);
+    };
+    // row L, columns c0 .. c0+15 of a channel-major [128][64] shared tile
+    auto store_cm = [&](unsigned char* tile, const uint32_t (&w)[8]) {
+        *reinterpret_cast<uint4*>(tile + tc::sw_chunk(L, c0 >> 3, 128)) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(tile + tc::sw_chunk(L, (c0 >> 3) + 1, 128)) = make_uint4(w[4], w[5], w[6], w[7]);
+    };
+    // raw q (or k) of this thread's channel and rows (staged in tensor memory) times the
+    // rows' inverse norm, the multiplier and the gate factor `kind`
+    auto derived = [&](bool isq, float mul, int kind, float (&o)[16]) {
+        float f[16], inv[16];
+        rows16(sFac + kind * CH, f, c0);
+        tc::ld16(tl((isq ? R_Q : R_K) + c0), o);
+        rows16(isq ? sInvQ : sInvK, inv, c0);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) o[i] = o[i] * derived_m(inv[i], mul, 1.f) * f[i];
+    };
+
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++it) {
+    const int chunk = item / p.H, h = item % p.H;
+    ChunkInfo ci;
+    lookup_chunk(chunk, p.N, p.chunk_off, p.cu_seqlens, p.seq_len, ci);
+    const int stg = it & 1;
+    const uint32_t st = sb + stg * STAGE;
+    unsigned char* sKQ = smem + stg * STAGE + oKQ;
+    unsigned char* sV = smem + stg * STAGE + oV;
+    const size_t tile_cc = ((size_t)chunk * p.H + h) * CH * CH;
+    const int trow = (chunk * p.H + h) * PD;  // the chunk-head's first row in the [D][C] tile maps
+    const bool has_next = item + (int)gridDim.x < n_items;
+    // the last item's stores have read their tiles (the other stage and the shared staging
+    // tiles); then the next item's tiles go into the other stage
+    if (tid == STORE_TID) {
+        tc::bulk_wait_read();
+        if (has_next) issue_loads(item + gridDim.x, stg ^ 1);
+    }
+    if (tid < 32) gdn_gate_scan(2 * tid < ci.len ? pg0 : 0.f, 2 * tid + 1 < ci.len ? pg1 : 0.f, G, true, p);
+    if (tid < CH) sBeta[tid] = tid < ci.len ? sigmoid_f(__bfloat162float(__ushort_as_bfloat16(pb))) : 0.f;
+
+    // operand tiles; rows past the chunk's end are zeroed before any product
+    {
+        const bool ok = tc::mbar_wait(mload0 + 8 * stg, (uint32_t)((it >> 1) & 1));
+        if (__syncthreads_or(!ok)) return bail();
+        pending = has_next ? (stg ^ 1) : -1;
+        pending_par = (uint32_t)(((it + 1) >> 1) & 1);
+    }
+    if (ci.len < CH) {
+        const int nz = (CH - ci.len) * 16;  // 16-byte chunks per 128-column row
+        for (int i = tid; i < 3 * nz; i += 512) {
+            const int t = i / nz, rem = i % nz, r = ci.len + rem / 16, jc = rem % 16;
+            unsigned char* base = t < 2 ? sKQ : sV;
+            const int row = t == 1 ? 64 + r : r, rows = t == 2 ? 64 : 128;
+            *reinterpret_cast<uint4*>(base + tc::sw_chunk(row, jc, rows)) = make_uint4(0, 0, 0, 0);
+        }
+        sync_all();
+    }
+
+    // ---- G1: [A; P]_raw = [k; q] k^T on the tiles as loaded, under the prologue below -----
+    if (tid == 0) {
+        constexpr uint32_t id1 = tc::idesc(128, 64, 0, 0);
+#pragma unroll
+        for (int k = 0; k < PD; k += 16)
+            tc::mma(tmem + R_G1, tc::kdesc(st + oKQ, 128, 0, k), tc::kdesc(st + oKQ, 128, 0, k), id1, k > 0);
+        tc::commit(mb);
+    }
+    {  // inverse row norms of q (rows 64..127 of the stacked tile) and k, 4 threads per row
+        const int r = (tid >> 2) & 63, part = tid & 3;
+        const int row = tid < 256 ? 64 + r : r;
+        float s = 0.f;
+        for (int j = part * 4; j < part * 4 + 4; ++j) {
+            const uint4 v = *reinterpret_cast<const uint4*>(sKQ + tc::sw_chunk(row, j, 128));
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 f = unpack_bf16(w[e]);
+                s += f.x * f.x + f.y * f.y;
+            }
+        }
+        s += __shfl_xor_sync(0xffffffffu, s, 1);
+        s += __shfl_xor_sync(0xffffffffu, s, 2);
+        if (part == 0) (tid < 256 ? sInvQ : sInvK)[r] = rsqrtf(s + 1e-6f);
+    }
+    if (tid < CH) {
+        sFac[F_KD * CH + tid] = gate_factor<F_KD>(G, tid, 0);
+        sFac[F_KDP * CH + tid] = gate_factor<F_KDP>(G, tid, 0);
+        sFac[F_KIP * CH + tid] = gate_factor<F_KIP>(G, tid, 0);
+        sFac[F_KR * CH + tid] = gate_factor<F_KR>(G, tid, 0);
+    }
+    {  // raw q and k of this thread's channel and rows into tensor memory
+        const int lch = (L & 63) >> 3, lsub = (L & 7) << 1;
+        float qs[16], ks[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {  // k row c0 + i; the q row sits 64 rows (8 KB) below
+            const uint32_t off = (uint32_t)((L >> 6) * 128 * 128 + (c0 + i) * 128 + ((lch ^ (i & 7)) << 4) + lsub);
+            ks[i] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(sKQ + off));
+            qs[i] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(sKQ + off + 64 * 128));
+        }
+        tc::st16(tl(R_Q + c0), qs);
+        tc::st16(tl(R_K + c0), ks);
+    }
+    __syncthreads();  // norms and gate factors
+    if (tid < CH) {   // combined row factors
+        const float ik = sInvK[tid], e1 = sFac[F_KDP * CH + tid], bt = sBeta[tid];
+        sTab[T_CF * CH + tid] = ik * sFac[F_KIP * CH + tid];       // ki' column factor
+        sTab[T_RA * CH + tid] = bt * ik * e1;                        // A row factor (with beta)
+        sTab[T_RP * CH + tid] = p.scale * sInvQ[tid] * e1;           // P row factor
+        sTab[T_CW * CH + tid] = bt * ik * sFac[F_KD * CH + tid];     // column factor of T for W
+    }
+    if (!wait_mma()) return;  // G1 (its barrier also publishes the tables)
+    {
+        float v[16], cf[16];
+        tc::ld16(tl(R_G1 + c0), v);
+        rows16(sTab + T_CF * CH, cf, c0);
+        if (L < 64) {  // A = strict_lower(beta A_raw), fp32 for the inversion
+            const int r = L;
+            const float rf = sTab[T_RA * CH + r];
+#pragma unroll
+            for (int i = 0; i < 16; i += 4)
+                *reinterpret_cast<float4*>(sA + r * LDF + c0 + i) =
+                    make_float4(c0 + i < r ? v[i] * rf * cf[i] : 0.f, c0 + i + 1 < r ? v[i + 1] * rf * cf[i + 1] : 0.f,
+                                c0 + i + 2 < r ? v[i + 2] * rf * cf[i + 2] : 0.f,
+                                c0 + i + 3 < r ? v[i + 3] * rf * cf[i + 3] : 0.f);
+        } else {  // P = lower(qd' ki'^T), bf16 [r][s]
+            const int r = L - 64;
+            const float rf = sTab[T_RP * CH + r];
+            uint32_t w[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int s0 = c0 + 2 * e;
+                w[e] = pack_bf16(s0 <= r ? v[2 * e] * rf * cf[2 * e] : 0.f,
+                                 s0 + 1 <= r ? v[2 * e + 1] * rf * cf[2 * e + 1] : 0.f);
+            }
+            *reinterpret_cast<uint4*>(sP + tc::sw_chunk(r, c0 >> 3, 64)) = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4*>(sP + tc::sw_chunk(r, (c0 >> 3) + 1, 64)) = make_uint4(w[4], w[5], w[6], w[7]);
+            if (p.Pm) {  // forward output: P [r][s] per chunk-head
+                uint4* g = reinterpret_cast<uint4*>(p.Pm + tile_cc + r * CH + c0);
+                g[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                g[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            }
+        }
+    }
+    __syncthreads();
+    if (warp < 8) inv::invert_tc(sA, sTf, sTmp, sT, nullptr);  // warps 8-15 wait at the barrier
+    __syncthreads();  // T complete (fp32 transposed in sTf, bf16 in sT)
+    {
+        // T diag(beta invk e^{gc}) -> T1 and T diag(beta) -> T2 (bf16 [r][s]), the B operands of
+        // W^T = k^T T1^T and U^T = v^T T2^T; thread: row r, 16 columns, one of the two copies
+        const int r = tid & 63, cq = 16 * ((tid >> 6) & 3), which = tid >> 8;
+        float f[16];
+        rows16(which == 0 ? sTab + T_CW * CH : sBeta, f, cq);
+        float v[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = cq + i <= r ? sTf[(cq + i) * LDF + r] * f[i] : 0.f;
+        uint32_t w[8];
+        pack8(v, w);
+        unsigned char* dst = which == 0 ? sT1 : sT2;
+        *reinterpret_cast<uint4*>(dst + tc::sw_chunk(r, cq >> 3, 64)) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(dst + tc::sw_chunk(r, (cq >> 3) + 1, 64)) = make_uint4(w[4], w[5], w[6], w[7]);
+    }
+    sync_all();
+    if (tid == STORE_TID) {  // T for the main backward
+        tc::tma_store_2d(&m.T, 0, (chunk * p.H + h) * CH, sb + oT);
+        tc::bulk_commit();
+    }
+
+    // ---- W^T = k^T T1^T ; U^T = v^T T2^T ------------------------------------------------
+    if (tid == 0) {
+        constexpr uint32_t id = tc::idesc(128, 64, 1, 0);
+#pragma unroll
+        for (int k = 0; k < CH; k += 16)
+            tc::mma(tmem + R_W, tc::mdesc(st + oKQ, 128, 0, k), tc::kdesc(sb + oT1, 64, 0, k), id, k > 0);
+#pragma unroll
+        for (int k = 0; k < CH; k += 16)
+            tc::mma(tmem + R_U, tc::mdesc(st + oV, 64, 0, k), tc::kdesc(sb + oT2, 64, 0, k), id, k > 0);
+        tc::commit(mb);
+    }
+    if (has_next) prefetch_small(item + gridDim.x);  // raw values, first read at the next item's top
+    if (!wait_mma()) return;
+    {
+        float v[16];
+        uint32_t w[8];
+        tc::ld16(tl(R_W + c0), v);
+        pack8(v, w);
+        store_cm(sW2, w);  // bf16 W^T [d][s]: the A operand of W^T P^T and W's store
+        tc::ld16(tl(R_U + c0), v);
+        pack8(v, w);
+        store_cm(sKQ, w);  // U^T over the dead k / q tiles
+    }
+    sync_all();
+    if (tid == STORE_TID) {
+        tc::tma_store_2d(&m.W, 0, trow, sb + oW2);
+        tc::tma_store_2d(&m.U, 0, trow, st + oKQ);
+        tc::bulk_commit();
+    }
+
+    // ---- R^T = qd^T - W^T P^T ----------------------------------------------------------------
+    if (tid == 0) {
+        constexpr uint32_t id = tc::idesc(128, 64, 0, 0);
+#pragma unroll
+        for (int k = 0; k < CH; k += 16)
+            tc::mma(tmem + R_R, tc::kdesc(sb + oW2, 128, 0, k), tc::kdesc(sb + oP, 64, 0, k), id, k > 0);
+        tc::commit(mb);
+    }
+    // while the tensor cores run: kr = kn e^{gT-gc} over the dead v tile ; gT, e^{gT}
+    {
+        float v[16];
+        uint32_t w[8];
+        derived(false, 1.f, F_KR, v);
+        pack8(v, w);
+        store_cm(sV, w);
+        tc::fence_async_smem();
+        if (hc == 0) {
+            const float gt = G.gTv(0);
+            p.gT[((size_t)chunk * p.H + h) * PD + L] = gt;
+            p.egT[((size_t)chunk * p.H + h) * PD + L] = __expf(gt);
+        }
+    }
+    if (!wait_mma()) return;
+    if (tid == STORE_TID) {
+        tc::tma_store_2d(&m.Kr, 0, trow, st + oV);
+        tc::bulk_commit();
+    }
+    {
+        float acc[16], qd[16];
+        uint32_t w[8], wl[8];
+        tc::ld16(tl(R_R + c0), acc);
+        derived(true, p.scale, F_KD, qd);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float r0 = qd[2 * e] - acc[2 * e], r1 = qd[2 * e + 1] - acc[2 * e + 1];
+            w[e] = pack_bf16(r0, r1);
+            const float2 hf = unpack_bf16(w[e]);
+            wl[e] = pack_bf16(r0 - hf.x, r1 - hf.y);
+        }
+        store_cm(sKQ + TILE, w);  // R_hi over the dead k / q tiles
+        store_cm(sT1, wl);        // R_lo over the dead T1, T2
+        tc::fence_async_smem();
+    }
+    tc::fence_before();
+    __syncthreads();  // this item's shared tiles and tensor memory are free
+    tc::fence_after();
+    if (tid == STORE_TID) {
+        tc::tma_store_2d(&m.R, 0, trow, st + oKQ + TILE);
+        tc::tma_store_2d(&m.Rlo, 0, trow, sb + oT1);
+        tc::bulk_commit();
+    }
+    }
+    if (tid == STORE_TID) tc::bulk_wait_all();
+    tc::fence_before();
+    __syncthreads();
+    if (warp == 0) tc::dealloc(tmem, 512);
+}
+
+cudaError_t launch_prep_gdn(const Params& p, cudaStream_t s) {
+    PrepGdnMaps m;
+    const uint64_t T = (uint64_t)p.T_total;
+    const uint64_t trows = (uint64_t)p.max_chunks * p.H * PD;  // rows of the [D][C] per chunk-head tiles
+    const uint64_t crows = (uint64_t)p.max_chunks * p.H * CH;  // rows of the [C][C] per chunk-head tiles
+    if (!(encode_tokens_map(&m.q, p.q, T, p.Hk, PD) && encode_tokens_map(&m.k, p.k, T, p.Hk, PD) &&
+          encode_blocked_tokens_map(&m.v, p.v, T, p.H) && encode_rows_map(&m.W, p.W, trows, CH, PD) &&
+          encode_rows_map(&m.U, p.U, trows, CH, PD) && encode_rows_map(&m.Kr, p.Kr, trows, CH, PD) &&
+          encode_rows_map(&m.R, p.R, trows, CH, PD) && encode_rows_map(&m.Rlo, p.Rlo, trows, CH, PD) &&
+          encode_rows_map(&m.T, p.Tm, crows, CH, CH)))
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(k_prep_gdn, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    const int items = p.max_chunks * p.H;
+    const int ctas = items < num_sms() ? items : num_sms();
+    k_prep_gdn<<<ctas, 512, SMEM_BYTES, s>>>(p, m);
+    return cudaGetLastError();
+}
+
+}  // namespace gdr
