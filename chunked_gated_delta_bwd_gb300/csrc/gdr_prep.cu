@@ -227,7 +227,7 @@ static cudaError_t launch_prep_t(const Params& p, cudaStream_t s) {
 
 cudaError_t launch_prep(const Params& p, cudaStream_t s) {
     if (p.max_chunks == 0) return cudaSuccess;
-    if (p.D == 128) return launch_prep_tc(p, s);
+    if (p.D == 128) return p.kda ? launch_prep_kda(p, s) : launch_prep_gdn(p, s);
     return p.kda ? launch_prep_t<64, true>(p, s) : launch_prep_t<64, false>(p, s);
 }
 

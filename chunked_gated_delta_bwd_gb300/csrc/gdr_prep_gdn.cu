@@ -2,7 +2,7 @@
 // persistent CTAs of 16 warps, one per SM, each looping over (chunk, head) items; the
 // q, k, v tiles of the next item arrive by TMA into a second stage while the current item
 // is computed.  The quantities of the X/R form of the FlashQLA dh kernel ("FlashQLA ...
-// GDN 反向", §三), as the per-channel kernel in gdr_prep_tc.cu computes them:
+// GDN 反向", §三), as the per-channel kernel in gdr_prep_kda.cu computes them:
 //
 //   [A; P] = [kd'; qd'] ki'^T        A = strict_lower(diag(beta) .) (fp32), P = lower(.)
 //   T   = (I + A)^-1                  W^T = (beta kd)^T T^T       U^T = (beta V)^T T^T

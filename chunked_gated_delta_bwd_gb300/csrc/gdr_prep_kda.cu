@@ -1,30 +1,26 @@
-// Chunk-parallel preparation on tcgen05 for D = 128, GDN and KDA: persistent CTAs of
-// 16 warps, one per SM, each looping over (chunk, head) items; the q, k, v tiles of the
-// next item arrive by TMA into a second buffer while the current item is computed.
-// Same quantities as the warp-level kernel in gdr_prep.cu (the X/R form of the FlashQLA
-// dh kernel, "FlashQLA ... GDN 反向", §三):
+// Chunk-parallel preparation on tcgen05 for D = 128 with the per-channel (KDA) gate:
+// persistent CTAs of 16 warps, one per SM, each looping over (chunk, head) items; the q, k,
+// v tiles of the next item arrive by TMA into a second buffer while the current item is
+// computed.  Same quantities as the warp-level kernel in gdr_prep.cu (the X/R form of the
+// FlashQLA dh kernel, "FlashQLA ... GDN 反向", §三; the scalar gate has its own kernel,
+// gdr_prep_gdn.cu):
 //
 //   [A_raw; P] = [kd'; qd'] ki'^T       A = strict_lower(diag(beta) A_raw) (fp32), P = lower(.)
-//   T   = (I + A)^-1                     (blocked inverse to fp32 accuracy, below)
+//   T   = (I + A)^-1                     (blocked inverse to fp32 accuracy, gdr_invert.cuh)
 //   W^T = (beta kd)^T T^T                U^T = (beta V)^T T^T
 //   R^T = qd^T - W^T P^T                 (a bf16 pair R_hi + R_lo)
 //   kr  = kn e^{gT-gc}
 //
 // Products whose natural output is C x D are computed transposed (lane = channel), so
 // a thread owns one channel for 16 rows; W, U, Kr, R_hi and R_lo are written
-// channel-major ([D][C], 32 contiguous bytes per thread and row), the layout the
-// D = 128 state recurrence reads; T is written [C][C].  The raw q and k rows and (KDA)
-// the per-channel cumulative gate are staged in tensor memory once.
+// channel-major ([D][C]), the layout the D = 128 state recurrence reads; T is written
+// [C][C].  The raw q and k rows and e^{gc - ref} of the per-channel cumulative gate are
+// staged in tensor memory once.
 //
 // The inverse runs on warps 0-7 while warps 8-15 build the T-independent operands of the
-// next products: the 16 x 16 diagonal blocks by forward substitution (one thread per
-// column), then every 8-column strip of the block rows below its diagonal block by block
-// forward substitution, T_i = -T_ii sum_k A_ik T_k, with the 16 x 8 products on warp-level
-// tf32 tensor-core instructions (m16n8k8) in a three-term split (hi hi + hi lo + lo hi of
-// a = hi + lo), which keeps fp32 accuracy.  The shapes are too small for tcgen05 (M >= 64).
-// The next item's gates and beta logits are read one item ahead (KDA: the raw-gate tile
-// by TMA into the space of the dead fp32 matrices).  W, U, Kr, R_hi and R_lo are staged in
-// shared tiles that are dead by then and written by TMA stores.
+// next products.  The next item's beta logits and gate parameters are read one item ahead,
+// its raw-gate tile by TMA into the space of the dead fp32 matrices.  W, U, Kr, R_hi and
+// R_lo are staged in shared tiles that are dead by then and written by TMA stores.
 #include "gdr_chunk.cuh"
 #include "gdr_tc.cuh"
 #include "gdr_tma.h"
@@ -48,16 +44,16 @@ constexpr int oW1 = oW0 + TILE; // qd'^T [d][r] (G1, A block 1)
 constexpr int oW2 = oW1 + TILE; // ki'^T [d][s] (G1, B) -> W^T bf16 [d][s]
 constexpr int oP = oW2 + TILE;  // P [r][s] bf16
 constexpr int oT = oP + 8192;   // T [r][s] bf16
-constexpr int oA = oT + 8192;   // A fp32 [64][LDF] row-major; (KDA) the next item's raw gates before
+constexpr int oA = oT + 8192;   // A fp32 [64][LDF] row-major; the next item's raw gates before
 constexpr int oTf = oA + CH * LDF * 4;  // T fp32, transposed [c][r], stride LDF
 constexpr int oTmp = oTf + CH * LDF * 4;  // 8 warps' transfer tiles [8][XLD]
 constexpr int nTmp = 8 * 8 * XLD;
 constexpr int oSmall = (oTmp + nTmp * 4 + 1023) / 1024 * 1024;
 static_assert(oTmp + nTmp * 4 <= oSmall, "inversion scratch overlaps the small arrays");
 static_assert(CH * LDF * 4 >= TILE, "the raw-gate tile fits the space of A");
-static_assert(nTmp >= 4 * PD, "the KDA gate scan's minima fit the transfer tiles");
-constexpr int nInvQ = 64, nInvK = 64, nBeta = 64, nFac = 256, nGate = 128, nRef = 128, nGT = 128, nScan = 512;
-constexpr int SMALL_FLOATS = nInvQ + nInvK + nBeta + nFac + nGate + nRef + nGT + nScan;
+static_assert(nTmp >= 4 * PD, "the gate scan's minima fit the transfer tiles");
+constexpr int nInvQ = 64, nInvK = 64, nBeta = 64, nFac = 256, nRef = 128, nGT = 128, nScan = 512;
+constexpr int SMALL_FLOATS = nInvQ + nInvK + nBeta + nFac + nRef + nGT + nScan;
 constexpr int SMEM_BYTES = oSmall + SMALL_FLOATS * 4 + 64 + 1024;
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 constexpr uint32_t R_G1 = 0, R_W = 64, R_U = 128, R_R = 192, R_Q = 256, R_K = 320, R_G = 384;
@@ -72,8 +68,8 @@ constexpr int STORE_TID = 416;
 
 }  // namespace
 
-template <bool KDA, int GATE>
-__global__ void __launch_bounds__(512, 1) k_prep_tc(const Params p, const __grid_constant__ PrepMaps m) {
+template <int GATE>
+__global__ void __launch_bounds__(512, 1) k_prep_kda(const Params p, const __grid_constant__ PrepMaps m) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     const uint32_t sb = smem_u32(smem);
@@ -94,20 +90,14 @@ __global__ void __launch_bounds__(512, 1) k_prep_tc(const Params p, const __grid
     float* sInvQ = fsm;
     float* sInvK = sInvQ + nInvQ;
     float* sBeta = sInvK + nInvK;
-    float* sFac = sBeta + nBeta;  // GDN [4][64]; KDA [2][128] e^{ref}, e^{gT-ref} per channel
-    float* sGate = sFac + nFac;   // GDN gc[64], ref, gT
-    float* sRef = sGate + nGate;  // KDA ref[d]
-    float* sGT = sRef + nRef;     // KDA gT[d]
-    float* sScan = sGT + nGT;     // KDA [4][128]
+    float* sFac = sBeta + nBeta;  // [2][128] e^{ref}, e^{gT-ref} per channel
+    float* sRef = sFac + nFac;    // ref[d]
+    float* sGT = sRef + nRef;     // gT[d]
+    float* sScan = sGT + nGT;     // [4][128]
     uint64_t* mbars = reinterpret_cast<uint64_t*>(sScan + nScan);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(mbars + 4);
     const uint32_t mb = smem_u32(mbars), mload0 = smem_u32(mbars + 1);  // load barriers: one per stage
-    const uint32_t mgr = smem_u32(mbars + 3);                            // (KDA) the raw-gate tile
-
-    Gates<PD, false> G;
-    G.gc = sGate;
-    G.ref = sGate + CH;
-    G.gT = sGate + CH + 1;
+    const uint32_t mgr = smem_u32(mbars + 3);                            // the raw-gate tile
 
     // q, k, v of item `it` into stage s: copy `which` (0 q, 1 k, 2 v) or all (which < 0); the
     // copies may be issued by different threads in any order (the barrier's transaction
@@ -124,7 +114,7 @@ __global__ void __launch_bounds__(512, 1) k_prep_tc(const Params p, const __grid
         if (which < 0 || which == 1) tc::tma_load_4d(st + oK, &m.k, 0, qk_head(p, hh), t0, 0, bar);
         if (which < 0 || which == 2) tc::tma_load_4d(st + oV, &m.v, 0, hh, t0, 0, bar);
     };
-    // (KDA) raw gates of `item`, token-major, into the space of A (dead from the end of the
+    // raw gates of `item`, token-major, into the space of A (dead from the end of the
     // inversion to the next item's G1)
     auto issue_gate_load = [&](int item) {
         ChunkInfo cj;
@@ -140,7 +130,7 @@ __global__ void __launch_bounds__(512, 1) k_prep_tc(const Params p, const __grid
         tc::mbar_init(mgr, 1);
         if ((int)blockIdx.x < n_items) {
             issue_loads(blockIdx.x, 0, -1);
-            if (KDA) issue_gate_load(blockIdx.x);
+            issue_gate_load(blockIdx.x);
         }
     }
     // T's blocks above the diagonal stay zero in the shared tile
@@ -161,7 +151,7 @@ __global__ void __launch_bounds__(512, 1) k_prep_tc(const Params p, const __grid
     };
     int pending = -1;  // stage with a load in flight that this item does not consume, or -1
     uint32_t pending_par = 0;
-    bool pending_g = KDA && (int)blockIdx.x < n_items;  // (KDA) a raw-gate tile is in flight
+    bool pending_g = (int)blockIdx.x < n_items;  // a raw-gate tile is in flight
     auto bail = [&]() {
         if (tid == 0) {
             atomicOr(p.status, ST_MMA_TIMEOUT);
@@ -183,11 +173,10 @@ __global__ void __launch_bounds__(512, 1) k_prep_tc(const Params p, const __grid
         }
         return true;
     };
-    // the next item's beta logit (thread r < 64), GDN gates (first warp, rows 2 lane and
-    // 2 lane + 1) and KDA gate parameters (every thread: its channel), read one item ahead
-    // as raw values (rows clamped into the chunk) that are first read at the next item's
-    // top, so no thread waits for them
-    float pg0 = 0.f, pg1 = 0.f, pbias = 0.f, palog = 0.f;
+    // the next item's beta logit (thread r < 64) and gate parameters (every thread: its
+    // channel), read one item ahead as raw values (row clamped into the chunk) that are
+    // first read at the next item's top, so no thread waits for them
+    float pbias = 0.f, palog = 0.f;
     unsigned short pb = 0;
     auto prefetch_small = [&](int item) {
         ChunkInfo cj;
@@ -195,14 +184,9 @@ __global__ void __launch_bounds__(512, 1) k_prep_tc(const Params p, const __grid
         const int hh = item % p.H;
         if (tid < CH)
             pb = reinterpret_cast<const unsigned short*>(p.beta_logit)[(cj.t0 + min(tid, cj.len - 1)) * p.H + hh];
-        if (!KDA && tid < 32) {
-            pg0 = p.g[(cj.t0 + min(2 * tid, cj.len - 1)) * p.H + hh];
-            pg1 = p.g[(cj.t0 + min(2 * tid + 1, cj.len - 1)) * p.H + hh];
-        }
-        if (KDA) {
-            pbias = p.dt_bias[hh * PD + L];
-            palog = p.A_log[hh];
-        }
+        pbias = p.dt_bias[hh * PD + L];
+        palog = p.A_log[hh];
+    
     };
     if ((int)blockIdx.x < n_items) prefetch_small(blockIdx.x);
     // a[cq .. cq+15]
@@ -245,15 +229,13 @@ __global__ void __launch_bounds__(512, 1) k_prep_tc(const Params p, const __grid
         pending = stg ^ 1;
         pending_par = (uint32_t)(((it + 1) >> 1) & 1);
     }
-    if constexpr (!KDA)
-        if (tid < 32) gdn_gate_scan(2 * tid < ci.len ? pg0 : 0.f, 2 * tid + 1 < ci.len ? pg1 : 0.f, G, true, p);
     if (tid < CH) sBeta[tid] = tid < ci.len ? sigmoid_f(__bfloat162float(__ushort_as_bfloat16(pb))) : 0.f;
 
-    // KDA: per-channel log gates of this thread's channel and rows (raw gates from the
+    // per-channel log gates of this thread's channel and rows (raw gates from the
     // token-major tile in the space of A), scanned across the four row quarters, staged in
     // tensor memory; the gate-range check of the chunk
     float refL = 0.f, gTL = 0.f;
-    if constexpr (KDA) {
+    {
         const float a = expf(palog);
         const float bias = pbias;
         {
@@ -327,7 +309,7 @@ __global__ void __launch_bounds__(512, 1) k_prep_tc(const Params p, const __grid
         }
     }
     __syncthreads();
-    if constexpr (KDA) {  // e^{gc - ref} of this thread's channel and rows replaces gc in tensor memory
+    {  // e^{gc - ref} of this thread's channel and rows replaces gc in tensor memory
         refL = sRef[L];
         gTL = sGT[L];
         float g[16];
@@ -353,14 +335,6 @@ __global__ void __launch_bounds__(512, 1) k_prep_tc(const Params p, const __grid
         s += __shfl_xor_sync(0xffffffffu, s, 2);
         if (part == 0) (tid < 256 ? sInvQ : sInvK)[r] = rsqrtf(s + 1e-6f);
     }
-    if constexpr (!KDA) {
-        for (int r = tid; r < CH; r += 512) {
-            sFac[0 * CH + r] = gate_factor<F_KD>(G, r, 0);
-            sFac[1 * CH + r] = gate_factor<F_KDP>(G, r, 0);
-            sFac[2 * CH + r] = gate_factor<F_KIP>(G, r, 0);
-            sFac[3 * CH + r] = gate_factor<F_KR>(G, r, 0);
-        }
-    }
     {  // raw q and k of this thread's channel and rows into tensor memory
         const int lch = (L & 63) >> 3, lsub = (L & 7) << 1;
         float qs[16], ks[16];
@@ -377,7 +351,7 @@ __global__ void __launch_bounds__(512, 1) k_prep_tc(const Params p, const __grid
 
     // gate factors of this thread's channel and rows cq .. cq+15
     auto factors = [&](int kind, float (&f)[16], int cq) {
-        if constexpr (KDA) {
+        {
             // e^{gc-ref} from tensor memory; e^{gc} = e^{gc-ref} e^{ref}, e^{ref-gc} = 1 / e^{gc-ref},
             // e^{gT-gc} = e^{gT-ref} / e^{gc-ref} (|gc - ref| <= 80: no overflow)
             const float eRef = sFac[L], eGTref = sFac[PD + L];
@@ -390,8 +364,6 @@ __global__ void __launch_bounds__(512, 1) k_prep_tc(const Params p, const __grid
                 else if (kind == F_KIP) f[i] = __fdividef(1.f, e[i]);
                 else f[i] = __fdividef(eGTref, e[i]);
             }
-        } else {
-            rows16(sFac + kind * CH, f, cq);
         }
     };
     // x (raw q or k of this channel and rows cq ..) * m_r * f, m_r = inv_r * mul * rowmul_r
@@ -485,9 +457,9 @@ __global__ void __launch_bounds__(512, 1) k_prep_tc(const Params p, const __grid
         }
     }
     sync_all();
-    if (has_next) {  // the space of A is free: the next item's small inputs and (KDA) raw gates
-        if (KDA && tid == 0) issue_gate_load(item + gridDim.x);
-        pending_g = KDA;
+    if (has_next) {  // the space of A is free: the next item's small inputs and raw gates
+        if (tid == 0) issue_gate_load(item + gridDim.x);
+        pending_g = true;
         prefetch_small(item + gridDim.x);
     }
 
@@ -538,7 +510,7 @@ __global__ void __launch_bounds__(512, 1) k_prep_tc(const Params p, const __grid
         store_cm(sV, w, c0);
         tc::fence_async_smem();
         if (hc == 0) {
-            const float gt = KDA ? gTL : G.gTv(0);
+            const float gt = gTL;
             p.gT[((size_t)chunk * p.H + h) * PD + L] = gt;
             p.egT[((size_t)chunk * p.H + h) * PD + L] = __expf(gt);
         }
@@ -579,29 +551,29 @@ __global__ void __launch_bounds__(512, 1) k_prep_tc(const Params p, const __grid
     if (warp == 0) tc::dealloc(tmem, 512);
 }
 
-template <bool KDA, int GATE>
-static cudaError_t launch_prep_tc_t(const Params& p, cudaStream_t s) {
+template <int GATE>
+static cudaError_t launch_prep_kda_t(const Params& p, cudaStream_t s) {
     PrepMaps m;
     const uint64_t T = (uint64_t)p.T_total;
     const uint64_t trows = (uint64_t)p.max_chunks * p.H * PD;  // rows of the [D][C] per chunk-head tiles
     if (!(encode_blocked_tokens_map(&m.q, p.q, T, p.Hk) && encode_blocked_tokens_map(&m.k, p.k, T, p.Hk) &&
           encode_blocked_tokens_map(&m.v, p.v, T, p.H) &&
-          encode_blocked_tokens_map(&m.graw, KDA ? p.g_raw : nullptr, T, p.H) &&
+          encode_blocked_tokens_map(&m.graw, p.g_raw, T, p.H) &&
           encode_rows_map(&m.W, p.W, trows, CH, PD) && encode_rows_map(&m.U, p.U, trows, CH, PD) &&
           encode_rows_map(&m.Kr, p.Kr, trows, CH, PD) && encode_rows_map(&m.R, p.R, trows, CH, PD) &&
           encode_rows_map(&m.Rlo, p.Rlo, trows, CH, PD)))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(k_prep_tc<KDA, GATE>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(k_prep_kda<GATE>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int items = p.max_chunks * p.H;
     const int ctas = items < num_sms() ? items : num_sms();
-    k_prep_tc<KDA, GATE><<<ctas, 512, SMEM_BYTES, s>>>(p, m);
+    k_prep_kda<GATE><<<ctas, 512, SMEM_BYTES, s>>>(p, m);
     return cudaGetLastError();
 }
 
-cudaError_t launch_prep_tc(const Params& p, cudaStream_t s) {
-    if (!p.kda) return launch_prep_gdn(p, s);
-    return p.kda_gate == 0 ? launch_prep_tc_t<true, 0>(p, s) : launch_prep_tc_t<true, 1>(p, s);
+cudaError_t launch_prep_kda(const Params& p, cudaStream_t s) {
+    // the KDA gate function is a template parameter: each instance carries only its own code
+    return p.kda_gate == 0 ? launch_prep_kda_t<0>(p, s) : launch_prep_kda_t<1>(p, s);
 }
 
 }  // namespace gdr
