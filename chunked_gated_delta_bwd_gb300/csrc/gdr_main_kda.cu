@@ -144,14 +144,18 @@ __global__ void __launch_bounds__(512, 1) k_main_kda(const Params p, const __gri
     bool pending = (int)blockIdx.x < n_items;  // a load batch is in flight
     uint32_t pend_par = 0;                     // ... on this phase parity of the load barrier
     bool pending_g = false;                    // a raw gate tile is in flight
-    // the next item's beta logit (thread r < 64), loaded one item ahead as a raw value (row
-    // clamped into the chunk) first read at the next item's top, so no thread waits for it
+    // the next item's beta logit (thread r < 64, a raw value, row clamped into the chunk) and
+    // gate parameters, loaded one item ahead and first read at the next item's top, so no
+    // thread waits for them
     unsigned short pb = 0;
+    float palog = 0.f, pbias = 0.f;  // the next item's gate parameters (this thread's channel)
     auto prefetch_small = [&](int item) {
+        const int hh = item % p.H;
+        palog = p.A_log[hh];
+        pbias = p.dt_bias[hh * MD + L];
         if (tid >= CH) return;
         ChunkInfo cj;
         lookup_chunk(item / p.H, p.N, p.chunk_off, p.cu_seqlens, p.seq_len, cj);
-        const int hh = item % p.H;
         pb = reinterpret_cast<const unsigned short*>(p.beta_logit)[(cj.t0 + min(tid, cj.len - 1)) * p.H + hh];
     };
     if ((int)blockIdx.x < n_items) prefetch_small(blockIdx.x);
@@ -249,8 +253,7 @@ __global__ void __launch_bounds__(512, 1) k_main_kda(const Params p, const __gri
     ChunkInfo ci;
     lookup_chunk(chunk, p.N, p.chunk_off, p.cu_seqlens, p.seq_len, ci);
     if (tid < CH) sBeta[tid] = tid < ci.len ? sigmoid_f(__bfloat162float(__ushort_as_bfloat16(pb))) : 0.f;
-    // gate parameters, read while the operand tiles land
-    const float alog = p.A_log[h], bias = p.dt_bias[h * MD + L];
+    const float alog = palog, bias = pbias;  // gate parameters, loaded one item ahead
 
     // wait for the operand tiles; rows past the chunk's end read as zero
     {
