@@ -34,8 +34,8 @@ constexpr int TILE = CH * PD * 2;  // 16 KB
 // shared-memory map (bytes from the 1024-aligned base); two input stages
 constexpr int STAGE = 3 * TILE;
 constexpr int oKQ = 0;            // [k; q] token-major, 128 rows -> U^T staged [j][s] (+16 KB: R_hi^T [d][r])
-constexpr int oV = 2 * TILE;      // v token-major -> kr staged [d][r]
-constexpr int oW2 = 2 * STAGE;    // W^T bf16 [d][s] (R's operand, W's store)
+constexpr int oV = 2 * TILE;      // v token-major
+constexpr int oW2 = 2 * STAGE;    // kr staged [d][r] -> W^T bf16 [d][s] (R's operand, W's store)
 constexpr int oP = oW2 + TILE;    // P [r][s] bf16
 constexpr int oT = oP + 8192;     // T [r][s] bf16 (blocks above the diagonal stay zero)
 constexpr int oT1 = oT + 8192;    // T diag(beta invk e^{gc}) [r][s] bf16 -> (with T2's space) R_lo^T staged
@@ -187,18 +187,18 @@ __global__ void __launch_bounds__(512, 1) k_prep_gdn(const Params p, const __gri
 #pragma unroll
         for (int e = 0; e < 8; ++e) w[e] = pack_bf16(v[2 * e], v[2 * e + 1]);
     };
-    // row L, columns c0 .. c0+15 of a channel-major [128][64] shared tile
-    auto store_cm = [&](unsigned char* tile, const uint32_t (&w)[8]) {
-        *reinterpret_cast<uint4*>(tile + tc::sw_chunk(L, c0 >> 3, 128)) = make_uint4(w[0], w[1], w[2], w[3]);
-        *reinterpret_cast<uint4*>(tile + tc::sw_chunk(L, (c0 >> 3) + 1, 128)) = make_uint4(w[4], w[5], w[6], w[7]);
+    // row L, columns cq .. cq+15 of a channel-major [128][64] shared tile
+    auto store_cm = [&](unsigned char* tile, const uint32_t (&w)[8], int cq) {
+        *reinterpret_cast<uint4*>(tile + tc::sw_chunk(L, cq >> 3, 128)) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(tile + tc::sw_chunk(L, (cq >> 3) + 1, 128)) = make_uint4(w[4], w[5], w[6], w[7]);
     };
-    // raw q (or k) of this thread's channel and rows (staged in tensor memory) times the
-    // rows' inverse norm, the multiplier and the gate factor `kind`
-    auto derived = [&](bool isq, float mul, int kind, float (&o)[16]) {
+    // raw q (or k) of this thread's channel and rows cq .. cq+15 (staged in tensor memory)
+    // times the rows' inverse norm, the multiplier and the gate factor `kind`
+    auto derived = [&](bool isq, float mul, int kind, float (&o)[16], int cq) {
         float f[16], inv[16];
-        rows16(sFac + kind * CH, f, c0);
-        tc::ld16(tl((isq ? R_Q : R_K) + c0), o);
-        rows16(isq ? sInvQ : sInvK, inv, c0);
+        rows16(sFac + kind * CH, f, cq);
+        tc::ld16(tl((isq ? R_Q : R_K) + cq), o);
+        rows16(isq ? sInvQ : sInvK, inv, cq);
 #pragma unroll
         for (int i = 0; i < 16; ++i) o[i] = o[i] * derived_m(inv[i], mul, 1.f) * f[i];
     };
@@ -326,8 +326,31 @@ __global__ void __launch_bounds__(512, 1) k_prep_gdn(const Params p, const __gri
         }
     }
     __syncthreads();
-    if (warp < 8) inv::invert_tc(sA, sTf, sTmp, sT, nullptr);  // warps 8-15 wait at the barrier
-    __syncthreads();  // T complete (fp32 transposed in sTf, bf16 in sT)
+    if (warp < 8) {
+        inv::invert_tc(sA, sTf, sTmp, sT, nullptr);
+    } else {
+        // meanwhile: kr = kn e^{gT-gc} (this warp's lanes, row quarters hc - 2 and hc) into the
+        // W^T tile, which W's epilogue fills only after kr's store has read it; gT, e^{gT}
+        uint32_t w[8];
+        for (int pass = 0; pass < 2; ++pass) {
+            const int cq = 16 * (hc - 2 + 2 * pass);
+            float v[16];
+            derived(false, 1.f, F_KR, v, cq);
+            pack8(v, w);
+            store_cm(sW2, w, cq);
+        }
+        tc::fence_async_smem();
+        if (hc == 2) {
+            const float gt = G.gTv(0);
+            p.gT[((size_t)chunk * p.H + h) * PD + L] = gt;
+            p.egT[((size_t)chunk * p.H + h) * PD + L] = __expf(gt);
+        }
+    }
+    __syncthreads();  // T complete (fp32 transposed in sTf, bf16 in sT); kr staged
+    if (tid == STORE_TID) {
+        tc::tma_store_2d(&m.Kr, 0, trow, sb + oW2);
+        tc::bulk_commit();
+    }
     {
         // T diag(beta invk e^{gc}) -> T1 and T diag(beta) -> T2 (bf16 [r][s]), the B operands of
         // W^T = k^T T1^T and U^T = v^T T2^T; thread: row r, 16 columns, one of the two copies
@@ -361,16 +384,17 @@ __global__ void __launch_bounds__(512, 1) k_prep_gdn(const Params p, const __gri
         tc::commit(mb);
     }
     if (has_next) prefetch_small(item + gridDim.x);  // raw values, first read at the next item's top
+    if (tid == STORE_TID) tc::bulk_wait_read();  // kr's store has read the W^T tile
     if (!wait_mma()) return;
     {
         float v[16];
         uint32_t w[8];
         tc::ld16(tl(R_W + c0), v);
         pack8(v, w);
-        store_cm(sW2, w);  // bf16 W^T [d][s]: the A operand of W^T P^T and W's store
+        store_cm(sW2, w, c0);  // bf16 W^T [d][s]: the A operand of W^T P^T and W's store
         tc::ld16(tl(R_U + c0), v);
         pack8(v, w);
-        store_cm(sKQ, w);  // U^T over the dead k / q tiles
+        store_cm(sKQ, w, c0);  // U^T over the dead k / q tiles
     }
     sync_all();
     if (tid == STORE_TID) {
@@ -387,30 +411,12 @@ __global__ void __launch_bounds__(512, 1) k_prep_gdn(const Params p, const __gri
             tc::mma(tmem + R_R, tc::kdesc(sb + oW2, 128, 0, k), tc::kdesc(sb + oP, 64, 0, k), id, k > 0);
         tc::commit(mb);
     }
-    // while the tensor cores run: kr = kn e^{gT-gc} over the dead v tile ; gT, e^{gT}
-    {
-        float v[16];
-        uint32_t w[8];
-        derived(false, 1.f, F_KR, v);
-        pack8(v, w);
-        store_cm(sV, w);
-        tc::fence_async_smem();
-        if (hc == 0) {
-            const float gt = G.gTv(0);
-            p.gT[((size_t)chunk * p.H + h) * PD + L] = gt;
-            p.egT[((size_t)chunk * p.H + h) * PD + L] = __expf(gt);
-        }
-    }
     if (!wait_mma()) return;
-    if (tid == STORE_TID) {
-        tc::tma_store_2d(&m.Kr, 0, trow, st + oV);
-        tc::bulk_commit();
-    }
     {
         float acc[16], qd[16];
         uint32_t w[8], wl[8];
         tc::ld16(tl(R_R + c0), acc);
-        derived(true, p.scale, F_KD, qd);
+        derived(true, p.scale, F_KD, qd, c0);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             const float r0 = qd[2 * e] - acc[2 * e], r1 = qd[2 * e + 1] - acc[2 * e + 1];
@@ -418,8 +424,8 @@ __global__ void __launch_bounds__(512, 1) k_prep_gdn(const Params p, const __gri
             const float2 hf = unpack_bf16(w[e]);
             wl[e] = pack_bf16(r0 - hf.x, r1 - hf.y);
         }
-        store_cm(sKQ + TILE, w);  // R_hi over the dead k / q tiles
-        store_cm(sT1, wl);        // R_lo over the dead T1, T2
+        store_cm(sKQ + TILE, w, c0);  // R_hi over the dead k / q tiles
+        store_cm(sT1, wl, c0);        // R_lo over the dead T1, T2
         tc::fence_async_smem();
     }
     tc::fence_before();
