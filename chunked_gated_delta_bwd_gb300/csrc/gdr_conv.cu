@@ -27,7 +27,7 @@ namespace {
 
 constexpr int CONV_TILE = 128;   // tokens per tile
 constexpr int CONV_THREADS = 128;
-constexpr int CONV_U = 16;       // tokens whose loads are issued together (interior tiles)
+constexpr int CONV_U = 8;        // tokens whose loads are issued together (interior tiles)
 
 __device__ __forceinline__ float2 ld_pair(const uint32_t* p) { return unpack_bf16(__ldg(p)); }
 
@@ -85,7 +85,7 @@ struct ConvLane {
 }  // namespace
 
 template <int K>
-__global__ void __launch_bounds__(CONV_THREADS) k_conv1d_bwd(const ConvParams p) {
+__global__ void __launch_bounds__(CONV_THREADS, 8) k_conv1d_bwd(const ConvParams p) {
     const int c0 = (blockIdx.x * CONV_THREADS + threadIdx.x) * 2;  // channels c0, c0 + 1
     if (c0 >= p.C) return;
     const int64_t ch = p.C / 2;  // row stride in channel pairs
@@ -193,22 +193,32 @@ __global__ void __launch_bounds__(CONV_THREADS) k_conv1d_bwd(const ConvParams p)
     }
 }
 
-cudaError_t launch_conv1d_bwd(const ConvParams& p, cudaStream_t s) {
-    if (p.T == 0) return cudaSuccess;
+template <int K>
+static cudaError_t launch_conv1d_bwd_t(const ConvParams& p, cudaStream_t s) {
+    // one wave: as many blocks as fit on the SMs at once (the blocks loop over token tiles)
     const int gx = (p.C / 2 + CONV_THREADS - 1) / CONV_THREADS;
     const int64_t ntiles = (p.T + CONV_TILE - 1) / CONV_TILE;
-    int64_t gy = (8 * (int64_t)num_sms() + gx - 1) / gx;  // about eight blocks per SM
+    int per_sm = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_conv1d_bwd<K>, CONV_THREADS, 0);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) per_sm = 1;
+    int64_t gy = (int64_t)per_sm * num_sms() / gx;
+    if (gy < 1) gy = 1;
     if (gy > ntiles) gy = ntiles;
     if (gy > 65535) gy = 65535;
-    dim3 grid(gx, (unsigned)gy);
+    k_conv1d_bwd<K><<<dim3(gx, (unsigned)gy), CONV_THREADS, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_conv1d_bwd(const ConvParams& p, cudaStream_t s) {
+    if (p.T == 0) return cudaSuccess;
     switch (p.K) {
-        case 1: k_conv1d_bwd<1><<<grid, CONV_THREADS, 0, s>>>(p); break;
-        case 2: k_conv1d_bwd<2><<<grid, CONV_THREADS, 0, s>>>(p); break;
-        case 3: k_conv1d_bwd<3><<<grid, CONV_THREADS, 0, s>>>(p); break;
-        case 4: k_conv1d_bwd<4><<<grid, CONV_THREADS, 0, s>>>(p); break;
+        case 1: return launch_conv1d_bwd_t<1>(p, s);
+        case 2: return launch_conv1d_bwd_t<2>(p, s);
+        case 3: return launch_conv1d_bwd_t<3>(p, s);
+        case 4: return launch_conv1d_bwd_t<4>(p, s);
         default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 }  // namespace gdr
