@@ -137,7 +137,9 @@ static gdr_status check_shape(const gdr_shape* sh) {
         return fail(GDR_ERR_INVALID, "gate_scale must be finite and <= 0 (a decaying gate)");
     const int64_t N = sh->num_seqs, T = sh->total_tokens;
     const int64_t mc = sh->cu_seqlens ? (T + (CH - 1) * N) / CH : N * ((T / N + CH - 1) / CH);
-    if (mc > (int64_t)1 << 30 || N * sh->num_heads * (sh->head_dim / 16) > ((int64_t)1 << 31) - 1)
+    // (the kernels address per chunk-head tiles by 32-bit row: chunk-heads x 128 rows must fit)
+    if (mc > (int64_t)1 << 30 || N * sh->num_heads * (sh->head_dim / 16) > ((int64_t)1 << 31) - 1 ||
+        mc * sh->num_heads * 128 > ((int64_t)1 << 31) - 1)
         return fail(GDR_ERR_INVALID, "problem too large for one call");
     return GDR_OK;
 }
