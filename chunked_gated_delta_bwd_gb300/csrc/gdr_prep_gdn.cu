@@ -1,7 +1,6 @@
 // Chunk-parallel preparation on tcgen05 for D = 128 with the scalar (GDN) gate:
-// persistent CTAs of 16 warps, one per SM, each looping over (chunk, head) items; the
-// q, k, v tiles of the next item arrive by TMA into a second stage while the current item
-// is computed.  The quantities of the X/R form of the FlashQLA dh kernel ("FlashQLA ...
+// persistent CTAs of 16 warps, one per SM, each looping over (chunk, head) items, with two
+// input stages.  The quantities of the X/R form of the FlashQLA dh kernel ("FlashQLA ...
 // GDN 反向", §三), as the per-channel kernel in gdr_prep_kda.cu computes them:
 //
 //   [A; P] = [kd'; qd'] ki'^T        A = strict_lower(diag(beta) .) (fp32), P = lower(.)
@@ -11,13 +10,19 @@
 // With one log gate per token every gated tile is a row scaling of the raw q or k tile,
 // so, as in the scalar-gate main kernel, the products read the raw bf16 tiles as loaded
 // (k and q stacked into one 128-row tile) and the row factors are applied in fp32:
-//   G1  [A; P]_raw = [k; q] k^T, issued as soon as the tiles land (under the norms and
-//       the gate factors), then A = G1 x beta_r invk_r e^{gc_r-ref} x invk_s e^{ref-gc_s}
+//   G1  [A; P]_raw = [k; q] k^T, then A = G1 x beta_r invk_r e^{gc_r-ref} x invk_s e^{ref-gc_s}
 //       and P = G1 x scale invq_r e^{gc_r-ref} x invk_s e^{ref-gc_s};
 //   W^T = k^T (T diag(beta invk e^{gc}))^T and U^T = v^T (T diag(beta))^T: the column
 //       factors go into two bf16 copies of T, no (beta kd)^T or (beta V)^T tile is built.
-// W, U, Kr, R_hi, R_lo and T are staged in shared tiles that are dead by then and written
-// by TMA stores; one thread issues those stores and the next item's copies.
+//
+// Schedule of one item: the row norms, gate factors and combined row factors (all warps);
+// E1 (A, P) from G1; then warps 0..7 invert T while warps 8..15 build kr and run the NEXT
+// item's front part: the wait for its tiles, its raw q, k rows into tensor memory, its gates
+// and beta, and its G1 issued on the raw tiles (small arrays and those tensor-memory columns
+// are kept per item parity); then T1, T2, the W / U product, R.  A stage's tiles are last
+// read by the W / U product, after which the tiles of the item after next are loaded into it.
+// W, U, Kr, R_hi, R_lo and T are staged in shared tiles that are dead by then (none in an
+// input stage) and written by TMA stores that one thread issues.
 #include "gdr_chunk.cuh"
 #include "gdr_invert.cuh"
 #include "gdr_tc.cuh"
@@ -33,28 +38,37 @@ constexpr int PD = 128;
 constexpr int TILE = CH * PD * 2;  // 16 KB
 // shared-memory map (bytes from the 1024-aligned base); two input stages
 constexpr int STAGE = 3 * TILE;
-constexpr int oKQ = 0;            // [k; q] token-major, 128 rows -> U^T staged [j][s] (+16 KB: R_hi^T [d][r])
+constexpr int oKQ = 0;            // [k; q] token-major, 128 rows
 constexpr int oV = 2 * TILE;      // v token-major
 constexpr int oW2 = 2 * STAGE;    // kr staged [d][r] -> W^T bf16 [d][s] (R's operand, W's store)
 constexpr int oP = oW2 + TILE;    // P [r][s] bf16
 constexpr int oT = oP + 8192;     // T [r][s] bf16 (blocks above the diagonal stay zero)
 constexpr int oT1 = oT + 8192;    // T diag(beta invk e^{gc}) [r][s] bf16 -> (with T2's space) R_lo^T staged
 constexpr int oT2 = oT1 + 8192;   // T diag(beta) [r][s] bf16
-constexpr int oA = oT2 + 8192;    // A fp32 [64][LDF] row-major
-constexpr int oTf = oA + CH * LDF * 4;    // T fp32, transposed [c][r], stride LDF
+constexpr int oA = oT2 + 8192;    // A fp32 [64][LDF] row-major -> U^T staged [j][s]
+static_assert(oA % 1024 == 0, "U's staging tile is 128-byte swizzled");
+constexpr int oTf = oA + CH * LDF * 4;    // T fp32, transposed [c][r], stride LDF -> R_hi^T staged [d][r]
+static_assert(oTf % 1024 == 0, "R_hi's staging tile is 128-byte swizzled");
 constexpr int oTmp = oTf + CH * LDF * 4;  // 8 warps' transfer tiles [8][XLD]
 constexpr int nTmp = 8 * 8 * XLD;
 constexpr int oSmall = (oTmp + nTmp * 4 + 1023) / 1024 * 1024;
-constexpr int nInvQ = 64, nInvK = 64, nBeta = 64, nFac = 4 * 64, nTab = 4 * 64, nGate = 66, nPad = 62;
-constexpr int SMALL_FLOATS = nInvQ + nInvK + nBeta + nFac + nTab + nGate + nPad;
+// one set per item parity (an item's front part fills its set while the item before it is
+// still in flight): inverse norms of q and k, beta, gate factors, gates gc[64], ref, gT
+constexpr int nInvQ = 64, nInvK = 64, nBeta = 64, nFac = 4 * 64, nGate = 68;
+constexpr int nPar = nInvQ + nInvK + nBeta + nFac + nGate;
+constexpr int nTab = 4 * 64, nPad = 8;
+constexpr int SMALL_FLOATS = 2 * nPar + nTab + nPad;
 constexpr int SMEM_BYTES = oSmall + SMALL_FLOATS * 4 + 64 + 1024;
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
-constexpr uint32_t R_G1 = 0, R_W = 64, R_U = 128, R_R = 192, R_Q = 256, R_K = 320;
+static_assert(nPar % 4 == 0, "16-byte aligned per-parity arrays");
+// tensor-memory columns; raw q, k rows of item parity x at R_Q0 + 128 x, R_K0 + 128 x
+constexpr uint32_t R_G1 = 0, R_W = 64, R_U = 128, R_R = 192, R_Q0 = 256, R_K0 = 320;
 // combined row-factor tables (each [64])
 enum Tab { T_CF = 0, T_RA = 1, T_RP = 2, T_CW = 3 };
-// The thread that issues the TMA stores of W, U, Kr, R_hi, R_lo and T and the copies of the
-// next item's q, k and v: its stores read the stage that those copies overwrite, and a bulk
-// store's completion is visible only to the thread that issued it.
+// The thread that issues the TMA stores of W, U, Kr, R_hi, R_lo and T (a bulk store's
+// completion is visible only to the thread that issued it, so it also waits for their reads
+// of the staging tiles before those are rewritten) and the q, k, v copies (a warp 8..15
+// thread, so that the next item's front clears its record of a copy in flight).
 constexpr int STORE_TID = 416;
 
 struct PrepGdnMaps {
@@ -81,40 +95,47 @@ __global__ void __launch_bounds__(512, 1) k_prep_gdn(const Params p, const __gri
     float* sTf = reinterpret_cast<float*>(smem + oTf);
     float* sTmp = reinterpret_cast<float*>(smem + oTmp);
     float* fsm = reinterpret_cast<float*>(smem + oSmall);
-    float* sInvQ = fsm;
-    float* sInvK = sInvQ + nInvQ;
-    float* sBeta = sInvK + nInvK;
-    float* sFac = sBeta + nBeta;  // [4][64] e^{gc}, e^{gc-ref}, e^{ref-gc}, e^{gT-gc} (Fac order)
-    float* sTab = sFac + nFac;    // [4][64] combined row factors (Tab order)
-    float* sGate = sTab + nTab;   // gc[64], ref, gT
-    uint64_t* mbars = reinterpret_cast<uint64_t*>(sGate + nGate + nPad);
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbars + 3);
-    const uint32_t mb = smem_u32(mbars), mload0 = smem_u32(mbars + 1);  // load barriers: one per stage
-
-    Gates<PD, false> G;
-    G.gc = sGate;
-    G.ref = sGate + CH;
-    G.gT = sGate + CH + 1;
+    // per-parity small arrays of the item with parity x
+    auto sInvQ = [&](int x) { return fsm + x * nPar; };
+    auto sInvK = [&](int x) { return fsm + x * nPar + nInvQ; };
+    auto sBeta = [&](int x) { return fsm + x * nPar + nInvQ + nInvK; };
+    auto sFac = [&](int x) {  // [4][64] e^{gc}, e^{gc-ref}, e^{ref-gc}, e^{gT-gc} (Fac order)
+        return fsm + x * nPar + nInvQ + nInvK + nBeta;
+    };
+    auto gates = [&](int x) {
+        Gates<PD, false> G;
+        G.gc = fsm + x * nPar + nInvQ + nInvK + nBeta + nFac;
+        G.ref = G.gc + CH;
+        G.gT = G.gc + CH + 1;
+        return G;
+    };
+    float* sTab = fsm + 2 * nPar;  // [4][64] combined row factors of the current item (Tab order)
+    uint64_t* mbars = reinterpret_cast<uint64_t*>(sTab + nTab + nPad);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbars + 4);
+    // product barrier, load barriers (one per stage), G1 barrier
+    const uint32_t mb = smem_u32(mbars), mload0 = smem_u32(mbars + 1), mg1 = smem_u32(mbars + 3);
 
     // q, k, v of `item` into stage `stg`: k and q stacked into one 128-row tile, one 64-column
-    // box at a time, v as two column blocks
-    auto issue_loads = [&](int item, int stg) {
+    // box at a time, v as two column blocks; copy `which` (0..4; the barrier's byte count goes
+    // with copy 4), or all five for which < 0
+    auto issue_loads = [&](int item, int stg, int which) {
         ChunkInfo cj;
         lookup_chunk(item / p.H, p.N, p.chunk_off, p.cu_seqlens, p.seq_len, cj);
         const int hh = item % p.H, hk = qk_head(p, hh), t0 = (int)cj.t0;
         const uint32_t bar = mload0 + 8 * stg, st = sb + stg * STAGE;
-        tc::mbar_expect_tx(bar, 3 * TILE);
-        tc::tma_load_3d(st + oKQ, &m.k, 0, hk, t0, bar);
-        tc::tma_load_3d(st + oKQ + 2 * 8192, &m.k, 64, hk, t0, bar);
-        tc::tma_load_3d(st + oKQ + 8192, &m.q, 0, hk, t0, bar);
-        tc::tma_load_3d(st + oKQ + 3 * 8192, &m.q, 64, hk, t0, bar);
-        tc::tma_load_4d(st + oV, &m.v, 0, hh, t0, 0, bar);
+        if (which < 0 || which == 4) tc::mbar_expect_tx(bar, 3 * TILE);
+        if (which < 0 || which == 0) tc::tma_load_3d(st + oKQ, &m.k, 0, hk, t0, bar);
+        if (which < 0 || which == 1) tc::tma_load_3d(st + oKQ + 2 * 8192, &m.k, 64, hk, t0, bar);
+        if (which < 0 || which == 2) tc::tma_load_3d(st + oKQ + 8192, &m.q, 0, hk, t0, bar);
+        if (which < 0 || which == 3) tc::tma_load_3d(st + oKQ + 3 * 8192, &m.q, 64, hk, t0, bar);
+        if (which < 0 || which == 4) tc::tma_load_4d(st + oV, &m.v, 0, hh, t0, 0, bar);
     };
     if (warp == 0) tc::alloc(smem_u32(tslot), 512);
     if (tid == 0) {
         tc::mbar_init(mb, 1);
         tc::mbar_init(mload0, 1);
         tc::mbar_init(mload0 + 8, 1);
+        tc::mbar_init(mg1, 1);
     }
     // T's blocks above the diagonal stay zero in the shared tile
     for (int i = tid; i < CH * CH * 2 / 16; i += 512)
@@ -123,10 +144,17 @@ __global__ void __launch_bounds__(512, 1) k_prep_gdn(const Params p, const __gri
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
-    if (tid == STORE_TID && (int)blockIdx.x < n_items) issue_loads(blockIdx.x, 0);
+    // bit j: stage j has a load in flight (the store thread's view) / that load's barrier parity
+    uint32_t pend = 0, pend_par = 0;
+    if (tid == STORE_TID)
+        for (int j = 0; j < 2; ++j)
+            if ((int)blockIdx.x + j * (int)gridDim.x < n_items) {
+                issue_loads(blockIdx.x + j * gridDim.x, j, -1);
+                pend |= 1u << j;
+            }
     const uint32_t tmem = *tslot;
     uint32_t phase = 0;
-    int it = 0;  // this CTA's item count (selects the stage)
+    int it = 0;  // this CTA's item count (selects the stage and the parity of the small arrays)
     auto tl = [&](uint32_t col) { return tmem + ((uint32_t)(32 * q4) << 16) + col; };
     auto sync_all = [&]() {
         tc::fence_async_smem();
@@ -134,11 +162,10 @@ __global__ void __launch_bounds__(512, 1) k_prep_gdn(const Params p, const __gri
         __syncthreads();
         tc::fence_after();
     };
-    int pending = (int)blockIdx.x < n_items ? 0 : -1;  // stage with a load in flight, or -1
-    uint32_t pending_par = 0;
     auto bail = [&]() {
         if (tid == STORE_TID) {
-            if (pending >= 0) tc::mbar_wait(mload0 + 8 * pending, pending_par);  // bounded drain
+            for (int j = 0; j < 2; ++j)
+                if ((pend >> j) & 1) tc::mbar_wait(mload0 + 8 * j, (pend_par >> j) & 1);  // bounded drain
             tc::bulk_wait_all();
         }
         if (tid == 0) atomicOr(p.status, ST_MMA_TIMEOUT);
@@ -156,23 +183,24 @@ __global__ void __launch_bounds__(512, 1) k_prep_gdn(const Params p, const __gri
         }
         return true;
     };
-    // the next item's beta logit (thread r < 64) and gates (first warp, rows 2 lane and
-    // 2 lane + 1), read one item ahead as raw values (rows clamped into the chunk) that are
-    // first read at the next item's top, so no thread waits for them
+    // an item's gates (warp 9, lane l: rows 2l and 2l + 1) and beta logits (warps 10 and 11,
+    // one row a thread), read as raw values (rows clamped into the chunk) a full item before
+    // they are used
     float pg0 = 0.f, pg1 = 0.f;
     unsigned short pb = 0;
     auto prefetch_small = [&](int item) {
-        if (tid >= CH) return;
+        if (warp < 9 || warp > 11) return;
         ChunkInfo cj;
         lookup_chunk(item / p.H, p.N, p.chunk_off, p.cu_seqlens, p.seq_len, cj);
         const int hh = item % p.H;
-        pb = reinterpret_cast<const unsigned short*>(p.beta_logit)[(cj.t0 + min(tid, cj.len - 1)) * p.H + hh];
-        if (tid < 32) {
-            pg0 = p.g[(cj.t0 + min(2 * tid, cj.len - 1)) * p.H + hh];
-            pg1 = p.g[(cj.t0 + min(2 * tid + 1, cj.len - 1)) * p.H + hh];
+        if (warp == 9) {
+            pg0 = p.g[(cj.t0 + min(2 * lane, cj.len - 1)) * p.H + hh];
+            pg1 = p.g[(cj.t0 + min(2 * lane + 1, cj.len - 1)) * p.H + hh];
+        } else {
+            const int r = tid - 320;
+            pb = reinterpret_cast<const unsigned short*>(p.beta_logit)[(cj.t0 + min(r, cj.len - 1)) * p.H + hh];
         }
     };
-    if ((int)blockIdx.x < n_items) prefetch_small(blockIdx.x);
     auto rows16 = [&](const float* a, float (&o)[16], int cq) {  // a[cq .. cq+15]
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -192,107 +220,140 @@ __global__ void __launch_bounds__(512, 1) k_prep_gdn(const Params p, const __gri
         *reinterpret_cast<uint4*>(tile + tc::sw_chunk(L, cq >> 3, 128)) = make_uint4(w[0], w[1], w[2], w[3]);
         *reinterpret_cast<uint4*>(tile + tc::sw_chunk(L, (cq >> 3) + 1, 128)) = make_uint4(w[4], w[5], w[6], w[7]);
     };
-    // raw q (or k) of this thread's channel and rows cq .. cq+15 (staged in tensor memory)
-    // times the rows' inverse norm, the multiplier and the gate factor `kind`
-    auto derived = [&](bool isq, float mul, int kind, float (&o)[16], int cq) {
+    // raw q (or k) of this thread's channel and rows cq .. cq+15 (staged in tensor memory for
+    // the item of parity x) times the rows' inverse norm, the multiplier and the gate factor
+    // `kind`
+    auto derived = [&](int x, bool isq, float mul, int kind, float (&o)[16], int cq) {
         float f[16], inv[16];
-        rows16(sFac + kind * CH, f, cq);
-        tc::ld16(tl((isq ? R_Q : R_K) + cq), o);
-        rows16(isq ? sInvQ : sInvK, inv, cq);
+        rows16(sFac(x) + kind * CH, f, cq);
+        tc::ld16(tl((isq ? R_Q0 : R_K0) + 128 * x + cq), o);
+        rows16(isq ? sInvQ(x) : sInvK(x), inv, cq);
 #pragma unroll
         for (int i = 0; i < 16; ++i) o[i] = o[i] * derived_m(inv[i], mul, 1.f) * f[i];
     };
+    // The front part of item number `itx` of this CTA, on warps 8..15 (u = tid - 256): what
+    // needs no product of the item before it.  It runs while warps 0..7 invert T of the item
+    // before (the first item's runs before the loop): the wait for the item's q, k, v tiles,
+    // rows past the chunk's end zeroed, its raw q and k rows into tensor memory, its gates
+    // (warp 9) and beta (warps 10, 11) from the raw values read an item ahead (and the next
+    // item's read), and G1 = [k; q] k^T issued on the raw tiles (warp 15); tensor-memory
+    // columns and small arrays of the item's parity.  False (on every participant) if the
+    // wait for the tiles timed out.
+    auto front = [&](int item, int itx) -> bool {
+        const int u = tid - 256, x = itx & 1;
+        const bool ok = tc::mbar_wait(mload0 + 8 * x, (uint32_t)((itx >> 1) & 1));
+        if (tc::named_or(2, 256, !ok)) return false;
+        if (tid == STORE_TID) pend &= ~(1u << x);
+        ChunkInfo cf;
+        lookup_chunk(item / p.H, p.N, p.chunk_off, p.cu_seqlens, p.seq_len, cf);
+        unsigned char* kq = smem + x * STAGE + oKQ;
+        if (cf.len < CH) {
+            const int nz = (CH - cf.len) * 16;  // 16-byte chunks per 128-column row
+            for (int i = u; i < 3 * nz; i += 256) {
+                const int t = i / nz, rem = i % nz, r = cf.len + rem / 16, jc = rem % 16;
+                unsigned char* base = t < 2 ? kq : smem + x * STAGE + oV;
+                const int row = t == 1 ? 64 + r : r, rows = t == 2 ? 64 : 128;
+                *reinterpret_cast<uint4*>(base + tc::sw_chunk(row, jc, rows)) = make_uint4(0, 0, 0, 0);
+            }
+            tc::fence_async_smem();
+            tc::named_sync(2, 256);
+        }
+        {  // raw q and k of this thread's channel, row blocks hc - 2 and hc, into tensor memory
+            const int lch = (L & 63) >> 3, lsub = (L & 7) << 1;
+            for (int pass = 0; pass < 2; ++pass) {
+                const int cb = 16 * (hc - 2 + 2 * pass);
+                float qs[16], ks[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {  // k row cb + i; the q row sits 64 rows (8 KB) below
+                    const uint32_t off = (uint32_t)((L >> 6) * 128 * 128 + (cb + i) * 128 + ((lch ^ (i & 7)) << 4) + lsub);
+                    ks[i] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(kq + off));
+                    qs[i] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(kq + off + 64 * 128));
+                }
+                tc::st16(tl(R_Q0 + 128 * x + cb), qs);
+                tc::st16(tl(R_K0 + 128 * x + cb), ks);
+            }
+        }
+        if (warp == 9)
+            gdn_gate_scan(2 * lane < cf.len ? pg0 : 0.f, 2 * lane + 1 < cf.len ? pg1 : 0.f, gates(x), true, p);
+        if (warp == 10 || warp == 11) {
+            const int r = tid - 320;
+            sBeta(x)[r] = r < cf.len ? sigmoid_f(__bfloat162float(__ushort_as_bfloat16(pb))) : 0.f;
+        }
+        if (item + (int)gridDim.x < n_items) prefetch_small(item + gridDim.x);
+        if (u == 224) {  // G1 on the tiles as loaded (by the last warp); the item's E1 waits for it
+            constexpr uint32_t id1 = tc::idesc(128, 64, 0, 0);
+            const uint32_t a = sb + x * STAGE + oKQ;
+#pragma unroll
+            for (int k = 0; k < PD; k += 16) tc::mma(tmem + R_G1, tc::kdesc(a, 128, 0, k), tc::kdesc(a, 128, 0, k), id1, k > 0);
+            tc::commit(mg1);
+        }
+        return true;
+    };
+    {  // the first item's front
+        bool fok = true;
+        if (tid >= 256 && (int)blockIdx.x < n_items) {
+            prefetch_small(blockIdx.x);
+            fok = front(blockIdx.x, 0);
+        }
+        tc::fence_before();
+        if (__syncthreads_or(!fok)) return bail();
+        tc::fence_after();
+    }
 
     for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++it) {
     const int chunk = item / p.H, h = item % p.H;
-    ChunkInfo ci;
-    lookup_chunk(chunk, p.N, p.chunk_off, p.cu_seqlens, p.seq_len, ci);
-    const int stg = it & 1;
+    const int stg = it & 1, x = stg;  // the stage and the parity of the small arrays
     const uint32_t st = sb + stg * STAGE;
     unsigned char* sKQ = smem + stg * STAGE + oKQ;
-    unsigned char* sV = smem + stg * STAGE + oV;
     const size_t tile_cc = ((size_t)chunk * p.H + h) * CH * CH;
     const int trow = (chunk * p.H + h) * PD;  // the chunk-head's first row in the [D][C] tile maps
     const bool has_next = item + (int)gridDim.x < n_items;
-    // the last item's stores have read their tiles (the other stage and the shared staging
-    // tiles); then the next item's tiles go into the other stage
-    if (tid == STORE_TID) {
-        tc::bulk_wait_read();
-        if (has_next) issue_loads(item + gridDim.x, stg ^ 1);
-    }
-    if (tid < 32) gdn_gate_scan(2 * tid < ci.len ? pg0 : 0.f, 2 * tid + 1 < ci.len ? pg1 : 0.f, G, true, p);
-    if (tid < CH) sBeta[tid] = tid < ci.len ? sigmoid_f(__bfloat162float(__ushort_as_bfloat16(pb))) : 0.f;
-
-    // operand tiles; rows past the chunk's end are zeroed before any product
-    {
-        const bool ok = tc::mbar_wait(mload0 + 8 * stg, (uint32_t)((it >> 1) & 1));
-        if (__syncthreads_or(!ok)) return bail();
-        pending = has_next ? (stg ^ 1) : -1;
-        pending_par = (uint32_t)(((it + 1) >> 1) & 1);
-    }
-    if (ci.len < CH) {
-        const int nz = (CH - ci.len) * 16;  // 16-byte chunks per 128-column row
-        for (int i = tid; i < 3 * nz; i += 512) {
-            const int t = i / nz, rem = i % nz, r = ci.len + rem / 16, jc = rem % 16;
-            unsigned char* base = t < 2 ? sKQ : sV;
-            const int row = t == 1 ? 64 + r : r, rows = t == 2 ? 64 : 128;
-            *reinterpret_cast<uint4*>(base + tc::sw_chunk(row, jc, rows)) = make_uint4(0, 0, 0, 0);
-        }
-        sync_all();
-    }
-
-    // ---- G1: [A; P]_raw = [k; q] k^T on the tiles as loaded, under the prologue below -----
-    if (tid == 0) {
-        constexpr uint32_t id1 = tc::idesc(128, 64, 0, 0);
-#pragma unroll
-        for (int k = 0; k < PD; k += 16)
-            tc::mma(tmem + R_G1, tc::kdesc(st + oKQ, 128, 0, k), tc::kdesc(st + oKQ, 128, 0, k), id1, k > 0);
-        tc::commit(mb);
-    }
-    {  // inverse row norms of q (rows 64..127 of the stacked tile) and k, 4 threads per row
-        const int r = (tid >> 2) & 63, part = tid & 3;
-        const int row = tid < 256 ? 64 + r : r;
+    // the last item's W, U store has read A's tile (written by E1); its R store (the latest
+    // group) is waited for before the inversion
+    if (tid == STORE_TID) tc::bulk_wait_read_but1();
+    {  // inverse row norms (8 threads per row: 4 for q, 4 for k), the gate factors and the
+       // combined row factors of row r, from the front's gates and beta
+        // (chunks p + 4i of the q row and p + 4 + 4i of the k row: the 8 threads of a row read
+        // 8 different 16-byte bank groups)
+        const int r = tid >> 3, part = tid & 7, row = part < 4 ? 64 + r : r;
         float s = 0.f;
-        for (int j = part * 4; j < part * 4 + 4; ++j) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int j = ((part & 3) + 4 * i + (part & 4)) & 15;
             const uint4 v = *reinterpret_cast<const uint4*>(sKQ + tc::sw_chunk(row, j, 128));
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const float2 f = unpack_bf16(w[e]);
+                const float2 f = unpack_bf16(wv[e]);
                 s += f.x * f.x + f.y * f.y;
             }
         }
         s += __shfl_xor_sync(0xffffffffu, s, 1);
         s += __shfl_xor_sync(0xffffffffu, s, 2);
-        if (part == 0) (tid < 256 ? sInvQ : sInvK)[r] = rsqrtf(s + 1e-6f);
-    }
-    if (tid < CH) {
-        sFac[F_KD * CH + tid] = gate_factor<F_KD>(G, tid, 0);
-        sFac[F_KDP * CH + tid] = gate_factor<F_KDP>(G, tid, 0);
-        sFac[F_KIP * CH + tid] = gate_factor<F_KIP>(G, tid, 0);
-        sFac[F_KR * CH + tid] = gate_factor<F_KR>(G, tid, 0);
-    }
-    {  // raw q and k of this thread's channel and rows into tensor memory
-        const int lch = (L & 63) >> 3, lsub = (L & 7) << 1;
-        float qs[16], ks[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {  // k row c0 + i; the q row sits 64 rows (8 KB) below
-            const uint32_t off = (uint32_t)((L >> 6) * 128 * 128 + (c0 + i) * 128 + ((lch ^ (i & 7)) << 4) + lsub);
-            ks[i] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(sKQ + off));
-            qs[i] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(sKQ + off + 64 * 128));
+        const float sk = __shfl_xor_sync(0xffffffffu, s, 4);
+        if (part == 0) {
+            const Gates<PD, false> G = gates(x);
+            const float iq = rsqrtf(s + 1e-6f), ik = rsqrtf(sk + 1e-6f), bt = sBeta(x)[r];
+            const float fkd = gate_factor<F_KD>(G, r, 0), fkdp = gate_factor<F_KDP>(G, r, 0);
+            const float fkip = gate_factor<F_KIP>(G, r, 0), fkr = gate_factor<F_KR>(G, r, 0);
+            float* fac = sFac(x);
+            sInvQ(x)[r] = iq;
+            sInvK(x)[r] = ik;
+            fac[F_KD * CH + r] = fkd;
+            fac[F_KDP * CH + r] = fkdp;
+            fac[F_KIP * CH + r] = fkip;
+            fac[F_KR * CH + r] = fkr;
+            sTab[T_CF * CH + r] = ik * fkip;          // ki' column factor
+            sTab[T_RA * CH + r] = bt * ik * fkdp;     // A row factor (with beta)
+            sTab[T_RP * CH + r] = p.scale * iq * fkdp;  // P row factor
+            sTab[T_CW * CH + r] = bt * ik * fkd;      // column factor of T for W
         }
-        tc::st16(tl(R_Q + c0), qs);
-        tc::st16(tl(R_K + c0), ks);
     }
-    __syncthreads();  // norms and gate factors
-    if (tid < CH) {   // combined row factors
-        const float ik = sInvK[tid], e1 = sFac[F_KDP * CH + tid], bt = sBeta[tid];
-        sTab[T_CF * CH + tid] = ik * sFac[F_KIP * CH + tid];       // ki' column factor
-        sTab[T_RA * CH + tid] = bt * ik * e1;                        // A row factor (with beta)
-        sTab[T_RP * CH + tid] = p.scale * sInvQ[tid] * e1;           // P row factor
-        sTab[T_CW * CH + tid] = bt * ik * sFac[F_KD * CH + tid];     // column factor of T for W
+    {  // G1, issued by the front (its barrier also publishes the tables)
+        const bool ok = tc::mbar_wait(mg1, (uint32_t)(it & 1));
+        tc::fence_after();
+        if (__syncthreads_or(!ok)) return bail();
     }
-    if (!wait_mma()) return;  // G1 (its barrier also publishes the tables)
     {
         float v[16], cf[16];
         tc::ld16(tl(R_G1 + c0), v);
@@ -325,28 +386,35 @@ __global__ void __launch_bounds__(512, 1) k_prep_gdn(const Params p, const __gri
             }
         }
     }
-    __syncthreads();
+    if (tid == STORE_TID) tc::bulk_wait_read();  // the last item's R stores have read T's fp32 tile and T1
+    sync_all();  // A and P staged; G1's tensor memory has been read (the next item's G1 reuses it)
+    bool fok = true;
     if (warp < 8) {
         inv::invert_tc(sA, sTf, sTmp, sT, nullptr);
     } else {
         // meanwhile: kr = kn e^{gT-gc} (this warp's lanes, row quarters hc - 2 and hc) into the
-        // W^T tile, which W's epilogue fills only after kr's store has read it; gT, e^{gT}
+        // W^T tile, which W's epilogue fills only after kr's store has read it; gT, e^{gT}; then
+        // the next item's front
         uint32_t w[8];
         for (int pass = 0; pass < 2; ++pass) {
             const int cq = 16 * (hc - 2 + 2 * pass);
             float v[16];
-            derived(false, 1.f, F_KR, v, cq);
+            derived(x, false, 1.f, F_KR, v, cq);
             pack8(v, w);
             store_cm(sW2, w, cq);
         }
         tc::fence_async_smem();
         if (hc == 2) {
-            const float gt = G.gTv(0);
+            const float gt = gates(x).gTv(0);
             p.gT[((size_t)chunk * p.H + h) * PD + L] = gt;
             p.egT[((size_t)chunk * p.H + h) * PD + L] = __expf(gt);
         }
+        if (has_next) fok = front(item + gridDim.x, it + 1);
     }
-    __syncthreads();  // T complete (fp32 transposed in sTf, bf16 in sT); kr staged
+    // T complete (fp32 transposed in sTf, bf16 in sT); kr staged; the next item's front done
+    tc::fence_before();
+    if (__syncthreads_or(!fok)) return bail();
+    tc::fence_after();
     if (tid == STORE_TID) {
         tc::tma_store_2d(&m.Kr, 0, trow, sb + oW2);
         tc::bulk_commit();
@@ -356,7 +424,7 @@ __global__ void __launch_bounds__(512, 1) k_prep_gdn(const Params p, const __gri
         // W^T = k^T T1^T and U^T = v^T T2^T; thread: row r, 16 columns, one of the two copies
         const int r = tid & 63, cq = 16 * ((tid >> 6) & 3), which = tid >> 8;
         float f[16];
-        rows16(which == 0 ? sTab + T_CW * CH : sBeta, f, cq);
+        rows16(which == 0 ? sTab + T_CW * CH : sBeta(x), f, cq);
         float v[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) v[i] = cq + i <= r ? sTf[(cq + i) * LDF + r] * f[i] : 0.f;
@@ -383,9 +451,15 @@ __global__ void __launch_bounds__(512, 1) k_prep_gdn(const Params p, const __gri
             tc::mma(tmem + R_U, tc::mdesc(st + oV, 64, 0, k), tc::kdesc(sb + oT2, 64, 0, k), id, k > 0);
         tc::commit(mb);
     }
-    if (has_next) prefetch_small(item + gridDim.x);  // raw values, first read at the next item's top
     if (tid == STORE_TID) tc::bulk_wait_read();  // kr's store has read the W^T tile
     if (!wait_mma()) return;
+    // the products have read this stage for the last time: the tiles of the item after next
+    // go into it, more than an item ahead of that item's front
+    if (tid == STORE_TID && item + 2 * (int)gridDim.x < n_items) {
+        issue_loads(item + 2 * gridDim.x, stg, -1);
+        pend |= 1u << stg;
+        pend_par = (pend_par & ~(1u << stg)) | ((uint32_t)(((it + 2) >> 1) & 1) << stg);
+    }
     {
         float v[16];
         uint32_t w[8];
@@ -394,12 +468,12 @@ __global__ void __launch_bounds__(512, 1) k_prep_gdn(const Params p, const __gri
         store_cm(sW2, w, c0);  // bf16 W^T [d][s]: the A operand of W^T P^T and W's store
         tc::ld16(tl(R_U + c0), v);
         pack8(v, w);
-        store_cm(sKQ, w, c0);  // U^T over the dead k / q tiles
+        store_cm(reinterpret_cast<unsigned char*>(sA), w, c0);  // U^T over the dead fp32 A
     }
     sync_all();
     if (tid == STORE_TID) {
         tc::tma_store_2d(&m.W, 0, trow, sb + oW2);
-        tc::tma_store_2d(&m.U, 0, trow, st + oKQ);
+        tc::tma_store_2d(&m.U, 0, trow, sb + oA);
         tc::bulk_commit();
     }
 
@@ -416,7 +490,7 @@ __global__ void __launch_bounds__(512, 1) k_prep_gdn(const Params p, const __gri
         float acc[16], qd[16];
         uint32_t w[8], wl[8];
         tc::ld16(tl(R_R + c0), acc);
-        derived(true, p.scale, F_KD, qd, c0);
+        derived(x, true, p.scale, F_KD, qd, c0);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             const float r0 = qd[2 * e] - acc[2 * e], r1 = qd[2 * e + 1] - acc[2 * e + 1];
@@ -424,7 +498,7 @@ __global__ void __launch_bounds__(512, 1) k_prep_gdn(const Params p, const __gri
             const float2 hf = unpack_bf16(w[e]);
             wl[e] = pack_bf16(r0 - hf.x, r1 - hf.y);
         }
-        store_cm(sKQ + TILE, w, c0);  // R_hi over the dead k / q tiles
+        store_cm(reinterpret_cast<unsigned char*>(sTf), w, c0);  // R_hi over the dead fp32 T
         store_cm(sT1, wl, c0);        // R_lo over the dead T1, T2
         tc::fence_async_smem();
     }
@@ -432,7 +506,7 @@ __global__ void __launch_bounds__(512, 1) k_prep_gdn(const Params p, const __gri
     __syncthreads();  // this item's shared tiles and tensor memory are free
     tc::fence_after();
     if (tid == STORE_TID) {
-        tc::tma_store_2d(&m.R, 0, trow, st + oKQ + TILE);
+        tc::tma_store_2d(&m.R, 0, trow, sb + oTf);
         tc::tma_store_2d(&m.Rlo, 0, trow, sb + oT1);
         tc::bulk_commit();
     }
