@@ -17,9 +17,10 @@
 //
 // Schedule of one item: the row norms, gate factors and combined row factors (all warps);
 // E1 (A, P) from G1; then warps 0..7 invert T while warps 8..15 build kr and run the NEXT
-// item's front part: the wait for its tiles, its raw q, k rows into tensor memory, its gates
-// and beta, and its G1 issued on the raw tiles (small arrays and those tensor-memory columns
-// are kept per item parity); then T1, T2, the W / U product, R.  A stage's tiles are last
+// item's front part (the wait for its tiles, its raw q, k rows into tensor memory, its G1
+// issued on the raw tiles) and warps 6, 7 (free after the inverse's diagonal blocks) scan the
+// next item's gates and beta and look up the chunk of the item after it (small arrays and
+// those tensor-memory columns are kept per item parity); then T1, T2, the W / U product, R.  A stage's tiles are last
 // read by the W / U product, after which the tiles of the item after next are loaded into it.
 // W, U, Kr, R_hi, R_lo and T are staged in shared tiles that are dead by then (none in an
 // input stage) and written by TMA stores that one thread issues.
@@ -58,7 +59,7 @@ constexpr int nInvQ = 64, nInvK = 64, nBeta = 64, nFac = 4 * 64, nGate = 68;
 constexpr int nPar = nInvQ + nInvK + nBeta + nFac + nGate;
 constexpr int nTab = 4 * 64, nPad = 8;
 constexpr int SMALL_FLOATS = 2 * nPar + nTab + nPad;
-constexpr int SMEM_BYTES = oSmall + SMALL_FLOATS * 4 + 64 + 1024;
+constexpr int SMEM_BYTES = oSmall + SMALL_FLOATS * 4 + 128 + 1024;  // + barriers, tensor-memory slot, chunk info
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 static_assert(nPar % 4 == 0, "16-byte aligned per-parity arrays");
 // tensor-memory columns; raw q, k rows of item parity x at R_Q0 + 128 x, R_K0 + 128 x
@@ -112,15 +113,26 @@ __global__ void __launch_bounds__(512, 1) k_prep_gdn(const Params p, const __gri
     float* sTab = fsm + 2 * nPar;  // [4][64] combined row factors of the current item (Tab order)
     uint64_t* mbars = reinterpret_cast<uint64_t*>(sTab + nTab + nPad);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(mbars + 4);
+    // chunk info of the items of parity 0 and 1 (an item's slot is filled two items ahead: the
+    // lookup's dependent integer chain costs hundreds of cycles inside the busy loop)
+    int* sCI = reinterpret_cast<int*>(mbars + 6);
+    auto put_ci = [&](int slot, const ChunkInfo& c) {
+        int* d = sCI + 8 * slot;
+        d[0] = c.seq, d[1] = c.local, d[2] = (int)(c.t0 & 0xffffffff), d[3] = (int)(c.t0 >> 32), d[4] = c.len;
+    };
+    auto get_ci = [&](int slot) {
+        const int* d = sCI + 8 * slot;
+        ChunkInfo c;
+        c.seq = d[0], c.local = d[1], c.t0 = (int64_t)(((uint64_t)(uint32_t)d[3] << 32) | (uint32_t)d[2]), c.len = d[4];
+        return c;
+    };
     // product barrier, load barriers (one per stage), G1 barrier
     const uint32_t mb = smem_u32(mbars), mload0 = smem_u32(mbars + 1), mg1 = smem_u32(mbars + 3);
 
     // q, k, v of `item` into stage `stg`: k and q stacked into one 128-row tile, one 64-column
     // box at a time, v as two column blocks; copy `which` (0..4; the barrier's byte count goes
     // with copy 4), or all five for which < 0
-    auto issue_loads = [&](int item, int stg, int which) {
-        ChunkInfo cj;
-        lookup_chunk(item / p.H, p.N, p.chunk_off, p.cu_seqlens, p.seq_len, cj);
+    auto issue_loads = [&](int item, const ChunkInfo& cj, int stg, int which) {
         const int hh = item % p.H, hk = qk_head(p, hh), t0 = (int)cj.t0;
         const uint32_t bar = mload0 + 8 * stg, st = sb + stg * STAGE;
         if (which < 0 || which == 4) tc::mbar_expect_tx(bar, 3 * TILE);
@@ -136,6 +148,12 @@ __global__ void __launch_bounds__(512, 1) k_prep_gdn(const Params p, const __gri
         tc::mbar_init(mload0, 1);
         tc::mbar_init(mload0 + 8, 1);
         tc::mbar_init(mg1, 1);
+        for (int j = 0; j < 2; ++j) {  // the first two items' chunk info
+            ChunkInfo c{};
+            if ((int)blockIdx.x + j * (int)gridDim.x < n_items)
+                lookup_chunk(((int)blockIdx.x + j * (int)gridDim.x) / p.H, p.N, p.chunk_off, p.cu_seqlens, p.seq_len, c);
+            put_ci(j, c);
+        }
     }
     // T's blocks above the diagonal stay zero in the shared tile
     for (int i = tid; i < CH * CH * 2 / 16; i += 512)
@@ -149,7 +167,7 @@ __global__ void __launch_bounds__(512, 1) k_prep_gdn(const Params p, const __gri
     if (tid == STORE_TID)
         for (int j = 0; j < 2; ++j)
             if ((int)blockIdx.x + j * (int)gridDim.x < n_items) {
-                issue_loads(blockIdx.x + j * gridDim.x, j, -1);
+                issue_loads(blockIdx.x + j * gridDim.x, get_ci(j), j, -1);
                 pend |= 1u << j;
             }
     const uint32_t tmem = *tslot;
@@ -183,22 +201,29 @@ __global__ void __launch_bounds__(512, 1) k_prep_gdn(const Params p, const __gri
         }
         return true;
     };
-    // an item's gates (warp 9, lane l: rows 2l and 2l + 1) and beta logits (warps 10 and 11,
-    // one row a thread), read as raw values (rows clamped into the chunk) a full item before
-    // they are used
+    // An item's gates (warp 6, lane l: rows 2l and 2l + 1) and beta logits (warp 7, lane l:
+    // rows l and l + 32), read as raw values (rows clamped into the chunk) a full item before
+    // warps 6 and 7, idle once the inversion's diagonal blocks are done, scan them.
     float pg0 = 0.f, pg1 = 0.f;
-    unsigned short pb = 0;
-    auto prefetch_small = [&](int item) {
-        if (warp < 9 || warp > 11) return;
-        ChunkInfo cj;
-        lookup_chunk(item / p.H, p.N, p.chunk_off, p.cu_seqlens, p.seq_len, cj);
+    unsigned short pb0 = 0, pb1 = 0;
+    auto prefetch_small = [&](int item, const ChunkInfo& cj) {
         const int hh = item % p.H;
-        if (warp == 9) {
+        if (warp == 6) {
             pg0 = p.g[(cj.t0 + min(2 * lane, cj.len - 1)) * p.H + hh];
             pg1 = p.g[(cj.t0 + min(2 * lane + 1, cj.len - 1)) * p.H + hh];
-        } else {
-            const int r = tid - 320;
-            pb = reinterpret_cast<const unsigned short*>(p.beta_logit)[(cj.t0 + min(r, cj.len - 1)) * p.H + hh];
+        } else if (warp == 7) {
+            const unsigned short* bl = reinterpret_cast<const unsigned short*>(p.beta_logit);
+            pb0 = bl[(cj.t0 + min(lane, cj.len - 1)) * p.H + hh];
+            pb1 = bl[(cj.t0 + min(lane + 32, cj.len - 1)) * p.H + hh];
+        }
+    };
+    // warps 6 and 7: gates and beta of the item of parity x (raw values read an item before)
+    auto scan_small = [&](int x, const ChunkInfo& cj) {
+        if (warp == 6) {
+            gdn_gate_scan(2 * lane < cj.len ? pg0 : 0.f, 2 * lane + 1 < cj.len ? pg1 : 0.f, gates(x), true, p);
+        } else if (warp == 7) {
+            sBeta(x)[lane] = lane < cj.len ? sigmoid_f(__bfloat162float(__ushort_as_bfloat16(pb0))) : 0.f;
+            sBeta(x)[lane + 32] = lane + 32 < cj.len ? sigmoid_f(__bfloat162float(__ushort_as_bfloat16(pb1))) : 0.f;
         }
     };
     auto rows16 = [&](const float* a, float (&o)[16], int cq) {  // a[cq .. cq+15]
@@ -234,18 +259,15 @@ __global__ void __launch_bounds__(512, 1) k_prep_gdn(const Params p, const __gri
     // The front part of item number `itx` of this CTA, on warps 8..15 (u = tid - 256): what
     // needs no product of the item before it.  It runs while warps 0..7 invert T of the item
     // before (the first item's runs before the loop): the wait for the item's q, k, v tiles,
-    // rows past the chunk's end zeroed, its raw q and k rows into tensor memory, its gates
-    // (warp 9) and beta (warps 10, 11) from the raw values read an item ahead (and the next
-    // item's read), and G1 = [k; q] k^T issued on the raw tiles (warp 15); tensor-memory
-    // columns and small arrays of the item's parity.  False (on every participant) if the
-    // wait for the tiles timed out.
+    // rows past the chunk's end zeroed, its raw q and k rows into the tensor-memory columns of
+    // the item's parity, and G1 = [k; q] k^T issued on the raw tiles (warp 15).  False (on
+    // every participant) if the wait for the tiles timed out.
     auto front = [&](int item, int itx) -> bool {
         const int u = tid - 256, x = itx & 1;
         const bool ok = tc::mbar_wait(mload0 + 8 * x, (uint32_t)((itx >> 1) & 1));
         if (tc::named_or(2, 256, !ok)) return false;
         if (tid == STORE_TID) pend &= ~(1u << x);
-        ChunkInfo cf;
-        lookup_chunk(item / p.H, p.N, p.chunk_off, p.cu_seqlens, p.seq_len, cf);
+        const ChunkInfo cf = get_ci(x);
         unsigned char* kq = smem + x * STAGE + oKQ;
         if (cf.len < CH) {
             const int nz = (CH - cf.len) * 16;  // 16-byte chunks per 128-column row
@@ -273,13 +295,6 @@ __global__ void __launch_bounds__(512, 1) k_prep_gdn(const Params p, const __gri
                 tc::st16(tl(R_K0 + 128 * x + cb), ks);
             }
         }
-        if (warp == 9)
-            gdn_gate_scan(2 * lane < cf.len ? pg0 : 0.f, 2 * lane + 1 < cf.len ? pg1 : 0.f, gates(x), true, p);
-        if (warp == 10 || warp == 11) {
-            const int r = tid - 320;
-            sBeta(x)[r] = r < cf.len ? sigmoid_f(__bfloat162float(__ushort_as_bfloat16(pb))) : 0.f;
-        }
-        if (item + (int)gridDim.x < n_items) prefetch_small(item + gridDim.x);
         if (u == 224) {  // G1 on the tiles as loaded (by the last warp); the item's E1 waits for it
             constexpr uint32_t id1 = tc::idesc(128, 64, 0, 0);
             const uint32_t a = sb + x * STAGE + oKQ;
@@ -291,9 +306,13 @@ __global__ void __launch_bounds__(512, 1) k_prep_gdn(const Params p, const __gri
     };
     {  // the first item's front
         bool fok = true;
-        if (tid >= 256 && (int)blockIdx.x < n_items) {
-            prefetch_small(blockIdx.x);
-            fok = front(blockIdx.x, 0);
+        if ((int)blockIdx.x < n_items) {  // (a packed batch can have fewer items than CTAs)
+            if (warp == 6 || warp == 7) {  // gates and beta of the first item; raw values of the second
+                prefetch_small(blockIdx.x, get_ci(0));
+                scan_small(0, get_ci(0));
+                if ((int)blockIdx.x + (int)gridDim.x < n_items) prefetch_small(blockIdx.x + gridDim.x, get_ci(1));
+            }
+            if (tid >= 256) fok = front(blockIdx.x, 0);
         }
         tc::fence_before();
         if (__syncthreads_or(!fok)) return bail();
@@ -391,6 +410,17 @@ __global__ void __launch_bounds__(512, 1) k_prep_gdn(const Params p, const __gri
     bool fok = true;
     if (warp < 8) {
         inv::invert_tc(sA, sTf, sTmp, sT, nullptr);
+        if (warp >= 6) {  // (warps 6, 7 leave the inversion after its diagonal blocks)
+            // the next item's gates and beta; the chunk info of the item after it (into this
+            // item's slot) and its raw gates and beta
+            if (has_next) scan_small(x ^ 1, get_ci(x ^ 1));
+            if (item + 2 * (int)gridDim.x < n_items) {
+                ChunkInfo c2;
+                lookup_chunk((item + 2 * (int)gridDim.x) / p.H, p.N, p.chunk_off, p.cu_seqlens, p.seq_len, c2);
+                if (tid == 192) put_ci(x, c2);
+                prefetch_small(item + 2 * gridDim.x, c2);
+            }
+        }
     } else {
         // meanwhile: kr = kn e^{gT-gc} (this warp's lanes, row quarters hc - 2 and hc) into the
         // W^T tile, which W's epilogue fills only after kr's store has read it; gT, e^{gT}; then
@@ -456,7 +486,7 @@ __global__ void __launch_bounds__(512, 1) k_prep_gdn(const Params p, const __gri
     // the products have read this stage for the last time: the tiles of the item after next
     // go into it, more than an item ahead of that item's front
     if (tid == STORE_TID && item + 2 * (int)gridDim.x < n_items) {
-        issue_loads(item + 2 * gridDim.x, stg, -1);
+        issue_loads(item + 2 * gridDim.x, get_ci(x), stg, -1);
         pend |= 1u << stg;
         pend_par = (pend_par & ~(1u << stg)) | ((uint32_t)(((it + 2) >> 1) & 1) << stg);
     }

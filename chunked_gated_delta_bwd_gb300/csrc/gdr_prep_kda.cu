@@ -40,7 +40,7 @@ constexpr int oQ = 0;         // q (token-major) -> (beta kd)^T [d][s]   (+ STAG
 constexpr int oK = 16384;     // k (token-major) -> (beta V)^T [j][s]
 constexpr int oV = 32768;     // v (token-major)
 constexpr int oW0 = 2 * STAGE;  // kd'^T [d][r] (G1, A block 0)
-constexpr int oW1 = oW0 + TILE; // qd'^T [d][r] (G1, A block 1)
+constexpr int oW1 = oW0 + TILE; // qd'^T [d][r] (G1, A block 1) -> R_hi^T staged
 constexpr int oW2 = oW1 + TILE; // ki'^T [d][s] (G1, B) -> W^T bf16 [d][s]
 constexpr int oP = oW2 + TILE;  // P [r][s] bf16
 constexpr int oT = oP + 8192;   // T [r][s] bf16
@@ -219,16 +219,7 @@ __global__ void __launch_bounds__(512, 1) k_prep_kda(const Params p, const __gri
     const uint32_t sQa = sb + stg * STAGE + oQ, sKa = sb + stg * STAGE + oK;
     const size_t tile_cc = ((size_t)chunk * p.H + h) * CH * CH;
     const bool has_next = item + (int)gridDim.x < n_items;
-    // the next item's tiles into the other stage (its previous tenant finished last iteration)
-    pending = -1;
-    if (has_next) {
-        if (tid == STORE_TID) {  // the last item's stores have read the stage these copies fill
-            tc::bulk_wait_read();
-            issue_loads(item + gridDim.x, stg ^ 1, -1);
-        }
-        pending = stg ^ 1;
-        pending_par = (uint32_t)(((it + 1) >> 1) & 1);
-    }
+    pending = -1;  // (the next item's tiles are requested while this item is inverted)
     if (tid < CH) sBeta[tid] = tid < ci.len ? sigmoid_f(__bfloat162float(__ushort_as_bfloat16(pb))) : 0.f;
 
     // per-channel log gates of this thread's channel and rows (raw gates from the
@@ -238,6 +229,7 @@ __global__ void __launch_bounds__(512, 1) k_prep_kda(const Params p, const __gri
     {
         const float a = expf(palog);
         const float bias = pbias;
+        if (has_next) prefetch_small(item + gridDim.x);  // raw values, first read at the next item's top
         {
             const bool ok = tc::mbar_wait(mgr, (uint32_t)(it & 1));
             if (__syncthreads_or(!ok)) return bail();
@@ -347,6 +339,7 @@ __global__ void __launch_bounds__(512, 1) k_prep_kda(const Params p, const __gri
         tc::st16(tl(R_Q + c0), qs);
         tc::st16(tl(R_K + c0), ks);
     }
+    if (tid == STORE_TID) tc::bulk_wait_read();  // the last item's R store has read the G1 operand tiles
     __syncthreads();  // norms, factors and the q / k tile reads are done
 
     // gate factors of this thread's channel and rows cq .. cq+15
@@ -455,12 +448,21 @@ __global__ void __launch_bounds__(512, 1) k_prep_kda(const Params p, const __gri
             pack8(v, w);
             store_cm(sK, w, cq);
         }
+        // the next item's tiles into the other stage, once the last item's stores have read it
+        // (its R_hi, R_lo store, the latest group, reads no stage)
+        if (has_next) {
+            if (tid == STORE_TID) {
+                tc::bulk_wait_read_but1();
+                issue_loads(item + gridDim.x, stg ^ 1, -1);
+            }
+            pending = stg ^ 1;
+            pending_par = (uint32_t)(((it + 1) >> 1) & 1);
+        }
     }
     sync_all();
     if (has_next) {  // the space of A is free: the next item's small inputs and raw gates
-        if (tid == 0) issue_gate_load(item + gridDim.x);
+        if (tid == 480) issue_gate_load(item + gridDim.x);  // (not the product-issuing thread)
         pending_g = true;
-        prefetch_small(item + gridDim.x);
     }
 
     // ---- W^T = (beta kd)^T T^T ; U^T = (beta V)^T T^T --------------------------------------
@@ -532,7 +534,7 @@ __global__ void __launch_bounds__(512, 1) k_prep_kda(const Params p, const __gri
             const float2 hf = unpack_bf16(w[e]);
             wl[e] = pack_bf16(r0 - hf.x, r1 - hf.y);
         }
-        store_cm(sQ, w, c0);   // R_hi over the dead (beta kd)^T
+        store_cm(sW1, w, c0);  // R_hi over the dead qd'^T
         store_cm(sW0, wl, c0);  // R_lo over the dead kd'^T
         tc::fence_async_smem();
     }
@@ -540,7 +542,7 @@ __global__ void __launch_bounds__(512, 1) k_prep_kda(const Params p, const __gri
     __syncthreads();  // this item's shared tiles and tensor memory are free
     tc::fence_after();
     if (tid == STORE_TID) {
-        tc::tma_store_2d(&m.R, 0, trow, sQa);
+        tc::tma_store_2d(&m.R, 0, trow, sb + oW1);
         tc::tma_store_2d(&m.Rlo, 0, trow, sb + oW0);
         tc::bulk_commit();
     }

@@ -27,19 +27,43 @@ def to_gpu(x):
     return {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
 
 
+def _workspace(d, x, workspace):
+    """The caller's workspace, else one sized for x (so that its device status can be read)."""
+    import chunked_gated_delta_bwd_gb300 as gdr
+    if workspace is not None:
+        return workspace
+    N = d["cu_seqlens"].numel() - 1
+    sh = gdr.make_shape(N, d["v"].shape[0], d["v"].shape[1], d["v"].shape[2], cu_seqlens=d["cu_seqlens"],
+                        kda_gate=x.get("kda_gate", "softplus"), gate_scale=x.get("gate_scale", 0.0),
+                        k_heads=d["q"].shape[1])
+    return torch.empty(max(gdr.workspace_bytes(sh), 16), dtype=torch.uint8, device="cuda")
+
+
+def assert_no_timeout(ws):
+    """No bounded wait of the call ran out (a CTA that gave up leaves its outputs unwritten)."""
+    import chunked_gated_delta_bwd_gb300 as gdr
+    st = gdr.workspace_status(ws)
+    assert not st & GDR_DEV_TIMEOUT, "a bounded wait ran out (device status %d)" % st
+
+
+GDR_DEV_TIMEOUT = 4  # include/gdr.h
+
+
 def run_gpu(x, states=None, workspace=None):
     """x: dict from inputs.make / inputs.custom (CPU tensors).  Returns CPU tensors."""
     import chunked_gated_delta_bwd_gb300 as gdr
     d = to_gpu(x)
     N = d["cu_seqlens"].numel() - 1
+    ws = _workspace(d, x, workspace)
     common = dict(h0=d["h0"], dht=d["dht"], cu_seqlens=d["cu_seqlens"], num_seqs=N,
-                  scale=d["scale"], states=states, workspace=workspace)
+                  scale=d["scale"], states=states, workspace=ws)
     if x["mode"] == "gdn":
         out = gdr.gdr_bwd(d["q"], d["k"], d["v"], d["g"], d["beta_logit"], d["dO"], **common)
     else:
         out = gdr.kda_bwd(d["q"], d["k"], d["v"], d["g_raw"], d["A_log"], d["dt_bias"],
                           d["beta_logit"], d["dO"], kda_gate=x["kda_gate"], gate_scale=x["gate_scale"], **common)
     torch.cuda.synchronize()
+    assert_no_timeout(ws)
     return {k: v.cpu() for k, v in out.items()}
 
 
@@ -127,14 +151,16 @@ def run_gpu_fwd(x, states=None, workspace=None):
     import chunked_gated_delta_bwd_gb300 as gdr
     d = to_gpu(x)
     N = d["cu_seqlens"].numel() - 1
+    ws = _workspace(d, x, workspace)
     common = dict(h0=d["h0"], cu_seqlens=d["cu_seqlens"], num_seqs=N, scale=d["scale"], states=states,
-                  workspace=workspace)
+                  workspace=ws)
     if x["mode"] == "gdn":
         out = gdr.gdr_fwd(d["q"], d["k"], d["v"], d["g"], d["beta_logit"], **common)
     else:
         out = gdr.kda_fwd(d["q"], d["k"], d["v"], d["g_raw"], d["A_log"], d["dt_bias"], d["beta_logit"],
                           kda_gate=x["kda_gate"], gate_scale=x["gate_scale"], **common)
     torch.cuda.synchronize()
+    assert_no_timeout(ws)
     return {k: v.cpu() for k, v in out.items()}
 
 
