@@ -54,7 +54,7 @@ static_assert(CH * LDF * 4 >= TILE, "the raw-gate tile fits the space of A");
 static_assert(nTmp >= 4 * PD, "the gate scan's minima fit the transfer tiles");
 constexpr int nInvQ = 64, nInvK = 64, nBeta = 64, nFac = 256, nRef = 128, nGT = 128, nScan = 512;
 constexpr int SMALL_FLOATS = nInvQ + nInvK + nBeta + nFac + nRef + nGT + nScan;
-constexpr int SMEM_BYTES = oSmall + SMALL_FLOATS * 4 + 64 + 1024;
+constexpr int SMEM_BYTES = oSmall + SMALL_FLOATS * 4 + 128 + 1024;  // + barriers, tensor-memory slot, chunk info
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 constexpr uint32_t R_G1 = 0, R_W = 64, R_U = 128, R_R = 192, R_Q = 256, R_K = 320, R_G = 384;
 
@@ -96,15 +96,26 @@ __global__ void __launch_bounds__(512, 1) k_prep_kda(const Params p, const __gri
     float* sScan = sGT + nGT;     // [4][128]
     uint64_t* mbars = reinterpret_cast<uint64_t*>(sScan + nScan);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(mbars + 4);
+    // chunk info of the items of parity 0 and 1 (an item's slot is filled two items ahead: the
+    // lookup's dependent integer chain costs hundreds of cycles inside the busy loop)
+    int* sCI = reinterpret_cast<int*>(mbars + 6);
+    auto put_ci = [&](int slot, const ChunkInfo& c) {
+        int* d = sCI + 8 * slot;
+        d[0] = c.seq, d[1] = c.local, d[2] = (int)(c.t0 & 0xffffffff), d[3] = (int)(c.t0 >> 32), d[4] = c.len;
+    };
+    auto get_ci = [&](int slot) {
+        const int* d = sCI + 8 * slot;
+        ChunkInfo c;
+        c.seq = d[0], c.local = d[1], c.t0 = (int64_t)(((uint64_t)(uint32_t)d[3] << 32) | (uint32_t)d[2]), c.len = d[4];
+        return c;
+    };
     const uint32_t mb = smem_u32(mbars), mload0 = smem_u32(mbars + 1);  // load barriers: one per stage
     const uint32_t mgr = smem_u32(mbars + 3);                            // the raw-gate tile
 
     // q, k, v of item `it` into stage s: copy `which` (0 q, 1 k, 2 v) or all (which < 0); the
     // copies may be issued by different threads in any order (the barrier's transaction
     // count can run ahead of the expectation registered with copy 0)
-    auto issue_loads = [&](int item, int stg, int which) {
-        ChunkInfo cj;
-        lookup_chunk(item / p.H, p.N, p.chunk_off, p.cu_seqlens, p.seq_len, cj);
+    auto issue_loads = [&](int item, const ChunkInfo& cj, int stg, int which) {
         const int hh = item % p.H, t0 = (int)cj.t0;
         const uint32_t bar = mload0 + 8 * stg, st = sb + stg * STAGE;
         if (which <= 0) {
@@ -116,9 +127,7 @@ __global__ void __launch_bounds__(512, 1) k_prep_kda(const Params p, const __gri
     };
     // raw gates of `item`, token-major, into the space of A (dead from the end of the
     // inversion to the next item's G1)
-    auto issue_gate_load = [&](int item) {
-        ChunkInfo cj;
-        lookup_chunk(item / p.H, p.N, p.chunk_off, p.cu_seqlens, p.seq_len, cj);
+    auto issue_gate_load = [&](int item, const ChunkInfo& cj) {
         tc::mbar_expect_tx(mgr, TILE);
         tc::tma_load_4d(sb + oA, &m.graw, 0, item % p.H, (int)cj.t0, 0, mgr);
     };
@@ -128,9 +137,15 @@ __global__ void __launch_bounds__(512, 1) k_prep_kda(const Params p, const __gri
         tc::mbar_init(mload0, 1);
         tc::mbar_init(mload0 + 8, 1);
         tc::mbar_init(mgr, 1);
-        if ((int)blockIdx.x < n_items) {
-            issue_loads(blockIdx.x, 0, -1);
-            issue_gate_load(blockIdx.x);
+        for (int j = 0; j < 2; ++j) {  // the first two items' chunk info
+            ChunkInfo c{};
+            if ((int)blockIdx.x + j * (int)gridDim.x < n_items)
+                lookup_chunk(((int)blockIdx.x + j * (int)gridDim.x) / p.H, p.N, p.chunk_off, p.cu_seqlens, p.seq_len, c);
+            put_ci(j, c);
+            if (j == 0 && (int)blockIdx.x < n_items) {
+                issue_loads(blockIdx.x, c, 0, -1);
+                issue_gate_load(blockIdx.x, c);
+            }
         }
     }
     // T's blocks above the diagonal stay zero in the shared tile
@@ -178,9 +193,7 @@ __global__ void __launch_bounds__(512, 1) k_prep_kda(const Params p, const __gri
     // first read at the next item's top, so no thread waits for them
     float pbias = 0.f, palog = 0.f;
     unsigned short pb = 0;
-    auto prefetch_small = [&](int item) {
-        ChunkInfo cj;
-        lookup_chunk(item / p.H, p.N, p.chunk_off, p.cu_seqlens, p.seq_len, cj);
+    auto prefetch_small = [&](int item, const ChunkInfo& cj) {
         const int hh = item % p.H;
         if (tid < CH)
             pb = reinterpret_cast<const unsigned short*>(p.beta_logit)[(cj.t0 + min(tid, cj.len - 1)) * p.H + hh];
@@ -188,7 +201,7 @@ __global__ void __launch_bounds__(512, 1) k_prep_kda(const Params p, const __gri
         palog = p.A_log[hh];
     
     };
-    if ((int)blockIdx.x < n_items) prefetch_small(blockIdx.x);
+    if ((int)blockIdx.x < n_items) prefetch_small(blockIdx.x, get_ci(0));  // (slot written before the barrier above)
     // a[cq .. cq+15]
     auto rows16 = [&](const float* a, float (&o)[16], int cq) {
 #pragma unroll
@@ -212,9 +225,8 @@ __global__ void __launch_bounds__(512, 1) k_prep_kda(const Params p, const __gri
 
     for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++it) {
     const int chunk = item / p.H, h = item % p.H;
-    ChunkInfo ci;
-    lookup_chunk(chunk, p.N, p.chunk_off, p.cu_seqlens, p.seq_len, ci);
     const int stg = it & 1;
+    const ChunkInfo ci = get_ci(stg);
     unsigned char *sQ = smem + stg * STAGE + oQ, *sK = smem + stg * STAGE + oK, *sV = smem + stg * STAGE + oV;
     const uint32_t sQa = sb + stg * STAGE + oQ, sKa = sb + stg * STAGE + oK;
     const size_t tile_cc = ((size_t)chunk * p.H + h) * CH * CH;
@@ -229,7 +241,7 @@ __global__ void __launch_bounds__(512, 1) k_prep_kda(const Params p, const __gri
     {
         const float a = expf(palog);
         const float bias = pbias;
-        if (has_next) prefetch_small(item + gridDim.x);  // raw values, first read at the next item's top
+        if (has_next) prefetch_small(item + gridDim.x, get_ci(stg ^ 1));  // raw values, first read at the next item's top
         {
             const bool ok = tc::mbar_wait(mgr, (uint32_t)(it & 1));
             if (__syncthreads_or(!ok)) return bail();
@@ -421,6 +433,13 @@ __global__ void __launch_bounds__(512, 1) k_prep_kda(const Params p, const __gri
     __syncthreads();
     if (warp < 8) {
         inv::invert_tc(sA, sTf, sTmp, sT, p.Tm + tile_cc);
+        // (warps 6, 7 leave the inversion after its diagonal blocks) the chunk info of the item
+        // after next, into this item's slot
+        if (tid == 192 && item + 2 * (int)gridDim.x < n_items) {
+            ChunkInfo c2;
+            lookup_chunk((item + 2 * (int)gridDim.x) / p.H, p.N, p.chunk_off, p.cu_seqlens, p.seq_len, c2);
+            put_ci(stg, c2);
+        }
     } else {
         // T's zero blocks above the diagonal in the global tile: rows 16 b .. 16 b + 15,
         // columns from 16 (b + 1), 16-byte pieces (6 + 4 + 2 per row of block rows 0, 1, 2)
@@ -453,7 +472,7 @@ __global__ void __launch_bounds__(512, 1) k_prep_kda(const Params p, const __gri
         if (has_next) {
             if (tid == STORE_TID) {
                 tc::bulk_wait_read_but1();
-                issue_loads(item + gridDim.x, stg ^ 1, -1);
+                issue_loads(item + gridDim.x, get_ci(stg ^ 1), stg ^ 1, -1);
             }
             pending = stg ^ 1;
             pending_par = (uint32_t)(((it + 1) >> 1) & 1);
@@ -461,7 +480,7 @@ __global__ void __launch_bounds__(512, 1) k_prep_kda(const Params p, const __gri
     }
     sync_all();
     if (has_next) {  // the space of A is free: the next item's small inputs and raw gates
-        if (tid == 480) issue_gate_load(item + gridDim.x);  // (not the product-issuing thread)
+        if (tid == 480) issue_gate_load(item + gridDim.x, get_ci(stg ^ 1));  // (not the product-issuing thread)
         pending_g = true;
     }
 
