@@ -20,7 +20,8 @@
 // The inverse runs on warps 0-7 while warps 8-15 build the T-independent operands of the
 // next products.  The next item's beta logits and gate parameters are read one item ahead,
 // its raw-gate tile by TMA into the space of the dead fp32 matrices.  W, U, Kr, R_hi and
-// R_lo are staged in shared tiles that are dead by then and written by TMA stores.
+// R_lo are staged in shared tiles that are dead by then and written by TMA stores, T from
+// its bf16 shared tile (whose blocks above the diagonal stay zero).
 #include "gdr_chunk.cuh"
 #include "gdr_tc.cuh"
 #include "gdr_tma.h"
@@ -59,9 +60,9 @@ static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 constexpr uint32_t R_G1 = 0, R_W = 64, R_U = 128, R_R = 192, R_Q = 256, R_K = 320, R_G = 384;
 
 struct PrepMaps {
-    CUtensorMap q, k, v, graw, W, U, Kr, R, Rlo;
+    CUtensorMap q, k, v, graw, W, U, Kr, R, Rlo, T;
 };
-// The thread that issues the TMA stores of W, U, Kr, R_hi and R_lo and the copies of the
+// The thread that issues the TMA stores of W, U, Kr, R_hi, R_lo and T and the copies of the
 // next item's q, k and v: its stores read the stage that those copies overwrite, and a
 // bulk store's completion is visible only to the thread that issued it.
 constexpr int STORE_TID = 416;
@@ -432,7 +433,7 @@ __global__ void __launch_bounds__(512, 1) k_prep_kda(const Params p, const __gri
     }
     __syncthreads();
     if (warp < 8) {
-        inv::invert_tc(sA, sTf, sTmp, sT, p.Tm + tile_cc);
+        inv::invert_tc(sA, sTf, sTmp, sT, nullptr);
         // (warps 6, 7 leave the inversion after its diagonal blocks) the chunk info of the item
         // after next, into this item's slot
         if (tid == 192 && item + 2 * (int)gridDim.x < n_items) {
@@ -441,15 +442,6 @@ __global__ void __launch_bounds__(512, 1) k_prep_kda(const Params p, const __gri
             put_ci(stg, c2);
         }
     } else {
-        // T's zero blocks above the diagonal in the global tile: rows 16 b .. 16 b + 15,
-        // columns from 16 (b + 1), 16-byte pieces (6 + 4 + 2 per row of block rows 0, 1, 2)
-        const int t2 = tid - 256;
-        if (t2 < 192) {
-            const int b = t2 < 96 ? 0 : t2 < 160 ? 1 : 2;
-            const int base = b == 0 ? 0 : b == 1 ? 96 : 160, per = 6 - 2 * b;
-            const int r = 16 * b + (t2 - base) / per, piece = (t2 - base) % per;
-            *reinterpret_cast<uint4*>(p.Tm + tile_cc + r * CH + 16 * (b + 1) + 8 * piece) = make_uint4(0, 0, 0, 0);
-        }
         // (beta kd)^T -> the q tile's space ; (beta V)^T -> the k tile's space; this warp's
         // lanes for row quarters (hc - 2) and hc
         for (int pass = 0; pass < 2; ++pass) {
@@ -479,6 +471,10 @@ __global__ void __launch_bounds__(512, 1) k_prep_kda(const Params p, const __gri
         }
     }
     sync_all();
+    if (tid == STORE_TID) {  // T for the main backward (its blocks above the diagonal stay zero in the tile)
+        tc::tma_store_2d(&m.T, 0, (chunk * p.H + h) * CH, sb + oT);
+        tc::bulk_commit();
+    }
     if (has_next) {  // the space of A is free: the next item's small inputs and raw gates
         if (tid == 480) issue_gate_load(item + gridDim.x, get_ci(stg ^ 1));  // (not the product-issuing thread)
         pending_g = true;
@@ -577,12 +573,13 @@ static cudaError_t launch_prep_kda_t(const Params& p, cudaStream_t s) {
     PrepMaps m;
     const uint64_t T = (uint64_t)p.T_total;
     const uint64_t trows = (uint64_t)p.max_chunks * p.H * PD;  // rows of the [D][C] per chunk-head tiles
+    const uint64_t crows = (uint64_t)p.max_chunks * p.H * CH;  // rows of the [C][C] per chunk-head tiles
     if (!(encode_blocked_tokens_map(&m.q, p.q, T, p.Hk) && encode_blocked_tokens_map(&m.k, p.k, T, p.Hk) &&
           encode_blocked_tokens_map(&m.v, p.v, T, p.H) &&
           encode_blocked_tokens_map(&m.graw, p.g_raw, T, p.H) &&
           encode_rows_map(&m.W, p.W, trows, CH, PD) && encode_rows_map(&m.U, p.U, trows, CH, PD) &&
           encode_rows_map(&m.Kr, p.Kr, trows, CH, PD) && encode_rows_map(&m.R, p.R, trows, CH, PD) &&
-          encode_rows_map(&m.Rlo, p.Rlo, trows, CH, PD)))
+          encode_rows_map(&m.Rlo, p.Rlo, trows, CH, PD) && encode_rows_map(&m.T, p.Tm, crows, CH, CH)))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(k_prep_kda<GATE>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
