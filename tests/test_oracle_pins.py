@@ -9,6 +9,9 @@
   v for the key just written), which fixes the order of decay and update;
 * tangency of the L2-norm backward ("FlashKDA之backward（K1）", §3.3.2);
 * varlen equals separate per-sequence runs; linearity in (dO, dht);
+* the KDA gate values at points where softplus and sigmoid have closed forms
+  (ln 2, ln 4, ln(4/3); 1/2, 3/4, 1/4) and the identities softplus(x) - softplus(-x)
+  = x and sigmoid(z) + sigmoid(-z) = 1, alone and through the whole KDA path;
 * the worked examples of the pages (tests/golden/).
 """
 import json
@@ -137,6 +140,96 @@ def test_sigmoid_gate_value_at_vanishing_slope():
     assert np.abs(a["dg_raw"]).max() < 1e-20
     # and the gate parameters' gradients are the chain-rule sums of the per-element terms
     np.testing.assert_allclose(a["ddt_bias"], a["dg_raw"].sum(axis=0), rtol=1e-12, atol=0)
+
+
+# ----------------------------------------------------------------------------
+# KDA gate values where they have a closed form (the finite-difference pins fix
+# only the chain rule of whatever gate the oracle computes, not its value)
+# ----------------------------------------------------------------------------
+LN2, LN3 = np.log(2.0), np.log(3.0)
+
+
+def _gate_inputs(x, A_log, dt_bias):
+    """g_raw [1, H, D] such that g_raw + dt_bias = x (x [D]), for every head."""
+    A_log = np.asarray(A_log, float)
+    dt_bias = np.asarray(dt_bias, float)
+    g_raw = (np.asarray(x, float)[None, :] - dt_bias)[None]
+    return g_raw, A_log, dt_bias
+
+
+def test_softplus_gate_values_at_closed_form_points():
+    # softplus(0) = ln 2, softplus(ln 3) = ln 4, softplus(-ln 3) = ln(4/3); the gate is
+    # -e^{A_log[h]} softplus(g_raw + dt_bias[h, d]); two heads with e^{A_log} = 1 and 2, and
+    # dt_bias different per head and channel, so that a dropped or subtracted dt_bias, a
+    # missing factor e^{A_log} or a wrong sign changes the value
+    x = np.array([0.0, LN3, -LN3])
+    g_raw, A_log, dt_bias = _gate_inputs(x, [0.0, LN2], [[0.25, -0.5, 1.0], [-0.75, 0.3, 0.1]])
+    g = oracle.kda_gate(g_raw, A_log, dt_bias)
+    sp = np.array([LN2, 2 * LN2, 2 * LN2 - LN3])
+    expect = -np.array([1.0, 2.0])[:, None] * sp[None, :]
+    np.testing.assert_allclose(g[0], expect, rtol=1e-14, atol=0)
+    # far from zero: softplus(x) -> x for large x and -> e^{x} for very negative x
+    g_raw, A_log, dt_bias = _gate_inputs([40.0, -40.0], [LN2], [[0.5, -0.5]])
+    g = oracle.kda_gate(g_raw, A_log, dt_bias)[0, 0]
+    assert g[0] == pytest.approx(-80.0, rel=1e-15)
+    assert g[1] < 0 and g[1] == pytest.approx(-2 * np.exp(-40.0), rel=1e-12)
+    # softplus(x) - softplus(-x) = x, so g(x) - g(-x) = -e^{A_log} x at any x
+    rng = np.random.default_rng(51)
+    xs = 3 * rng.standard_normal(16)
+    gp = oracle.kda_gate(*_gate_inputs(xs, [-0.4], np.zeros((1, 16))))[0, 0]
+    gm = oracle.kda_gate(*_gate_inputs(-xs, [-0.4], np.zeros((1, 16))))[0, 0]
+    np.testing.assert_allclose(gp - gm, -np.exp(-0.4) * xs, rtol=1e-12, atol=1e-14)
+
+
+def test_sigmoid_gate_values_at_closed_form_points():
+    # sigmoid(0) = 1/2, sigmoid(ln 3) = 3/4, sigmoid(-ln 3) = 1/4; the natural-log gate is
+    # ln2 gate_scale sigmoid(e^{A_log} (g_raw + dt_bias)); with e^{A_log} = 2, x = ln(3)/2
+    # reaches the argument ln 3
+    gs = -2.5
+    x = np.array([0.0, LN3 / 2, -LN3 / 2])
+    g_raw, A_log, dt_bias = _gate_inputs(x, [LN2], [[0.2, -0.7, 0.4]])
+    g = oracle.kda_sigmoid_gate(g_raw, A_log, dt_bias, gs)[0, 0]
+    np.testing.assert_allclose(g, LN2 * gs * np.array([0.5, 0.75, 0.25]), rtol=1e-14, atol=0)
+    # sigmoid(z) + sigmoid(-z) = 1, so g(x) + g(-x) = ln2 gate_scale at any x
+    rng = np.random.default_rng(52)
+    xs = 2 * rng.standard_normal(16)
+    gp = oracle.kda_sigmoid_gate(*_gate_inputs(xs, [0.3], np.zeros((1, 16))), gs)[0, 0]
+    gm = oracle.kda_sigmoid_gate(*_gate_inputs(-xs, [0.3], np.zeros((1, 16))), gs)[0, 0]
+    np.testing.assert_allclose(gp + gm, LN2 * gs, rtol=1e-13, atol=0)
+
+
+@pytest.mark.parametrize("gate", ["softplus", "sigmoid"])
+def test_kda_path_at_a_closed_form_gate(gate):
+    # g_raw + dt_bias = x0 for every token and channel puts the whole KDA path on a constant
+    # log gate known in closed form, so it must equal the plain recurrence with that gate;
+    # its gradients are then the chain rule with the closed-form slope:
+    #   softplus, e^{A_log} = 1, x0 = ln 3:  g = -ln 4,          dg/dx = -3/4,     dg/dA_log = g
+    #   sigmoid,  e^{A_log} = 2, x0 = ln(3)/2: g = (3/4) ln2 gs,   dg/dx = 2 ln2 gs (3/16),
+    #                                         dg/dA_log = x0 dg/dx
+    rng = np.random.default_rng(53)
+    c = _rand_case(rng, (7, 5), 2, 4, "kda")
+    gs = -2.0
+    if gate == "softplus":
+        a, x0 = 1.0, LN3
+        glog0, slope = -2 * LN2, -0.75
+        dA_fac = glog0
+    else:
+        a, x0 = 2.0, LN3 / 2
+        glog0, slope = 0.75 * LN2 * gs, a * LN2 * gs * 3.0 / 16.0
+        dA_fac = x0 * slope
+    T = c["q"].shape[0]
+    A_log = np.full(2, np.log(a))
+    g_raw = np.broadcast_to(x0 - c["dt_bias"][None], (T, 2, 4)).copy()
+    r = oracle.kda(c["q"], c["k"], c["v"], g_raw, A_log, c["dt_bias"], c["b"], c["scale"], c["cu"],
+                   h0=c["h0"], dO=c["dO"], dht=c["dht"], gate=gate, gate_scale=gs)
+    glog = np.full(c["q"].shape, glog0)
+    b = oracle.gated_delta(c["q"], c["k"], c["v"], glog, c["b"], c["scale"], c["cu"], h0=c["h0"], dO=c["dO"],
+                           dht=c["dht"])
+    for key in ("o", "ht", "dq", "dk", "dv", "dbeta", "dh0"):
+        np.testing.assert_allclose(r[key], b[key], rtol=1e-12, atol=1e-13, err_msg=key)
+    np.testing.assert_allclose(r["dg_raw"], slope * b["dglog"], rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(r["ddt_bias"], slope * b["dglog"].sum(axis=0), rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(r["dA_log"], dA_fac * b["dglog"].sum(axis=(0, 2)), rtol=1e-12, atol=1e-13)
 
 
 @pytest.mark.parametrize("mode", ["gdn", "kda"])
