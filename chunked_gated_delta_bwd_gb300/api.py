@@ -22,6 +22,8 @@ _LIB = None
 
 GDR_DEV_BAD_SEQLENS = 1
 GDR_DEV_GATE_RANGE = 2
+GDR_DEV_TIMEOUT = 4
+GDR_DEV_STATES_MISMATCH = 8
 
 
 class GdrShape(ctypes.Structure):
@@ -74,6 +76,8 @@ def lib():
         L.gdr_profile_begin.argtypes = [ctypes.c_int]
         L.gdr_profile_end.restype = ctypes.c_int
         L.gdr_profile_end.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)]
+        L.gdr_test_stall_next_call.restype = None
+        L.gdr_test_stall_next_call.argtypes = [ctypes.c_int]
         _LIB = L
     return _LIB
 
@@ -343,6 +347,12 @@ def workspace_status(workspace) -> int:
     st = ctypes.c_int(0)
     _check(lib().gdr_workspace_status(_ptr(workspace), _stream(), ctypes.byref(st)), "gdr_workspace_status")
     return st.value
+
+
+def test_stall_next_call(cta: int):
+    """Test hook: hold CTA ``cta`` of the next GDN backward's main kernel (head_dim 128) on a
+    barrier nothing arrives on, so that its bounded wait runs out (GDR_DEV_TIMEOUT)."""
+    lib().gdr_test_stall_next_call(int(cta))
 
 
 KERNEL_NAMES = ("chunk_table", "prep", "states", "main", "out", "conv")

@@ -3,6 +3,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "../../include/gdr.h"
@@ -102,6 +103,34 @@ cudaError_t launch_group_sum(const Params& p, cudaStream_t s) {
     if (p.T_total == 0) return cudaSuccess;
     k_group_sum<<<8 * num_sms(), 256, 0, s>>>(p.dq, p.dk, p.dq_out, p.dk_out, p.T_total, p.H, p.Hk, p.D);
     return cudaGetLastError();
+}
+
+// The header of a saved-states buffer: what the states were computed for.
+struct StatesTag {
+    int v[16];
+};
+static StatesTag states_tag(const gdr_shape* sh, int kda, const float* h0, int64_t max_chunks) {
+    StatesTag t;
+    memset(&t, 0, sizeof(t));
+    t.v[0] = 0x53524447;  // "GDRS"
+    t.v[1] = 1;           // header version
+    t.v[2] = kda ? 1 + sh->kda_gate : 0;
+    t.v[3] = sh->num_seqs;
+    t.v[4] = sh->num_heads;
+    t.v[5] = sh->num_k_heads > 0 ? sh->num_k_heads : sh->num_heads;
+    t.v[6] = sh->head_dim;
+    t.v[7] = (int)(sh->total_tokens & 0xffffffff);
+    t.v[8] = (int)(sh->total_tokens >> 32);
+    t.v[9] = (int)max_chunks;
+    if (kda && sh->kda_gate == GDR_KDA_GATE_SIGMOID) memcpy(&t.v[10], &sh->gate_scale, 4);
+    t.v[11] = sh->cu_seqlens != nullptr;
+    t.v[12] = h0 != nullptr;
+    return t;
+}
+
+// writes the whole header (the tag, then zeros up to GDR_STATES_HEADER_BYTES)
+__global__ void k_states_tag(int* hdr, const StatesTag t) {
+    for (int i = threadIdx.x; i < GDR_STATES_HEADER_BYTES / 4; i += blockDim.x) hdr[i] = i < 16 ? t.v[i] : 0;
 }
 
 cudaError_t launch_chunk_table(const Params& p, cudaStream_t s) {
@@ -295,12 +324,14 @@ static gdr_status fwd_states_impl(const gdr_shape* sh, const void* q, const void
     p.beta_logit = (const __nv_bfloat16*)beta;
     p.g = g; p.g_raw = (const __nv_bfloat16*)g_raw; p.A_log = A_log; p.dt_bias = dt_bias;
     p.h0 = h0;
-    p.S0 = (__nv_bfloat16*)states;
+    p.S0 = reinterpret_cast<__nv_bfloat16*>(static_cast<unsigned char*>(states) + GDR_STATES_HEADER_BYTES);
     cudaStream_t s = (cudaStream_t)stream;
     gdr_status st = common_front(p, s);
     if (st != GDR_OK) return st;
     cudaError_t e = timed(GDR_KERNEL_STATES, s, [&] { return launch_states(p, true, false, s); });
     if (e != cudaSuccess) return cuda_fail(e, "state recurrence launch");
+    k_states_tag<<<1, 32, 0, s>>>(static_cast<int*>(states), states_tag(sh, kda, h0, L.max_chunks));
+    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "states header launch");
     g_err[0] = 0;
     return GDR_OK;
 }
@@ -324,7 +355,8 @@ static gdr_status fwd_impl(const gdr_shape* sh, const void* q, const void* k, co
     p.h0 = h0;
     p.o = (__nv_bfloat16*)o;
     p.ht = ht;
-    if (states) p.S0 = (__nv_bfloat16*)states;
+    if (states)
+        p.S0 = reinterpret_cast<__nv_bfloat16*>(static_cast<unsigned char*>(states) + GDR_STATES_HEADER_BYTES);
     p.Pm = p.dS;  // the state-gradient tiles of the backward are free in a forward call
     cudaStream_t s = (cudaStream_t)stream;
     gdr_status st = common_front(p, s);
@@ -333,9 +365,15 @@ static gdr_status fwd_impl(const gdr_shape* sh, const void* q, const void* k, co
     if (e != cudaSuccess) return cuda_fail(e, "state recurrence launch");
     e = timed(GDR_KERNEL_OUT, s, [&] { return launch_out(p, s); });
     if (e != cudaSuccess) return cuda_fail(e, "output launch");
+    if (states) {
+        k_states_tag<<<1, 32, 0, s>>>(static_cast<int*>(states), states_tag(sh, kda, h0, L.max_chunks));
+        if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "states header launch");
+    }
     g_err[0] = 0;
     return GDR_OK;
 }
+
+static std::atomic<int> g_test_stall{0};  // gdr_test_stall_next_call: CTA index + 1, or 0
 
 static gdr_status bwd_impl(const gdr_shape* sh, const void* q, const void* k, const void* v,
                            const float* g, const void* g_raw, const float* A_log, const float* dt_bias,
@@ -357,7 +395,14 @@ static gdr_status bwd_impl(const gdr_shape* sh, const void* q, const void* k, co
     p.dO = (const __nv_bfloat16*)dO; p.beta_logit = (const __nv_bfloat16*)beta;
     p.g = g; p.g_raw = (const __nv_bfloat16*)g_raw; p.A_log = A_log; p.dt_bias = dt_bias;
     p.h0 = h0; p.dht = dht;
-    if (states) p.S0 = (__nv_bfloat16*)states;
+    if (states) {
+        p.S0 = reinterpret_cast<__nv_bfloat16*>(const_cast<unsigned char*>(static_cast<const unsigned char*>(states)) +
+                                                GDR_STATES_HEADER_BYTES);
+        p.states_hdr = static_cast<const int*>(states);
+        const StatesTag t = states_tag(sh, kda, h0, L.max_chunks);
+        memcpy(p.states_tag, t.v, sizeof(t.v));
+    }
+    if (!kda && p.D == 128) p.test_stall = g_test_stall.exchange(0);
     p.dq = (__nv_bfloat16*)dq; p.dk = (__nv_bfloat16*)dk; p.dv = (__nv_bfloat16*)dv;
     if (p.Hk < p.H) {  // GQA: per-value-head terms in the workspace, summed over each group at the end
         p.dq_out = p.dq;
@@ -401,8 +446,10 @@ size_t gdr_workspace_bytes(const gdr_shape* shape) {
 size_t gdr_states_bytes(const gdr_shape* shape) {
     if (check_shape(shape) != GDR_OK) return 0;
     const Layout L = layout(shape);
-    return (size_t)L.max_chunks * shape->num_heads * shape->head_dim * shape->head_dim * 2;
+    return GDR_STATES_HEADER_BYTES + (size_t)L.max_chunks * shape->num_heads * shape->head_dim * shape->head_dim * 2;
 }
+
+void gdr_test_stall_next_call(int cta) { g_test_stall.store(cta >= 0 ? cta + 1 : 0); }
 
 gdr_status gdr_fwd_states(const gdr_shape* shape, const void* q, const void* k, const void* v,
                           const float* g, const void* beta_logit, const float* h0, void* states,

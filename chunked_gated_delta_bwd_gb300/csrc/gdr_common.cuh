@@ -21,6 +21,7 @@ constexpr int CH = 64;  // chunk length
 constexpr int ST_BAD_SEQLENS = 1;  // cu_seqlens not monotone / wrong total
 constexpr int ST_GATE_RANGE = 2;   // a chunk's gate span exceeds the exponent range handled
 constexpr int ST_MMA_TIMEOUT = 4;  // a bounded wait for the tensor cores ran out (the CTA gave up)
+constexpr int ST_STATES_MISMATCH = 8;  // the states buffer was written for another variant or shape
 
 // --------------------------------------------------------------------------
 // small utilities

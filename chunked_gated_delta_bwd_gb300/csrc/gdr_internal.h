@@ -44,6 +44,12 @@ struct Params {
     int seg_G, seg_G1;
     float *segL, *segLb, *segP, *segS;
 
+    // saved chunk states (a backward from the buffer of a forward call): the buffer's header,
+    // which the main kernels compare with the header this call expects, or nullptr
+    const int* states_hdr;
+    int states_tag[16];
+    int test_stall;                 // test hook: main-kernel CTA index + 1 held at its first item (0: none)
+
     // outputs
     __nv_bfloat16* o;               // forward output [T,H,D]
     float* ht;                      // forward final state [N,H,D,D] (key-major), or nullptr
@@ -55,6 +61,18 @@ struct Params {
 
 // q / k head of value head h
 __host__ __device__ __forceinline__ int qk_head(const Params& p, int h) { return h / (p.H / p.Hk); }
+
+#ifdef __CUDACC__
+// The saved states' header matches this call (or the states are recomputed inside the call).
+// Every thread of a CTA reads the same 16 words, so the answer is uniform over the CTA.
+__device__ __forceinline__ bool states_header_ok(const Params& p) {
+    if (!p.states_hdr) return true;
+    bool ok = true;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) ok &= __ldg(p.states_hdr + i) == p.states_tag[i];
+    return ok;
+}
+#endif
 
 // multiprocessors of the current device (cached per device)
 inline int num_sms() {

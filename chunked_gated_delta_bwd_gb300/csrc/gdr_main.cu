@@ -51,6 +51,10 @@ struct MainSmem {
 
 template <int D, bool KDA>
 __global__ void __launch_bounds__(256, 1) k_main(const Params p) {
+    if (!states_header_ok(p)) {  // saved states of another variant or shape: write nothing
+        if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(p.status, ST_STATES_MISMATCH);
+        return;
+    }
     using SM = MainSmem<D, KDA>;
     using TileCD = SwzTile<SM::ROWB>;
     using TileCC = SwzTile<128>;

@@ -73,6 +73,10 @@ constexpr int STORE_TID = 96;  // the thread that issues the TMA stores of dq, d
 }  // namespace
 
 __global__ void __launch_bounds__(512, 1) k_main_gdn(const Params p, const __grid_constant__ GdnMaps m) {
+    if (!states_header_ok(p)) {  // saved states of another variant or shape: write nothing
+        if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(p.status, ST_STATES_MISMATCH);
+        return;
+    }
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     const uint32_t sb = smem_u32(smem);
@@ -110,6 +114,7 @@ __global__ void __launch_bounds__(512, 1) k_main_gdn(const Params p, const __gri
     // operand tiles of an item; MMA completion of the batches with 1, 2 and 3 issuing threads
     const uint32_t mload = smem_u32(mbars), mb1 = smem_u32(mbars + 1), mb2 = smem_u32(mbars + 2),
                    mb3 = smem_u32(mbars + 3);
+    const uint32_t mstall = smem_u32(mbars + 5);  // test hook only: a barrier nothing arrives on
 
     Gates<MD, false> G;
     G.gc = sGate;
@@ -153,6 +158,7 @@ __global__ void __launch_bounds__(512, 1) k_main_gdn(const Params p, const __gri
         tc::mbar_init(mb1, 1);
         tc::mbar_init(mb2, 2);
         tc::mbar_init(mb3, 3);
+        tc::mbar_init(mstall, 1);
         if ((int)blockIdx.x < n_items) {
             ChunkInfo c0i;
             lookup_chunk((int)blockIdx.x / p.H, p.N, p.chunk_off, p.cu_seqlens, p.seq_len, c0i);
@@ -277,7 +283,11 @@ __global__ void __launch_bounds__(512, 1) k_main_gdn(const Params p, const __gri
 
     // wait for the operand tiles; rows past the chunk's end are zeroed before any product
     {
-        const bool ok = tc::mbar_wait(mload, (uint32_t)(it & 1));
+        bool ok = tc::mbar_wait(mload, (uint32_t)(it & 1));
+        // test hook: the chosen CTA also waits, briefly, on a barrier that no copy, product or
+        // thread ever completes, and so takes the same exit as a timed-out wait (its loads in
+        // flight have landed: the wait above completed; no product has been issued)
+        if (p.test_stall == (int)blockIdx.x + 1 && it == 0 && tid == 0) ok = ok && tc::mbar_wait(mstall, 0, 1 << 12);
         if (__syncthreads_or(!ok)) return bail();
         pending = false;
     }

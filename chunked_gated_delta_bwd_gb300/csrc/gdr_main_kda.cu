@@ -71,6 +71,10 @@ constexpr int STORE_TID = 96;  // the thread that issues the TMA stores of dq, d
 
 template <int GATE>
 __global__ void __launch_bounds__(512, 1) k_main_kda(const Params p, const __grid_constant__ MainMaps m) {
+    if (!states_header_ok(p)) {  // saved states of another variant or shape: write nothing
+        if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(p.status, ST_STATES_MISMATCH);
+        return;
+    }
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     const uint32_t sb = smem_u32(smem);

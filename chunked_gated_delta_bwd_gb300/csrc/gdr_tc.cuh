@@ -66,9 +66,9 @@ __device__ __forceinline__ void mbar_init(uint32_t mbar, int count) {
 
 // Bounded wait for the phase `parity` of an mbarrier.  Returns false (and the
 // caller records an error) if the phase did not complete within the limit.
-__device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity, int limit = 1 << 24) {
     uint32_t done = 0;
-    for (int it = 0; it < (1 << 24) && !done; ++it) {
+    for (int it = 0; it < limit && !done; ++it) {
         asm volatile(
             "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
             : "=r"(done)

@@ -66,6 +66,9 @@ typedef enum {
 #define GDR_DEV_BAD_SEQLENS 1 /* cu_seqlens not non-decreasing from 0 to T_total */
 #define GDR_DEV_GATE_RANGE 2  /* a chunk's log-gate span exceeded 160 (or a cumulative gate > 80) */
 #define GDR_DEV_TIMEOUT 4     /* a bounded wait for the tensor cores ran out; that CTA's outputs are missing */
+#define GDR_DEV_STATES_MISMATCH 8 /* gdr_bwd / kda_bwd got a states buffer written for another variant,
+                                     gate function, h0 presence or shape: the main backward wrote none
+                                     of dq, dk, dv, dg / dg_raw, dbeta, dA_log, ddt_bias */
 
 typedef struct {
     int32_t num_seqs;          /* N >= 1 */
@@ -95,10 +98,21 @@ typedef struct {
  * kda_bwd need for this shape (returns 0 for an invalid shape). */
 size_t gdr_workspace_bytes(const gdr_shape* shape);
 
-/* Bytes of the per-chunk state buffer written by gdr_fwd_states / kda_fwd_states:
- * the bf16 chunk-start state of every 64-token chunk and head, stored value-major
- * ([chunk][head][dv][dk], i.e. S^T, the layout the tensor-core products read), with
- * chunks numbered sequence after sequence. */
+/* Bytes of the per-chunk state buffer written by gdr_fwd_states / kda_fwd_states /
+ * gdr_fwd / kda_fwd: a header of GDR_STATES_HEADER_BYTES, then the bf16 chunk-start
+ * state of every 64-token chunk and head, stored value-major ([chunk][head][dv][dk],
+ * i.e. S^T, the layout the tensor-core products read), with chunks numbered sequence
+ * after sequence.
+ *
+ * The header records what the states were computed for: the variant (GDN, KDA with
+ * the softplus gate, KDA with the sigmoid-bounded gate and its gate_scale), whether
+ * h0 was given, N, H, Hk, D, T_total and dense / varlen.  gdr_bwd and kda_bwd compare
+ * it on the device with their own call (the call itself is asynchronous and cannot
+ * wait for the buffer): on any difference the main backward writes nothing and
+ * raises GDR_DEV_STATES_MISMATCH in the workspace status word.  The header cannot
+ * tell two inputs of one shape apart: the caller passes the states of the inputs it
+ * differentiates. */
+#define GDR_STATES_HEADER_BYTES 256
 size_t gdr_states_bytes(const gdr_shape* shape);
 
 /* Forward chunk states for GDN (the "forward workspace" of the FlashKDA
@@ -118,8 +132,9 @@ gdr_status kda_fwd_states(const gdr_shape* shape, const void* q, const void* k, 
 
 /* GDN forward: the output o (bf16 [T_total, H, D]) and, if ht is not NULL, the final
  * state of every sequence and head (fp32 [N, H, D, D], row = key channel), from the
- * chunked form of the recurrence ("FlashKDA之backward（K1）" §2: per chunk
- * o = qd S0 + P u with the WY/UT factors).  If `states` is not NULL it also receives
+ * chunked form of the recurrence (the forward that the backward of
+ * "FlashKDA之backward（K1）" undoes, its §0.1: per chunk o = qd S0 + P u with the
+ * WY/UT factors).  If `states` is not NULL it also receives
  * the chunk-start states (the buffer of gdr_fwd_states; states_bytes >=
  * gdr_states_bytes), so a following gdr_bwd can skip their recomputation.  Uses the
  * same workspace as gdr_bwd (gdr_workspace_bytes). */
@@ -165,7 +180,10 @@ gdr_status kda_bwd(const gdr_shape* shape, const void* q, const void* k, const v
  *    GDR_ERR_WORKSPACE (message in gdr_last_error) before anything is enqueued.
  *  * The first call on a device (per process) resolves the array's device
  *    address with cudaGetSymbolAddress, with that device current; make that
- *    first call before any stream capture.
+ *    first call before any stream capture.  The address is kept for the life of
+ *    the process: after a cudaDeviceReset of that device (which unloads the
+ *    library's device code and may move the array) this entry point must not be
+ *    called again in the same process.
  *  * Every call on a device shares the one array and leaves its contents
  *    behind: calls that overlap on the GPU (different streams, or threads
  *    without ordering) race; serialise them, e.g. on one stream.
@@ -200,6 +218,16 @@ gdr_status gdr_conv1d_bwd(int32_t num_seqs, int64_t total_tokens, int32_t channe
 /* Waits for `stream`, then returns in *device_status the OR of the GDR_DEV_*
  * bits raised by the last call that used `workspace` (0 = none). */
 gdr_status gdr_workspace_status(const void* workspace, void* stream, int* device_status);
+
+/* Test hook (not part of the method; off unless called).  Makes the next gdr_bwd
+ * call on any thread with head_dim 128 hold CTA `cta` of its main backward kernel at
+ * its first item on an mbarrier that nothing arrives on, under a short bounded wait
+ * (no copy or tensor-core operation is pending on that barrier).  The wait runs out,
+ * the CTA records GDR_DEV_TIMEOUT, drains the tile loads it has issued, releases its
+ * tensor memory and exits; the other CTAs finish.  It exercises the path every bounded
+ * wait of the kernels takes when the tensor cores do not answer, without a GPU fault.
+ * cta < 0 clears a pending request.  Not thread-safe with concurrent gdr_bwd calls. */
+void gdr_test_stall_next_call(int cta);
 
 /* Message of the last error returned on the calling thread ("" if none). */
 const char* gdr_last_error(void);

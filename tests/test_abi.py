@@ -41,7 +41,8 @@ def test_library_exports_every_declared_symbol(L):
 def test_workspace_sizes(L):
     sh = gdr.make_shape(1, 32768, 16, 128)
     chunks = 512
-    assert gdr.states_bytes(sh) == chunks * 16 * 128 * 128 * 2
+    HDR = 256  # GDR_STATES_HEADER_BYTES
+    assert gdr.states_bytes(sh) == HDR + chunks * 16 * 128 * 128 * 2
     ws = gdr.workspace_bytes(sh)
     tiles = chunks * 16 * (5 * 64 * 128 * 2 + 64 * 64 * 2 + 2 * 128 * 4 + 2 * 128 * 128 * 2)
     # time-parallel state passing: 4 segments per (sequence, head) when both directions run,
@@ -51,7 +52,7 @@ def test_workspace_sizes(L):
     # varlen bound: sum ceil(len/64) <= (T + 63 N) / 64
     fake_cu = ctypes.c_void_p(256)
     sh2 = api.GdrShape(3, 130, 2, 64, fake_cu.value, 0.125)
-    assert gdr.states_bytes(sh2) == ((130 + 63 * 3) // 64) * 2 * 64 * 64 * 2
+    assert gdr.states_bytes(sh2) == HDR + ((130 + 63 * 3) // 64) * 2 * 64 * 64 * 2
 
 
 @pytest.mark.parametrize("mutate,code", [

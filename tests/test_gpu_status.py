@@ -1,0 +1,83 @@
+"""Device-side status reporting, on the GPU, with no fault: a states buffer written
+for another variant or shape is refused by the backward, and a bounded wait that runs
+out (the test hook holds one CTA on a barrier that nothing arrives on) leaves a
+status bit and a usable context behind."""
+import pytest
+import torch
+
+import chunked_gated_delta_bwd_gb300 as gdr
+from chunked_gated_delta_bwd_gb300 import inputs
+from tests import helpers as H
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from chunked_gated_delta_bwd_gb300 import build
+    build.build()
+
+
+def _states(mode, x, **kw):
+    d = H.to_gpu(x)
+    if mode == "gdn":
+        return gdr.gdr_fwd_states(d["q"], d["k"], d["v"], d["g"], d["beta_logit"], h0=d["h0"],
+                                  cu_seqlens=d["cu_seqlens"], scale=d["scale"], **kw)
+    return gdr.gdr_fwd_states(d["q"], d["k"], d["v"], None, d["beta_logit"], h0=d["h0"],
+                              cu_seqlens=d["cu_seqlens"], scale=d["scale"], gate="kda", g_raw=d["g_raw"],
+                              A_log=d["A_log"], dt_bias=d["dt_bias"], **kw)
+
+
+def _status_after(x, states):
+    ws = H._workspace(H.to_gpu(x), x, None)
+    d = H.to_gpu(x)
+    N = d["cu_seqlens"].numel() - 1
+    common = dict(h0=d["h0"], dht=d["dht"], cu_seqlens=d["cu_seqlens"], num_seqs=N, scale=d["scale"],
+                  states=states, workspace=ws)
+    if x["mode"] == "gdn":
+        gdr.gdr_bwd(d["q"], d["k"], d["v"], d["g"], d["beta_logit"], d["dO"], **common)
+    else:
+        gdr.kda_bwd(d["q"], d["k"], d["v"], d["g_raw"], d["A_log"], d["dt_bias"], d["beta_logit"], d["dO"],
+                    kda_gate=x["kda_gate"], gate_scale=x["gate_scale"], **common)
+    torch.cuda.synchronize()
+    return gdr.workspace_status(ws)
+
+
+@pytest.mark.parametrize("dim", [64, 128])
+def test_states_of_another_variant_or_shape_are_refused(dim):
+    lens = [200, 77]
+    xg = inputs.custom("gdn", lens, heads=2, dim=dim, seed=120, with_h0=True, with_dht=True)
+    xk = inputs.custom("kda", lens, heads=2, dim=dim, seed=120, with_h0=True, with_dht=True)
+    st_g, st_k = _states("gdn", xg), _states("kda", xk)
+    # the matching buffers are accepted
+    assert _status_after(xg, st_g) == 0
+    assert _status_after(xk, st_k) == 0
+    # a GDN buffer given to the KDA backward and the other way round
+    assert _status_after(xk, st_g) & gdr.api.GDR_DEV_STATES_MISMATCH
+    assert _status_after(xg, st_k) & gdr.api.GDR_DEV_STATES_MISMATCH
+    # the sigmoid-bounded gate is another variant of KDA
+    xs = dict(xk, kda_gate="sigmoid", gate_scale=-2.0)
+    assert _status_after(xs, st_k) & gdr.api.GDR_DEV_STATES_MISMATCH
+    # states computed without h0 for a call with h0
+    st_noh0 = _states("gdn", dict(xg, h0=None))
+    assert _status_after(xg, st_noh0) & gdr.api.GDR_DEV_STATES_MISMATCH
+    # another shape (a larger buffer: the same lengths plus a third sequence)
+    x3 = inputs.custom("gdn", lens + [64], heads=2, dim=dim, seed=121, with_h0=True, with_dht=True)
+    assert _status_after(xg, _states("gdn", x3)) & gdr.api.GDR_DEV_STATES_MISMATCH
+
+
+def test_timed_out_wait_sets_the_status_and_leaves_the_context_usable():
+    x = inputs.custom("gdn", [700, 300, 64], heads=4, dim=128, seed=122, with_h0=True, with_dht=True)
+    d = H.to_gpu(x)
+    ws = H._workspace(d, x, None)
+    gdr.api.test_stall_next_call(0)
+    gdr.gdr_bwd(d["q"], d["k"], d["v"], d["g"], d["beta_logit"], d["dO"], h0=d["h0"], dht=d["dht"],
+                cu_seqlens=d["cu_seqlens"], num_seqs=3, scale=d["scale"], workspace=ws)
+    torch.cuda.synchronize()  # the call returned and its work completed
+    assert gdr.workspace_status(ws) & gdr.api.GDR_DEV_TIMEOUT
+    # the hook is one-shot: the next call on the same device runs in full and passes parity
+    gpu = H.run_gpu(x, workspace=ws)
+    assert gdr.workspace_status(ws) == 0
+    print(H.assert_parity(H.compare(gpu, H.run_oracle(x), x), "after timeout"))
