@@ -35,13 +35,20 @@ UNIT = "Mtokens/s"
 CASE_G, CASE_K = inputs.CASES["gdn_h16_t32k"], inputs.CASES["kda_h16_t32k"]
 TOKENS_PER_STEP = CASE_G.seq_len * CASE_G.num_seqs + CASE_K.seq_len * CASE_K.num_seqs
 
-# Algorithmic figures of the main backward kernel per token-head (D = 128, C = 64):
-# 16 products per chunk: 5 of C*D*D and 11 of C*C*D  ->  10 D^2 + 22 C D flops;
-# bytes: q,k,v,dO + beta + gate + S0 + dS_C + T read, dq,dk,dv + dbeta + dgate written.
+# Algorithmic figures of the backward per token-head (D = 128, C = 64), the method's own:
+#   flops: the 18 products of a chunk (7 of C*D*D, 11 of C*C*D) = 14 D^2 + 22 C D = 409 600;
+#   bytes with the chunk-start states saved in bf16: q, k, v, dO (4 * 2D) + gate + beta +
+#   S0 (2 D^2 / C) read, dq, dk, dv (3 * 2D) + dgate + dbeta written = 2316 (GDN: fp32 scalar gate
+#   and gradient) or 2820 (KDA: bf16 per-channel raw gate and gradient, 2D each); plus 4 D^2 per
+#   (sequence, head) for each of h0, dht and dh0.
 D_, C_ = 128, 64
-MAIN_FLOP_PER_TH = 10 * D_ * D_ + 22 * C_ * D_
-MAIN_BYTES_PER_TH = {"gdn": 4 * 2 * D_ + 2 + 4 + 2 * (2 * D_ * D_ // C_) + 2 * C_ + 3 * 2 * D_ + 2 + 4,
-                     "kda": 4 * 2 * D_ + 2 + 2 * D_ + 2 * (2 * D_ * D_ // C_) + 2 * C_ + 3 * 2 * D_ + 2 + 2 * D_}
+BWD_FLOP_PER_TH = 14 * D_ * D_ + 22 * C_ * D_
+BWD_BYTES_PER_TH = {"gdn": 4 * 2 * D_ + 4 + 2 + 2 * D_ * D_ // C_ + 3 * 2 * D_ + 4 + 2,
+                    "kda": 4 * 2 * D_ + 2 * D_ + 2 + 2 * D_ * D_ // C_ + 3 * 2 * D_ + 2 * D_ + 2}
+assert BWD_FLOP_PER_TH == 409600 and BWD_BYTES_PER_TH == {"gdn": 2316, "kda": 2820}
+# What this design's main kernel moves per token-head besides (the dS_C and T tiles it reads
+# from the state and prep kernels' output), for the design-byte figure reported beside.
+MAIN_DESIGN_EXTRA_PER_TH = 2 * D_ * D_ // C_ + 2 * C_
 # Forward output kernel (o = R S0 + P U per chunk) per token-head: reads S0 (2 D^2 / C), R^T and
 # U^T (2 D each), P (2 C); writes o (2 D).  Flops: 2 (D^2 + C D).
 OUT_BYTES_PER_TH = 2 * D_ * D_ // C_ + 2 * D_ + 2 * D_ + 2 * C_ + 2 * D_
@@ -491,13 +498,18 @@ def main_gpu(args):
         fr.update(peak=hbm, frac=fr["achieved"] / hbm, peak_source=src + " (hbm_gbs)")
     dom = max(prof, key=lambda k: prof[k][0])
     th = CASE_G.seq_len * CASE_G.heads  # token-heads per variant
+    pair_bytes = 3 * 4 * D_ * D_ * CASE_G.num_seqs * CASE_G.heads  # h0, dht read, dh0 written
+    alg_bytes = {m: th * BWD_BYTES_PER_TH[m] + pair_bytes for m in ("gdn", "kda")}
+    alg_flop = th * BWD_FLOP_PER_TH
     roof = None
     if dom == "main" and prof["main"][1] > 0:
+        # the dominant kernel: the method's algorithmic bytes and flops of one backward over its
+        # launch time (the main kernel is the step that reads the inputs and writes the gradients)
         n_main = prof["main"][1]
         avg_s = prof["main"][0] / n_main * 1e-3
-        bytes_avg = th * (MAIN_BYTES_PER_TH["gdn"] + MAIN_BYTES_PER_TH["kda"]) / 2
-        flop = th * MAIN_FLOP_PER_TH
+        bytes_avg = (alg_bytes["gdn"] + alg_bytes["kda"]) / 2
         ach = bytes_avg / avg_s / 1e9
+        design = bytes_avg + th * MAIN_DESIGN_EXTRA_PER_TH
         traffic = None
         tp = os.path.join(ROOT, "profiles", "main_traffic.json")
         if os.path.exists(tp):
@@ -507,12 +519,27 @@ def main_gpu(args):
         roof = {"kernel": "k_main (avg of the GDN and KDA launches)", "bound": "hbm", "achieved": ach,
                 "peak": hbm, "unit": "GB/s", "frac": ach / hbm, "traffic": traffic,
                 "peak_source": src + " (hbm_gbs)",
-                "tensor_tflops": flop / avg_s / 1e12, "tensor_frac": flop / avg_s / 1e12 / tf_sus,
-                "tensor_peak": tf_sus}
+                "bytes_per_launch": bytes_avg, "bytes_basis": "the method's: 2316 / 2820 B per token-head",
+                "design_bytes_per_launch": design,
+                "design_achieved": design / avg_s / 1e9,
+                "design_basis": "the builder's count: also the dS_C and T tiles this design reads",
+                "tensor_tflops": alg_flop / avg_s / 1e12, "tensor_frac": alg_flop / avg_s / 1e12 / tf_burst,
+                "tensor_peak": tf_burst, "tensor_peak_source": src + " (bf16_tflops, burst)"}
     else:
         k = dom
         roof = {"kernel": k, "bound": "hbm", "achieved": None, "peak": hbm, "unit": "GB/s", "frac": None,
                 "traffic": None, "note": "dominant kernel has no algorithmic figure yet"}
+    # the whole backward call (every kernel of gdr_bwd / kda_bwd), per variant
+    whole = {"flop_per_token_head": BWD_FLOP_PER_TH, "bytes_per_token_head": BWD_BYTES_PER_TH,
+             "hbm_peak_gbs": hbm, "tensor_peak_tflops": {"burst": tf_burst, "sustained": tf_sus},
+             "peak_source": src}
+    for m, ms_v in (("gdn", ms_g), ("kda", ms_k)):
+        s_ = ms_v * 1e-3
+        tfl = alg_flop / s_ / 1e12
+        gbs = alg_bytes[m] / s_ / 1e9
+        whole[m] = {"ms": ms_v, "mtokens_per_s": CASE_G.seq_len / s_ / 1e6, "tflops": tfl,
+                    "tensor_frac_burst": tfl / tf_burst, "tensor_frac_sustained": tfl / tf_sus,
+                    "gbs": gbs, "hbm_frac": gbs / hbm}
 
     csum = clk.summary(t_clk0, t_clk1)
     line = {
@@ -522,6 +549,7 @@ def main_gpu(args):
         "config": {"workload": WORKLOAD, "variants_ms": {"gdn": ms_g, "kda": ms_k},
                    "l2": "inputs larger than L2 (no flush)", "parallelism": "replicas" if world > 1 else "1 GPU"},
         "roofline": roof,
+        "backward_roofline": whole,
         "kernels_ms_per_step": {k: v[0] / args.steps for k, v in prof.items()},
         "kernels_ms_per_variant": per_variant,
         "forward": forward,

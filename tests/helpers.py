@@ -96,8 +96,60 @@ def run_oracle(x, heads=None):
                       b, x["scale"], cu, h0=h0, dO=dO, dht=dht, gate=x["kda_gate"], gate_scale=x["gate_scale"])
 
 
+# Blocks (one sequence or one 64-token chunk of one head, or one boundary row) are
+# judged against their own norm, floored at the norm a block of their size has on
+# average in the tensor: the scalar gradients (dbeta, dg) are sums over the channels
+# that can nearly cancel at one token, so a small block of them has no meaningful
+# relative error of its own, while a wrong or unwritten block has an error of the
+# order of the tensor's values and fails.
+BLOCK_FLOOR = 1.0
+# A block check is there to find a wrong, misplaced or unwritten block, whose error is of
+# the order of its values: blocks are held to BLOCK_TOL_FACTOR times the tensor's
+# tolerance.  The factor leaves room for the noise of blocks of a few values: the largest
+# block errors on the repo's cases are ~3% of the floored norm, at the last tokens of
+# sequences, where dht makes the gradients' terms an order of magnitude larger than
+# elsewhere and the scalar gradients (dbeta, dg) sums of them that partly cancel.
+BLOCK_TOL_FACTOR = 5.0
+
+
+def _block_rel(a, b, size, total_norm, total_size):
+    num = np.linalg.norm(a - b)
+    den = max(np.linalg.norm(b), BLOCK_FLOOR * total_norm * np.sqrt(size / max(total_size, 1)))
+    if den == 0.0:
+        return 0.0 if num == 0.0 else float("inf")
+    return float(num / den)
+
+
+def block_errors(g, r, cu):
+    """Worst relative L2 of token-major tensors ([T, H, ...]) over (sequence, head)
+    blocks, (64-token chunk, head) blocks and the rows on both sides of every sequence
+    boundary (the last valid row of a sequence and the first row of the next, all heads).
+    Returns (worst per sequence-head, worst per chunk-head, worst boundary row)."""
+    g = np.asarray(g, np.float64)
+    r = np.asarray(r, np.float64)
+    tn, ts = np.linalg.norm(r), r.size
+    per_tok = r[0].size if r.shape[0] else 1
+    per_th = per_tok // r.shape[1] if r.ndim > 1 and r.shape[0] else 1
+    ws = wc = wr = 0.0
+    for s in range(len(cu) - 1):
+        a, b = int(cu[s]), int(cu[s + 1])
+        if b <= a:
+            continue
+        for h in range(r.shape[1]):
+            ws = max(ws, _block_rel(g[a:b, h], r[a:b, h], (b - a) * per_th, tn, ts))
+            for c in range(a, b, 64):
+                e = min(c + 64, b)
+                wc = max(wc, _block_rel(g[c:e, h], r[c:e, h], (e - c) * per_th, tn, ts))
+        for row in (a, b - 1):
+            wr = max(wr, _block_rel(g[row], r[row], per_tok, tn, ts))
+    return ws, wc, wr
+
+
 def compare(gpu, ref, x, heads=None, conditioned=False):
-    """Per-tensor relative L2 errors and their tolerances.
+    """Relative L2 errors and their tolerances: per tensor, and (``name@seq``,
+    ``name@chunk``, ``name@row``) the worst (sequence, head) block, the worst (64-token
+    chunk, head) block and the worst row at a sequence boundary of every token-major
+    gradient, the worst (sequence, head) of dh0 and the worst head of dA_log / ddt_bias.
 
     With ``conditioned`` (edge-case inputs outside the task's workloads, e.g. a
     few hundred tokens), dA_log and ddt_bias -- sums of dg terms with random
@@ -113,6 +165,7 @@ def compare(gpu, ref, x, heads=None, conditioned=False):
     else:
         pairs.update(dg_raw=("dg_raw", TOL_BF16), dA_log=("dA_log", TOL_FP32),
                      ddt_bias=("ddt_bias", TOL_FP32))
+    cu = np.asarray(x["cu_seqlens"], dtype=np.int64)
     res = {}
     for name, (rname, tol) in pairs.items():
         g = f64(gpu[name])
@@ -126,7 +179,22 @@ def compare(gpu, ref, x, heads=None, conditioned=False):
             g = sel(g)
         res[name] = (rel_l2(g, ref[rname]), tol)
         if conditioned and name in ("dA_log", "ddt_bias"):
+            # judged against the term magnitudes; the strict figure is printed beside it, unchecked
+            res[name + "(strict, unchecked)"] = (res[name][0], float("inf"))
             res[name] = (conditioned_error(g, ref, x, name, heads), tol)
+        elif name == "ddt_bias":  # every head's channel vector on its own
+            r = np.asarray(ref[rname], np.float64)
+            res[name + "@head"] = (max(rel_l2(g[i], r[i]) for i in range(r.shape[0])), tol)
+        elif name == "dA_log":
+            pass  # one number per head: the tensor's relative L2 over the heads above
+        elif name == "dh0":
+            r = np.asarray(ref[rname], np.float64)
+            res[name + "@seq"] = (max(_block_rel(g[n, i], r[n, i], r[n, i].size, np.linalg.norm(r), r.size)
+                                      for n in range(r.shape[0]) for i in range(r.shape[1])), tol * BLOCK_TOL_FACTOR)
+        else:
+            ws, wc, wr = block_errors(g, ref[rname], cu)
+            bt = tol * BLOCK_TOL_FACTOR
+            res[name + "@seq"], res[name + "@chunk"], res[name + "@row"] = (ws, bt), (wc, bt), (wr, bt)
     return res
 
 
@@ -142,6 +210,8 @@ def conditioned_error(g, ref, x, name, heads=None):
 def assert_parity(res, label=""):
     bad = {k: v for k, v in res.items() if not (v[0] <= v[1])}
     msg = ", ".join("%s=%.2e(tol %.0e)" % (k, v[0], v[1]) for k, v in res.items())
+    if bad:
+        msg = "FAILED " + ", ".join(sorted(bad)) + ": " + msg
     assert not bad, "%s parity failed: %s" % (label, msg)
     return msg
 
@@ -190,10 +260,20 @@ def run_oracle_fwd(x, heads=None):
 TOL_HT = 5e-3
 
 
-def compare_fwd(gpu, ref, heads=None):
-    """Relative L2 of o (bf16 output: TOL_BF16) and ht (TOL_HT)."""
+def compare_fwd(gpu, ref, heads=None, x=None):
+    """Relative L2 of o (bf16 output: TOL_BF16) and ht (TOL_HT); with ``x``, also the
+    worst (sequence, head), (chunk, head) and boundary-row blocks of o and the worst
+    (sequence, head) of ht."""
     o = f64(gpu["o"])
     ht = f64(gpu["ht"])
     if heads is not None:
         o, ht = o[:, heads], ht[:, heads]
-    return {"o": (rel_l2(o, ref["o"]), TOL_BF16), "ht": (rel_l2(ht, ref["ht"]), TOL_HT)}
+    res = {"o": (rel_l2(o, ref["o"]), TOL_BF16), "ht": (rel_l2(ht, ref["ht"]), TOL_HT)}
+    if x is not None:
+        ws, wc, wr = block_errors(o, ref["o"], np.asarray(x["cu_seqlens"], dtype=np.int64))
+        bt = TOL_BF16 * BLOCK_TOL_FACTOR
+        res["o@seq"], res["o@chunk"], res["o@row"] = (ws, bt), (wc, bt), (wr, bt)
+        r = np.asarray(ref["ht"], np.float64)
+        res["ht@seq"] = (max(_block_rel(ht[n, i], r[n, i], r[n, i].size, np.linalg.norm(r), r.size)
+                             for n in range(r.shape[0]) for i in range(r.shape[1])), TOL_HT * BLOCK_TOL_FACTOR)
+    return res
