@@ -352,7 +352,11 @@ __global__ void __launch_bounds__(512, 1) k_prep_kda(const Params p, const __gri
         tc::st16(tl(R_Q + c0), qs);
         tc::st16(tl(R_K + c0), ks);
     }
-    if (tid == STORE_TID) tc::bulk_wait_read();  // the last item's R store has read the G1 operand tiles
+    // the last item's stores have read their shared tiles: the R store (the G1 operand tiles,
+    // rewritten below) and the T store (sT, which this item's inversion rewrites).  Both
+    // orderings rest on this one full wait: a narrower form (one store still reading) would
+    // let the next inversion overwrite T while its store is in flight.
+    if (tid == STORE_TID) tc::bulk_wait_read();
     __syncthreads();  // norms, factors and the q / k tile reads are done
 
     // gate factors of this thread's channel and rows cq .. cq+15
@@ -471,7 +475,9 @@ __global__ void __launch_bounds__(512, 1) k_prep_kda(const Params p, const __gri
         }
     }
     sync_all();
-    if (tid == STORE_TID) {  // T for the main backward (its blocks above the diagonal stay zero in the tile)
+    if (tid == STORE_TID) {  // T for the main backward (its blocks above the diagonal stay zero in the tile);
+                             // the next item's inversion rewrites sT only after the full read wait
+                             // of the store thread at that item's top
         tc::tma_store_2d(&m.T, 0, (chunk * p.H + h) * CH, sb + oT);
         tc::bulk_commit();
     }

@@ -254,9 +254,9 @@ def run_oracle_fwd(x, heads=None):
 
 # Forward final state ht: the chunk tiles it is built from are bf16 (U, kr and the
 # per-chunk operand U - W S0 of kr^T (U - W S0) each carry one rounding of unit
-# roundoff 2^-9; a float64 rounding-site simulation of the chain gives ~1.6e-3 relative
-# from each and ~2.3e-3 together, whatever the length, because the gates of these
-# workloads forget a chunk's start state within the chunk).  Tolerance: 5e-3.
+# roundoff 2^-9; a float64 rounding-site simulation of the chain, tests/test_tolerance_ht.py,
+# gives ~1.6e-3 relative from each and ~2.3e-3 together, whatever the length, because the
+# gates of these workloads forget a chunk's start state within the chunk).  Tolerance: 5e-3.
 TOL_HT = 5e-3
 
 
