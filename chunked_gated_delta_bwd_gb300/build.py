@@ -12,7 +12,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libgdr.so")
-SOURCES = ["gdr_api.cu", "gdr_prep.cu", "gdr_prep_kda.cu", "gdr_prep_gdn.cu", "gdr_states.cu", "gdr_states_tc.cu", "gdr_main.cu", "gdr_main_kda.cu", "gdr_main_gdn.cu", "gdr_out.cu", "gdr_conv.cu"]
+SOURCES = ["gdr_api.cu", "gdr_prep_kda.cu", "gdr_prep_gdn.cu", "gdr_states_tc.cu", "gdr_main_kda.cu", "gdr_main_gdn.cu", "gdr_out.cu", "gdr_conv.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC = os.environ.get("NVCC", "nvcc")
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

@@ -109,7 +109,7 @@ cudaError_t launch_group_sum(const Params& p, cudaStream_t s) {
 struct StatesTag {
     int v[16];
 };
-static StatesTag states_tag(const gdr_shape* sh, int kda, const float* h0, int64_t max_chunks) {
+static StatesTag states_tag(const gdr_shape* sh, int kda, const float* h0, int64_t max_chunks, int orig_dim) {
     StatesTag t;
     memset(&t, 0, sizeof(t));
     t.v[0] = 0x53524447;  // "GDRS"
@@ -125,12 +125,30 @@ static StatesTag states_tag(const gdr_shape* sh, int kda, const float* h0, int64
     if (kda && sh->kda_gate == GDR_KDA_GATE_SIGMOID) memcpy(&t.v[10], &sh->gate_scale, 4);
     t.v[11] = sh->cu_seqlens != nullptr;
     t.v[12] = h0 != nullptr;
+    t.v[13] = orig_dim;  // the caller's head dim (64 runs zero-padded to 128)
     return t;
 }
 
 // writes the whole header (the tag, then zeros up to GDR_STATES_HEADER_BYTES)
 __global__ void k_states_tag(int* hdr, const StatesTag t) {
     for (int i = threadIdx.x; i < GDR_STATES_HEADER_BYTES / 4; i += blockDim.x) hdr[i] = i < 16 ? t.v[i] : 0;
+}
+
+// Every kernel runs on 128 channels (head_dim 64 is zero-padded to 128 by the entry
+// points); the gate variant picks the prep and main kernels.
+cudaError_t launch_prep(const Params& p, cudaStream_t s) {
+    if (p.max_chunks == 0) return cudaSuccess;
+    if (p.D != 128) return cudaErrorInvalidValue;
+    return p.kda ? launch_prep_kda(p, s) : launch_prep_gdn(p, s);
+}
+cudaError_t launch_states(const Params& p, bool fwd, bool bwd, cudaStream_t s) {
+    if (p.D != 128) return cudaErrorInvalidValue;
+    return launch_states_tc(p, fwd, bwd, s);
+}
+cudaError_t launch_main(const Params& p, cudaStream_t s) {
+    if (p.max_chunks == 0) return cudaSuccess;
+    if (p.D != 128) return cudaErrorInvalidValue;
+    return p.kda ? launch_main_kda(p, s) : launch_main_gdn(p, s);
 }
 
 cudaError_t launch_chunk_table(const Params& p, cudaStream_t s) {
@@ -307,11 +325,11 @@ static gdr_status common_front(const Params& p, cudaStream_t s) {
     return GDR_OK;
 }
 
-static gdr_status fwd_states_impl(const gdr_shape* sh, const void* q, const void* k, const void* v,
+static gdr_status fwd_states_impl128(const gdr_shape* sh, const void* q, const void* k, const void* v,
                                   const float* g, const void* g_raw, const float* A_log,
                                   const float* dt_bias, const void* beta, const float* h0,
                                   void* states, size_t states_bytes, void* ws, size_t ws_bytes,
-                                  void* stream, int kda) {
+                                  void* stream, int kda, int orig_dim) {
     if (gdr_status st0 = check_shape(sh)) return st0;
     NEED(q); NEED(k); NEED(v); NEED(beta); NEED(ws); NEED(states); OPT(h0);
     if (kda) { NEED(g_raw); NEED(A_log); NEED(dt_bias); } else { NEED(g); }
@@ -330,17 +348,17 @@ static gdr_status fwd_states_impl(const gdr_shape* sh, const void* q, const void
     if (st != GDR_OK) return st;
     cudaError_t e = timed(GDR_KERNEL_STATES, s, [&] { return launch_states(p, true, false, s); });
     if (e != cudaSuccess) return cuda_fail(e, "state recurrence launch");
-    k_states_tag<<<1, 32, 0, s>>>(static_cast<int*>(states), states_tag(sh, kda, h0, L.max_chunks));
+    k_states_tag<<<1, 32, 0, s>>>(static_cast<int*>(states), states_tag(sh, kda, h0, L.max_chunks, orig_dim));
     if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "states header launch");
     g_err[0] = 0;
     return GDR_OK;
 }
 
 // forward: chunk tiles (with P), the chunk-start states and final states, the output
-static gdr_status fwd_impl(const gdr_shape* sh, const void* q, const void* k, const void* v, const float* g,
+static gdr_status fwd_impl128(const gdr_shape* sh, const void* q, const void* k, const void* v, const float* g,
                            const void* g_raw, const float* A_log, const float* dt_bias, const void* beta,
                            const float* h0, void* o, float* ht, void* states, size_t states_bytes, void* ws,
-                           size_t ws_bytes, void* stream, int kda) {
+                           size_t ws_bytes, void* stream, int kda, int orig_dim) {
     if (gdr_status st0 = check_shape(sh)) return st0;
     NEED(q); NEED(k); NEED(v); NEED(beta); NEED(ws); NEED(o); OPT(h0); OPT(ht); OPT(states);
     if (kda) { NEED(g_raw); NEED(A_log); NEED(dt_bias); } else { NEED(g); }
@@ -366,7 +384,7 @@ static gdr_status fwd_impl(const gdr_shape* sh, const void* q, const void* k, co
     e = timed(GDR_KERNEL_OUT, s, [&] { return launch_out(p, s); });
     if (e != cudaSuccess) return cuda_fail(e, "output launch");
     if (states) {
-        k_states_tag<<<1, 32, 0, s>>>(static_cast<int*>(states), states_tag(sh, kda, h0, L.max_chunks));
+        k_states_tag<<<1, 32, 0, s>>>(static_cast<int*>(states), states_tag(sh, kda, h0, L.max_chunks, orig_dim));
         if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "states header launch");
     }
     g_err[0] = 0;
@@ -375,12 +393,12 @@ static gdr_status fwd_impl(const gdr_shape* sh, const void* q, const void* k, co
 
 static std::atomic<int> g_test_stall{0};  // gdr_test_stall_next_call: CTA index + 1, or 0
 
-static gdr_status bwd_impl(const gdr_shape* sh, const void* q, const void* k, const void* v,
+static gdr_status bwd_impl128(const gdr_shape* sh, const void* q, const void* k, const void* v,
                            const float* g, const void* g_raw, const float* A_log, const float* dt_bias,
                            const void* beta, const float* h0, const void* dO, const float* dht,
                            const void* states, void* ws, size_t ws_bytes, void* dq, void* dk, void* dv,
                            float* dg, void* dg_raw, void* dbeta, float* dh0, float* dA_log,
-                           float* ddt_bias, void* stream, int kda) {
+                           float* ddt_bias, void* stream, int kda, int orig_dim) {
     if (gdr_status st0 = check_shape(sh)) return st0;
     NEED(q); NEED(k); NEED(v); NEED(beta); NEED(dO); NEED(ws);
     NEED(dq); NEED(dk); NEED(dv); NEED(dbeta); NEED(dh0);
@@ -399,7 +417,7 @@ static gdr_status bwd_impl(const gdr_shape* sh, const void* q, const void* k, co
         p.S0 = reinterpret_cast<__nv_bfloat16*>(const_cast<unsigned char*>(static_cast<const unsigned char*>(states)) +
                                                 GDR_STATES_HEADER_BYTES);
         p.states_hdr = static_cast<const int*>(states);
-        const StatesTag t = states_tag(sh, kda, h0, L.max_chunks);
+        const StatesTag t = states_tag(sh, kda, h0, L.max_chunks, orig_dim);
         memcpy(p.states_tag, t.v, sizeof(t.v));
     }
     if (!kda && p.D == 128) p.test_stall = g_test_stall.exchange(0);
@@ -432,6 +450,206 @@ static gdr_status bwd_impl(const gdr_shape* sh, const void* q, const void* k, co
     return GDR_OK;
 }
 
+// ---------------------------------------------------------------------------
+// head_dim 64: the same tcgen05 kernels on channels zero-padded to 128
+//
+// A zero key channel adds nothing to any product and keeps its row of the state at zero
+// from a zero start (k has no component there, so the delta update never writes it), and
+// a zero value channel keeps its column at zero; the L2 norms, dot products and channel
+// sums of the method are unchanged by zero channels.  So the D = 64 problem is the
+// D = 128 problem on inputs padded with zeros, and its results are the first 64 channels
+// of the padded results (the padded channels' gradients are exactly zero).  The pads
+// live in the workspace after the D = 128 layout; saved states keep the padded layout.
+// ---------------------------------------------------------------------------
+
+// dst[b][r][v] = src[b][r][v] for r < rin, v < vin, else 0 (pad); or the first rin rows and
+// vin units of every block of src into a dense dst (unpad).  Units are 16 bytes.
+__global__ void __launch_bounds__(256) k_pad16(const uint4* __restrict__ src, uint4* __restrict__ dst, int64_t nb,
+                                               int rin, int vin, int rout, int vout, int unpad) {
+    const int64_t per = unpad ? (int64_t)rin * vin : (int64_t)rout * vout;
+    const int64_t n = nb * per;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t b = i / per;
+        const int rem = (int)(i % per);
+        if (unpad) {
+            const int r = rem / vin, v = rem % vin;
+            dst[i] = src[(b * rout + r) * vout + v];
+        } else {
+            const int r = rem / vout, v = rem % vout;
+            dst[i] = (r < rin && v < vin) ? src[(b * rin + r) * vin + v] : make_uint4(0, 0, 0, 0);
+        }
+    }
+}
+
+// nb blocks of rin x cin elements of esz bytes <-> blocks of rout x cout (cin, cout: 16-byte multiples)
+static cudaError_t pad_copy(const void* src, void* dst, int64_t nb, int rin, int cin, int rout, int cout, int esz,
+                            bool unpad, cudaStream_t s) {
+    const int64_t units = nb * (unpad ? (int64_t)rin * cin : (int64_t)rout * cout) * esz / 16;
+    if (units == 0) return cudaSuccess;
+    const int64_t want = (units + 255) / 256;
+    const int grid = (int)(want < 8 * num_sms() ? want : 8 * num_sms());
+    k_pad16<<<grid, 256, 0, s>>>(static_cast<const uint4*>(src), static_cast<uint4*>(dst), nb, rin, cin * esz / 16,
+                                 rout, cout * esz / 16, unpad ? 1 : 0);
+    return cudaGetLastError();
+}
+
+struct Pad64 {  // byte offsets of the padded tensors, from the end of the D = 128 layout
+    size_t q, k, v, dO, gr, dtb, h0, dht, dq, dk, dv, dgr, dh0, ddt, o, ht, total;
+};
+static gdr_shape shape128(const gdr_shape* sh) {
+    gdr_shape t = *sh;
+    t.head_dim = 128;
+    return t;
+}
+static Pad64 pad64_layout(const gdr_shape* sh) {
+    Pad64 P{};
+    const size_t T = (size_t)sh->total_tokens, H = (size_t)sh->num_heads, N = (size_t)sh->num_seqs;
+    const size_t Hk = sh->num_k_heads > 0 ? (size_t)sh->num_k_heads : H;
+    const size_t tok_k = T * Hk * 128 * 2, tok = T * H * 128 * 2, st = N * H * 128 * 128 * 4, hd = H * 128 * 4;
+    size_t o = 0;
+    auto put = [&](size_t& f, size_t bytes) { f = o; o = align256(o + bytes); };
+    put(P.q, tok_k); put(P.k, tok_k); put(P.v, tok); put(P.dO, tok); put(P.gr, tok); put(P.dtb, hd);
+    put(P.h0, st); put(P.dht, st); put(P.dq, tok_k); put(P.dk, tok_k); put(P.dv, tok); put(P.dgr, tok);
+    put(P.dh0, st); put(P.ddt, hd); put(P.o, tok); put(P.ht, st);
+    P.total = o;
+    return P;
+}
+// the whole workspace of a call: the layout of the kernels' shape, then (D = 64) the pads
+static size_t workspace_total(const gdr_shape* sh) {
+    if (sh->head_dim == 128) return layout(sh).total;
+    const gdr_shape s128 = shape128(sh);
+    return align256(layout(&s128).total) + pad64_layout(sh).total;
+}
+
+// The padded inputs of a D = 64 call: q, k, v (and dO, the KDA gate inputs, h0, dht when
+// given) into the pad region.  `base` is the pad region; `P` its layout.
+struct Pad64In {
+    const void *q, *k, *v, *dO, *g_raw;
+    const float *dt_bias, *h0, *dht;
+};
+static gdr_status pad64_inputs(const gdr_shape* sh, const Pad64& P, unsigned char* base, Pad64In& in, int kda,
+                               cudaStream_t s) {
+    const int64_t T = sh->total_tokens, H = sh->num_heads, N = sh->num_seqs;
+    const int64_t Hk = sh->num_k_heads > 0 ? sh->num_k_heads : H;
+    cudaError_t e = cudaSuccess;
+    auto tok = [&](const void*& x, size_t off, int64_t heads) {
+        if (!x || e != cudaSuccess) return;
+        e = pad_copy(x, base + off, T * heads, 1, 64, 1, 128, 2, false, s);
+        x = base + off;
+    };
+    tok(in.q, P.q, Hk);
+    tok(in.k, P.k, Hk);
+    tok(in.v, P.v, H);
+    tok(in.dO, P.dO, H);
+    if (kda) tok(in.g_raw, P.gr, H);
+    auto st = [&](const float*& x, size_t off) {
+        if (!x || e != cudaSuccess) return;
+        e = pad_copy(x, base + off, N * H, 64, 64, 128, 128, 4, false, s);
+        x = reinterpret_cast<const float*>(base + off);
+    };
+    st(in.h0, P.h0);
+    st(in.dht, P.dht);
+    if (kda && in.dt_bias && e == cudaSuccess) {
+        e = pad_copy(in.dt_bias, base + P.dtb, H, 1, 64, 1, 128, 4, false, s);
+        in.dt_bias = reinterpret_cast<const float*>(base + P.dtb);
+    }
+    return e == cudaSuccess ? GDR_OK : cuda_fail(e, "channel padding launch");
+}
+
+static gdr_status fwd_states_impl(const gdr_shape* sh, const void* q, const void* k, const void* v,
+                                  const float* g, const void* g_raw, const float* A_log,
+                                  const float* dt_bias, const void* beta, const float* h0,
+                                  void* states, size_t states_bytes, void* ws, size_t ws_bytes,
+                                  void* stream, int kda) {
+    if (gdr_status st0 = check_shape(sh)) return st0;
+    if (sh->head_dim == 128)
+        return fwd_states_impl128(sh, q, k, v, g, g_raw, A_log, dt_bias, beta, h0, states, states_bytes, ws,
+                                  ws_bytes, stream, kda, 128);
+    NEED(q); NEED(k); NEED(v); NEED(beta); NEED(ws); NEED(states); OPT(h0);
+    if (kda) { NEED(g_raw); NEED(A_log); NEED(dt_bias); } else { NEED(g); }
+    const gdr_shape s128 = shape128(sh);
+    if (gdr_status st1 = check_shape(&s128)) return st1;
+    if (ws_bytes < workspace_total(sh)) return fail(GDR_ERR_WORKSPACE, "workspace too small%s");
+    if (states_bytes < gdr_states_bytes(sh)) return fail(GDR_ERR_WORKSPACE, "states buffer too small%s");
+    const size_t inner = align256(layout(&s128).total);
+    unsigned char* base = static_cast<unsigned char*>(ws) + inner;
+    Pad64In in{q, k, v, nullptr, g_raw, dt_bias, h0, nullptr};
+    cudaStream_t s = (cudaStream_t)stream;
+    if (gdr_status st = pad64_inputs(sh, pad64_layout(sh), base, in, kda, s)) return st;
+    return fwd_states_impl128(&s128, in.q, in.k, in.v, g, in.g_raw, A_log, in.dt_bias, beta, in.h0, states,
+                              states_bytes, ws, inner, stream, kda, 64);
+}
+
+static gdr_status fwd_impl(const gdr_shape* sh, const void* q, const void* k, const void* v, const float* g,
+                           const void* g_raw, const float* A_log, const float* dt_bias, const void* beta,
+                           const float* h0, void* o, float* ht, void* states, size_t states_bytes, void* ws,
+                           size_t ws_bytes, void* stream, int kda) {
+    if (gdr_status st0 = check_shape(sh)) return st0;
+    if (sh->head_dim == 128)
+        return fwd_impl128(sh, q, k, v, g, g_raw, A_log, dt_bias, beta, h0, o, ht, states, states_bytes, ws, ws_bytes,
+                           stream, kda, 128);
+    NEED(q); NEED(k); NEED(v); NEED(beta); NEED(ws); NEED(o); OPT(h0); OPT(ht); OPT(states);
+    if (kda) { NEED(g_raw); NEED(A_log); NEED(dt_bias); } else { NEED(g); }
+    const gdr_shape s128 = shape128(sh);
+    if (gdr_status st1 = check_shape(&s128)) return st1;
+    if (ws_bytes < workspace_total(sh)) return fail(GDR_ERR_WORKSPACE, "workspace too small%s");
+    if (states && states_bytes < gdr_states_bytes(sh)) return fail(GDR_ERR_WORKSPACE, "states buffer too small%s");
+    const size_t inner = align256(layout(&s128).total);
+    unsigned char* base = static_cast<unsigned char*>(ws) + inner;
+    const Pad64 P = pad64_layout(sh);
+    Pad64In in{q, k, v, nullptr, g_raw, dt_bias, h0, nullptr};
+    cudaStream_t s = (cudaStream_t)stream;
+    if (gdr_status st = pad64_inputs(sh, P, base, in, kda, s)) return st;
+    float* htp = ht ? reinterpret_cast<float*>(base + P.ht) : nullptr;
+    gdr_status st = fwd_impl128(&s128, in.q, in.k, in.v, g, in.g_raw, A_log, in.dt_bias, beta, in.h0, base + P.o, htp,
+                                states, states_bytes, ws, inner, stream, kda, 64);
+    if (st != GDR_OK) return st;
+    const int64_t T = sh->total_tokens, H = sh->num_heads, N = sh->num_seqs;
+    cudaError_t e = pad_copy(base + P.o, o, T * H, 1, 64, 1, 128, 2, true, s);
+    if (e == cudaSuccess && ht) e = pad_copy(htp, ht, N * H, 64, 64, 128, 128, 4, true, s);
+    return e == cudaSuccess ? GDR_OK : cuda_fail(e, "channel unpadding launch");
+}
+
+static gdr_status bwd_impl(const gdr_shape* sh, const void* q, const void* k, const void* v,
+                           const float* g, const void* g_raw, const float* A_log, const float* dt_bias,
+                           const void* beta, const float* h0, const void* dO, const float* dht,
+                           const void* states, void* ws, size_t ws_bytes, void* dq, void* dk, void* dv,
+                           float* dg, void* dg_raw, void* dbeta, float* dh0, float* dA_log,
+                           float* ddt_bias, void* stream, int kda) {
+    if (gdr_status st0 = check_shape(sh)) return st0;
+    if (sh->head_dim == 128)
+        return bwd_impl128(sh, q, k, v, g, g_raw, A_log, dt_bias, beta, h0, dO, dht, states, ws, ws_bytes, dq, dk, dv,
+                           dg, dg_raw, dbeta, dh0, dA_log, ddt_bias, stream, kda, 128);
+    NEED(q); NEED(k); NEED(v); NEED(beta); NEED(dO); NEED(ws);
+    NEED(dq); NEED(dk); NEED(dv); NEED(dbeta); NEED(dh0);
+    OPT(h0); OPT(dht); OPT(states);
+    if (kda) { NEED(g_raw); NEED(A_log); NEED(dt_bias); NEED(dg_raw); NEED(dA_log); NEED(ddt_bias); }
+    else { NEED(g); NEED(dg); }
+    const gdr_shape s128 = shape128(sh);
+    if (gdr_status st1 = check_shape(&s128)) return st1;
+    if (ws_bytes < workspace_total(sh)) return fail(GDR_ERR_WORKSPACE, "workspace too small%s");
+    const size_t inner = align256(layout(&s128).total);
+    unsigned char* base = static_cast<unsigned char*>(ws) + inner;
+    const Pad64 P = pad64_layout(sh);
+    Pad64In in{q, k, v, dO, g_raw, dt_bias, h0, dht};
+    cudaStream_t s = (cudaStream_t)stream;
+    if (gdr_status st = pad64_inputs(sh, P, base, in, kda, s)) return st;
+    gdr_status st = bwd_impl128(&s128, in.q, in.k, in.v, g, in.g_raw, A_log, in.dt_bias, beta, in.h0, in.dO, in.dht,
+                                states, ws, inner, base + P.dq, base + P.dk, base + P.dv, dg,
+                                kda ? base + P.dgr : nullptr, dbeta, reinterpret_cast<float*>(base + P.dh0), dA_log,
+                                kda ? reinterpret_cast<float*>(base + P.ddt) : nullptr, stream, kda, 64);
+    if (st != GDR_OK) return st;
+    const int64_t T = sh->total_tokens, H = sh->num_heads, N = sh->num_seqs;
+    const int64_t Hk = sh->num_k_heads > 0 ? sh->num_k_heads : H;
+    cudaError_t e = pad_copy(base + P.dq, dq, T * Hk, 1, 64, 1, 128, 2, true, s);
+    if (e == cudaSuccess) e = pad_copy(base + P.dk, dk, T * Hk, 1, 64, 1, 128, 2, true, s);
+    if (e == cudaSuccess) e = pad_copy(base + P.dv, dv, T * H, 1, 64, 1, 128, 2, true, s);
+    if (e == cudaSuccess) e = pad_copy(base + P.dh0, dh0, N * H, 64, 64, 128, 128, 4, true, s);
+    if (kda && e == cudaSuccess) e = pad_copy(base + P.dgr, dg_raw, T * H, 1, 64, 1, 128, 2, true, s);
+    if (kda && e == cudaSuccess) e = pad_copy(base + P.ddt, ddt_bias, H, 1, 64, 1, 128, 4, true, s);
+    return e == cudaSuccess ? GDR_OK : cuda_fail(e, "channel unpadding launch");
+}
+
 }  // namespace gdr
 
 using namespace gdr;
@@ -440,13 +658,14 @@ extern "C" {
 
 size_t gdr_workspace_bytes(const gdr_shape* shape) {
     if (check_shape(shape) != GDR_OK) return 0;
-    return layout(shape).total;
+    return workspace_total(shape);
 }
 
 size_t gdr_states_bytes(const gdr_shape* shape) {
     if (check_shape(shape) != GDR_OK) return 0;
     const Layout L = layout(shape);
-    return GDR_STATES_HEADER_BYTES + (size_t)L.max_chunks * shape->num_heads * shape->head_dim * shape->head_dim * 2;
+    // (head_dim 64 keeps its states in the layout of the zero-padded 128-channel problem)
+    return GDR_STATES_HEADER_BYTES + (size_t)L.max_chunks * shape->num_heads * 128 * 128 * 2;
 }
 
 void gdr_test_stall_next_call(int cta) { g_test_stall.store(cta >= 0 ? cta + 1 : 0); }
@@ -628,7 +847,7 @@ extern "C" gdr_status gdr_bwd_fixed(const gdr_shape* shape, const void* q, const
                                     const float* dht, const void* states, void* dq, void* dk, void* dv,
                                     float* dg, void* dbeta, float* dh0, void* stream) {
     if (gdr_status st0 = check_shape(shape)) return st0;
-    const size_t need = layout(shape).total;
+    const size_t need = workspace_total(shape);
     if (need > (size_t)GDR_FIXED_WORKSPACE_BYTES) {
         snprintf(g_err, sizeof(g_err),
                  "gdr_bwd_fixed: this problem needs %zu bytes of scratch; the fixed workspace holds %zu "

@@ -1,13 +1,12 @@
 // Shared device helpers for the gated delta-rule kernels (sm_103a).
 //
 // Conventions used by every kernel in this directory:
-//   * chunk length C = 64 tokens; head dim D = dk = dv in {64, 128};
+//   * chunk length C = 64 tokens; the kernels run on D = dk = dv = 128 channels
+//     (head_dim 64 reaches them zero-padded to 128);
 //   * activations are token-major [T_total, H, D] bf16, per-chunk workspace
 //     tiles are [chunk][H][rows][cols] contiguous;
-//   * shared-memory bf16 tiles are row-major with rows of >= 128 bytes and the
-//     16-byte chunks of row r XOR-swizzled by (r & 7), so that ldmatrix of 8
-//     consecutive rows is bank-conflict free;
-//   * warp-level tensor-core products use mma.sync m16n8k16 bf16 -> fp32.
+//   * shared-memory operand tiles use the 128-byte swizzle of the tensor-core
+//     descriptors (gdr_tc.cuh).
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -41,125 +40,6 @@ __device__ __forceinline__ float2 unpack_bf16(uint32_t u) {
 }
 
 __device__ __forceinline__ float bf2f(__nv_bfloat16 x) { return __bfloat162float(x); }
-
-// --------------------------------------------------------------------------
-// shared-memory tiles
-// --------------------------------------------------------------------------
-// Swizzled bf16 tile: ROWB bytes per row (>= 128, multiple of 128).
-template <int ROWB>
-struct SwzTile {
-    static_assert(ROWB % 128 == 0, "swizzled rows must be multiples of 128 bytes");
-    unsigned char* base;
-    __device__ __forceinline__ uint32_t off(int r, int c) const {  // c: element column
-        return r * ROWB + ((((c >> 3) ^ (r & 7))) << 4) + ((c & 7) << 1);
-    }
-    __device__ __forceinline__ unsigned char* ptr(int r, int c) const { return base + off(r, c); }
-    __device__ __forceinline__ uint32_t addr(int r, int c) const { return smem_u32(base) + off(r, c); }
-    // 16-byte chunk j of row r (j counts 8-element chunks)
-    __device__ __forceinline__ unsigned char* chunk(int r, int j) const {
-        return base + r * ROWB + ((j ^ (r & 7)) << 4);
-    }
-};
-
-// Padded bf16 tile: LDE elements per row (rows of 48 bytes for 16 columns).
-template <int LDE>
-struct PadTile {
-    unsigned char* base;
-    __device__ __forceinline__ uint32_t off(int r, int c) const { return (r * LDE + c) * 2; }
-    __device__ __forceinline__ unsigned char* ptr(int r, int c) const { return base + off(r, c); }
-    __device__ __forceinline__ uint32_t addr(int r, int c) const { return smem_u32(base) + off(r, c); }
-    __device__ __forceinline__ unsigned char* chunk(int r, int j) const { return base + (r * LDE + j * 8) * 2; }
-};
-
-// --------------------------------------------------------------------------
-// ldmatrix / mma.sync
-// --------------------------------------------------------------------------
-__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t a) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(a));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], uint32_t a) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(a));
-}
-
-__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};\n"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-// Operand storage forms for warp_mma:
-//   A_ROW: A stored [M][K] (K contiguous)   A_COL: A stored [K][M] (A^T stored)
-//   B_COL: B stored [N][K] (K contiguous)   B_ROW: B stored [K][N] (N contiguous)
-enum { A_ROW = 0, A_COL = 1 };
-enum { B_COL = 0, B_ROW = 1 };
-
-// acc[MT][NT] (16x8 fp32 fragments) += A[m0.., k0..k0+K) * B[k0.., n0..]
-// Rows m0 + 16*mt, columns n0 + 8*nt.  NT must be even.
-template <int MT, int NT, int AF, int BF, class TA, class TB>
-__device__ __forceinline__ void warp_mma(float (&acc)[MT][NT][4], const TA& A, const TB& B, int m0,
-                                         int n0, int k0, int K) {
-    static_assert(NT % 2 == 0, "NT must be even");
-    const int lane = threadIdx.x & 31;
-    const int li = lane >> 3, lj = lane & 7;
-#pragma unroll 2
-    for (int k = k0; k < k0 + K; k += 16) {
-        uint32_t af[MT][4];
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-            const int m = m0 + mt * 16;
-            if (AF == A_ROW) {
-                ldsm_x4(af[mt], A.addr(m + (lane & 15), k + ((lane >> 4) << 3)));
-            } else {
-                ldsm_x4_t(af[mt], A.addr(k + ((li >> 1) << 3) + lj, m + ((li & 1) << 3)));
-            }
-        }
-#pragma unroll
-        for (int nt = 0; nt < NT; nt += 2) {
-            const int n = n0 + nt * 8;
-            uint32_t bf[4];
-            if (BF == B_COL) {
-                ldsm_x4(bf, B.addr(n + ((li >> 1) << 3) + lj, k + ((li & 1) << 3)));
-            } else {
-                ldsm_x4_t(bf, B.addr(k + ((li & 1) << 3) + lj, n + ((li >> 1) << 3)));
-            }
-#pragma unroll
-            for (int mt = 0; mt < MT; ++mt) {
-                mma16816(acc[mt][nt], af[mt], bf[0], bf[1]);
-                mma16816(acc[mt][nt + 1], af[mt], bf[2], bf[3]);
-            }
-        }
-    }
-}
-
-template <int MT, int NT>
-__device__ __forceinline__ void zero_acc(float (&acc)[MT][NT][4]) {
-#pragma unroll
-    for (int i = 0; i < MT; ++i)
-#pragma unroll
-        for (int j = 0; j < NT; ++j)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[i][j][e] = 0.f;
-}
-
-// Fragment element coordinates: element e of fragment (mt, nt) of a warp tile
-// at (m0, n0) sits at row m0 + 16 mt + g + 8*(e >> 1), column n0 + 8 nt + 2c + (e & 1).
-__device__ __forceinline__ int frag_g() { return (threadIdx.x & 31) >> 2; }
-__device__ __forceinline__ int frag_c() { return threadIdx.x & 3; }
-
-// --------------------------------------------------------------------------
-// cp.async
-// --------------------------------------------------------------------------
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool valid) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_u32(smem)),
-                 "l"(gmem), "r"(valid ? 16 : 0));
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N)); }
 
 // --------------------------------------------------------------------------
 // chunk table lookup
@@ -239,9 +119,6 @@ __device__ __forceinline__ float kda_gate_fn(float gs, float a, float x) {
     if constexpr (MODE == 0) return -a * softplus_f(x);
     else return kLn2f * gs * sigmoid_f(a * x);
 }
-__device__ __forceinline__ float kda_gate_fn(int mode, float gs, float a, float x) {
-    return mode == 0 ? kda_gate_fn<0>(gs, a, x) : kda_gate_fn<1>(gs, a, x);
-}
 // Its chain rule for one element: dgl = dL/dg.  Returns dL/dg_raw (which is also the
 // element's dt_bias term) and sets dA, the element's term of dL/dA_log.
 //   mode 0: dg/dx = -a sigmoid(x), dg/dA_log = g
@@ -259,9 +136,6 @@ __device__ __forceinline__ float kda_gate_bwd(float gs, float a, float x, float 
         dA = dz * a * x;
         return dz * a;
     }
-}
-__device__ __forceinline__ float kda_gate_bwd(int mode, float gs, float a, float x, float dgl, float& dA) {
-    return mode == 0 ? kda_gate_bwd<0>(gs, a, x, dgl, dA) : kda_gate_bwd<1>(gs, a, x, dgl, dA);
 }
 
 }  // namespace gdr

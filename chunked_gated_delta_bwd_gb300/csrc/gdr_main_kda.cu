@@ -1,9 +1,8 @@
 // Chunk-parallel main backward on tcgen05 for D = 128 with the per-channel (KDA) gate:
 // persistent CTAs of 16 warps, one per SM, each looping over (chunk, head) items; the
 // next item's operand tiles arrive by TMA while the current item's epilogue runs (every
-// large shared tile is dead after the last product group).  Same algebra as the
-// warp-level kernel in gdr_main.cu (the scalar gate has its own kernel, gdr_main_gdn.cu);
-// every product is a 128-row tcgen05 MMA into tensor memory, written feature-major
+// large shared tile is dead after the last product group).  The scalar gate has its
+// own kernel, gdr_main_gdn.cu.  Every product is a 128-row tcgen05 MMA into tensor memory, written feature-major
 // where the natural output is C x D: the accumulator holds X^T (lane = key channel d
 // or value channel j, column = token row r), so a thread owns one channel for 16
 // rows.  The raw q and k rows and e^{gc - ref} of the per-channel cumulative gate gc
@@ -24,7 +23,7 @@
 // (du^T, ki' lo, the dY rows of [dO; dY], the raw-gate tile) and written by TMA stores; a
 // chunk cut by its sequence's end copies its valid rows from the staged tile instead.
 //
-// KDA runs the precise mode of the warp-level kernel: the operands that carry the
+// KDA runs in precise mode: the operands that carry the
 // per-channel gate gradient (beta E, u, dP and beta dA, and ki', qd', kd' of G10 / G11)
 // are bf16 pairs hi + lo and each of those products is hi*hi + lo*hi + hi*lo, because
 // dA_log and ddt_bias sum dg over every token of a head.

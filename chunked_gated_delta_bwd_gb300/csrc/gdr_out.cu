@@ -3,7 +3,7 @@
 //
 //   o = qd S0 + P u,  u = U - W S0    =>    o = (qd - P W) S0 + P U = R S0 + P U
 //
-// (the chunked forward of "FlashKDA之backward（K1）" §2, whose o is the starting point
+// (the chunked forward of "FlashKDA之backward（K1）" §0.1, whose o is the starting point
 // of the backward; qd carries the output scale; R is the same tile the state-gradient
 // recurrence reads, the X/R form of the FlashQLA GDN backward page, §三).  Rows past a
 // sequence's end are not written.
@@ -11,8 +11,8 @@
 // D = 128: one CTA of 4 warps per (chunk, head), several CTAs per SM.  S0 (value-major
 // [dv][dk]), R^T and U^T (channel-major [D][C]) and P ([C][C]) arrive by TMA; the
 // product o^T = S0^T R^T + U^T P^T (M = 128 value channels) runs on tcgen05 into 64
-// tensor-memory columns; thread = value channel, 64 token rows.
-// D = 64: the same product with warp-level mma.sync ([C][D] tiles).
+// tensor-memory columns; thread = value channel, 64 token rows.  (head_dim 64 runs on
+// the channels zero-padded to 128.)
 #include "gdr_chunk.cuh"
 #include "gdr_tc.cuh"
 #include "gdr_tma.h"
@@ -110,62 +110,19 @@ __global__ void __launch_bounds__(128) k_out_tc(const Params p, const __grid_con
     if (warp == 0) tc::dealloc(tmem, 64);
 }
 
-// D = 64: one CTA of 4 warps per (chunk, head); warp w owns rows 16 w .. 16 w + 15.
-template <int D>
-__global__ void __launch_bounds__(128) k_out(const Params p) {
-    using Tile = SwzTile<2 * D>;
-    extern __shared__ __align__(1024) unsigned char smem[];
-    const int item = blockIdx.x, chunk = item / p.H, h = item % p.H;
-    ChunkInfo ci;
-    if (!lookup_chunk(chunk, p.N, p.chunk_off, p.cu_seqlens, p.seq_len, ci)) return;
-    constexpr int TCD = CH * 2 * D, TDD = D * 2 * D, TCC = CH * 2 * CH;
-    const Tile sR{smem}, sU{smem + TCD}, sS{smem + 2 * TCD};
-    const SwzTile<2 * CH> sP{smem + 2 * TCD + TDD};
-    const size_t tcd = (size_t)item * CH * D, tdd = (size_t)item * D * D, tcc = (size_t)item * CH * CH;
-    async_load_tile<CH, D>(sR, p.R + tcd);
-    async_load_tile<CH, D>(sU, p.U + tcd);
-    async_load_tile<D, D>(sS, p.S0 + tdd);
-    async_load_tile<CH, CH>(sP, p.Pm + tcc);
-    (void)TCC;
-    cp_async_commit();
-    cp_async_wait<0>();
-    __syncthreads();
-    const int warp = threadIdx.x >> 5, m0 = 16 * warp;
-    float acc[1][D / 8][4];
-    zero_acc(acc);
-    warp_mma<1, D / 8, A_ROW, B_COL>(acc, sR, sS, m0, 0, 0, D);   // R S0 (S0 stored value-major: [j][d])
-    warp_mma<1, D / 8, A_ROW, B_ROW>(acc, sP, sU, m0, 0, 0, CH);  // + P U
-    const int g = frag_g(), c = frag_c();
-#pragma unroll
-    for (int nt = 0; nt < D / 8; ++nt)
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-            const int r = m0 + g + 8 * hf, col = 8 * nt + 2 * c;
-            if (r < ci.len)
-                *reinterpret_cast<uint32_t*>(p.o + ((ci.t0 + r) * p.H + h) * D + col) =
-                    pack_bf16(acc[0][nt][2 * hf], acc[0][nt][2 * hf + 1]);
-        }
-}
-
 cudaError_t launch_out(const Params& p, cudaStream_t s) {
     const int items = p.max_chunks * p.H;
     if (items == 0) return cudaSuccess;
-    if (p.D == OD) {
-        OutMaps m;
-        const uint64_t rows_dd = (uint64_t)p.max_chunks * p.H * OD;
-        const uint64_t rows_cc = (uint64_t)p.max_chunks * p.H * CH;
-        if (!(encode_blocked_rows_map(&m.S0, p.S0, rows_dd, OD) && encode_rows_map(&m.R, p.R, rows_dd, CH, OD) &&
-              encode_rows_map(&m.U, p.U, rows_dd, CH, OD) && encode_rows_map(&m.P, p.Pm, rows_cc, CH, CH)))
-            return cudaErrorInvalidValue;
-        cudaError_t e = cudaFuncSetAttribute(k_out_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, OUT_SMEM);
-        if (e != cudaSuccess) return e;
-        k_out_tc<<<items, 128, OUT_SMEM, s>>>(p, m);
-        return cudaGetLastError();
-    }
-    constexpr int D = 64, bytes = 2 * CH * 2 * D + D * 2 * D + CH * 2 * CH;
-    cudaError_t e = cudaFuncSetAttribute(k_out<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (p.D != OD) return cudaErrorInvalidValue;  // (head_dim 64 runs zero-padded to 128)
+    OutMaps m;
+    const uint64_t rows_dd = (uint64_t)p.max_chunks * p.H * OD;
+    const uint64_t rows_cc = (uint64_t)p.max_chunks * p.H * CH;
+    if (!(encode_blocked_rows_map(&m.S0, p.S0, rows_dd, OD) && encode_rows_map(&m.R, p.R, rows_dd, CH, OD) &&
+          encode_rows_map(&m.U, p.U, rows_dd, CH, OD) && encode_rows_map(&m.P, p.Pm, rows_cc, CH, CH)))
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(k_out_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, OUT_SMEM);
     if (e != cudaSuccess) return e;
-    k_out<D><<<items, 128, bytes, s>>>(p);
+    k_out_tc<<<items, 128, OUT_SMEM, s>>>(p, m);
     return cudaGetLastError();
 }
 

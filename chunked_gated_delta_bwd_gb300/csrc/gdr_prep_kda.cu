@@ -1,9 +1,9 @@
 // Chunk-parallel preparation on tcgen05 for D = 128 with the per-channel (KDA) gate:
 // persistent CTAs of 16 warps, one per SM, each looping over (chunk, head) items; the q, k,
 // v tiles of the next item arrive by TMA into a second buffer while the current item is
-// computed.  Same quantities as the warp-level kernel in gdr_prep.cu (the X/R form of the
-// FlashQLA dh kernel, "FlashQLA ... GDN 反向", §三; the scalar gate has its own kernel,
-// gdr_prep_gdn.cu):
+// computed.  Its outputs are the per-chunk tiles of the state recurrences and the main
+// backward (the X/R form of the FlashQLA dh kernel, "FlashQLA ... GDN 反向", §三; the
+// scalar gate has its own kernel, gdr_prep_gdn.cu):
 //
 //   [A_raw; P] = [kd'; qd'] ki'^T       A = strict_lower(diag(beta) A_raw) (fp32), P = lower(.)
 //   T   = (I + A)^-1                     (blocked inverse to fp32 accuracy, gdr_invert.cuh)

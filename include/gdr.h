@@ -74,7 +74,10 @@ typedef struct {
     int32_t num_seqs;          /* N >= 1 */
     int64_t total_tokens;      /* T_total >= 0 */
     int32_t num_heads;         /* H >= 1 */
-    int32_t head_dim;          /* D = dk = dv, 64 or 128 */
+    int32_t head_dim;          /* D = dk = dv, 64 or 128.  64 runs the 128-channel kernels on
+                                * inputs zero-padded to 128 channels in the workspace (zero
+                                * channels leave every product, norm and sum of the method
+                                * unchanged; the results are the first 64 channels) */
     const int64_t* cu_seqlens; /* device int64 [N + 1], or NULL for dense */
     float scale;               /* output scale, usually 1 / sqrt(D) */
     /* KDA only (ignored by the GDN calls): the per-channel gate function, with
@@ -95,7 +98,8 @@ typedef struct {
 #define GDR_KDA_GATE_SIGMOID 1
 
 /* Bytes of the scratch workspace that gdr_fwd_states / gdr_bwd / kda_fwd_states /
- * kda_bwd need for this shape (returns 0 for an invalid shape). */
+ * kda_bwd need for this shape (returns 0 for an invalid shape); for head_dim 64 it
+ * includes the zero-padded copies of the inputs and outputs. */
 size_t gdr_workspace_bytes(const gdr_shape* shape);
 
 /* Bytes of the per-chunk state buffer written by gdr_fwd_states / kda_fwd_states /
@@ -103,6 +107,9 @@ size_t gdr_workspace_bytes(const gdr_shape* shape);
  * state of every 64-token chunk and head, stored value-major ([chunk][head][dv][dk],
  * i.e. S^T, the layout the tensor-core products read), with chunks numbered sequence
  * after sequence.
+ *
+ * head_dim 64 runs on the channels zero-padded to 128 (see gdr_shape.head_dim), and
+ * its states keep that padded layout ([chunk][head][128][128]).
  *
  * The header records what the states were computed for: the variant (GDN, KDA with
  * the softplus gate, KDA with the sigmoid-bounded gate and its gate_scale), whether

@@ -52,7 +52,13 @@ def test_workspace_sizes(L):
     # varlen bound: sum ceil(len/64) <= (T + 63 N) / 64
     fake_cu = ctypes.c_void_p(256)
     sh2 = api.GdrShape(3, 130, 2, 64, fake_cu.value, 0.125)
-    assert gdr.states_bytes(sh2) == HDR + ((130 + 63 * 3) // 64) * 2 * 64 * 64 * 2
+    # head_dim 64 runs on channels zero-padded to 128: its states keep the padded layout, and
+    # its workspace holds the padded inputs and outputs beyond the 128-channel layout
+    assert gdr.states_bytes(sh2) == HDR + ((130 + 63 * 3) // 64) * 2 * 128 * 128 * 2
+    sh3 = api.GdrShape(3, 130, 2, 128, fake_cu.value, 0.125)
+    # (10 token-major bf16 tensors, 4 fp32 states-shaped ones, dt_bias and ddt_bias)
+    pads = 10 * 130 * 2 * 128 * 2 + 4 * 3 * 2 * 128 * 128 * 4 + 2 * 2 * 128 * 4
+    assert gdr.workspace_bytes(sh3) + pads <= gdr.workspace_bytes(sh2) <= gdr.workspace_bytes(sh3) + pads + 17 * 256
 
 
 @pytest.mark.parametrize("mutate,code", [
