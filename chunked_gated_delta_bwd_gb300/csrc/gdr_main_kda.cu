@@ -279,44 +279,42 @@ __global__ void __launch_bounds__(512, 1) k_main_kda(const Params p, const __gri
             g[i] = c0 + i < ci.len ? __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(sW0 + off)) : 0.f;
         }
     }
-    float acc = 0.f;
+    // the quarter's scan, its total and extrema; one exchange gives every thread the
+    // prefix, the chunk total and the chunk's extrema of its channel (the maximum over the
+    // rows is the largest quarter maximum plus that quarter's prefix: fp32 addition is
+    // monotone, so this is the maximum of the prefixed values bit for bit)
+    float acc = 0.f, lmx = -3.0e38f, lmn = 3.0e38f;
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
         if (c0 + i < ci.len) acc += kda_gate_fn<GATE>(p.gate_scale, a, g[i] + bias);
         g[i] = acc;
+        lmx = fmaxf(lmx, acc);
+        lmn = fminf(lmn, acc);
     }
-    sScan[hc * MD + L] = acc;  // this quarter's total
+    // (sRow holds the row dots later in the item and sDgTp the kr part of dgT: both free here)
+    sScan[hc * MD + L] = acc;
+    sRow[hc * MD + L] = lmx;
+    sDgTp[hc * MD + L] = lmn;
     __syncthreads();
-    float pre = 0.f, tot = 0.f;
+    float pre = 0.f, tot = 0.f, M = -3.0e38f, N = 3.0e38f;
 #pragma unroll
     for (int h2 = 0; h2 < 4; ++h2) {
         const float t = sScan[h2 * MD + L];
+        M = fmaxf(M, tot + sRow[h2 * MD + L]);
+        N = fminf(N, tot + sDgTp[h2 * MD + L]);
         if (h2 < hc) pre += t;
         tot += t;
     }
-    float mx = -3.0e38f, mn = 3.0e38f;
+    const float refL = 0.5f * (M + N);
+    float f[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        g[i] += pre;
-        mx = fmaxf(mx, g[i]);
-        mn = fminf(mn, g[i]);
-    }
-    tc::st16(tl(R_G + c0), g);
-    __syncthreads();  // totals read
-    sScan[hc * MD + L] = mx;
-    sRow[hc * MD + L] = mn;
-    __syncthreads();
+    for (int i = 0; i < 16; ++i) f[i] = __expf((g[i] + pre) - refL);
+    tc::st16(tl(R_G + c0), f);
     if (hc == 0) {
-        float M = sScan[L], N = sRow[L];
-#pragma unroll
-        for (int h2 = 1; h2 < 4; ++h2) {
-            M = fmaxf(M, sScan[h2 * MD + L]);
-            N = fminf(N, sRow[h2 * MD + L]);
-        }
-        sRef[L] = 0.5f * (M + N);
+        sRef[L] = refL;
         sGT[L] = tot;
-        sFac[L] = __expf(0.5f * (M + N));              // e^{ref}
-        sFac[MD + L] = __expf(tot - 0.5f * (M + N));   // e^{gT - ref}
+        sFac[L] = __expf(refL);             // e^{ref}
+        sFac[MD + L] = __expf(tot - refL);  // e^{gT - ref}
     }
 
     if (ci.len < CH) {
@@ -329,11 +327,6 @@ __global__ void __launch_bounds__(512, 1) k_main_kda(const Params p, const __gri
         }
     }
     __syncthreads();
-    const float refL = sRef[L];
-    float f[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) f[i] = __expf(g[i] - refL);
-    tc::st16(tl(R_G + c0), f);
 
     // inverse row norms of q (from W2) and k, 4 threads per row;
     // dgT state part (column sums of the value-major dS . S0)
@@ -423,6 +416,31 @@ __global__ void __launch_bounds__(512, 1) k_main_kda(const Params p, const __gri
         else
             store_cm(tile, x);
     };
+    // several derived tiles of k at once (e^{gc-ref} and the k rows read from tensor memory
+    // once): kd' (e), ki' (1 / e) and, if given, kr (e^{gT-ref} / e); each value exactly as
+    // build() forms it.  With `pair`, kd' and ki' are stored as bf16 pairs (lo tiles given).
+    auto build_k = [&](unsigned char* kdp, unsigned char* kdp_lo, unsigned char* kip, unsigned char* kip_lo,
+                       unsigned char* kr) {
+        float e[16], x[16], inv[16], v[16];
+        tc::ld16(tl(R_G + c0), e);
+        load_x(false, x, inv);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) x[i] = x[i] * derived_m(inv[i], 1.f, 1.f);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = x[i] * e[i];
+        if (kdp_lo) store_cm_pair(kdp, kdp_lo, v);
+        else store_cm(kdp, v);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = x[i] * __fdividef(1.f, e[i]);
+        if (kip_lo) store_cm_pair(kip, kip_lo, v);
+        else store_cm(kip, v);
+        if (kr) {
+            const float eGTref = sFac[MD + L];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = x[i] * __fdividef(eGTref, e[i]);
+            store_cm(kr, v);
+        }
+    };
 
     // per-thread accumulators (channel L, rows c0 .. c0+15)
     float dQn[NCOL], dKn[NCOL], dGc[NCOL], v[NCOL];
@@ -436,10 +454,10 @@ __global__ void __launch_bounds__(512, 1) k_main_kda(const Params p, const __gri
 
     // ---- G1: [A_raw; P] = [kd'; qd'] ki'^T ; then G3: dqd^T = S0 dO^T, G5b: dS^T kr^T --------
     // (G3 and G5b need no G1 result: they run while the G1 epilogue does)
-    build(sW0, nullptr, false, 1.f, F_KDP);    // kd'
-    build(sW1, nullptr, true, p.scale, F_KDP);  // qd'
-    build(sW2, nullptr, false, 1.f, F_KIP);     // ki' (the q tile is dead)
-    build(sK, nullptr, false, 1.f, F_KR);       // kr (the k tile is dead: staged in tensor memory)
+    // kd' -> W0, ki' -> W2 (the q tile is dead), kr -> K (the k tile is dead: q and k are
+    // staged in tensor memory), qd' -> W1
+    build_k(sW0, nullptr, sW2, nullptr, sK);
+    build(sW1, nullptr, true, p.scale, F_KDP);
     sync_all();
     if (tid == 0) {
         constexpr uint32_t id = tc::idesc(128, 64, 1, 1);
@@ -676,9 +694,8 @@ __global__ void __launch_bounds__(512, 1) k_main_kda(const Params p, const __gri
         store_cm_pair(sDS, sDS + TILE, o);
     }
     // rebuilds for G10 / G11: ki' -> W0 (lo W1), qd' -> W2 (lo K), kd' -> S0 (lo S0 + 16 KB)
-    build(sW0, sW1, false, 1.f, F_KIP);
+    build_k(sS0, sS0 + TILE, sW0, sW1, nullptr);
     build(sW2, sK, true, p.scale, F_KDP);
-    build(sS0, sS0 + TILE, false, 1.f, F_KDP);
     sync_all();
   // the raw gates again, for the gate chain rule, into the dead A and P tiles
     if (tid == 0) {
@@ -809,6 +826,13 @@ __global__ void __launch_bounds__(512, 1) k_main_kda(const Params p, const __gri
     // reverse cumsum of dgc over the rows per channel: this thread's 16 rows in registers,
     // the later row quarters' totals and the chunk constant dgT as the suffix; then the
     // gate chain rule per element, with per-channel partial sums
+    float sfx = 0.f;
+#pragma unroll
+    for (int i = 15; i >= 0; --i) {
+        sfx += dGc[i];
+        dGc[i] = sfx;
+    }
+    sScan[hc * MD + L] = sfx;  // read after the barrier of the raw-gate wait below
     float xr[16];
     const float dtb = sGate[L];
     {
@@ -823,14 +847,6 @@ __global__ void __launch_bounds__(512, 1) k_main_kda(const Params p, const __gri
             xr[i] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(gt + off)) + dtb;
         }
     }
-    float sfx = 0.f;
-#pragma unroll
-    for (int i = 15; i >= 0; --i) {
-        sfx += dGc[i];
-        dGc[i] = sfx;
-    }
-    sScan[hc * MD + L] = sfx;
-    __syncthreads();
     float post = dgT_of(L);
 #pragma unroll
     for (int h2 = 3; h2 >= 0; --h2)
@@ -849,14 +865,15 @@ __global__ void __launch_bounds__(512, 1) k_main_kda(const Params p, const __gri
             dA_acc += dA;
         }
     }
-    sync_all();  // suffix totals read; dg_raw staged
-    put_tile(&m.dgr, true, oA, 8192, p.dg_raw, ci, h);
-    sScan[hc * MD + L] = ddt;
+    // the partial sums go to the row-dot space (dead since the L2 backward) and the
+    // per-warp slots, so that one barrier serves them and the staged dg_raw
+    sRow[hc * MD + L] = ddt;
     dA_acc = warp_sum(dA_acc);
     if (lane == 0) sMisc[warp] = dA_acc;
-    __syncthreads();
+    sync_all();  // dg_raw staged; partial sums written
+    put_tile(&m.dgr, true, oA, 8192, p.dg_raw, ci, h);
     if (tid < MD) {
-        const float t = ((sScan[tid] + sScan[MD + tid]) + sScan[2 * MD + tid]) + sScan[3 * MD + tid];
+        const float t = ((sRow[tid] + sRow[MD + tid]) + sRow[2 * MD + tid]) + sRow[3 * MD + tid];
         atomicAdd(&p.ddt_bias[h * MD + tid], t);
     }
     if (tid == 0) {

@@ -258,44 +258,42 @@ __global__ void __launch_bounds__(512, 1) k_prep_kda(const Params p, const __gri
                 g[i] = c0 + i < ci.len ? __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(gt + off)) : 0.f;
             }
         }
-        float acc = 0.f;
+        // the quarter's scan, its total and extrema; one exchange gives every thread the
+        // prefix, the chunk total and the chunk's extrema of its channel (the maximum over
+        // the rows is the largest quarter maximum plus that quarter's prefix, bit for bit:
+        // fp32 addition is monotone)
+        float acc = 0.f, lmx = -3.0e38f, lmn = 3.0e38f;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             if (c0 + i < ci.len) acc += kda_gate_fn<GATE>(p.gate_scale, a, g[i] + bias);
             g[i] = acc;
+            lmx = fmaxf(lmx, acc);
+            lmn = fminf(lmn, acc);
         }
         sScan[hc * PD + L] = acc;
+        sTmp[hc * PD + L] = lmx;  // the inversion scratch is not in use yet
+        sTmp[4 * PD + hc * PD + L] = lmn;
         __syncthreads();
-        float pre = 0.f, tot = 0.f;
+        float pre = 0.f, tot = 0.f, M = -3.0e38f, N = 3.0e38f;
 #pragma unroll
         for (int h2 = 0; h2 < 4; ++h2) {
             const float t = sScan[h2 * PD + L];
+            M = fmaxf(M, tot + sTmp[h2 * PD + L]);
+            N = fminf(N, tot + sTmp[4 * PD + h2 * PD + L]);
             if (h2 < hc) pre += t;
             tot += t;
         }
-        float mx = -3.0e38f, mn = 3.0e38f;
+        refL = 0.5f * (M + N);
+        gTL = tot;
+        // e^{gc - ref} of this thread's channel and rows, in tensor memory
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            g[i] += pre;
-            mx = fmaxf(mx, g[i]);
-            mn = fminf(mn, g[i]);
-        }
+        for (int i = 0; i < 16; ++i) g[i] = __expf((g[i] + pre) - refL);
         tc::st16(tl(R_G + c0), g);
-        __syncthreads();
-        sScan[hc * PD + L] = mx;
-        sTmp[hc * PD + L] = mn;  // the inversion scratch is not in use yet
-        __syncthreads();
         if (hc == 0) {
-            float M = sScan[L], N = sTmp[L];
-#pragma unroll
-            for (int h2 = 1; h2 < 4; ++h2) {
-                M = fmaxf(M, sScan[h2 * PD + L]);
-                N = fminf(N, sTmp[h2 * PD + L]);
-            }
-            sRef[L] = 0.5f * (M + N);
+            sRef[L] = refL;
             sGT[L] = tot;
-            sFac[L] = __expf(0.5f * (M + N));             // e^{ref}
-            sFac[PD + L] = __expf(tot - 0.5f * (M + N));  // e^{gT - ref}
+            sFac[L] = __expf(refL);             // e^{ref}
+            sFac[PD + L] = __expf(tot - refL);  // e^{gT - ref}
             if (0.5f * (M - N) > 80.f || M > 80.f) atomicOr(p.status, ST_GATE_RANGE);
         }
     }
@@ -314,15 +312,6 @@ __global__ void __launch_bounds__(512, 1) k_prep_kda(const Params p, const __gri
         }
     }
     __syncthreads();
-    {  // e^{gc - ref} of this thread's channel and rows replaces gc in tensor memory
-        refL = sRef[L];
-        gTL = sGT[L];
-        float g[16];
-        tc::ld16(tl(R_G + c0), g);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) g[i] = __expf(g[i] - refL);
-        tc::st16(tl(R_G + c0), g);
-    }
     {  // inverse row norms of q and k, 4 threads per row
         const int r = (tid >> 2) & 63, part = tid & 3;
         const unsigned char* src = tid < 256 ? sQ : sK;
