@@ -41,6 +41,16 @@ __device__ __forceinline__ float2 unpack_bf16(uint32_t u) {
 
 __device__ __forceinline__ float bf2f(__nv_bfloat16 x) { return __bfloat162float(x); }
 
+// Elements i, i + 1 of a register array as a pair for the two-wide fp32 instructions
+// (__fmul2_rn, __fadd2_rn, __ffma2_rn), and a pair written back.
+#define F2(a, i) make_float2((a)[i], (a)[(i) + 1])
+#define ACC2(a, i, expr)            \
+    do {                            \
+        const float2 r_ = (expr);   \
+        (a)[i] = r_.x;              \
+        (a)[(i) + 1] = r_.y;        \
+    } while (0)
+
 // --------------------------------------------------------------------------
 // chunk table lookup
 // --------------------------------------------------------------------------

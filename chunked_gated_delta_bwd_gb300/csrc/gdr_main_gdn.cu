@@ -454,7 +454,10 @@ __global__ void __launch_bounds__(512, 1) k_main_gdn(const Params p, const __gri
         tc::ld16(tl(R_G5 + c0), w);
         rows16(sTab + T_KRF * CH, kf);
 #pragma unroll
-        for (int i = 0; i < NCOL; ++i) v[i] += w[i] * kf[i];  // + dS^T kr^T
+        for (int i = 0; i < NCOL; i += 2) {  // + dS^T kr^T
+            const float2 r = __ffma2_rn(F2(w, i), F2(kf, i), F2(v, i));
+            v[i] = r.x, v[i + 1] = r.y;
+        }
         store_cm(sDU, v);  // du^T [j][r]
     }
     sync_all();
@@ -533,31 +536,32 @@ __global__ void __launch_bounds__(512, 1) k_main_gdn(const Params p, const __gri
         tc::ld16(tl(R_A + c0), v);  // dqd^T (lane = key channel)
         load_x(true, x, inv);
 #pragma unroll
-        for (int i = 0; i < NCOL; ++i) {  // dqd
-            const float t = p.scale * v[i] * f[i];
-            dQn[i] += t;
-            dGc[i] += x[i] * inv[i] * t;
+        for (int i = 0; i < NCOL; i += 2) {  // dqd
+            const float2 t = __fmul2_rn(__fmul2_rn(make_float2(p.scale, p.scale), F2(v, i)), F2(f, i));
+            ACC2(dQn, i, __fadd2_rn(F2(dQn, i), t));
+            ACC2(dGc, i, __ffma2_rn(__fmul2_rn(F2(x, i), F2(inv, i)), t, F2(dGc, i)));
         }
         tc::ld16(tl(R_A + 64 + c0), v);  // Z^T
         load_x(false, x, inv);
         rows16(sBeta, bt);
 #pragma unroll
-        for (int i = 0; i < NCOL; ++i) {  // dkd (from E) = -beta Z
-            const float t = -bt[i] * v[i] * f[i];
-            dKn[i] += t;
-            dGc[i] += x[i] * inv[i] * t;
+        for (int i = 0; i < NCOL; i += 2) {  // dkd (from E) = -beta Z
+            const float2 t = __fmul2_rn(__fmul2_rn(make_float2(-bt[i], -bt[i + 1]), F2(v, i)), F2(f, i));
+            ACC2(dKn, i, __fadd2_rn(F2(dKn, i), t));
+            ACC2(dGc, i, __ffma2_rn(__fmul2_rn(F2(x, i), F2(inv, i)), t, F2(dGc, i)));
         }
         tc::ld16(tl(R_C + c0), v);
         rows16(sFac + F_KR * CH, f);
-        float dgt = 0.f;
+        float2 dgt2 = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int i = 0; i < NCOL; ++i) {  // dkr
-            const float t = v[i] * f[i];
-            dKn[i] += t;
-            const float kt = x[i] * inv[i] * t;
-            dGc[i] -= kt;
-            dgt += kt;
+        for (int i = 0; i < NCOL; i += 2) {  // dkr
+            const float2 t = __fmul2_rn(F2(v, i), F2(f, i));
+            ACC2(dKn, i, __fadd2_rn(F2(dKn, i), t));
+            const float2 kt = __fmul2_rn(__fmul2_rn(F2(x, i), F2(inv, i)), t);
+            ACC2(dGc, i, __fadd2_rn(F2(dGc, i), make_float2(-kt.x, -kt.y)));
+            dgt2 = __fadd2_rn(dgt2, kt);
         }
+        const float dgt = dgt2.x + dgt2.y;
         sDgTp[hc * MD + L] = dgt;
     }
     {
@@ -601,11 +605,11 @@ __global__ void __launch_bounds__(512, 1) k_main_gdn(const Params p, const __gri
         float o[16], cf[16];
         rows16(sTab + T_CF * CH, cf);
 #pragma unroll
-        for (int i = 0; i < NCOL; ++i) o[i] = br * v[i] * cf[i];
+        for (int i = 0; i < NCOL; i += 2) ACC2(o, i, __fmul2_rn(__fmul2_rn(make_float2(br, br), F2(v, i)), F2(cf, i)));
         store_cm(sDS, o);
         const float rf = isP ? sTab[T_RP * CH + r] : br * sTab[T_RK * CH + r];
 #pragma unroll
-        for (int i = 0; i < NCOL; ++i) o[i] = v[i] * rf;
+        for (int i = 0; i < NCOL; i += 2) ACC2(o, i, __fmul2_rn(F2(v, i), make_float2(rf, rf)));
         store_cm(sDS + TILE, o);
     }
     sync_all();
@@ -637,14 +641,15 @@ __global__ void __launch_bounds__(512, 1) k_main_gdn(const Params p, const __gri
         rows16(sFac + F_KDP * CH, f);
         tc::ld16(tl(R_A + c0), v);
 #pragma unroll
-        for (int i = 0; i < NCOL; ++i) dQn[i] += p.scale * v[i] * f[i];  // dqd'
+        for (int i = 0; i < NCOL; i += 2)  // dqd'
+            ACC2(dQn, i, __ffma2_rn(__fmul2_rn(make_float2(p.scale, p.scale), F2(v, i)), F2(f, i), F2(dQn, i)));
         tc::ld16(tl(R_A + 64 + c0), v);
 #pragma unroll
-        for (int i = 0; i < NCOL; ++i) dKn[i] += v[i] * f[i];  // dkd'
+        for (int i = 0; i < NCOL; i += 2) ACC2(dKn, i, __ffma2_rn(F2(v, i), F2(f, i), F2(dKn, i)));  // dkd'
         rows16(sFac + F_KIP * CH, f);
         tc::ld16(tl(R_B + c0), v);
 #pragma unroll
-        for (int i = 0; i < NCOL; ++i) dKn[i] += v[i] * f[i];  // dki'
+        for (int i = 0; i < NCOL; i += 2) ACC2(dKn, i, __ffma2_rn(F2(v, i), F2(f, i), F2(dKn, i)));  // dki'
     }
 
     // ---- epilogue: L2-norm backward, dq / dk, dbeta, the gate gradient ----------------------
@@ -659,10 +664,10 @@ __global__ void __launch_bounds__(512, 1) k_main_gdn(const Params p, const __gri
             float x[16], inv[16];
             load_x(true, x, inv);
 #pragma unroll
-            for (int i = 0; i < NCOL; ++i) t[i] = dQn[i] * x[i] * inv[i];
+            for (int i = 0; i < NCOL; i += 2) ACC2(t, i, __fmul2_rn(__fmul2_rn(F2(dQn, i), F2(x, i)), F2(inv, i)));
             load_x(false, x, inv);
 #pragma unroll
-            for (int i = 0; i < NCOL; ++i) t[16 + i] = dKn[i] * x[i] * inv[i];
+            for (int i = 0; i < NCOL; i += 2) ACC2(t, 16 + i, __fmul2_rn(__fmul2_rn(F2(dKn, i), F2(x, i)), F2(inv, i)));
         }
         const float s = warp_transpose_sum32(t);  // lane l: value l (l < 16: q row c0+l, else k row c0+l-16)
         (lane < 16 ? sRowQ : sRowK)[q4 * CH + c0 + (lane & 15)] = s;
