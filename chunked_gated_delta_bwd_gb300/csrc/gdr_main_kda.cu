@@ -334,7 +334,8 @@ __global__ void __launch_bounds__(512, 1) k_main_kda(const Params p, const __gri
         const int r = (tid >> 2) & 63, part = tid & 3;
         const unsigned char* src = tid < 256 ? sW2 : sK;
         float s = 0.f;
-        for (int j = part * 4; j < part * 4 + 4; ++j) {
+        for (int jj = 0; jj < 4; ++jj) {
+            const int j = tc::rowpart_chunk(part, jj);
             const uint4 v = *reinterpret_cast<const uint4*>(src + tc::sw_chunk(r, j, 64));
             const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -610,7 +611,8 @@ __global__ void __launch_bounds__(512, 1) k_main_kda(const Params p, const __gri
     if (tid < 4 * CH) {
         const int r = tid >> 2, part = tid & 3;
         float s2 = 0.f;
-        for (int j = part * 4; j < part * 4 + 4; ++j) {
+        for (int jj = 0; jj < 4; ++jj) {
+            const int j = tc::rowpart_chunk(part, jj);
             const uint4 a = *reinterpret_cast<const uint4*>(sDOY + tc::sw_chunk(64 + r, j, 128));
             const uint4 b = *reinterpret_cast<const uint4*>(sV + tc::sw_chunk(r, j, 64));
             const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};

@@ -316,7 +316,8 @@ __global__ void __launch_bounds__(512, 1) k_prep_kda(const Params p, const __gri
         const int r = (tid >> 2) & 63, part = tid & 3;
         const unsigned char* src = tid < 256 ? sQ : sK;
         float s = 0.f;
-        for (int j = part * 4; j < part * 4 + 4; ++j) {
+        for (int jj = 0; jj < 4; ++jj) {
+            const int j = tc::rowpart_chunk(part, jj);
             const uint4 v = *reinterpret_cast<const uint4*>(src + tc::sw_chunk(r, j, 64));
             const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll

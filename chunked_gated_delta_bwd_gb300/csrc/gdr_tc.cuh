@@ -25,6 +25,12 @@ __device__ __forceinline__ uint32_t sw_chunk(int r, int j, int rows) {
     return (uint32_t)((j >> 3) * rows * 128 + r * 128 + (((j & 7) ^ (r & 7)) << 4));
 }
 
+// Four threads per row reading a 128-column swizzled row in 16-byte chunks: part p (0..3)
+// takes chunks 2p, 2p + 1, 2p + 8, 2p + 9 at steps jj = 0..3.  In each quarter warp (two
+// rows, four parts) the eight requests of a step then fall on eight different chunk
+// positions (one row's on even positions, the other's on odd), so no bank is hit twice.
+__device__ __forceinline__ int rowpart_chunk(int part, int jj) { return 2 * part + (jj & 1) + 8 * (jj >> 1); }
+
 __device__ __forceinline__ uint64_t desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
     return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
            ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
