@@ -54,14 +54,15 @@ def test_empty_and_single_token_sequences(dim):
     torch.testing.assert_close(gpu["ht"][2], x["h0"][2], rtol=0, atol=0)
 
 
-@pytest.mark.parametrize("mode", ["gdn", "kda"])
-@pytest.mark.parametrize("lengths", [[200, 77], [16000, 64]])
-def test_forward_states_feed_the_backward(mode, lengths):
+@pytest.mark.parametrize("mode,lengths,dim", [("gdn", [200, 77], 128), ("kda", [200, 77], 128),
+                                             ("gdn", [16000, 64], 128), ("kda", [16000, 64], 128),
+                                             ("gdn", [200, 77], 64), ("kda", [200, 77], 64)])
+def test_forward_states_feed_the_backward(mode, lengths, dim):
     # the chunk-start states kept by the forward equal gdr_fwd_states's, and a backward from
     # them equals the backward that recomputes them (the long case runs the state chains as
     # segments: forward-only, backward-only and both directions)
     import chunked_gated_delta_bwd_gb300 as gdr
-    x = inputs.custom(mode, lengths, heads=2, dim=128, seed=113, with_h0=True, with_dht=True)
+    x = inputs.custom(mode, lengths, heads=2, dim=dim, seed=113, with_h0=True, with_dht=True)
     d = H.to_gpu(x)
     kw = dict(h0=d["h0"], cu_seqlens=d["cu_seqlens"], scale=d["scale"])
     if mode == "gdn":
@@ -71,7 +72,8 @@ def test_forward_states_feed_the_backward(mode, lengths):
                                         g_raw=d["g_raw"], A_log=d["A_log"], dt_bias=d["dt_bias"], **kw)
     fwd = H.run_gpu_fwd(x, states=True)
     # chunks are numbered sequence after sequence; the buffer's tail past the last chunk
-    # (its size is a bound for varlen) is not written
+    # (its size is a bound for varlen) is not written; head_dim 64 keeps the states of the
+    # channels zero-padded to 128
     used = 256 + sum((n + 63) // 64 for n in lengths) * 2 * 128 * 128 * 2  # header + the states
     assert torch.equal(fwd["states"][:used], ref_states.cpu()[:used])
     a = H.run_gpu(x, states=fwd["states"].cuda())

@@ -96,10 +96,11 @@ def test_empty_and_single_token_sequences():
     torch.testing.assert_close(gpu["dh0"][2], x["dht"][2], rtol=0, atol=0)
 
 
-def test_saved_states_match_recompute():
+@pytest.mark.parametrize("dim", [64, 128])
+def test_saved_states_match_recompute(dim):
     import chunked_gated_delta_bwd_gb300 as gdr
     for mode in ("gdn", "kda"):
-        x = inputs.custom(mode, [200, 77], heads=2, dim=128, seed=105, with_h0=True, with_dht=True)
+        x = inputs.custom(mode, [200, 77], heads=2, dim=dim, seed=105, with_h0=True, with_dht=True)
         d = H.to_gpu(x)
         if mode == "gdn":
             st = gdr.gdr_fwd_states(d["q"], d["k"], d["v"], d["g"], d["beta_logit"], h0=d["h0"],
