@@ -49,9 +49,9 @@ constexpr int oA = oT + 8192;   // A fp32 [64][LDF] row-major; the next item's r
 constexpr int oTf = oA + CH * LDF * 4;  // T fp32, transposed [c][r], stride LDF
 constexpr int oTmp = oTf + CH * LDF * 4;  // 8 warps' transfer tiles [8][XLD]
 constexpr int nTmp = 8 * 8 * XLD;
-constexpr int oSmall = (oTmp + nTmp * 4 + 1023) / 1024 * 1024;
-static_assert(oTmp + nTmp * 4 <= oSmall, "inversion scratch overlaps the small arrays");
-static_assert(CH * LDF * 4 >= TILE, "the raw-gate tile fits the space of A");
+constexpr int oGR = (oTmp + nTmp * 4 + 1023) / 1024 * 1024;  // raw gates (token-major) of the item
+static_assert(oTmp + nTmp * 4 <= oGR, "inversion scratch overlaps the raw-gate tile");
+constexpr int oSmall = oGR + TILE;
 static_assert(nTmp >= 4 * PD, "the gate scan's minima fit the transfer tiles");
 constexpr int nInvQ = 64, nInvK = 64, nBeta = 64, nFac = 256, nRef = 128, nGT = 128, nScan = 512;
 constexpr int SMALL_FLOATS = nInvQ + nInvK + nBeta + nFac + nRef + nGT + nScan;
@@ -126,11 +126,11 @@ __global__ void __launch_bounds__(512, 1) k_prep_kda(const Params p, const __gri
         if (which < 0 || which == 1) tc::tma_load_4d(st + oK, &m.k, 0, qk_head(p, hh), t0, 0, bar);
         if (which < 0 || which == 2) tc::tma_load_4d(st + oV, &m.v, 0, hh, t0, 0, bar);
     };
-    // raw gates of `item`, token-major, into the space of A (dead from the end of the
-    // inversion to the next item's G1)
+    // raw gates of `item`, token-major, into their own tile (requested as soon as the item
+    // before has read its gates, a whole item ahead of their use)
     auto issue_gate_load = [&](int item, const ChunkInfo& cj) {
         tc::mbar_expect_tx(mgr, TILE);
-        tc::tma_load_4d(sb + oA, &m.graw, 0, item % p.H, (int)cj.t0, 0, mgr);
+        tc::tma_load_4d(sb + oGR, &m.graw, 0, item % p.H, (int)cj.t0, 0, mgr);
     };
     if (warp == 0) tc::alloc(smem_u32(tslot), 512);
     if (tid == 0) {
@@ -167,12 +167,13 @@ __global__ void __launch_bounds__(512, 1) k_prep_kda(const Params p, const __gri
     };
     int pending = -1;  // stage with a load in flight that this item does not consume, or -1
     uint32_t pending_par = 0;
-    bool pending_g = (int)blockIdx.x < n_items;  // a raw-gate tile is in flight
+    bool pending_g = (int)blockIdx.x < n_items;  // a raw-gate tile is in flight ...
+    uint32_t pend_g_par = 0;                       // ... completing this phase parity of its barrier
     auto bail = [&]() {
         if (tid == 0) {
             atomicOr(p.status, ST_MMA_TIMEOUT);
             if (pending >= 0) tc::mbar_wait(mload0 + 8 * pending, pending_par);  // bounded drain
-            if (pending_g) tc::mbar_wait(mgr, (uint32_t)(it & 1));
+            if (pending_g) tc::mbar_wait(mgr, pend_g_par);
         }
         if (tid == STORE_TID) tc::bulk_wait_all();
         tc::fence_before();
@@ -250,7 +251,7 @@ __global__ void __launch_bounds__(512, 1) k_prep_kda(const Params p, const __gri
         }
         float g[16];
         {
-            const unsigned char* gt = smem + oA;
+            const unsigned char* gt = smem + oGR;
             const int lch = (L & 63) >> 3, lsub = (L & 7) << 1;
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
@@ -274,6 +275,11 @@ __global__ void __launch_bounds__(512, 1) k_prep_kda(const Params p, const __gri
         sTmp[hc * PD + L] = lmx;  // the inversion scratch is not in use yet
         sTmp[4 * PD + hc * PD + L] = lmn;
         __syncthreads();
+        if (has_next) {  // every thread has read this item's raw gates: the next item's, into the tile
+            if (tid == 480) issue_gate_load(item + gridDim.x, get_ci(stg ^ 1));  // (not the product-issuing thread)
+            pending_g = true;
+            pend_g_par = (uint32_t)((it + 1) & 1);
+        }
         float pre = 0.f, tot = 0.f, M = -3.0e38f, N = 3.0e38f;
 #pragma unroll
         for (int h2 = 0; h2 < 4; ++h2) {
@@ -470,10 +476,6 @@ __global__ void __launch_bounds__(512, 1) k_prep_kda(const Params p, const __gri
                              // of the store thread at that item's top
         tc::tma_store_2d(&m.T, 0, (chunk * p.H + h) * CH, sb + oT);
         tc::bulk_commit();
-    }
-    if (has_next) {  // the space of A is free: the next item's small inputs and raw gates
-        if (tid == 480) issue_gate_load(item + gridDim.x, get_ci(stg ^ 1));  // (not the product-issuing thread)
-        pending_g = true;
     }
 
     // ---- W^T = (beta kd)^T T^T ; U^T = (beta V)^T T^T --------------------------------------
