@@ -15,23 +15,20 @@
 
 namespace gdr {
 
-// fp32 gate storage in shared memory
-template <int D, bool KDA>
-struct Gates {
-    static constexpr int LDG = D + 8;  // row stride of gc (KDA)
-    float* gc;   // KDA [C][LDG]; GDN [C]
-    float* ref;  // KDA [D];      GDN [1]
-    float* gT;   // KDA [D];      GDN [1]
-    __device__ __forceinline__ float gcv(int r, int d) const { return KDA ? gc[r * LDG + d] : gc[r]; }
-    __device__ __forceinline__ float refv(int d) const { return KDA ? ref[d] : ref[0]; }
-    __device__ __forceinline__ float gTv(int d) const { return KDA ? gT[d] : gT[0]; }
-    static constexpr int floats() { return KDA ? CH * LDG + 2 * D : CH + 2; }
+// fp32 storage in shared memory of the scalar (GDN) gate of one chunk: the inclusive cumsum
+// gc[r], ref = (max gc + min gc) / 2 and gT = gc[C-1]
+struct ScalarGates {
+    float* gc;   // [C]
+    float* ref;  // [1]
+    float* gT;   // [1]
+    __device__ __forceinline__ float gcv(int r) const { return gc[r]; }
+    __device__ __forceinline__ float refv() const { return ref[0]; }
+    __device__ __forceinline__ float gTv() const { return gT[0]; }
 };
 
 // GDN gate of one chunk by the first warp: lane l holds g of rows 2l and 2l + 1 (0 past
 // the chunk's end); writes gc (inclusive cumsum), gT and ref = (max gc + min gc) / 2.
-template <int D>
-__device__ __forceinline__ void gdn_gate_scan(float g0, float g1, const Gates<D, false>& G, bool flag_range,
+__device__ __forceinline__ void gdn_gate_scan(float g0, float g1, const ScalarGates& G, bool flag_range,
                                               const Params& p) {
     const int lane = threadIdx.x & 31, r0 = 2 * lane;
     const float s = g0 + g1;
@@ -61,18 +58,18 @@ __device__ __forceinline__ void gdn_gate_scan(float g0, float g1, const Gates<D,
 // Exponent kinds of the derived tiles (factor e^{a gc + b ref + c gT}).
 enum Fac { F_KD = 0, F_KDP = 1, F_KIP = 2, F_KR = 3 };  // e^{gc}, e^{gc-ref}, e^{ref-gc}, e^{gT-gc}
 
-template <int KIND, int D, bool KDA>
-__device__ __forceinline__ float gate_exponent(const Gates<D, KDA>& G, int r, int d) {
-    const float gc = G.gcv(r, d);
+template <int KIND>
+__device__ __forceinline__ float gate_exponent(const ScalarGates& G, int r) {
+    const float gc = G.gcv(r);
     if (KIND == F_KD) return gc;
-    if (KIND == F_KDP) return gc - G.refv(d);
-    if (KIND == F_KIP) return G.refv(d) - gc;
-    return G.gTv(d) - gc;
+    if (KIND == F_KDP) return gc - G.refv();
+    if (KIND == F_KIP) return G.refv() - gc;
+    return G.gTv() - gc;
 }
 
-template <int KIND, int D, bool KDA>
-__device__ __forceinline__ float gate_factor(const Gates<D, KDA>& G, int r, int d) {
-    return __expf(gate_exponent<KIND>(G, r, d));
+template <int KIND>
+__device__ __forceinline__ float gate_factor(const ScalarGates& G, int r) {
+    return __expf(gate_exponent<KIND>(G, r));
 }
 
 // Row factor of a derived tile element as the tensor cores see it: bf16(x * m * f) with

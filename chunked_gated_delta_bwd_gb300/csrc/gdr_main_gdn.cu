@@ -116,7 +116,7 @@ __global__ void __launch_bounds__(512, 1) k_main_gdn(const Params p, const __gri
                    mb3 = smem_u32(mbars + 3);
     const uint32_t mstall = smem_u32(mbars + 5);  // test hook only: a barrier nothing arrives on
 
-    Gates<MD, false> G;
+    ScalarGates G;
     G.gc = sGate;
     G.ref = sGate + CH;
     G.gT = sGate + CH + 1;
@@ -337,10 +337,10 @@ __global__ void __launch_bounds__(512, 1) k_main_gdn(const Params p, const __gri
         if (part == 0) (tid < 256 ? sInvQ : sInvK)[r] = rsqrtf(s + 1e-6f);
     }
     if (tid < CH) {
-        sFac[F_KD * CH + tid] = gate_factor<F_KD>(G, tid, 0);
-        sFac[F_KDP * CH + tid] = gate_factor<F_KDP>(G, tid, 0);
-        sFac[F_KIP * CH + tid] = gate_factor<F_KIP>(G, tid, 0);
-        sFac[F_KR * CH + tid] = gate_factor<F_KR>(G, tid, 0);
+        sFac[F_KD * CH + tid] = gate_factor<F_KD>(G, tid);
+        sFac[F_KDP * CH + tid] = gate_factor<F_KDP>(G, tid);
+        sFac[F_KIP * CH + tid] = gate_factor<F_KIP>(G, tid);
+        sFac[F_KR * CH + tid] = gate_factor<F_KR>(G, tid);
     }
     {
         const int cp = tid >> 3, g = tid & 7;  // column pair, row group
@@ -357,7 +357,7 @@ __global__ void __launch_bounds__(512, 1) k_main_gdn(const Params p, const __gri
             s1 += __shfl_xor_sync(0xffffffffu, s1, o);
         }
         if (g == 0) {
-            const float eg = __expf(G.gTv(0));
+            const float eg = __expf(G.gTv());
             sDgTs[2 * cp] = s0 * eg;
             sDgTs[2 * cp + 1] = s1 * eg;
         }

@@ -104,7 +104,7 @@ __global__ void __launch_bounds__(512, 1) k_prep_gdn(const Params p, const __gri
         return fsm + x * nPar + nInvQ + nInvK + nBeta;
     };
     auto gates = [&](int x) {
-        Gates<PD, false> G;
+        ScalarGates G;
         G.gc = fsm + x * nPar + nInvQ + nInvK + nBeta + nFac;
         G.ref = G.gc + CH;
         G.gT = G.gc + CH + 1;
@@ -351,10 +351,10 @@ __global__ void __launch_bounds__(512, 1) k_prep_gdn(const Params p, const __gri
         s += __shfl_xor_sync(0xffffffffu, s, 2);
         const float sk = __shfl_xor_sync(0xffffffffu, s, 4);
         if (part == 0) {
-            const Gates<PD, false> G = gates(x);
+            const ScalarGates G = gates(x);
             const float iq = rsqrtf(s + 1e-6f), ik = rsqrtf(sk + 1e-6f), bt = sBeta(x)[r];
-            const float fkd = gate_factor<F_KD>(G, r, 0), fkdp = gate_factor<F_KDP>(G, r, 0);
-            const float fkip = gate_factor<F_KIP>(G, r, 0), fkr = gate_factor<F_KR>(G, r, 0);
+            const float fkd = gate_factor<F_KD>(G, r), fkdp = gate_factor<F_KDP>(G, r);
+            const float fkip = gate_factor<F_KIP>(G, r), fkr = gate_factor<F_KR>(G, r);
             float* fac = sFac(x);
             sInvQ(x)[r] = iq;
             sInvK(x)[r] = ik;
@@ -435,7 +435,7 @@ __global__ void __launch_bounds__(512, 1) k_prep_gdn(const Params p, const __gri
         }
         tc::fence_async_smem();
         if (hc == 2) {
-            const float gt = gates(x).gTv(0);
+            const float gt = gates(x).gTv();
             p.gT[((size_t)chunk * p.H + h) * PD + L] = gt;
             p.egT[((size_t)chunk * p.H + h) * PD + L] = __expf(gt);
         }
