@@ -43,6 +43,9 @@
  *    kernels cannot represent) set bits in the workspace status word; read
  *    it with gdr_workspace_status after the work completes.
  *  * Calls that share a workspace must not run concurrently.
+ *  * Stream capture: gdr_bwd and kda_bwd enqueue only kernels and memsets on `stream`
+ *    and never wait on the host, so a call can be captured into a CUDA graph and
+ *    replayed (with the same buffers); the replay gives the same results.
  */
 #ifndef GDR_H
 #define GDR_H

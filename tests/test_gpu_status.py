@@ -81,3 +81,42 @@ def test_timed_out_wait_sets_the_status_and_leaves_the_context_usable():
     gpu = H.run_gpu(x, workspace=ws)
     assert gdr.workspace_status(ws) == 0
     print(H.assert_parity(H.compare(gpu, H.run_oracle(x), x), "after timeout"))
+
+
+@pytest.mark.parametrize("mode", ["gdn", "kda"])
+def test_backward_captures_into_a_cuda_graph(mode):
+    # every step of a call is a kernel or memset on the caller's stream and nothing waits on
+    # the host, so a call can be captured once and replayed: the replay equals an eager call
+    x = inputs.custom(mode, [700, 300, 64], heads=4, dim=128, seed=123, with_h0=True, with_dht=True)
+    d = H.to_gpu(x)
+    ws = H._workspace(d, x, None)
+    N = d["cu_seqlens"].numel() - 1
+    common = dict(h0=d["h0"], dht=d["dht"], cu_seqlens=d["cu_seqlens"], num_seqs=N, scale=d["scale"], workspace=ws)
+    T, Hh, D = d["v"].shape
+    out = gdr.alloc_outputs(T, Hh, D, N, mode)
+
+    def call():
+        if mode == "gdn":
+            gdr.gdr_bwd(d["q"], d["k"], d["v"], d["g"], d["beta_logit"], d["dO"], out=out, **common)
+        else:
+            gdr.kda_bwd(d["q"], d["k"], d["v"], d["g_raw"], d["A_log"], d["dt_bias"], d["beta_logit"], d["dO"],
+                        out=out, **common)
+
+    call()  # eager, also the warm-up before capture
+    torch.cuda.synchronize()
+    eager = {k: v.clone() for k, v in out.items()}
+    for v in out.values():
+        v.zero_()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        call()
+    for v in out.values():
+        v.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert gdr.workspace_status(ws) == 0
+    for k, v in out.items():
+        if k in ("dA_log", "ddt_bias"):  # fp32 atomics: the order of the additions may differ
+            torch.testing.assert_close(v, eager[k], rtol=1e-5, atol=1e-6)
+        else:
+            assert torch.equal(v, eager[k]), k
