@@ -556,12 +556,37 @@ static gdr_status pad64_inputs(const gdr_shape* sh, const Pad64& P, unsigned cha
     return e == cudaSuccess ? GDR_OK : cuda_fail(e, "channel padding launch");
 }
 
+// Calls with no token at all (every sequence empty): nothing to differentiate but h0, whose
+// gradient is dht; the final state of a forward is h0.  The token tensors may be NULL.
+static gdr_status empty_state_copy(float* dst, const float* src, const gdr_shape* sh, cudaStream_t s) {
+    const size_t bytes = (size_t)sh->num_seqs * sh->num_heads * sh->head_dim * sh->head_dim * 4;
+    cudaError_t e = src ? cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, s) : cudaMemsetAsync(dst, 0, bytes, s);
+    return e == cudaSuccess ? GDR_OK : cuda_fail(e, "state copy (no tokens)");
+}
+static gdr_status empty_front(void* ws, size_t ws_bytes, const gdr_shape* sh, cudaStream_t s) {
+    if (!ws) return fail(GDR_ERR_INVALID, "required pointer ws is NULL%s");
+    if (ws_bytes < workspace_total(sh)) return fail(GDR_ERR_WORKSPACE, "workspace too small%s");
+    cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(int), s);
+    return e == cudaSuccess ? GDR_OK : cuda_fail(e, "cudaMemsetAsync(status)");
+}
+
 static gdr_status fwd_states_impl(const gdr_shape* sh, const void* q, const void* k, const void* v,
                                   const float* g, const void* g_raw, const float* A_log,
                                   const float* dt_bias, const void* beta, const float* h0,
                                   void* states, size_t states_bytes, void* ws, size_t ws_bytes,
                                   void* stream, int kda) {
     if (gdr_status st0 = check_shape(sh)) return st0;
+    if (sh->total_tokens == 0) {
+        NEED(states); OPT(h0);
+        if (states_bytes < gdr_states_bytes(sh)) return fail(GDR_ERR_WORKSPACE, "states buffer too small%s");
+        cudaStream_t s = (cudaStream_t)stream;
+        if (gdr_status st = empty_front(ws, ws_bytes, sh, s)) return st;
+        k_states_tag<<<1, 32, 0, s>>>(static_cast<int*>(states), states_tag(sh, kda, h0, 0, sh->head_dim));
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail(e, "states header launch");
+        g_err[0] = 0;
+        return GDR_OK;
+    }
     if (sh->head_dim == 128)
         return fwd_states_impl128(sh, q, k, v, g, g_raw, A_log, dt_bias, beta, h0, states, states_bytes, ws,
                                   ws_bytes, stream, kda, 128);
@@ -585,6 +610,21 @@ static gdr_status fwd_impl(const gdr_shape* sh, const void* q, const void* k, co
                            const float* h0, void* o, float* ht, void* states, size_t states_bytes, void* ws,
                            size_t ws_bytes, void* stream, int kda) {
     if (gdr_status st0 = check_shape(sh)) return st0;
+    if (sh->total_tokens == 0) {
+        OPT(h0); OPT(ht); OPT(states);
+        if (states && states_bytes < gdr_states_bytes(sh)) return fail(GDR_ERR_WORKSPACE, "states buffer too small%s");
+        cudaStream_t s = (cudaStream_t)stream;
+        if (gdr_status st = empty_front(ws, ws_bytes, sh, s)) return st;
+        if (ht)
+            if (gdr_status st = empty_state_copy(ht, h0, sh, s)) return st;
+        if (states) {
+            k_states_tag<<<1, 32, 0, s>>>(static_cast<int*>(states), states_tag(sh, kda, h0, 0, sh->head_dim));
+            cudaError_t e = cudaGetLastError();
+            if (e != cudaSuccess) return cuda_fail(e, "states header launch");
+        }
+        g_err[0] = 0;
+        return GDR_OK;
+    }
     if (sh->head_dim == 128)
         return fwd_impl128(sh, q, k, v, g, g_raw, A_log, dt_bias, beta, h0, o, ht, states, states_bytes, ws, ws_bytes,
                            stream, kda, 128);
@@ -617,6 +657,20 @@ static gdr_status bwd_impl(const gdr_shape* sh, const void* q, const void* k, co
                            float* dg, void* dg_raw, void* dbeta, float* dh0, float* dA_log,
                            float* ddt_bias, void* stream, int kda) {
     if (gdr_status st0 = check_shape(sh)) return st0;
+    if (sh->total_tokens == 0) {
+        NEED(dh0); OPT(h0); OPT(dht); OPT(states);
+        if (kda) { NEED(A_log); NEED(dt_bias); NEED(dA_log); NEED(ddt_bias); }
+        cudaStream_t s = (cudaStream_t)stream;
+        if (gdr_status st = empty_front(ws, ws_bytes, sh, s)) return st;
+        if (gdr_status st = empty_state_copy(dh0, dht, sh, s)) return st;
+        if (kda) {
+            cudaError_t e = cudaMemsetAsync(dA_log, 0, sizeof(float) * sh->num_heads, s);
+            if (e == cudaSuccess) e = cudaMemsetAsync(ddt_bias, 0, sizeof(float) * sh->num_heads * sh->head_dim, s);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(dA_log/ddt_bias)");
+        }
+        g_err[0] = 0;
+        return GDR_OK;
+    }
     if (sh->head_dim == 128)
         return bwd_impl128(sh, q, k, v, g, g_raw, A_log, dt_bias, beta, h0, dO, dht, states, ws, ws_bytes, dq, dk, dv,
                            dg, dg_raw, dbeta, dh0, dA_log, ddt_bias, stream, kda, 128);

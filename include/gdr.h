@@ -31,6 +31,8 @@
  *    NULL means dense: N sequences of T_total / N tokens each.
  *  * h0 and dht may be NULL (zero).  All outputs are written in full (rows of
  *    every sequence); the library never writes outside the given tensors.
+ *  * T_total = 0 (every sequence empty) is a valid call: the token tensors may then be
+ *    NULL, dh0 receives dht (or zeros), ht receives h0, dA_log and ddt_bias are zero.
  *  * Ownership: the caller allocates every buffer, including the workspace
  *    (size from gdr_workspace_bytes) and the states buffer (gdr_states_bytes).
  *    The library allocates no device memory and keeps no state besides a

@@ -166,3 +166,14 @@ def test_many_short_sequences(mode, dim):
     # states; the per-head sums dA_log / ddt_bias then reach ~2e-3 of their (cancelling) value
     # and are judged against their terms' magnitudes (the strict figure is printed beside)
     _check(x, label="many_%s_d%d" % (mode, dim), conditioned=(mode == "kda"))
+
+
+@pytest.mark.parametrize("mode,dim", [("gdn", 128), ("kda", 64)])
+def test_no_tokens_at_all(mode, dim):
+    # every sequence empty (T_total = 0): nothing to differentiate but h0, which receives dht
+    x = inputs.custom(mode, [0, 0, 0], heads=2, dim=dim, seed=125, with_h0=True, with_dht=True)
+    gpu = H.run_gpu(x)
+    torch.testing.assert_close(gpu["dh0"], x["dht"], rtol=0, atol=0)
+    assert gpu["dq"].numel() == 0 and gpu["dv"].numel() == 0
+    if mode == "kda":
+        assert torch.count_nonzero(gpu["dA_log"]) == 0 and torch.count_nonzero(gpu["ddt_bias"]) == 0
