@@ -67,6 +67,7 @@ def test_workspace_sizes(L):
     (dict(num_seqs=0), 1),
     (dict(total_tokens=-1), 1),
     (dict(total_tokens=100, num_seqs=3), 1),  # dense needs T % N == 0
+    (dict(total_tokens=1 << 34, num_seqs=2), 1),  # beyond the 32-bit tile addressing of one call
 ])
 def test_bad_shapes_rejected(L, mutate, code):
     sh = gdr.make_shape(2, 128, 2, 64)
