@@ -52,21 +52,27 @@ def test_kda_varlen_ragged(dim, gate):
     _check(x, label="kda_%s_ragged_d%d" % (gate, dim), conditioned=True)
 
 
-@pytest.mark.parametrize("mode", ["gdn", "kda"])
-def test_segmented_state_passing_varlen(mode):
+@pytest.mark.parametrize("mode,dim", [("gdn", 128), ("kda", 128), ("gdn", 64), ("kda", 64)])
+def test_segmented_state_passing_varlen(mode, dim):
     # few (sequence, head) pairs and long sequences: the state chains run as time-parallel
     # segments (3 here); the 64-token sequence leaves two of its three segments empty
-    x = inputs.custom(mode, [16000, 64], heads=2, dim=128, seed=109, with_h0=True, with_dht=True)
-    _check(x, label="segments_%s" % mode)
+    # (head_dim 64 runs the same path on zero-padded channels)
+    x = inputs.custom(mode, [16000, 64], heads=2, dim=dim, seed=109, with_h0=True, with_dht=True)
+    # KDA at 64 channels: head 1's dA_log sum cancels to 1/1345 of the sum of its terms'
+    # magnitudes (1/206 .. 1/681 at 128 channels), and with two heads nothing else carries the
+    # tensor's norm, so there dA_log / ddt_bias are judged against the term magnitudes
+    _check(x, label="segments_%s_d%d" % (mode, dim), conditioned=(mode == "kda" and dim == 64))
 
 
-@pytest.mark.parametrize("mode", ["gdn", "kda"])
+@pytest.mark.parametrize("mode", ["gdn", "kda", "kda_sigmoid"])
 @pytest.mark.parametrize("dim", [64, 128])
 def test_grouped_qk_heads_varlen(mode, dim):
     # GQA: 2 q / k heads shared by 6 value heads (3 per group)
+    gate = "sigmoid" if mode == "kda_sigmoid" else "softplus"
+    mode = mode.split("_")[0]
     x = inputs.custom(mode, [1, 63, 200, 130], heads=6, dim=dim, seed=116, with_h0=True, with_dht=True,
-                      k_heads=2)
-    gpu = _check(x, label="gqa_%s_d%d" % (mode, dim), conditioned=(mode == "kda"))
+                      k_heads=2, kda_gate=gate, gate_scale=-2.0)
+    gpu = _check(x, label="gqa_%s_%s_d%d" % (mode, gate, dim), conditioned=(mode == "kda"))
     assert tuple(gpu["dq"].shape) == (x["q"].shape[0], 2, dim)
 
 
