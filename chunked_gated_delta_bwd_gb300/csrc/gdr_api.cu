@@ -194,7 +194,7 @@ static gdr_status check_shape(const gdr_shape* sh) {
 // Segments of the time-parallel state passing (1 = the serial chains), for calls that run
 // both directions or one.  A function of the shape only, sized for one wave of about 150
 // SMs: phase 1 runs 3G - 4 CTAs per (sequence, head) for both directions and 2G - 3 for
-// one, phase 3 runs G per direction; each segment keeps at least 32 chunks, and G <= 8
+// one, phase 3 runs G - 1 per direction; each segment keeps at least 32 chunks, and G <= 8
 // keeps the serial boundary composition short.
 static int seg_count(const gdr_shape* sh, int64_t max_chunks, bool two_dirs) {
     if (sh->head_dim != 128) return 1;
@@ -202,7 +202,7 @@ static int seg_count(const gdr_shape* sh, int64_t max_chunks, bool two_dirs) {
     const int64_t per_seq = max_chunks / sh->num_seqs;
     int G = 1;
     for (int g = 2; g <= 8; ++g) {
-        const int64_t p1 = two_dirs ? 3 * g - 4 : 2 * g - 3, p3 = two_dirs ? 2 * g : g;
+        const int64_t p1 = two_dirs ? 3 * g - 4 : 2 * g - 3, p3 = two_dirs ? 2 * g - 2 : g - 1;
         if (p1 * pairs <= 148 && p3 * pairs <= 148 && per_seq >= 32 * g) G = g;
     }
     return G;

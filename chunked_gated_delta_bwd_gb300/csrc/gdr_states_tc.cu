@@ -71,9 +71,12 @@ struct StateTask {
 //   phase 1  segment phase 1, per (sequence, head): the role-0 chains of segments 0 .. G-2
 //            (segment 0 from h0, the others from zero) and the role-1 chains of segments
 //            1 .. G-1 (segment G-1 from dht, the others from zero), each if its role is
-//            asked, and the transition chains of segments 1 .. G-2
-//   phase 3  segment phase 3, per (sequence, head): every segment of each asked role from
-//            its true start state, saving the per-chunk states (and dh0 / ht)
+//            asked, and the transition chains of segments 1 .. G-2.  Segment 0 of role 0 and
+//            segment G-1 of role 1 start from their true states here, so these two chains
+//            save their per-chunk states in this phase.
+//   phase 3  segment phase 3, per (sequence, head): the other segments of each asked role
+//            (1 .. G-1 of role 0, 0 .. G-2 of role 1) from their true start states, saving
+//            the per-chunk states (and dh0 / ht)
 __host__ __device__ inline int phase1_tasks(int G, int roles) {
     return ((roles & 1) ? G - 1 : 0) + ((roles & 2) ? G - 1 : 0) + G - 2;
 }
@@ -96,17 +99,19 @@ __device__ __forceinline__ StateTask decode_task(const Params& p, int phase, int
             t.role = 0, g = k - n0 - n1 + 1, kind = 1;
         }
     } else {
-        const int per = (roles == 3 ? 2 : 1) * G;
+        const int per = (roles == 3 ? 2 : 1) * (G - 1);
         pair = blockIdx.x / per;
         const int rem = blockIdx.x % per;
-        t.role = roles == 3 ? rem / G : (roles == 1 ? 0 : 1), g = rem % G;
+        t.role = roles == 3 ? rem / (G - 1) : (roles == 1 ? 0 : 1);
+        g = rem % (G - 1) + (t.role == 0 ? 1 : 0);
     }
     t.seq = pair / p.H, t.h = pair % p.H;
     const int cb = seq_chunk_begin(p, t.seq), ce = seq_chunk_begin(p, t.seq + 1);
     const size_t pd = (size_t)pair * G;
     t.input = kind == 0;
     t.identity = kind == 1;
-    t.save = phase != 1;
+    // phase 1 saves along the two chains that start from their true states (h0, dht)
+    t.save = phase != 1 || (kind == 0 && (t.role == 0 ? g == 0 : g == G - 1));
     t.out = nullptr;
     if (phase == 0) {
         t.cb = cb, t.ce = ce;
@@ -482,7 +487,7 @@ cudaError_t launch_states_tc(const Params& p, bool fwd, bool bwd, cudaStream_t s
         if (e != cudaSuccess) return e;
         k_seg_combine<<<dim3(pairs, nroles, CMB_SLICES), 256, cbytes, s>>>(q, roles);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        k_states_tc<<<pairs * nroles * G, NTHREADS, SMEM_BYTES, s>>>(q, 3, roles, m);
+        k_states_tc<<<pairs * nroles * (G - 1), NTHREADS, SMEM_BYTES, s>>>(q, 3, roles, m);
         return cudaGetLastError();
     }
     k_states_tc<<<dim3(pairs, nroles), NTHREADS, SMEM_BYTES, s>>>(q, 0, roles, m);
