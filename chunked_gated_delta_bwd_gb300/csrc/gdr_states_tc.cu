@@ -12,22 +12,24 @@
 //
 // Every product has M = 128 (the value rows), so every tensor-memory lane holds a
 // useful row and the element-wise steps spread over all four SM sub-partitions.
-// Per chunk: consumers write bf16 S^T (the saved state, copied out by a TMA
-// store); the MMA warp issues X^T (or Y^T) = S^T [C x D tile]^T; consumers
-// write bf16 (U - X)^T (or -Y^T); the MMA warp issues the update product (role 1
-// also the state-independent dO^T R terms), which consumers add to the decayed
-// state.  A separate TMA warp streams each chunk's tiles (and its e^{gT} row) two
-// chunks ahead and stores the saved states, so that neither issuing thread waits
-// behind the other's instructions.  All waits are bounded; a wait that runs out
-// sets a flag that turns every later wait and issue into a no-op, so all warps
-// still meet every barrier and the CTA ends with its copies drained and its
-// tensor memory released.
+// Per chunk: consumers write bf16 S^T into tensor memory, where it is the A operand of
+// X^T (or Y^T) = S^T [C x D tile]^T; consumers write bf16 (U - X)^T (or -Y^T) into
+// tensor memory, the A operand of the update product (role 1 also the state-independent
+// dO^T R terms), which consumers add to the decayed state.  Both A operands stay in
+// tensor memory (the thread of value row j owns lane j), so the chain's only shared
+// operands are the chunk tiles.  A chain that saves its states also writes bf16 S^T to
+// shared memory, off the chain's path, for a TMA store.  A separate TMA warp streams each
+// chunk's tiles (and its e^{gT} row) two chunks ahead, refilling a stage when the
+// products that read it have completed (one barrier per stage), and stores the saved
+// states, so that neither issuing thread waits behind the other's instructions.  All
+// waits are bounded; a wait that runs out sets a flag that turns every later wait and
+// issue into a no-op, so all warps still meet every barrier and the CTA ends with its
+// copies drained and its tensor memory released.
 #include "gdr_chunk.cuh"
 #include "gdr_tc.cuh"
 #include "gdr_tma.h"
 
 namespace gdr {
-
 namespace {
 
 constexpr int SD = 128;
@@ -35,15 +37,18 @@ constexpr int TILE = CH * SD * 2;       // one C x D bf16 tile, 16 KB
 constexpr int oEG = 5 * TILE;           // within a stage: e^{gT} row (fp32 [D])
 constexpr int STAGE = 5 * TILE + 1024;  // role 0: W^T, kr^T, U^T ; role 1: kr^T, W^T, R_hi^T, R_lo^T, dO
 // (the per-chunk tiles of the prep kernel are channel-major [D][C]; dO is token-major)
-constexpr int oBS = 2 * STAGE;          // bf16 S^T   [128 rows j][128 cols d]
-constexpr int oBY = oBS + 2 * TILE;     // bf16 (U - X)^T or -Y^T [128 rows j][64 cols t]
-constexpr int oBar = oBY + TILE;        // full[2], y, z mbarriers; tmem slot; abort flag
+constexpr int oBS = 2 * STAGE;          // bf16 S^T [128 rows j][128 cols d]: the saved state's store source
+constexpr int oBar = oBS + 2 * TILE;    // full[2], y, z, empty[2] mbarriers; tmem slot; abort flag
 constexpr int SMEM_BYTES = oBar + 64 + 1024;
 constexpr int NCONS = 256, NTHREADS = NCONS + 64;  // 8 consumer warps, the MMA warp, the TMA warp
 constexpr int MMA_WARP = NCONS / 32, TMA_WARP = MMA_WARP + 1;
-constexpr int N_BS_READY = NTHREADS, N_BY_READY = NCONS + 32, N_BS_FREE = NCONS + 32;  // barrier sizes
-constexpr uint32_t R_Y = 0, R_Z0 = 128, R_Z1 = 256;  // tensor-memory columns
-constexpr int BAR_BS_READY = 1, BAR_BY_READY = 2, BAR_BS_FREE = 3;
+constexpr int N_PAIR = NCONS + 32;  // named barriers between the consumers and one of the other warps
+// tensor-memory columns: Y^T / X^T (fp32), S^T (bf16 pairs, A operand), the update
+// accumulators of the two stages (fp32), (U - X)^T / -Y^T (bf16 pairs, A operand)
+constexpr uint32_t R_Y = 0, R_SA = 64, R_Z0 = 128, R_Z1 = 256, R_BA = 384;
+// named barriers: S^T / the update operand ready (consumers -> MMA warp), the saved
+// state's shared copy written (consumers -> TMA warp) and free again (TMA warp -> consumers)
+constexpr int BAR_BS_READY = 1, BAR_BY_READY = 2, BAR_BS_FREE = 3, BAR_SAVE_READY = 4;
 
 struct StateMaps {
     CUtensorMap W, Kr, Ut, R, Rlo, dO, S0, dS;
@@ -155,9 +160,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_states_tc(const Params p, int p
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + oBar);
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 4);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 4) + 1;
-    const uint32_t full0 = smem_u32(bars), mby = smem_u32(bars + 2), mbz = smem_u32(bars + 3);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 6);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 6) + 1;
+    const uint32_t full0 = smem_u32(bars), mby = smem_u32(bars + 2), mbz = smem_u32(bars + 3),
+                   empty0 = smem_u32(bars + 4);
 
     if (warp == 0) tc::alloc(smem_u32(tslot), 512);
     if (tid == 0) {
@@ -165,6 +171,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_states_tc(const Params p, int p
         tc::mbar_init(full0 + 8, 1);
         tc::mbar_init(mby, 1);
         tc::mbar_init(mbz, 1);
+        tc::mbar_init(empty0, 1);
+        tc::mbar_init(empty0 + 8, 1);
         *abort_flag = 0;
     }
     tc::fence_before();
@@ -221,22 +229,27 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_states_tc(const Params p, int p
             if (n > 1) issue(1);
         }
         __syncwarp();
-        if (n > 0) tc::named_arrive(BAR_BS_FREE, N_BS_FREE);
+        if (task.save && n > 0) tc::named_arrive(BAR_BS_FREE, N_PAIR);
         for (int it = 0; it < n; ++it) {
             const int c = chunk_of(it);
-            tc::named_sync(BAR_BS_READY, N_BS_READY);
-            if (lane == 0) {
-                if (task.save && !failed()) {  // save the state entering this step (S0 of chunk c, or dS_C of chunk c)
-                    tc::tma_store_3d(role == 0 ? &m.S0 : &m.dS, 0, (c * p.H + h) * SD, 0, sb + oBS);
-                    tc::bulk_commit();
+            if (task.save) {  // store the state entering this step (S0 of chunk c, or dS_C of chunk c)
+                tc::named_sync(BAR_SAVE_READY, N_PAIR);
+                if (lane == 0) {
+                    if (!failed()) {
+                        tc::tma_store_3d(role == 0 ? &m.S0 : &m.dS, 0, (c * p.H + h) * SD, 0, sb + oBS);
+                        tc::bulk_commit();
+                    }
+                    tc::bulk_wait_read();  // the shared copy may be rewritten
                 }
-                tc::bulk_wait_read();  // the state tile may be rewritten
+                __syncwarp();
+                if (it + 1 < n) tc::named_arrive(BAR_BS_FREE, N_PAIR);
             }
-            __syncwarp();
-            if (it + 1 < n) tc::named_arrive(BAR_BS_FREE, N_BS_FREE);
-            if (lane == 0) {
-                wait(mbz, it & 1);  // every product reading stage it & 1 has completed
-                if (!failed() && it + 2 < n) issue(it + 2);
+            if (lane == 0 && it + 2 < n) {
+                // every product reading stage it & 1 has completed (its barrier completes once per
+                // use of the stage, and the stage's next use needs the loads issued here, so the
+                // wait cannot miss a phase)
+                wait(empty0 + 8 * (it & 1), (uint32_t)((it >> 1) & 1));
+                if (!failed()) issue(it + 2);
             }
             __syncwarp();
         }
@@ -266,30 +279,33 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_states_tc(const Params p, int p
         for (int it = 0; it < n; ++it) {
             const uint32_t st = sb + (it & 1) * STAGE;
             const uint32_t z = tmem + ((it & 1) ? R_Z1 : R_Z0);
-            tc::named_sync(BAR_BS_READY, N_BS_READY);
+            tc::named_sync(BAR_BS_READY, N_PAIR);
             tc::fence_after();
             if (lane == 0) {
                 wait(full_bar(it), full_par(it));
                 if (!failed()) {
-                    // X^T = S^T W^T (role 0) or Y^T = dS^T kr^T (role 1): B = the stage's first tile
+                    // X^T = S^T W^T (role 0) or Y^T = dS^T kr^T (role 1): A = S^T in tensor
+                    // memory, B = the stage's first tile
                     constexpr uint32_t idy = tc::idesc(128, 64, 0, 1);
 #pragma unroll
                     for (int k = 0; k < SD; k += 16)
-                        tc::mma(tmem + R_Y, tc::kdesc(sb + oBS, SD, 0, k), tc::mdesc(st, SD, 0, k), idy, k > 0);
+                        tc::mma_ts(tmem + R_Y, tmem + R_SA + k / 2, tc::mdesc(st, SD, 0, k), idy, k > 0);
                     tc::commit(mby);
                     if (role == 1) r_part(it, 2, 1);  // + dO^T R_hi
                 }
             }
             __syncwarp();
-            tc::named_sync(BAR_BY_READY, N_BY_READY);
+            tc::named_sync(BAR_BY_READY, N_PAIR);
             tc::fence_after();
             if (lane == 0 && !failed()) {
-                // role 0: Z = (U - X)^T kr ; role 1: Z += (-Y^T) W   (B = the stage's second tile)
+                // role 0: Z = (U - X)^T kr ; role 1: Z += (-Y^T) W   (A in tensor memory, B = the
+                // stage's second tile)
                 constexpr uint32_t idz = tc::idesc(128, 128, 0, 0);
 #pragma unroll
                 for (int k = 0; k < CH; k += 16)
-                    tc::mma(z, tc::kdesc(sb + oBY, SD, 0, k), tc::kdesc(st + TILE, SD, 0, k), idz, role == 1 || k > 0);
+                    tc::mma_ts(z, tmem + R_BA + k / 2, tc::kdesc(st + TILE, SD, 0, k), idz, role == 1 || k > 0);
                 tc::commit(mbz);
+                if (it + 2 < n) tc::commit(empty0 + 8 * (it & 1));  // the stage may be refilled
                 if (role == 1 && it + 1 < n) {  // the next chunk's dO^T R_lo (its consumers read that buffer last step)
                     wait(full_bar(it + 1), full_par(it + 1));
                     if (!failed()) r_part(it + 1, 3, 0);
@@ -309,18 +325,32 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_states_tc(const Params p, int p
         for (int it = 0; it < n; ++it) {
             const unsigned char* stp = smem + (it & 1) * STAGE;
             const uint32_t z = (it & 1) ? R_Z1 : R_Z0;
-            tc::named_sync(BAR_BS_FREE, N_BS_FREE);
+            {
+                // bf16 S^T[j][64 cg ..]: the A operand of this chunk's first product, in tensor memory
+                uint32_t w0[16], w1[16];
 #pragma unroll
-            for (int jc = 0; jc < 8; ++jc) {
-                uint32_t w[4];
+                for (int e = 0; e < 16; ++e) {
+                    w0[e] = pack_bf16(S[2 * e], S[2 * e + 1]);
+                    w1[e] = pack_bf16(S[32 + 2 * e], S[32 + 2 * e + 1]);
+                }
+                tc::st16u_nowait(tl(R_SA + 32 * cg), w0);
+                tc::st16u_nowait(tl(R_SA + 32 * cg + 16), w1);
+                tc::st_wait();
+                tc::fence_before();
+                tc::named_arrive(BAR_BS_READY, N_PAIR);
+                if (task.save) {  // the same values to shared memory, the TMA store's source
+                    tc::named_sync(BAR_BS_FREE, N_PAIR);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) w[e] = pack_bf16(S[8 * jc + 2 * e], S[8 * jc + 2 * e + 1]);
-                *reinterpret_cast<uint4*>(smem + oBS + tc::sw_chunk(j, 8 * cg + jc, SD)) =
-                    make_uint4(w[0], w[1], w[2], w[3]);
+                    for (int jc = 0; jc < 4; ++jc) {
+                        *reinterpret_cast<uint4*>(smem + oBS + tc::sw_chunk(j, 8 * cg + jc, SD)) =
+                            make_uint4(w0[4 * jc], w0[4 * jc + 1], w0[4 * jc + 2], w0[4 * jc + 3]);
+                        *reinterpret_cast<uint4*>(smem + oBS + tc::sw_chunk(j, 8 * cg + 4 + jc, SD)) =
+                            make_uint4(w1[4 * jc], w1[4 * jc + 1], w1[4 * jc + 2], w1[4 * jc + 3]);
+                    }
+                    tc::fence_async_smem();
+                    tc::named_arrive(BAR_SAVE_READY, N_PAIR);
+                }
             }
-            tc::fence_async_smem();
-            tc::fence_before();
-            tc::named_arrive(BAR_BS_READY, N_BS_READY);
 
             // this chunk's decay of the 64 columns (read before the stage can be refilled)
             wait(full_bar(it), full_par(it));
@@ -335,6 +365,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_states_tc(const Params p, int p
             }
             wait(mby, it & 1);
             tc::fence_after();
+            uint32_t wb[16];  // bf16 pairs of (U - X)^T or -Y^T, tokens 32 cg .. 32 cg + 31
 #pragma unroll
             for (int qq = 0; qq < 2; ++qq) {  // tokens 32 cg + 16 qq .. +15
                 float y[16];
@@ -354,12 +385,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_states_tc(const Params p, int p
 #pragma unroll
                     for (int e = 0; e < 8; ++e) w[e] = pack_bf16(-y[2 * e], -y[2 * e + 1]);
                 }
-                *reinterpret_cast<uint4*>(smem + oBY + tc::sw_chunk(j, jc, SD)) = make_uint4(w[0], w[1], w[2], w[3]);
-                *reinterpret_cast<uint4*>(smem + oBY + tc::sw_chunk(j, jc + 1, SD)) = make_uint4(w[4], w[5], w[6], w[7]);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) wb[8 * qq + e] = w[e];
             }
-            tc::fence_async_smem();
+            tc::st16u_nowait(tl(R_BA + 16 * cg), wb);
+            tc::st_wait();
             tc::fence_before();
-            tc::named_arrive(BAR_BY_READY, N_BY_READY);
+            tc::named_arrive(BAR_BY_READY, N_PAIR);
 
             wait(mbz, it & 1);
             tc::fence_after();
@@ -495,3 +527,4 @@ cudaError_t launch_states_tc(const Params& p, bool fwd, bool bwd, cudaStream_t s
 }
 
 }  // namespace gdr
+

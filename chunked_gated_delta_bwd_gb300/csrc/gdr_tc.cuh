@@ -61,6 +61,16 @@ __device__ __forceinline__ void mma(uint32_t tmem_d, uint64_t a, uint64_t b, uin
         "l"(a), "l"(b), "r"(id), "r"(accumulate));
 }
 
+// The same with the A operand in tensor memory (K-major, lane = row of A; a 16-bit A
+// packs two consecutive K elements per 32-bit column, the lower K index in the low half,
+// so one K step of 16 spans 8 columns): the "[a-tmem]" form of tcgen05.mma.
+__device__ __forceinline__ void mma_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t b, uint32_t id, uint32_t accumulate) {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.u32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(tmem_d),
+        "r"(tmem_a), "l"(b), "r"(id), "r"(accumulate));
+}
+
 __device__ __forceinline__ void commit(uint32_t mbar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(mbar));
 }
@@ -138,6 +148,18 @@ __device__ __forceinline__ void st16(uint32_t taddr, const float (&v)[16]) {
         "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15])));
     asm volatile("tcgen05.wait::st.sync.aligned;\n" ::);
 }
+
+// stores 16 / 32 32-bit words (e.g. packed bf16 pairs) into consecutive columns of this
+// thread's lane, without waiting: tcgen05.wait::st (st_wait) orders them before a fence
+// and a barrier that hands the columns to the tensor cores
+__device__ __forceinline__ void st16u_nowait(uint32_t taddr, const uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n" ::"r"(
+            taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+        "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]));
+}
+__device__ __forceinline__ void st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
 
 // ---- TMA (tensor-map bulk copies) -------------------------------------------------
 // The tensor maps are kernel parameters (__grid_constant__); the copies use the
