@@ -102,19 +102,31 @@ __global__ void __launch_bounds__(512, 1) k_main_kda(const Params p, const __gri
     float* sDbP = sDgTp + nDgTp;     // [64] <dY, beta E> per row
     float* sDbA = sDbP + nDbP;       // [4][64] rowsum(dA . A) per column quarter
     float* sRow = sDbA + nDbA;       // [2][4][64] row dots; earlier the [4][128] per-quarter gate minima
-    float* sMisc = sRow + nRow;      // [64]: per-warp partials [0, 16); e^{A_log} at [32]
+    float* sMisc = sRow + nRow;      // [64]: per-warp partials [0, 16); e^{A_log} at [32]; chunk slots at [48, 64)
     float* sTot = sMisc + nMisc;     // [2][64] row dots summed over the lane quarters (q, k)
     uint64_t* mbars = reinterpret_cast<uint64_t*>(sTot + nTot);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(mbars + 3);
     // MMA completion; operand tiles of an item; the raw gate tile for the gate chain rule
     const uint32_t mb = smem_u32(mbars), mload = smem_u32(mbars + 1), mgr = smem_u32(mbars + 2);
 
+    // chunk of the current and of the next item, by item parity (seq, local, t0 lo / hi, len):
+    // the next item's is looked up by one thread at the top of an item, so no thread waits for
+    // the chunk table where the next item's copies are requested
+    int* sCI = reinterpret_cast<int*>(sMisc + 48);
+    auto put_ci = [&](int slot, const ChunkInfo& c) {
+        int* d = sCI + 8 * slot;
+        d[0] = c.seq, d[1] = c.local, d[2] = (int)(c.t0 & 0xffffffff), d[3] = (int)(c.t0 >> 32), d[4] = c.len;
+    };
+    auto get_ci = [&](int slot) {
+        const int* d = sCI + 8 * slot;
+        ChunkInfo c;
+        c.seq = d[0], c.local = d[1], c.t0 = (int64_t)(((uint64_t)(uint32_t)d[3] << 32) | (uint32_t)d[2]), c.len = d[4];
+        return c;
+    };
     // the operand tiles of an item: copy `which` (0 .. 8), or all of them (which < 0).  The
     // copies may be issued by different threads and in any order: the transaction count of
     // the barrier can run ahead of the expectation that copy 0's thread registers.
-    auto issue_loads = [&](int item, int which) {
-        ChunkInfo cj;
-        lookup_chunk(item / p.H, p.N, p.chunk_off, p.cu_seqlens, p.seq_len, cj);
+    auto issue_loads = [&](int item, const ChunkInfo& cj, int which) {
         const int hh = item % p.H, t0 = (int)cj.t0, rcd = item * CH, rdd = item * MD;
         if (which <= 0) tc::mbar_expect_tx(mload, 4 * TILE + 2 * 2 * TILE + CH * CH * 2 + TILE);
         if (which < 0 || which == 0)
@@ -136,7 +148,12 @@ __global__ void __launch_bounds__(512, 1) k_main_kda(const Params p, const __gri
         tc::mbar_init(mb, 1);
         tc::mbar_init(mload, 1);
         tc::mbar_init(mgr, 1);
-        if ((int)blockIdx.x < n_items) issue_loads(blockIdx.x, -1);
+        if ((int)blockIdx.x < n_items) {
+            ChunkInfo c0i;
+            lookup_chunk((int)blockIdx.x / p.H, p.N, p.chunk_off, p.cu_seqlens, p.seq_len, c0i);
+            put_ci(0, c0i);
+            issue_loads(blockIdx.x, c0i, -1);
+        }
     }
     tc::fence_before();
     __syncthreads();
@@ -152,16 +169,14 @@ __global__ void __launch_bounds__(512, 1) k_main_kda(const Params p, const __gri
     // thread waits for them
     unsigned short pb = 0;
     float palog = 0.f, pbias = 0.f;  // the next item's gate parameters (this thread's channel)
-    auto prefetch_small = [&](int item) {
+    auto prefetch_small = [&](int item, const ChunkInfo& cj) {
         const int hh = item % p.H;
         palog = p.A_log[hh];
         pbias = p.dt_bias[hh * MD + L];
         if (tid >= CH) return;
-        ChunkInfo cj;
-        lookup_chunk(item / p.H, p.N, p.chunk_off, p.cu_seqlens, p.seq_len, cj);
         pb = reinterpret_cast<const unsigned short*>(p.beta_logit)[(cj.t0 + min(tid, cj.len - 1)) * p.H + hh];
     };
-    if ((int)blockIdx.x < n_items) prefetch_small(blockIdx.x);
+    if ((int)blockIdx.x < n_items) prefetch_small(blockIdx.x, get_ci(0));
     auto sync_all = [&]() {  // make smem writes visible to the tensor cores and order TMEM use
         tc::fence_async_smem();
         tc::fence_before();
@@ -252,9 +267,13 @@ __global__ void __launch_bounds__(512, 1) k_main_kda(const Params p, const __gri
     };
 
     for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++it) {
-    const int chunk = item / p.H, h = item % p.H;
-    ChunkInfo ci;
-    lookup_chunk(chunk, p.N, p.chunk_off, p.cu_seqlens, p.seq_len, ci);
+    const int h = item % p.H;
+    const ChunkInfo ci = get_ci(it & 1);
+    if (tid == 32 && item + (int)gridDim.x < n_items) {  // the next item's chunk
+        ChunkInfo cn;
+        lookup_chunk((item + (int)gridDim.x) / p.H, p.N, p.chunk_off, p.cu_seqlens, p.seq_len, cn);
+        put_ci((it + 1) & 1, cn);
+    }
     if (tid < CH) sBeta[tid] = tid < ci.len ? sigmoid_f(__bfloat162float(__ushort_as_bfloat16(pb))) : 0.f;
     const float alog = palog, bias = pbias;  // gate parameters, loaded one item ahead
 
@@ -740,10 +759,11 @@ __global__ void __launch_bounds__(512, 1) k_main_kda(const Params p, const __gri
     if (!wait_mma()) return;
     // every large shared tile is dead: the next item's operands may land while this epilogue runs
     if (item + (int)gridDim.x < n_items) {
-        if (lane == 0 && warp < 9) issue_loads(item + gridDim.x, warp);  // one copy per warp
+        const ChunkInfo cn = get_ci((it + 1) & 1);
+        if (lane == 0 && warp < 9) issue_loads(item + gridDim.x, cn, warp);  // one copy per warp
         pending = true;
         pend_par = (uint32_t)((it + 1) & 1);
-        prefetch_small(item + gridDim.x);
+        prefetch_small(item + gridDim.x, cn);
     }
     // the gate-gradient term takes the derived-tile value the products consumed: the fp32
     // value of the hi + lo pair
