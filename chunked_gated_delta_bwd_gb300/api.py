@@ -359,12 +359,13 @@ KERNEL_NAMES = ("chunk_table", "prep", "states", "main", "out", "conv")
 
 
 def profile_begin(max_launches: int):
-    """Time the next ``max_launches`` kernel launches of the library with CUDA events."""
+    """Time the next ``max_launches`` timed sections of the library (one kernel kind of one
+    call) with CUDA events."""
     _check(lib().gdr_profile_begin(int(max_launches)), "gdr_profile_begin")
 
 
 def profile_end():
-    """Returns {kernel: (total_ms, launches)} for the launches recorded since profile_begin."""
+    """Returns {kernel: (total_ms, kernels launched)} for the sections recorded since profile_begin."""
     n = len(KERNEL_NAMES)
     ms = (ctypes.c_double * n)()
     cnt = (ctypes.c_int * n)()

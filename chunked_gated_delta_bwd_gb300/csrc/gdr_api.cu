@@ -295,17 +295,20 @@ static void base_params(Params& p, const gdr_shape* sh, const Layout& L, void* w
 struct Prof {
     bool on = false;
     int max_launches = 0, n = 0;
-    cudaEvent_t* ev = nullptr;  // 2 per launch
+    cudaEvent_t* ev = nullptr;  // 2 per timed section
     int* kind = nullptr;
+    int* kernels = nullptr;     // kernels launched in each timed section
 };
 static Prof g_prof;
 
-// Launches `f` between two recorded events when profiling is on.
+// Launches `f` (which launches `kernels` kernels) between two recorded events when
+// profiling is on.
 template <class F>
-static cudaError_t timed(int kind, cudaStream_t s, F&& f) {
+static cudaError_t timed(int kind, cudaStream_t s, F&& f, int kernels = 1) {
     if (!g_prof.on || g_prof.n >= g_prof.max_launches) return f();
     const int i = g_prof.n++;
     g_prof.kind[i] = kind;
+    g_prof.kernels[i] = kernels;
     cudaEventRecord(g_prof.ev[2 * i], s);
     cudaError_t e = f();
     cudaEventRecord(g_prof.ev[2 * i + 1], s);
@@ -346,7 +349,8 @@ static gdr_status fwd_states_impl128(const gdr_shape* sh, const void* q, const v
     cudaStream_t s = (cudaStream_t)stream;
     gdr_status st = common_front(p, s);
     if (st != GDR_OK) return st;
-    cudaError_t e = timed(GDR_KERNEL_STATES, s, [&] { return launch_states(p, true, false, s); });
+    cudaError_t e = timed(GDR_KERNEL_STATES, s, [&] { return launch_states(p, true, false, s); },
+                          states_kernel_count(p, true, false));
     if (e != cudaSuccess) return cuda_fail(e, "state recurrence launch");
     k_states_tag<<<1, 32, 0, s>>>(static_cast<int*>(states), states_tag(sh, kda, h0, L.max_chunks, orig_dim));
     if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "states header launch");
@@ -379,7 +383,8 @@ static gdr_status fwd_impl128(const gdr_shape* sh, const void* q, const void* k,
     cudaStream_t s = (cudaStream_t)stream;
     gdr_status st = common_front(p, s);
     if (st != GDR_OK) return st;
-    cudaError_t e = timed(GDR_KERNEL_STATES, s, [&] { return launch_states(p, true, false, s); });
+    cudaError_t e = timed(GDR_KERNEL_STATES, s, [&] { return launch_states(p, true, false, s); },
+                          states_kernel_count(p, true, false));
     if (e != cudaSuccess) return cuda_fail(e, "state recurrence launch");
     e = timed(GDR_KERNEL_OUT, s, [&] { return launch_out(p, s); });
     if (e != cudaSuccess) return cuda_fail(e, "output launch");
@@ -438,7 +443,8 @@ static gdr_status bwd_impl128(const gdr_shape* sh, const void* q, const void* k,
     }
     gdr_status st = common_front(p, s);
     if (st != GDR_OK) return st;
-    cudaError_t e = timed(GDR_KERNEL_STATES, s, [&] { return launch_states(p, states == nullptr, true, s); });
+    cudaError_t e = timed(GDR_KERNEL_STATES, s, [&] { return launch_states(p, states == nullptr, true, s); },
+                          states_kernel_count(p, states == nullptr, true));
     if (e != cudaSuccess) return cuda_fail(e, "state recurrence launch");
     e = timed(GDR_KERNEL_MAIN, s, [&] { return launch_main(p, s); });
     if (e != cudaSuccess) return cuda_fail(e, "main backward launch");
@@ -827,10 +833,12 @@ gdr_status gdr_profile_begin(int max_launches) {
         for (int i = 0; i < 2 * g_prof.max_launches; ++i) cudaEventDestroy(g_prof.ev[i]);
         delete[] g_prof.ev;
         delete[] g_prof.kind;
+        delete[] g_prof.kernels;
     }
     g_prof = Prof();
     g_prof.ev = new cudaEvent_t[2 * max_launches];
     g_prof.kind = new int[max_launches];
+    g_prof.kernels = new int[max_launches];
     for (int i = 0; i < 2 * max_launches; ++i) {
         cudaError_t e = cudaEventCreate(&g_prof.ev[i]);
         if (e != cudaSuccess) {
@@ -854,7 +862,7 @@ gdr_status gdr_profile_end(double* total_ms, int* launches) {
         e = cudaEventElapsedTime(&ms, g_prof.ev[2 * i], g_prof.ev[2 * i + 1]);
         if (e != cudaSuccess) return cuda_fail(e, "cudaEventElapsedTime");
         total_ms[g_prof.kind[i]] += ms;
-        launches[g_prof.kind[i]] += 1;
+        launches[g_prof.kind[i]] += g_prof.kernels[i];
     }
     g_prof.n = 0;
     return GDR_OK;

@@ -106,6 +106,7 @@ cudaError_t launch_prep_kda(const Params& p, cudaStream_t s);  // KDA, D = 128, 
 cudaError_t launch_prep_gdn(const Params& p, cudaStream_t s);  // GDN, D = 128, tcgen05 + TMA on the raw q, k tiles
 cudaError_t launch_states(const Params& p, bool fwd, bool bwd, cudaStream_t s);
 cudaError_t launch_states_tc(const Params& p, bool fwd, bool bwd, cudaStream_t s);  // D = 128, tcgen05 + TMA
+int states_kernel_count(const Params& p, bool fwd, bool bwd);  // kernels launch_states_tc launches
 cudaError_t launch_main(const Params& p, cudaStream_t s);
 cudaError_t launch_main_kda(const Params& p, cudaStream_t s);  // KDA, D = 128, tcgen05 + TMA
 cudaError_t launch_main_gdn(const Params& p, cudaStream_t s);  // GDN, D = 128, tcgen05 + TMA on the raw q, k tiles

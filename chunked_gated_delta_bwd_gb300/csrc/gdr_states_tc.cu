@@ -489,6 +489,13 @@ __global__ void __launch_bounds__(256) k_seg_combine(const Params p, int roles) 
     }
 }
 
+// kernels that launch_states_tc launches for these directions (for the launch counts of
+// gdr_profile_end): phase 1, the boundaries and phase 3 with segments, else one
+int states_kernel_count(const Params& p, bool fwd, bool bwd) {
+    if (!fwd && !bwd) return 0;
+    return ((fwd && bwd) ? p.seg_G : p.seg_G1) >= 2 ? 3 : 1;
+}
+
 cudaError_t launch_states_tc(const Params& p, bool fwd, bool bwd, cudaStream_t s) {
     if (!fwd && !bwd) return cudaSuccess;
     StateMaps m;

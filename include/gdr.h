@@ -245,10 +245,12 @@ void gdr_test_stall_next_call(int cta);
 const char* gdr_last_error(void);
 
 /* Instrumentation (not part of the method): per-kernel device timing.
- * gdr_profile_begin(n) makes the next n kernel launches of this library (on
- * any thread, not thread-safe) record a CUDA event pair on their stream;
+ * gdr_profile_begin(n) makes the next n timed sections of this library (one
+ * kernel kind of one call; the state recurrences of a call are one section of
+ * up to three kernels: two chain phases and the segment boundaries) record a
+ * CUDA event pair on their stream (on any thread, not thread-safe);
  * gdr_profile_end waits for them and writes, per kernel kind, the summed
- * milliseconds and the number of launches (arrays of GDR_KERNEL_COUNT). */
+ * milliseconds and the number of kernels launched (arrays of GDR_KERNEL_COUNT). */
 #define GDR_KERNEL_CHUNK_TABLE 0 /* varlen chunk table */
 #define GDR_KERNEL_PREP 1        /* chunk-parallel intra-chunk preparation */
 #define GDR_KERNEL_STATES 2      /* serial state / state-gradient recurrences */

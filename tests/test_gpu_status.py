@@ -120,3 +120,23 @@ def test_backward_captures_into_a_cuda_graph(mode):
             torch.testing.assert_close(v, eager[k], rtol=1e-5, atol=1e-6)
         else:
             assert torch.equal(v, eager[k]), k
+
+
+def test_profile_counts_kernels_not_sections():
+    """The instrumentation counts kernels: a dense backward with time-parallel state
+    passing launches the prep, two chain phases and the boundary kernel, and the main
+    kernel (five), recorded as three timed sections."""
+    from chunked_gated_delta_bwd_gb300 import api
+    x = inputs.make(inputs.Case("prof", "gdn", 1, 4096, 2, 128, seed=3, with_h0=True, with_dht=True))
+    d = H.to_gpu(x)
+    gdr.gdr_bwd(d["q"], d["k"], d["v"], d["g"], d["beta_logit"], d["dO"], h0=d["h0"], dht=d["dht"],
+                num_seqs=1, scale=d["scale"])
+    torch.cuda.synchronize()
+    api.profile_begin(8)
+    gdr.gdr_bwd(d["q"], d["k"], d["v"], d["g"], d["beta_logit"], d["dO"], h0=d["h0"], dht=d["dht"],
+                num_seqs=1, scale=d["scale"])
+    prof = api.profile_end()
+    counts = {k: n for k, (ms, n) in prof.items() if n}
+    # one sequence of 64 chunks over 2 heads: two segments per (sequence, head)
+    assert counts == {"prep": 1, "states": 3, "main": 1}, counts
+    assert all(prof[k][0] > 0 for k in counts)
