@@ -499,7 +499,6 @@ int states_kernel_count(const Params& p, bool fwd, bool bwd) {
 cudaError_t launch_states_tc(const Params& p, bool fwd, bool bwd, cudaStream_t s) {
     if (!fwd && !bwd) return cudaSuccess;
     StateMaps m;
-    const uint64_t rows = (uint64_t)p.max_chunks * p.H * CH;  // C x D tiles
     const uint64_t srows = (uint64_t)p.max_chunks * p.H * SD;  // D x D states
     bool ok = encode_rows_map(&m.W, p.W, srows, CH, SD) && encode_rows_map(&m.Kr, p.Kr, srows, CH, SD) &&
               encode_rows_map(&m.Ut, fwd ? p.U : nullptr, srows, CH, SD) &&
@@ -508,7 +507,6 @@ cudaError_t launch_states_tc(const Params& p, bool fwd, bool bwd, cudaStream_t s
               encode_blocked_tokens_map(&m.dO, bwd ? p.dO : nullptr, (uint64_t)p.T_total, p.H) &&
               encode_blocked_rows_map(&m.S0, fwd ? p.S0 : nullptr, srows, SD) &&
               encode_blocked_rows_map(&m.dS, bwd ? p.dS : nullptr, srows, SD);
-    (void)rows;
     if (!ok) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(k_states_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;

@@ -49,6 +49,11 @@ def test_workspace_sizes(L):
     # 6 when one does; the buffers hold the larger count
     segments = 5 * 16 * 6 * 128 * 128 * 4
     assert tiles + segments <= ws <= tiles + segments + 64 * 256
+    # one sequence of 256 chunks over 2 heads: the most segments (8) in both directions
+    sh8 = gdr.make_shape(1, 16384, 2, 128)
+    tiles8 = 256 * 2 * (5 * 64 * 128 * 2 + 64 * 64 * 2 + 2 * 128 * 4 + 2 * 128 * 128 * 2)
+    segments8 = 5 * 2 * 8 * 128 * 128 * 4
+    assert tiles8 + segments8 <= gdr.workspace_bytes(sh8) <= tiles8 + segments8 + 64 * 256
     # varlen bound: sum ceil(len/64) <= (T + 63 N) / 64
     fake_cu = ctypes.c_void_p(256)
     sh2 = api.GdrShape(3, 130, 2, 64, fake_cu.value, 0.125)

@@ -93,6 +93,14 @@ def test_segmented_forward_varlen(mode):
     _check(x, label="fwd_segments_%s" % mode)
 
 
+@pytest.mark.parametrize("mode", ["gdn", "kda"])
+def test_forward_eight_segments(mode):
+    # one sequence of 256 chunks over 2 heads: the forward's chains run as the most segments
+    # (8), whose boundary composition takes 7 steps
+    x = inputs.custom(mode, [16384], heads=2, dim=128, seed=132, with_h0=True)
+    _check(x, label="fwd_eight_segments_%s" % mode)
+
+
 def test_forward_is_deterministic():
     x = inputs.custom("gdn", [500, 3], heads=4, dim=128, seed=114, with_h0=True)
     a, b = H.run_gpu_fwd(x), H.run_gpu_fwd(x)

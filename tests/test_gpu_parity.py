@@ -64,6 +64,15 @@ def test_segmented_state_passing_varlen(mode, dim):
     _check(x, label="segments_%s_d%d" % (mode, dim), conditioned=(mode == "kda" and dim == 64))
 
 
+@pytest.mark.parametrize("mode", ["gdn", "kda"])
+def test_eight_segments_long_sequence(mode):
+    # one sequence of 256 chunks over 2 heads: the most segments the state passing uses (8
+    # per (sequence, head), 32 chunks each), so phase 1 runs 20 chains per pair and the
+    # boundary composition 7 steps
+    x = inputs.custom(mode, [16384], heads=2, dim=128, seed=131, with_h0=True, with_dht=True)
+    _check(x, label="eight_segments_%s" % mode)
+
+
 @pytest.mark.parametrize("mode", ["gdn", "kda", "kda_sigmoid"])
 @pytest.mark.parametrize("dim", [64, 128])
 def test_grouped_qk_heads_varlen(mode, dim):
