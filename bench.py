@@ -572,10 +572,19 @@ def main_gpu(args):
 
 def run_profile_case(args):
     """Small case for ncu captures: a few GDN or KDA backwards (or, with the _fwd cases,
-    forwards) at B=1 H=16 T=8192 D=128 (inputs ~150 MB, larger than L2); no timing line."""
+    forwards) at B=1 H=16 T=8192 D=128 (inputs ~150 MB, larger than L2), or (conv) conv1d
+    backwards of the benchmark's layer (T=32768, 6144 channels, ~1.2 GB); no timing line."""
     import chunked_gated_delta_bwd_gb300 as gdr
     from chunked_gated_delta_bwd_gb300 import build
     build.build()
+    if args.profile_case == "conv":
+        cc = inputs.conv_case([CASE_G.seq_len], 3 * CASE_G.heads * CASE_G.dim, 4, seed=230)
+        cx = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in cc.items()}
+        for _ in range(args.steps):
+            gdr.conv1d_bwd(cx["x"], cx["weight"], cx["bias"], cx["dy"], silu=True)
+        torch.cuda.synchronize()
+        print("profile case conv: %d calls done" % args.steps)
+        return
     mode = args.profile_case.replace("_fwd", "")
     fwd = args.profile_case.endswith("_fwd")
     case = inputs.Case("profile_" + mode, mode, 1, 8192, 16, 128, seed=5, with_h0=True, with_dht=True)
@@ -621,7 +630,7 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=8192)
     ap.add_argument("--ref-tokens", type=int, default=1024)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile-case", choices=["gdn", "kda", "gdn_fwd", "kda_fwd"], default=None,
+    ap.add_argument("--profile-case", choices=["gdn", "kda", "gdn_fwd", "kda_fwd", "conv"], default=None,
                     help="run a small case (B=1 H=16 T=8192) for ncu captures instead of the benchmark")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
