@@ -15,12 +15,16 @@ reproduces the oracle's gradients (a test checks this).  Sites:
     A, P   the in-chunk matrices as operands                   T    the inverse T
     uF     beta E = beta (V - X)                               uG   u
     du     du (and dY)                                         dP   dP and beta dA
-    chain  the state recurrences run on bf16 W, kr, Y and R (as the state kernel does)
+    chain  the state recurrences run as the state kernel runs them, i.e. all three of
+           chainW  the chunk tiles W, kr (and U) in bf16
+           chainS  the state (or state gradient) as the first product's operand in bf16
+           chainY  the second product's operand (U - X, or Y = kr dS) in bf16
 
 The per-channel (KDA) kernel keeps uF, uG, dP and derG as bf16 pairs, which this replay
 treats as exact ("precise mode"); the scalar-gate kernel rounds every site once.
 ``python -m oracle.precision_sites`` prints the error of dg and of the per-head dA_log sum
-over 16 heads for both models and with each remaining site made exact.
+over 16 heads for both models and with each remaining site made exact.  ``replay`` also returns
+dh0, which only the chain sites touch.
 """
 import numpy as np
 
@@ -38,43 +42,38 @@ def bf16(x):
     return r.astype(np.uint32).view(np.float32).astype(np.float64)
 
 
-def replay(q, k, v, glog, blogit, dO, scale, sites, C=64):
-    """q, k, v, glog, dO: [L, D]; blogit [L] (bf16-representable inputs).  Returns the
-    gradients dq, dk, dv and dglog (the per-channel log-gate gradient) of one sequence
-    with h0 = 0 and no dht, computed with the named sites rounded to bf16."""
+def replay(q, k, v, glog, blogit, dO, scale, sites, C=64, h0=None, dht=None):
+    """q, k, v, glog, dO: [L, D]; blogit [L] (bf16-representable inputs); h0, dht [D, D] or
+    None (zero).  Returns the gradients dq, dk, dv and dglog (the per-channel log-gate
+    gradient) and dh0 of one sequence, computed with the named sites rounded to bf16."""
     R = lambda name, x: bf16(x) if name in sites else x
+    cW, cS, cY = (("chain" in sites) or (n in sites) for n in ("chainW", "chainS", "chainY"))
+    rW = lambda x: bf16(x) if cW else x
+    rS = lambda x: bf16(x) if cS else x
+    rY = lambda x: bf16(x) if cY else x
     L, D = q.shape
     qn, nq = chunk_form._l2n(q)
     kn, nk = chunk_form._l2n(k)
     beta = chunk_form._sigmoid(blogit)
     spans = [(r0, min(r0 + C, L)) for r0 in range(0, L, C)]
-    # forward state chain: the chunk-start states
-    S = np.zeros((D, D))
+    # forward state chain (S_C = e^{gT} S0 + kr^T (U - W S0)): the chunk-start states
+    S = np.zeros((D, D)) if h0 is None else np.array(h0, dtype=np.float64)
     starts = []
     for r0, r1 in spans:
         c = chunk_form._chunk_consts(qn[r0:r1], kn[r0:r1], glog[r0:r1], beta[r0:r1], scale)
         starts.append(S.copy())
-        if "chain" in sites:
-            W, U = bf16(c["W"]), bf16(c["T"] @ (beta[r0:r1, None] * v[r0:r1]))
-            S = np.exp(c["gT"])[:, None] * S + bf16(c["Kr"]).T @ bf16(U - W @ bf16(S))
-        else:
-            u = c["T"] @ (beta[r0:r1, None] * (v[r0:r1] - c["Kd"] @ S))
-            S = np.exp(c["gT"])[:, None] * S + c["Kr"].T @ u
-    # backward state-gradient chain: dS at each chunk's end
-    dS = np.zeros((D, D))
+        U = c["T"] @ (beta[r0:r1, None] * v[r0:r1])
+        S = np.exp(c["gT"])[:, None] * S + rW(c["Kr"]).T @ rY(rW(U) - rW(c["W"]) @ rS(S))
+    # backward state-gradient chain (dS0 = e^{gT} dS_C + R^T dO - W^T (kr dS_C), R = qd - P W
+    # carried exactly, as the kernel's bf16 pair): dS at each chunk's end
+    dS = np.zeros((D, D)) if dht is None else np.array(dht, dtype=np.float64)
     ends = [None] * len(spans)
     for i in range(len(spans) - 1, -1, -1):
         r0, r1 = spans[i]
         c = chunk_form._chunk_consts(qn[r0:r1], kn[r0:r1], glog[r0:r1], beta[r0:r1], scale)
         ends[i] = dS.copy()
-        if "chain" in sites:
-            W, Rm = bf16(c["W"]), c["Qd"] - c["P"] @ c["W"]
-            dS = np.exp(c["gT"])[:, None] * dS + Rm.T @ dO[r0:r1] - W.T @ bf16(bf16(c["Kr"]) @ bf16(dS))
-        else:
-            u = c["T"] @ (beta[r0:r1, None] * (v[r0:r1] - c["Kd"] @ starts[i]))
-            du = c["P"].T @ dO[r0:r1] + c["Kr"] @ dS
-            dV = beta[r0:r1, None] * (c["T"].T @ du)
-            dS = np.exp(c["gT"])[:, None] * dS + c["Qd"].T @ dO[r0:r1] - c["Kd"].T @ dV
+        Rm = c["Qd"] - c["P"] @ c["W"]
+        dS = np.exp(c["gT"])[:, None] * dS + Rm.T @ dO[r0:r1] - rW(c["W"]).T @ rY(rW(c["Kr"]) @ rS(dS))
     dg = np.zeros((L, D))
     dqn = np.zeros((L, D))
     dkn = np.zeros((L, D))
@@ -113,7 +112,7 @@ def replay(q, k, v, glog, blogit, dO, scale, sites, C=64):
         dkn[sl] = eg * (-bt[:, None] * Z) + egp * dKdp + egi * dKip + egr * dKr
     dq = (dqn - qn * (dqn * qn).sum(axis=1, keepdims=True)) / nq
     dk = (dkn - kn * (dkn * kn).sum(axis=1, keepdims=True)) / nk
-    return dict(dq=dq, dk=dk, dv=dv, dglog=dg)
+    return dict(dq=dq, dk=dk, dv=dv, dglog=dg, dh0=dS)
 
 
 def kda_head(seed, L=512, D=128):

@@ -7,6 +7,13 @@ import torch
 # float64 oracle, and the fp32 state / parameter gradients.
 TOL_BF16 = 2e-2
 TOL_FP32 = 1e-3
+# dh0 with no decay at all (every log gate 0, the ungated delta rule): nothing is forgotten,
+# so the bf16 operands of the state-gradient chain -- the chunk tiles W and kr, the state
+# gradient in the first product and Y = kr dS_C in the second -- each leave ~1.1-1.5e-3 on
+# dh0, ~2.2e-3 together, in the float64 rounding-site replay of the chain
+# (tests/test_precision_sites.py pins these figures); the bound is twice that.  With decay
+# (every workload of the task) those contributions fade and dh0 stays within TOL_FP32.
+TOL_DH0_NO_DECAY = 5e-3
 
 
 def rel_l2(a, b):
@@ -145,7 +152,7 @@ def block_errors(g, r, cu):
     return ws, wc, wr
 
 
-def compare(gpu, ref, x, heads=None, conditioned=False):
+def compare(gpu, ref, x, heads=None, conditioned=False, tol=None):
     """Relative L2 errors and their tolerances: per tensor, and (``name@seq``,
     ``name@chunk``, ``name@row``) the worst (sequence, head) block, the worst (64-token
     chunk, head) block and the worst row at a sequence boundary of every token-major
@@ -154,7 +161,8 @@ def compare(gpu, ref, x, heads=None, conditioned=False):
     With ``conditioned`` (edge-case inputs outside the task's workloads, e.g. a
     few hundred tokens), dA_log and ddt_bias -- sums of dg terms with random
     signs -- are judged relative to the sum of the magnitudes of their terms
-    instead of to the (possibly near-cancelling) sum itself."""
+    instead of to the (possibly near-cancelling) sum itself.  ``tol`` maps tensor names to
+    tolerances that replace the defaults (a degenerate case's derived bound)."""
     sel = (lambda t: t) if heads is None else (lambda t: t[:, heads])
     kh = k_heads_of(x, heads)
     selk = (lambda t: t) if kh is None else (lambda t: t[:, kh])
@@ -165,6 +173,8 @@ def compare(gpu, ref, x, heads=None, conditioned=False):
     else:
         pairs.update(dg_raw=("dg_raw", TOL_BF16), dA_log=("dA_log", TOL_FP32),
                      ddt_bias=("ddt_bias", TOL_FP32))
+    for name, t in (tol or {}).items():
+        pairs[name] = (pairs[name][0], t)
     cu = np.asarray(x["cu_seqlens"], dtype=np.int64)
     res = {}
     for name, (rname, tol) in pairs.items():
