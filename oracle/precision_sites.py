@@ -24,7 +24,7 @@ The per-channel (KDA) kernel keeps uF, uG, dP and derG as bf16 pairs, which this
 treats as exact ("precise mode"); the scalar-gate kernel rounds every site once.
 ``python -m oracle.precision_sites`` prints the error of dg and of the per-head dA_log sum
 over 16 heads for both models and with each remaining site made exact.  ``replay`` also returns
-dh0, which only the chain sites touch.
+dh0 and ht, which only the chain sites touch.
 """
 import numpy as np
 
@@ -45,7 +45,8 @@ def bf16(x):
 def replay(q, k, v, glog, blogit, dO, scale, sites, C=64, h0=None, dht=None):
     """q, k, v, glog, dO: [L, D]; blogit [L] (bf16-representable inputs); h0, dht [D, D] or
     None (zero).  Returns the gradients dq, dk, dv and dglog (the per-channel log-gate
-    gradient) and dh0 of one sequence, computed with the named sites rounded to bf16."""
+    gradient), dh0 and the forward's final state ht of one sequence, computed with the named
+    sites rounded to bf16."""
     R = lambda name, x: bf16(x) if name in sites else x
     cW, cS, cY = (("chain" in sites) or (n in sites) for n in ("chainW", "chainS", "chainY"))
     rW = lambda x: bf16(x) if cW else x
@@ -64,6 +65,7 @@ def replay(q, k, v, glog, blogit, dO, scale, sites, C=64, h0=None, dht=None):
         starts.append(S.copy())
         U = c["T"] @ (beta[r0:r1, None] * v[r0:r1])
         S = np.exp(c["gT"])[:, None] * S + rW(c["Kr"]).T @ rY(rW(U) - rW(c["W"]) @ rS(S))
+    ht = S.copy()  # the final state
     # backward state-gradient chain (dS0 = e^{gT} dS_C + R^T dO - W^T (kr dS_C), R = qd - P W
     # carried exactly, as the kernel's bf16 pair): dS at each chunk's end
     dS = np.zeros((D, D)) if dht is None else np.array(dht, dtype=np.float64)
@@ -112,7 +114,7 @@ def replay(q, k, v, glog, blogit, dO, scale, sites, C=64, h0=None, dht=None):
         dkn[sl] = eg * (-bt[:, None] * Z) + egp * dKdp + egi * dKip + egr * dKr
     dq = (dqn - qn * (dqn * qn).sum(axis=1, keepdims=True)) / nq
     dk = (dkn - kn * (dkn * kn).sum(axis=1, keepdims=True)) / nk
-    return dict(dq=dq, dk=dk, dv=dv, dglog=dg, dh0=dS)
+    return dict(dq=dq, dk=dk, dv=dv, dglog=dg, dh0=dS, ht=ht)
 
 
 def kda_head(seed, L=512, D=128):

@@ -268,22 +268,26 @@ def run_oracle_fwd(x, heads=None):
 # gives ~1.6e-3 relative from each and ~2.3e-3 together, whatever the length, because the
 # gates of these workloads forget a chunk's start state within the chunk).  Tolerance: 5e-3.
 TOL_HT = 5e-3
+# ht with no decay at all (every log gate 0): the state is never forgotten, and the chain's
+# bf16 operands leave ~3.9e-3 on ht together in the rounding-site replay of the chain
+# (tests/test_precision_sites.py); the bound is twice that.
+TOL_HT_NO_DECAY = 8e-3
 
 
-def compare_fwd(gpu, ref, heads=None, x=None):
-    """Relative L2 of o (bf16 output: TOL_BF16) and ht (TOL_HT); with ``x``, also the
-    worst (sequence, head), (chunk, head) and boundary-row blocks of o and the worst
-    (sequence, head) of ht."""
+def compare_fwd(gpu, ref, heads=None, x=None, tol_ht=TOL_HT):
+    """Relative L2 of o (bf16 output: TOL_BF16) and ht (``tol_ht``, TOL_HT unless a
+    degenerate case's derived bound is given); with ``x``, also the worst (sequence, head),
+    (chunk, head) and boundary-row blocks of o and the worst (sequence, head) of ht."""
     o = f64(gpu["o"])
     ht = f64(gpu["ht"])
     if heads is not None:
         o, ht = o[:, heads], ht[:, heads]
-    res = {"o": (rel_l2(o, ref["o"]), TOL_BF16), "ht": (rel_l2(ht, ref["ht"]), TOL_HT)}
+    res = {"o": (rel_l2(o, ref["o"]), TOL_BF16), "ht": (rel_l2(ht, ref["ht"]), tol_ht)}
     if x is not None:
         ws, wc, wr = block_errors(o, ref["o"], np.asarray(x["cu_seqlens"], dtype=np.int64))
         bt = TOL_BF16 * BLOCK_TOL_FACTOR
         res["o@seq"], res["o@chunk"], res["o@row"] = (ws, bt), (wc, bt), (wr, bt)
         r = np.asarray(ref["ht"], np.float64)
         res["ht@seq"] = (max(_block_rel(ht[n, i], r[n, i], r[n, i].size, np.linalg.norm(r), r.size)
-                             for n in range(r.shape[0]) for i in range(r.shape[1])), TOL_HT * BLOCK_TOL_FACTOR)
+                             for n in range(r.shape[0]) for i in range(r.shape[1])), tol_ht * BLOCK_TOL_FACTOR)
     return res

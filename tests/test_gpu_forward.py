@@ -19,10 +19,10 @@ def _built():
     build.build()
 
 
-def _check(x, heads=None, label=""):
+def _check(x, heads=None, label="", tol_ht=H.TOL_HT):
     gpu = H.run_gpu_fwd(x)
     ref = H.run_oracle_fwd(x, heads)
-    print(label, H.assert_parity(H.compare_fwd(gpu, ref, heads, x=x), label))
+    print(label, H.assert_parity(H.compare_fwd(gpu, ref, heads, x=x, tol_ht=tol_ht), label))
     return gpu
 
 
@@ -99,6 +99,15 @@ def test_forward_eight_segments(mode):
     # (8), whose boundary composition takes 7 steps
     x = inputs.custom(mode, [16384], heads=2, dim=128, seed=132, with_h0=True)
     _check(x, label="fwd_eight_segments_%s" % mode)
+
+
+def test_forward_without_decay():
+    # degenerate gate: g = 0 everywhere (the ungated delta rule); nothing is forgotten, so
+    # every bf16 operand of the forward chain counts in ht: held to the no-decay bound derived
+    # beside TOL_HT_NO_DECAY (o keeps its usual bound)
+    x = inputs.custom("gdn", [3072, 130], heads=2, dim=128, seed=133, with_h0=True)
+    x["g"] = torch.zeros_like(x["g"])
+    _check(x, label="fwd_no_decay", tol_ht=H.TOL_HT_NO_DECAY)
 
 
 def test_forward_is_deterministic():

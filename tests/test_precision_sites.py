@@ -57,3 +57,17 @@ def test_dh0_error_without_decay():
     together = err({"chain"}, decay=False)
     assert 1.5e-3 < together < H.TOL_DH0_NO_DECAY / 2, together
     assert err({"chain"}, decay=True) < H.TOL_FP32 / 2
+
+
+def test_ht_error_without_decay():
+    """The forward's final state without decay: the chain's bf16 operands leave ~3.9e-3 on
+    ht together (the bound of the no-decay GPU case is twice that), against ~2.3e-3 with the
+    workloads' decay (within TOL_HT)."""
+    def err(decay):
+        q, k, v, glog, b, dO, scale, h0, dht = _scalar_gate_head(12, 1024, 128, decay)
+        exact = ps.replay(q, k, v, glog, b, dO, scale, frozenset(), h0=h0, dht=dht)["ht"]
+        got = ps.replay(q, k, v, glog, b, dO, scale, frozenset({"chain"}), h0=h0, dht=dht)["ht"]
+        return H.rel_l2(got, exact)
+    e = err(False)
+    assert 3e-3 < e <= H.TOL_HT_NO_DECAY / 2, e
+    assert err(True) < H.TOL_HT, "the decayed workloads' bound"
