@@ -193,6 +193,25 @@ def test_gdn_without_decay(dim):
     _check(x, label="no_decay_d%d" % dim, tol={"dh0": H.TOL_DH0_NO_DECAY})
 
 
+def test_strong_decay_near_the_gate_range():
+    # log gates of about -2 per token (GDN) and -1.4 per token and channel (KDA): a chunk's
+    # cumulative gate spans up to ~145 nats, near the 160 that the chunk's mid-range reference
+    # represents (derived-tile factors up to ~e^72; the masked-out entries of the in-chunk
+    # products overflow and are discarded)
+    xg = inputs.custom("gdn", [700, 300], heads=2, dim=128, seed=128, with_h0=True, with_dht=True)
+    gen = torch.Generator().manual_seed(128)
+    xg["g"] = (-torch.nn.functional.softplus(torch.randn(xg["g"].shape, generator=gen) * 0.3 + 2.0)).float()
+    _check(xg, label="strong_decay_gdn")
+    xk = inputs.custom("kda", [700, 300], heads=2, dim=128, seed=129, with_h0=True, with_dht=True)
+    xk["A_log"] = torch.full_like(xk["A_log"], float(torch.log(torch.tensor(1.8))))
+    _check(xk, label="strong_decay_kda", conditioned=True)  # 1000 tokens: short sums
+    import chunked_gated_delta_bwd_gb300 as gdr
+    for x in (xg, xk):  # inside the representable range: no status bit at all, the range flag included
+        ws = H._workspace(H.to_gpu(x), x, None)
+        H.run_gpu(x, workspace=ws)
+        assert gdr.workspace_status(ws) == 0
+
+
 def test_gdn_vanishing_beta():
     # degenerate write strength: beta = sigmoid(-30) ~ 1e-13, so the state only decays (the
     # output is read from h0) and every gradient that beta carries is ~1e-13; relative
