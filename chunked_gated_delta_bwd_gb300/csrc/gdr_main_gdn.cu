@@ -54,7 +54,7 @@ constexpr int oDU = 188416;     // du^T [j][r]
 constexpr int oSmall = 204800;
 constexpr int NCOL = 16;  // rows per thread (16 warps: 4 lane quarters x 4 row quarters)
 // small arrays (floats)
-constexpr int nInvQ = 64, nInvK = 64, nBeta = 64, nFac = 4 * 64, nTab = 6 * 64, nGate = 66, nPad = 62,
+constexpr int nInvQ = 64, nInvK = 64, nBeta = 128, nFac = 4 * 64, nTab = 6 * 64, nGate = 66, nPad = 62,
               nDgTs = 128, nDgTp = 512, nDbP = 64, nPairR = 512, nPairC = 256, nRowG = 256, nRow = 512, nTot = 128;
 constexpr int SMALL_FLOATS = nInvQ + nInvK + nBeta + nFac + nTab + nGate + nPad + nDgTs + nDgTp + nDbP + nPairR +
                              nPairC + nRowG + nRow + nTot;
@@ -94,7 +94,7 @@ __global__ void __launch_bounds__(512, 1) k_main_gdn(const Params p, const __gri
     float* fsm = reinterpret_cast<float*>(smem + oSmall);
     float* sInvQ = fsm;
     float* sInvK = sInvQ + nInvQ;
-    float* sBeta = sInvK + nInvK;
+    float* sBeta = sInvK + nInvK;         // [2][64]: beta, then 1 - beta
     float* sFac = sBeta + nBeta;          // [4][64] e^{gc}, e^{gc-ref}, e^{ref-gc}, e^{gT-gc} (Fac order)
     float* sTab = sFac + nFac;            // [6][64] combined row factors (Tab order)
     float* sGate = sTab + nTab;           // gc[64], ref, gT
@@ -279,7 +279,11 @@ __global__ void __launch_bounds__(512, 1) k_main_gdn(const Params p, const __gri
         put_ci((it + 1) & 1, cn);
     }
     if (tid < 32) gdn_gate_scan(2 * tid < ci.len ? pg0 : 0.f, 2 * tid + 1 < ci.len ? pg1 : 0.f, G, false, p);
-    if (tid < CH) sBeta[tid] = tid < ci.len ? sigmoid_f(__bfloat162float(__ushort_as_bfloat16(pb))) : 0.f;
+    if (tid < CH) {  // beta and 1 - beta = sigmoid(-logit) (exact where beta rounds to 1 in fp32)
+        const float x = __bfloat162float(__ushort_as_bfloat16(pb));
+        sBeta[tid] = tid < ci.len ? sigmoid_f(x) : 0.f;
+        sBeta[CH + tid] = tid < ci.len ? sigmoid_f(-x) : 0.f;
+    }
 
     // wait for the operand tiles; rows past the chunk's end are zeroed before any product
     {
@@ -702,7 +706,7 @@ __global__ void __launch_bounds__(512, 1) k_main_gdn(const Params p, const __gri
     // dbeta (logit space): <dY, beta E> + rowsum(dA . A)
     for (int r = tid; r < ci.len; r += 512) {
         const float dA_A = ((sPairR[CH + r] + sPairR[128 + CH + r]) + sPairR[256 + CH + r]) + sPairR[384 + CH + r];
-        p.dbeta[(ci.t0 + r) * p.H + h] = __float2bfloat16((1.f - sBeta[r]) * (sDbP[r] + dA_A));
+        p.dbeta[(ci.t0 + r) * p.H + h] = __float2bfloat16(sBeta[CH + r] * (sDbP[r] + dA_A));
     }
     // dg: per row, the channel sums of the per-element terms plus the pair terms (row sums
     // minus column sums), suffix sums over the rows, plus the chunk constant dgT

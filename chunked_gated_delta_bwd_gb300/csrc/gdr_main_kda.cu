@@ -53,7 +53,7 @@ constexpr int oW2 = 188416;     // q (token-major) -> ki' [d][r] -> du^T -> qd' 
 constexpr int oSmall = 204800;
 // small arrays (floats)
 constexpr int NCOL = 16;  // rows per thread (16 warps: 4 lane quarters x 4 row quarters)
-constexpr int nInvQ = 64, nInvK = 64, nBeta = 64, nFac = 256, nGate = 128, nRef = 128, nGT = 128,
+constexpr int nInvQ = 64, nInvK = 64, nBeta = 128, nFac = 256, nGate = 128, nRef = 128, nGT = 128,
               nScan = 512, nDgTs = 128, nDgTp = 512, nDbP = 64, nDbA = 256, nRow = 512, nMisc = 64, nTot = 128;
 constexpr int SMALL_FLOATS =
     nInvQ + nInvK + nBeta + nFac + nGate + nRef + nGT + nScan + nDgTs + nDgTp + nDbP + nDbA + nRow + nMisc + nTot;
@@ -91,7 +91,7 @@ __global__ void __launch_bounds__(512, 1) k_main_kda(const Params p, const __gri
     float* fsm = reinterpret_cast<float*>(smem + oSmall);
     float* sInvQ = fsm;
     float* sInvK = sInvQ + nInvQ;
-    float* sBeta = sInvK + nInvK;
+    float* sBeta = sInvK + nInvK;         // [2][64]: beta, then 1 - beta
     float* sFac = sBeta + nBeta;     // [2][128]: e^{ref}, e^{gT-ref} per channel
     float* sGate = sFac + nFac;      // dt_bias[d]
     float* sRef = sGate + nGate;     // ref[d]
@@ -274,7 +274,11 @@ __global__ void __launch_bounds__(512, 1) k_main_kda(const Params p, const __gri
         lookup_chunk((item + (int)gridDim.x) / p.H, p.N, p.chunk_off, p.cu_seqlens, p.seq_len, cn);
         put_ci((it + 1) & 1, cn);
     }
-    if (tid < CH) sBeta[tid] = tid < ci.len ? sigmoid_f(__bfloat162float(__ushort_as_bfloat16(pb))) : 0.f;
+    if (tid < CH) {  // beta and 1 - beta = sigmoid(-logit) (exact where beta rounds to 1 in fp32)
+        const float x = __bfloat162float(__ushort_as_bfloat16(pb));
+        sBeta[tid] = tid < ci.len ? sigmoid_f(x) : 0.f;
+        sBeta[CH + tid] = tid < ci.len ? sigmoid_f(-x) : 0.f;
+    }
     const float alog = palog, bias = pbias;  // gate parameters, loaded one item ahead
 
     // wait for the operand tiles; rows past the chunk's end read as zero
@@ -840,7 +844,7 @@ __global__ void __launch_bounds__(512, 1) k_main_kda(const Params p, const __gri
     // dbeta (logit space)
     for (int r = tid; r < ci.len; r += 512) {
         const float dA_A = ((sDbA[r] + sDbA[CH + r]) + sDbA[2 * CH + r]) + sDbA[3 * CH + r];
-        p.dbeta[(ci.t0 + r) * p.H + h] = __float2bfloat16((1.f - sBeta[r]) * (sDbP[r] + dA_A));
+        p.dbeta[(ci.t0 + r) * p.H + h] = __float2bfloat16(sBeta[CH + r] * (sDbP[r] + dA_A));
     }
     auto dgT_of = [&](int d) -> float {
         return (((sDgTs[d] + sDgTp[d]) + sDgTp[MD + d]) + sDgTp[2 * MD + d]) + sDgTp[3 * MD + d];

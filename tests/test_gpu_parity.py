@@ -212,6 +212,16 @@ def test_strong_decay_near_the_gate_range():
         assert gdr.workspace_status(ws) == 0
 
 
+@pytest.mark.parametrize("mode", ["gdn", "kda"])
+def test_saturated_beta(mode):
+    # write strength saturated: beta logits of +25, so beta rounds to 1 in fp32 and the
+    # logit-space factor 1 - beta (1.4e-11) has to come from sigmoid(-logit); the oracle's
+    # float64 beta (1 - beta) is still good to ~1e-5 there
+    x = inputs.custom(mode, [300, 129], heads=2, dim=128, seed=130, with_h0=True, with_dht=True)
+    x["beta_logit"] = torch.full_like(x["beta_logit"], 25.0)
+    _check(x, label="saturated_beta_%s" % mode, conditioned=(mode == "kda"))  # 429 tokens: short sums
+
+
 def test_gdn_vanishing_beta():
     # degenerate write strength: beta = sigmoid(-30) ~ 1e-13, so the state only decays (the
     # output is read from h0) and every gradient that beta carries is ~1e-13; relative
