@@ -141,9 +141,11 @@ __device__ __forceinline__ float kda_gate_bwd(float gs, float a, float x, float 
         dA = dgl * (-a * sp);
         return dgl * (-a * sg);
     } else {
-        const float s = sigmoid_f(a * x);
-        const float dz = dgl * (kLn2f * gs) * (s * (1.f - s));
-        dA = dz * a * x;
+        // s (1 - s) from one exponential y = e^{-|z|}: s and 1 - s are 1 / (1 + y) and
+        // y / (1 + y) (in the order of the sign of z), neither formed by a cancelling subtraction
+        const float z = a * x, y = __expf(-fabsf(z)), inv = __fdividef(1.f, 1.f + y);
+        const float dz = dgl * (kLn2f * gs) * (y * inv * inv);
+        dA = dz * z;
         return dz * a;
     }
 }

@@ -222,6 +222,19 @@ def test_saturated_beta(mode):
     _check(x, label="saturated_beta_%s" % mode, conditioned=(mode == "kda"))  # 429 tokens: short sums
 
 
+def test_kda_saturated_sigmoid_gate():
+    # the sigmoid-bounded gate in saturation: e^{A_log} = 30 and raw gates near 0.8, so
+    # z = e^{A_log} (g_raw + dt_bias) lies in ~[15, 33] and the gate's slope s (1 - s) in
+    # ~[5e-15, 3e-7], which 1 minus the fp32 sigmoid cannot give; the gate is then about
+    # -1.4 per token and channel (gate_scale -2)
+    x = inputs.custom("kda", [300, 129], heads=2, dim=128, seed=134, with_h0=True, with_dht=True,
+                      kda_gate="sigmoid", gate_scale=-2.0)
+    gen = torch.Generator().manual_seed(134)
+    x["g_raw"] = (0.8 + 0.05 * torch.randn(x["g_raw"].shape, generator=gen)).to(torch.bfloat16)
+    x["A_log"] = torch.full_like(x["A_log"], float(torch.log(torch.tensor(30.0))))
+    _check(x, label="saturated_sigmoid_gate", conditioned=True)  # 429 tokens: short sums
+
+
 def test_gdn_vanishing_beta():
     # degenerate write strength: beta = sigmoid(-30) ~ 1e-13, so the state only decays (the
     # output is read from h0) and every gradient that beta carries is ~1e-13; relative
