@@ -235,6 +235,18 @@ def test_kda_saturated_sigmoid_gate():
     _check(x, label="saturated_sigmoid_gate", conditioned=True)  # 429 tokens: short sums
 
 
+@pytest.mark.parametrize("mode", ["gdn", "kda"])
+def test_zero_query_and_key_rows(mode):
+    # degenerate rows: q = 0 at every 7th token and k = 0 at every 11th, so those rows
+    # normalise to 0 (the L2 norm's eps, 1e-6 inside the square root, keeps them finite), a
+    # zero key writes nothing to the state, and the L2 backward scales those rows' gradients
+    # by 1 / sqrt(eps) = 1000
+    x = inputs.custom(mode, [300, 129], heads=2, dim=128, seed=135, with_h0=True, with_dht=True)
+    x["q"][::7] = 0
+    x["k"][::11] = 0
+    _check(x, label="zero_rows_%s" % mode, conditioned=(mode == "kda"))  # 429 tokens: short sums
+
+
 def test_gdn_vanishing_beta():
     # degenerate write strength: beta = sigmoid(-30) ~ 1e-13, so the state only decays (the
     # output is read from h0) and every gradient that beta carries is ~1e-13; relative
