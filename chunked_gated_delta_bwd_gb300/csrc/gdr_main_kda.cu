@@ -25,8 +25,9 @@
 //
 // KDA runs in precise mode: the operands that carry the
 // per-channel gate gradient (beta E, u, dP and beta dA, and ki', qd', kd' of G10 / G11)
-// are bf16 pairs hi + lo and each of those products is hi*hi + lo*hi + hi*lo, because
-// dA_log and ddt_bias sum dg over every token of a head.
+// are bf16 pairs hi + lo and each of those products is hi*hi + lo*hi + hi*lo, and P is a
+// pair in G5a (dO^T P_hi + dO^T P_lo), because dA_log and ddt_bias sum dg over every token
+// of a head.
 #include "gdr_chunk.cuh"
 #include "gdr_tc.cuh"
 #include "gdr_tma.h"
@@ -50,7 +51,8 @@ constexpr int oW0 = 155648;     // raw gate tile -> kd' [d][r] (G1, A block 0) -
                                 //   -> u^T lo -> ki' [d][r]
 constexpr int oW1 = 172032;     // qd' [d][r] (G1, A block 1) -> u^T [j][r] -> ki' lo
 constexpr int oW2 = 188416;     // q (token-major) -> ki' [d][r] -> du^T -> qd' [d][r]
-constexpr int oSmall = 204800;
+constexpr int oPL = 204800;     // P lo: the residual P - bf16(P), the pair's second half (G5a)
+constexpr int oSmall = oPL + 8192;
 // small arrays (floats)
 constexpr int NCOL = 16;  // rows per thread (16 warps: 4 lane quarters x 4 row quarters)
 constexpr int nInvQ = 64, nInvK = 64, nBeta = 128, nFac = 256, nGate = 128, nRef = 128, nGT = 128,
@@ -58,6 +60,7 @@ constexpr int nInvQ = 64, nInvK = 64, nBeta = 128, nFac = 256, nGate = 128, nRef
 constexpr int SMALL_FLOATS =
     nInvQ + nInvK + nBeta + nFac + nGate + nRef + nGT + nScan + nDgTs + nDgTp + nDbP + nDbA + nRow + nMisc + nTot;
 constexpr int SMEM_BYTES = oSmall + SMALL_FLOATS * 4 + 64 + 1024;  // + mbarriers / tmem slot + alignment
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 // tensor-memory columns
 constexpr uint32_t R_A = 0, R_B = 128, R_C = 192, R_D = 256, R_Q = 320, R_K = 384, R_G = 448;
 
@@ -87,7 +90,8 @@ __global__ void __launch_bounds__(512, 1) k_main_kda(const Params p, const __gri
     const int c0 = NCOL * hc;                 // first of this thread's 16 rows
 
     unsigned char *sK = smem + oK, *sV = smem + oV, *sDOY = smem + oDOY, *sS0 = smem + oS0, *sDS = smem + oDS,
-                  *sA = smem + oA, *sP = smem + oP, *sW0 = smem + oW0, *sW1 = smem + oW1, *sW2 = smem + oW2;
+                  *sA = smem + oA, *sP = smem + oP, *sW0 = smem + oW0, *sW1 = smem + oW1, *sW2 = smem + oW2,
+                  *sPL = smem + oPL;
     float* fsm = reinterpret_cast<float*>(smem + oSmall);
     float* sInvQ = fsm;
     float* sInvK = sInvQ + nInvQ;
@@ -508,7 +512,7 @@ __global__ void __launch_bounds__(512, 1) k_main_kda(const Params p, const __gri
         const float br = sBeta[r];
 #pragma unroll
         for (int jc = 0; jc < NCOL / 8; ++jc) {
-            uint32_t w[4];
+            uint32_t w[4], wl[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int s0 = c0 + jc * 8 + 2 * e;
@@ -521,8 +525,13 @@ __global__ void __launch_bounds__(512, 1) k_main_kda(const Params p, const __gri
                     a1 = s0 + 1 <= r ? a1 : 0.f;
                 }
                 w[e] = pack_bf16(a0, a1);
+                const float2 hf = unpack_bf16(w[e]);
+                wl[e] = pack_bf16(a0 - hf.x, a1 - hf.y);
             }
-            *reinterpret_cast<uint4*>(dst + tc::sw_chunk(r, (c0 >> 3) + jc, 64)) = make_uint4(w[0], w[1], w[2], w[3]);
+            const uint32_t off = tc::sw_chunk(r, (c0 >> 3) + jc, 64);
+            *reinterpret_cast<uint4*>(dst + off) = make_uint4(w[0], w[1], w[2], w[3]);
+            if (!isA)  // P as a bf16 pair
+                *reinterpret_cast<uint4*>(sPL + off) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
         }
     }
     build(sW0, nullptr, false, 1.f, F_KD);  // kd (G1 has completed: kd' is dead)
@@ -576,6 +585,9 @@ __global__ void __launch_bounds__(512, 1) k_main_kda(const Params p, const __gri
 #pragma unroll
         for (int k = 0; k < CH; k += 16)
             tc::mma(tmem + R_A, tc::mdesc(sb + oDOY, 128, 0, k), tc::mdesc(sb + oP, 64, 0, k), id5, 1);
+#pragma unroll
+        for (int k = 0; k < CH; k += 16)  // + dO^T P lo
+            tc::mma(tmem + R_A, tc::mdesc(sb + oDOY, 128, 0, k), tc::mdesc(sb + oPL, 64, 0, k), id5, 1);
         tc::commit(mb);
     }
     if (!wait_mma()) return;

@@ -20,7 +20,7 @@ reproduces the oracle's gradients (a test checks this).  Sites:
            chainS  the state (or state gradient) as the first product's operand in bf16
            chainY  the second product's operand (U - X, or Y = kr dS) in bf16
 
-The per-channel (KDA) kernel keeps uF, uG, dP and derG as bf16 pairs, which this replay
+The per-channel (KDA) kernel keeps uF, uG, dP, derG and P as bf16 pairs, which this replay
 treats as exact ("precise mode"); the scalar-gate kernel rounds every site once.
 ``python -m oracle.precision_sites`` prints the error of dg and of the per-head dA_log sum
 over 16 heads for both models and with each remaining site made exact.  ``replay`` also returns
@@ -31,7 +31,7 @@ import numpy as np
 from . import chunk_form, oracle
 
 ALL_SITES = frozenset({"S", "dS", "derX", "derR", "derA", "derG", "A", "P", "T", "uF", "uG", "du", "dP", "chain"})
-PRECISE_MODE = ALL_SITES - {"uF", "uG", "dP", "derG"}
+PRECISE_MODE = ALL_SITES - {"uF", "uG", "dP", "derG", "P"}
 
 
 def bf16(x):
