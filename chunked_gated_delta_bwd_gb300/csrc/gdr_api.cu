@@ -161,7 +161,7 @@ cudaError_t launch_chunk_table(const Params& p, cudaStream_t s) {
 // ---------------------------------------------------------------------------
 struct Layout {
     int64_t max_chunks;
-    size_t status, chunk_off, W, U, Kr, R, Rlo, T, gT, egT, S0, dS, segL, segLb, segP, segS, dqk, total;
+    size_t status, chunk_off, W, U, Kr, R, Rlo, T, AP, gT, egT, S0, dS, segL, segLb, segP, segS, dqk, total;
     int seg_G, seg_G1;  // segments for calls that run both state directions / one
 };
 
@@ -184,9 +184,10 @@ static gdr_status check_shape(const gdr_shape* sh) {
         return fail(GDR_ERR_INVALID, "gate_scale must be finite and <= 0 (a decaying gate)");
     const int64_t N = sh->num_seqs, T = sh->total_tokens;
     const int64_t mc = sh->cu_seqlens ? (T + (CH - 1) * N) / CH : N * ((T / N + CH - 1) / CH);
-    // (the kernels address per chunk-head tiles by 32-bit row: chunk-heads x 128 rows must fit)
+    // (the kernels address per chunk-head tiles by 32-bit row: chunk-heads x 192 rows, the A / P
+    // block of the KDA backward, must fit)
     if (mc > (int64_t)1 << 30 || N * sh->num_heads * (sh->head_dim / 16) > ((int64_t)1 << 31) - 1 ||
-        mc * sh->num_heads * 128 > ((int64_t)1 << 31) - 1)
+        mc * sh->num_heads * 192 > ((int64_t)1 << 31) - 1)
         return fail(GDR_ERR_INVALID, "problem too large for one call");
     return GDR_OK;
 }
@@ -223,6 +224,7 @@ static Layout layout(const gdr_shape* sh) {
     L.R = o; o = align256(o + mc * H * CH * D * 2);
     L.Rlo = o; o = align256(o + mc * H * CH * D * 2);
     L.T = o; o = align256(o + mc * H * CH * CH * 2);
+    L.AP = o; o = align256(o + mc * H * 3 * CH * CH * 2);  // A, P hi, P lo (the KDA backward's)
     L.gT = o; o = align256(o + mc * H * D * 4);
     L.egT = o; o = align256(o + mc * H * D * 4);
     L.S0 = o; o = align256(o + mc * H * D * D * 2);
@@ -435,6 +437,7 @@ static gdr_status bwd_impl128(const gdr_shape* sh, const void* q, const void* k,
     }
     p.dbeta = (__nv_bfloat16*)dbeta; p.dg = dg; p.dg_raw = (__nv_bfloat16*)dg_raw;
     p.dh0 = dh0; p.dA_log = dA_log; p.ddt_bias = ddt_bias;
+    if (kda) p.APm = reinterpret_cast<__nv_bfloat16*>(static_cast<unsigned char*>(ws) + L.AP);
     cudaStream_t s = (cudaStream_t)stream;
     if (kda) {
         cudaError_t e = cudaMemsetAsync(dA_log, 0, sizeof(float) * p.H, s);

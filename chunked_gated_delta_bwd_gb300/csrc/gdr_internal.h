@@ -35,6 +35,10 @@ struct Params {
     // (D = 128, the layout the tcgen05 state recurrence reads); T [C][C]
     __nv_bfloat16 *W, *U, *Kr, *R, *Rlo, *Tm;
     __nv_bfloat16* Pm;                   // forward only: P = lower(qd ki^T) [C][C] per chunk-head, or nullptr
+    // KDA backward only: the in-chunk matrices of the prep kernel's first product for the main
+    // kernel, [3][C][C] bf16 per chunk-head: A = strict_lower(diag(beta) A_raw), then P as a
+    // bf16 pair (hi, lo); or nullptr
+    __nv_bfloat16* APm;
     float *gT, *egT;                     // [chunk][H][D]: chunk gate total and its exponential
     __nv_bfloat16 *S0, *dS;              // per chunk-head states, value-major [dv][dk]
     // time-parallel state passing (seg_G > 1): per (sequence, head) and segment, fp32 key-major

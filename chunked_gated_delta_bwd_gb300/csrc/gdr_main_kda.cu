@@ -11,7 +11,9 @@
 //
 // With S0 = chunk-start state, dS = state gradient at the chunk end (both value-major
 // [j][d]) and [X; Y] a 128-row operand stacked from two 64-row tiles:
-//   G1  [A_raw; P]   = [kd'; qd'] ki'^T                 G7  Z^T    = S0 dY^T
+//   G1  [A_raw; P]   = [kd'; qd'] ki'^T  (computed by the prep kernel, which needs A for the
+//                      inverse: A = beta A_raw and P (a bf16 pair) arrive by TMA)
+//                                                       G7  Z^T    = S0 dY^T
 //   G2  X^T          = S0^T kd^T                        G8  dkr^T  = dS u^T
 //   G3  dqd^T        = S0 dO^T                          G9  [dP; dA] = [dO; dY] u^T
 //   G4  u^T          = (beta E)^T T^T                   G10 [dqd', dkd']^T = ki'^T [dP; beta dA]^T
@@ -45,13 +47,12 @@ constexpr int oDOY = 32768;     // [dO; dY] token-major, 128 rows
 constexpr int oS0 = 65536;      // S0 [j][d]          -> kd' [d][r] (+ lo at +16 KB)
 constexpr int oDS = 98304;      // dS [j][d]          -> [dP; beta dA] [m][s] (+ lo at +16 KB)
 constexpr int oT = 131072;      // T  [r][s]
-constexpr int oA = 139264;      // beta A_raw, strict lower [r][s]   -> raw gate tile, with P's space
-constexpr int oP = 147456;      // P, lower [r][s]
-constexpr int oW0 = 155648;     // raw gate tile -> kd' [d][r] (G1, A block 0) -> kd [d][r]
-                                //   -> u^T lo -> ki' [d][r]
-constexpr int oW1 = 172032;     // qd' [d][r] (G1, A block 1) -> u^T [j][r] -> ki' lo
-constexpr int oW2 = 188416;     // q (token-major) -> ki' [d][r] -> du^T -> qd' [d][r]
-constexpr int oPL = 204800;     // P lo: the residual P - bf16(P), the pair's second half (G5a)
+constexpr int oA = 139264;      // A = beta A_raw, strict lower [r][s] (prep) -> raw gate tile, with P's space
+constexpr int oP = 147456;      // P, lower [r][s] (prep)
+constexpr int oW0 = 155648;     // raw gate tile -> kd [d][r] -> u^T lo -> ki' [d][r]
+constexpr int oW1 = 172032;     // u^T [j][r] -> ki' lo -> dq (staged)
+constexpr int oW2 = 188416;     // q (token-major) -> du^T -> dv (staged) -> qd' [d][r]
+constexpr int oPL = 204800;     // P lo: the residual P - bf16(P), the pair's second half (prep; G5a)
 constexpr int oSmall = oPL + 8192;
 // small arrays (floats)
 constexpr int NCOL = 16;  // rows per thread (16 warps: 4 lane quarters x 4 row quarters)
@@ -65,7 +66,7 @@ static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 constexpr uint32_t R_A = 0, R_B = 128, R_C = 192, R_D = 256, R_Q = 320, R_K = 384, R_G = 448;
 
 struct MainMaps {
-    CUtensorMap q, k, v, dO, S0, dS, T, graw, dq, dk, dv, dgr;
+    CUtensorMap q, k, v, dO, S0, dS, T, ap, graw, dq, dk, dv, dgr;
 };
 constexpr int STORE_TID = 96;  // the thread that issues the TMA stores of dq, dk, dv and dg_raw
 
@@ -90,8 +91,7 @@ __global__ void __launch_bounds__(512, 1) k_main_kda(const Params p, const __gri
     const int c0 = NCOL * hc;                 // first of this thread's 16 rows
 
     unsigned char *sK = smem + oK, *sV = smem + oV, *sDOY = smem + oDOY, *sS0 = smem + oS0, *sDS = smem + oDS,
-                  *sA = smem + oA, *sP = smem + oP, *sW0 = smem + oW0, *sW1 = smem + oW1, *sW2 = smem + oW2,
-                  *sPL = smem + oPL;
+                  *sA = smem + oA, *sW0 = smem + oW0, *sW1 = smem + oW1, *sW2 = smem + oW2;
     float* fsm = reinterpret_cast<float*>(smem + oSmall);
     float* sInvQ = fsm;
     float* sInvK = sInvQ + nInvQ;
@@ -109,9 +109,11 @@ __global__ void __launch_bounds__(512, 1) k_main_kda(const Params p, const __gri
     float* sMisc = sRow + nRow;      // [64]: per-warp partials [0, 16); e^{A_log} at [32]; chunk slots at [48, 64)
     float* sTot = sMisc + nMisc;     // [2][64] row dots summed over the lane quarters (q, k)
     uint64_t* mbars = reinterpret_cast<uint64_t*>(sTot + nTot);
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbars + 3);
-    // MMA completion; operand tiles of an item; the raw gate tile for the gate chain rule
-    const uint32_t mb = smem_u32(mbars), mload = smem_u32(mbars + 1), mgr = smem_u32(mbars + 2);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbars + 4);
+    // MMA completion; operand tiles of an item; the raw gate tile for the gate chain rule; the
+    // item's A and P pair from the prep kernel
+    const uint32_t mb = smem_u32(mbars), mload = smem_u32(mbars + 1), mgr = smem_u32(mbars + 2),
+                   mAP = smem_u32(mbars + 3);
 
     // chunk of the current and of the next item, by item parity (seq, local, t0 lo / hi, len):
     // the next item's is looked up by one thread at the top of an item, so no thread waits for
@@ -152,6 +154,7 @@ __global__ void __launch_bounds__(512, 1) k_main_kda(const Params p, const __gri
         tc::mbar_init(mb, 1);
         tc::mbar_init(mload, 1);
         tc::mbar_init(mgr, 1);
+        tc::mbar_init(mAP, 1);
         if ((int)blockIdx.x < n_items) {
             ChunkInfo c0i;
             lookup_chunk((int)blockIdx.x / p.H, p.N, p.chunk_off, p.cu_seqlens, p.seq_len, c0i);
@@ -168,6 +171,7 @@ __global__ void __launch_bounds__(512, 1) k_main_kda(const Params p, const __gri
     bool pending = (int)blockIdx.x < n_items;  // a load batch is in flight
     uint32_t pend_par = 0;                     // ... on this phase parity of the load barrier
     bool pending_g = false;                    // a raw gate tile is in flight
+    bool pending_ap = false;                   // the item's A and P pair are in flight
     // the next item's beta logit (thread r < 64, a raw value, row clamped into the chunk) and
     // gate parameters, loaded one item ahead and first read at the next item's top, so no
     // thread waits for them
@@ -195,6 +199,7 @@ __global__ void __launch_bounds__(512, 1) k_main_kda(const Params p, const __gri
             atomicOr(p.status, ST_MMA_TIMEOUT);
             if (pending) tc::mbar_wait(mload, pend_par);  // bounded drain of the loads in flight
             if (pending_g) tc::mbar_wait(mgr, (uint32_t)(it & 1));
+            if (pending_ap) tc::mbar_wait(mAP, (uint32_t)(it & 1));
         }
         if (tid == STORE_TID) tc::bulk_wait_all();
         tc::fence_before();
@@ -323,6 +328,17 @@ __global__ void __launch_bounds__(512, 1) k_main_kda(const Params p, const __gri
     sRow[hc * MD + L] = lmx;
     sDgTp[hc * MD + L] = lmn;
     __syncthreads();
+    if (tid == STORE_TID) {
+        // the item's A and the P pair (written by the prep kernel) into the A, P and P-lo
+        // tiles: dead since the last item's dg_raw store read them (A, P) and its G5a (P lo);
+        // first needed by G5a, several thousand cycles from here
+        tc::bulk_wait_read();
+        tc::mbar_expect_tx(mAP, 3 * CH * CH * 2);
+        tc::tma_load_2d(sb + oA, &m.ap, 0, 3 * item * CH, mAP);
+        tc::tma_load_2d(sb + oP, &m.ap, 0, (3 * item + 1) * CH, mAP);
+        tc::tma_load_2d(sb + oPL, &m.ap, 0, (3 * item + 2) * CH, mAP);
+    }
+    pending_ap = true;
     float pre = 0.f, tot = 0.f, M = -3.0e38f, N = 3.0e38f;
 #pragma unroll
     for (int h2 = 0; h2 < 4; ++h2) {
@@ -470,6 +486,22 @@ __global__ void __launch_bounds__(512, 1) k_main_kda(const Params p, const __gri
         }
     };
 
+    // kd (e^{ref} e) and kr (e^{gT-ref} / e) of k at once, each value exactly as build() forms it
+    auto build_kr_kd = [&](unsigned char* kr, unsigned char* kd) {
+        float e[16], x[16], inv[16], v[16];
+        tc::ld16(tl(R_G + c0), e);
+        load_x(false, x, inv);
+        const float eRef = sFac[L], eGTref = sFac[MD + L];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) x[i] = x[i] * derived_m(inv[i], 1.f, 1.f);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = x[i] * (e[i] * eRef);
+        store_cm(kd, v);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = x[i] * __fdividef(eGTref, e[i]);
+        store_cm(kr, v);
+    };
+
     // per-thread accumulators (channel L, rows c0 .. c0+15)
     float dQn[NCOL], dKn[NCOL], dGc[NCOL], v[NCOL];
 #pragma unroll
@@ -480,69 +512,24 @@ __global__ void __launch_bounds__(512, 1) k_main_kda(const Params p, const __gri
         return (uint32_t)((L >> 6) * rows * 128 + (c0 + i) * 128 + ((lch ^ (i & 7)) << 4) + lsub);
     };
 
-    // ---- G1: [A_raw; P] = [kd'; qd'] ki'^T ; then G3: dqd^T = S0 dO^T, G5b: dS^T kr^T --------
-    // (G3 and G5b need no G1 result: they run while the G1 epilogue does)
-    // kd' -> W0, ki' -> W2 (the q tile is dead), kr -> K (the k tile is dead: q and k are
-    // staged in tensor memory), qd' -> W1
-    build_k(sW0, nullptr, sW2, nullptr, sK);
-    build(sW1, nullptr, true, p.scale, F_KDP);
+    // ---- G2: X^T = S0^T kd^T, G3: dqd^T = S0 dO^T, G5b: du^T = dS^T kr^T (+ dO^T P later) ----
+    // ([A_raw; P] of G1 come from the prep kernel, which computes them for the inverse)
+    // kr -> K (the k tile is dead: q and k are staged in tensor memory), kd -> W0 (the raw
+    // gate tile is dead after the scan)
+    build_kr_kd(sK, sW0);
     sync_all();
     if (tid == 0) {
-        constexpr uint32_t id = tc::idesc(128, 64, 1, 1);
-#pragma unroll
-        for (int k = 0; k < MD; k += 16)
-            tc::mma(tmem + R_B, tc::mdesc(sb + oW0, 128, 0, k), tc::mdesc(sb + oW2, 128, 0, k), id, k > 0);
-        tc::commit(mb);
-        constexpr uint32_t id3 = tc::idesc(128, 64, 1, 0), id5 = tc::idesc(128, 64, 0, 1);
-#pragma unroll
-        for (int k = 0; k < MD; k += 16)
-            tc::mma(tmem + R_D, tc::mdesc(sb + oS0, 128, 0, k), tc::kdesc(sb + oDOY, 128, 0, k), id3, k > 0);
-        // second half of G5 (independent of beta E): du^T = dS^T kr^T (+ dO^T P later); the
-        // next commit (after G2) covers these two groups
-#pragma unroll
-        for (int k = 0; k < MD; k += 16)
-            tc::mma(tmem + R_A, tc::kdesc(sb + oDS, 128, 0, k), tc::mdesc(sb + oK, 128, 0, k), id5, k > 0);
-    }
-    if (!wait_mma()) return;
-    tc::ld16(tl(R_B + c0), v);
-    {
-        const bool isA = L < 64;
-        const int r = isA ? L : L - 64;
-        unsigned char* dst = isA ? sA : sP;
-        const float br = sBeta[r];
-#pragma unroll
-        for (int jc = 0; jc < NCOL / 8; ++jc) {
-            uint32_t w[4], wl[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int s0 = c0 + jc * 8 + 2 * e;
-                float a0 = v[jc * 8 + 2 * e], a1 = v[jc * 8 + 2 * e + 1];
-                if (isA) {
-                    a0 = s0 < r ? br * a0 : 0.f;
-                    a1 = s0 + 1 < r ? br * a1 : 0.f;
-                } else {
-                    a0 = s0 <= r ? a0 : 0.f;
-                    a1 = s0 + 1 <= r ? a1 : 0.f;
-                }
-                w[e] = pack_bf16(a0, a1);
-                const float2 hf = unpack_bf16(w[e]);
-                wl[e] = pack_bf16(a0 - hf.x, a1 - hf.y);
-            }
-            const uint32_t off = tc::sw_chunk(r, (c0 >> 3) + jc, 64);
-            *reinterpret_cast<uint4*>(dst + off) = make_uint4(w[0], w[1], w[2], w[3]);
-            if (!isA)  // P as a bf16 pair
-                *reinterpret_cast<uint4*>(sPL + off) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
-        }
-    }
-    build(sW0, nullptr, false, 1.f, F_KD);  // kd (G1 has completed: kd' is dead)
-    sync_all();
-
-    // ---- G2: X^T = S0^T kd^T (its commit also covers G3 and G5b) ---------------------------
-    if (tid == 0) {
-        constexpr uint32_t id2 = tc::idesc(128, 64, 0, 1);
+        constexpr uint32_t id2 = tc::idesc(128, 64, 0, 1), id3 = tc::idesc(128, 64, 1, 0),
+                           id5 = tc::idesc(128, 64, 0, 1);
 #pragma unroll
         for (int k = 0; k < MD; k += 16)
             tc::mma(tmem + R_C, tc::kdesc(sb + oS0, 128, 0, k), tc::mdesc(sb + oW0, 128, 0, k), id2, k > 0);
+#pragma unroll
+        for (int k = 0; k < MD; k += 16)
+            tc::mma(tmem + R_D, tc::mdesc(sb + oS0, 128, 0, k), tc::kdesc(sb + oDOY, 128, 0, k), id3, k > 0);
+#pragma unroll
+        for (int k = 0; k < MD; k += 16)
+            tc::mma(tmem + R_A, tc::kdesc(sb + oDS, 128, 0, k), tc::mdesc(sb + oK, 128, 0, k), id5, k > 0);
         tc::commit(mb);
     }
     if (!wait_mma()) return;
@@ -573,6 +560,11 @@ __global__ void __launch_bounds__(512, 1) k_main_kda(const Params p, const __gri
     }
     sync_all();
 
+    {  // the item's A and P pair have landed (G5a reads P; the dP / dA epilogue reads A)
+        const bool ok = tc::mbar_wait(mAP, (uint32_t)(it & 1));
+        if (__syncthreads_or(!ok)) return bail();
+        pending_ap = false;
+    }
     // ---- G4: u^T = (beta E)^T T^T ; G5a: du^T += dO^T P ------------------------------
     if (tid == 0) {
         constexpr uint32_t id4 = tc::idesc(128, 64, 1, 0), id5 = tc::idesc(128, 64, 1, 1);
@@ -938,7 +930,7 @@ static cudaError_t launch_main_kda_t(const Params& p, cudaStream_t s) {
     bool ok = encode_blocked_tokens_map(&m.q, p.q, T, p.Hk) && encode_blocked_tokens_map(&m.k, p.k, T, p.Hk) &&
               encode_blocked_tokens_map(&m.v, p.v, T, p.H) && encode_tokens_map(&m.dO, p.dO, T, p.H, MD) &&
               encode_blocked_rows_map(&m.S0, p.S0, rows_dd, MD) && encode_blocked_rows_map(&m.dS, p.dS, rows_dd, MD) &&
-              encode_rows_map(&m.T, p.Tm, rows_cc, CH, CH) &&
+              encode_rows_map(&m.T, p.Tm, rows_cc, CH, CH) && encode_rows_map(&m.ap, p.APm, 3 * rows_cc, CH, CH) &&
               encode_blocked_tokens_map(&m.graw, p.g_raw, T, p.H) &&
               encode_blocked_tokens_map(&m.dq, p.dq, T, p.H) && encode_tokens_map(&m.dk, p.dk, T, p.H, MD) &&
               encode_blocked_tokens_map(&m.dv, p.dv, T, p.H) &&

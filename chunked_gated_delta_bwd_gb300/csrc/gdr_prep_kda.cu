@@ -6,6 +6,8 @@
 // scalar gate has its own kernel, gdr_prep_gdn.cu):
 //
 //   [A_raw; P] = [kd'; qd'] ki'^T       A = strict_lower(diag(beta) A_raw) (fp32), P = lower(.)
+//                                        (a KDA backward also gets A (bf16) and P (a bf16
+//                                        pair) for its main kernel, which needs both)
 //   T   = (I + A)^-1                     (blocked inverse to fp32 accuracy, gdr_invert.cuh)
 //   W^T = (beta kd)^T T^T                U^T = (beta V)^T T^T
 //   R^T = qd^T - W^T P^T                 (a bf16 pair R_hi + R_lo)
@@ -406,21 +408,37 @@ __global__ void __launch_bounds__(512, 1) k_prep_kda(const Params p, const __gri
     {
         float v[16];
         tc::ld16(tl(R_G1 + c0), v);
+        // (the KDA backward also takes A and P for its main kernel, which then needs no first
+        // product of its own: [r][s] bf16 rows written straight from these registers, A, then
+        // P as a bf16 pair)
+        __nv_bfloat16* ap = p.APm ? p.APm + 3 * tile_cc : nullptr;
         if (L < 64) {  // A = strict_lower(beta A_raw), fp32 for the inversion
             const int r = L;
             const float br = sBeta[r];
+            float a[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) a[i] = c0 + i < r ? br * v[i] : 0.f;
 #pragma unroll
             for (int i = 0; i < 16; i += 4)
-                *reinterpret_cast<float4*>(sA + r * LDF + c0 + i) =
-                    make_float4(c0 + i < r ? br * v[i] : 0.f, c0 + i + 1 < r ? br * v[i + 1] : 0.f,
-                                c0 + i + 2 < r ? br * v[i + 2] : 0.f, c0 + i + 3 < r ? br * v[i + 3] : 0.f);
+                *reinterpret_cast<float4*>(sA + r * LDF + c0 + i) = make_float4(a[i], a[i + 1], a[i + 2], a[i + 3]);
+            if (ap) {
+                uint32_t w[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) w[e] = pack_bf16(a[2 * e], a[2 * e + 1]);
+                uint4* g = reinterpret_cast<uint4*>(ap + r * CH + c0);
+                g[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                g[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            }
         } else {  // P = lower(qd' ki'^T), bf16 [r][s]
             const int r = L - 64;
             uint32_t w[8];
+            float pv[16];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const int s0 = c0 + 2 * e;
-                w[e] = pack_bf16(s0 <= r ? v[2 * e] : 0.f, s0 + 1 <= r ? v[2 * e + 1] : 0.f);
+                pv[2 * e] = s0 <= r ? v[2 * e] : 0.f;
+                pv[2 * e + 1] = s0 + 1 <= r ? v[2 * e + 1] : 0.f;
+                w[e] = pack_bf16(pv[2 * e], pv[2 * e + 1]);
             }
             *reinterpret_cast<uint4*>(sP + tc::sw_chunk(r, c0 >> 3, 64)) = make_uint4(w[0], w[1], w[2], w[3]);
             *reinterpret_cast<uint4*>(sP + tc::sw_chunk(r, (c0 >> 3) + 1, 64)) = make_uint4(w[4], w[5], w[6], w[7]);
@@ -428,6 +446,20 @@ __global__ void __launch_bounds__(512, 1) k_prep_kda(const Params p, const __gri
                 uint4* g = reinterpret_cast<uint4*>(p.Pm + tile_cc + r * CH + c0);
                 g[0] = make_uint4(w[0], w[1], w[2], w[3]);
                 g[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            }
+            if (ap) {  // P hi, then its residual P - hi
+                uint32_t wl[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float2 hf = unpack_bf16(w[e]);
+                    wl[e] = pack_bf16(pv[2 * e] - hf.x, pv[2 * e + 1] - hf.y);
+                }
+                uint4* g = reinterpret_cast<uint4*>(ap + CH * CH + r * CH + c0);
+                g[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                g[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                g = reinterpret_cast<uint4*>(ap + 2 * CH * CH + r * CH + c0);
+                g[0] = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+                g[1] = make_uint4(wl[4], wl[5], wl[6], wl[7]);
             }
         }
     }

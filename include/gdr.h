@@ -61,7 +61,9 @@ extern "C" {
 
 typedef enum {
     GDR_OK = 0,
-    GDR_ERR_INVALID = 1,      /* null / misaligned pointer, bad size or shape */
+    GDR_ERR_INVALID = 1,      /* null / misaligned pointer, bad size or shape (also a problem
+                                 whose per-chunk tiles exceed 32-bit row addressing: chunks x
+                                 heads x 192 rows must stay below 2^31) */
     GDR_ERR_UNSUPPORTED = 2,  /* head_dim not in {64, 128} */
     GDR_ERR_WORKSPACE = 3,    /* workspace or states buffer too small */
     GDR_ERR_CUDA = 4          /* a CUDA runtime call or kernel launch failed */

@@ -44,14 +44,15 @@ def test_workspace_sizes(L):
     HDR = 256  # GDR_STATES_HEADER_BYTES
     assert gdr.states_bytes(sh) == HDR + chunks * 16 * 128 * 128 * 2
     ws = gdr.workspace_bytes(sh)
-    tiles = chunks * 16 * (5 * 64 * 128 * 2 + 64 * 64 * 2 + 2 * 128 * 4 + 2 * 128 * 128 * 2)
+    # per chunk-head: W, U, Kr, R_hi, R_lo; T; A, P hi, P lo (the KDA backward's); gT, e^{gT}; S0, dS
+    tiles = chunks * 16 * (5 * 64 * 128 * 2 + 64 * 64 * 2 + 3 * 64 * 64 * 2 + 2 * 128 * 4 + 2 * 128 * 128 * 2)
     # time-parallel state passing: 4 segments per (sequence, head) when both directions run,
     # 6 when one does; the buffers hold the larger count
     segments = 5 * 16 * 6 * 128 * 128 * 4
     assert tiles + segments <= ws <= tiles + segments + 64 * 256
     # one sequence of 256 chunks over 2 heads: the most segments (8) in both directions
     sh8 = gdr.make_shape(1, 16384, 2, 128)
-    tiles8 = 256 * 2 * (5 * 64 * 128 * 2 + 64 * 64 * 2 + 2 * 128 * 4 + 2 * 128 * 128 * 2)
+    tiles8 = 256 * 2 * (5 * 64 * 128 * 2 + 64 * 64 * 2 + 3 * 64 * 64 * 2 + 2 * 128 * 4 + 2 * 128 * 128 * 2)
     segments8 = 5 * 2 * 8 * 128 * 128 * 4
     assert tiles8 + segments8 <= gdr.workspace_bytes(sh8) <= tiles8 + segments8 + 64 * 256
     # varlen bound: sum ceil(len/64) <= (T + 63 N) / 64
