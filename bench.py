@@ -46,9 +46,10 @@ BWD_FLOP_PER_TH = 14 * D_ * D_ + 22 * C_ * D_
 BWD_BYTES_PER_TH = {"gdn": 4 * 2 * D_ + 4 + 2 + 2 * D_ * D_ // C_ + 3 * 2 * D_ + 4 + 2,
                     "kda": 4 * 2 * D_ + 2 * D_ + 2 + 2 * D_ * D_ // C_ + 3 * 2 * D_ + 2 * D_ + 2}
 assert BWD_FLOP_PER_TH == 409600 and BWD_BYTES_PER_TH == {"gdn": 2316, "kda": 2820}
-# What this design's main kernel moves per token-head besides (the dS_C and T tiles it reads
-# from the state and prep kernels' output), for the design-byte figure reported beside.
-MAIN_DESIGN_EXTRA_PER_TH = 2 * D_ * D_ // C_ + 2 * C_
+# What this design's main kernel moves per token-head besides, for the design-byte figure
+# reported beside: the dS_C and T tiles it reads from the state and prep kernels' output, and
+# (KDA) A and the P pair from the prep kernel.
+MAIN_DESIGN_EXTRA_PER_TH = {"gdn": 2 * D_ * D_ // C_ + 2 * C_, "kda": 2 * D_ * D_ // C_ + 2 * C_ + 3 * 2 * C_}
 # Forward output kernel (o = R S0 + P U per chunk) per token-head: reads S0 (2 D^2 / C), R^T and
 # U^T (2 D each), P (2 C); writes o (2 D).  Flops: 2 (D^2 + C D).
 OUT_BYTES_PER_TH = 2 * D_ * D_ // C_ + 2 * D_ + 2 * D_ + 2 * C_ + 2 * D_
@@ -509,7 +510,7 @@ def main_gpu(args):
         avg_s = prof["main"][0] / n_main * 1e-3
         bytes_avg = (alg_bytes["gdn"] + alg_bytes["kda"]) / 2
         ach = bytes_avg / avg_s / 1e9
-        design = bytes_avg + th * MAIN_DESIGN_EXTRA_PER_TH
+        design = bytes_avg + th * (MAIN_DESIGN_EXTRA_PER_TH["gdn"] + MAIN_DESIGN_EXTRA_PER_TH["kda"]) / 2
         traffic = None
         tp = os.path.join(ROOT, "profiles", "main_traffic.json")
         if os.path.exists(tp):
