@@ -523,7 +523,7 @@ def main_gpu(args):
                 "bytes_per_launch": bytes_avg, "bytes_basis": "the method's: 2316 / 2820 B per token-head",
                 "design_bytes_per_launch": design,
                 "design_achieved": design / avg_s / 1e9,
-                "design_basis": "the builder's count: also the dS_C and T tiles this design reads",
+                "design_basis": "the builder's count: also the dS_C and T tiles (and, KDA, A and the P pair) this design reads",
                 "tensor_tflops": alg_flop / avg_s / 1e12, "tensor_frac": alg_flop / avg_s / 1e12 / tf_burst,
                 "tensor_peak": tf_burst, "tensor_peak_source": src + " (bf16_tflops, burst)"}
     else:
