@@ -6,7 +6,7 @@
  *
  * What it computes (plain definition, token by token, no chunking):
  *
- *   recurrence (the benchmark spec of the task, with the decay applied before the
+ *   recurrence (the gated delta rule with the decay applied before the
  *   delta update -- the order the FlashKDA derived quantities kd = k*e^{gc},
  *   ki = k*e^{-gc}, kr = k*e^{gT-gc} imply; "FlashKDA之backward（K1）", §3.2 and
  *   the kernel's workspace comments; for a scalar gate both orders coincide):
