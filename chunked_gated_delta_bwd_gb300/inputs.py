@@ -7,7 +7,7 @@ can take their inputs from it.  Everything is generated on the CPU with one
 
     varlen lengths (if any), q, k, v, beta logits, gate inputs, h0, dht, dO
 
-Value recipes (the workloads the pages benchmark and the benchmark's configs):
+Value recipes (the workloads the pages benchmark):
 
 * q, k, v, dO ~ N(0, 1), stored bf16 [T_total, H, D] (token-major);
 * beta logits ~ N(0, 1), bf16 [T_total, H];
@@ -45,7 +45,7 @@ class Case:
     note: str = field(default="", compare=False)
 
 
-# The five workloads of the benchmark spec (sizes, seeds, distributions).
+# The five benchmark workloads (sizes, seeds, distributions).
 CASES = {
     "gdn_tiny": Case("gdn_tiny", "gdn", 1, 128, 2, 64, seed=0,
                      note="GDN bwd tiny: B=1 H=2 T=128 D=64, h0=0, no dht"),

@@ -11,7 +11,7 @@ This module adds the two gate front ends:
 * GDN: one natural-log gate per (token, head).  It is broadcast over the
   channels and its gradient is the channel sum of the per-channel gradient.
 * KDA: ``g = -exp(A_log[h]) * softplus(g_raw + dt_bias[h, d])`` per channel (the
-  gate function of the KDA configuration in the benchmark spec).  Its chain
+  gate function of the KDA benchmark workload).  Its chain
   rule follows the pattern of "FlashKDA之backward（K1）", §5.2 (chain through
   the gate function per element, parameter gradients summed over tokens, the
   A_log gradient picking up one factor from the exp):

@@ -12,7 +12,7 @@ TOL_FP32 = 1e-3
 # gradient in the first product and Y = kr dS_C in the second -- each leave ~1.1-1.5e-3 on
 # dh0, ~2.2e-3 together, in the float64 rounding-site replay of the chain
 # (tests/test_precision_sites.py pins these figures); the bound is twice that.  With decay
-# (every workload of the task) those contributions fade and dh0 stays within TOL_FP32.
+# (every benchmark workload) those contributions fade and dh0 stays within TOL_FP32.
 TOL_DH0_NO_DECAY = 5e-3
 
 
@@ -158,7 +158,7 @@ def compare(gpu, ref, x, heads=None, conditioned=False, tol=None):
     chunk, head) block and the worst row at a sequence boundary of every token-major
     gradient, the worst (sequence, head) of dh0 and the worst head of dA_log / ddt_bias.
 
-    With ``conditioned`` (edge-case inputs outside the task's workloads, e.g. a
+    With ``conditioned`` (edge-case inputs outside the benchmark workloads, e.g. a
     few hundred tokens), dA_log and ddt_bias -- sums of dg terms with random
     signs -- are judged relative to the sum of the magnitudes of their terms
     instead of to the (possibly near-cancelling) sum itself.  ``tol`` maps tensor names to

@@ -160,7 +160,7 @@ def test_bad_cu_seqlens_are_flagged_not_faulted():
     assert gdr.workspace_status(ws) & gdr.api.GDR_DEV_BAD_SEQLENS
 
 
-# -- the task's full-size workloads, every head ------------------------------------
+# -- the full-size benchmark workloads, every head ----------------------------------
 @pytest.mark.parametrize("name", ["gdn_b2_h16_t4k", "kda_b1_h16_t8k", "kda_sigmoid_b1_h16_t8k",
                                   "gdn_gqa_hk16_hv32_t4k", "gdn_varlen_h32", "gdn_h16_t32k", "kda_h16_t32k"])
 def test_full_size_all_heads(name):

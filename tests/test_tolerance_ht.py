@@ -8,7 +8,7 @@ replays that chain in float64 on the oracle's chunk algebra, rounding exactly th
 sites to bf16, and checks that the error it predicts for ht sits in the class the
 tolerance assumes: each of the roundings of U, kr and U - W S0 costs about 1.6e-3
 relative (2^-9 unit roundoff, averaged over a tile), ~2.3e-3 together, at any
-length, because the task's gates forget a chunk's start state within the chunk.
+length, because the workloads' gates forget a chunk's start state within the chunk.
 TOL_HT = 5e-3 is about twice that.  (The backward's dh0 is built from R = qd - P W
 carried as a bf16 pair, which is why it meets 1e-3.)
 """
