@@ -85,6 +85,14 @@ def test_grouped_qk_heads_varlen(mode, dim):
     assert tuple(gpu["dq"].shape) == (x["q"].shape[0], 2, dim)
 
 
+@pytest.mark.parametrize("mode", ["gdn", "kda"])
+def test_one_key_head_for_eight_value_heads(mode):
+    # GQA at a large group: a single q / k head read by 8 value heads (dq, dk sum 8 terms)
+    x = inputs.custom(mode, [200, 77], heads=8, dim=128, seed=136, with_h0=True, with_dht=True, k_heads=1)
+    gpu = _check(x, label="gqa1x8_%s" % mode, conditioned=(mode == "kda"))  # 277 tokens: short sums
+    assert tuple(gpu["dq"].shape) == (x["q"].shape[0], 1, 128)
+
+
 def test_gdn_dense_layout():
     # equal lengths passed without cu_seqlens (dense B x T)
     import chunked_gated_delta_bwd_gb300 as gdr
