@@ -42,7 +42,8 @@ constexpr int STAGE = 3 * TILE;
 constexpr int oQ = 0;         // q (token-major) -> (beta kd)^T [d][s]   (+ STAGE for the other stage)
 constexpr int oK = 16384;     // k (token-major) -> (beta V)^T [j][s]
 constexpr int oV = 32768;     // v (token-major)
-constexpr int oW0 = 2 * STAGE;  // kd'^T [d][r] (G1, A block 0)
+constexpr int oW0 = 2 * STAGE;  // kd'^T [d][r] (G1, A block 0) -> (KDA backward) A, P lo [r][s] bf16 staged
+                                //   -> R_lo^T staged
 constexpr int oW1 = oW0 + TILE; // qd'^T [d][r] (G1, A block 1) -> R_hi^T staged
 constexpr int oW2 = oW1 + TILE; // ki'^T [d][s] (G1, B) -> W^T bf16 [d][s]
 constexpr int oP = oW2 + TILE;  // P [r][s] bf16
@@ -62,7 +63,7 @@ static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 constexpr uint32_t R_G1 = 0, R_W = 64, R_U = 128, R_R = 192, R_Q = 256, R_K = 320, R_G = 384;
 
 struct PrepMaps {
-    CUtensorMap q, k, v, graw, W, U, Kr, R, Rlo, T;
+    CUtensorMap q, k, v, graw, W, U, Kr, R, Rlo, T, ap;
 };
 // The thread that issues the TMA stores of W, U, Kr, R_hi, R_lo and T and the copies of the
 // next item's q, k and v: its stores read the stage that those copies overwrite, and a
@@ -409,9 +410,9 @@ __global__ void __launch_bounds__(512, 1) k_prep_kda(const Params p, const __gri
         float v[16];
         tc::ld16(tl(R_G1 + c0), v);
         // (the KDA backward also takes A and P for its main kernel, which then needs no first
-        // product of its own: [r][s] bf16 rows written straight from these registers, A, then
-        // P as a bf16 pair)
-        __nv_bfloat16* ap = p.APm ? p.APm + 3 * tile_cc : nullptr;
+        // product of its own: A and P lo are staged [r][s] bf16 in the dead kd' tile, P hi is
+        // sP, and one thread stores the three below)
+        const bool ap = p.APm != nullptr;
         if (L < 64) {  // A = strict_lower(beta A_raw), fp32 for the inversion
             const int r = L;
             const float br = sBeta[r];
@@ -425,9 +426,8 @@ __global__ void __launch_bounds__(512, 1) k_prep_kda(const Params p, const __gri
                 uint32_t w[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) w[e] = pack_bf16(a[2 * e], a[2 * e + 1]);
-                uint4* g = reinterpret_cast<uint4*>(ap + r * CH + c0);
-                g[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                g[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                *reinterpret_cast<uint4*>(sW0 + tc::sw_chunk(r, c0 >> 3, 64)) = make_uint4(w[0], w[1], w[2], w[3]);
+                *reinterpret_cast<uint4*>(sW0 + tc::sw_chunk(r, (c0 >> 3) + 1, 64)) = make_uint4(w[4], w[5], w[6], w[7]);
             }
         } else {  // P = lower(qd' ki'^T), bf16 [r][s]
             const int r = L - 64;
@@ -447,23 +447,28 @@ __global__ void __launch_bounds__(512, 1) k_prep_kda(const Params p, const __gri
                 g[0] = make_uint4(w[0], w[1], w[2], w[3]);
                 g[1] = make_uint4(w[4], w[5], w[6], w[7]);
             }
-            if (ap) {  // P hi, then its residual P - hi
+            if (ap) {  // P's residual P - hi (P hi is sP)
                 uint32_t wl[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const float2 hf = unpack_bf16(w[e]);
                     wl[e] = pack_bf16(pv[2 * e] - hf.x, pv[2 * e + 1] - hf.y);
                 }
-                uint4* g = reinterpret_cast<uint4*>(ap + CH * CH + r * CH + c0);
-                g[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                g[1] = make_uint4(w[4], w[5], w[6], w[7]);
-                g = reinterpret_cast<uint4*>(ap + 2 * CH * CH + r * CH + c0);
-                g[0] = make_uint4(wl[0], wl[1], wl[2], wl[3]);
-                g[1] = make_uint4(wl[4], wl[5], wl[6], wl[7]);
+                unsigned char* lo = sW0 + CH * CH * 2;
+                *reinterpret_cast<uint4*>(lo + tc::sw_chunk(r, c0 >> 3, 64)) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+                *reinterpret_cast<uint4*>(lo + tc::sw_chunk(r, (c0 >> 3) + 1, 64)) = make_uint4(wl[4], wl[5], wl[6], wl[7]);
             }
         }
+        if (ap) tc::fence_async_smem();  // the staged tiles (and sP) go out by TMA after the barrier
     }
     __syncthreads();
+    if (p.APm && tid == STORE_TID) {  // A, P hi, P lo for the main kernel, one group of stores
+        const int row = 3 * (chunk * p.H + h) * CH;
+        tc::tma_store_2d(&m.ap, 0, row, sb + oW0);
+        tc::tma_store_2d(&m.ap, 0, row + CH, sb + oP);
+        tc::tma_store_2d(&m.ap, 0, row + 2 * CH, sb + oW0 + CH * CH * 2);
+        tc::bulk_commit();
+    }
     if (warp < 8) {
         inv::invert_tc(sA, sTf, sTmp, sT, nullptr);
         // (warps 6, 7 leave the inversion after its diagonal blocks) the chunk info of the item
@@ -538,6 +543,9 @@ __global__ void __launch_bounds__(512, 1) k_prep_kda(const Params p, const __gri
         tc::tma_store_2d(&m.W, 0, trow, sb + oW2);
         tc::tma_store_2d(&m.U, 0, trow, sKa);
         tc::bulk_commit();
+        // (KDA backward) the A / P stores, two groups back, have read the kd' tile, where R_lo
+        // is staged next, and sP; the wait of the next product orders this for every thread
+        if (p.APm) tc::bulk_wait_read_but1();
     }
 
     // ---- R^T = qd^T - W^T P^T ----------------------------------------------------------------
@@ -609,7 +617,8 @@ static cudaError_t launch_prep_kda_t(const Params& p, cudaStream_t s) {
           encode_blocked_tokens_map(&m.graw, p.g_raw, T, p.H) &&
           encode_rows_map(&m.W, p.W, trows, CH, PD) && encode_rows_map(&m.U, p.U, trows, CH, PD) &&
           encode_rows_map(&m.Kr, p.Kr, trows, CH, PD) && encode_rows_map(&m.R, p.R, trows, CH, PD) &&
-          encode_rows_map(&m.Rlo, p.Rlo, trows, CH, PD) && encode_rows_map(&m.T, p.Tm, crows, CH, CH)))
+          encode_rows_map(&m.Rlo, p.Rlo, trows, CH, PD) && encode_rows_map(&m.T, p.Tm, crows, CH, CH) &&
+          encode_rows_map(&m.ap, p.APm, 3 * crows, CH, CH)))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(k_prep_kda<GATE>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
