@@ -419,6 +419,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_states_tc(const Params p, int p
 // (S_end = P^T S_start + L acts on each column alone), so every slice walks the G - 1
 // boundaries by itself; each output is summed over the key index in ascending order.
 constexpr int CMB_COLS = 16, CMB_SLICES = 128 / CMB_COLS;
+// 16-byte global -> shared copies that stay in flight together (LDGSTS), and the wait for them
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
 __global__ void __launch_bounds__(256) k_seg_combine(const Params p, int roles) {
     extern __shared__ float sm[];
     float* tr = sm;               // [128][128] the segment's transition (P^T, key-major)
@@ -432,8 +437,9 @@ __global__ void __launch_bounds__(256) k_seg_combine(const Params p, int roles) 
     const float* first = role == 0 ? p.segL + (pd + 0) * DD : p.segLb + (pd + G - 1) * DD;
     for (int i = tid; i < 128 * CMB_COLS / 4; i += 256) {
         const int e = i / (CMB_COLS / 4), q = i % (CMB_COLS / 4);
-        reinterpret_cast<float4*>(cur)[i] = *reinterpret_cast<const float4*>(first + e * 128 + j0 + 4 * q);
+        cp_async16(cur + 4 * i, first + e * 128 + j0 + 4 * q);
     }
+    cp_async_wait_all();
     __syncthreads();
     for (int step = 0; step < G - 1; ++step) {
         const int g = role == 0 ? step + 1 : G - 2 - step;  // the segment that starts from `cur`
@@ -445,13 +451,18 @@ __global__ void __launch_bounds__(256) k_seg_combine(const Params p, int roles) 
         if (step == G - 2) break;  // the last segment's start is all phase 3 needs
         const float* P = p.segP + (pd + g) * DD;
         const float* L = (role == 0 ? p.segL : p.segLb) + (pd + g) * DD;
-        for (int i = tid; i < DD / 4; i += 256) reinterpret_cast<float4*>(tr)[i] = reinterpret_cast<const float4*>(P)[i];
-        __syncthreads();
+        // the whole transition in flight at once, this thread's part of L read meanwhile
+#pragma unroll
+        for (int u = 0; u < 128 * 128 / 4 / 256; ++u) cp_async16(tr + 4 * (tid + 256 * u), P + 4 * (tid + 256 * u));
         float acc[4][2];
 #pragma unroll
-        for (int r = 0; r < 4; ++r)
-#pragma unroll
-            for (int c = 0; c < 2; ++c) acc[r][c] = L[(size_t)(4 * rb + r) * 128 + j0 + 2 * cb + c];
+        for (int r = 0; r < 4; ++r) {
+            const float2 l2 = *reinterpret_cast<const float2*>(L + (size_t)(4 * rb + r) * 128 + j0 + 2 * cb);
+            acc[r][0] = l2.x;
+            acc[r][1] = l2.y;
+        }
+        cp_async_wait_all();
+        __syncthreads();
 #pragma unroll 2
         for (int e = 0; e < 128; e += 4) {
             float2 s[4];
