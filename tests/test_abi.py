@@ -86,6 +86,23 @@ def test_bad_shapes_rejected(L, mutate, code):
     assert L.gdr_last_error()
 
 
+def test_largest_problem_accepted_next_token_rejected(L):
+    # the kernels address the per chunk-head tiles by 32-bit row, the largest block being the
+    # KDA backward's A / P pair block of 192 rows per chunk-head: chunks x heads x 192 < 2^31.
+    # With 16 heads that allows 699050 chunks (44.7 M tokens in one sequence); one token more
+    # opens chunk 699051 and is refused before any device work
+    limit = ((1 << 31) - 1) // (16 * 192)
+    assert limit == 699050
+    ok = gdr.make_shape(1, limit * 64, 16, 128)
+    assert L.gdr_workspace_bytes(ctypes.byref(ok)) > 0
+    assert L.gdr_states_bytes(ctypes.byref(ok)) > 0
+    over = gdr.make_shape(1, limit * 64 + 1, 16, 128)
+    assert L.gdr_workspace_bytes(ctypes.byref(over)) == 0
+    A = ctypes.c_void_p(4096)
+    rc = L.gdr_bwd(ctypes.byref(over), *([A] * 6), A, None, None, A, 1 << 40, *([A] * 6), None)
+    assert rc == 1 and b"too large" in L.gdr_last_error()
+
+
 def _bwd_args(A, ws_bytes):
     # q k v g beta h0 dO dht states ws ws_bytes dq dk dv dg dbeta dh0 stream
     return [A, A, A, A, A, None, A, None, None, A, ws_bytes, A, A, A, A, A, A, None]
