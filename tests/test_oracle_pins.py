@@ -12,7 +12,11 @@
 * the KDA gate values at points where softplus and sigmoid have closed forms
   (ln 2, ln 4, ln(4/3); 1/2, 3/4, 1/4) and the identities softplus(x) - softplus(-x)
   = x and sigmoid(z) + sigmoid(-z) = 1, alone and through the whole KDA path;
-* the worked examples of the pages (tests/golden/).
+* the worked examples of the pages (tests/golden/);
+* torch float64 autograd through a token recurrence written out independently (both gate
+  kinds, both per-channel gate functions, grouped q / k heads, sequences crossing the
+  oracle's checkpoint blocks);
+* the chunk form at chunk lengths 16, 32 and 64 equals the token recurrence.
 """
 import json
 import os
@@ -404,3 +408,87 @@ def test_chunk_form_matches_token_oracle(gate):
     for key in ("o", "ht", "dq", "dk", "dv", "dglog", "dbeta", "dh0"):
         np.testing.assert_allclose(b[key], a[key], rtol=1e-8, atol=1e-9 * np.abs(a[key]).max(),
                                    err_msg=key)
+
+
+# ----------------------------------------------------------------------------
+# torch float64 autograd through an independently written token recurrence
+# ----------------------------------------------------------------------------
+def _autograd_case(c, mode, gate_scale, Hk):
+    """The loss sum(o . dO) + sum(ht . dht) of the recurrence written out token by token in
+    torch float64 (decay, then the delta update, then the read-out), differentiated by autograd.
+    Returns the leaf gradients by input name."""
+    import torch
+    t = {n: torch.tensor(c[n], dtype=torch.float64, requires_grad=True)
+         for n in ("q", "k", "v", "b", "h0") + (("g",) if mode == "gdn" else ("g_raw", "A_log", "dt_bias"))}
+    if mode == "gdn":
+        glog = t["g"][:, :, None].expand_as(t["v"])
+    elif mode == "softplus":
+        glog = -torch.exp(t["A_log"])[None, :, None] * torch.nn.functional.softplus(t["g_raw"] + t["dt_bias"][None])
+    else:
+        glog = np.log(2.0) * gate_scale * torch.sigmoid(torch.exp(t["A_log"])[None, :, None] *
+                                                        (t["g_raw"] + t["dt_bias"][None]))
+    dO, dht = torch.tensor(c["dO"]), torch.tensor(c["dht"])
+    H = c["v"].shape[1]
+    r = H // Hk
+    loss = torch.zeros((), dtype=torch.float64)
+    for s in range(len(c["cu"]) - 1):
+        for h in range(H):
+            S = t["h0"][s, h]
+            for i in range(int(c["cu"][s]), int(c["cu"][s + 1])):
+                qv, kv = t["q"][i, h // r], t["k"][i, h // r]
+                qn = qv / torch.sqrt((qv * qv).sum() + 1e-6)
+                kn = kv / torch.sqrt((kv * kv).sum() + 1e-6)
+                beta = torch.sigmoid(t["b"][i, h])
+                S = torch.exp(glog[i, h])[:, None] * S
+                S = S - beta * torch.outer(kn, kn @ S) + beta * torch.outer(kn, t["v"][i, h])
+                loss = loss + ((c["scale"] * (S.T @ qn)) * dO[i, h]).sum()
+            loss = loss + (S * dht[s, h]).sum()
+    loss.backward()
+    return {n: x.grad.numpy() for n, x in t.items()}
+
+
+@pytest.mark.parametrize("mode,Hk", [("gdn", 2), ("softplus", 2), ("sigmoid", 2), ("softplus", 1)])
+def test_backward_matches_torch_autograd(mode, Hk):
+    """Every gradient of the hand-derived reverse mode equals autograd's on 150 + 70 tokens
+    (both sequences cross the oracle's 64-token checkpoint blocks), with h0 and dht, for
+    the scalar gate, both per-channel gate functions, and two value heads sharing one q / k
+    head."""
+    rng = np.random.default_rng(61)
+    c = _rand_case(rng, (150, 70), 2, 6, "gdn" if mode == "gdn" else "kda")
+    if Hk < 2:
+        c["q"], c["k"] = c["q"][:, :Hk].copy(), c["k"][:, :Hk].copy()
+    gs = -2.0 if mode == "sigmoid" else None
+    if mode == "gdn":
+        an = oracle.gdn(c["q"], c["k"], c["v"], c["g"], c["b"], c["scale"], c["cu"], h0=c["h0"],
+                        dO=c["dO"], dht=c["dht"])
+        pairs = (("q", "dq"), ("k", "dk"), ("v", "dv"), ("g", "dg"), ("b", "dbeta"), ("h0", "dh0"))
+    else:
+        an = oracle.kda(c["q"], c["k"], c["v"], c["g_raw"], c["A_log"], c["dt_bias"], c["b"], c["scale"],
+                        c["cu"], h0=c["h0"], dO=c["dO"], dht=c["dht"], gate=mode, gate_scale=gs)
+        pairs = (("q", "dq"), ("k", "dk"), ("v", "dv"), ("g_raw", "dg_raw"), ("A_log", "dA_log"),
+                 ("dt_bias", "ddt_bias"), ("b", "dbeta"), ("h0", "dh0"))
+    ag = _autograd_case(c, mode, gs, Hk)
+    for name, key in pairs:
+        np.testing.assert_allclose(an[key], ag[name], rtol=1e-9, atol=1e-11 * np.abs(ag[name]).max(),
+                                   err_msg=name)
+
+
+# ----------------------------------------------------------------------------
+# the chunk algebra does not depend on the chunk length
+# ----------------------------------------------------------------------------
+def test_chunk_form_is_independent_of_chunk_length():
+    """The chunk form at C = 16, 32 and 64 (the kernels' length) gives the token recurrence's
+    outputs and gradients on one sequence of 150 tokens: every C leaves a ragged last chunk
+    and puts chunk boundaries in different places."""
+    rng = np.random.default_rng(62)
+    c = _rand_case(rng, (150,), 1, 8, "glog")
+    ref = oracle.gated_delta(c["q"], c["k"], c["v"], c["glog"], c["b"], c["scale"], c["cu"], h0=c["h0"],
+                             dO=c["dO"], dht=c["dht"])
+    for C in (16, 32, 64):
+        got = chunk_form.pair(c["q"][:, 0], c["k"][:, 0], c["v"][:, 0], c["glog"][:, 0], c["b"][:, 0],
+                              c["h0"][0, 0], c["dO"][:, 0], c["dht"][0, 0], c["scale"], C=C)
+        for key, want in (("o", ref["o"][:, 0]), ("ht", ref["ht"][0, 0]), ("dq", ref["dq"][:, 0]),
+                          ("dk", ref["dk"][:, 0]), ("dv", ref["dv"][:, 0]), ("dglog", ref["dglog"][:, 0]),
+                          ("dbeta", ref["dbeta"][:, 0]), ("dh0", ref["dh0"][0, 0])):
+            np.testing.assert_allclose(got[key], want, rtol=1e-8, atol=1e-9 * np.abs(want).max(),
+                                       err_msg="%s at C = %d" % (key, C))
