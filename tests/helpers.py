@@ -214,7 +214,10 @@ def conditioned_error(g, ref, x, name, heads=None):
         mag = np.abs(ref["dg_raw"]).sum(axis=0)
     else:
         mag = np.abs(ref["dA_terms"]).sum(axis=(0, 2))
-    return float(np.linalg.norm(g - ref[name]) / np.linalg.norm(mag))
+    err, den = float(np.linalg.norm(g - ref[name])), float(np.linalg.norm(mag))
+    if den == 0.0:  # no terms at all (no tokens): the sums must be exactly zero
+        return 0.0 if err == 0.0 else float("inf")
+    return err / den
 
 
 def assert_parity(res, label=""):
