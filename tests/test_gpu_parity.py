@@ -148,6 +148,38 @@ def test_deterministic_outputs():
         assert torch.equal(a[k], b[k]), k
 
 
+@pytest.mark.parametrize("name", ["gdn_b2_h16_t4k", "kda_b1_h16_t8k"])
+def test_repeated_calls_are_stable(name):
+    # fifty back-to-back calls on one workspace: every output equals the first call's bitwise
+    # (dA_log / ddt_bias, summed with float atomics in no fixed order, to fp32 rounding) and
+    # every call's status word is clear -- a check for rare races in the persistent kernels
+    import chunked_gated_delta_bwd_gb300 as gdr
+    x = inputs.make(inputs.CASES[name])
+    d = H.to_gpu(x)
+    ws = H._workspace(d, x, None)
+    common = dict(h0=d["h0"], dht=d["dht"], cu_seqlens=d["cu_seqlens"], num_seqs=d["cu_seqlens"].numel() - 1,
+                  scale=d["scale"], workspace=ws)
+
+    def call():
+        if x["mode"] == "gdn":
+            return gdr.gdr_bwd(d["q"], d["k"], d["v"], d["g"], d["beta_logit"], d["dO"], **common)
+        return gdr.kda_bwd(d["q"], d["k"], d["v"], d["g_raw"], d["A_log"], d["dt_bias"], d["beta_logit"], d["dO"],
+                           kda_gate=x["kda_gate"], gate_scale=x["gate_scale"], **common)
+
+    ref = call()
+    torch.cuda.synchronize()
+    assert gdr.workspace_status(ws) == 0
+    for i in range(50):
+        out = call()
+        torch.cuda.synchronize()
+        assert gdr.workspace_status(ws) == 0, (i, gdr.workspace_status(ws))
+        for k, v in out.items():
+            if k in ("dA_log", "ddt_bias"):
+                torch.testing.assert_close(v, ref[k], rtol=1e-5, atol=1e-6 * float(ref[k].abs().max()))
+            else:
+                assert torch.equal(v, ref[k]), (i, k)
+
+
 def test_gate_range_is_flagged_not_faulted():
     import chunked_gated_delta_bwd_gb300 as gdr
     x = inputs.custom("kda", [128], heads=1, dim=64, seed=107)
