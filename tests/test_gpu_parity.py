@@ -85,6 +85,20 @@ def test_grouped_qk_heads_varlen(mode, dim):
     assert tuple(gpu["dq"].shape) == (x["q"].shape[0], 2, dim)
 
 
+@pytest.mark.parametrize("gate", ["softplus", "sigmoid"])
+def test_grouped_heads_segmented_kda(gate):
+    # one 8k-token sequence, four value heads on two q / k heads: the segmented state passing
+    # (four segments per pair) under grouped heads, both per-channel gate functions
+    x = inputs.custom("kda", [8192], heads=4, dim=128, seed=137, with_h0=True, with_dht=True, k_heads=2,
+                      kda_gate=gate, gate_scale=-2.0 if gate == "sigmoid" else 0.0)
+    # dA_log: with the softplus gate each head's sum is 1/170 - 1/500 of its terms' magnitudes
+    # and the strict 1e-3 holds (2.8e-4); with the sigmoid gate all four cancel to
+    # 1/1300 - 1/1700, which takes the strict figure to ~1.5e-3 (about 1e-6 times the
+    # cancellation in both), so that one is judged against the terms' magnitudes, the strict
+    # figure printed beside
+    _check(x, label="gqa_segmented_kda_%s" % gate, conditioned=(gate == "sigmoid"))
+
+
 @pytest.mark.parametrize("mode", ["gdn", "kda"])
 def test_one_key_head_for_eight_value_heads(mode):
     # GQA at a large group: a single q / k head read by 8 value heads (dq, dk sum 8 terms)
