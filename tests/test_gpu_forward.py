@@ -121,3 +121,12 @@ def test_forward_is_deterministic():
                                   "kda_h16_t32k"])
 def test_full_size_all_heads(name):
     _check(inputs.make(inputs.CASES[name]), label="fwd_" + name)
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_shapes(seed):
+    # the backward's seeded random shapes (tests/test_gpu_parity.py), through the forward:
+    # gate kinds, head dims, head grouping, packed sequences of 0-1500 tokens, h0 or not
+    from tests.test_gpu_parity import _random_case
+    x, label = _random_case(seed)
+    _check(x, label="fwd_" + label)
